@@ -1,0 +1,181 @@
+"""Quantize-on-append for one KV head: key and value records, and their canonical byte packing.
+
+Steps, following [Guide] §二 (rotate -> Lloyd-Max -> QJL residual sign -> value group quantisation
+-> bit packing). The magnitude/direction split follows [Overview] §核心技术解析 (PolarQuant).
+
+Key k in R^d (3 bits/coordinate = 2-bit Lloyd-Max + 1-bit QJL, [Guide] §二 and §五 key_bits=3):
+  n = ||k||_2;  y = Pi (k / n)  (y = 0 when n = 0);
+  idx_j = #{ i : t_i < y_j }  (t = Lloyd-Max boundaries; the comparison is taken in fp32);
+  r = y - c[idx];  gamma = ||r||_2;  z = S r;  sign_j = 1 if fp32(z_j) >= 0 else 0;
+  stored: idx, sign bits, fp16(n), fp16(gamma)  (each fp16 rounded via fp32).
+
+Value v in R^d (symmetric b-bit, groups of 32, fp16 scale per group, [Guide] §二 step 4):
+  v' = Pi v;  per group G: s = fp16( fp32(max_G |v'|) / (2^(b-1) - 1/2) );
+  code = clamp(floor(fp32(v') / s), -2^(b-1), 2^(b-1) - 1) + 2^(b-1)  (code = 2^(b-1) when s = 0);
+  level = (code - 2^(b-1) + 1/2) * s  (mid-rise: +-absmax is a level up to the fp16 rounding of s).
+
+Readings (the pages are silent; the plainest reading is used):
+* values are rotated with the same Pi as keys;
+* the fp16 scale is clamped to 65504;
+* fp16 rounding goes through fp32, matching a kernel that computes in fp32;
+* decisions (code index, sign, floor) are taken in fp32, the kernel's precision.
+
+Canonical record bytes (bit packing, [Guide] §二 step 5: four 2-bit values per byte):
+  element j of a b-bit array sits at bit b*(j mod 8/b) of byte floor(j*b/8) (little-endian in the byte);
+  key record   = idx (2 bits) | sign (1 bit) | n (fp16 LE) | gamma (fp16 LE)  -> d/4 + d/8 + 4 bytes;
+  value record = codes (b bits) | scales (fp16 LE, d/32 of them)            -> d*b/8 + d/16 bytes.
+"""
+
+from dataclasses import dataclass
+
+import numpy as np
+
+from .rotation import rotation_matrix
+
+KEY_MSE_BITS = 2
+VALUE_GROUP = 32
+RING = 128
+
+
+@dataclass
+class KeyRecords:
+    idx: np.ndarray    # uint8 [T, d]
+    sign: np.ndarray   # uint8 [T, d], 1 = projection >= 0
+    norm: np.ndarray   # float16 [T]
+    gamma: np.ndarray  # float16 [T]
+
+
+@dataclass
+class ValueRecords:
+    codes: np.ndarray   # uint8 [T, d]
+    scales: np.ndarray  # float16 [T, d / 32]
+    bits: int
+
+
+def _fp16_via_fp32(x):
+    return np.asarray(x, dtype=np.float64).astype(np.float32).astype(np.float16)
+
+
+def quantize_keys(k, D, S, centroids, boundaries):
+    """Key records for k [T, d] (fp64 values). S is the QJL matrix [d, d], D the rotation signs."""
+    k = np.atleast_2d(np.asarray(k, dtype=np.float64))
+    Pi = rotation_matrix(D)
+    n = np.sqrt(np.sum(k * k, axis=1))
+    y = (k @ Pi.T) / np.where(n > 0, n, 1.0)[:, None]
+    y[n == 0] = 0.0
+    y32 = y.astype(np.float32)
+    t32 = np.asarray(boundaries, dtype=np.float64).astype(np.float32)
+    idx = np.sum(y32[:, :, None] > t32[None, None, :], axis=2).astype(np.uint8)
+    r = y - np.asarray(centroids, dtype=np.float64)[idx]
+    gamma = np.sqrt(np.sum(r * r, axis=1))
+    z = r @ np.asarray(S, dtype=np.float64).T
+    sign = (z.astype(np.float32) >= 0).astype(np.uint8)
+    return KeyRecords(idx=idx, sign=sign, norm=_fp16_via_fp32(n), gamma=_fp16_via_fp32(gamma))
+
+
+def quantize_values(v, D, bits, group=VALUE_GROUP):
+    """Value records for v [T, d] (fp64 values) at `bits` in {2, 4}."""
+    v = np.atleast_2d(np.asarray(v, dtype=np.float64))
+    T, d = v.shape
+    half = 1 << (bits - 1)
+    vr = (v @ rotation_matrix(D).T).reshape(T, d // group, group)
+    absmax = np.max(np.abs(vr), axis=2)
+    s32 = absmax.astype(np.float32) / np.float32(half - 0.5)
+    s16 = np.minimum(s32, np.float32(65504.0)).astype(np.float16)
+    s = s16.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.floor(vr.astype(np.float32) / s)
+    code = np.clip(q, -half, half - 1) + half
+    code = np.where(s == 0, half, code)
+    return ValueRecords(codes=code.reshape(T, d).astype(np.uint8), scales=s16, bits=bits)
+
+
+def dequantize_values(rec, D, rotated=False):
+    """v_hat = Pi^T (level * s) per token; `rotated=True` returns the rotated-basis levels."""
+    half = 1 << (rec.bits - 1)
+    T, d = rec.codes.shape
+    groups = rec.scales.shape[1]
+    lev = (rec.codes.astype(np.float64) - half + 0.5).reshape(T, groups, d // groups)
+    vr = (lev * rec.scales.astype(np.float64)[:, :, None]).reshape(T, d)
+    if rotated:
+        return vr
+    return vr @ rotation_matrix(D)  # row form of Pi^T v'
+
+
+def dequantize_keys(rec, D, S, centroids, with_qjl=True):
+    """k_hat = n * Pi^T (c[idx] + sqrt(pi/2)/d * gamma * S^T (2 sign - 1)) (QJL term optional)."""
+    T, d = rec.idx.shape
+    y = np.asarray(centroids, dtype=np.float64)[rec.idx]
+    if with_qjl:
+        kappa = np.sqrt(np.pi / 2.0) / d
+        pm = 2.0 * rec.sign.astype(np.float64) - 1.0
+        y = y + kappa * rec.gamma.astype(np.float64)[:, None] * (pm @ np.asarray(S, dtype=np.float64))
+    return rec.norm.astype(np.float64)[:, None] * (y @ rotation_matrix(D))
+
+
+def history_split(L, ring=RING):
+    """(packed, ring) token counts of a sequence of length L: whole ring blocks are flushed when full."""
+    if L <= 0:
+        return 0, 0
+    packed = ring * ((L - 1) // ring)
+    return packed, L - packed
+
+
+def _pack_bits(a, bits):
+    a = np.asarray(a, dtype=np.uint8)
+    T, d = a.shape
+    per = 8 // bits
+    a = a.reshape(T, d // per, per).astype(np.uint16)
+    shifts = (np.arange(per) * bits).astype(np.uint16)
+    return np.bitwise_or.reduce(a << shifts, axis=2).astype(np.uint8)
+
+
+def _unpack_bits(b, bits, d):
+    b = np.asarray(b, dtype=np.uint8)
+    per = 8 // bits
+    shifts = (np.arange(per) * bits).astype(np.uint8)
+    out = (b[:, :, None] >> shifts) & ((1 << bits) - 1)
+    return out.reshape(b.shape[0], d).astype(np.uint8)
+
+
+def key_record_bytes(d):
+    return d * KEY_MSE_BITS // 8 + d // 8 + 4
+
+
+def value_record_bytes(d, bits, group=VALUE_GROUP):
+    return d * bits // 8 + 2 * (d // group)
+
+
+def pack_key_records(rec):
+    T, d = rec.idx.shape
+    return np.concatenate([
+        _pack_bits(rec.idx, KEY_MSE_BITS), _pack_bits(rec.sign, 1),
+        rec.norm.astype("<f2").view(np.uint8).reshape(T, 2),
+        rec.gamma.astype("<f2").view(np.uint8).reshape(T, 2)], axis=1)
+
+
+def unpack_key_records(buf, d):
+    buf = np.asarray(buf, dtype=np.uint8)
+    T = buf.shape[0]
+    o1 = d * KEY_MSE_BITS // 8
+    o2 = o1 + d // 8
+    return KeyRecords(
+        idx=_unpack_bits(buf[:, :o1], KEY_MSE_BITS, d),
+        sign=_unpack_bits(buf[:, o1:o2], 1, d),
+        norm=np.ascontiguousarray(buf[:, o2:o2 + 2]).view("<f2").reshape(T).astype(np.float16),
+        gamma=np.ascontiguousarray(buf[:, o2 + 2:o2 + 4]).view("<f2").reshape(T).astype(np.float16))
+
+
+def pack_value_records(rec, group=VALUE_GROUP):
+    T, d = rec.codes.shape
+    return np.concatenate([
+        _pack_bits(rec.codes, rec.bits),
+        rec.scales.astype("<f2").view(np.uint8).reshape(T, 2 * (d // group))], axis=1)
+
+
+def unpack_value_records(buf, d, bits, group=VALUE_GROUP):
+    buf = np.asarray(buf, dtype=np.uint8)
+    T = buf.shape[0]
+    o1 = d * bits // 8
+    scales = np.ascontiguousarray(buf[:, o1:o1 + 2 * (d // group)]).view("<f2").reshape(T, d // group)
+    return ValueRecords(codes=_unpack_bits(buf[:, :o1], bits, d), scales=scales.astype(np.float16), bits=bits)

@@ -1,0 +1,126 @@
+"""Pins for the oracle's key/value quantisers, canonical packing and ring split."""
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+from oracle import (gaussian_matrix_bf16, history_split, key_record_bytes, lloyd_max_codebook,
+                    pack_key_records, pack_value_records, quantize_keys, quantize_values, rademacher_signs,
+                    unpack_key_records, unpack_value_records, value_record_bytes, dequantize_values)
+from oracle.quant import _pack_bits, _unpack_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _rotate(x, D):
+    """Pi x computed with scipy's Hadamard (independent of the oracle's construction)."""
+    d = x.shape[-1]
+    return (x * D[None, :]) @ scipy.linalg.hadamard(d).T / np.sqrt(d)
+
+
+@pytest.mark.parametrize("bits", [1, 2, 4])
+def test_pack_unpack_exhaustive(bits):
+    per = 8 // bits
+    allbytes = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    codes = _unpack_bits(allbytes, bits, 256 * per)
+    assert np.array_equal(_pack_bits(codes, bits), allbytes)
+    rnd = np.random.default_rng(bits).integers(0, 1 << bits, size=(7, 256), dtype=np.uint8)
+    assert np.array_equal(_unpack_bits(_pack_bits(rnd, bits), bits, 256), rnd)
+
+
+def test_pack_bit_order_little_endian():
+    assert _pack_bits(np.array([[0, 1, 2, 3]], np.uint8), 2)[0, 0] == 0b11100100
+    assert _pack_bits(np.array([[1, 0, 0, 0, 0, 0, 0, 1]], np.uint8), 1)[0, 0] == 0b10000001
+    assert _pack_bits(np.array([[0x3, 0xA]], np.uint8), 4)[0, 0] == 0xA3
+
+
+def test_record_sizes_and_golden_constants():
+    g = json.load(open(os.path.join(GOLDEN, "memory_figures.json")))["pipeline_constants"]
+    assert g["key_bits"] == 2 + g["qjl_bits_per_dim"]
+    assert g["values_per_byte_at_2bit"] == 8 // 2
+    assert key_record_bytes(128) == 52 and key_record_bytes(256) == 100
+    assert value_record_bytes(128, 2) == 40 and value_record_bytes(128, 4) == 72
+    assert value_record_bytes(256, 2) == 80 and value_record_bytes(256, 4) == 144
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_key_records(d):
+    rng = np.random.default_rng(d)
+    k = rng.standard_normal((64, d))
+    k[:, 3] *= 8.0
+    k[5] = 0.0
+    D, S = rademacher_signs(1, d), gaussian_matrix_bf16(1, d)
+    c, t = lloyd_max_codebook(d, 2)
+    rec = quantize_keys(k, D, S, c, t)
+    n = np.linalg.norm(k, axis=1)
+    assert np.array_equal(rec.norm, n.astype(np.float32).astype(np.float16))
+    y = _rotate(k, D) / np.where(n > 0, n, 1)[:, None]
+    y[5] = 0
+    # the boundary rule equals the nearest-centroid rule (midpoint boundaries)
+    nearest = np.argmin(np.abs(y[:, :, None] - c[None, None, :]), axis=2)
+    assert np.array_equal(rec.idx, nearest)
+    r = y - c[rec.idx]
+    assert np.allclose(rec.gamma.astype(np.float64), np.linalg.norm(r, axis=1), rtol=2 ** -10)
+    z = r @ S.T
+    pm = 2.0 * rec.sign - 1.0
+    assert np.allclose(np.sum(pm * z, axis=1), np.sum(np.abs(z), axis=1), rtol=1e-12)
+    # round trip through the canonical bytes
+    buf = pack_key_records(rec)
+    assert buf.shape == (64, key_record_bytes(d))
+    back = unpack_key_records(buf, d)
+    for f in ("idx", "sign", "norm", "gamma"):
+        assert np.array_equal(getattr(back, f), getattr(rec, f))
+
+
+@pytest.mark.parametrize("bits", [2, 4])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_value_records(bits, d):
+    rng = np.random.default_rng(bits * d)
+    v = rng.standard_t(5, size=(50, d))
+    v[7] = 0.0
+    D = rademacher_signs(2, d)
+    rec = quantize_values(v, D, bits)
+    half = 1 << (bits - 1)
+    vr = _rotate(v, D).reshape(50, d // 32, 32)
+    s = rec.scales.astype(np.float64)[:, :, None]
+    absmax = np.abs(vr).max(axis=2)
+    assert np.allclose(rec.scales.astype(np.float64), absmax / (half - 0.5), rtol=2 ** -10)
+    lev = (rec.codes.reshape(50, d // 32, 32).astype(np.float64) - half + 0.5) * s
+    # mid-rise quantiser: error within half a step (plus the fp16 rounding of the scale at the top level)
+    assert np.all(np.abs(vr - lev) <= 0.5 * s + absmax[:, :, None] * 2 ** -10 + 1e-12)
+    assert np.all(rec.codes[7] == half) and np.all(rec.scales[7] == 0)
+    # the group's absmax element is reproduced by a top level (up to fp16 rounding of the scale)
+    top = np.abs(lev).max(axis=2)
+    assert np.allclose(top, absmax, rtol=2 ** -10)
+    # dequantisation rotates back with Pi^T
+    back = dequantize_values(rec, D)
+    assert np.allclose(_rotate(back, D), lev.reshape(50, d), atol=1e-12)
+    buf = pack_value_records(rec)
+    assert buf.shape == (50, value_record_bytes(d, bits))
+    r2 = unpack_value_records(buf, d, bits)
+    assert np.array_equal(r2.codes, rec.codes) and np.array_equal(r2.scales, rec.scales)
+
+
+def test_values_on_the_grid_are_lossless():
+    d, bits = 128, 2
+    D = rademacher_signs(9, d)
+    rng = np.random.default_rng(0)
+    codes = rng.integers(0, 4, size=(10, d))
+    codes[:, ::32] = 3  # make each group's absmax exactly 1.5 * s with s = 0.5 (exact in fp16)
+    vr = (codes - 1.5) * 0.5
+    v = vr.reshape(10, d) @ (scipy.linalg.hadamard(d) * D[None, :] / np.sqrt(d))  # Pi^T v'
+    rec = quantize_values(v, D, bits)
+    assert np.all(rec.scales == np.float16(0.5))
+    assert np.array_equal(rec.codes, codes)
+    assert np.allclose(dequantize_values(rec, D), v, atol=1e-12)
+
+
+def test_history_split_ring_semantics():
+    assert history_split(0) == (0, 0)
+    assert history_split(1) == (0, 1)
+    assert history_split(128) == (0, 128)
+    assert history_split(129) == (128, 1)
+    assert history_split(1152) == (1024, 128)  # 1024 packed + 128-token ring
+    assert history_split(32768) == (32640, 128)
