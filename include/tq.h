@@ -1,0 +1,197 @@
+/*
+ * tq.h - C ABI of libtq: TurboQuant KV-cache hot path on one GB300 (sm_103a).
+ *
+ * The method, as the sources state it. [Guide] = the TurboQuant-on-vLLM guide at
+ * hotelren.com/news/5528865.
+ *   - quantize-on-append ([Guide] §二, the five-step pipeline): rotate each key/value head vector
+ *     with a seeded randomised Hadamard transform and store the key norm. Then code the key with a
+ *     2-bit Lloyd-Max codebook for the rotated-coordinate (Beta) distribution, and add one QJL
+ *     sign bit per dimension on the key residual (3-bit keys). Values are quantised symmetrically
+ *     at 2 or 4 bits in groups of 32 with an fp16 scale per group. Everything is bit-packed.
+ *   - hybrid decode attention ([Guide] §五.1 and §七): scores are estimated straight from the
+ *     packed keys plus the QJL correction, against a rotated, projected query. Values are
+ *     dequantised inside an online softmax. The result is merged exactly with a bf16 ring buffer
+ *     of the most recent 128 tokens (buffer_size=128, [Guide] §五.1).
+ *
+ * Conventions (all calls):
+ *   - Pointers prefixed d_ are DEVICE pointers; all others are host pointers.
+ *   - The caller owns every device buffer (tables, cache, workspace). The library never allocates
+ *     device memory; it allocates only its small host-side context.
+ *   - Work is enqueued asynchronously on the caller's CUDA stream `stream`. Calls on one layer must
+ *     be ordered by the caller (same stream, or events).
+ *   - Every argument is validated on the host before any launch. A bad argument returns
+ *     TQ_ERR_INVALID_ARG and an unsupported shape returns TQ_ERR_UNSUPPORTED; nothing is launched
+ *     in either case. A launch failure returns TQ_ERR_CUDA. tq_last_error() gives the reason
+ *     (thread-local string).
+ *   - Conditions that only the device can see (a sequence growing past max_ctx, a bad sequence id)
+ *     set bits of a device status word instead of faulting. tq_check_status() reads that word.
+ *     Kernels never trap and never wait without a bound.
+ *   - No C++ exception crosses this ABI.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tq_stream_t; /* a cudaStream_t; NULL = legacy default stream */
+
+typedef enum tq_status {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,
+  TQ_ERR_UNSUPPORTED = 2,
+  TQ_ERR_CAPACITY = 3,
+  TQ_ERR_CUDA = 4,
+  TQ_ERR_DEVICE = 5 /* the device status word is non-zero (see tq_check_status) */
+} tq_status;
+
+typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
+
+/* Device status word bits. */
+#define TQ_DEV_ERR_CAPACITY 0x1u /* an append would grow a sequence past max_ctx; the row was skipped */
+#define TQ_DEV_ERR_SEQ_ID 0x2u   /* a sequence id outside [0, max_seqs); the row was skipped */
+#define TQ_DEV_ERR_SPLITS 0x4u   /* decode saw more packed pages than its grid covers (max_ctx_hint too small) */
+#define TQ_DEV_ERR_TIMEOUT 0x8u  /* a bounded wait on a bulk copy gave up; that split was dropped */
+
+/* Configuration. The key is 3 bits per coordinate: a 2-bit Lloyd-Max code plus 1 QJL sign bit
+ * ([Guide] §二 steps 2-3; §五.1 key_bits=3). */
+typedef struct tq_config {
+  int32_t head_dim;    /* d: 128 or 256 */
+  int32_t key_bits;    /* 3 */
+  int32_t value_bits;  /* 2 or 4 ([Guide] §二 step 4) */
+  int32_t value_group; /* 32 ([Guide] §二 step 4) */
+  int32_t ring_size;   /* 128: exact recent buffer ([Guide] §五.1 buffer_size=128) */
+  int32_t n_layers;
+  int32_t n_kv_heads;
+  int32_t n_q_heads;   /* multiple of n_kv_heads, with n_q_heads / n_kv_heads in {1, 2, 4} (GQA) */
+  int32_t max_seqs;    /* number of sequence slots in the cache */
+  int32_t max_ctx;     /* maximum tokens per sequence (packed + ring) */
+  uint64_t seed;       /* seeds the rotation signs D and the QJL matrix S (SplitMix64) */
+} tq_config;
+
+typedef struct tq_ctx tq_ctx; /* opaque host object owned by the library */
+
+/* Bytes of the device tables buffer (rotation signs, S, S^T, codebook) for `cfg`; 0 if cfg is invalid. */
+size_t tq_tables_bytes(const tq_config* cfg);
+
+/* Bytes of the device cache buffer for `cfg`; 0 if invalid. Layout, in order:
+ *   - packed pages [layer][slot][kv_head][page][page_bytes];
+ *   - bf16 ring K and V [layer][slot][kv_head][ring][d];
+ *   - int32 state [layer][slot][2]: total length L and flushed ring prefix F;
+ *   - the int32 device status word. */
+size_t tq_cache_bytes(const tq_config* cfg);
+
+/* Bytes of one packed page of 128 tokens of one KV head (the fragment-major record layout). */
+size_t tq_page_bytes(const tq_config* cfg);
+
+/* tq_init_codebooks: creates a context for `cfg`.
+ *   - Computes on the host, in fp64: the 2-bit Lloyd-Max codebook of the density
+ *     f_d(x) ~ (1-x^2)^((d-3)/2) ([Guide] §二 step 2: "Beta-distribution-optimal codebook").
+ *   - Computes the seeded rotation signs D and QJL matrix S (SplitMix64, Box-Muller, bf16).
+ *   - Uploads both with cudaMemcpyAsync on `stream` into the caller's d_tables (at least
+ *     tq_tables_bytes(cfg) bytes, 256-byte aligned).
+ * The context is bound to the current CUDA device. *out is freed by tq_destroy. */
+tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_bytes, tq_stream_t stream,
+                            tq_ctx** out);
+
+/* Binds the caller's cache buffer: d_cache (at least tq_cache_bytes, 256-byte aligned). The
+ * sequence state and status word are zeroed on `stream`, so every slot starts empty. */
+tq_status tq_cache_bind(tq_ctx* ctx, void* d_cache, size_t cache_bytes, tq_stream_t stream);
+
+/* Empties the sequences d_seq_ids[0..batch) of `layer` (layer = -1: every layer). */
+tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream);
+
+/* tq_quantize_append: appends new tokens to sequences of one layer ([Guide] §二 pipeline and §五.1:
+ * prefill is captured in bulk, decode tokens go into the ring buffer).
+ *   - k, v: device arrays [batch][max_new][n_kv_heads][d] of dtype `dt`. Row b uses its first
+ *     d_n_new[b] tokens.
+ *   - d_seq_ids[b]: the cache slot of row b. d_n_new[b] is in [0, max_new].
+ *   - Ring semantics: the ring holds the last R = L - 128*floor((L-1)/128) tokens of a length-L
+ *     sequence. When an append overflows the ring, every complete 128-token block is quantised
+ *     into the packed history. So a sequence is 128*floor((L-1)/128) packed tokens + R ring tokens.
+ *   - f32 inputs enter the ring rounded to bf16. Blocks that never pass through the ring are
+ *     quantised from the f32 values.
+ *   - A row that would exceed max_ctx is skipped and sets TQ_DEV_ERR_CAPACITY.
+ *   - Launches: one quantize kernel over the pages to write, then one ring-update kernel. */
+tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
+                             const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
+                             tq_stream_t stream);
+
+/* tq_ring_flush: quantises the ring of each row into the packed history now ("periodically flush
+ * the residual cache into the main cache", [Overview] §核心技术解析, Bonsai residual cache).
+ *   - Afterwards decode treats all L tokens as packed.
+ *   - The bf16 copies stay in the ring until the block is complete, and that block is re-quantised
+ *     with identical codes when it overflows. Quantisation is per token, so the codes do not change.
+ *   - Rows with an empty ring are unchanged. */
+tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream);
+
+/* Bytes of the decode workspace for `batch` rows and a longest sequence of `max_ctx_hint` tokens
+ * (0 = cfg.max_ctx). */
+size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
+
+/* tq_decode_attention: one decode step of hybrid attention for one layer ([Guide] §五.1 and §七).
+ *   - q: device bf16 [batch][n_q_heads][d] (one query token per row).
+ *   - out: device f32 [batch][n_q_heads][d].
+ *   - Query head h attends KV head h / (n_q_heads / n_kv_heads).
+ *   - softmax_scale <= 0 selects 1/sqrt(d).
+ *   - Scores use the TurboQuant estimator n*(<Pi q, c[idx]> + sqrt(pi/2)/d * gamma * <S Pi q, sign>)
+ *     over the packed history, and exact dot products over the ring.
+ *   - One softmax runs over both.
+ *   - d_workspace: at least tq_workspace_bytes(ctx, batch, max_ctx_hint) bytes, 256-byte aligned,
+ *     scratch owned by the caller.
+ *   - max_ctx_hint: an upper bound on every row's length (0 = cfg.max_ctx). It only sizes the grid;
+ *     a row longer than the hint sets TQ_DEV_ERR_SPLITS.
+ *   - Launches: query prep, split-K decode (+ ring split), combine. */
+tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                              int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                              int max_ctx_hint, tq_stream_t stream);
+
+/* Synchronises `stream` and reads the device status word. It returns TQ_OK if the word is zero.
+ * Otherwise it returns TQ_ERR_DEVICE and stores the word in *word (if non-NULL). `clear` != 0
+ * zeroes the word afterwards. */
+tq_status tq_check_status(tq_ctx* ctx, tq_stream_t stream, uint32_t* word, int clear);
+
+/* Frees the host context (device buffers stay owned by the caller). */
+void tq_destroy(tq_ctx* ctx);
+
+/* Thread-local description of the last error (empty string if none). */
+const char* tq_last_error(void);
+
+/* ---- Host-only inspection helpers (tests and tools; no device work) ---- */
+
+/* Byte offset, inside the cache buffer, of one packed page of (layer, slot, kv_head, page). */
+size_t tq_page_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int page);
+/* Byte offsets of the ring K (which = 0) / V (which = 1) block of (layer, slot, kv_head). */
+size_t tq_ring_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int which);
+/* Byte offset of the int32 pair {L, F} of (layer, slot), and of the status word. */
+size_t tq_state_offset(const tq_ctx* ctx, int layer, int slot);
+size_t tq_status_offset(const tq_ctx* ctx);
+
+/* Converts the first n_tokens of one packed page (a host copy of tq_page_bytes bytes) into canonical
+ * records ([Guide] §二 step 5 bit packing, little-endian within bytes):
+ *   - key record = idx (2 bits/coord) | QJL sign (1 bit/coord, 1 = projection >= 0) | fp16 n | fp16 gamma;
+ *   - value record = codes (value_bits/coord) | fp16 scale per 32 coords.
+ * out_keys holds n_tokens * (d/4 + d/8 + 4) bytes; out_values holds n_tokens * (d*vb/8 + d/16). */
+tq_status tq_page_to_records(const tq_ctx* ctx, const void* h_page, int n_tokens, uint8_t* out_keys,
+                             uint8_t* out_values);
+/* Inverse of tq_page_to_records (host): builds a page from canonical records (unused tokens zero). */
+tq_status tq_records_to_page(const tq_ctx* ctx, const uint8_t* keys, const uint8_t* values, int n_tokens,
+                             void* h_page);
+
+/* Host copies of the tables this context uploaded:
+ *   - D: float[d] (+-1);
+ *   - S_bf16: uint16[d*d], row-major bf16 bits;
+ *   - centroids: double[4];
+ *   - boundaries: double[3].
+ * Any pointer may be NULL. */
+tq_status tq_get_tables(const tq_ctx* ctx, float* D, uint16_t* S_bf16, double* centroids, double* boundaries);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,66 @@
+// Device helpers shared by the libtq kernels.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cstdint>
+
+#include "tq_internal.h"
+
+namespace tq {
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  __nv_bfloat16 h = __float2bfloat16_rn(f);
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Unnormalised Walsh-Hadamard transform (Sylvester order) of a d-vector spread over one warp.
+// Lane l holds coordinates 4l + e (e = 0..3) in x[e] and, for d = 256, 128 + 4l + e in x[4 + e].
+// Coordinate bits 0-1 (and 7) are butterflied in registers; bits 2-6 across lanes with shuffles.
+template <int NE>
+__device__ __forceinline__ void warp_fwht(float (&x)[NE], int lane) {
+#pragma unroll
+  for (int base = 0; base < NE; base += 4) {
+    float a0 = x[base + 0] + x[base + 1], a1 = x[base + 0] - x[base + 1];
+    float a2 = x[base + 2] + x[base + 3], a3 = x[base + 2] - x[base + 3];
+    x[base + 0] = a0 + a2;
+    x[base + 2] = a0 - a2;
+    x[base + 1] = a1 + a3;
+    x[base + 3] = a1 - a3;
+  }
+  if (NE == 8) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = x[e], b = x[4 + e];
+      x[e] = a + b;
+      x[4 + e] = a - b;
+    }
+  }
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int e = 0; e < NE; ++e) {
+      const float o = __shfl_xor_sync(0xffffffffu, x[e], m);
+      x[e] = upper ? (o - x[e]) : (x[e] + o);
+    }
+  }
+}
+
+__device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
+
+}  // namespace tq

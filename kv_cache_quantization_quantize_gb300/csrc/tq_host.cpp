@@ -1,0 +1,542 @@
+// Host side of libtq: argument validation, tables (codebook, rotation signs, QJL matrix), cache
+// layout, canonical record conversion and the C ABI entry points.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "tq_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+tq_status fail(tq_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+tq_status ok() {
+  g_last_error.clear();
+  return TQ_OK;
+}
+
+tq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(TQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+tq_status validate(const tq_config* c) {
+  if (!c) return fail(TQ_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->head_dim != 128 && c->head_dim != 256)
+    return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: supported 128, 256", c->head_dim);
+  if (c->key_bits != 3) return fail(TQ_ERR_UNSUPPORTED, "key_bits %d: supported 3 (2-bit Lloyd-Max + 1-bit QJL)", c->key_bits);
+  if (c->value_bits != 2 && c->value_bits != 4)
+    return fail(TQ_ERR_UNSUPPORTED, "value_bits %d: supported 2, 4", c->value_bits);
+  if (c->value_group != 32) return fail(TQ_ERR_UNSUPPORTED, "value_group %d: supported 32", c->value_group);
+  if (c->ring_size != tq::kPage) return fail(TQ_ERR_UNSUPPORTED, "ring_size %d: supported 128", c->ring_size);
+  if (c->n_layers < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 || c->max_seqs < 1 || c->max_ctx < 1)
+    return fail(TQ_ERR_INVALID_ARG, "n_layers, n_kv_heads, n_q_heads, max_seqs, max_ctx must be >= 1");
+  if (c->n_q_heads % c->n_kv_heads != 0)
+    return fail(TQ_ERR_INVALID_ARG, "n_q_heads %d not a multiple of n_kv_heads %d", c->n_q_heads, c->n_kv_heads);
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return fail(TQ_ERR_UNSUPPORTED, "GQA group %d: supported 1, 2, 4", G);
+  if (c->max_ctx > (1 << 24)) return fail(TQ_ERR_UNSUPPORTED, "max_ctx %d above 2^24", c->max_ctx);
+  return TQ_OK;
+}
+
+// ---- SplitMix64 (Steele, Lea & Flood 2014), written from its published definition ----
+inline uint64_t splitmix64(uint64_t seed, uint64_t counter) {
+  uint64_t z = seed + counter * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return z ^ (z >> 31);
+}
+inline double uniform_open(uint64_t x) { return (double(x >> 11) + 0.5) * 0x1p-53; }
+
+// Nearest-even rounding of a double to bf16 (8 significant bits); returns the bf16 bit pattern.
+uint16_t bf16_rne_bits(double v) {
+  int e = 0;
+  const double m = std::frexp(v, &e);              // v = m * 2^e, 0.5 <= |m| < 1
+  const double r = std::ldexp(std::nearbyint(m * 256.0), e - 8);  // default rounding: to nearest even
+  const float f = static_cast<float>(r);           // exact: r has <= 8 significant bits
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// ---- Lloyd-Max codebook of f_d(x) ~ (1-x^2)^((d-3)/2) on [-1, 1] ([Guide] §二 step 2) ----
+// Cell integrals by composite 16-point Gauss-Legendre quadrature (nodes from Newton iteration on
+// the Legendre polynomial), independent of any closed form.
+struct GaussLegendre {
+  double x[16], w[16];
+  GaussLegendre() {
+    const int n = 16;
+    for (int i = 0; i < n; ++i) {
+      double z = std::cos(M_PI * (i + 0.75) / (n + 0.5));
+      for (int it = 0; it < 100; ++it) {
+        double p0 = 1.0, p1 = z;
+        for (int k = 2; k <= n; ++k) {
+          const double p2 = ((2.0 * k - 1.0) * z * p1 - (k - 1.0) * p0) / k;
+          p0 = p1;
+          p1 = p2;
+        }
+        const double dp = n * (z * p1 - p0) / (z * z - 1.0);
+        const double dz = p1 / dp;
+        z -= dz;
+        if (std::fabs(dz) < 1e-16) break;
+      }
+      double p0 = 1.0, p1 = z;
+      for (int k = 2; k <= n; ++k) {
+        const double p2 = ((2.0 * k - 1.0) * z * p1 - (k - 1.0) * p0) / k;
+        p0 = p1;
+        p1 = p2;
+      }
+      const double dp = n * (z * p1 - p0) / (z * z - 1.0);
+      x[i] = z;
+      w[i] = 2.0 / ((1.0 - z * z) * dp * dp);
+    }
+  }
+};
+
+struct BetaMarginal {
+  int d;
+  double log_c;
+  explicit BetaMarginal(int dd) : d(dd) {
+    log_c = std::lgamma(d / 2.0) - 0.5 * std::log(M_PI) - std::lgamma((d - 1) / 2.0);
+  }
+  double pdf(double x) const {
+    if (std::fabs(x) >= 1.0) return 0.0;
+    return std::exp(log_c + 0.5 * (d - 3) * std::log1p(-x * x));
+  }
+  // integrals of f and x f over [a, b]
+  void integrate(double a, double b, double& m0, double& m1) const {
+    static const GaussLegendre gl;
+    const int panels = 256;
+    m0 = m1 = 0.0;
+    const double h = (b - a) / panels;
+    for (int p = 0; p < panels; ++p) {
+      const double lo = a + p * h, mid = lo + 0.5 * h;
+      for (int i = 0; i < 16; ++i) {
+        const double x = mid + 0.5 * h * gl.x[i];
+        const double f = pdf(x) * gl.w[i] * 0.5 * h;
+        m0 += f;
+        m1 += x * f;
+      }
+    }
+  }
+};
+
+void lloyd_max(int d, int bits, double* cent, double* bnd) {
+  const int L = 1 << bits;
+  const BetaMarginal f(d);
+  // initial boundaries: uniform over +-3 standard deviations of the N(0, 1/d) approximation
+  std::vector<double> t(L - 1), c(L);
+  for (int i = 0; i < L - 1; ++i) t[i] = (-3.0 + 6.0 * (i + 1) / L) / std::sqrt((double)d);
+  // integrate only where the density is non-negligible
+  const double span = std::min(1.0, 40.0 / std::sqrt((double)d));
+  for (int it = 0; it < 100000; ++it) {
+    for (int i = 0; i < L; ++i) {
+      const double a = i == 0 ? -span : t[i - 1];
+      const double b = i == L - 1 ? span : t[i];
+      double m0, m1;
+      f.integrate(a, b, m0, m1);
+      c[i] = m1 / m0;
+    }
+    double delta = 0.0;
+    for (int i = 0; i < L - 1; ++i) {
+      const double nt = 0.5 * (c[i] + c[i + 1]);
+      delta = std::max(delta, std::fabs(nt - t[i]));
+      t[i] = nt;
+    }
+    if (delta < 1e-16) break;
+  }
+  // the density is even: make the codebook exactly odd-symmetric (middle boundary exactly 0)
+  for (int i = 0; i < L; ++i) cent[i] = 0.5 * (c[i] - c[L - 1 - i]);
+  for (int i = 0; i < L - 1; ++i) bnd[i] = 0.5 * (t[i] - t[L - 2 - i]);
+}
+
+size_t ring_elems(const tq_config& c) { return (size_t)2 * tq::kPage * c.head_dim; }
+
+void compute_offsets(tq_ctx* ctx) {
+  const tq_config& c = ctx->cfg;
+  ctx->pl = tq::page_layout(c.head_dim, c.value_bits);
+  ctx->to = tq::table_offsets(c.head_dim);
+  ctx->max_pages = (c.max_ctx + tq::kPage - 1) / tq::kPage;
+  const size_t units = (size_t)c.n_layers * c.max_seqs * c.n_kv_heads;
+  ctx->pages_off = 0;
+  ctx->ring_off = align_up(units * ctx->max_pages * ctx->pl.bytes, 256);
+  ctx->state_off = align_up(ctx->ring_off + units * ring_elems(c) * 2, 256);
+  ctx->status_off = align_up(ctx->state_off + (size_t)c.n_layers * c.max_seqs * 8, 256);
+  ctx->total_bytes = ctx->status_off + 256;
+}
+
+}  // namespace
+
+namespace tq {
+
+TableOffsets table_offsets(int d) {
+  TableOffsets o;
+  o.D = 0;
+  o.S = align_up(o.D + sizeof(float) * d, 256);
+  o.St = align_up(o.S + 2ull * d * d, 256);
+  o.cb = align_up(o.St + 2ull * d * d, 256);
+  o.bytes = align_up(o.cb + sizeof(float) * kCbFloats, 256);
+  return o;
+}
+
+LayerView layer_view(const tq_ctx* ctx, int layer) {
+  const tq_config& c = ctx->cfg;
+  LayerView v;
+  v.d = c.head_dim;
+  v.vb = c.value_bits;
+  v.G = c.n_q_heads / c.n_kv_heads;
+  v.Hkv = c.n_kv_heads;
+  v.Hq = c.n_q_heads;
+  v.max_seqs = c.max_seqs;
+  v.max_ctx = c.max_ctx;
+  v.max_pages = ctx->max_pages;
+  v.page_bytes = ctx->pl.bytes;
+  uint8_t* tb = static_cast<uint8_t*>(ctx->d_tables);
+  v.D = reinterpret_cast<const float*>(tb + ctx->to.D);
+  v.S = reinterpret_cast<const uint16_t*>(tb + ctx->to.S);
+  v.St = reinterpret_cast<const uint16_t*>(tb + ctx->to.St);
+  v.cb = reinterpret_cast<const float*>(tb + ctx->to.cb);
+  uint8_t* cb = static_cast<uint8_t*>(ctx->d_cache);
+  const size_t units_per_layer = (size_t)c.max_seqs * c.n_kv_heads;
+  v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
+  v.ring = reinterpret_cast<uint16_t*>(cb + ctx->ring_off) + (size_t)layer * units_per_layer * ring_elems(c);
+  v.state = reinterpret_cast<int32_t*>(cb + ctx->state_off) + (size_t)layer * c.max_seqs * 2;
+  v.status = reinterpret_cast<uint32_t*>(cb + ctx->status_off);
+  return v;
+}
+
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
+  const tq_config& c = ctx->cfg;
+  const int hint = (max_ctx_hint <= 0 || max_ctx_hint > c.max_ctx) ? c.max_ctx : max_ctx_hint;
+  const int max_pages = std::max(1, (hint + kPage - 1) / kPage);
+  const int units = batch * c.n_kv_heads;
+  const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
+  const int target = 3 * sms;  // resident CTAs: about three 128-thread CTAs per SM
+  int splits = std::max(1, (target + units - 1) / units);
+  splits = std::min(splits, max_pages);
+  DecodePlan p;
+  p.pages_per_split = (max_pages + splits - 1) / splits;
+  p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
+  const int d = c.head_dim;
+  p.prep_off = 0;
+  p.prep_stride = align_up((size_t)3 * (d / 32) * 32 * 16 + 4 * 4 * sizeof(float), 256);
+  p.part_off = align_up(p.prep_off + p.prep_stride * units, 256);
+  p.part_stride = align_up((size_t)(2 * kMaxG + kMaxG * d) * sizeof(float), 16);
+  p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
+  return p;
+}
+
+}  // namespace tq
+
+// =============================================================================================
+// C ABI
+// =============================================================================================
+extern "C" {
+
+const char* tq_last_error(void) { return g_last_error.c_str(); }
+
+size_t tq_tables_bytes(const tq_config* cfg) {
+  if (validate(cfg) != TQ_OK) return 0;
+  return tq::table_offsets(cfg->head_dim).bytes;
+}
+
+size_t tq_page_bytes(const tq_config* cfg) {
+  if (validate(cfg) != TQ_OK) return 0;
+  return tq::page_layout(cfg->head_dim, cfg->value_bits).bytes;
+}
+
+size_t tq_cache_bytes(const tq_config* cfg) {
+  if (validate(cfg) != TQ_OK) return 0;
+  tq_ctx tmp;
+  tmp.cfg = *cfg;
+  compute_offsets(&tmp);
+  return tmp.total_bytes;
+}
+
+tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_bytes, tq_stream_t stream,
+                            tq_ctx** out) {
+  if (!out) return fail(TQ_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  tq_status st = validate(cfg);
+  if (st != TQ_OK) return st;
+  const size_t need = tq::table_offsets(cfg->head_dim).bytes;
+  if (d_tables) {
+    if (tables_bytes < need) return fail(TQ_ERR_INVALID_ARG, "tables_bytes %zu < %zu", tables_bytes, need);
+    if (reinterpret_cast<uintptr_t>(d_tables) % 256) return fail(TQ_ERR_INVALID_ARG, "d_tables not 256-byte aligned");
+  }
+  tq_ctx* ctx = new (std::nothrow) tq_ctx();
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "host allocation failed");
+  ctx->cfg = *cfg;
+  compute_offsets(ctx);
+  const int d = cfg->head_dim;
+  // rotation signs D and QJL matrix S (bf16), from SplitMix64 streams 1 and 2 of the seed
+  const uint64_t seed_D = splitmix64(cfg->seed, 1), seed_S = splitmix64(cfg->seed, 2);
+  ctx->D.resize(d);
+  for (int i = 0; i < d; ++i) ctx->D[i] = (splitmix64(seed_D, (uint64_t)i + 1) >> 63) ? -1.0f : 1.0f;
+  ctx->S.resize((size_t)d * d);
+  for (uint64_t k = 0; k < (uint64_t)d * d; ++k) {
+    const double u1 = uniform_open(splitmix64(seed_S, 2 * k + 1));
+    const double u2 = uniform_open(splitmix64(seed_S, 2 * k + 2));
+    const double g = std::sqrt(-2.0 * std::log(u1)) * std::cos(6.283185307179586476925286766559 * u2);
+    ctx->S[k] = bf16_rne_bits(g);
+  }
+  lloyd_max(d, 2, ctx->cent, ctx->bnd);
+  if (!d_tables) {  // host-only context: inspection helpers only
+    ctx->host_only = true;
+    *out = ctx;
+    return ok();
+  }
+  cudaError_t e = cudaGetDevice(&ctx->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device);
+  if (e != cudaSuccess) {
+    delete ctx;
+    return cuda_fail(e, "cudaGetDevice");
+  }
+  // Stage the tables in a host buffer and upload it with one copy. The pageable source is copied
+  // before cudaMemcpyAsync returns, so the buffer can be freed right after.
+  std::vector<uint8_t> host(need, 0);
+  std::memcpy(host.data() + ctx->to.D, ctx->D.data(), sizeof(float) * d);
+  std::memcpy(host.data() + ctx->to.S, ctx->S.data(), 2ull * d * d);
+  uint16_t* st_h = reinterpret_cast<uint16_t*>(host.data() + ctx->to.St);
+  for (int i = 0; i < d; ++i)
+    for (int j = 0; j < d; ++j) st_h[(size_t)j * d + i] = ctx->S[(size_t)i * d + j];
+  float cb[tq::kCbFloats] = {0};
+  for (int i = 0; i < 4; ++i) cb[i] = (float)ctx->cent[i];
+  for (int i = 0; i < 3; ++i) cb[4 + i] = (float)ctx->bnd[i];
+  cb[8] = (float)(0.5 * (ctx->cent[2] + ctx->cent[3]));
+  cb[9] = (float)(0.5 * (ctx->cent[3] - ctx->cent[2]));
+  std::memcpy(host.data() + ctx->to.cb, cb, sizeof(cb));
+  e = cudaMemcpyAsync(d_tables, host.data(), need, cudaMemcpyHostToDevice, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) {
+    delete ctx;
+    return cuda_fail(e, "upload tables");
+  }
+  ctx->d_tables = d_tables;
+  *out = ctx;
+  return ok();
+}
+
+tq_status tq_cache_bind(tq_ctx* ctx, void* d_cache, size_t cache_bytes, tq_stream_t stream) {
+  if (!ctx || !d_cache) return fail(TQ_ERR_INVALID_ARG, "ctx or d_cache is NULL");
+  if (ctx->host_only) return fail(TQ_ERR_INVALID_ARG, "host-only context (created without d_tables)");
+  if (cache_bytes < ctx->total_bytes)
+    return fail(TQ_ERR_INVALID_ARG, "cache_bytes %zu < %zu", cache_bytes, ctx->total_bytes);
+  if (reinterpret_cast<uintptr_t>(d_cache) % 256) return fail(TQ_ERR_INVALID_ARG, "d_cache not 256-byte aligned");
+  uint8_t* base = static_cast<uint8_t*>(d_cache);
+  cudaError_t e = cudaMemsetAsync(base + ctx->state_off, 0, ctx->total_bytes - ctx->state_off, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(state)");
+  ctx->d_cache = d_cache;
+  ctx->cache_bytes = cache_bytes;
+  return ok();
+}
+
+static tq_status check_ready(const tq_ctx* ctx, int layer) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "ctx is NULL");
+  if (ctx->host_only || !ctx->d_cache) return fail(TQ_ERR_INVALID_ARG, "no cache bound (tq_cache_bind)");
+  if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(TQ_ERR_INVALID_ARG, "layer %d out of range", layer);
+  return TQ_OK;
+}
+
+tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "ctx is NULL");
+  if (layer != -1) {
+    tq_status st = check_ready(ctx, layer);
+    if (st != TQ_OK) return st;
+  } else if (ctx->host_only || !ctx->d_cache) {
+    return fail(TQ_ERR_INVALID_ARG, "no cache bound");
+  }
+  if (batch < 0 || (batch > 0 && !d_seq_ids)) return fail(TQ_ERR_INVALID_ARG, "bad batch / d_seq_ids");
+  if (batch == 0) return ok();
+  cudaError_t e = tq::launch_reset(ctx, layer, d_seq_ids, batch, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "reset kernel");
+}
+
+tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
+                             const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
+                             tq_stream_t stream) {
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (dt != TQ_BF16 && dt != TQ_F32) return fail(TQ_ERR_INVALID_ARG, "dtype %d", (int)dt);
+  if (batch < 0 || max_new < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d / max_new %d negative", batch, max_new);
+  if (batch == 0 || max_new == 0) return ok();
+  if (!k || !v || !d_seq_ids || !d_n_new) return fail(TQ_ERR_INVALID_ARG, "NULL k/v/d_seq_ids/d_n_new");
+  if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  if (max_new > ctx->cfg.max_ctx) return fail(TQ_ERR_CAPACITY, "max_new %d > max_ctx %d", max_new, ctx->cfg.max_ctx);
+  const size_t esz = dt == TQ_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(k) % (esz * 4) || reinterpret_cast<uintptr_t>(v) % (esz * 4))
+    return fail(TQ_ERR_INVALID_ARG, "k/v must be %zu-byte aligned", esz * 4);
+  cudaError_t e = tq::launch_append(ctx, layer, k, v, (int)dt, d_seq_ids, d_n_new, batch, max_new, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "append kernels");
+}
+
+tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream) {
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d negative", batch);
+  if (batch == 0) return ok();
+  if (!d_seq_ids) return fail(TQ_ERR_INVALID_ARG, "d_seq_ids is NULL");
+  if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  cudaError_t e = tq::launch_flush(ctx, layer, d_seq_ids, batch, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "flush kernel");
+}
+
+size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint) {
+  if (!ctx || batch < 1) return 0;
+  return tq::decode_plan(ctx, batch, max_ctx_hint).bytes;
+}
+
+tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                              int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                              int max_ctx_hint, tq_stream_t stream) {
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d negative", batch);
+  if (batch == 0) return ok();
+  if (!q || !out || !d_seq_ids || !d_workspace) return fail(TQ_ERR_INVALID_ARG, "NULL q/out/d_seq_ids/d_workspace");
+  if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
+  const tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
+  if (workspace_bytes < plan.bytes)
+    return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+  cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "decode kernels");
+}
+
+tq_status tq_check_status(tq_ctx* ctx, tq_stream_t stream, uint32_t* word, int clear) {
+  if (!ctx || ctx->host_only || !ctx->d_cache) return fail(TQ_ERR_INVALID_ARG, "no cache bound");
+  uint32_t w = 0;
+  uint8_t* p = static_cast<uint8_t*>(ctx->d_cache) + ctx->status_off;
+  cudaError_t e = cudaMemcpyAsync(&w, p, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "read status");
+  if (word) *word = w;
+  if (clear && w) {
+    e = cudaMemsetAsync(p, 0, 4, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status");
+  }
+  if (w) return fail(TQ_ERR_DEVICE, "device status word 0x%x", w);
+  return ok();
+}
+
+void tq_destroy(tq_ctx* ctx) { delete ctx; }
+
+size_t tq_page_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int page) {
+  const tq_config& c = ctx->cfg;
+  return ctx->pages_off +
+         ((((size_t)layer * c.max_seqs + slot) * c.n_kv_heads + kv_head) * ctx->max_pages + page) * ctx->pl.bytes;
+}
+
+size_t tq_ring_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int which) {
+  const tq_config& c = ctx->cfg;
+  return ctx->ring_off +
+         ((((size_t)layer * c.max_seqs + slot) * c.n_kv_heads + kv_head) * 2 + which) * tq::kPage * c.head_dim * 2;
+}
+
+size_t tq_state_offset(const tq_ctx* ctx, int layer, int slot) {
+  return ctx->state_off + ((size_t)layer * ctx->cfg.max_seqs + slot) * 8;
+}
+
+size_t tq_status_offset(const tq_ctx* ctx) { return ctx->status_off; }
+
+tq_status tq_page_to_records(const tq_ctx* ctx, const void* h_page, int n_tokens, uint8_t* out_keys,
+                             uint8_t* out_values) {
+  if (!ctx || !h_page || !out_keys || !out_values) return fail(TQ_ERR_INVALID_ARG, "NULL argument");
+  if (n_tokens < 0 || n_tokens > tq::kPage) return fail(TQ_ERR_INVALID_ARG, "n_tokens %d", n_tokens);
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
+  const tq::PageLayout& pl = ctx->pl;
+  const uint8_t* pg = static_cast<const uint8_t*>(h_page);
+  const uint32_t* kw = reinterpret_cast<const uint32_t*>(pg + pl.kbits_off);
+  const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + pl.vbits_off);
+  const size_t krec = d / 4 + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
+  for (int t = 0; t < n_tokens; ++t) {
+    uint8_t* kr = out_keys + t * krec;
+    uint8_t* vr = out_values + t * vrec;
+    std::memset(kr, 0, krec);
+    std::memset(vr, 0, vrec);
+    for (int j = 0; j < d; ++j) {
+      int w, b;
+      tq::kbit_loc(d, t, j, 0, w, b);
+      const int hi = (kw[w] >> b) & 1;
+      tq::kbit_loc(d, t, j, 1, w, b);
+      const int lo = (kw[w] >> b) & 1;
+      tq::kbit_loc(d, t, j, 2, w, b);
+      const int sg = (kw[w] >> b) & 1;
+      kr[j / 4] |= (uint8_t)((2 * hi + lo) << (2 * (j % 4)));
+      kr[d / 4 + j / 8] |= (uint8_t)(sg << (j % 8));
+      tq::vcode_loc(d, vb, t, j, w, b);
+      const int code = (vw[w] >> b) & ((1 << vb) - 1);
+      const int per = 8 / vb;
+      vr[j / per] |= (uint8_t)(code << (vb * (j % per)));
+    }
+    std::memcpy(kr + d / 4 + d / 8, pg + pl.norms_off + 4 * t, 4);
+    std::memcpy(vr + (size_t)d * vb / 8, pg + pl.vscale_off + 2 * (size_t)t * (d / 32), 2 * (d / 32));
+  }
+  return ok();
+}
+
+tq_status tq_records_to_page(const tq_ctx* ctx, const uint8_t* keys, const uint8_t* values, int n_tokens,
+                             void* h_page) {
+  if (!ctx || !keys || !values || !h_page) return fail(TQ_ERR_INVALID_ARG, "NULL argument");
+  if (n_tokens < 0 || n_tokens > tq::kPage) return fail(TQ_ERR_INVALID_ARG, "n_tokens %d", n_tokens);
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
+  const tq::PageLayout& pl = ctx->pl;
+  uint8_t* pg = static_cast<uint8_t*>(h_page);
+  std::memset(pg, 0, pl.bytes);
+  uint32_t* kw = reinterpret_cast<uint32_t*>(pg + pl.kbits_off);
+  uint32_t* vw = reinterpret_cast<uint32_t*>(pg + pl.vbits_off);
+  const size_t krec = d / 4 + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
+  for (int t = 0; t < n_tokens; ++t) {
+    const uint8_t* kr = keys + t * krec;
+    const uint8_t* vr = values + t * vrec;
+    for (int j = 0; j < d; ++j) {
+      const int idx = (kr[j / 4] >> (2 * (j % 4))) & 3;
+      const int sg = (kr[d / 4 + j / 8] >> (j % 8)) & 1;
+      int w, b;
+      tq::kbit_loc(d, t, j, 0, w, b);
+      kw[w] |= (uint32_t)(idx >> 1) << b;
+      tq::kbit_loc(d, t, j, 1, w, b);
+      kw[w] |= (uint32_t)(idx & 1) << b;
+      tq::kbit_loc(d, t, j, 2, w, b);
+      kw[w] |= (uint32_t)sg << b;
+      const int per = 8 / vb;
+      const int code = (vr[j / per] >> (vb * (j % per))) & ((1 << vb) - 1);
+      tq::vcode_loc(d, vb, t, j, w, b);
+      vw[w] |= (uint32_t)code << b;
+    }
+    std::memcpy(pg + pl.norms_off + 4 * t, kr + d / 4 + d / 8, 4);
+    std::memcpy(pg + pl.vscale_off + 2 * (size_t)t * (d / 32), vr + (size_t)d * vb / 8, 2 * (d / 32));
+  }
+  return ok();
+}
+
+tq_status tq_get_tables(const tq_ctx* ctx, float* D, uint16_t* S_bf16, double* centroids, double* boundaries) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "ctx is NULL");
+  const int d = ctx->cfg.head_dim;
+  if (D) std::memcpy(D, ctx->D.data(), sizeof(float) * d);
+  if (S_bf16) std::memcpy(S_bf16, ctx->S.data(), 2ull * d * d);
+  if (centroids) std::memcpy(centroids, ctx->cent, sizeof(ctx->cent));
+  if (boundaries) std::memcpy(boundaries, ctx->bnd, sizeof(ctx->bnd));
+  return ok();
+}
+
+}  // extern "C"

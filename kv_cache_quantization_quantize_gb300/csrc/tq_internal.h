@@ -1,0 +1,154 @@
+// Internal declarations of libtq: page layout, context, kernel launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "tq.h"
+
+#if defined(__CUDACC__)
+#define TQ_HD __host__ __device__ __forceinline__
+#else
+#define TQ_HD inline
+#endif
+
+namespace tq {
+
+constexpr int kPage = 128;  // tokens per packed page = ring capacity ([Guide] §五.1 buffer_size=128)
+constexpr int kMaxG = 4;    // query heads per KV head served by one decode CTA (GQA <= 4)
+
+// ---------------------------------------------------------------------------------------------
+// Packed page of 128 tokens of one KV head. The layout is fragment-major: the decode kernel's
+// mma.sync operand registers are cut out of it with one LOP3 per 2-4 elements. Sections:
+//   KBITS  [n-tile 16][plane 3][half d/128][lane 32] u32.
+//          Planes: 0 = high bit of the Lloyd-Max index, 1 = low bit, 2 = QJL sign (1 = z >= 0).
+//   NORMS  [token 128] {fp16 n, fp16 gamma}.
+//   VBITS  2-bit: [block 4][m-tile d/16][lane 32] u32; 4-bit: [block 4][m-tile d/16][lane 32][2] u32.
+//   VSCALE [token 128][group d/32] fp16.
+// Per token: K (3*d/8 + 4 B) + V (d*vb/8 + d/16 B); d=128, V2 -> 92 B, identical to the canonical
+// record size. A page is therefore the canonical records in another order.
+// ---------------------------------------------------------------------------------------------
+struct PageLayout {
+  int d, vb;
+  uint32_t kbits_off, norms_off, vbits_off, vscale_off, bytes;
+};
+
+TQ_HD PageLayout page_layout(int d, int vb) {
+  PageLayout p;
+  p.d = d;
+  p.vb = vb;
+  p.kbits_off = 0;
+  p.norms_off = p.kbits_off + 3u * kPage * d / 8;
+  p.vbits_off = p.norms_off + 4u * kPage;
+  p.vscale_off = p.vbits_off + (uint32_t)kPage * d * vb / 8;
+  p.bytes = p.vscale_off + 2u * kPage * (d / 32);
+  return p;
+}
+
+// Location of the key bit of (token t, coordinate j, plane pi) in KBITS: u32 word index and bit.
+// Word (nt, pi, half, lane=4g+c) holds token 8nt+g; bit 8i + 2ks + h holds coordinate
+// 128*half + 32ks + 16h + 4c + i. Each byte of a word is one fp8 operand of m16n8k32 (B matrix,
+// k = 16h + 4c + i, column g), selected by masking bit (2ks + h) of every byte.
+TQ_HD void kbit_loc(int d, int t, int j, int pi, int& word, int& bit) {
+  const int nt = t >> 3, g = t & 7;
+  const int half = j >> 7, jj = j & 127;
+  const int ks = jj >> 5, h = (jj >> 4) & 1, c = (jj >> 2) & 3, i = jj & 3;
+  word = ((nt * 3 + pi) * (d >> 7) + half) * 32 + 4 * g + c;
+  bit = 8 * i + 2 * ks + h;
+}
+
+// Field tables of the value words (see vcode_loc): which 2-bit (4-bit) field of the word feeds
+// A-fragment register r of m16n8k16 for k-step kap of a 32-token block.
+TQ_HD int vfield2(int kap, int r) { return ((kap ? 0x7463 : 0x5210) >> (4 * r)) & 0xF; }
+TQ_HD int vfield4(int r) { return (0x3120 >> (4 * r)) & 0xF; }
+// Effective mantissa position (after the decoder's shift) of the field for the low/high token half
+// of a k-step; the decoder's B operand is prescaled by 2^(24 - pos).
+TQ_HD int vpos2(int kap, int hiT) { return kap ? (hiT ? 8 : 6) : (hiT ? 4 : 0); }
+TQ_HD int vpos4(int hiT) { return hiT ? 4 : 0; }
+
+// Location of the value code of (token t, coordinate j) in VBITS: u32 word index and LSB of the field.
+// A-fragment (m16n8k16, rows = coordinates, k = tokens) register r = rowhi + 2*hiT of lane (g, c)
+// holds tokens (2c+8hiT, 2c+8hiT+1) in its two f16 halves e = token parity.
+TQ_HD void vcode_loc(int d, int vb, int t, int j, int& word, int& bit) {
+  const int blk = t >> 5, tau = t & 31, kap = tau >> 4, kk = tau & 15;
+  const int c = (kk >> 1) & 3, e = kk & 1, hiT = kk >> 3;
+  const int mt = j >> 4, g = j & 7, rowhi = (j >> 3) & 1;
+  const int lane = 4 * g + c, r = rowhi + 2 * hiT;
+  if (vb == 2) {
+    word = (blk * (d >> 4) + mt) * 32 + lane;
+    bit = 16 * e + 2 * vfield2(kap, r);
+  } else {
+    word = ((blk * (d >> 4) + mt) * 32 + lane) * 2 + kap;
+    bit = 16 * e + 4 * vfield4(r);
+  }
+}
+
+// Device tables (inside the caller's d_tables buffer).
+struct TableOffsets {
+  size_t D, S, St, cb, bytes;
+};
+TableOffsets table_offsets(int d);
+
+// Codebook block: cb[0..3] centroids, cb[4..6] boundaries, cb[8] alpha=(c2+c3)/2, cb[9] beta=(c3-c2)/2.
+constexpr int kCbFloats = 16;
+
+}  // namespace tq
+
+struct tq_ctx {
+  tq_config cfg;
+  int device = -1;
+  int sm_count = 0;
+  bool host_only = false;
+  tq::PageLayout pl;
+  tq::TableOffsets to;
+  int max_pages = 0;  // pages per (layer, slot, head)
+  void* d_tables = nullptr;
+  void* d_cache = nullptr;
+  size_t cache_bytes = 0;
+  size_t pages_off = 0, ring_off = 0, state_off = 0, status_off = 0, total_bytes = 0;
+  std::vector<float> D;
+  std::vector<uint16_t> S;  // bf16 bits, row-major
+  double cent[4] = {0, 0, 0, 0};
+  double bnd[3] = {0, 0, 0};
+};
+
+namespace tq {
+
+// Pointers and sizes for one layer, passed to kernels by value.
+struct LayerView {
+  int d, vb, G, Hkv, Hq, max_seqs, max_ctx, max_pages;
+  uint32_t page_bytes;
+  const float* D;
+  const uint16_t* S;   // bf16 [d][d]
+  const uint16_t* St;  // bf16 [d][d] transposed
+  const float* cb;
+  uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
+  uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
+  int32_t* state;      // this layer: [slot][2] = {L, F}
+  uint32_t* status;
+};
+
+LayerView layer_view(const tq_ctx* ctx, int layer);
+
+// Decode workspace plan.
+struct DecodePlan {
+  int n_splits;        // history splits per (row, kv head); the ring is one extra split
+  int pages_per_split;
+  size_t prep_off, prep_stride;  // per (row, kv head) query-prep block
+  size_t part_off, part_stride;  // per (row, kv head, split) partial
+  size_t bytes;
+};
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint);
+
+cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const void* v, int dt,
+                          const int32_t* seq_ids, const int32_t* n_new, int batch, int max_new, cudaStream_t s);
+cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
+cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
+cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
+                          int batch, float scale, void* ws, const DecodePlan& plan, cudaStream_t s);
+
+}  // namespace tq

@@ -1,0 +1,176 @@
+"""CPU tests of libtq's C ABI: exports, argument validation, tables vs the oracle, page layout."""
+import ctypes
+import json
+import os
+
+import numpy as np
+import pytest
+
+import kv_cache_quantization_quantize_gb300 as tqm
+from kv_cache_quantization_quantize_gb300 import _abi
+from oracle import gaussian_matrix_bf16, rademacher_signs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_quantization_quantize_gb300 import build
+    build.build()
+
+
+def test_library_exports_every_header_function():
+    lib = _abi.load()
+    names = _abi.header_functions()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_abi._SIGS)
+
+
+@pytest.mark.parametrize("field,value,status", [
+    ("head_dim", 64, _abi.TQ_ERR_UNSUPPORTED), ("head_dim", 96, _abi.TQ_ERR_UNSUPPORTED),
+    ("value_bits", 3, _abi.TQ_ERR_UNSUPPORTED), ("key_bits", 4, _abi.TQ_ERR_UNSUPPORTED),
+    ("value_group", 64, _abi.TQ_ERR_UNSUPPORTED), ("ring_size", 64, _abi.TQ_ERR_UNSUPPORTED),
+    ("n_layers", 0, _abi.TQ_ERR_INVALID_ARG), ("n_q_heads", 12, _abi.TQ_ERR_UNSUPPORTED),
+    ("n_q_heads", 9, _abi.TQ_ERR_INVALID_ARG), ("max_ctx", 0, _abi.TQ_ERR_INVALID_ARG),
+])
+def test_invalid_configs_rejected(field, value, status):
+    lib = _abi.load()
+    cfg = tqm.config(n_kv_heads=2, n_q_heads=8)
+    setattr(cfg, field, value)
+    assert lib.tq_tables_bytes(ctypes.byref(cfg)) == 0
+    ctx = ctypes.c_void_p()
+    assert lib.tq_init_codebooks(ctypes.byref(cfg), None, 0, None, ctypes.byref(ctx)) == status
+    assert not ctx.value
+    assert lib.tq_last_error()
+
+
+def test_null_and_host_only_misuse_is_rejected():
+    lib = _abi.load()
+    assert lib.tq_init_codebooks(None, None, 0, None, None) == _abi.TQ_ERR_INVALID_ARG
+    h = tqm.HostTables(tqm.config())
+    # device calls on a host-only context are refused before any launch
+    assert lib.tq_cache_bind(h.ctx, ctypes.c_void_p(256), 1 << 30, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_quantize_append(h.ctx, 0, None, None, 0, None, None, 1, 1, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_decode_attention(h.ctx, 0, None, None, None, 1, 0.0, None, 0, 0, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_ring_flush(h.ctx, 0, None, 1, None) == _abi.TQ_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("seed", [0, 1, 12345])
+def test_tables_match_oracle_bitwise(d, seed):
+    h = tqm.HostTables(tqm.config(head_dim=d, seed=seed))
+    D, S, c, t = h.tables()
+    assert np.array_equal(D.astype(np.float64), rademacher_signs(seed, d))
+    S_lib = (S.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert np.array_equal(S_lib, gaussian_matrix_bf16(seed, d))
+    g = json.load(open(os.path.join(GOLDEN, "codebooks.json")))["codebooks"][f"d{d}_b2"]
+    assert np.allclose(c, g["centroids"], rtol=0, atol=1e-13)
+    assert np.allclose(t, g["boundaries"], rtol=0, atol=1e-13)
+    assert t[1] == 0.0 and np.array_equal(c, -c[::-1])
+    # the fp32 values the kernels use agree exactly
+    assert np.array_equal(c.astype(np.float32), np.array(g["centroids"]).astype(np.float32))
+
+
+@pytest.mark.parametrize("d,vb,expect", [(128, 2, 92), (128, 4, 124), (256, 2, 180), (256, 4, 244)])
+def test_page_bytes_equal_canonical_records(d, vb, expect):
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+    assert h.key_record_bytes() + h.value_record_bytes() == expect
+    assert h.page_bytes() == 128 * expect
+
+
+def _random_records(h, n, rng):
+    kr = rng.integers(0, 256, size=(n, h.key_record_bytes()), dtype=np.uint8)
+    vr = rng.integers(0, 256, size=(n, h.value_record_bytes()), dtype=np.uint8)
+    return kr, vr
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2), (256, 4)])
+def test_records_page_round_trip(d, vb):
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+    rng = np.random.default_rng(d + vb)
+    kr, vr = _random_records(h, 128, rng)
+    page = h.records_to_page(kr, vr)
+    k2, v2 = h.page_to_records(page, 128)
+    assert np.array_equal(k2, kr) and np.array_equal(v2, vr)
+    # partial page: the unused tail is zero and the first tokens survive
+    page = h.records_to_page(kr[:37], vr[:37])
+    k3, v3 = h.page_to_records(page, 37)
+    assert np.array_equal(k3, kr[:37]) and np.array_equal(v3, vr[:37])
+
+
+def _unpack(rec, bits, d):
+    per = 8 // bits
+    b = rec[:, :d * bits // 8]
+    sh = (np.arange(per) * bits).astype(np.uint8)
+    return ((b[:, :, None] >> sh) & ((1 << bits) - 1)).reshape(rec.shape[0], d)
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2), (256, 4)])
+def test_decoder_operand_extraction_matches_records(d, vb):
+    """Emulate, on the CPU, how the decode kernel cuts mma.sync operands out of a page.
+
+    Key side (fp8 m16n8k32, B operand): every byte of b0/b1 must be 0 or the power of two of its bit
+    position, set exactly when the bit-plane value of (token, coordinate) is 1.
+    Value side (f16 m16n8k16, A operand): every f16 half must equal code * 2^(pos - 24) for the
+    position that the B operand is prescaled with.
+    """
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+    rng = np.random.default_rng(7)
+    kr, vr = _random_records(h, 128, rng)
+    page = h.records_to_page(kr, vr)
+    idx = _unpack(kr, 2, d)
+    sign = _unpack(kr[:, d // 4:], 1, d)
+    codes = _unpack(vr, vb, d)
+    planes = [(idx >> 1) & 1, idx & 1, sign]
+    kw = page[:3 * 128 * d // 8].view(np.uint32)
+    halves = d // 128
+    e4m3_bits = {0: 0x01, 1: 0x02, 2: 0x04, 3: 0x08, 4: 0x10, 5: 0x20}
+    for nt in range(16):
+        for pi in range(3):
+            for hf in range(halves):
+                for lane in range(32):
+                    g, c = lane >> 2, lane & 3
+                    w = int(kw[((nt * 3 + pi) * halves + hf) * 32 + lane])
+                    for ks in range(4):
+                        if ks < 3:
+                            b0, b1 = w & (0x01010101 << (2 * ks)), w & (0x02020202 << (2 * ks))
+                            p0, p1 = 2 * ks, 2 * ks + 1
+                        else:
+                            b0, b1 = (w >> 2) & 0x10101010, (w >> 2) & 0x20202020
+                            p0, p1 = 4, 5
+                        for reg, p, kbase in ((b0, p0, 0), (b1, p1, 16)):
+                            for i in range(4):
+                                byte = (reg >> (8 * i)) & 0xFF
+                                j = 128 * hf + 32 * ks + kbase + 4 * c + i
+                                expect = e4m3_bits[p] if planes[pi][8 * nt + g, j] else 0
+                                assert byte == expect
+    off = 3 * 128 * d // 8 + 4 * 128
+    vw = page[off:off + 128 * d * vb // 8].view(np.uint32)
+    nmt = d // 16
+    pos2 = {(0, 0): 0, (0, 1): 4, (1, 0): 6, (1, 1): 8}
+    for blk in range(4):
+        for mt in range(nmt):
+            for lane in range(32):
+                g, c = lane >> 2, lane & 3
+                if vb == 2:
+                    w = int(vw[(blk * nmt + mt) * 32 + lane])
+                    w2, w6 = w >> 2, w >> 6
+                    regs = {0: [w & 0x00030003, w2 & 0x00030003, w & 0x00300030, w6 & 0x00300030],
+                            1: [w & 0x00C000C0, w6 & 0x00C000C0, w & 0x03000300, w6 & 0x03000300]}
+                else:
+                    x = int(vw[((blk * nmt + mt) * 32 + lane) * 2])
+                    y = int(vw[((blk * nmt + mt) * 32 + lane) * 2 + 1])
+                    regs = {0: [x & 0x000F000F, (x >> 8) & 0x000F000F, x & 0x00F000F0, (x >> 8) & 0x00F000F0],
+                            1: [y & 0x000F000F, (y >> 8) & 0x000F000F, y & 0x00F000F0, (y >> 8) & 0x00F000F0]}
+                for kap in (0, 1):
+                    for r in range(4):
+                        rowhi, hiT = r & 1, r >> 1
+                        pos = pos2[(kap, hiT)] if vb == 2 else (4 if hiT else 0)
+                        for e in (0, 1):
+                            half = (regs[kap][r] >> (16 * e)) & 0xFFFF
+                            val = np.array([half], np.uint16).view(np.float16).astype(np.float64)[0]
+                            t = 32 * blk + 16 * kap + 8 * hiT + 2 * c + e
+                            j = 16 * mt + 8 * rowhi + g
+                            assert val == codes[t, j] * 2.0 ** (pos - 24)

@@ -1,0 +1,192 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on the same seeded inputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kv_cache_quantization_quantize_gb300 import TurboQuantCache, config, synth
+from tests.parity import check_key_records, check_value_records, rel_l2
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from kv_cache_quantization_quantize_gb300 import build
+    build.build()
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _i32(x):
+    return torch.tensor(x, dtype=torch.int32, device=DEV)
+
+
+def _oracle_tables(cache):
+    D, S, c, t = cache.tables()
+    S64 = (S.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return D.astype(np.float64), S64, c, t
+
+
+def _check_sequence(cache, layer, slot, k_all, v_all, tables, heads=None):
+    """k_all, v_all: [L, Hkv, d] torch (bf16/f32 on any device): check packed records and ring."""
+    D, S, c, t = tables
+    L = k_all.shape[0]
+    Lg, F = cache.state(layer, slot)
+    assert Lg == L
+    Np, R = oracle.history_split(L)
+    P = Np + F
+    stats = []
+    for h in (range(k_all.shape[1]) if heads is None else heads):
+        kr, vr = cache.records(layer, slot, h, P)
+        if P:
+            kk = oracle.unpack_key_records(kr, cache.cfg.head_dim)
+            vv = oracle.unpack_value_records(vr, cache.cfg.head_dim, cache.cfg.value_bits)
+            stats.append(check_key_records(kk, _f64(k_all[:P, h]), D, S, c, t))
+            stats.append(check_value_records(vv, _f64(v_all[:P, h]), D, cache.cfg.value_bits))
+        rk, rv = cache.ring(layer, slot, h)
+        assert torch.equal(rk[:R].cpu(), k_all[Np:L, h].to(torch.bfloat16).cpu())
+        assert torch.equal(rv[:R].cpu(), v_all[Np:L, h].to(torch.bfloat16).cpu())
+    return stats
+
+
+def _oracle_decode(cache, layer, slot, q_row, tables, scale=None):
+    """Oracle hybrid attention for one sequence on the device's own packed records and ring."""
+    D, S, c, t = tables
+    cfg = cache.cfg
+    G = cfg.n_q_heads // cfg.n_kv_heads
+    L, F = cache.state(layer, slot)
+    Np, R = oracle.history_split(L)
+    P = Np + F
+    out = np.zeros((cfg.n_q_heads, cfg.head_dim))
+    for h in range(cfg.n_kv_heads):
+        kr, vr = cache.records(layer, slot, h, P)
+        keys = oracle.unpack_key_records(kr, cfg.head_dim) if P else None
+        vals = oracle.unpack_value_records(vr, cfg.head_dim, cfg.value_bits) if P else None
+        rk, rv = cache.ring(layer, slot, h)
+        out[h * G:(h + 1) * G] = oracle.decode_attention(
+            _f64(q_row[h * G:(h + 1) * G]), keys, vals, _f64(rk[F:R]), _f64(rv[F:R]), D, S, c, softmax_scale=scale)
+    return out
+
+
+def test_tiny_single_head_config():
+    """1 layer, 1 KV head, 1 query head, d=128: 1024 packed + 128 ring tokens, fp32 N(0,1), seed 0,
+    K channels 3 and 77 scaled x8; 3-bit keys, 2-bit values (g32); one decode step."""
+    cfg = config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0)
+    cache = TurboQuantCache(cfg)
+    k, v = synth.kv_tokens(1152, 1, 128, seed=0, outliers=("fixed", (3, 77), 8.0), dtype=torch.float32)
+    cache.append(0, k[None].to(DEV).contiguous(), v[None].to(DEV).contiguous(), _i32([0]), _i32([1152]))
+    torch.cuda.synchronize()
+    tables = _oracle_tables(cache)
+    assert cache.state(0, 0) == (1152, 0)
+    _check_sequence(cache, 0, 0, k, v, tables)
+    q = synth.queries(1, 1, 128, seed=0)
+    out = cache.decode(0, q.to(DEV), _i32([0]))
+    ref = _oracle_decode(cache, 0, 0, q[0], tables)
+    assert rel_l2(out[0].cpu().numpy(), ref) <= 2e-3
+    assert cache.check_status() == 0
+
+
+@pytest.mark.parametrize("d,vb,G", [(128, 2, 4), (128, 4, 4), (256, 2, 4), (256, 4, 2), (128, 2, 1)])
+def test_ragged_batch_appends_and_decode(d, vb, G):
+    """Ragged lengths across several tiles and a ragged tail: 1, 127, 128, 129, 300, 1000 tokens,
+    built by a prefill append and then single-token decode appends (ring overflow and flush)."""
+    Hkv = 2
+    lens = [1, 127, 128, 129, 300, 1000]
+    B = len(lens)
+    cfg = config(head_dim=d, value_bits=vb, n_layers=2, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=8,
+                 max_ctx=1200, seed=11)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    layer, decode_steps = 1, 3
+    seqs = [synth.kv_tokens(L + decode_steps, Hkv, d, seed=100 + i, outliers=("random", 4, 10.0))
+            for i, L in enumerate(lens)]
+    slots = [7, 0, 3, 1, 5, 2]
+    max_new = max(lens)
+    kb = torch.zeros(B, max_new, Hkv, d, dtype=torch.bfloat16)
+    vbuf = torch.zeros_like(kb)
+    for i, L in enumerate(lens):
+        kb[i, :L] = seqs[i][0][:L]
+        vbuf[i, :L] = seqs[i][1][:L]
+    cache.append(layer, kb.to(DEV), vbuf.to(DEV), _i32(slots), _i32(lens))
+    for s in range(decode_steps):
+        kd = torch.stack([seqs[i][0][L + s] for i, L in enumerate(lens)])[:, None].contiguous()
+        vd = torch.stack([seqs[i][1][L + s] for i, L in enumerate(lens)])[:, None].contiguous()
+        cache.append(layer, kd.to(DEV), vd.to(DEV), _i32(slots), _i32([1] * B))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    for i, L in enumerate(lens):
+        _check_sequence(cache, layer, slots[i], seqs[i][0], seqs[i][1], tables)
+    q = synth.queries(B, Hkv * G, d, seed=5)
+    for scale in (0.0, 0.05):
+        out = cache.decode(layer, q.to(DEV), _i32(slots), softmax_scale=scale).cpu().numpy()
+        for i in range(B):
+            ref = _oracle_decode(cache, layer, slots[i], q[i], tables, scale=None if scale == 0 else scale)
+            for hq in range(Hkv * G):
+                assert rel_l2(out[i, hq], ref[hq]) <= 2e-3, (i, hq, rel_l2(out[i, hq], ref[hq]))
+    # other layer untouched: empty sequences attend to nothing
+    out0 = cache.decode(0, q.to(DEV), _i32(slots)).cpu()
+    assert torch.all(out0 == 0)
+
+
+def test_ring_flush_then_decode_and_overflow():
+    d, vb, G, Hkv = 128, 2, 4, 2
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
+                 max_ctx=600, seed=3)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    k, v = synth.kv_tokens(400, Hkv, d, seed=9)
+    cache.append(0, k[None, :290].to(DEV).contiguous(), v[None, :290].to(DEV).contiguous(), _i32([1]), _i32([290]))
+    cache.flush(0, _i32([1]))
+    torch.cuda.synchronize()
+    assert cache.state(0, 1) == (290, 34)  # 256 packed + 34-token ring, flushed in full
+    _check_sequence(cache, 0, 1, k[:290], v[:290], tables)
+    q = synth.queries(1, Hkv * G, d, seed=1)
+    out = cache.decode(0, q.to(DEV), _i32([1])).cpu().numpy()
+    ref = _oracle_decode(cache, 0, 1, q[0], tables)
+    assert rel_l2(out[0], ref) <= 2e-3
+    # continue appending past the block: the flushed block is re-quantised identically
+    cache.append(0, k[None, 290:400].to(DEV).contiguous(), v[None, 290:400].to(DEV).contiguous(), _i32([1]), _i32([110]))
+    torch.cuda.synchronize()
+    assert cache.state(0, 1) == (400, 0)
+    _check_sequence(cache, 0, 1, k[:400], v[:400], tables)
+    # capacity overflow is reported on the device status word and leaves the row untouched
+    big = torch.zeros(1, 300, Hkv, d, dtype=torch.bfloat16, device=DEV)
+    cache.append(0, big, big, _i32([1]), _i32([300]))
+    assert cache.check_status() & 0x1
+    assert cache.state(0, 1) == (400, 0)
+    # a bad sequence id is reported and skipped
+    cache.append(0, big[:, :1].contiguous(), big[:, :1].contiguous(), _i32([5]), _i32([1]))
+    assert cache.check_status() & 0x2
+
+
+def test_full_size_llama_layer_sampled():
+    """One layer at the Llama-3.1-8B decode shape (32 q heads, 8 KV heads, d=128, 32K context, K3/V2,
+    bf16 N(0,1) seed 1 with 4 random K channels x10), in the bench's launch configuration; sampled heads
+    are checked against the oracle."""
+    d, Hkv, Hq, L = 128, 8, 32, 32768
+    cfg = config(head_dim=d, value_bits=2, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=1, max_ctx=L + 64, seed=1)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    k, v = synth.kv_tokens(L, Hkv, d, seed=1, outliers=("random", 4, 10.0), device=DEV)
+    cache.append(0, k[None].contiguous(), v[None].contiguous(), _i32([0]), _i32([L]))
+    q = synth.queries(1, Hq, d, seed=1)
+    out = cache.decode(0, q.to(DEV), _i32([0]), max_ctx_hint=L).cpu().numpy()
+    assert cache.check_status() == 0
+    kc, vc = k.cpu(), v.cpu()
+    for h in (0, 5):
+        _check_sequence(cache, 0, 0, kc, vc, tables, heads=[h])
+    G = Hq // Hkv
+    D, S, c, t = tables
+    Np, R = oracle.history_split(L)
+    for h in (0, 5):
+        kr, vr = cache.records(0, 0, h, Np)
+        keys = oracle.unpack_key_records(kr, d)
+        vals = oracle.unpack_value_records(vr, d, 2)
+        rk, rv = cache.ring(0, 0, h)
+        ref = oracle.decode_attention(_f64(q[0, h * G:(h + 1) * G]), keys, vals, _f64(rk[:R]), _f64(rv[:R]), D, S, c)
+        for g in range(G):
+            assert rel_l2(out[0, h * G + g], ref[g]) <= 2e-3
