@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark of the TurboQuant KV-cache hot path on GB300 (one JSON line on stdout).
+
+Workload (N=1): the Llama-3.1-8B-shaped decode.
+* Shape: 32 layers, 32 query heads, 8 KV heads (GQA 4:1), head_dim 128, batch 1, context 32768.
+* Codes: 3-bit keys (2-bit Lloyd-Max + 1-bit QJL), 2-bit values in groups of 32, 128-token bf16 ring.
+* Inputs: bf16 N(0,1) with 4 random K channels per head scaled x10, generated per layer with seed 1000+layer.
+
+One step = for every layer: append one token (ring write; ring overflow quantises a 128-token block)
+and run hybrid decode attention. The step is captured once as a CUDA graph and replayed. The
+sequence state lives on the device, so every replay advances the context by one token.
+
+Each step reads about 785 MB of packed records, more than the 129 MB L2. Consecutive steps
+therefore cannot hit L2 for the previous step's layers, and no flush is needed.
+
+Also reported:
+* roofline: the split-K decode kernel alone, from a graph of its 32 per-layer launches, against
+  the measured copy bandwidth.
+* e2e: the same step through the public API, with pinned-host H2D copies of q/k/v and D2H of the
+  output inside the timed region.
+* quantize: bulk prefill of 65536 bf16 tokens x 8 KV heads x 32 layers (seed 4, K outliers), in tok/s.
+* cpu_baseline: the fp64 oracle timed on a bounded sample, on this host's cores.
+
+`--impl reference` times the oracle as the reference arm, on the same metric and workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn context-tok/s & packed-KV HBM GB/s (% of 8 TB/s); quantize tok/s"
+UNIT = "context-tok/s"
+WL = dict(name="llama3.1-8b-shaped decode, batch 1, context 32768, K3/V2",
+          layers=32, hq=32, hkv=8, d=128, batch=1, ctx=32768, vb=2, outliers=("random", 4, 10.0))
+PREFILL = dict(tokens=65536, hkv=8, layers=32, d=128, vb=2, seed=4)
+NOMINAL_HBM_GBS = 8000.0
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------------------------
+# nvidia-smi clock sampler (runs during warm-up and the timed region)
+# --------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-i", str(self.gpu_id),
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [s for t, s in self.samples if t0 <= t <= t1 and len(s) >= 9]
+        window = "timed"
+        if not inside:
+            inside = [s for _, s in self.samples if len(s) >= 9]
+            window = "warm-up and timed (timed region shorter than the sampling period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "note": "nvidia-smi unavailable"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[1]) for s in inside if num(s[1]) is not None]
+        mx = [num(s[2]) for s in inside if num(s[2]) is not None]
+        pw = [num(s[3]) for s in inside if num(s[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i in range(4) if s[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# --------------------------------------------------------------------------------------------
+# our arm
+# --------------------------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from kv_cache_quantization_quantize_gb300 import build as _build
+    _build.build()
+    import kv_cache_quantization_quantize_gb300 as tqm
+    from kv_cache_quantization_quantize_gb300 import synth
+
+    K, W = args.steps, args.warmup
+    L_layers, Hq, Hkv, d, B, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["batch"], WL["ctx"], WL["vb"]
+    n_e2e_warm = 2
+    extra = 1 + W + K + (n_e2e_warm + K) + K + 8  # tokens appended after prefill by all passes
+    max_ctx = ctx + extra
+    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=B,
+                     max_ctx=max_ctx, seed=1)
+    cache = tqm.TurboQuantCache(cfg, device=dev)
+    ids = torch.arange(B, dtype=torch.int32, device=dev)
+    L0 = ctx - W - 2  # after the eager step and the W warm-up replays the first timed step attends ctx tokens
+    n0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
+    for l in range(L_layers):
+        k, v = synth.kv_tokens(L0, Hkv, d, seed=1000 + l, outliers=WL["outliers"], device=dev)
+        cache.append(l, k[None].expand(B, -1, -1, -1).contiguous(), v[None].expand(B, -1, -1, -1).contiguous(), ids, n0)
+        del k, v
+    torch.cuda.synchronize()
+    if cache.check_status():
+        raise RuntimeError("device status after prefill")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    knew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    vnew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    qs = torch.randn((L_layers, B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    outs = torch.empty((L_layers, B, Hq, d), dtype=torch.float32, device=dev)
+    ones = torch.ones(B, dtype=torch.int32, device=dev)
+    ws = cache.workspace(B, max_ctx)
+
+    def step():
+        for l in range(L_layers):
+            cache.append(l, knew[l], vnew[l], ids, ones)
+            cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws)
+
+    s = torch.cuda.Stream(device=dev)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # eager: sets kernel attributes before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    launches_per_step = L_layers * 5  # quantize + ring update + prep + split-K + combine per layer
+
+    gpu_id = local
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    L_first = cache.state(0, 0)[0] + 1
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record()
+    for _ in range(K):
+        g.replay()
+    ev1.record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        dist.barrier()
+    time.sleep(0.2)
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    status = cache.check_status()
+    ctx_tokens = sum(B * (L_first + i) for i in range(K))  # each step attends its full context
+    # max over ranks of the timed region; whole-job throughput
+    t_max = ms
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    value = ctx_tokens * world / (t_max * 1e-3)
+    ms_per_step = t_max / K
+
+    # algorithmic bytes per step: packed K3/V2 records + ring (K,V bf16) + q + out, all layers
+    rec = (d // 4 + d // 8 + 4) + (d * vb // 8 + d // 16)
+    Lmid = L_first + (K - 1) / 2.0
+    packed = 128 * ((Lmid - 1) // 128)
+    ring = Lmid - packed
+    step_bytes = L_layers * B * (Hkv * (packed * rec + ring * d * 2 * 2) + Hq * d * (2 + 4))
+    hbm_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # ---- roofline of the split-K kernel alone: graph of its 32 per-layer launches ----
+    for l in range(L_layers):
+        cache.decode_phase(0, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        for l in range(L_layers):
+            cache.decode_phase(1, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws)
+    for _ in range(3):
+        g2.replay()
+    torch.cuda.synchronize()
+    Lk, Fk = cache.state(0, 0)
+    packed_k = 128 * ((Lk - 1) // 128) + Fk
+    ring_k = Lk - packed_k
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(K, 10)
+    e0.record()
+    for _ in range(reps):
+        g2.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
+    kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
+    kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "k_decode_traffic.json")
+    if os.path.exists(tfile):
+        try:
+            traffic = json.load(open(tfile)).get("bytes_per_launch")
+        except Exception:
+            traffic = None
+
+    # ---- end to end through the public API with pinned host buffers ----
+    hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
+    hk = torch.empty(knew.shape, dtype=knew.dtype, pin_memory=True)
+    hv = torch.empty(vnew.shape, dtype=vnew.dtype, pin_memory=True)
+    ho = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
+    hq.copy_(qs)
+    hk.copy_(knew)
+    hv.copy_(vnew)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = ho.numel() * 4
+
+    def e2e_step():
+        with torch.cuda.stream(s):
+            qs.copy_(hq, non_blocking=True)
+            knew.copy_(hk, non_blocking=True)
+            vnew.copy_(hv, non_blocking=True)
+            g.replay()
+            ho.copy_(outs, non_blocking=True)
+
+    for _ in range(n_e2e_warm):
+        e2e_step()
+    torch.cuda.synchronize()
+    L_e2e = cache.state(0, 0)[0] + 1
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(s)
+    for _ in range(K):
+        e2e_step()
+    f1.record(s)
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1)
+    e2e_value = sum(B * (L_e2e + i) for i in range(K)) * world / (e2e_ms * 1e-3)
+    if cache.check_status():
+        status |= 1 << 16
+
+    # ---- bulk prefill quantise (tok/s over all layers and heads) ----
+    quant = None
+    if not args.skip_quantize:
+        del g, g2
+        quant = bench_quantize(tqm, synth, dev, args, peak)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3/f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
+        "config": {"workload": WL["name"], "layers": L_layers, "q_heads": Hq, "kv_heads": Hkv, "head_dim": d,
+                   "batch_per_gpu": B, "context": ctx, "value_bits": vb, "ring": 128,
+                   "l2": "inputs larger than L2 (~785 MB of packed records per step vs 129 MB L2)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "step": "append 1 token + hybrid decode attention, all 32 layers, one CUDA graph replay"},
+        "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
+        "pct_of_measured_hbm": 100.0 * hbm_gbs / peak,
+        "roofline": {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
+                     "achieved": kern_gbs, "peak": peak, "unit": "GB/s", "frac": kern_gbs / peak,
+                     "peak_kind": peak_kind, "traffic": traffic, "bytes_per_launch": kern_bytes,
+                     "us_per_launch": kern_us, "frac_of_8TBps": kern_gbs / NOMINAL_HBM_GBS},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms / K},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if quant is not None:
+        line["quantize_tok_s"] = quant["tok_s"]
+        line["quantize"] = quant
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def bench_quantize(tqm, synth, dev, args, peak):
+    import torch
+    T, Hkv, L_layers, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["layers"], PREFILL["d"], PREFILL["vb"]
+    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=4 * Hkv, max_seqs=1,
+                     max_ctx=T, seed=PREFILL["seed"])
+    qc = tqm.TurboQuantCache(cfg, device=dev)
+    k, v = synth.kv_tokens(T, Hkv, d, seed=PREFILL["seed"], outliers=WL["outliers"], device=dev)
+    k, v = k[None].contiguous(), v[None].contiguous()
+    ids = torch.zeros(1, dtype=torch.int32, device=dev)
+    nn = torch.full((1,), T, dtype=torch.int32, device=dev)
+
+    def one_pass():
+        qc.reset(ids)
+        for l in range(L_layers):
+            qc.append(l, k, v, ids, nn)
+
+    for _ in range(2):
+        one_pass()
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        one_pass()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    if qc.check_status():
+        raise RuntimeError("device status after quantise")
+    rec = (d // 4 + d // 8 + 4) + (d * vb // 8 + d // 16)
+    packed = 128 * ((T - 1) // 128)
+    ring = T - packed
+    bytes_pass = L_layers * Hkv * (T * d * 2 * 2 + packed * rec + ring * d * 2 * 2)
+    gbs = bytes_pass / (ms * 1e-3) / 1e9
+    return {"tok_s": T / (ms * 1e-3), "token_head_layers_per_s": T * Hkv * L_layers / (ms * 1e-3),
+            "ms_per_pass": ms, "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K3/V{vb}",
+            "path": "CUDA-core quantise kernel (fp32 FMA QJL projection)",
+            "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
+
+
+# --------------------------------------------------------------------------------------------
+# oracle timing (cpu_baseline leg and --impl reference)
+# --------------------------------------------------------------------------------------------
+def oracle_sample_setup():
+    """Packed records + ring of one (layer 0, KV head 0) unit of the workload, built by the oracle."""
+    import numpy as np
+    import oracle
+    from kv_cache_quantization_quantize_gb300 import synth
+    d, ctx, Hkv = WL["d"], WL["ctx"], WL["hkv"]
+    k, v = synth.kv_tokens(ctx, Hkv, d, seed=1000, outliers=WL["outliers"])
+    k = k[:, 0].double().numpy()
+    v = v[:, 0].double().numpy()
+    D = oracle.rademacher_signs(1, d)
+    S = oracle.gaussian_matrix_bf16(1, d)
+    c, t = oracle.lloyd_max_codebook(d, 2)
+    Np, R = oracle.history_split(ctx)
+    keys = oracle.quantize_keys(k[:Np], D, S, c, t)
+    vals = oracle.quantize_values(v[:Np], D, WL["vb"])
+    q = np.random.default_rng(0).standard_normal((WL["hq"] // Hkv, d))
+    return dict(keys=keys, vals=vals, rk=k[Np:], rv=v[Np:], q=q, D=D, S=S, c=c, t=t, k_new=k[-1:], v_new=v[-1:])
+
+
+def oracle_unit_step(st):
+    """One decode step of one (layer, KV head): quantise the new token's records, then attend."""
+    import oracle
+    oracle.quantize_keys(st["k_new"], st["D"], st["S"], st["c"], st["t"])
+    oracle.quantize_values(st["v_new"], st["D"], WL["vb"])
+    return oracle.decode_attention(st["q"], st["keys"], st["vals"], st["rk"], st["rv"], st["D"], st["S"], st["c"])
+
+
+def cpu_baseline(args):
+    """Times the oracle in a child process so that its thread count is known."""
+    cores = os.cpu_count() or 1
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[var] = str(cores)
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "150"], env=env,
+                           capture_output=True, text=True, timeout=600)
+        res = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception as e:  # report, do not fail the GPU line
+        return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": f"failed: {e}"}
+    return {"value": res["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": res["sample"], "seconds": res["seconds"]}
+
+
+def oracle_sample_main(reps):
+    st = oracle_sample_setup()
+    oracle_unit_step(st)  # warm
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_unit_step(st)
+    dt = (time.perf_counter() - t0) / reps
+    units = WL["layers"] * WL["hkv"]
+    step_s = dt * units  # extrapolated linearly to all layers and KV heads
+    value = WL["batch"] * WL["ctx"] / step_s
+    print(json.dumps({"value": value, "seconds": dt * reps,
+                      "sample": f"{reps} decode steps of 1 layer x 1 KV head (4 query heads, {WL['ctx']} context) "
+                                f"timed; extrapolated linearly x{units} (32 layers x 8 KV heads)"}))
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    st = oracle_sample_setup()
+    for _ in range(args.warmup):
+        oracle_unit_step(st)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_unit_step(st)
+    dt = (time.perf_counter() - t0) / max(args.steps, 1)
+    units = WL["layers"] * WL["hkv"]
+    value = WL["batch"] * WL["ctx"] / (dt * units)
+    cores = os.cpu_count() or 1
+    sample = (f"each step = 1 layer x 1 KV head (4 query heads) of the {WL['ctx']}-token decode step, "
+              f"extrapolated linearly x{units}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * units * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WL["name"], "context": WL["ctx"], "layers": WL["layers"], "kv_heads": WL["hkv"],
+                       "q_heads": WL["hq"], "head_dim": WL["d"], "value_bits": WL["vb"]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--skip-quantize", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
+    args = p.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.oracle_sample:
+        oracle_sample_main(args.oracle_sample)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

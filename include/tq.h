@@ -150,6 +150,18 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream);
 
+/* tq_decode_phase: launches one phase of tq_decode_attention with the same arguments, for callers that
+ * interleave the phases with other work or time them one by one. The three phases run in order on
+ * one workspace:
+ *   0 = query prep (rotate, project, fp8 operand limbs);
+ *   1 = split-K decode over packed pages plus the exact ring split;
+ *   2 = combine (log-sum-exp merge, inverse rotation, ring merge -> out).
+ * Phase 1 needs phase 0's workspace and phase 2 needs phase 1's. Calling them in the order 0, 1, 2 is
+ * equivalent to one tq_decode_attention call. */
+tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                          int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                          int max_ctx_hint, tq_stream_t stream);
+
 /* Synchronises `stream` and reads the device status word. It returns TQ_OK if the word is zero.
  * Otherwise it returns TQ_ERR_DEVICE and stores the word in *word (if non-NULL). `clear` != 0
  * zeroes the word afterwards. */

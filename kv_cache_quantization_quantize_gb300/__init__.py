@@ -140,6 +140,15 @@ class TurboQuantCache(HostTables):
                                            float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint, _stream(stream)))
         return out
 
+    def decode_phase(self, phase, layer, q, seq_ids, out, softmax_scale=0.0, max_ctx_hint=0, workspace=None,
+                     stream=None):
+        """One phase (0 prep, 1 splits, 2 combine) of decode(); the three in order equal decode()."""
+        batch = q.shape[0]
+        ws = workspace if workspace is not None else self.workspace(batch, max_ctx_hint)
+        check(self.lib.tq_decode_phase(self.ctx, phase, layer, _ptr(q), _ptr(out), _ptr(seq_ids), batch,
+                                       float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint, _stream(stream)))
+        return out
+
     def check_status(self, clear=True, stream=None):
         """Device status word (0 = fine); raises TQError on a non-zero word unless clear-and-return is wanted."""
         w = ctypes.c_uint32(0)

@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(kDThreads) k_combine(DecodeArgs a) {
 }
 
 template <int D, int VB>
-cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, cudaStream_t s) {
+cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s) {
   constexpr int STAGES = D == 128 ? 4 : 3;
   const PageLayout pl = page_layout(D, VB);
   const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * (D / 32) + 16 * D);
@@ -645,22 +645,33 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, cudaStream_t s) {
   size_t smem = 128 + (size_t)STAGES * pl.bytes;
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_bytes);
-  cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  k_prep<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_decode<D, VB, STAGES><<<dim3(a.plan.n_splits + 1, a.lv.Hkv, batch), kDThreads, smem, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  k_combine<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  static bool attr_set = false;  // set once, outside any stream capture that follows
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  if (phase < 0 || phase == 0) {
+    k_prep<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (phase < 0 || phase == 1) {
+    k_decode<D, VB, STAGES><<<dim3(a.plan.n_splits + 1, a.lv.Hkv, batch), kDThreads, smem, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (phase < 0 || phase == 2) {
+    k_combine<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
+    return cudaGetLastError();
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
-                          int batch, float scale, void* ws, const DecodePlan& plan, cudaStream_t s) {
+                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s) {
   DecodeArgs a;
   a.lv = layer_view(ctx, layer);
   a.q = static_cast<const uint16_t*>(q);
@@ -670,10 +681,10 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.ws = static_cast<uint8_t*>(ws);
   a.plan = plan;
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
-  if (d == 128 && vb == 2) return launch_decode_dv<128, 2>(a, batch, s);
-  if (d == 128 && vb == 4) return launch_decode_dv<128, 4>(a, batch, s);
-  if (d == 256 && vb == 2) return launch_decode_dv<256, 2>(a, batch, s);
-  return launch_decode_dv<256, 4>(a, batch, s);
+  if (d == 128 && vb == 2) return launch_decode_dv<128, 2>(a, batch, phase, s);
+  if (d == 128 && vb == 4) return launch_decode_dv<128, 4>(a, batch, phase, s);
+  if (d == 256 && vb == 2) return launch_decode_dv<256, 2>(a, batch, phase, s);
+  return launch_decode_dv<256, 4>(a, batch, phase, s);
 }
 
 }  // namespace tq

@@ -400,9 +400,28 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   return tq::decode_plan(ctx, batch, max_ctx_hint).bytes;
 }
 
+static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                               int max_ctx_hint, tq_stream_t stream);
+
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream) {
+  return decode_common(ctx, -1, layer, q, out, d_seq_ids, batch, softmax_scale, d_workspace, workspace_bytes,
+                       max_ctx_hint, stream);
+}
+
+tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                          int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                          int max_ctx_hint, tq_stream_t stream) {
+  if (phase < 0 || phase > 2) return fail(TQ_ERR_INVALID_ARG, "phase %d not in {0, 1, 2}", phase);
+  return decode_common(ctx, phase, layer, q, out, d_seq_ids, batch, softmax_scale, d_workspace, workspace_bytes,
+                       max_ctx_hint, stream);
+}
+
+static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
+                               int max_ctx_hint, tq_stream_t stream) {
   tq_status st = check_ready(ctx, layer);
   if (st != TQ_OK) return st;
   if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d negative", batch);
@@ -417,7 +436,8 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
   if (workspace_bytes < plan.bytes)
     return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
-  cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, (cudaStream_t)stream);
+  cudaError_t e =
+      tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, phase, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "decode kernels");
 }
 

@@ -148,7 +148,8 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
                           const int32_t* seq_ids, const int32_t* n_new, int batch, int max_new, cudaStream_t s);
 cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
 cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
+// phase -1 = all three phases; 0 = prep, 1 = splits, 2 = combine.
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
-                          int batch, float scale, void* ws, const DecodePlan& plan, cudaStream_t s);
+                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s);
 
 }  // namespace tq

@@ -356,8 +356,12 @@ size_t quantize_smem_bytes() {
 template <int D>
 cudaError_t launch_quantize_d(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
   const size_t smem = quantize_smem_bytes<D>();
-  cudaError_t e = cudaFuncSetAttribute(k_quantize_pages<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  static bool attr_set = false;  // set once, outside any stream capture that follows
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_pages<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
   dim3 grid(batch, a.lv.Hkv, pages);
   k_quantize_pages<D><<<grid, kQThreads, smem, s>>>(a);
   return cudaGetLastError();
