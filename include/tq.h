@@ -162,6 +162,23 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream);
 
+/* tq_decode_attention_noalloc: the same decode step as tq_decode_attention, for callers that cannot
+ * allocate device memory when they decode. Examples: code on a path where cudaMalloc's implicit
+ * synchronisation is forbidden, or a host runtime that owns all device memory and only hands over the
+ * operation's own tensors. The sources have no counterpart of this call; it is an ABI convenience.
+ *   - The caller passes only inputs and outputs (q, out, d_seq_ids). The scratch lives in a 4 MiB
+ *     device array inside libtq, which every GPU that loads the library holds until the process exits.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ *   - Sizes whose scratch (tq_workspace_bytes(ctx, batch, max_ctx_hint)) exceeds 4 MiB are rejected
+ *     with TQ_ERR_CAPACITY and a message; nothing is launched.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ *     that device current. Make that first call before any stream capture.
+ *   - Every call shares the one array, whose contents persist between calls. Nothing in it needs to
+ *     start at zero: each call writes every entry it later reads. Calls that overlap on the GPU (on
+ *     different streams, or from different host threads) race on it and give wrong results; order them. */
+tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                                      int batch, float softmax_scale, int max_ctx_hint, tq_stream_t stream);
+
 /* Synchronises `stream` and reads the device status word. It returns TQ_OK if the word is zero.
  * Otherwise it returns TQ_ERR_DEVICE and stores the word in *word (if non-NULL). `clear` != 0
  * zeroes the word afterwards. */

@@ -38,6 +38,8 @@ _SIGS = {
                                     c_int, c_void_p]),
     "tq_decode_phase": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p,
                                 c_size_t, c_int, c_void_p]),
+    "tq_decode_attention_noalloc": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_int,
+                                            c_void_p]),
     "tq_check_status": (c_int, [c_void_p, c_void_p, _P(ctypes.c_uint32), c_int]),
     "tq_destroy": (None, [c_void_p]),
     "tq_last_error": (ctypes.c_char_p, []),

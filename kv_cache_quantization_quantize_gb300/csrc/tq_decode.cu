@@ -14,6 +14,9 @@
 // m16n8k16) by P' = p * s * 2^(24-pos). The mid-rise offset (2^(b-1) - 1/2) * sum(p*s) is removed at
 // the end of the split.
 #include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
 
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -688,3 +691,76 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
 }
 
 }  // namespace tq
+
+// =============================================================================================
+// Decode without caller-provided scratch.
+//
+// Some callers cannot allocate device memory at the point where they decode. Examples:
+//   - a host thread that runs inside a graph-building or real-time path, where cudaMalloc
+//     (which can synchronise the device) is not allowed;
+//   - an embedding runtime that owns all device memory and exposes no allocator;
+//   - a plugin ABI that passes in only the tensors of the operation itself.
+// For them this variant takes only inputs and outputs. Its scratch (query-prep operands and split
+// partials) lives in the file-scope device array below, so it has a fixed maximum size.
+// =============================================================================================
+namespace tq {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB, held by every device that loads libtq
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device. The first call on each device looks it
+// up with cudaGetSymbolAddress; later calls reuse the cached address.
+cudaError_t noalloc_scratch(void** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace tq
+
+extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, float* out,
+                                                 const int32_t* d_seq_ids, int batch, float softmax_scale,
+                                                 int max_ctx_hint, tq_stream_t stream) {
+  tq_status st = tq::check_layer_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (batch < 0) return tq::set_error(TQ_ERR_INVALID_ARG, "batch is negative");
+  if (batch == 0) return tq::set_error(TQ_OK, "");
+  if (!q || !out || !d_seq_ids) return tq::set_error(TQ_ERR_INVALID_ARG, "NULL q/out/d_seq_ids");
+  if (batch > ctx->cfg.max_seqs) return tq::set_error(TQ_ERR_CAPACITY, "batch > max_seqs");
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return tq::set_error(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (!(softmax_scale == softmax_scale)) return tq::set_error(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
+  if (ctx->device >= tq::kMaxDevices) return tq::set_error(TQ_ERR_UNSUPPORTED, "device index >= 64");
+  const tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
+  if (plan.bytes > tq::kNoAllocScratchBytes) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "decode scratch of %zu bytes exceeds the built-in %zu-byte scratch of tq_decode_attention_noalloc; "
+             "lower batch or max_ctx_hint, or use tq_decode_attention with a caller workspace",
+             plan.bytes, tq::kNoAllocScratchBytes);
+    return tq::set_error(TQ_ERR_CAPACITY, msg);
+  }
+  void* scratch = nullptr;
+  cudaError_t e = tq::noalloc_scratch(&scratch);
+  if (e != cudaSuccess) return tq::set_error(TQ_ERR_CUDA, cudaGetErrorString(e));
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+  e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, scratch, plan, -1, (cudaStream_t)stream);
+  if (e != cudaSuccess) return tq::set_error(TQ_ERR_CUDA, cudaGetErrorString(e));
+  return tq::set_error(TQ_OK, "");
+}

@@ -240,6 +240,18 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   return p;
 }
 
+tq_status set_error(tq_status st, const char* msg) {
+  g_last_error = msg ? msg : "";
+  return st;
+}
+
+tq_status check_layer_ready(const tq_ctx* ctx, int layer) {
+  if (!ctx) return fail(TQ_ERR_INVALID_ARG, "ctx is NULL");
+  if (ctx->host_only || !ctx->d_cache) return fail(TQ_ERR_INVALID_ARG, "no cache bound (tq_cache_bind)");
+  if (layer < 0 || layer >= ctx->cfg.n_layers) return fail(TQ_ERR_INVALID_ARG, "layer %d out of range", layer);
+  return TQ_OK;
+}
+
 }  // namespace tq
 
 // =============================================================================================

@@ -144,6 +144,11 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint);
 
+// Records `msg` as the thread-local last error and returns `st` (for entry points outside tq_host.cpp).
+tq_status set_error(tq_status st, const char* msg);
+// True when ctx has a bound cache and `layer` is in range (sets the last error otherwise).
+tq_status check_layer_ready(const tq_ctx* ctx, int layer);
+
 cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const void* v, int dt,
                           const int32_t* seq_ids, const int32_t* n_new, int batch, int max_new, cudaStream_t s);
 cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
