@@ -145,7 +145,8 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
  *     scratch owned by the caller.
  *   - max_ctx_hint: an upper bound on every row's length (0 = cfg.max_ctx). It only sizes the grid;
  *     a row longer than the hint sets TQ_DEV_ERR_SPLITS.
- *   - Launches: query prep, split-K decode (+ ring split), combine. */
+ *   - Launches: query prep, then split-K decode (+ ring split); the last CTA of each (row, KV head)
+ *     runs the combine. */
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream);
@@ -153,11 +154,12 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
 /* tq_decode_phase: launches one phase of tq_decode_attention with the same arguments, for callers that
  * interleave the phases with other work or time them one by one. The three phases run in order on
  * one workspace:
- *   0 = query prep (rotate, project, fp8 operand limbs);
- *   1 = split-K decode over packed pages plus the exact ring split;
- *   2 = combine (log-sum-exp merge, inverse rotation, ring merge -> out).
- * Phase 1 needs phase 0's workspace and phase 2 needs phase 1's. Calling them in the order 0, 1, 2 is
- * equivalent to one tq_decode_attention call. */
+ *   0 = query prep (rotate, project, f16 operands of the key bit-plane MMAs);
+ *   1 = split-K decode over packed pages plus the exact ring split. The last CTA of every
+ *       (row, KV head) also runs the combine: log-sum-exp merge, inverse rotation, ring merge -> out;
+ *   2 = nothing (accepted for callers written against a separate combine phase).
+ * Phase 1 needs phase 0's workspace, including the arrival counters that phase 0 zeroes. Calling the
+ * phases in the order 0, 1, 2 is equivalent to one tq_decode_attention call. */
 tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream);

@@ -5,20 +5,19 @@
 //   s = scale * n * ( <Pi q, c[idx]> + sqrt(pi/2)/d * gamma * <S Pi q, 2 sign - 1> )  ([Guide] §二, TurboQuantProd).
 // The 2-bit codebook is odd-symmetric, so c[idx] = alpha*(2 b_hi - 1) + beta*(2 b_lo - 1), with
 // alpha = (c2+c3)/2 and beta = (c3-c2)/2. Each score is therefore a sum of three bit-plane dot
-// products.
-//   - They run on fp8 tensor cores (mma.sync m16n8k32 e4m3). Operand A = 4 fp8 limbs of the scaled
-//     query for up to 4 heads (16 rows). Operand B = key bits masked straight out of the packed
-//     words; each byte is 0 or a power of two.
-//   - The powers of two are undone by prescaling A.
-// Values. Code fields are masked into f16 subnormals code * 2^(pos-24) and multiplied (mma.sync
-// m16n8k16) by P' = p * s * 2^(24-pos). The mid-rise offset (2^(b-1) - 1/2) * sum(p*s) is removed at
-// the end of the split.
+// products on f16 tensor cores (mma.sync m16n8k16):
+//   - A = key bits masked straight out of the packed words. Bits 0..11 of an f16 half are exactly
+//     2^(q-24) when set, and 0 otherwise.
+//   - B = the query, prescaled by 2^(24-q), for up to 4 heads.
+//   - The -1 of each +-1 plane is a per-head constant, subtracted once.
+// Values. Code fields are masked into f16 subnormals code * 2^(pos-24) and multiplied (m16n8k16) by
+// P' = p * s * 2^(24-pos). The mid-rise offset (2^(b-1) - 1/2) * sum(P') is removed at the end of
+// the split, using the same f16 weights.
 #include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
 
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -27,7 +26,7 @@ namespace tq {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kDThreads = 128;  // 4 warps; warp w owns tokens 32w..32w+31 of every page
+constexpr int kPrepThreads = 128;
 
 struct DecodeArgs {
   LayerView lv;
@@ -38,20 +37,6 @@ struct DecodeArgs {
   uint8_t* ws;
   DecodePlan plan;
 };
-
-// e4m3 value of bit position p (0..5) of a byte: mantissa bits give subnormals 2^-9, 2^-8, 2^-7;
-// exponent bits 3, 4, 5 give 2^-6, 2^-5, 2^-3.
-__host__ __device__ __forceinline__ int e4m3_bit_exp(int p) {
-  return p == 0 ? -9 : p == 1 ? -8 : p == 2 ? -7 : p == 3 ? -6 : p == 4 ? -5 : -3;
-}
-
-__device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint4& a, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
-}
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
                                         uint32_t b1) {
@@ -64,6 +49,22 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1,
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
+  const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+__device__ __forceinline__ float2 half2_to_float2(uint32_t a) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&a));
+}
+
+// 8x8 transpose of 16-bit elements across the warp (C-fragment rows -> B-fragment columns).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
+  return y;
 }
 
 // ---- mbarrier / bulk copy (async proxy) ----
@@ -99,6 +100,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return false;
 }
 
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L, int& Np, int& P) {
   L = lv.state[2 * slot];
   const int F = lv.state[2 * slot + 1];
@@ -106,137 +111,136 @@ __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L
   P = Np + F;
 }
 
-// =============================================================================================
-// Query prep: q_rot = Pi q, q_proj = S q_rot; fp8 limbs of the three bit-plane operands
-// =============================================================================================
 template <int D>
-__global__ void __launch_bounds__(kDThreads) k_prep(DecodeArgs a) {
+__host__ __device__ constexpr int decode_threads() {
+  return 32 * 4 * (D / 128);  // 4 token groups x (d/128) coordinate halves
+}
+
+// =============================================================================================
+// Query prep: q_rot = Pi q, q_proj = S q_rot; f16 operands of the three key bit-plane MMAs
+// =============================================================================================
+// Effective f16 bit position that carries coordinate j in the key words (kbit_loc, kpair_pos).
+__device__ __forceinline__ int key_qeff(int j) {
+  const int jj = j & 127;
+  return kpair_pos(2 * (jj >> 4) + ((jj >> 3) & 1));
+}
+
+template <int D>
+__host__ __device__ constexpr size_t prep_smem_bytes() {
+  return 128 + 2 * D * D + 2 * kMaxG * D * 4 + 64;
+}
+
+// Workspace of one (row, KV head): B fragments [plane 3][half D/128][kstep 8][lane 32] uint2, then
+// 4 floats per head {u_mse, C_mse, u_qjl, C_qjl}.
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads) k_prep(DecodeArgs a) {
   constexpr int NE = D / 32;
-  constexpr int KST = 3 * D / 32;  // k-steps of 32 coordinates over the three planes
-  __shared__ float qr[kMaxG][D];
-  __shared__ float qp[kMaxG][D];
-  __shared__ float red[kMaxG][4];
+  constexpr int HALVES = D / 128;
+  extern __shared__ __align__(128) uint8_t psm[];
+  uint64_t* bar = reinterpret_cast<uint64_t*>(psm);
+  const uint16_t* st = reinterpret_cast<const uint16_t*>(psm + 128);  // S^T bf16 [D][D]
+  float* qr = reinterpret_cast<float*>(psm + 128 + 2 * D * D);        // [4][D]
+  float* qp = qr + kMaxG * D;                                         // [4][D]
+  float* red = qp + kMaxG * D;                                        // lambda [4][2], sums [2][4]
   const int b = blockIdx.x, h = blockIdx.y;
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int G = lv.G;
-  // warp w rotates head w (zero rows for heads >= G)
-  {
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_expect_tx(bar, 2u * D * D);
+    bulk_g2s(psm + 128, lv.St, 2u * D * D, bar);
+  }
+  // S^T (a constant table) streams in while the previous kernel finishes; q and the workspace are
+  // touched only after it has completed. Dependents are released after that point, so the decode
+  // kernel may read the cache as soon as it starts.
+  pdl_wait();
+  pdl_launch();
+  if (tid < 8) red[8 + tid] = 0.f;
+  if (tid == 0) reinterpret_cast<int32_t*>(a.ws + a.plan.cnt_off)[b * lv.Hkv + h] = 0;
+  {  // warp w rotates head w (zero rows for heads >= G) while S^T streams in
     float x[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       const int j = (e >> 2) * 128 + 4 * lane + (e & 3);
-      float qv = 0.f;
-      if (warp < G) qv = bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + warp) * D + j]);
+      const float qv = warp < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + warp) * D + j]) : 0.f;
       x[e] = qv * lv.D[j];
     }
     warp_fwht<NE>(x, lane);
     const float s = rsqrtf((float)D);
 #pragma unroll
-    for (int e = 0; e < NE; ++e) qr[warp][(e >> 2) * 128 + 4 * lane + (e & 3)] = x[e] * s;
+    for (int e = 0; e < NE; ++e) qr[warp * D + (e >> 2) * 128 + 4 * lane + (e & 3)] = x[e] * s;
   }
   __syncthreads();
-  // q_proj[i] = sum_j S[i][j] q_rot[j] = sum_j St[j][i] q_rot[j]
-  for (int i = tid; i < D; i += kDThreads) {
+  if (!mbar_wait(bar, 0)) {
+    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+    return;
+  }
+  for (int i = tid; i < D; i += kPrepThreads) {  // q_proj[i] = sum_j St[j][i] q_rot[j]
     float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
     for (int j = 0; j < D; ++j) {
-      const float sv = bf16_to_f32(lv.St[(size_t)j * D + i]);
+      const float sv = bf16_to_f32(st[j * D + i]);
 #pragma unroll
-      for (int g = 0; g < kMaxG; ++g) acc[g] = fmaf(sv, qr[g][j], acc[g]);
+      for (int g = 0; g < kMaxG; ++g) acc[g] = fmaf(sv, qr[g * D + j], acc[g]);
     }
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) qp[g][i] = acc[g];
+    for (int g = 0; g < kMaxG; ++g) qp[g * D + i] = acc[g];
   }
   __syncthreads();
   const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
-  // per-head power-of-two scales: largest prescaled operand magnitude in [128, 256) (e4m3 max 448)
-  if (warp < kMaxG) {
+  {  // per-head power-of-two scales: largest prescaled operand in [2^14, 2^15) (f16 max 65504)
     float mm = 0.f, mq = 0.f;
     for (int j = lane; j < D; j += 32) {
-      const int jj = j & 127, ks = jj >> 5, hb = (jj >> 4) & 1;
-      int p = 2 * ks + hb;
-      p = p < 6 ? p : p - 2;
-      const float pre = exp2f((float)-e4m3_bit_exp(p));
-      mm = fmaxf(mm, fabsf(alpha2 * qr[warp][j]) * pre);
-      mq = fmaxf(mq, fabsf(2.f * qp[warp][j]) * pre);
+      const float pre = exp2f((float)(24 - key_qeff(j)));
+      mm = fmaxf(mm, fabsf(alpha2 * qr[warp * D + j]) * pre);
+      mq = fmaxf(mq, fabsf(2.f * qp[warp * D + j]) * pre);
     }
     mm = warp_max(mm);
     mq = warp_max(mq);
     if (lane == 0) {
-      red[warp][0] = mm > 0.f ? exp2f(floorf(log2f(256.f / mm))) : 1.f;
-      red[warp][1] = mq > 0.f ? exp2f(floorf(log2f(256.f / mq))) : 1.f;
+      red[2 * warp + 0] = mm > 0.f ? exp2f(floorf(log2f(32768.f / mm))) : 1.f;
+      red[2 * warp + 1] = mq > 0.f ? exp2f(floorf(log2f(32768.f / mq))) : 1.f;
     }
   }
   __syncthreads();
-  // fragments: frag[kidx][lane] = 4 u32 (16 fp8); row = 4*limb + head
   uint8_t* prep = a.ws + a.plan.prep_off + ((size_t)b * lv.Hkv + h) * a.plan.prep_stride;
-  uint32_t* frag = reinterpret_cast<uint32_t*>(prep);
-  float* cst = reinterpret_cast<float*>(prep + (size_t)KST * 32 * 16);
-  float csum_m[kMaxG] = {0, 0, 0, 0}, csum_q[kMaxG] = {0, 0, 0, 0};
-  for (int item = tid; item < KST * 32; item += kDThreads) {
-    const int kidx = item / 32, ln = item % 32;
-    const int g = ln >> 2, c = ln & 3;
-    const int pi = kidx / (D / 32), loc = kidx % (D / 32), half = loc / 4, ks = loc % 4;
-    uint32_t regs[4];
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int row = g + 8 * (r & 1);
-      const int limb = row >> 2, head = row & 3;
-      uint32_t word = 0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int k = 4 * c + i + 16 * (r >> 1);
-        const int j = 128 * half + 32 * ks + k;
-        int p = 2 * ks + (k >> 4);
-        p = p < 6 ? p : p - 2;
-        const float pre = exp2f((float)-e4m3_bit_exp(p));
-        const float base = pi == 0 ? alpha2 * qr[head][j] : pi == 1 ? beta2 * qr[head][j] : 2.f * qp[head][j];
-        const float lam = pi < 2 ? red[head][0] : red[head][1];
-        float x = base * lam * pre;
-        float limb_v = 0.f;
-        __nv_fp8_e4m3 f8;
-        for (int l = 0; l <= limb; ++l) {
-          f8 = __nv_fp8_e4m3(x);
-          limb_v = float(f8);
-          x -= limb_v;
-        }
-        word |= (uint32_t)f8.__x << (8 * i);
-        // represented operand value (sum of limbs) times the bit weight 2^e, for the offset constants
-        if (limb == 0) {
-          float xx = base * lam * pre, rep = 0.f;
-          for (int l = 0; l < 4; ++l) {
-            const __nv_fp8_e4m3 t8(xx);
-            rep += float(t8);
-            xx -= float(t8);
-          }
-          const float w = rep * exp2f((float)e4m3_bit_exp(p));
-          if (pi < 2) csum_m[head] += w; else csum_q[head] += w;
-        }
-      }
-      regs[r] = word;
-    }
-    reinterpret_cast<uint4*>(frag)[item] = make_uint4(regs[0], regs[1], regs[2], regs[3]);
+  uint2* frag = reinterpret_cast<uint2*>(prep);
+  float* cst = reinterpret_cast<float*>(prep + (size_t)3 * HALVES * 8 * 32 * 8);
+  const int head = lane >> 2, c = lane & 3;  // the same lane (and head) for every item of this thread
+  const bool live = head < G;
+  float sum_m = 0.f, sum_q = 0.f;
+  for (int item = tid; item < 3 * HALVES * 8 * 32; item += kPrepThreads) {
+    const int s = (item >> 5) & 7, half = (item >> 8) % HALVES, pi = item / (256 * HALVES);
+    const int j0 = 128 * half + 16 * s + 2 * c, j1 = j0 + 8;
+    const float w = pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f;
+    const float* base = (pi < 2 ? qr : qp) + (live ? head : 0) * D;
+    const float lam = live ? red[2 * head + (pi < 2 ? 0 : 1)] : 0.f;
+    const float pre0 = exp2f((float)(24 - key_qeff(j0))), pre1 = exp2f((float)(24 - key_qeff(j1)));
+    const uint32_t b0 = pack_half2(w * base[j0] * lam * pre0, w * base[j0 + 1] * lam * pre0);
+    const uint32_t b1 = pack_half2(w * base[j1] * lam * pre1, w * base[j1 + 1] * lam * pre1);
+    frag[item] = make_uint2(b0, b1);
+    // represented operand values times the bit weights 2^(q-24), for the +-1 offsets
+    const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
+    const float v = (r0.x + r0.y) / pre0 + (r1.x + r1.y) / pre1;
+    if (pi < 2) sum_m += v; else sum_q += v;
   }
-  // reduce the offset constants over the block
-  __syncthreads();
-  __shared__ float cs[2][kMaxG];
-  if (tid < 2 * kMaxG) cs[tid / kMaxG][tid % kMaxG] = 0.f;
-  __syncthreads();
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) {
-    const float vm = warp_sum(csum_m[g]), vq = warp_sum(csum_q[g]);
-    if (lane == 0) {
-      atomicAdd(&cs[0][g], vm);
-      atomicAdd(&cs[1][g], vq);
-    }
+  sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 1);
+  sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
+  sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
+  sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
+  if (c == 0 && head < kMaxG) {
+    atomicAdd(&red[8 + head], sum_m);
+    atomicAdd(&red[12 + head], sum_q);
   }
   __syncthreads();
   if (tid < kMaxG) {
     const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
-    cst[4 * tid + 0] = a.scale * kLog2e / red[tid][0];
-    cst[4 * tid + 1] = 0.5f * cs[0][tid];
-    cst[4 * tid + 2] = a.scale * kLog2e * kappa / red[tid][1];
-    cst[4 * tid + 3] = 0.5f * cs[1][tid];
+    cst[4 * tid + 0] = a.scale * kLog2e / red[2 * tid + 0];
+    cst[4 * tid + 1] = 0.5f * red[8 + tid];
+    cst[4 * tid + 2] = a.scale * kLog2e * kappa / red[2 * tid + 1];
+    cst[4 * tid + 3] = 0.5f * red[12 + tid];
   }
 }
 
@@ -244,99 +248,274 @@ __global__ void __launch_bounds__(kDThreads) k_prep(DecodeArgs a) {
 // Split-K decode over packed pages (blockIdx.x < n_splits) and the exact ring split (== n_splits)
 // =============================================================================================
 template <int D>
-__device__ void ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
+__host__ __device__ constexpr size_t ring_smem_bytes() {
+  return 128 + 2 * kPage * D + kPage * kMaxG * 4 + 64;
+}
+
+__device__ __forceinline__ void write_empty_partial(float* part, int D, int tid, int nt) {
+  for (int i = tid; i < 2 * kMaxG + kMaxG * D; i += nt) part[i] = i < kMaxG ? -INFINITY : 0.f;
+}
+
+// Exact attention over the unflushed ring tokens [F, R) of one (row, KV head): K rows, then V rows,
+// are bulk-copied into shared memory; scores are warp-per-token with lane-split coordinates.
+template <int D, int NT>
+__device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
+  constexpr int NE = D / 32;
+  constexpr int NW = NT / 32;
   const LayerView& lv = a.lv;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L, Np, P;
   seq_packed(lv, slot, L, Np, P);
-  const int F = P - Np, R = L - Np;
-  float* qs = reinterpret_cast<float*>(smem_raw);        // [4][D]
-  float* sc = qs + kMaxG * D;                             // [4][128]
-  float* red = sc + kMaxG * kPage;                        // [4][4] scratch
-  const int G = lv.G;
-  for (int i = tid; i < kMaxG * D; i += kDThreads) {
-    const int g = i / D, j = i % D;
-    qs[i] = g < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + g) * D + j]) : 0.f;
+  const int F = P - Np, R = L - Np, n = R - F;
+  if (n <= 0) {
+    write_empty_partial(part, D, tid, NT);
+    return;
   }
-  __syncthreads();
-  const uint16_t* rk = lv.ring + (((size_t)slot * lv.Hkv + h) * 2 + 0) * kPage * D;
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
+  const uint16_t* rows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16: K, then V
+  float* sc = reinterpret_cast<float*>(smem_raw + 128 + 2 * kPage * D);       // [128][4] scores, then p
+  float* red = sc + kPage * kMaxG;                                           // [4][2]
+  const uint16_t* rk = lv.ring + (((size_t)slot * lv.Hkv + h) * 2) * kPage * D + (size_t)F * D;
   const uint16_t* rv = rk + (size_t)kPage * D;
+  const uint32_t bytes = (uint32_t)n * D * 2;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(smem_raw + 128, rk, bytes, bar);
+  }
+  const int G = lv.G;
+  float qv[kMaxG][NE];
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g)
+#pragma unroll
+    for (int e = 0; e < NE; ++e)
+      qv[g][e] = g < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + g) * D + (e >> 2) * 128 + 4 * lane + (e & 3)])
+                       : 0.f;
+  __syncthreads();
+  bool ok = mbar_wait(bar, 0);
   const float s2 = a.scale * kLog2e;
-  {
-    const int i = F + tid;
-    float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
-    if (i < R) {
-      const uint2* row = reinterpret_cast<const uint2*>(rk + (size_t)i * D);
-      for (int q4 = 0; q4 < D / 4; ++q4) {
-        const uint2 u = row[q4];
+  if (ok) {
+    for (int t = warp; t < n; t += NW) {
+      float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hf = 0; hf < NE / 4; ++hf) {
+        const uint2 u = *reinterpret_cast<const uint2*>(rows + (size_t)t * D + 128 * hf + 4 * lane);
         const float k0 = __uint_as_float(u.x << 16), k1 = __uint_as_float(u.x & 0xffff0000u);
         const float k2 = __uint_as_float(u.y << 16), k3 = __uint_as_float(u.y & 0xffff0000u);
 #pragma unroll
-        for (int g = 0; g < kMaxG; ++g) {
-          const float* qq = qs + g * D + 4 * q4;
-          acc[g] = fmaf(qq[0], k0, fmaf(qq[1], k1, fmaf(qq[2], k2, fmaf(qq[3], k3, acc[g]))));
-        }
+        for (int g = 0; g < kMaxG; ++g)
+          acc[g] = fmaf(qv[g][4 * hf], k0, fmaf(qv[g][4 * hf + 1], k1,
+                   fmaf(qv[g][4 * hf + 2], k2, fmaf(qv[g][4 * hf + 3], k3, acc[g]))));
       }
-    }
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) sc[g * kPage + tid] = i < R ? acc[g] * s2 : -INFINITY;
+      for (int g = 0; g < kMaxG; ++g) acc[g] = warp_sum(acc[g]);
+      if (lane < kMaxG) sc[t * kMaxG + lane] = acc[lane] * s2;
+    }
   }
-  __syncthreads();
-  const int lane = tid & 31, warp = tid >> 5;
-  // warp g reduces head g: max and sum of exp2
-  {
+  __syncthreads();  // every K row has been read
+  if (tid == 0 && ok) {
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(smem_raw + 128, rv, bytes, bar);
+  }
+  if (warp < kMaxG) {  // softmax statistics: warp g reduces head g
     float m = -INFINITY;
-    for (int t = lane; t < kPage; t += 32) m = fmaxf(m, sc[warp * kPage + t]);
+    for (int t = lane; t < n; t += 32) m = fmaxf(m, sc[t * kMaxG + warp]);
     m = warp_max(m);
     float l = 0.f;
-    for (int t = lane; t < kPage; t += 32) {
-      const float s = sc[warp * kPage + t];
-      const float p = s == -INFINITY ? 0.f : exp2f(s - m);
-      sc[warp * kPage + t] = p;
+    for (int t = lane; t < n; t += 32) {
+      const float p = exp2f(sc[t * kMaxG + warp] - m);
+      sc[t * kMaxG + warp] = p;
       l += p;
     }
     l = warp_sum(l);
     if (lane == 0) {
-      red[warp * 4 + 0] = m;
-      red[warp * 4 + 1] = l;
+      red[2 * warp] = m;
+      red[2 * warp + 1] = l;
     }
   }
   __syncthreads();
-  for (int j = tid; j < D; j += kDThreads) {
+  ok = ok && mbar_wait(bar, 1);
+  if (!ok) {
+    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+    write_empty_partial(part, D, tid, NT);
+    return;
+  }
+  for (int j = tid; j < D; j += NT) {
     float o[kMaxG] = {0.f, 0.f, 0.f, 0.f};
-    for (int i = F; i < R; ++i) {
-      const float vv = bf16_to_f32(rv[(size_t)i * D + j]);
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) o[g] = fmaf(sc[g * kPage + (i - F)], vv, o[g]);
+#pragma unroll 4
+    for (int t = 0; t < n; ++t) {
+      const float4 p = *reinterpret_cast<const float4*>(sc + t * kMaxG);
+      const float vv = bf16_to_f32(rows[(size_t)t * D + j]);
+      o[0] = fmaf(p.x, vv, o[0]);
+      o[1] = fmaf(p.y, vv, o[1]);
+      o[2] = fmaf(p.z, vv, o[2]);
+      o[3] = fmaf(p.w, vv, o[3]);
     }
 #pragma unroll
     for (int g = 0; g < kMaxG; ++g) part[2 * kMaxG + g * D + j] = o[g];
   }
   if (tid < kMaxG) {
-    part[tid] = red[tid * 4 + 0];
-    part[kMaxG + tid] = red[tid * 4 + 1];
+    part[tid] = red[2 * tid];
+    part[kMaxG + tid] = red[2 * tid + 1];
   }
 }
 
+// =============================================================================================
+// Combine: LSE merge of history splits (rotated basis) -> Pi^T -> exact merge with the ring split.
+// Run by the last CTA of a (row, KV head) to finish its partial; warp w merges query head w.
+// =============================================================================================
+template <int D, int NT>
+__device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, float* sm) {
+  constexpr int NE = D / 32;
+  constexpr int NW = NT / 32;
+  const LayerView& lv = a.lv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nsp = a.plan.n_splits;
+  const size_t stride = a.plan.part_stride / sizeof(float);
+  const float* base = reinterpret_cast<const float*>(a.ws + a.plan.part_off +
+                                                     ((size_t)b * lv.Hkv + h) * (nsp + 1) * a.plan.part_stride);
+  float* red = sm;            // [NW][4]
+  float* fs = sm + 4 * NW;    // [nsp][4] split weights
+  // 1. max over splits, per head (block-wide)
+  float mloc[kMaxG] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  for (int s = tid; s < nsp; s += NT) {
+    const float4 m4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride));
+    mloc[0] = fmaxf(mloc[0], m4.x);
+    mloc[1] = fmaxf(mloc[1], m4.y);
+    mloc[2] = fmaxf(mloc[2], m4.z);
+    mloc[3] = fmaxf(mloc[3], m4.w);
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g) mloc[g] = warp_max(mloc[g]);
+  if (lane < kMaxG) red[warp * 4 + lane] = mloc[lane];
+  __syncthreads();
+  float M[kMaxG];
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) m = fmaxf(m, red[w * 4 + g]);
+    M[g] = m;
+  }
+  __syncthreads();
+  // 2. per-split weights and the weighted sum of l
+  float lloc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+  for (int s = tid; s < nsp; s += NT) {
+    const float4 m4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride));
+    const float4 l4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride + kMaxG));
+    const float mv[4] = {m4.x, m4.y, m4.z, m4.w}, lv4[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+    for (int g = 0; g < kMaxG; ++g) {
+      const float f = mv[g] == -INFINITY ? 0.f : exp2f(mv[g] - M[g]);
+      fs[s * 4 + g] = f;
+      lloc[g] = fmaf(f, lv4[g], lloc[g]);
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < kMaxG; ++g) lloc[g] = warp_sum(lloc[g]);
+  if (lane < kMaxG) red[warp * 4 + lane] = lloc[lane];
+  __syncthreads();
+  if (warp >= lv.G) return;
+  const int hd = warp;  // warps 0..G-1 merge query head = warp; lane holds coordinates 4*lane+e (+128)
+  float l = 0.f;
+#pragma unroll
+  for (int w = 0; w < NW; ++w) l += red[w * 4 + hd];
+  // 3. weighted sum of the split outputs (independent loads, 8 splits in flight)
+  float o[NE];
+#pragma unroll
+  for (int e = 0; e < NE; ++e) o[e] = 0.f;
+  const float* ob = base + 2 * kMaxG + hd * D + 4 * lane;
+#pragma unroll 8
+  for (int s = 0; s < nsp; ++s) {  // empty splits hold weight 0 and O = 0
+    const float f = fs[s * 4 + hd];
+#pragma unroll
+    for (int hf = 0; hf < NE / 4; ++hf) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(ob + s * stride + 128 * hf));
+      o[4 * hf + 0] = fmaf(f, v.x, o[4 * hf + 0]);
+      o[4 * hf + 1] = fmaf(f, v.y, o[4 * hf + 1]);
+      o[4 * hf + 2] = fmaf(f, v.z, o[4 * hf + 2]);
+      o[4 * hf + 3] = fmaf(f, v.w, o[4 * hf + 3]);
+    }
+  }
+  // 4. Pi^T o = D * (H o) / sqrt(d), then the exact merge with the ring split
+  warp_fwht<NE>(o, lane);
+  const float rs = rsqrtf((float)D);
+#pragma unroll
+  for (int e = 0; e < NE; ++e) o[e] *= rs * lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
+  const float* rp = base + nsp * stride;
+  const float m = M[hd];
+  const float mr = __ldcg(rp + hd), lr = __ldcg(rp + kMaxG + hd);
+  const float mm = fmaxf(m, mr);
+  const float fh = (m == -INFINITY) ? 0.f : exp2f(m - mm);
+  const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mm);
+  const float den = fh * l + fr * lr;
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  float* out = a.out + ((size_t)b * lv.Hq + h * lv.G + hd) * D;
+#pragma unroll
+  for (int hf = 0; hf < NE / 4; ++hf) {
+    const float4 rv = __ldcg(reinterpret_cast<const float4*>(rp + 2 * kMaxG + hd * D + 128 * hf + 4 * lane));
+    float4 r;
+    r.x = (fh * o[4 * hf + 0] + fr * rv.x) * inv;
+    r.y = (fh * o[4 * hf + 1] + fr * rv.y) * inv;
+    r.z = (fh * o[4 * hf + 2] + fr * rv.z) * inv;
+    r.w = (fh * o[4 * hf + 3] + fr * rv.w) * inv;
+    *reinterpret_cast<float4*>(out + 128 * hf + 4 * lane) = r;
+  }
+}
+
+// After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
+// merges all of them (threadfence reduction; no CTA waits on another).
+template <int D, int NT>
+__device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    int* cnt = reinterpret_cast<int*>(a.ws + a.plan.cnt_off) + b * a.lv.Hkv + h;
+    const int old = atomicAdd(cnt, 1);
+    s_last = old == a.plan.n_splits;
+    if (s_last) *cnt = 0;  // ready for the next call
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  combine_unit<D, NT>(a, b, h, reinterpret_cast<float*>(smem + 128));
+}
+
+// Split-K decode CTA: 4 token groups x (d/128) coordinate halves of warps. Warp (tg, hf) owns
+// tokens 32tg..32tg+31 of every page and coordinates 128hf..128hf+127.
+// Scores: each 16-token tile is three bit-plane m16n8k16 MMA chains. A = masked key bits
+// (f16 2^(q-24) or 0), B = prepped f16 query (4 heads + 4 zero columns). For d=256 the two halves
+// exchange partial sums through shared memory.
+// Values: P is moved from C to B fragment layout with movmatrix and scaled per value group. Then
+// P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
 template <int D, int VB, int STAGES>
-__global__ void __launch_bounds__(kDThreads) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
+  constexpr int HALVES = D / 128;
+  constexpr int NT = decode_threads<D>();
+  constexpr int NG = D / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerView& lv = a.lv;
   const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tg = warp & 3, hf = warp >> 2;
   const int nsp = a.plan.n_splits;
   float* part = reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                          (((size_t)b * lv.Hkv + h) * (nsp + 1) + sp) * a.plan.part_stride);
+  pdl_launch();
   const int slot = a.seq_ids[b];
   if (slot < 0 || slot >= lv.max_seqs) {
-    if (tid < kMaxG) {
-      part[tid] = -INFINITY;
-      part[kMaxG + tid] = 0.f;
-    }
+    pdl_wait();
+    write_empty_partial(part, D, tid, NT);
+    finish_unit<D, NT>(a, b, h, smem);
     return;
   }
   if (sp == nsp) {
-    ring_split<D>(a, b, h, slot, part, smem);
+    pdl_wait();
+    ring_split<D, NT>(a, b, h, slot, part, smem);
+    finish_unit<D, NT>(a, b, h, smem);
     return;
   }
   int L, Np, P;
@@ -346,16 +525,16 @@ __global__ void __launch_bounds__(kDThreads) k_decode(DecodeArgs a) {
   if (sp == 0 && tid == 0 && n_pages > nsp * pps) set_status(lv.status, TQ_DEV_ERR_SPLITS);
   const int pg0 = sp * pps, pg1 = min(n_pages, pg0 + pps);
   if (pg0 >= pg1) {
-    if (tid < kMaxG) {
-      part[tid] = -INFINITY;
-      part[kMaxG + tid] = 0.f;
-    }
+    pdl_wait();
+    write_empty_partial(part, D, tid, NT);
+    finish_unit<D, NT>(a, b, h, smem);
     return;
   }
   const PageLayout pl = page_layout(D, VB);
   const uint32_t PB = pl.bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint8_t* stage0 = smem + 128;
+  float* xbuf = reinterpret_cast<float*>(stage0 + (size_t)STAGES * PB);  // [NT][2 tiles][8] partial scores
   const uint8_t* gpages = lv.pages + ((size_t)slot * lv.Hkv + h) * lv.max_pages * PB;
   const int npg = pg1 - pg0;
   if (tid == 0) {
@@ -366,197 +545,246 @@ __global__ void __launch_bounds__(kDThreads) k_decode(DecodeArgs a) {
       bulk_g2s(stage0 + (size_t)s * PB, gpages + (size_t)(pg0 + s) * PB, PB, &full[s]);
     }
   }
-  // score operand A (q limbs) and per-head constants
-  constexpr int KST = 3 * D / 32;
-  constexpr int HALVES = D / 128;
+  pdl_wait();  // the query-prep operands (and the arrival counters) of this call are ready
   const uint8_t* prep = a.ws + a.plan.prep_off + ((size_t)b * lv.Hkv + h) * a.plan.prep_stride;
-  uint4 af[KST];
+  uint2 bq[3][8];
 #pragma unroll
-  for (int k = 0; k < KST; ++k) af[k] = reinterpret_cast<const uint4*>(prep)[k * 32 + lane];
-  const int g = lane >> 2, c = lane & 3, hh = g & 3;
-  const float* cst = reinterpret_cast<const float*>(prep + (size_t)KST * 32 * 16);
-  const float u_m = cst[4 * hh + 0], c_m = cst[4 * hh + 1], u_q = cst[4 * hh + 2], c_q = cst[4 * hh + 3];
-  const bool live_col = g < lv.G;  // B columns >= G (padding heads) are zero
-  constexpr int NG = D / 32;       // value groups
-  constexpr int NMT = D / 16;      // m-tiles of the value accumulator
-  float O[NMT][4];
+  for (int pi = 0; pi < 3; ++pi)
 #pragma unroll
-  for (int mt = 0; mt < NMT; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
-  float m_eff = -INFINITY, l_acc = 0.f;
-  float lg[NG];
+    for (int s = 0; s < 8; ++s) bq[pi][s] = reinterpret_cast<const uint2*>(prep)[((pi * HALVES + hf) * 8 + s) * 32 + lane];
+  const int g = lane >> 2, c = lane & 3;
+  const float* cst = reinterpret_cast<const float*>(prep + (size_t)3 * HALVES * 8 * 32 * 8);
+  const int G = lv.G;
+  float um[2], cm[2], uq[2], cq[2];
+  bool colok[2];
 #pragma unroll
-  for (int q = 0; q < NG; ++q) lg[q] = 0.f;
+  for (int i = 0; i < 2; ++i) {
+    const int hd = min(2 * c + i, kMaxG - 1);
+    um[i] = cst[4 * hd + 0];
+    cm[i] = cst[4 * hd + 1];
+    uq[i] = cst[4 * hd + 2];
+    cq[i] = cst[4 * hd + 3];
+    colok[i] = 2 * c + i < G;
+  }
+  float O[8][4];
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
+  float m_eff[2] = {-INFINITY, -INFINITY}, l_acc[2] = {0.f, 0.f};
+  float lg[4] = {0.f, 0.f, 0.f, 0.f};  // B layout: head g, the four value groups of this half
   __syncthreads();
   bool timed_out = false;
 
   for (int ip = 0; ip < npg; ++ip) {
-    const int s = ip % STAGES;
-    if (!mbar_wait(&full[s], (ip / STAGES) & 1)) {
+    const int s_ = ip % STAGES;
+    if (!mbar_wait(&full[s_], (ip / STAGES) & 1)) {
       timed_out = true;
       break;
     }
-    const uint8_t* pg = stage0 + (size_t)s * PB;
+    const uint8_t* pg = stage0 + (size_t)s_ * PB;
     const int valid = min(kPage, P - (pg0 + ip) * kPage);
-    const uint32_t* kw = reinterpret_cast<const uint32_t*>(pg + pl.kbits_off);
-    // ---- scores of the warp's 32 tokens (4 n-tiles of 8) ----
-    float sc[4][2];
+    const uint2* kw2 = reinterpret_cast<const uint2*>(pg + pl.kbits_off);
+    const uint32_t* nrm = reinterpret_cast<const uint32_t*>(pg + pl.norms_off);
+    const uint32_t* vsc = reinterpret_cast<const uint32_t*>(pg + pl.vscale_off);  // [token pair][group] f16x2
+    float sc[2][4];
+    // six independent MMA chains: (tile, plane); both tiles' words are loaded up front
+    float acc[2][3][4];
+    uint2 kwv[2][3];
 #pragma unroll
-    for (int ntl = 0; ntl < 4; ++ntl) {
-      const int nt = 4 * warp + ntl;
-      float am[4] = {0.f, 0.f, 0.f, 0.f}, aq[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int kap = 0; kap < 2; ++kap)
 #pragma unroll
       for (int pi = 0; pi < 3; ++pi) {
+        acc[kap][pi][0] = acc[kap][pi][1] = acc[kap][pi][2] = acc[kap][pi][3] = 0.f;
+        kwv[kap][pi] = kw2[(((2 * tg + kap) * 3 + pi) * HALVES + hf) * 32 + lane];
+      }
 #pragma unroll
-        for (int hf = 0; hf < HALVES; ++hf) {
-          const uint32_t w = kw[((nt * 3 + pi) * HALVES + hf) * 32 + lane];
-          const uint32_t ws = w >> 2;
+    for (int s = 0; s < 8; ++s) {
+      const int q0 = s < 6 ? 2 * s : 2 * s - 4;
+      const uint32_t m0 = 0x00010001u << q0, m1 = 0x00010001u << (q0 + 1);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t b0 = ks < 3 ? (w & (0x01010101u << (2 * ks))) : (ws & 0x10101010u);
-            const uint32_t b1 = ks < 3 ? (w & (0x02020202u << (2 * ks))) : (ws & 0x20202020u);
-            const int kidx = pi * (D / 32) + hf * 4 + ks;
-            if (pi < 2) mma_e4m3(am, af[kidx], b0, b1);
-            else mma_e4m3(aq, af[kidx], b0, b1);
-          }
+      for (int pi = 0; pi < 3; ++pi)
+#pragma unroll
+        for (int kap = 0; kap < 2; ++kap) {
+          const uint32_t x0 = s < 6 ? kwv[kap][pi].x : kwv[kap][pi].x >> 4;
+          const uint32_t x1 = s < 6 ? kwv[kap][pi].y : kwv[kap][pi].y >> 4;
+          mma_f16(acc[kap][pi], x0 & m0, x1 & m0, x0 & m1, x1 & m1, bq[pi][s].x, bq[pi][s].y);
+        }
+    }
+#pragma unroll
+    for (int kap = 0; kap < 2; ++kap) {
+      const int tile = 2 * tg + kap;
+      float am[4], aq[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        am[i] = acc[kap][0][i] + acc[kap][1][i];
+        aq[i] = acc[kap][2][i];
+      }
+      if (HALVES == 2) {  // add the partner half's partial sums
+        float* mine = xbuf + ((size_t)tid * 2 + kap) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          mine[i] = am[i];
+          mine[4 + i] = aq[i];
+        }
+        named_barrier(1 + tg, 64);
+        const float* other = xbuf + ((size_t)(tid ^ 128) * 2 + kap) * 8;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          am[i] += other[i];
+          aq[i] += other[4 + i];
         }
       }
-      float m0 = am[0] + am[2], m1 = am[1] + am[3];
-      float q0 = aq[0] + aq[2], q1 = aq[1] + aq[3];
-      m0 += __shfl_xor_sync(0xffffffffu, m0, 16);
-      m1 += __shfl_xor_sync(0xffffffffu, m1, 16);
-      q0 += __shfl_xor_sync(0xffffffffu, q0, 16);
-      q1 += __shfl_xor_sync(0xffffffffu, q1, 16);
-      const int t0 = 8 * nt + 2 * c;
-      const uint2 nr = *reinterpret_cast<const uint2*>(pg + pl.norms_off + 4 * t0);
-      const float n0 = __half2float(__ushort_as_half((uint16_t)(nr.x & 0xffff)));
-      const float g0 = __half2float(__ushort_as_half((uint16_t)(nr.x >> 16)));
-      const float n1 = __half2float(__ushort_as_half((uint16_t)(nr.y & 0xffff)));
-      const float g1 = __half2float(__ushort_as_half((uint16_t)(nr.y >> 16)));
-      sc[ntl][0] = t0 < valid ? n0 * fmaf(u_m, m0 - c_m, u_q * g0 * (q0 - c_q)) : -INFINITY;
-      sc[ntl][1] = t0 + 1 < valid ? n1 * fmaf(u_m, m1 - c_m, u_q * g1 * (q1 - c_q)) : -INFINITY;
-    }
-    // ---- largest value scale among the warp's 32 tokens ----
-    const uint16_t* vsc = reinterpret_cast<const uint16_t*>(pg + pl.vscale_off);
-    float smax = 0.f;
-    {
-      const uint16_t* row = vsc + (32 * warp + lane) * NG;
+      const int t0 = 16 * tile + g, t1 = t0 + 8;
+      const uint32_t n0w = nrm[t0], n1w = nrm[t1];
+      const float nv[2] = {__half2float(__ushort_as_half((uint16_t)(n0w & 0xffff))),
+                           __half2float(__ushort_as_half((uint16_t)(n1w & 0xffff)))};
+      const float gv[2] = {__half2float(__ushort_as_half((uint16_t)(n0w >> 16))),
+                           __half2float(__ushort_as_half((uint16_t)(n1w >> 16)))};
 #pragma unroll
-      for (int q = 0; q < NG; ++q) smax = fmaxf(smax, __half2float(__ushort_as_half(row[q])));
+      for (int i = 0; i < 4; ++i) {
+        const int row = i >> 1, col = i & 1;
+        const bool ok = (row ? t1 : t0) < valid && colok[col];
+        sc[kap][i] = ok ? nv[row] * fmaf(um[col], am[i] - cm[col], uq[col] * gv[row] * (aq[i] - cq[col])) : -INFINITY;
+      }
+    }
+    // ---- online softmax (exp2 units); m_eff also keeps p * s * 2^(24 - pos) inside f16 range ----
+    float mx[2];
+#pragma unroll
+    for (int col = 0; col < 2; ++col) {
+      float m = fmaxf(fmaxf(sc[0][col], sc[0][2 + col]), fmaxf(sc[1][col], sc[1][2 + col]));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 8));
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
+      mx[col] = m;
+    }
+    float smax = 0.f;
+    for (int i = lane; i < 16 * NG; i += 32) {
+      const float2 sv = half2_to_float2(vsc[16 * tg * NG + i]);
+      smax = fmaxf(smax, fmaxf(sv.x, sv.y));
     }
     smax = warp_max(smax);
-    // ---- online softmax in exp2 units; m_eff also keeps P' = p * s * 2^24 inside f16 range ----
-    float mx = -INFINITY;
-#pragma unroll
-    for (int ntl = 0; ntl < 4; ++ntl) mx = fmaxf(mx, fmaxf(sc[ntl][0], sc[ntl][1]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
     int e2 = 0;
     frexpf(smax, &e2);
-    const float E = smax > 0.f ? (float)(9 + e2) : 0.f;
-    const float m_new = fmaxf(m_eff, mx + E);
-    const float alpha = (m_new == -INFINITY) ? 1.f : exp2f(m_eff - m_new);
-    m_eff = m_new;
-    l_acc *= alpha;
+    // p * 2^(24-pos) <= 2^(15 - max(e2, 0)) keeps both P (packed before the scale) and P * s below 2^15
+    const float E = smax > 0.f ? (float)(9 + max(e2, 0)) : 9.f;
+    float alpha[2];
 #pragma unroll
-    for (int q = 0; q < NG; ++q) lg[q] *= alpha;
-    const float aA = __shfl_sync(0xffffffffu, alpha, (8 * c) & 31);
-    const float aB = __shfl_sync(0xffffffffu, alpha, (8 * c + 4) & 31);
-#pragma unroll
-    for (int mt = 0; mt < NMT; ++mt) {
-      O[mt][0] *= aA;
-      O[mt][1] *= aB;
-      O[mt][2] *= aA;
-      O[mt][3] *= aB;
+    for (int col = 0; col < 2; ++col) {
+      const float m_new = fmaxf(m_eff[col], mx[col] + E);
+      alpha[col] = (m_new == -INFINITY) ? 1.f : exp2f(m_eff[col] - m_new);
+      m_eff[col] = m_new;
+      l_acc[col] *= alpha[col];
     }
-    float p[4][2];
 #pragma unroll
-    for (int ntl = 0; ntl < 4; ++ntl)
+    for (int mt = 0; mt < 8; ++mt) {
+      O[mt][0] *= alpha[0];
+      O[mt][1] *= alpha[1];
+      O[mt][2] *= alpha[0];
+      O[mt][3] *= alpha[1];
+    }
+    {  // lg lives in the B layout (head g): fetch alpha of head g from lane (g >> 1)
+      const float a0 = __shfl_sync(0xffffffffu, alpha[0], g >> 1), a1 = __shfl_sync(0xffffffffu, alpha[1], g >> 1);
+      const float ab = (g & 1) ? a1 : a0;
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const float x = sc[ntl][e];
-        p[ntl][e] = (x == -INFINITY || !live_col) ? 0.f : exp2f(x - m_eff);
-        l_acc += p[ntl][e];
+      for (int q = 0; q < 4; ++q) lg[q] *= ab;
+    }
+    uint32_t pb[2][2];  // B fragments of P (no value scale yet): [k-step][tokens 0-7 / 8-15]
+#pragma unroll
+    for (int kap = 0; kap < 2; ++kap) {
+      float pv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int row = i >> 1, col = i & 1;
+        const float x = sc[kap][i];
+        const float pn = x == -INFINITY ? 0.f : exp2f(x - m_eff[col]);
+        l_acc[col] += pn;
+        const int pos = VB == 2 ? vpos2(kap, row) : vpos4(row);
+        pv[i] = pn * (float)(1u << (24 - pos));
       }
-    // ---- P.V on f16 tensor cores, one value group (two m-tiles) at a time ----
+      pb[kap][0] = movmatrix_trans(pack_half2(pv[0], pv[1]));
+      pb[kap][1] = movmatrix_trans(pack_half2(pv[2], pv[3]));
+    }
+    // ---- P.V, one value group (two m-tiles) of this half at a time ----
     const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + pl.vbits_off);
 #pragma unroll
-    for (int q = 0; q < NG; ++q) {
+    for (int q = 0; q < 4; ++q) {
+      const int gq = 4 * hf + q;
       uint32_t bf[2][2];
 #pragma unroll
-      for (int kap = 0; kap < 2; ++kap)
-#pragma unroll
-        for (int hi = 0; hi < 2; ++hi) {
-          const int ntl = 2 * kap + hi;
-          const int t0 = 8 * (4 * warp + ntl) + 2 * c;
-          const float s0 = __half2float(__ushort_as_half(vsc[t0 * NG + q]));
-          const float s1 = __half2float(__ushort_as_half(vsc[(t0 + 1) * NG + q]));
-          const int pos = VB == 2 ? vpos2(kap, hi) : vpos4(hi);
-          const float pre = (float)(1u << (24 - pos));
-          bf[kap][hi] = pack_half2(p[ntl][0] * s0 * pre, p[ntl][1] * s1 * pre);
-          // the mid-rise offset is removed with the same f16-rounded weights the MMA multiplies
-          const float2 wr = __half22float2(*reinterpret_cast<const __half2*>(&bf[kap][hi]));
-          lg[q] = fmaf(wr.x + wr.y, 1.0f / pre, lg[q]);
-        }
+      for (int kap = 0; kap < 2; ++kap) {
+        const int tile = 2 * tg + kap;
+        bf[kap][0] = hmul2_u32(pb[kap][0], vsc[(8 * tile + c) * NG + gq]);
+        bf[kap][1] = hmul2_u32(pb[kap][1], vsc[(8 * tile + 4 + c) * NG + gq]);
+        // the mid-rise offset is removed with the same f16 weights the MMA multiplies
+        const float2 r0 = half2_to_float2(bf[kap][0]), r1 = half2_to_float2(bf[kap][1]);
+        const int p0 = VB == 2 ? vpos2(kap, 0) : vpos4(0), p1 = VB == 2 ? vpos2(kap, 1) : vpos4(1);
+        lg[q] = fmaf(r0.x + r0.y, 1.0f / (float)(1u << (24 - p0)), lg[q]);
+        lg[q] = fmaf(r1.x + r1.y, 1.0f / (float)(1u << (24 - p1)), lg[q]);
+      }
 #pragma unroll
       for (int mh = 0; mh < 2; ++mh) {
-        const int mt = 2 * q + mh;
+        const int mt = 2 * q + mh, mtg = 8 * hf + mt;
         if (VB == 2) {
-          const uint32_t w = vw[(warp * NMT + mt) * 32 + lane];
+          const uint32_t w = vw[(tg * (D / 16) + mtg) * 32 + lane];
           const uint32_t w2 = w >> 2, w6 = w >> 6;
           mma_f16(O[mt], w & 0x00030003u, w2 & 0x00030003u, w & 0x00300030u, w6 & 0x00300030u, bf[0][0], bf[0][1]);
           mma_f16(O[mt], w & 0x00C000C0u, w6 & 0x00C000C0u, w & 0x03000300u, w6 & 0x03000300u, bf[1][0], bf[1][1]);
         } else {
-          const uint2 ww = reinterpret_cast<const uint2*>(vw)[(warp * NMT + mt) * 32 + lane];
+          const uint2 ww = reinterpret_cast<const uint2*>(vw)[(tg * (D / 16) + mtg) * 32 + lane];
           const uint32_t x0 = ww.x, x8 = ww.x >> 8, y0 = ww.y, y8 = ww.y >> 8;
           mma_f16(O[mt], x0 & 0x000F000Fu, x8 & 0x000F000Fu, x0 & 0x00F000F0u, x8 & 0x00F000F0u, bf[0][0], bf[0][1]);
           mma_f16(O[mt], y0 & 0x000F000Fu, y8 & 0x000F000Fu, y0 & 0x00F000F0u, y8 & 0x00F000F0u, bf[1][0], bf[1][1]);
         }
       }
     }
-    __syncthreads();  // every warp is done with stage s
+    __syncthreads();  // every warp is done with stage s_ (and with xbuf)
     if (tid == 0 && ip + STAGES < npg) {
-      mbar_expect_tx(&full[s], PB);
-      bulk_g2s(stage0 + (size_t)s * PB, gpages + (size_t)(pg0 + ip + STAGES) * PB, PB, &full[s]);
+      mbar_expect_tx(&full[s_], PB);
+      bulk_g2s(stage0 + (size_t)s_ * PB, gpages + (size_t)(pg0 + ip + STAGES) * PB, PB, &full[s_]);
     }
   }
-  if (timed_out) {
-    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
-  }
-  // ---- merge the four warps' partials through shared memory ----
+  if (timed_out && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  // ---- merge the token groups' partials through shared memory ----
   __syncthreads();
-  float* wm = reinterpret_cast<float*>(stage0);   // [4 warps][4 heads]
-  float* wl = wm + 16;                            // [4][4]
-  float* wlg = wl + 16;                           // [4][4][NG]
-  float* wo = wlg + 16 * NG;                      // [4][4][D]
+  float* wm = reinterpret_cast<float*>(stage0);  // [4 token groups][4 heads]
+  float* wl = wm + 16;                           // [4][4]
+  float* wlg = wl + 16;                          // [4][4][NG]
+  float* wo = wlg + 16 * NG;                     // [4][4][D]
   {
-    float l = l_acc;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    float l0 = l_acc[0], l1 = l_acc[1];
 #pragma unroll
-    for (int q = 0; q < NG; ++q) {
+    for (int o = 4; o < 32; o <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
       lg[q] += __shfl_xor_sync(0xffffffffu, lg[q], 1);
       lg[q] += __shfl_xor_sync(0xffffffffu, lg[q], 2);
     }
+    if (hf == 0 && g == 0 && c < 2) {
+      wm[tg * 4 + 2 * c] = m_eff[0];
+      wm[tg * 4 + 2 * c + 1] = m_eff[1];
+      wl[tg * 4 + 2 * c] = l0;
+      wl[tg * 4 + 2 * c + 1] = l1;
+    }
     if (c == 0 && g < kMaxG) {
-      wm[warp * 4 + g] = m_eff;
-      wl[warp * 4 + g] = l;
 #pragma unroll
-      for (int q = 0; q < NG; ++q) wlg[(warp * 4 + g) * NG + q] = lg[q];
+      for (int q = 0; q < 4; ++q) wlg[(tg * 4 + g) * NG + 4 * hf + q] = lg[q];
     }
     if (c < 2) {
 #pragma unroll
-      for (int mt = 0; mt < NMT; ++mt) {
-        const int j0 = 16 * mt + g;
-        wo[(warp * 4 + 2 * c) * D + j0] = O[mt][0];
-        wo[(warp * 4 + 2 * c + 1) * D + j0] = O[mt][1];
-        wo[(warp * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
-        wo[(warp * 4 + 2 * c + 1) * D + j0 + 8] = O[mt][3];
+      for (int mt = 0; mt < 8; ++mt) {
+        const int j0 = 128 * hf + 16 * mt + g;
+        wo[(tg * 4 + 2 * c) * D + j0] = O[mt][0];
+        wo[(tg * 4 + 2 * c + 1) * D + j0] = O[mt][1];
+        wo[(tg * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
+        wo[(tg * 4 + 2 * c + 1) * D + j0 + 8] = O[mt][3];
       }
     }
   }
   __syncthreads();
   const float off = (float)(1 << (VB - 1)) - 0.5f;
-  for (int i = tid; i < kMaxG * D; i += kDThreads) {
+  for (int i = tid; i < kMaxG * D; i += NT) {
     const int hd = i / D, j = i % D;
     float m = -INFINITY;
 #pragma unroll
@@ -577,101 +805,77 @@ __global__ void __launch_bounds__(kDThreads) k_decode(DecodeArgs a) {
       part[kMaxG + hd] = l;
     }
   }
+  finish_unit<D, NT>(a, b, h, smem);
 }
 
-// =============================================================================================
-// Combine: LSE merge of history splits (rotated basis) -> Pi^T -> exact merge with the ring split
-// =============================================================================================
-template <int D>
-__global__ void __launch_bounds__(kDThreads) k_combine(DecodeArgs a) {
-  constexpr int NE = D / 32;
-  const LayerView& lv = a.lv;
-  const int b = blockIdx.x, h = blockIdx.y;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;  // warp = query head within the group
-  if (warp >= lv.G) return;
-  const int nsp = a.plan.n_splits;
-  const uint8_t* base = a.ws + a.plan.part_off + ((size_t)b * lv.Hkv + h) * (nsp + 1) * a.plan.part_stride;
-  float m = -INFINITY;
-  for (int s = 0; s < nsp; ++s) m = fmaxf(m, reinterpret_cast<const float*>(base + s * a.plan.part_stride)[warp]);
-  float o[NE];
-#pragma unroll
-  for (int e = 0; e < NE; ++e) o[e] = 0.f;
-  float l = 0.f;
-  if (m != -INFINITY) {
-    for (int s = 0; s < nsp; ++s) {
-      const float* pt = reinterpret_cast<const float*>(base + s * a.plan.part_stride);
-      const float ms = pt[warp];
-      if (ms == -INFINITY) continue;
-      const float f = exp2f(ms - m);
-      l = fmaf(f, pt[kMaxG + warp], l);
-#pragma unroll
-      for (int hf = 0; hf < NE / 4; ++hf) {
-        const float4 v = *reinterpret_cast<const float4*>(pt + 2 * kMaxG + warp * D + 128 * hf + 4 * lane);
-        o[4 * hf + 0] = fmaf(f, v.x, o[4 * hf + 0]);
-        o[4 * hf + 1] = fmaf(f, v.y, o[4 * hf + 1]);
-        o[4 * hf + 2] = fmaf(f, v.z, o[4 * hf + 2]);
-        o[4 * hf + 3] = fmaf(f, v.w, o[4 * hf + 3]);
-      }
-    }
+template <int D, int VB>
+constexpr int decode_stages() {
+  return D == 128 ? 4 : 3;
+}
+
+template <int D, int VB>
+size_t decode_smem_bytes() {
+  const PageLayout pl = page_layout(D, VB);
+  constexpr int NT = decode_threads<D>();
+  const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * (D / 32) + 16 * D);
+  const size_t xbuf_bytes = D == 256 ? sizeof(float) * NT * 2 * 8 : 0;
+  size_t smem = 128 + (size_t)decode_stages<D, VB>() * pl.bytes + xbuf_bytes;
+  smem = std::max(smem, 128 + merge_bytes);
+  smem = std::max(smem, ring_smem_bytes<D>());
+  smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 4 * 1025));  // combine: split weights
+  return smem;
+}
+
+// Sets the kernels' shared-memory attributes once and returns resident split-K CTAs per SM.
+template <int D, int VB>
+int decode_setup() {
+  static int resident = 0;  // set once, outside any stream capture that follows
+  if (resident == 0) {
+    constexpr int STAGES = decode_stages<D, VB>();
+    const size_t smem = decode_smem_bytes<D, VB>();
+    if (cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(k_prep<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem_bytes<D>()) !=
+            cudaSuccess)
+      return -1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES>, decode_threads<D>(), smem) !=
+            cudaSuccess ||
+        n < 1)
+      n = 1;
+    resident = n;
   }
-  // Pi^T o = D * (H o) / sqrt(d)
-  warp_fwht<NE>(o, lane);
-  const float rs = rsqrtf((float)D);
-#pragma unroll
-  for (int e = 0; e < NE; ++e) o[e] *= rs * lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
-  const float* rp = reinterpret_cast<const float*>(base + nsp * a.plan.part_stride);
-  const float mr = rp[warp], lr = rp[kMaxG + warp];
-  const float mm = fmaxf(m, mr);
-  const float fh = (m == -INFINITY) ? 0.f : exp2f(m - mm);
-  const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mm);
-  const float den = fh * l + fr * lr;
-  const float inv = den > 0.f ? 1.f / den : 0.f;
-  float* out = a.out + ((size_t)b * lv.Hq + h * lv.G + warp) * D;
-#pragma unroll
-  for (int hf = 0; hf < NE / 4; ++hf) {
-    const float4 rv = *reinterpret_cast<const float4*>(rp + 2 * kMaxG + warp * D + 128 * hf + 4 * lane);
-    float4 r;
-    r.x = (fh * o[4 * hf + 0] + fr * rv.x) * inv;
-    r.y = (fh * o[4 * hf + 1] + fr * rv.y) * inv;
-    r.z = (fh * o[4 * hf + 2] + fr * rv.z) * inv;
-    r.w = (fh * o[4 * hf + 3] + fr * rv.w) * inv;
-    *reinterpret_cast<float4*>(out + 128 * hf + 4 * lane) = r;
-  }
+  return resident;
 }
 
 template <int D, int VB>
 cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s) {
-  constexpr int STAGES = D == 128 ? 4 : 3;
-  const PageLayout pl = page_layout(D, VB);
-  const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * (D / 32) + 16 * D);
-  const size_t ring_bytes = sizeof(float) * (kMaxG * D + kMaxG * kPage + 16);
-  size_t smem = 128 + (size_t)STAGES * pl.bytes;
-  smem = std::max(smem, 128 + merge_bytes);
-  smem = std::max(smem, ring_bytes);
-  static bool attr_set = false;  // set once, outside any stream capture that follows
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  constexpr int STAGES = decode_stages<D, VB>();
+  if (decode_setup<D, VB>() < 0) return cudaErrorInvalidValue;
+  const size_t smem = decode_smem_bytes<D, VB>();
   if (phase < 0 || phase == 0) {
-    k_prep<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_prep<D>, dim3(batch, a.lv.Hkv), dim3(kPrepThreads), prep_smem_bytes<D>(), s, a);
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
-    k_decode<D, VB, STAGES><<<dim3(a.plan.n_splits + 1, a.lv.Hkv, batch), kDThreads, smem, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(k_decode<D, VB, STAGES>, dim3(a.plan.n_splits + 1, a.lv.Hkv, batch),
+                               dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
   }
-  if (phase < 0 || phase == 2) {
-    k_combine<D><<<dim3(batch, a.lv.Hkv), kDThreads, 0, s>>>(a);
-    return cudaGetLastError();
-  }
-  return cudaSuccess;
+  return cudaSuccess;  // phase 2 (combine) runs inside phase 1's last CTA of every (row, KV head)
 }
 
 }  // namespace
+
+int decode_resident_ctas(const tq_ctx* ctx) {
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
+  int n;
+  if (d == 128 && vb == 2) n = decode_setup<128, 2>();
+  else if (d == 128 && vb == 4) n = decode_setup<128, 4>();
+  else if (d == 256 && vb == 2) n = decode_setup<256, 2>();
+  else n = decode_setup<256, 4>();
+  return n > 0 ? n : 1;
+}
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s) {

@@ -225,9 +225,13 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   const int max_pages = std::max(1, (hint + kPage - 1) / kPage);
   const int units = batch * c.n_kv_heads;
   const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
-  const int target = 3 * sms;  // resident CTAs: about three 128-thread CTAs per SM
-  int splits = std::max(1, (target + units - 1) / units);
+  const int per_sm = ctx->host_only ? 2 : decode_resident_ctas(ctx);
+  const int target = per_sm * sms;  // split-K CTAs that fit in one wave
+  // Small batches: one wave of (splits + ring) CTAs per (row, KV head). Large batches: about three
+  // waves, so that the tail of the last wave is short.
+  int splits = units * 2 <= target ? std::max(1, target / units - 1) : std::max(2, (3 * target + units - 1) / units);
   splits = std::min(splits, max_pages);
+  splits = std::min(splits, 1024);  // the combine keeps 4 weights per split in shared memory
   DecodePlan p;
   p.pages_per_split = (max_pages + splits - 1) / splits;
   p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
@@ -236,7 +240,8 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   p.prep_stride = align_up((size_t)3 * (d / 32) * 32 * 16 + 4 * 4 * sizeof(float), 256);
   p.part_off = align_up(p.prep_off + p.prep_stride * units, 256);
   p.part_stride = align_up((size_t)(2 * kMaxG + kMaxG * d) * sizeof(float), 16);
-  p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
+  p.cnt_off = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
+  p.bytes = align_up(p.cnt_off + sizeof(int32_t) * (size_t)units, 256);
   return p;
 }
 
@@ -521,7 +526,8 @@ tq_status tq_page_to_records(const tq_ctx* ctx, const void* h_page, int n_tokens
       vr[j / per] |= (uint8_t)(code << (vb * (j % per)));
     }
     std::memcpy(kr + d / 4 + d / 8, pg + pl.norms_off + 4 * t, 4);
-    std::memcpy(vr + (size_t)d * vb / 8, pg + pl.vscale_off + 2 * (size_t)t * (d / 32), 2 * (d / 32));
+    for (int q = 0; q < d / 32; ++q)
+      std::memcpy(vr + (size_t)d * vb / 8 + 2 * q, pg + pl.vscale_off + 2 * (size_t)tq::vscale_idx(d, t, q), 2);
   }
   return ok();
 }
@@ -556,7 +562,8 @@ tq_status tq_records_to_page(const tq_ctx* ctx, const uint8_t* keys, const uint8
       vw[w] |= (uint32_t)code << b;
     }
     std::memcpy(pg + pl.norms_off + 4 * t, kr + d / 4 + d / 8, 4);
-    std::memcpy(pg + pl.vscale_off + 2 * (size_t)t * (d / 32), vr + (size_t)d * vb / 8, 2 * (d / 32));
+    for (int q = 0; q < d / 32; ++q)
+      std::memcpy(pg + pl.vscale_off + 2 * (size_t)tq::vscale_idx(d, t, q), vr + (size_t)d * vb / 8 + 2 * q, 2);
   }
   return ok();
 }

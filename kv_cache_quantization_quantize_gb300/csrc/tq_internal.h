@@ -23,12 +23,12 @@ constexpr int kMaxG = 4;    // query heads per KV head served by one decode CTA 
 
 // ---------------------------------------------------------------------------------------------
 // Packed page of 128 tokens of one KV head. The layout is fragment-major: the decode kernel's
-// mma.sync operand registers are cut out of it with one LOP3 per 2-4 elements. Sections:
-//   KBITS  [n-tile 16][plane 3][half d/128][lane 32] u32.
+// mma.sync operand registers are cut out of it with one LOP3 per 2 elements. Sections:
+//   KBITS  [tile 8][plane 3][half d/128][lane 32][row 2] u32 (see kbit_loc).
 //          Planes: 0 = high bit of the Lloyd-Max index, 1 = low bit, 2 = QJL sign (1 = z >= 0).
 //   NORMS  [token 128] {fp16 n, fp16 gamma}.
 //   VBITS  2-bit: [block 4][m-tile d/16][lane 32] u32; 4-bit: [block 4][m-tile d/16][lane 32][2] u32.
-//   VSCALE [token 128][group d/32] fp16.
+//   VSCALE [token/2 64][group d/32][token&1 2] fp16 (pairs of consecutive tokens per group).
 // Per token: K (3*d/8 + 4 B) + V (d*vb/8 + d/16 B); d=128, V2 -> 92 B, identical to the canonical
 // record size. A page is therefore the canonical records in another order.
 // ---------------------------------------------------------------------------------------------
@@ -50,16 +50,20 @@ TQ_HD PageLayout page_layout(int d, int vb) {
 }
 
 // Location of the key bit of (token t, coordinate j, plane pi) in KBITS: u32 word index and bit.
-// Word (nt, pi, half, lane=4g+c) holds token 8nt+g; bit 8i + 2ks + h holds coordinate
-// 128*half + 32ks + 16h + 4c + i. Each byte of a word is one fp8 operand of m16n8k32 (B matrix,
-// k = 16h + 4c + i, column g), selected by masking bit (2ks + h) of every byte.
+// KBITS is [tile 8][plane 3][half d/128][lane 32][row 2] u32. Tile = 16 tokens, row r = token bit 3,
+// lane = 4g + c with g = token bits 0-2. Bit q + 16e of a word holds coordinate
+// 128*half + 16s + 8sub + 2c + e, with pair index q = 2s + sub. Masking bits q and q + 16 of a word
+// gives the f16 pair of m16n8k16 operand A (rows = tokens, k = coordinates). For q < 12 each half is
+// exactly 2^(q-24) when set; pairs 12..15 are shifted down by 4 first.
 TQ_HD void kbit_loc(int d, int t, int j, int pi, int& word, int& bit) {
-  const int nt = t >> 3, g = t & 7;
+  const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
   const int half = j >> 7, jj = j & 127;
-  const int ks = jj >> 5, h = (jj >> 4) & 1, c = (jj >> 2) & 3, i = jj & 3;
-  word = ((nt * 3 + pi) * (d >> 7) + half) * 32 + 4 * g + c;
-  bit = 8 * i + 2 * ks + h;
+  const int s = jj >> 4, sub = (jj >> 3) & 1, c = (jj >> 1) & 3, e = jj & 1;
+  word = ((((tile * 3 + pi) * (d >> 7) + half) * 32) + 4 * g + c) * 2 + r;
+  bit = 2 * s + sub + 16 * e;
 }
+// Effective bit position (after the decoder's shift) of pair index q.
+TQ_HD int kpair_pos(int q) { return q < 12 ? q : q - 4; }
 
 // Field tables of the value words (see vcode_loc): which 2-bit (4-bit) field of the word feeds
 // A-fragment register r of m16n8k16 for k-step kap of a 32-token block.
@@ -86,6 +90,9 @@ TQ_HD void vcode_loc(int d, int vb, int t, int j, int& word, int& bit) {
     bit = 16 * e + 4 * vfield4(r);
   }
 }
+
+// Index (in fp16 units) of the value scale of (token t, group q) inside VSCALE.
+TQ_HD int vscale_idx(int d, int t, int q) { return ((t >> 1) * (d / 32) + q) * 2 + (t & 1); }
 
 // Device tables (inside the caller's d_tables buffer).
 struct TableOffsets {
@@ -140,9 +147,13 @@ struct DecodePlan {
   int pages_per_split;
   size_t prep_off, prep_stride;  // per (row, kv head) query-prep block
   size_t part_off, part_stride;  // per (row, kv head, split) partial
+  size_t cnt_off;                // per (row, kv head) int32 arrival counter (zeroed by the prep phase)
   size_t bytes;
 };
 DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint);
+
+// Split-K decode CTAs resident per SM for ctx's (head_dim, value_bits); sets kernel attributes once.
+int decode_resident_ctas(const tq_ctx* ctx);
 
 // Records `msg` as the thread-local last error and returns `st` (for entry points outside tq_host.cpp).
 tq_status set_error(tq_status st, const char* msg);

@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   float* rbuf = reinterpret_cast<float*>(scales + kPage * (D / 32));    // [8 warps][D]
 
   const int b = blockIdx.x, h = blockIdx.y;
+  pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
+  pdl_launch();
   int slot, L, Np, pg, valid;
   if (!page_task(a, b, blockIdx.z, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
 
@@ -231,20 +233,21 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   constexpr int HALVES = D / 128;
-  for (int w = tid; w < 16 * 3 * HALVES * 32; w += kQThreads) {
-    const int ln = w & 31, hf = (w >> 5) % HALVES, pi = (w / (32 * HALVES)) % 3, nt = w / (32 * HALVES * 3);
-    const int t = 8 * nt + (ln >> 2), c = ln & 3;
-    const uint8_t* kc = kcode + t * D + 128 * hf + 4 * c;
+  for (int w = tid; w < 8 * 3 * HALVES * 32 * 2; w += kQThreads) {
+    const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % 3;
+    const int tile = w / (192 * HALVES);
+    const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
+    const uint8_t* kc = kcode + t * D + 128 * hf + 2 * c;
     uint32_t word = 0;
 #pragma unroll
-    for (int ks = 0; ks < 4; ++ks)
+    for (int sq = 0; sq < 8; ++sq)
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb)
+      for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int code = kc[32 * ks + 16 * hb + i];
+        for (int e = 0; e < 2; ++e) {
+          const int code = kc[16 * sq + 8 * sub + e];
           const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
-          word |= (uint32_t)bit << (8 * i + 2 * ks + hb);
+          word |= (uint32_t)bit << (2 * sq + sub + 16 * e);
         }
     kw[w] = word;
   }
@@ -285,12 +288,14 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
     }
   }
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
-  for (int i = tid; i < kPage * (D / 32); i += kQThreads) sw[i] = scales[i];
+  for (int i = tid; i < kPage * (D / 32); i += kQThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
 }
 
 // Ring update after the quantise launch: write the new ring tail and the sequence state.
 __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
   const int b = blockIdx.x;
+  pdl_wait();  // the quantise launch has read the old ring and state
+  pdl_launch();
   const LayerView& lv = a.lv;
   const int slot = a.seq_ids[b];
   if (slot < 0 || slot >= lv.max_seqs) return;
@@ -363,8 +368,7 @@ cudaError_t launch_quantize_d(const AppendArgs& a, int batch, int pages, cudaStr
     attr_set = true;
   }
   dim3 grid(batch, a.lv.Hkv, pages);
-  k_quantize_pages<D><<<grid, kQThreads, smem, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_quantize_pages<D>, grid, dim3(kQThreads), smem, s, a);
 }
 
 cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
@@ -388,8 +392,7 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   const int pages = (max_new + kPage - 1) / kPage;
   cudaError_t e = launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
-  k_ring_update<<<batch, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_ring_update, dim3(batch), dim3(256), 0, s, a);
 }
 
 cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s) {
@@ -403,8 +406,7 @@ cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
   a.flush = 1;
   cudaError_t e = launch_quantize(a, batch, 1, s);
   if (e != cudaSuccess) return e;
-  k_ring_update<<<batch, 32, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(k_ring_update, dim3(batch), dim3(32), 0, s, a);
 }
 
 cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s) {

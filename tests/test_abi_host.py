@@ -111,8 +111,8 @@ def _unpack(rec, bits, d):
 def test_decoder_operand_extraction_matches_records(d, vb):
     """Emulate, on the CPU, how the decode kernel cuts mma.sync operands out of a page.
 
-    Key side (fp8 m16n8k32, B operand): every byte of b0/b1 must be 0 or the power of two of its bit
-    position, set exactly when the bit-plane value of (token, coordinate) is 1.
+    Key side (f16 m16n8k16, A operand, rows = tokens, k = coordinates): every f16 half must be 0, or
+    2^(q-24) for the bit position q it was masked from, exactly when the bit-plane value is 1.
     Value side (f16 m16n8k16, A operand): every f16 half must equal code * 2^(pos - 24) for the
     position that the B operand is prescaled with.
     """
@@ -126,26 +126,30 @@ def test_decoder_operand_extraction_matches_records(d, vb):
     planes = [(idx >> 1) & 1, idx & 1, sign]
     kw = page[:3 * 128 * d // 8].view(np.uint32)
     halves = d // 128
-    e4m3_bits = {0: 0x01, 1: 0x02, 2: 0x04, 3: 0x08, 4: 0x10, 5: 0x20}
-    for nt in range(16):
+    for tile in range(8):
         for pi in range(3):
             for hf in range(halves):
                 for lane in range(32):
                     g, c = lane >> 2, lane & 3
-                    w = int(kw[((nt * 3 + pi) * halves + hf) * 32 + lane])
-                    for ks in range(4):
-                        if ks < 3:
-                            b0, b1 = w & (0x01010101 << (2 * ks)), w & (0x02020202 << (2 * ks))
-                            p0, p1 = 2 * ks, 2 * ks + 1
+                    base = (((tile * 3 + pi) * halves + hf) * 32 + lane) * 2
+                    w0, w1 = int(kw[base]), int(kw[base + 1])  # rows g and g + 8 of the tile
+                    for s_ in range(8):
+                        if s_ < 6:
+                            x0, x1, q0 = w0, w1, 2 * s_
                         else:
-                            b0, b1 = (w >> 2) & 0x10101010, (w >> 2) & 0x20202020
-                            p0, p1 = 4, 5
-                        for reg, p, kbase in ((b0, p0, 0), (b1, p1, 16)):
-                            for i in range(4):
-                                byte = (reg >> (8 * i)) & 0xFF
-                                j = 128 * hf + 32 * ks + kbase + 4 * c + i
-                                expect = e4m3_bits[p] if planes[pi][8 * nt + g, j] else 0
-                                assert byte == expect
+                            x0, x1, q0 = w0 >> 4, w1 >> 4, 2 * s_ - 4
+                        m0, m1 = 0x00010001 << q0, 0x00010001 << (q0 + 1)
+                        regs = [x0 & m0, x1 & m0, x0 & m1, x1 & m1]  # a0..a3 of m16n8k16
+                        for r, reg in enumerate(regs):
+                            row, kofs = r & 1, 8 * (r >> 1)
+                            t = 16 * tile + g + 8 * row
+                            for e in (0, 1):
+                                half = (reg >> (16 * e)) & 0xFFFF
+                                val = np.array([half], np.uint16).view(np.float16).astype(np.float64)[0]
+                                j = 128 * hf + 16 * s_ + kofs + 2 * c + e
+                                qeff = q0 + (r >> 1)
+                                expect = 2.0 ** (qeff - 24) if planes[pi][t, j] else 0.0
+                                assert val == expect
     off = 3 * 128 * d // 8 + 4 * 128
     vw = page[off:off + 128 * d * vb // 8].view(np.uint32)
     nmt = d // 16
