@@ -369,8 +369,41 @@ def bench_quantize(tqm, synth, dev, args, peak):
     gbs = bytes_pass / (ms * 1e-3) / 1e9
     return {"tok_s": T / (ms * 1e-3), "token_head_layers_per_s": T * Hkv * L_layers / (ms * 1e-3),
             "ms_per_pass": ms, "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K3/V{vb}",
-            "path": "CUDA-core quantise kernel (fp32 FMA QJL projection)",
+            "path": ("tcgen05 QJL projection (bf16 hi/lo split, TMEM accumulator) + CUDA-core rotation and codes"
+                     if d == 128 else "CUDA-core quantise kernel (fp32 FMA QJL projection)"),
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
+
+
+def profile_quantize(passes):
+    """A small quantise-only run for profilers: one layer of the prefill workload, `passes` times.
+
+    Prints one line with the measured time per layer; it is not a bench line.
+    """
+    import torch
+    import kv_cache_quantization_quantize_gb300 as tqm
+    from kv_cache_quantization_quantize_gb300 import synth
+    dev = torch.device("cuda", 0)
+    T, Hkv, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["d"], PREFILL["vb"]
+    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=4 * Hkv, max_seqs=1,
+                     max_ctx=T, seed=PREFILL["seed"])
+    qc = tqm.TurboQuantCache(cfg, device=dev)
+    k, v = synth.kv_tokens(T, Hkv, d, seed=PREFILL["seed"], outliers=WL["outliers"], device=dev)
+    k, v = k[None].contiguous(), v[None].contiguous()
+    ids = torch.zeros(1, dtype=torch.int32, device=dev)
+    nn = torch.full((1,), T, dtype=torch.int32, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    times = []
+    for _ in range(passes):
+        qc.reset(ids)
+        e0.record()
+        qc.append(0, k, v, ids, nn)
+        e1.record()
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    if qc.check_status():
+        raise RuntimeError("device status after quantise")
+    print(json.dumps({"profile": "quantize", "tokens": T, "kv_heads": Hkv, "head_dim": d, "value_bits": vb,
+                      "ms_per_layer": times}), flush=True)
 
 
 # --------------------------------------------------------------------------------------------
@@ -471,10 +504,14 @@ def main():
     p.add_argument("--skip-quantize", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
+    p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
+                   help="only run one layer of the prefill quantisation PASSES times (for profilers)")
     args = p.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.oracle_sample:
+    if args.profile_quantize:
+        profile_quantize(args.profile_quantize)
+    elif args.oracle_sample:
         oracle_sample_main(args.oracle_sample)
     elif args.impl == "reference":
         run_reference(args)

@@ -189,7 +189,8 @@ TableOffsets table_offsets(int d) {
   o.S = align_up(o.D + sizeof(float) * d, 256);
   o.St = align_up(o.S + 2ull * d * d, 256);
   o.cb = align_up(o.St + 2ull * d * d, 256);
-  o.bytes = align_up(o.cb + sizeof(float) * kCbFloats, 256);
+  o.S_sw = align_up(o.cb + sizeof(float) * kCbFloats, 1024);
+  o.bytes = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 256);
   return o;
 }
 
@@ -210,6 +211,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   v.S = reinterpret_cast<const uint16_t*>(tb + ctx->to.S);
   v.St = reinterpret_cast<const uint16_t*>(tb + ctx->to.St);
   v.cb = reinterpret_cast<const float*>(tb + ctx->to.cb);
+  v.S_sw = reinterpret_cast<const uint16_t*>(tb + ctx->to.S_sw);
   uint8_t* cb = static_cast<uint8_t*>(ctx->d_cache);
   const size_t units_per_layer = (size_t)c.max_seqs * c.n_kv_heads;
   v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
@@ -337,6 +339,11 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
   cb[8] = (float)(0.5 * (ctx->cent[2] + ctx->cent[3]));
   cb[9] = (float)(0.5 * (ctx->cent[3] - ctx->cent[2]));
   std::memcpy(host.data() + ctx->to.cb, cb, sizeof(cb));
+  if (d == 128) {
+    uint8_t* sw = host.data() + ctx->to.S_sw;
+    for (int n = 0; n < d; ++n)
+      for (int k = 0; k < d; ++k) std::memcpy(sw + tq::sw128_offset(n, k), &ctx->S[(size_t)n * d + k], 2);
+  }
   e = cudaMemcpyAsync(d_tables, host.data(), need, cudaMemcpyHostToDevice, (cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) {

@@ -94,9 +94,18 @@ TQ_HD void vcode_loc(int d, int vb, int t, int j, int& word, int& bit) {
 // Index (in fp16 units) of the value scale of (token t, group q) inside VSCALE.
 TQ_HD int vscale_idx(int d, int t, int q) { return ((t >> 1) * (d / 32) + q) * 2 + (t & 1); }
 
-// Device tables (inside the caller's d_tables buffer).
+// Byte offset of element (row n, column k) of a 128 x 128 bf16 matrix stored K-major in the
+// tcgen05 canonical 128-byte-swizzled layout: two 64-column atoms of 128 rows; within an atom,
+// 8-row groups of 1024 B, and the 16-byte chunk c of row r stored at chunk c ^ (r & 7).
+TQ_HD uint32_t sw128_offset(int n, int k) {
+  return (uint32_t)((k >> 6) * 16384 + (n >> 3) * 1024 + (n & 7) * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) +
+                    (k & 7) * 2);
+}
+
+// Device tables (inside the caller's d_tables buffer). S_sw is S (rows = projection index,
+// columns = coordinate) in the swizzled layout above; present for head_dim 128.
 struct TableOffsets {
-  size_t D, S, St, cb, bytes;
+  size_t D, S, St, cb, S_sw, bytes;
 };
 TableOffsets table_offsets(int d);
 
@@ -133,6 +142,7 @@ struct LayerView {
   const uint16_t* S;   // bf16 [d][d]
   const uint16_t* St;  // bf16 [d][d] transposed
   const float* cb;
+  const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128)
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
   uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
   int32_t* state;      // this layer: [slot][2] = {L, F}

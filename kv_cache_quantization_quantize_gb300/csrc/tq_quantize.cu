@@ -1,6 +1,8 @@
 // Quantize-on-append ([Guide] §二, five-step pipeline): one CTA writes one packed page (128 tokens of
 // one KV head). This is the CUDA-core path for ring flushes and appends. The QJL projection z = S r
 // is an fp32 FMA contraction against S^T staged in shared memory.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -291,6 +293,298 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   for (int i = tid; i < kPage * (D / 32); i += kQThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
 }
 
+// =============================================================================================
+// Bulk quantise (head_dim 128): the QJL projection z = S r on tcgen05 tensor cores.
+//   - The residual r of a 128-token page is split into bf16 hi + lo (|r - hi - lo| <= 2^-18 |r|) and
+//     written as operand A (128 tokens x 128 coordinates, K-major, 128-byte swizzle).
+//   - S (operand B) is loaded once per persistent CTA from its pre-swizzled table.
+//   - 16 MMAs (M = N = 128, K = 16; hi then lo) accumulate z in TMEM (fp32, 128 columns).
+//   - Each thread reads back one token row with tcgen05.ld and keeps the signs.
+// =============================================================================================
+constexpr int kTcThreads = 256;
+constexpr uint32_t kTcS = 0, kTcAhi = 32768, kTcAlo = 65536, kTcKcode = 98304, kTcVcode = kTcKcode + 16384;
+constexpr uint32_t kTcSign = kTcVcode + 16384, kTcNorm = kTcSign + 2048, kTcScale = kTcNorm + 512;
+constexpr uint32_t kTcBar = kTcScale + 1024, kTcEnd = kTcBar + 64;
+constexpr size_t kTcSmem = kTcEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+// Instruction descriptor, kind::f16: D = f32, A = B = bf16, both K-major, N = 128, M = 128.
+constexpr uint32_t kIdescBf16M128N128 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32(w%4)..+31).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) k_quantize_bulk128(AppendArgs a, int pages_per_row, int batch) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* kcode = sm + kTcKcode;
+  uint8_t* vcode = sm + kTcVcode;
+  uint32_t* sgn = reinterpret_cast<uint32_t*>(sm + kTcSign);   // [128 tokens][4] sign words
+  uint32_t* norms = reinterpret_cast<uint32_t*>(sm + kTcNorm);
+  uint16_t* scales = reinterpret_cast<uint16_t*>(sm + kTcScale);
+  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kTcBar);
+  uint64_t* bar_mma = bar_s + 1;
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_s + 2);
+  const LayerView& lv = a.lv;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_launch();
+  if (tid == 0) {
+    mbar_init(bar_s, 1);
+    mbar_init(bar_mma, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_expect_tx(bar_s, 2u * D * D);
+    bulk_g2s(sm + kTcS, lv.S_sw, 2u * D * D, bar_s);
+  }
+  if (warp == 0) {  // 128 TMEM columns: the fp32 accumulator of one 128 x 128 page
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;\n" ::"r"(smem_u32(tslot))
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tslot;
+  float Dv[4], cent[4], bnd[3];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) Dv[e] = lv.D[4 * lane + e];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cent[i] = lv.cb[i];
+#pragma unroll
+  for (int i = 0; i < 3; ++i) bnd[i] = lv.cb[4 + i];
+  bool ok = __syncthreads_and(mbar_wait(bar_s, 0)) != 0;
+  const int vb = lv.vb, vhalf = 1 << (vb - 1);
+  const float inv_sqrt_d = rsqrtf((float)D);
+  const uint32_t s_addr = smem_u32(sm + kTcS), ahi_addr = smem_u32(sm + kTcAhi), alo_addr = smem_u32(sm + kTcAlo);
+  uint32_t mma_phase = 0;
+  const int ntasks = batch * lv.Hkv * pages_per_row;
+  for (int task = blockIdx.x; ok && task < ntasks; task += gridDim.x) {
+    const int b = task / (lv.Hkv * pages_per_row), h = (task / pages_per_row) % lv.Hkv, j = task % pages_per_row;
+    int slot, L, Np, pg, valid;
+    if (!page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && tid == 0)) continue;  // CTA-uniform
+    // ---- per token (warp): key rotation, norm, Lloyd-Max code, residual -> A; value quantisation.
+    // The 16 tokens of a warp are handled in chunks of 8 whose K and V rows are loaded together. ----
+    for (int c0 = 0; c0 < kPage / (kTcThreads / 32); c0 += 8) {
+    float kx[8][4], vx[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = warp + (kTcThreads / 32) * (c0 + i);
+      if (t < valid) {
+        load4(a, 0, slot, b, h, pg * kPage + t, L, Np, 4 * lane, kx[i]);
+        load4(a, 1, slot, b, h, pg * kPage + t, L, Np, 4 * lane, vx[i]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) kx[i][e] = vx[i][e] = 0.f;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int t = warp + (kTcThreads / 32) * (c0 + i);
+      float x[4], y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = kx[i][e];
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ss = fmaf(x[e], x[e], ss);
+      ss = warp_sum(ss);
+      const float n = sqrtf(ss);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) y[e] = x[e] * Dv[e];
+      warp_fwht<4>(y, lane);
+      const float scale = n > 0.f ? 1.0f / (n * sqrtf((float)D)) : 0.f;
+      float rr = 0.f, res[4];
+      uint32_t codes4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float yy = y[e] * scale;
+        const int idx = (yy > bnd[0]) + (yy > bnd[1]) + (yy > bnd[2]);
+        res[e] = yy - cent[idx];
+        rr = fmaf(res[e], res[e], rr);
+        codes4 |= (uint32_t)idx << (8 * e);
+      }
+      *reinterpret_cast<uint32_t*>(kcode + t * D + 4 * lane) = codes4;
+      rr = warp_sum(rr);
+      uint32_t hi[2], lo[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const uint16_t h0 = f32_to_bf16_rn(res[2 * e]), h1 = f32_to_bf16_rn(res[2 * e + 1]);
+        const uint16_t l0 = f32_to_bf16_rn(res[2 * e] - bf16_to_f32(h0));
+        const uint16_t l1 = f32_to_bf16_rn(res[2 * e + 1] - bf16_to_f32(h1));
+        hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
+      }
+      const uint32_t off = sw128_offset(t, 4 * lane);
+      *reinterpret_cast<uint2*>(sm + kTcAhi + off) = make_uint2(hi[0], hi[1]);
+      *reinterpret_cast<uint2*>(sm + kTcAlo + off) = make_uint2(lo[0], lo[1]);
+      if (lane == 0) {
+        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
+        norms[t] = (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[e] = vx[i][e] * Dv[e];
+      warp_fwht<4>(x, lane);
+      float am = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        x[e] *= inv_sqrt_d;
+        am = fmaxf(am, fabsf(x[e]));
+      }
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
+      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
+      const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
+      const __half sh = __float2half_rn(s32);
+      const float sv = __half2float(sh);
+      uint32_t vc4 = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int code = vhalf;
+        if (sv > 0.f) {
+          const float qv = floorf(__fdiv_rn(x[e], sv));
+          code = (int)fminf(fmaxf(qv, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
+        }
+        vc4 |= (uint32_t)code << (8 * e);
+      }
+      *reinterpret_cast<uint32_t*>(vcode + t * D + 4 * lane) = vc4;
+      if ((lane & 7) == 0) scales[t * (D / 32) + (lane >> 3)] = __half_as_ushort(sh);
+    }
+    }
+    // ---- z = S r on the tensor cores ----
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+        umma_bf16(tmem, umma_desc_sw128(ahi_addr + koff), umma_desc_sw128(s_addr + koff), kIdescBf16M128N128,
+                  ks > 0 ? 1u : 0u);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+        umma_bf16(tmem, umma_desc_sw128(alo_addr + koff), umma_desc_sw128(s_addr + koff), kIdescBf16M128N128, 1u);
+      }
+      umma_commit(bar_mma);
+    }
+    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase)) != 0;
+    mma_phase ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    {  // warp w: TMEM lanes 32(w%4).. (tokens), columns 64(w/4).. (projection rows)
+      const int q = warp & 3, ch = warp >> 2, t = 32 * q + lane;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t z[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * ch + 32 * cc), z);
+        uint32_t bits = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) bits |= (uint32_t)(__uint_as_float(z[i]) >= 0.f) << i;
+        sgn[t * 4 + 2 * ch + cc] = bits;
+      }
+    }
+    tc_fence_before();
+    __syncthreads();
+    // ---- pack the page (fragment-major layout) ----
+    uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
+    const PageLayout pl = page_layout(D, vb);
+    uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+    for (int w = tid; w < 8 * 3 * 32 * 2; w += kTcThreads) {
+      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3, tile = w / 192;
+      const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
+      uint32_t word = 0;
+      if (pi < 2) {
+        const uint8_t* kc = kcode + t * D + 2 * c;
+#pragma unroll
+        for (int sq = 0; sq < 8; ++sq)
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int code = kc[16 * sq + 8 * sub + e];
+              word |= (uint32_t)((pi == 0 ? code >> 1 : code) & 1) << (2 * sq + sub + 16 * e);
+            }
+      } else {
+#pragma unroll
+        for (int sq = 0; sq < 8; ++sq)
+#pragma unroll
+          for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int jj = 16 * sq + 8 * sub + 2 * c + e;
+              word |= ((sgn[t * 4 + (jj >> 5)] >> (jj & 31)) & 1u) << (2 * sq + sub + 16 * e);
+            }
+      }
+      kw[w] = word;
+    }
+    uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
+    for (int t = tid; t < kPage; t += kTcThreads) nw[t] = norms[t];
+    uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
+    if (vb == 2) {
+      for (int w = tid; w < 4 * (D / 16) * 32; w += kTcThreads) {
+        const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
+        const int g = ln >> 2, c = ln & 3;
+        uint32_t word = 0;
+#pragma unroll
+        for (int kap = 0; kap < 2; ++kap)
+#pragma unroll
+          for (int rg = 0; rg < 4; ++rg)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+              word |= (uint32_t)vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
+            }
+        vw[w] = word;
+      }
+    } else {
+      for (int w = tid; w < 4 * (D / 16) * 32 * 2; w += kTcThreads) {
+        const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
+        const int g = ln >> 2, c = ln & 3;
+        uint32_t word = 0;
+#pragma unroll
+        for (int rg = 0; rg < 4; ++rg)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+            word |= (uint32_t)vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
+          }
+        vw[w] = word;
+      }
+    }
+    uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
+    for (int i = tid; i < kPage * (D / 32); i += kTcThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
+    __syncthreads();  // shared buffers are reused by the next page
+  }
+  if (!ok && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;\n" ::"r"(tmem) : "memory");
+}
+
 // Ring update after the quantise launch: write the new ring tail and the sequence state.
 __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
   const int b = blockIdx.x;
@@ -376,6 +670,19 @@ cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStrea
   return launch_quantize_d<256>(a, batch, pages, s);
 }
 
+// Bulk appends of head_dim 128 use the tcgen05 kernel: one persistent CTA per SM over all pages.
+cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+  static bool attr_set = false;  // set once, outside any stream capture that follows
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int ntasks = batch * a.lv.Hkv * pages;
+  const int grid = std::max(1, std::min(ntasks, sms));
+  return launch_pdl(k_quantize_bulk128, dim3(grid), dim3(kTcThreads), kTcSmem, s, a, pages, batch);
+}
+
 }  // namespace
 
 cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const void* v, int dt,
@@ -390,7 +697,9 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.max_new = max_new;
   a.flush = 0;
   const int pages = (max_new + kPage - 1) / kPage;
-  cudaError_t e = launch_quantize(a, batch, pages, s);
+  cudaError_t e = (a.lv.d == 128 && max_new >= kPage)
+                      ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
+                      : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_ring_update, dim3(batch), dim3(256), 0, s, a);
 }
