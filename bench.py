@@ -118,6 +118,61 @@ class ClockSampler:
 # --------------------------------------------------------------------------------------------
 # our arm
 # --------------------------------------------------------------------------------------------
+def aggregate_over_ranks(ms, units, world, device):
+    """Whole-job throughput of `world` replicas: every rank processed `units`; time = max over ranks."""
+    t_max = float(ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        tt = torch.tensor([t_max], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+    return t_max, units * world / (t_max * 1e-3)
+
+
+def bench_config(world):
+    return {"workload": WL["name"], "layers": WL["layers"], "q_heads": WL["hq"], "kv_heads": WL["hkv"],
+            "head_dim": WL["d"], "batch_per_gpu": WL["batch"], "context": WL["ctx"], "value_bits": WL["vb"],
+            "ring": 128, "l2": "inputs larger than L2 (~785 MB of packed records per step vs 129 MB L2)",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "step": "append 1 token + hybrid decode attention, all 32 layers, one CUDA graph replay"}
+
+
+DECODE_SOURCES = ("tq_decode.cu", "tq_device.cuh", "tq_internal.h")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_llama8b_b1_ctx32k.md")
+
+
+def decode_source_digest():
+    """sha256 over the sources that make up the decode kernel (ties ncu counters to a kernel version)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "kv_cache_quantization_quantize_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(path=DECODE_PROFILE):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the current sources."""
+    try:
+        with open(path) as f:
+            text = f.read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        line = line.strip().strip("`- ")
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("source_digest") != decode_source_digest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -176,7 +231,7 @@ def run_ours(args):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         step()
-    launches_per_step = L_layers * 5  # quantize + ring update + prep + split-K + combine per layer
+    launches_per_step = L_layers * 4  # quantize + ring update + prep + split-K (combine inside) per layer
 
     gpu_id = local
     try:
@@ -211,12 +266,7 @@ def run_ours(args):
     status = cache.check_status()
     ctx_tokens = sum(B * (L_first + i) for i in range(K))  # each step attends its full context
     # max over ranks of the timed region; whole-job throughput
-    t_max = ms
-    if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
-    value = ctx_tokens * world / (t_max * 1e-3)
+    t_max, value = aggregate_over_ranks(ms, ctx_tokens, world, dev)
     ms_per_step = t_max / K
 
     # algorithmic bytes per step: packed K3/V2 records + ring (K,V bf16) + q + out, all layers
@@ -252,13 +302,7 @@ def run_ours(args):
     kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
     kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
-    traffic = None
-    tfile = os.path.join(ROOT, "profiles", "k_decode_traffic.json")
-    if os.path.exists(tfile):
-        try:
-            traffic = json.load(open(tfile)).get("bytes_per_launch")
-        except Exception:
-            traffic = None
+    traffic = profiled_traffic()
 
     # ---- end to end through the public API with pinned host buffers ----
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
@@ -303,12 +347,8 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3/f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
-        "config": {"workload": WL["name"], "layers": L_layers, "q_heads": Hq, "kv_heads": Hkv, "head_dim": d,
-                   "batch_per_gpu": B, "context": ctx, "value_bits": vb, "ring": 128,
-                   "l2": "inputs larger than L2 (~785 MB of packed records per step vs 129 MB L2)",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "step": "append 1 token + hybrid decode attention, all 32 layers, one CUDA graph replay"},
+        "dtype": "f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
+        "config": bench_config(world),
         "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * hbm_gbs / peak,
         "roofline": {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
@@ -488,8 +528,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * units * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WL["name"], "context": WL["ctx"], "layers": WL["layers"], "kv_heads": WL["hkv"],
-                       "q_heads": WL["hq"], "head_dim": WL["d"], "value_bits": WL["vb"]},
+            "config": bench_config(world),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
