@@ -51,6 +51,11 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
+// f16x2 pattern of -v * 2^(pos-24) in both halves (an f16 subnormal: v << pos with the sign bit).
+__host__ __device__ constexpr uint32_t voff_pattern(uint32_t v, int pos) {
+  return (0x8000u | (v << pos)) * 0x00010001u;
+}
+
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   const __half2 r = __hmul2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
   return *reinterpret_cast<const uint32_t*>(&r);
@@ -537,7 +542,6 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
   float m_eff[2] = {-INFINITY, -INFINITY}, l_acc[2] = {0.f, 0.f};
-  float lg[4] = {0.f, 0.f, 0.f, 0.f};  // B layout: head g, the four value groups of this half
   __syncthreads();
   bool timed_out = false;
 
@@ -641,19 +645,6 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       m_eff[col] = m_new;
       l_acc[col] *= alpha[col];
     }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) {
-      O[mt][0] *= alpha[0];
-      O[mt][1] *= alpha[1];
-      O[mt][2] *= alpha[0];
-      O[mt][3] *= alpha[1];
-    }
-    {  // lg lives in the B layout (head g): fetch alpha of head g from lane (g >> 1)
-      const float a0 = __shfl_sync(0xffffffffu, alpha[0], g >> 1), a1 = __shfl_sync(0xffffffffu, alpha[1], g >> 1);
-      const float ab = (g & 1) ? a1 : a0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) lg[q] *= ab;
-    }
     uint32_t pb[2][2];  // B fragments of P (no value scale yet): [k-step][tokens 0-7 / 8-15]
 #pragma unroll
     for (int kap = 0; kap < 2; ++kap) {
@@ -671,7 +662,16 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       pb[kap][1] = movmatrix_trans(pack_half2(pv[2], pv[3]));
     }
     // ---- P.V, one value group (two m-tiles) of this half at a time ----
+    // Each page's product starts from its own mid-rise offset: C = -off * sum_t p_t s_t per head,
+    // made by one MMA pair whose A is the constant -(2^VB - 1) * 2^(pos-24) (= -2 off at each token's
+    // position) and halved. The codes then add sum_t code_t p_t s_t, so the cancellation between the
+    // code sum and the offset stays inside one page, however long the context.
     const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + pl.vbits_off);
+    constexpr uint32_t kVmax = (1u << VB) - 1u;
+    constexpr uint32_t kOff00 = voff_pattern(kVmax, VB == 2 ? vpos2(0, 0) : vpos4(0));
+    constexpr uint32_t kOff01 = voff_pattern(kVmax, VB == 2 ? vpos2(0, 1) : vpos4(1));
+    constexpr uint32_t kOff10 = voff_pattern(kVmax, VB == 2 ? vpos2(1, 0) : vpos4(0));
+    constexpr uint32_t kOff11 = voff_pattern(kVmax, VB == 2 ? vpos2(1, 1) : vpos4(1));
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int gq = 4 * hf + q;
@@ -681,26 +681,31 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
         const int tile = 2 * tg + kap;
         bf[kap][0] = hmul2_u32(pb[kap][0], vsc[(8 * tile + c) * NG + gq]);
         bf[kap][1] = hmul2_u32(pb[kap][1], vsc[(8 * tile + 4 + c) * NG + gq]);
-        // the mid-rise offset is removed with the same f16 weights the MMA multiplies
-        const float2 r0 = half2_to_float2(bf[kap][0]), r1 = half2_to_float2(bf[kap][1]);
-        const int p0 = VB == 2 ? vpos2(kap, 0) : vpos4(0), p1 = VB == 2 ? vpos2(kap, 1) : vpos4(1);
-        lg[q] = fmaf(r0.x + r0.y, 1.0f / (float)(1u << (24 - p0)), lg[q]);
-        lg[q] = fmaf(r1.x + r1.y, 1.0f / (float)(1u << (24 - p1)), lg[q]);
       }
+      float coff[4] = {0.f, 0.f, 0.f, 0.f};
+      mma_f16(coff, kOff00, kOff00, kOff01, kOff01, bf[0][0], bf[0][1]);
+      mma_f16(coff, kOff10, kOff10, kOff11, kOff11, bf[1][0], bf[1][1]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) coff[i] *= 0.5f;
 #pragma unroll
       for (int mh = 0; mh < 2; ++mh) {
         const int mt = 2 * q + mh, mtg = 8 * hf + mt;
+        float acc[4] = {coff[0], coff[1], coff[2], coff[3]};
         if (VB == 2) {
           const uint32_t w = vw[(tg * (D / 16) + mtg) * 32 + lane];
           const uint32_t w2 = w >> 2, w6 = w >> 6;
-          mma_f16(O[mt], w & 0x00030003u, w2 & 0x00030003u, w & 0x00300030u, w6 & 0x00300030u, bf[0][0], bf[0][1]);
-          mma_f16(O[mt], w & 0x00C000C0u, w6 & 0x00C000C0u, w & 0x03000300u, w6 & 0x03000300u, bf[1][0], bf[1][1]);
+          mma_f16(acc, w & 0x00030003u, w2 & 0x00030003u, w & 0x00300030u, w6 & 0x00300030u, bf[0][0], bf[0][1]);
+          mma_f16(acc, w & 0x00C000C0u, w6 & 0x00C000C0u, w & 0x03000300u, w6 & 0x03000300u, bf[1][0], bf[1][1]);
         } else {
           const uint2 ww = reinterpret_cast<const uint2*>(vw)[(tg * (D / 16) + mtg) * 32 + lane];
           const uint32_t x0 = ww.x, x8 = ww.x >> 8, y0 = ww.y, y8 = ww.y >> 8;
-          mma_f16(O[mt], x0 & 0x000F000Fu, x8 & 0x000F000Fu, x0 & 0x00F000F0u, x8 & 0x00F000F0u, bf[0][0], bf[0][1]);
-          mma_f16(O[mt], y0 & 0x000F000Fu, y8 & 0x000F000Fu, y0 & 0x00F000F0u, y8 & 0x00F000F0u, bf[1][0], bf[1][1]);
+          mma_f16(acc, x0 & 0x000F000Fu, x8 & 0x000F000Fu, x0 & 0x00F000F0u, x8 & 0x00F000F0u, bf[0][0], bf[0][1]);
+          mma_f16(acc, y0 & 0x000F000Fu, y8 & 0x000F000Fu, y0 & 0x00F000F0u, y8 & 0x00F000F0u, bf[1][0], bf[1][1]);
         }
+        O[mt][0] = fmaf(O[mt][0], alpha[0], acc[0]);
+        O[mt][1] = fmaf(O[mt][1], alpha[1], acc[1]);
+        O[mt][2] = fmaf(O[mt][2], alpha[0], acc[2]);
+        O[mt][3] = fmaf(O[mt][3], alpha[1], acc[3]);
       }
     }
     __syncthreads();  // every warp is done with stage s_ (and with xbuf)
@@ -714,8 +719,7 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
   __syncthreads();
   float* wm = reinterpret_cast<float*>(stage0);  // [4 token groups][4 heads]
   float* wl = wm + 16;                           // [4][4]
-  float* wlg = wl + 16;                          // [4][4][NG]
-  float* wo = wlg + 16 * NG;                     // [4][4][D]
+  float* wo = wl + 16;                           // [4][4][D]
   {
     float l0 = l_acc[0], l1 = l_acc[1];
 #pragma unroll
@@ -723,20 +727,11 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      lg[q] += __shfl_xor_sync(0xffffffffu, lg[q], 1);
-      lg[q] += __shfl_xor_sync(0xffffffffu, lg[q], 2);
-    }
     if (hf == 0 && g == 0 && c < 2) {
       wm[tg * 4 + 2 * c] = m_eff[0];
       wm[tg * 4 + 2 * c + 1] = m_eff[1];
       wl[tg * 4 + 2 * c] = l0;
       wl[tg * 4 + 2 * c + 1] = l1;
-    }
-    if (c == 0 && g < kMaxG) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) wlg[(tg * 4 + g) * NG + 4 * hf + q] = lg[q];
     }
     if (c < 2) {
 #pragma unroll
@@ -750,7 +745,6 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
     }
   }
   __syncthreads();
-  const float off = (float)(1 << (VB - 1)) - 0.5f;
   for (int i = tid; i < kMaxG * D; i += NT) {
     const int hd = i / D, j = i % D;
     float m = -INFINITY;
@@ -762,7 +756,7 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       for (int w = 0; w < 4; ++w) {
         const float mw = wm[w * 4 + hd];
         const float f = mw == -INFINITY ? 0.f : exp2f(mw - m);
-        o += f * (wo[(w * 4 + hd) * D + j] - off * wlg[(w * 4 + hd) * NG + j / 32]);
+        o += f * wo[(w * 4 + hd) * D + j];
         l += f * wl[w * 4 + hd];
       }
     }
@@ -784,7 +778,7 @@ template <int D, int VB>
 size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB);
   constexpr int NT = decode_threads<D>();
-  const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * (D / 32) + 16 * D);
+  const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * D);
   const size_t xbuf_bytes = D == 256 ? sizeof(float) * NT * 2 * 8 : 0;
   size_t smem = 128 + (size_t)decode_stages<D, VB>() * pl.bytes + xbuf_bytes;
   smem = std::max(smem, 128 + merge_bytes);

@@ -71,8 +71,8 @@ TQ_HD int vfield2(int kap, int r) { return ((kap ? 0x7463 : 0x5210) >> (4 * r)) 
 TQ_HD int vfield4(int r) { return (0x3120 >> (4 * r)) & 0xF; }
 // Effective mantissa position (after the decoder's shift) of the field for the low/high token half
 // of a k-step; the decoder's B operand is prescaled by 2^(24 - pos).
-TQ_HD int vpos2(int kap, int hiT) { return kap ? (hiT ? 8 : 6) : (hiT ? 4 : 0); }
-TQ_HD int vpos4(int hiT) { return hiT ? 4 : 0; }
+TQ_HD constexpr int vpos2(int kap, int hiT) { return kap ? (hiT ? 8 : 6) : (hiT ? 4 : 0); }
+TQ_HD constexpr int vpos4(int hiT) { return hiT ? 4 : 0; }
 
 // Location of the value code of (token t, coordinate j) in VBITS: u32 word index and LSB of the field.
 // A-fragment (m16n8k16, rows = coordinates, k = tokens) register r = rowhi + 2*hiT of lane (g, c)

@@ -20,17 +20,17 @@ Readings of points the pages leave open are listed with each function.
 
 Parity status:
 * Every function here is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle_*.py``, except
-  ``key_cos_sim_report``. Its page figure (key cos_sim of about 1.000000, [Guide] §六) names no quantity
+  the key figure of ``cos_sim_report``. Its page figure (key cos_sim of about 1.000000, [Guide] §六) names no quantity
   that can be reproduced. It is **parity unpinned** and is only reported.
 """
 
 from .rng import splitmix64, derive_seed, rademacher_signs, gaussian_matrix_bf16, round_to_bf16
 from .rotation import hadamard, rotation_matrix
-from .codebook import lloyd_max_codebook, beta_marginal_pdf
+from .codebook import lloyd_max_codebook, beta_marginal_pdf, mse_distortion
 from .quant import (
     KeyRecords, ValueRecords, quantize_keys, quantize_values, dequantize_keys, dequantize_values,
     pack_key_records, unpack_key_records, pack_value_records, unpack_value_records,
-    key_record_bytes, value_record_bytes, history_split,
+    key_record_bytes, value_record_bytes, history_split, cos_sim_report,
 )
 from .attention import decode_attention, estimated_scores, qjl_inner_product_estimate
 from .memory import kv_bytes_dense, kv_bytes_turboquant, kv_bytes_bits_per_element

@@ -124,3 +124,27 @@ def test_history_split_ring_semantics():
     assert history_split(129) == (128, 1)
     assert history_split(1152) == (1024, 128)  # 1024 packed + 128-token ring
     assert history_split(32768) == (32640, 128)
+
+
+def test_cos_sim_report_pins():
+    """Values on the quantiser grid reconstruct exactly (cos 1). For keys, the Lloyd-Max centroid
+    condition gives E<y, c[idx]> = E||c[idx]||^2 = 1 - D, so the MSE-only cosine of rotated unit vectors
+    tends to sqrt(1 - D), with D = d x the codebook's per-coordinate distortion. Adding the QJL term (unbiased, not
+    MSE-optimal) lowers the cosine."""
+    from oracle import cos_sim_report, lloyd_max_codebook, mse_distortion, gaussian_matrix_bf16
+    d, bits = 128, 2
+    D = rademacher_signs(9, d)
+    rng = np.random.default_rng(0)
+    codes = rng.integers(0, 4, size=(10, d))
+    codes[:, ::32] = 3
+    v = ((codes - 1.5) * 0.5) @ (scipy.linalg.hadamard(d) * D[None, :] / np.sqrt(d))
+    vrec = quantize_values(v, D, bits)
+    c, t = lloyd_max_codebook(d, 2)
+    S = gaussian_matrix_bf16(9, d)
+    k = rng.standard_normal((4000, d))
+    krec = quantize_keys(k, D, S, c, t)
+    rep = cos_sim_report(k, v, krec, vrec, D, S, c)
+    assert abs(rep["value_cos"] - 1.0) < 1e-12
+    expect = np.sqrt(1.0 - d * mse_distortion(d, c, t))  # per-coordinate distortion x d = unit-vector D
+    assert abs(rep["key_cos_mse"] - expect) < 3e-3, (rep, expect)
+    assert rep["key_cos_qjl"] < rep["key_cos_mse"]
