@@ -142,11 +142,13 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
  *     over the packed history, and exact dot products over the ring.
  *   - One softmax runs over both.
  *   - d_workspace: at least tq_workspace_bytes(ctx, batch, max_ctx_hint) bytes, 256-byte aligned,
- *     scratch owned by the caller.
+ *     scratch owned by the caller. It holds per-(row, KV head) arrival counters that must be zero
+ *     before the first call on a workspace (zero-fill it once, or run tq_decode_phase 0); every call
+ *     leaves them at zero again.
  *   - max_ctx_hint: an upper bound on every row's length (0 = cfg.max_ctx). It only sizes the grid;
  *     a row longer than the hint sets TQ_DEV_ERR_SPLITS.
- *   - Launches: query prep, then split-K decode (+ ring split); the last CTA of each (row, KV head)
- *     runs the combine. */
+ *   - Launches: one split-K decode kernel (+ the ring split). Every split CTA rotates and projects
+ *     the query itself; the last CTA of each (row, KV head) runs the combine. */
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream);
@@ -154,12 +156,14 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
 /* tq_decode_phase: launches one phase of tq_decode_attention with the same arguments, for callers that
  * interleave the phases with other work or time them one by one. The three phases run in order on
  * one workspace:
- *   0 = query prep (rotate, project, f16 operands of the key bit-plane MMAs);
- *   1 = split-K decode over packed pages plus the exact ring split. The last CTA of every
+ *   0 = zero the workspace's arrival counters (a memset; needed once before the first phase-1 call
+ *       on a workspace that was not zero-filled);
+ *   1 = split-K decode over packed pages (each split CTA prepares the query: rotation, projection,
+ *       f16 operands of the key bit-plane MMAs) plus the exact ring split. The last CTA of every
  *       (row, KV head) also runs the combine: log-sum-exp merge, inverse rotation, ring merge -> out;
- *   2 = nothing (accepted for callers written against a separate combine phase).
- * Phase 1 needs phase 0's workspace, including the arrival counters that phase 0 zeroes. Calling the
- * phases in the order 0, 1, 2 is equivalent to one tq_decode_attention call. */
+ *   2 = nothing (accepted for callers written against separate prep and combine phases).
+ * Phase 1 leaves the counters at zero, so calling 0, 1, 2 or just 1 on a zeroed workspace is
+ * equivalent to one tq_decode_attention call. */
 tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream);
@@ -175,9 +179,11 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *     with TQ_ERR_CAPACITY and a message; nothing is launched.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current. Make that first call before any stream capture.
- *   - Every call shares the one array, whose contents persist between calls. Nothing in it needs to
- *     start at zero: each call writes every entry it later reads. Calls that overlap on the GPU (on
- *     different streams, or from different host threads) race on it and give wrong results; order them. */
+ *   - Every call shares the one array, whose contents persist between calls. The only entries that
+ *     must start at zero are the arrival counters: the array is zero-filled when the library loads and
+ *     every call leaves the counters at zero; everything else a call reads, it writes first. Calls that
+ *     overlap on the GPU (on different streams, or from different host threads) race on it and give
+ *     wrong results; order them. */
 tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                       int batch, float softmax_scale, int max_ctx_hint, tq_stream_t stream);
 

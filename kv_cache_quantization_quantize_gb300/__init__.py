@@ -126,7 +126,7 @@ class TurboQuantCache(HostTables):
     def workspace(self, batch, max_ctx_hint=0):
         n = self.workspace_bytes(batch, max_ctx_hint)
         if self._ws is None or self._ws.numel() < n:
-            self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self._ws = torch.zeros(n, dtype=torch.uint8, device=self.device)  # arrival counters start at 0
         return self._ws
 
     def decode(self, layer, q, seq_ids, softmax_scale=0.0, out=None, max_ctx_hint=0, workspace=None, stream=None):

@@ -26,7 +26,6 @@ namespace tq {
 namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kPrepThreads = 128;
 
 struct DecodeArgs {
   LayerView lv;
@@ -84,6 +83,14 @@ __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L
 }
 
 template <int D>
+__host__ __device__ constexpr int decode_threads();
+// Floats of the d=256 partial-score exchange buffer of a split CTA ([NT][2 tiles][8]).
+template <int D>
+__host__ __device__ constexpr int decode_xbuf_floats() {
+  return D == 256 ? decode_threads<D>() * 2 * 8 : 0;
+}
+
+template <int D>
 __host__ __device__ constexpr int decode_threads() {
   return 32 * 4 * (D / 128);  // 4 token groups x (d/128) coordinate halves
 }
@@ -91,47 +98,68 @@ __host__ __device__ constexpr int decode_threads() {
 // =============================================================================================
 // Query prep: q_rot = Pi q, q_proj = S q_rot; f16 operands of the three key bit-plane MMAs
 // =============================================================================================
-// Effective f16 bit position that carries coordinate j in the key words (kbit_loc, kpair_pos).
-__device__ __forceinline__ int key_qeff(int j) {
-  const int jj = j & 127;
-  return kpair_pos(2 * (jj >> 4) + ((jj >> 3) & 1));
+
+// Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
+template <int D>
+__host__ __device__ constexpr size_t prep_scratch_bytes() {
+  return sizeof(float) * (2 * kMaxG * D + 16);
 }
 
+// 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
+__host__ __device__ constexpr float key_prescale(int q) { return (float)(1u << (24 - (q < 12 ? q : q - 4))); }
+
+// Query prep of one (row, KV head), run by every split CTA of that unit (all NT threads):
+//   q_rot = Pi q (warp-per-head FWHT), q_proj = S q_rot (m16n8k16 with A = S in f16 from the tables
+//   and B = q_rot split into f16 hi + lo), then the f16 B fragments of the three key bit-plane MMAs
+//   for this warp's coordinate half and the per-head constants of the score epilogue.
+// The B operand of plane pi at coordinate j is w_pi * lambda * x_j * 2^(24 - pos(j)), with w = 2 alpha,
+// 2 beta (x = q_rot) or 2 (x = q_proj) and lambda a power of two that puts the largest operand in
+// [2^14, 2^15). um / uq undo lambda (and apply the softmax scale in log2 units); cm / cq are half the
+// sums of the represented (rounded) operands, i.e. the +-1 offsets of the bit planes.
+// A fragments of S (f16) that this warp's q_proj rows need: m-tiles 2 warp + {0, 1}. For head_dim 128
+// they are loaded into registers before the kernel waits on earlier stream work (the tables are
+// constant); for head_dim 256 query_prep loads them itself.
 template <int D>
-__host__ __device__ constexpr size_t prep_smem_bytes() {
-  return 128 + 2 * D * D + 2 * kMaxG * D * 4 + 64;
+struct SFrag {
+  uint4 a[D == 128 ? 2 : 1][D == 128 ? D / 16 : 1];
+};
+template <int D>
+__device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f) {
+  if (D == 128) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int m2 = 0; m2 < 2; ++m2)
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) f.a[m2 % (D == 128 ? 2 : 1)][ks % (D == 128 ? D / 16 : 1)] =
+          __ldg(lv.S_frag + sfrag_idx(D, 2 * warp + m2, ks, lane));
+  }
 }
 
-// Workspace of one (row, KV head): B fragments [plane 3][half D/128][kstep 8][lane 32] uint2, then
-// 4 floats per head {u_mse, C_mse, u_qjl, C_qjl}.
-template <int D>
-__global__ void __launch_bounds__(kPrepThreads) k_prep(DecodeArgs a) {
+// Query prep of one (row, KV head), run by every split CTA of that unit (all NT threads):
+//   q_rot = Pi q (warp-per-head FWHT), q_proj = S q_rot (m16n8k16 with A = S in f16 from the tables
+//   and B = q_rot split into f16 hi + lo), then the f16 B fragments of the three key bit-plane MMAs
+//   for this warp's coordinate half and the per-head constants of the score epilogue.
+// The B operand of plane pi at coordinate j is w_pi * lambda * x_j * 2^(24 - pos(j)), with w = 2 alpha,
+// 2 beta (x = q_rot) or 2 (x = q_proj). lambda is a power of two that keeps every operand below 2^15
+// (f16 max 65504), from bounds: max|w x_j| 2^24 with max|q_proj| <= max_i sum_j |S_ij| * max|q_rot|.
+// um / uq undo lambda (and apply the softmax scale in log2 units); cm / cq are half the sums of the
+// represented (rounded) operands, i.e. the +-1 offsets of the bit planes.
+template <int D, int NT>
+__device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
+                                           uint2 (&bq)[3][8], float (&um)[2], float (&cm)[2], float (&uq)[2],
+                                           float (&cq)[2]) {
   constexpr int NE = D / 32;
   constexpr int HALVES = D / 128;
-  extern __shared__ __align__(128) uint8_t psm[];
-  uint64_t* bar = reinterpret_cast<uint64_t*>(psm);
-  const uint16_t* st = reinterpret_cast<const uint16_t*>(psm + 128);  // S^T bf16 [D][D]
-  float* qr = reinterpret_cast<float*>(psm + 128 + 2 * D * D);        // [4][D]
-  float* qp = qr + kMaxG * D;                                         // [4][D]
-  float* red = qp + kMaxG * D;                                        // lambda [4][2], sums [2][4]
-  const int b = blockIdx.x, h = blockIdx.y;
+  constexpr int MT = D / 16;
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3, hf = warp >> 2;
   const int G = lv.G;
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    mbar_expect_tx(bar, 2u * D * D);
-    bulk_g2s(psm + 128, lv.St, 2u * D * D, bar);
-  }
-  // S^T (a constant table) streams in while the previous kernel finishes; q and the workspace are
-  // touched only after it has completed. Dependents are released after that point, so the decode
-  // kernel may read the cache as soon as it starts.
-  pdl_wait();
-  pdl_launch();
-  if (tid < 8) red[8 + tid] = 0.f;
-  if (tid == 0) reinterpret_cast<int32_t*>(a.ws + a.plan.cnt_off)[b * lv.Hkv + h] = 0;
-  {  // warp w rotates head w (zero rows for heads >= G) while S^T streams in
+  const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
+  float* qr = ps;               // [4][D]
+  float* qp = qr + kMaxG * D;   // [4][D]
+  float* red = qp + kMaxG * D;  // [hd]: projection lambda; [4 + 2 hd + {0, 1}]: operand lambdas
+  if (warp < kMaxG) {           // q_rot: warp w rotates head w (zero rows for heads >= G)
     float x[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
@@ -140,100 +168,126 @@ __global__ void __launch_bounds__(kPrepThreads) k_prep(DecodeArgs a) {
       x[e] = qv * lv.D[j];
     }
     warp_fwht<NE>(x, lane);
-    const float s = rsqrtf((float)D);
+    const float rs = rsqrtf((float)D);
+    float mx = 0.f;
 #pragma unroll
-    for (int e = 0; e < NE; ++e) qr[warp * D + (e >> 2) * 128 + 4 * lane + (e & 3)] = x[e] * s;
-  }
-  __syncthreads();
-  if (!mbar_wait(bar, 0)) {
-    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
-    return;
-  }
-  for (int i = tid; i < D; i += kPrepThreads) {  // q_proj[i] = sum_j St[j][i] q_rot[j]
-    float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
-    for (int j = 0; j < D; ++j) {
-      const float sv = bf16_to_f32(st[j * D + i]);
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) acc[g] = fmaf(sv, qr[g * D + j], acc[g]);
+    for (int e = 0; e < NE; ++e) {
+      const float v = x[e] * rs;
+      qr[warp * D + (e >> 2) * 128 + 4 * lane + (e & 3)] = v;
+      mx = fmaxf(mx, fabsf(v));
     }
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) qp[g * D + i] = acc[g];
-  }
-  __syncthreads();
-  const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
-  {  // per-head power-of-two scales: largest prescaled operand in [2^14, 2^15) (f16 max 65504)
-    float mm = 0.f, mq = 0.f;
-    for (int j = lane; j < D; j += 32) {
-      const float pre = exp2f((float)(24 - key_qeff(j)));
-      mm = fmaxf(mm, fabsf(alpha2 * qr[warp * D + j]) * pre);
-      mq = fmaxf(mq, fabsf(2.f * qp[warp * D + j]) * pre);
-    }
-    mm = warp_max(mm);
-    mq = warp_max(mq);
+    mx = warp_max(mx);
     if (lane == 0) {
-      red[2 * warp + 0] = mm > 0.f ? exp2f(floorf(log2f(32768.f / mm))) : 1.f;
-      red[2 * warp + 1] = mq > 0.f ? exp2f(floorf(log2f(32768.f / mq))) : 1.f;
+      const float big = 16777216.f;  // 2^24, the largest bit-plane prescale
+      red[warp] = mx > 0.f ? exp2f(floorf(log2f(16384.f / mx))) : 1.f;
+      const float bm = fmaxf(alpha2, beta2) * mx * big, bp = 2.f * lv.cb[10] * mx * big;
+      red[4 + 2 * warp + 0] = bm > 0.f ? exp2f(floorf(log2f(32768.f / bm))) : 1.f;
+      red[4 + 2 * warp + 1] = bp > 0.f ? exp2f(floorf(log2f(32768.f / bp))) : 1.f;
     }
   }
   __syncthreads();
-  uint8_t* prep = a.ws + a.plan.prep_off + ((size_t)b * lv.Hkv + h) * a.plan.prep_stride;
-  uint2* frag = reinterpret_cast<uint2*>(prep);
-  float* cst = reinterpret_cast<float*>(prep + (size_t)3 * HALVES * 8 * 32 * 8);
-  const int head = lane >> 2, c = lane & 3;  // the same lane (and head) for every item of this thread
-  const bool live = head < G;
+  {  // q_proj rows 16 mt .. 16 mt + 15, mt = 2 warp + {0, 1}; B column n = head g (zero for g >= 4)
+    const bool col = g < kMaxG;
+    const float lam = col ? red[g] : 0.f;
+    const float* qrow = qr + (col ? g : 0) * D + 2 * c;
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < MT; ++ks) {
+      const float x0 = qrow[16 * ks] * lam, x1 = qrow[16 * ks + 1] * lam;
+      const float x2 = qrow[16 * ks + 8] * lam, x3 = qrow[16 * ks + 9] * lam;
+      const uint32_t h0 = pack_half2(x0, x1), h1 = pack_half2(x2, x3);
+      const float2 r0 = half2_to_float2(h0), r1 = half2_to_float2(h1);
+      const uint32_t l0 = pack_half2(x0 - r0.x, x1 - r0.y), l1 = pack_half2(x2 - r1.x, x3 - r1.y);
+#pragma unroll
+      for (int m2 = 0; m2 < 2; ++m2) {
+        const uint4 A = D == 128 ? sf.a[m2 % (D == 128 ? 2 : 1)][ks % (D == 128 ? MT : 1)]
+                                 : __ldg(lv.S_frag + sfrag_idx(D, 2 * warp + m2, ks, lane));
+        mma_f16(acc[m2], A.x, A.y, A.z, A.w, h0, h1);
+        mma_f16(acc[m2], A.x, A.y, A.z, A.w, l0, l1);
+      }
+    }
+    if (2 * c < kMaxG) {  // C columns 2c, 2c + 1 are heads
+      const float i0 = 1.f / red[2 * c], i1 = 1.f / red[2 * c + 1];
+#pragma unroll
+      for (int m2 = 0; m2 < 2; ++m2) {
+        const int r = 16 * (2 * warp + m2) + g;
+        qp[(2 * c) * D + r] = acc[m2][0] * i0;
+        qp[(2 * c + 1) * D + r] = acc[m2][1] * i1;
+        qp[(2 * c) * D + r + 8] = acc[m2][2] * i0;
+        qp[(2 * c + 1) * D + r + 8] = acc[m2][3] * i1;
+      }
+    }
+  }
+  __syncthreads();
+  const bool live = g < G;
+  const float lam_m = live ? red[4 + 2 * g] : 0.f, lam_q = live ? red[4 + 2 * g + 1] : 0.f;
+  const float* bm = qr + (live ? g : 0) * D;
+  const float* bp = qp + (live ? g : 0) * D;
   float sum_m = 0.f, sum_q = 0.f;
-  for (int item = tid; item < 3 * HALVES * 8 * 32; item += kPrepThreads) {
-    const int s = (item >> 5) & 7, half = (item >> 8) % HALVES, pi = item / (256 * HALVES);
-    const int j0 = 128 * half + 16 * s + 2 * c, j1 = j0 + 8;
-    const float w = pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f;
-    const float* base = (pi < 2 ? qr : qp) + (live ? head : 0) * D;
-    const float lam = live ? red[2 * head + (pi < 2 ? 0 : 1)] : 0.f;
-    const float pre0 = exp2f((float)(24 - key_qeff(j0))), pre1 = exp2f((float)(24 - key_qeff(j1)));
-    const uint32_t b0 = pack_half2(w * base[j0] * lam * pre0, w * base[j0 + 1] * lam * pre0);
-    const uint32_t b1 = pack_half2(w * base[j1] * lam * pre1, w * base[j1 + 1] * lam * pre1);
-    frag[item] = make_uint2(b0, b1);
-    // represented operand values times the bit weights 2^(q-24), for the +-1 offsets
-    const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
-    const float v = (r0.x + r0.y) / pre0 + (r1.x + r1.y) / pre1;
-    if (pi < 2) sum_m += v; else sum_q += v;
+#pragma unroll
+  for (int hv = 0; hv < HALVES; ++hv) {
+#pragma unroll
+    for (int pi = 0; pi < 3; ++pi) {
+      const float w = (pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f) * (pi < 2 ? lam_m : lam_q);
+      const float* base = pi < 2 ? bm : bp;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
+        const float pre0 = key_prescale(2 * s), pre1 = key_prescale(2 * s + 1);
+        const float2 x0 = *reinterpret_cast<const float2*>(base + j0);
+        const float2 x1 = *reinterpret_cast<const float2*>(base + j1);
+        const uint32_t b0 = pack_half2(w * x0.x * pre0, w * x0.y * pre0);
+        const uint32_t b1 = pack_half2(w * x1.x * pre1, w * x1.y * pre1);
+        if (hv == hf) bq[pi][s] = make_uint2(b0, b1);
+        const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
+        const float v = (r0.x + r0.y) * (1.f / pre0) + (r1.x + r1.y) * (1.f / pre1);
+        if (pi < 2) sum_m += v;
+        else sum_q += v;
+      }
+    }
   }
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 1);
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
-  if (c == 0 && head < kMaxG) {
-    atomicAdd(&red[8 + head], sum_m);
-    atomicAdd(&red[12 + head], sum_q);
-  }
-  __syncthreads();
-  if (tid < kMaxG) {
-    const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
-    cst[4 * tid + 0] = a.scale * kLog2e / red[2 * tid + 0];
-    cst[4 * tid + 1] = 0.5f * red[8 + tid];
-    cst[4 * tid + 2] = a.scale * kLog2e * kappa / red[2 * tid + 1];
-    cst[4 * tid + 3] = 0.5f * red[12 + tid];
+  const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd; its sums live in lanes 4 hd ..
+    const int hd = min(2 * c + i, kMaxG - 1);
+    const float sm_ = __shfl_sync(0xffffffffu, sum_m, 4 * hd), sq_ = __shfl_sync(0xffffffffu, sum_q, 4 * hd);
+    um[i] = a.scale * kLog2e / red[4 + 2 * hd];
+    cm[i] = 0.5f * sm_;
+    uq[i] = a.scale * kLog2e * kappa / red[4 + 2 * hd + 1];
+    cq[i] = 0.5f * sq_;
   }
 }
 
 // =============================================================================================
 // Split-K decode over packed pages (blockIdx.x < n_splits) and the exact ring split (== n_splits)
 // =============================================================================================
+// Ring split shared memory: K rows (and, for head_dim 128, V rows next to them, so both copies are
+// in flight together), then [128][4] scores, the softmax statistics and q as fp32 [4][D].
+template <int D>
+__host__ __device__ constexpr bool ring_kv_together() {
+  return D == 128;
+}
 template <int D>
 __host__ __device__ constexpr size_t ring_smem_bytes() {
-  return 128 + 2 * kPage * D + kPage * kMaxG * 4 + 64;
+  return 128 + (ring_kv_together<D>() ? 2 : 1) * 2 * kPage * D + kPage * kMaxG * 4 + 64 + kMaxG * D * 4;
 }
 
 __device__ __forceinline__ void write_empty_partial(float* part, int D, int tid, int nt) {
   for (int i = tid; i < 2 * kMaxG + kMaxG * D; i += nt) part[i] = i < kMaxG ? -INFINITY : 0.f;
 }
 
-// Exact attention over the unflushed ring tokens [F, R) of one (row, KV head): K rows, then V rows,
-// are bulk-copied into shared memory; scores are warp-per-token with lane-split coordinates.
+// Exact attention over the unflushed ring tokens [F, R) of one (row, KV head). K and V rows are
+// bulk-copied into shared memory (together for head_dim 128). Scores are thread-per-token: thread t
+// walks its K row in 16-byte chunks starting at chunk t, so the 8 lanes of each quarter-warp read
+// 8 different bank groups. P.V is thread-per-coordinate.
 template <int D, int NT>
 __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
-  constexpr int NE = D / 32;
-  constexpr int NW = NT / 32;
+  constexpr int NC = D / 8;  // 16-byte chunks per row
+  constexpr bool KV = ring_kv_together<D>();
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L, Np, P;
@@ -244,49 +298,58 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     return;
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
-  const uint16_t* rows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16: K, then V
-  float* sc = reinterpret_cast<float*>(smem_raw + 128 + 2 * kPage * D);       // [128][4] scores, then p
-  float* red = sc + kPage * kMaxG;                                           // [4][2]
+  const uint16_t* krows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16
+  const uint16_t* vrows = KV ? krows + (size_t)kPage * D : krows;             // [n][D] bf16
+  float* sc = reinterpret_cast<float*>(smem_raw + 128 + (KV ? 2 : 1) * 2 * kPage * D);  // [128][4]
+  float* red = sc + kPage * kMaxG;                                                       // [4][2]
+  float* qs = red + 16;                                                                  // [4][D]
   const uint16_t* rk = lv.ring + (((size_t)slot * lv.Hkv + h) * 2) * kPage * D + (size_t)F * D;
   const uint16_t* rv = rk + (size_t)kPage * D;
   const uint32_t bytes = (uint32_t)n * D * 2;
   if (tid == 0) {
     mbar_init(bar, 1);
+    if (KV) mbar_init(bar + 1, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(bar, bytes);
     bulk_g2s(smem_raw + 128, rk, bytes, bar);
+    if (KV) {
+      mbar_expect_tx(bar + 1, bytes);
+      bulk_g2s(smem_raw + 128 + 2 * kPage * D, rv, bytes, bar + 1);
+    }
   }
   const int G = lv.G;
-  float qv[kMaxG][NE];
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g)
-#pragma unroll
-    for (int e = 0; e < NE; ++e)
-      qv[g][e] = g < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + g) * D + (e >> 2) * 128 + 4 * lane + (e & 3)])
-                       : 0.f;
+  for (int i = tid; i < kMaxG * D; i += NT) {
+    const int g = i / D;
+    qs[i] = g < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + g) * D + (i % D)]) : 0.f;
+  }
   __syncthreads();
   bool ok = mbar_wait(bar, 0);
   const float s2 = a.scale * kLog2e;
   if (ok) {
-    for (int t = warp; t < n; t += NW) {
+    for (int t = tid; t < n; t += NT) {
       float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+      const uint16_t* row = krows + (size_t)t * D;
+#pragma unroll 4
+      for (int i = 0; i < NC; ++i) {
+        const int ci = (i + t) & (NC - 1);
+        const uint4 u = *reinterpret_cast<const uint4*>(row + 8 * ci);
+        const float k[8] = {__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                            __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u),
+                            __uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u),
+                            __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u)};
 #pragma unroll
-      for (int hf = 0; hf < NE / 4; ++hf) {
-        const uint2 u = *reinterpret_cast<const uint2*>(rows + (size_t)t * D + 128 * hf + 4 * lane);
-        const float k0 = __uint_as_float(u.x << 16), k1 = __uint_as_float(u.x & 0xffff0000u);
-        const float k2 = __uint_as_float(u.y << 16), k3 = __uint_as_float(u.y & 0xffff0000u);
-#pragma unroll
-        for (int g = 0; g < kMaxG; ++g)
-          acc[g] = fmaf(qv[g][4 * hf], k0, fmaf(qv[g][4 * hf + 1], k1,
-                   fmaf(qv[g][4 * hf + 2], k2, fmaf(qv[g][4 * hf + 3], k3, acc[g]))));
+        for (int g = 0; g < kMaxG; ++g) {
+          const float4 q0 = *reinterpret_cast<const float4*>(qs + g * D + 8 * ci);
+          const float4 q1 = *reinterpret_cast<const float4*>(qs + g * D + 8 * ci + 4);
+          acc[g] = fmaf(q0.x, k[0], fmaf(q0.y, k[1], fmaf(q0.z, k[2], fmaf(q0.w, k[3], acc[g]))));
+          acc[g] = fmaf(q1.x, k[4], fmaf(q1.y, k[5], fmaf(q1.z, k[6], fmaf(q1.w, k[7], acc[g]))));
+        }
       }
-#pragma unroll
-      for (int g = 0; g < kMaxG; ++g) acc[g] = warp_sum(acc[g]);
-      if (lane < kMaxG) sc[t * kMaxG + lane] = acc[lane] * s2;
+      *reinterpret_cast<float4*>(sc + t * kMaxG) = make_float4(acc[0] * s2, acc[1] * s2, acc[2] * s2, acc[3] * s2);
     }
   }
   __syncthreads();  // every K row has been read
-  if (tid == 0 && ok) {
+  if (!KV && tid == 0 && ok) {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     mbar_expect_tx(bar, bytes);
     bulk_g2s(smem_raw + 128, rv, bytes, bar);
@@ -308,25 +371,37 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     }
   }
   __syncthreads();
-  ok = ok && mbar_wait(bar, 1);
+  ok = ok && mbar_wait(KV ? bar + 1 : bar, KV ? 0 : 1);
   if (!ok) {
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
     write_empty_partial(part, D, tid, NT);
     return;
   }
   for (int j = tid; j < D; j += NT) {
-    float o[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+    float o[2][kMaxG] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    int t = 0;
 #pragma unroll 4
-    for (int t = 0; t < n; ++t) {
+    for (; t + 1 < n; t += 2) {  // two independent accumulator sets
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float4 p = *reinterpret_cast<const float4*>(sc + (t + u) * kMaxG);
+        const float vv = bf16_to_f32(vrows[(size_t)(t + u) * D + j]);
+        o[u][0] = fmaf(p.x, vv, o[u][0]);
+        o[u][1] = fmaf(p.y, vv, o[u][1]);
+        o[u][2] = fmaf(p.z, vv, o[u][2]);
+        o[u][3] = fmaf(p.w, vv, o[u][3]);
+      }
+    }
+    if (t < n) {
       const float4 p = *reinterpret_cast<const float4*>(sc + t * kMaxG);
-      const float vv = bf16_to_f32(rows[(size_t)t * D + j]);
-      o[0] = fmaf(p.x, vv, o[0]);
-      o[1] = fmaf(p.y, vv, o[1]);
-      o[2] = fmaf(p.z, vv, o[2]);
-      o[3] = fmaf(p.w, vv, o[3]);
+      const float vv = bf16_to_f32(vrows[(size_t)t * D + j]);
+      o[0][0] = fmaf(p.x, vv, o[0][0]);
+      o[0][1] = fmaf(p.y, vv, o[0][1]);
+      o[0][2] = fmaf(p.z, vv, o[0][2]);
+      o[0][3] = fmaf(p.w, vv, o[0][3]);
     }
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) part[2 * kMaxG + g * D + j] = o[g];
+    for (int g = 0; g < kMaxG; ++g) part[2 * kMaxG + g * D + j] = o[0][g] + o[1][g];
   }
   if (tid < kMaxG) {
     part[tid] = red[2 * tid];
@@ -348,12 +423,16 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   const size_t stride = a.plan.part_stride / sizeof(float);
   const float* base = reinterpret_cast<const float*>(a.ws + a.plan.part_off +
                                                      ((size_t)b * lv.Hkv + h) * (nsp + 1) * a.plan.part_stride);
-  float* red = sm;            // [NW][4]
-  float* fs = sm + 4 * NW;    // [nsp][4] split weights
-  // 1. max over splits, per head (block-wide)
+  float* red = sm;                      // [NW][4]
+  float* fs = sm + 4 * NW;              // [nsp][4] split maxima, then split weights
+  float* ls = fs + 4 * (nsp + 1);       // [nsp][4] split sums
+  // 1. one pass over the splits' (m, l): kept in shared memory; block-wide max per head
   float mloc[kMaxG] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   for (int s = tid; s < nsp; s += NT) {
     const float4 m4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride));
+    const float4 l4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride + kMaxG));
+    *reinterpret_cast<float4*>(fs + 4 * s) = m4;
+    *reinterpret_cast<float4*>(ls + 4 * s) = l4;
     mloc[0] = fmaxf(mloc[0], m4.x);
     mloc[1] = fmaxf(mloc[1], m4.y);
     mloc[2] = fmaxf(mloc[2], m4.z);
@@ -372,17 +451,15 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
     M[g] = m;
   }
   __syncthreads();
-  // 2. per-split weights and the weighted sum of l
+  // 2. per-split weights (in place of the maxima) and the weighted sum of l
   float lloc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
   for (int s = tid; s < nsp; s += NT) {
-    const float4 m4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride));
-    const float4 l4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride + kMaxG));
-    const float mv[4] = {m4.x, m4.y, m4.z, m4.w}, lv4[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
     for (int g = 0; g < kMaxG; ++g) {
-      const float f = mv[g] == -INFINITY ? 0.f : exp2f(mv[g] - M[g]);
-      fs[s * 4 + g] = f;
-      lloc[g] = fmaf(f, lv4[g], lloc[g]);
+      const float mv = fs[4 * s + g];
+      const float f = mv == -INFINITY ? 0.f : exp2f(mv - M[g]);
+      fs[4 * s + g] = f;
+      lloc[g] = fmaf(f, ls[4 * s + g], lloc[g]);
     }
   }
 #pragma unroll
@@ -394,23 +471,45 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float l = 0.f;
 #pragma unroll
   for (int w = 0; w < NW; ++w) l += red[w * 4 + hd];
-  // 3. weighted sum of the split outputs (independent loads, 8 splits in flight)
-  float o[NE];
+  // 3. weighted sum of the split outputs: 16 splits' loads in flight, two accumulator sets
+  float o[NE], o2[NE];
 #pragma unroll
-  for (int e = 0; e < NE; ++e) o[e] = 0.f;
+  for (int e = 0; e < NE; ++e) o[e] = o2[e] = 0.f;
   const float* ob = base + 2 * kMaxG + hd * D + 4 * lane;
-#pragma unroll 8
-  for (int s = 0; s < nsp; ++s) {  // empty splits hold weight 0 and O = 0
-    const float f = fs[s * 4 + hd];
+  int s0 = 0;
+  for (; s0 + 16 <= nsp; s0 += 16) {  // empty splits hold weight 0 and O = 0
+    float4 v[16][NE / 4];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+#pragma unroll
+      for (int hf = 0; hf < NE / 4; ++hf)
+        v[u][hf] = __ldcg(reinterpret_cast<const float4*>(ob + (s0 + u) * stride + 128 * hf));
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const float f = fs[(s0 + u) * 4 + hd];
+      float* acc = (u & 1) ? o2 : o;
+#pragma unroll
+      for (int hf = 0; hf < NE / 4; ++hf) {
+        acc[4 * hf + 0] = fmaf(f, v[u][hf].x, acc[4 * hf + 0]);
+        acc[4 * hf + 1] = fmaf(f, v[u][hf].y, acc[4 * hf + 1]);
+        acc[4 * hf + 2] = fmaf(f, v[u][hf].z, acc[4 * hf + 2]);
+        acc[4 * hf + 3] = fmaf(f, v[u][hf].w, acc[4 * hf + 3]);
+      }
+    }
+  }
+  for (; s0 < nsp; ++s0) {
+    const float f = fs[s0 * 4 + hd];
 #pragma unroll
     for (int hf = 0; hf < NE / 4; ++hf) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(ob + s * stride + 128 * hf));
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(ob + s0 * stride + 128 * hf));
       o[4 * hf + 0] = fmaf(f, v.x, o[4 * hf + 0]);
       o[4 * hf + 1] = fmaf(f, v.y, o[4 * hf + 1]);
       o[4 * hf + 2] = fmaf(f, v.z, o[4 * hf + 2]);
       o[4 * hf + 3] = fmaf(f, v.w, o[4 * hf + 3]);
     }
   }
+#pragma unroll
+  for (int e = 0; e < NE; ++e) o[e] += o2[e];
   // 4. Pi^T o = D * (H o) / sqrt(d), then the exact merge with the ring split
   warp_fwht<NE>(o, lane);
   const float rs = rsqrtf((float)D);
@@ -517,27 +616,17 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       bulk_g2s(stage0 + (size_t)s * PB, gpages + (size_t)(pg0 + s) * PB, PB, &full[s]);
     }
   }
-  pdl_wait();  // the query-prep operands (and the arrival counters) of this call are ready
-  const uint8_t* prep = a.ws + a.plan.prep_off + ((size_t)b * lv.Hkv + h) * a.plan.prep_stride;
+  SFrag<D> sfrag;
+  sfrag_prefetch<D>(lv, sfrag);
+  pdl_wait();  // earlier work on the stream (q, and the partials of any decode that shares ws) is done
   uint2 bq[3][8];
-#pragma unroll
-  for (int pi = 0; pi < 3; ++pi)
-#pragma unroll
-    for (int s = 0; s < 8; ++s) bq[pi][s] = reinterpret_cast<const uint2*>(prep)[((pi * HALVES + hf) * 8 + s) * 32 + lane];
-  const int g = lane >> 2, c = lane & 3;
-  const float* cst = reinterpret_cast<const float*>(prep + (size_t)3 * HALVES * 8 * 32 * 8);
-  const int G = lv.G;
   float um[2], cm[2], uq[2], cq[2];
+  query_prep<D, NT>(a, b, h, reinterpret_cast<float*>(xbuf + decode_xbuf_floats<D>()), sfrag, bq, um, cm, uq, cq);
+  const int g = lane >> 2, c = lane & 3;
+  const int G = lv.G;
   bool colok[2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int hd = min(2 * c + i, kMaxG - 1);
-    um[i] = cst[4 * hd + 0];
-    cm[i] = cst[4 * hd + 1];
-    uq[i] = cst[4 * hd + 2];
-    cq[i] = cst[4 * hd + 3];
-    colok[i] = 2 * c + i < G;
-  }
+  for (int i = 0; i < 2; ++i) colok[i] = 2 * c + i < G;
   float O[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
@@ -779,11 +868,11 @@ size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB);
   constexpr int NT = decode_threads<D>();
   const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * D);
-  const size_t xbuf_bytes = D == 256 ? sizeof(float) * NT * 2 * 8 : 0;
-  size_t smem = 128 + (size_t)decode_stages<D, VB>() * pl.bytes + xbuf_bytes;
+  const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
+  size_t smem = 128 + (size_t)decode_stages<D, VB>() * pl.bytes + xbuf_bytes + prep_scratch_bytes<D>();
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_smem_bytes<D>());
-  smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 4 * 1025));  // combine: split weights
+  smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 8 * 1026));  // combine: split (m, l)
   return smem;
 }
 
@@ -795,9 +884,7 @@ int decode_setup() {
     constexpr int STAGES = decode_stages<D, VB>();
     const size_t smem = decode_smem_bytes<D, VB>();
     if (cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess ||
-        cudaFuncSetAttribute(k_prep<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem_bytes<D>()) !=
-            cudaSuccess)
+        cudaSuccess)
       return -1;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES>, decode_threads<D>(), smem) !=
@@ -814,8 +901,8 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
   constexpr int STAGES = decode_stages<D, VB>();
   if (decode_setup<D, VB>() < 0) return cudaErrorInvalidValue;
   const size_t smem = decode_smem_bytes<D, VB>();
-  if (phase < 0 || phase == 0) {
-    cudaError_t e = launch_pdl(k_prep<D>, dim3(batch, a.lv.Hkv), dim3(kPrepThreads), prep_smem_bytes<D>(), s, a);
+  if (phase == 0) {  // zero the arrival counters (every decode call leaves them at zero)
+    cudaError_t e = cudaMemsetAsync(a.ws + a.plan.cnt_off, 0, sizeof(int32_t) * (size_t)batch * a.lv.Hkv, s);
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
@@ -865,8 +952,8 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
 //     (which can synchronise the device) is not allowed;
 //   - an embedding runtime that owns all device memory and exposes no allocator;
 //   - a plugin ABI that passes in only the tensors of the operation itself.
-// For them this variant takes only inputs and outputs. Its scratch (query-prep operands and split
-// partials) lives in the file-scope device array below, so it has a fixed maximum size.
+// For them this variant takes only inputs and outputs. Its scratch (split partials and arrival
+// counters) lives in the file-scope device array below, so it has a fixed maximum size.
 // =============================================================================================
 namespace tq {
 namespace {

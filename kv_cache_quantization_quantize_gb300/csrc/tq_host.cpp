@@ -34,6 +34,36 @@ tq_status cuda_fail(cudaError_t e, const char* what) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+float bf16_to_float(uint16_t b) {
+  const uint32_t x = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &x, 4);
+  return f;
+}
+
+// bf16 bits -> f16 bits, round to nearest even (overflow to inf; values below 2^-14 become subnormal).
+uint16_t bf16_to_f16_rne(uint16_t b) {
+  const uint32_t x = (uint32_t)b << 16;
+  const uint16_t sign = (uint16_t)((x >> 16) & 0x8000u);
+  const uint32_t ax = x & 0x7fffffffu;
+  if (ax >= 0x7f800000u) return sign | (ax > 0x7f800000u ? 0x7e00u : 0x7c00u);
+  if (ax >= 0x477ff000u) return sign | 0x7c00u;  // >= 65520 rounds to inf
+  if (ax <= 0x33000000u) return sign;            // <= 2^-25 rounds to zero (ties to even)
+  const int e = (int)(ax >> 23) - 127;
+  const uint32_t mant = (ax & 0x7fffffu) | 0x800000u;
+  if (e >= -14) {
+    uint32_t h = ((uint32_t)(e + 15) << 10) | ((mant >> 13) & 0x3ffu);
+    const uint32_t rem = mant & 0x1fffu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) ++h;  // a carry moves into the exponent
+    return sign | (uint16_t)h;
+  }
+  const int sh = -(e + 1);  // units of 2^-24: mant * 2^(e + 1)
+  uint32_t m = mant >> sh;
+  const uint32_t rem = mant & ((1u << sh) - 1u), half = 1u << (sh - 1);
+  if (rem > half || (rem == half && (m & 1u))) ++m;
+  return sign | (uint16_t)m;
+}
+
 tq_status validate(const tq_config* c) {
   if (!c) return fail(TQ_ERR_INVALID_ARG, "cfg is NULL");
   if (c->head_dim != 128 && c->head_dim != 256)
@@ -190,7 +220,8 @@ TableOffsets table_offsets(int d) {
   o.St = align_up(o.S + 2ull * d * d, 256);
   o.cb = align_up(o.St + 2ull * d * d, 256);
   o.S_sw = align_up(o.cb + sizeof(float) * kCbFloats, 1024);
-  o.bytes = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 256);
+  o.S_frag = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 256);
+  o.bytes = align_up(o.S_frag + 2ull * d * d, 256);
   return o;
 }
 
@@ -212,6 +243,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   v.St = reinterpret_cast<const uint16_t*>(tb + ctx->to.St);
   v.cb = reinterpret_cast<const float*>(tb + ctx->to.cb);
   v.S_sw = reinterpret_cast<const uint16_t*>(tb + ctx->to.S_sw);
+  v.S_frag = reinterpret_cast<const uint4*>(tb + ctx->to.S_frag);
   uint8_t* cb = static_cast<uint8_t*>(ctx->d_cache);
   const size_t units_per_layer = (size_t)c.max_seqs * c.n_kv_heads;
   v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
@@ -238,12 +270,12 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   p.pages_per_split = (max_pages + splits - 1) / splits;
   p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
   const int d = c.head_dim;
-  p.prep_off = 0;
-  p.prep_stride = align_up((size_t)3 * (d / 32) * 32 * 16 + 4 * 4 * sizeof(float), 256);
-  p.part_off = align_up(p.prep_off + p.prep_stride * units, 256);
+  // The arrival counters sit at a fixed place (offset 0, sized for max_seqs rows), so that calls with
+  // other batch sizes or hints on the same workspace find them where the last call left them (zero).
+  p.cnt_off = 0;
+  p.part_off = align_up(sizeof(int32_t) * (size_t)c.max_seqs * c.n_kv_heads, 256);
   p.part_stride = align_up((size_t)(2 * kMaxG + kMaxG * d) * sizeof(float), 16);
-  p.cnt_off = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
-  p.bytes = align_up(p.cnt_off + sizeof(int32_t) * (size_t)units, 256);
+  p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
   return p;
 }
 
@@ -338,11 +370,34 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
   for (int i = 0; i < 3; ++i) cb[4 + i] = (float)ctx->bnd[i];
   cb[8] = (float)(0.5 * (ctx->cent[2] + ctx->cent[3]));
   cb[9] = (float)(0.5 * (ctx->cent[3] - ctx->cent[2]));
+  {  // cb[10]: max_i sum_j |S_ij| (rounded up), a bound on |(S x)_i| / max|x|
+    double m = 0.0;
+    for (int i = 0; i < d; ++i) {
+      double r = 0.0;
+      for (int j = 0; j < d; ++j) r += std::fabs((double)bf16_to_float(ctx->S[(size_t)i * d + j]));
+      m = std::max(m, r);
+    }
+    cb[10] = (float)(m * (1.0 + 1e-6));
+  }
   std::memcpy(host.data() + ctx->to.cb, cb, sizeof(cb));
   if (d == 128) {
     uint8_t* sw = host.data() + ctx->to.S_sw;
     for (int n = 0; n < d; ++n)
       for (int k = 0; k < d; ++k) std::memcpy(sw + tq::sw128_offset(n, k), &ctx->S[(size_t)n * d + k], 2);
+  }
+  {  // S as f16 m16n8k16 A fragments (bf16 -> f16 is exact except below 2^-14, rounded to nearest even)
+    uint16_t* fr = reinterpret_cast<uint16_t*>(host.data() + ctx->to.S_frag);
+    for (int mt = 0; mt < d / 16; ++mt)
+      for (int ks = 0; ks < d / 16; ++ks)
+        for (int lane = 0; lane < 32; ++lane) {
+          const int g = lane >> 2, c = lane & 3;
+          uint16_t* w = fr + (size_t)tq::sfrag_idx(d, mt, ks, lane) * 8;
+          for (int r = 0; r < 4; ++r)
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const int row = 16 * mt + g + 8 * (r & 1), col = 16 * ks + 2 * c + 8 * (r >> 1) + e2;
+              w[2 * r + e2] = bf16_to_f16_rne(ctx->S[(size_t)row * d + col]);
+            }
+        }
   }
   e = cudaMemcpyAsync(d_tables, host.data(), need, cudaMemcpyHostToDevice, (cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);

@@ -103,13 +103,19 @@ TQ_HD uint32_t sw128_offset(int n, int k) {
 }
 
 // Device tables (inside the caller's d_tables buffer). S_sw is S (rows = projection index,
-// columns = coordinate) in the swizzled layout above; present for head_dim 128.
+// columns = coordinate) in the swizzled layout above; present for head_dim 128. S_frag is S in f16
+// as m16n8k16 A fragments (see sfrag_idx), for the decode kernels' query projection.
 struct TableOffsets {
-  size_t D, S, St, cb, S_sw, bytes;
+  size_t D, S, St, cb, S_sw, S_frag, bytes;
 };
+
+// S_frag: [m-tile d/16][k-step d/16][lane 32] of {a0, a1, a2, a3} (four f16 pairs). Lane (g, c) of
+// m-tile mt, k-step ks holds S[16mt + g (+8 for a1, a3)][16ks + 2c (+8 for a2, a3) + {0, 1}].
+TQ_HD int sfrag_idx(int d, int mt, int ks, int lane) { return (mt * (d / 16) + ks) * 32 + lane; }
 TableOffsets table_offsets(int d);
 
-// Codebook block: cb[0..3] centroids, cb[4..6] boundaries, cb[8] alpha=(c2+c3)/2, cb[9] beta=(c3-c2)/2.
+// Codebook block: cb[0..3] centroids, cb[4..6] boundaries, cb[8] alpha=(c2+c3)/2, cb[9] beta=(c3-c2)/2,
+// cb[10] = max_i sum_j |S_ij| (rounded up).
 constexpr int kCbFloats = 16;
 
 }  // namespace tq
@@ -143,6 +149,7 @@ struct LayerView {
   const uint16_t* St;  // bf16 [d][d] transposed
   const float* cb;
   const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128)
+  const uint4* S_frag;   // S in f16 m16n8k16 A fragments (sfrag_idx)
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
   uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
   int32_t* state;      // this layer: [slot][2] = {L, F}
@@ -155,9 +162,9 @@ LayerView layer_view(const tq_ctx* ctx, int layer);
 struct DecodePlan {
   int n_splits;        // history splits per (row, kv head); the ring is one extra split
   int pages_per_split;
-  size_t prep_off, prep_stride;  // per (row, kv head) query-prep block
   size_t part_off, part_stride;  // per (row, kv head, split) partial
-  size_t cnt_off;                // per (row, kv head) int32 arrival counter (zeroed by the prep phase)
+  size_t cnt_off;                // per (row, kv head) int32 arrival counters at offset 0, room for
+                                 // max_seqs rows (left at zero by every call)
   size_t bytes;
 };
 DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint);

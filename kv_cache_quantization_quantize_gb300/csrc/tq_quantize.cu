@@ -586,10 +586,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_quantize_bulk128(AppendArgs a
 }
 
 // Ring update after the quantise launch: write the new ring tail and the sequence state.
+// Dependents (the decode of this layer) are released only after the state is written: they read the
+// sequence state before their own griddepcontrol.wait to start fetching pages early.
 __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
   const int b = blockIdx.x;
   pdl_wait();  // the quantise launch has read the old ring and state
-  pdl_launch();
   const LayerView& lv = a.lv;
   const int slot = a.seq_ids[b];
   if (slot < 0 || slot >= lv.max_seqs) return;
@@ -597,7 +598,12 @@ __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
   const int Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
   if (a.flush) {
     __syncthreads();
-    if (threadIdx.x == 0) lv.state[2 * slot + 1] = L - Np;
+    if (threadIdx.x == 0) {
+      lv.state[2 * slot + 1] = L - Np;
+      __threadfence();
+    }
+    __syncthreads();
+    pdl_launch();
     return;
   }
   const int nn = a.n_new[b];
@@ -631,7 +637,10 @@ __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
   if (threadIdx.x == 0) {
     lv.state[2 * slot] = L2;
     lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
+    __threadfence();
   }
+  __syncthreads();
+  pdl_launch();
 }
 
 __global__ void k_reset(int32_t* state_base, int n_layers, int max_seqs, int layer, const int32_t* seq_ids,

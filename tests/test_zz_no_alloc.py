@@ -65,16 +65,17 @@ def test_noalloc_matches_workspace_decode_on_two_calls():
 
 
 def test_noalloc_rejects_scratch_above_its_limit():
-    # batch 32 x 8 KV heads at head_dim 256 needs more than the built-in 4 MiB of decode scratch
-    d, Hkv, G, B = 256, 8, 4, 32
-    cfg = config(head_dim=d, value_bits=2, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B, max_ctx=256,
+    # batch 64 x 8 KV heads at head_dim 256 needs more than the built-in 4 MiB of scratch: every plan has at
+    # least 3 partials of 4128 bytes per (row, KV head)
+    d, Hkv, G, B, L = 256, 8, 4, 64, 256
+    cfg = config(head_dim=d, value_bits=2, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B, max_ctx=L,
                  seed=2)
     cache = TurboQuantCache(cfg)
-    assert cache.workspace_bytes(B, 256) > (4 << 20)
+    assert cache.workspace_bytes(B, L) > (4 << 20)
     ids = torch.arange(B, dtype=torch.int32, device=DEV)
     q = torch.zeros(B, Hkv * G, d, dtype=torch.bfloat16, device=DEV)
     out = torch.full((B, Hkv * G, d), 7.0, dtype=torch.float32, device=DEV)
-    st = _noalloc(cache, 0, q, out, ids, hint=256)
+    st = _noalloc(cache, 0, q, out, ids, hint=L)
     assert st == _abi.TQ_ERR_CAPACITY
     msg = _abi.load().tq_last_error().decode()
     assert "exceeds" in msg and str(4 << 20) in msg
