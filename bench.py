@@ -231,7 +231,7 @@ def run_ours(args):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         step()
-    launches_per_step = L_layers * 4  # quantize + ring update + prep + split-K (combine inside) per layer
+    launches_per_step = L_layers * 2  # small append + split-K decode (query prep and combine inside) per layer
 
     gpu_id = local
     try:

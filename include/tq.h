@@ -116,7 +116,9 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
  *   - f32 inputs enter the ring rounded to bf16. Blocks that never pass through the ring are
  *     quantised from the f32 values.
  *   - A row that would exceed max_ctx is skipped and sets TQ_DEV_ERR_CAPACITY.
- *   - Launches: one quantize kernel over the pages to write, then one ring-update kernel. */
+ *   - Launches: for max_new < 128, one kernel (the page that an overflow completes, the ring rows and
+ *     the new length); otherwise one quantize kernel over the pages to write, then one ring-update
+ *     kernel. */
 tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
                              const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
                              tq_stream_t stream);

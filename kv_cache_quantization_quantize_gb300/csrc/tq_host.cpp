@@ -205,7 +205,8 @@ void compute_offsets(tq_ctx* ctx) {
   ctx->pages_off = 0;
   ctx->ring_off = align_up(units * ctx->max_pages * ctx->pl.bytes, 256);
   ctx->state_off = align_up(ctx->ring_off + units * ring_elems(c) * 2, 256);
-  ctx->status_off = align_up(ctx->state_off + (size_t)c.n_layers * c.max_seqs * 8, 256);
+  ctx->acnt_off = align_up(ctx->state_off + (size_t)c.n_layers * c.max_seqs * 8, 256);
+  ctx->status_off = align_up(ctx->acnt_off + (size_t)c.n_layers * c.max_seqs * 4, 256);
   ctx->total_bytes = ctx->status_off + 256;
 }
 
@@ -249,6 +250,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
   v.ring = reinterpret_cast<uint16_t*>(cb + ctx->ring_off) + (size_t)layer * units_per_layer * ring_elems(c);
   v.state = reinterpret_cast<int32_t*>(cb + ctx->state_off) + (size_t)layer * c.max_seqs * 2;
+  v.acnt = reinterpret_cast<int32_t*>(cb + ctx->acnt_off) + (size_t)layer * c.max_seqs;
   v.status = reinterpret_cast<uint32_t*>(cb + ctx->status_off);
   return v;
 }

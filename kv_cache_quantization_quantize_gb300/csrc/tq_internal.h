@@ -131,7 +131,7 @@ struct tq_ctx {
   void* d_tables = nullptr;
   void* d_cache = nullptr;
   size_t cache_bytes = 0;
-  size_t pages_off = 0, ring_off = 0, state_off = 0, status_off = 0, total_bytes = 0;
+  size_t pages_off = 0, ring_off = 0, state_off = 0, acnt_off = 0, status_off = 0, total_bytes = 0;
   std::vector<float> D;
   std::vector<uint16_t> S;  // bf16 bits, row-major
   double cent[4] = {0, 0, 0, 0};
@@ -153,6 +153,7 @@ struct LayerView {
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
   uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
   int32_t* state;      // this layer: [slot][2] = {L, F}
+  int32_t* acnt;       // this layer: [slot] arrival counters of the small-append kernel (left at zero)
   uint32_t* status;
 };
 

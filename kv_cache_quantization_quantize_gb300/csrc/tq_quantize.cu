@@ -83,23 +83,18 @@ __device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int
   return true;
 }
 
+// Quantises page pg of (row b, KV head h): its first `valid` tokens come from the ring (positions
+// below L) and then from the new input. Run by all kQThreads threads of the CTA.
 template <int D>
-__global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
+__device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
+                                                  int valid, uint8_t* smem) {
   constexpr int NE = D / 32;  // coordinates per lane
-  extern __shared__ __align__(16) uint8_t smem[];
   uint32_t* st2 = reinterpret_cast<uint32_t*>(smem);                    // S^T as bf16 pairs [D][D/2]
   uint8_t* kcode = smem + 2 * D * D;                                    // [128][D]: idx | sign << 2
   uint8_t* vcode = kcode + kPage * D;                                   // [128][D]
   uint32_t* norms = reinterpret_cast<uint32_t*>(vcode + kPage * D);     // [128] n16 | gamma16 << 16
   uint16_t* scales = reinterpret_cast<uint16_t*>(norms + kPage);        // [128][D/32]
   float* rbuf = reinterpret_cast<float*>(scales + kPage * (D / 32));    // [8 warps][D]
-
-  const int b = blockIdx.x, h = blockIdx.y;
-  pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
-  pdl_launch();
-  int slot, L, Np, pg, valid;
-  if (!page_task(a, b, blockIdx.z, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
-
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LayerView& lv = a.lv;
   // stage S^T (bf16) in shared memory
@@ -291,6 +286,76 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   }
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
   for (int i = tid; i < kPage * (D / 32); i += kQThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
+}
+
+template <int D>
+__global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int b = blockIdx.x, h = blockIdx.y;
+  pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
+  pdl_launch();
+  int slot, L, Np, pg, valid;
+  if (!page_task(a, b, blockIdx.z, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
+  quantize_page_cta<D>(a, b, h, slot, L, Np, pg, valid, smem);
+}
+
+// Appends of fewer than 128 tokens per row in one launch: CTA (row b, KV head h) packs the page that
+// completes when the ring overflows (at most one), then writes head h's new ring rows. The last CTA
+// of the row to arrive publishes the new length. Dependents (the decode) are released only after
+// that, so they may read the state before their own stream wait.
+template <int D>
+__global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
+  const LayerView& lv = a.lv;
+  const int slot = a.seq_ids[b];
+  if (slot < 0 || slot >= lv.max_seqs) {
+    if (h == 0 && tid == 0) set_status(lv.status, TQ_DEV_ERR_SEQ_ID);
+    return;
+  }
+  const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
+  const int Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+  const int nn = a.n_new[b];
+  const int L2 = L + nn;
+  if (nn < 0 || nn > a.max_new || L2 > lv.max_ctx) {
+    if (h == 0 && tid == 0) set_status(lv.status, TQ_DEV_ERR_CAPACITY);
+    return;
+  }
+  const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
+  if (Np2 > Np) quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, smem);  // Np2 - Np == 128
+  __syncthreads();  // the page read the old ring rows of head h
+  const int p0 = max(L, Np2);
+  const int d = lv.d, q4 = d / 4;
+  const int n_items = (L2 - p0) * 2 * q4;  // (pos, which, quad) of head h
+  for (int it = tid; it < n_items; it += blockDim.x) {
+    const int quad = it % q4, which = (it / q4) & 1, pos = p0 + it / (2 * q4);
+    const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + h) * d + 4 * quad;
+    uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + h) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
+    const void* base = which ? a.v : a.k;
+    uint2 out;
+    if (a.dt == 0) {
+      out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
+    } else {
+      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
+      out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
+      out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
+    }
+    *reinterpret_cast<uint2*>(dst) = out;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const int old = atomicAdd(lv.acnt + slot, 1);
+    if (old == lv.Hkv - 1) {  // every head of the row is done with the old state
+      lv.acnt[slot] = 0;
+      lv.state[2 * slot] = L2;
+      lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
+      __threadfence();
+    }
+  }
+  __syncthreads();
+  pdl_launch();
 }
 
 // =============================================================================================
@@ -674,6 +739,17 @@ cudaError_t launch_quantize_d(const AppendArgs& a, int batch, int pages, cudaStr
   return launch_pdl(k_quantize_pages<D>, grid, dim3(kQThreads), smem, s, a);
 }
 
+template <int D>
+cudaError_t launch_append_small_d(const AppendArgs& a, int batch, size_t smem, cudaStream_t s) {
+  static bool attr_set = false;  // set once, outside any stream capture that follows
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(k_append_small<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  return launch_pdl(k_append_small<D>, dim3(batch, a.lv.Hkv), dim3(kQThreads), smem, s, a);
+}
+
 cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
   if (a.lv.d == 128) return launch_quantize_d<128>(a, batch, pages, s);
   return launch_quantize_d<256>(a, batch, pages, s);
@@ -705,6 +781,10 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.n_new = n_new;
   a.max_new = max_new;
   a.flush = 0;
+  if (max_new < kPage) {  // decode-sized appends: one launch (page on ring overflow + ring rows + state)
+    const size_t smem = a.lv.d == 128 ? quantize_smem_bytes<128>() : quantize_smem_bytes<256>();
+    return a.lv.d == 128 ? launch_append_small_d<128>(a, batch, smem, s) : launch_append_small_d<256>(a, batch, smem, s);
+  }
   const int pages = (max_new + kPage - 1) / kPage;
   cudaError_t e = (a.lv.d == 128 && max_new >= kPage)
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
