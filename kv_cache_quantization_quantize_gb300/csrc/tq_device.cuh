@@ -63,6 +63,11 @@ __device__ __forceinline__ void warp_fwht(float (&x)[NE], int lane) {
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
+// Barrier `id` (1..15) over the first `threads` threads that reach it (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ---- mbarrier / bulk copy (async proxy) ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 

@@ -221,7 +221,8 @@ TableOffsets table_offsets(int d) {
   o.St = align_up(o.S + 2ull * d * d, 256);
   o.cb = align_up(o.St + 2ull * d * d, 256);
   o.S_sw = align_up(o.cb + sizeof(float) * kCbFloats, 1024);
-  o.S_frag = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 256);
+  o.HD_sw = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 1024);
+  o.S_frag = align_up(o.HD_sw + (d == 128 ? 2ull * d * d : 0), 256);
   o.bytes = align_up(o.S_frag + 2ull * d * d, 256);
   return o;
 }
@@ -245,6 +246,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   v.cb = reinterpret_cast<const float*>(tb + ctx->to.cb);
   v.S_sw = reinterpret_cast<const uint16_t*>(tb + ctx->to.S_sw);
   v.S_frag = reinterpret_cast<const uint4*>(tb + ctx->to.S_frag);
+  v.HD_sw = reinterpret_cast<const uint16_t*>(tb + ctx->to.HD_sw);
   uint8_t* cb = static_cast<uint8_t*>(ctx->d_cache);
   const size_t units_per_layer = (size_t)c.max_seqs * c.n_kv_heads;
   v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
@@ -386,6 +388,14 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
     uint8_t* sw = host.data() + ctx->to.S_sw;
     for (int n = 0; n < d; ++n)
       for (int k = 0; k < d; ++k) std::memcpy(sw + tq::sw128_offset(n, k), &ctx->S[(size_t)n * d + k], 2);
+    // (H diag(D))[i][j] = (-1)^popcount(i & j) * D[j], exact in bf16 (+-1)
+    uint8_t* hd = host.data() + ctx->to.HD_sw;
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < d; ++j) {
+        const bool neg = (__builtin_popcount((unsigned)(i & j)) & 1) != (ctx->D[j] < 0.f);
+        const uint16_t v = neg ? 0xBF80u : 0x3F80u;
+        std::memcpy(hd + tq::sw128_offset(i, j), &v, 2);
+      }
   }
   {  // S as f16 m16n8k16 A fragments (bf16 -> f16 is exact except below 2^-14, rounded to nearest even)
     uint16_t* fr = reinterpret_cast<uint16_t*>(host.data() + ctx->to.S_frag);

@@ -103,10 +103,11 @@ TQ_HD uint32_t sw128_offset(int n, int k) {
 }
 
 // Device tables (inside the caller's d_tables buffer). S_sw is S (rows = projection index,
-// columns = coordinate) in the swizzled layout above; present for head_dim 128. S_frag is S in f16
+// columns = coordinate) in the swizzled layout above; HD_sw is H diag(D) (entries +-1, bf16) in the
+// same layout; both present for head_dim 128. S_frag is S in f16
 // as m16n8k16 A fragments (see sfrag_idx), for the decode kernels' query projection.
 struct TableOffsets {
-  size_t D, S, St, cb, S_sw, S_frag, bytes;
+  size_t D, S, St, cb, S_sw, HD_sw, S_frag, bytes;
 };
 
 // S_frag: [m-tile d/16][k-step d/16][lane 32] of {a0, a1, a2, a3} (four f16 pairs). Lane (g, c) of
@@ -150,6 +151,7 @@ struct LayerView {
   const float* cb;
   const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128)
   const uint4* S_frag;   // S in f16 m16n8k16 A fragments (sfrag_idx)
+  const uint16_t* HD_sw;  // H diag(D) in the tcgen05 swizzled K-major layout (head_dim 128)
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
   uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
   int32_t* state;      // this layer: [slot][2] = {L, F}

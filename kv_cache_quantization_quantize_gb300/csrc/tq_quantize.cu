@@ -1,8 +1,13 @@
-// Quantize-on-append ([Guide] §二, five-step pipeline): one CTA writes one packed page (128 tokens of
-// one KV head). This is the CUDA-core path for ring flushes and appends. The QJL projection z = S r
-// is an fp32 FMA contraction against S^T staged in shared memory.
+// Quantize-on-append ([Guide] §二, five-step pipeline). Two paths write packed pages (128 tokens of
+// one KV head):
+//   - CUDA-core kernels (one CTA per page) for ring flushes, decode-sized appends, f32 inputs and
+//     head_dim 256; their QJL projection z = S r is an fp32 FMA contraction against S^T in shared memory;
+//   - a persistent tcgen05 kernel for bulk bf16 appends at head_dim 128 (rotation and projection on
+//     the tensor cores).
 #include <algorithm>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "tq_device.cuh"
@@ -359,18 +364,24 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
 }
 
 // =============================================================================================
-// Bulk quantise (head_dim 128): the QJL projection z = S r on tcgen05 tensor cores.
-//   - The residual r of a 128-token page is split into bf16 hi + lo (|r - hi - lo| <= 2^-18 |r|) and
-//     written as operand A (128 tokens x 128 coordinates, K-major, 128-byte swizzle).
-//   - S (operand B) is loaded once per persistent CTA from its pre-swizzled table.
-//   - 16 MMAs (M = N = 128, K = 16; hi then lo) accumulate z in TMEM (fp32, 128 columns).
-//   - Each thread reads back one token row with tcgen05.ld and keeps the signs.
+// Bulk quantise (head_dim 128) on tcgen05 tensor cores. One persistent CTA per SM walks its pages:
+//   - The bf16 K and V rows of the next page stream into shared memory (cp.async, 128-byte swizzled
+//     K-major tiles) while the current page is coded.
+//   - Rotation: y' = (H diag(D)) x for all 128 tokens of K and of V as two M = N = 128, K = 128 MMAs
+//     (the +-1 entries are exact in bf16, products are exact, fp32 accumulation) into TMEM.
+//   - Warps 0-3 code the keys thread-per-token from TMEM: norm, Lloyd-Max index, residual, bf16
+//     hi + lo split of the residual (written over the consumed K tile), then the QJL projection
+//     z = S r as 16 more MMAs (|r - hi - lo| <= 2^-18 |r|) and the signs of z.
+//   - Warps 4-7 code the values thread-per-token: groups of 32, fp16 scale, mid-rise codes.
+//   - Key words, norms and value scales go to the page straight from registers; value codes are
+//     staged in shared memory for the fragment-major value layout.
 // =============================================================================================
-constexpr int kTcThreads = 256;
-constexpr uint32_t kTcS = 0, kTcAhi = 32768, kTcAlo = 65536, kTcKcode = 98304, kTcVcode = kTcKcode + 16384;
-constexpr uint32_t kTcSign = kTcVcode + 16384, kTcNorm = kTcSign + 2048, kTcScale = kTcNorm + 512;
-constexpr uint32_t kTcBar = kTcScale + 1024, kTcEnd = kTcBar + 64;
-constexpr size_t kTcSmem = kTcEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+constexpr int kTcThreads = 512;  // warps 0-7 keys, 8-15 values; two warps (column halves) per token row
+constexpr uint32_t kQbHD = 0, kQbS = 32768, kQbBuf = 65536;  // 2 x [K tile 32 KB | V tile 32 KB]
+constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 value codes
+constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
+constexpr uint32_t kQbBar = kQbX + 2048 + 4096 + 2048, kQbEnd = kQbBar + 64;
+constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
@@ -401,31 +412,88 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) k_quantize_bulk128(AppendArgs a, int pages_per_row, int batch) {
+// Loads page pg's K and V rows (bf16) into buffer `buf` (K tile at 0, V tile at 32 KB; each two
+// 16 KB swizzle atoms of 64 coordinates). Pages made of new input only are fetched by four TMA tensor
+// copies (tensor [batch][max_new][Hkv][128], box 64 x 1 x 128 x 1, 128-byte swizzle) that complete on
+// `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
+// all threads (at most one page per row and append).
+__device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
+                                             int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
+                                             uint64_t* bar) {
+  constexpr int D = 128;
+  if (pg * kPage >= L) {
+    if (threadIdx.x == 0) {
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      mbar_expect_tx(bar, 4u * 16384u);
+      const int z = pg * kPage - L;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const CUtensorMap* m = i < 2 ? tmk : tmv;
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(
+                smem_u32(buf + i * 16384)),
+            "l"(reinterpret_cast<uint64_t>(m)), "r"(64 * (i & 1)), "r"(h), "r"(z), "r"(b), "r"(smem_u32(bar))
+            : "memory");
+      }
+    }
+    return true;
+  }
+  for (int q = threadIdx.x; q < 2 * kPage * (D / 8); q += kTcThreads) {
+    const int which = q >> 11, t = (q >> 4) & 127, c = q & 15;
+    const int pos = pg * kPage + t;
+    const uint16_t* src;
+    if (pos < L) {
+      src = a.lv.ring + ((((size_t)slot * a.lv.Hkv + h) * 2 + which) * kPage + (pos - Np)) * D;
+    } else {
+      src = static_cast<const uint16_t*>(which ? a.v : a.k) + (((size_t)b * a.max_new + (pos - L)) * a.lv.Hkv + h) * D;
+    }
+    *reinterpret_cast<uint4*>(buf + which * 32768u + sw128_offset(t, 8 * c)) = *reinterpret_cast<const uint4*>(src + 8 * c);
+  }
+  return false;
+}
+
+// Next task (>= task, stepping by the grid) that has a page to write, or ntasks.
+__device__ __forceinline__ int bulk128_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, int& b,
+                                            int& h, int& slot, int& L, int& Np, int& pg) {
+  for (; task < ntasks; task += gridDim.x) {
+    b = task / (a.lv.Hkv * pages_per_row);
+    h = (task / pages_per_row) % a.lv.Hkv;
+    const int j = task % pages_per_row;
+    int valid;
+    if (page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && threadIdx.x == 0)) return task;
+  }
+  return ntasks;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    k_quantize_bulk128(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AppendArgs a,
+                       int pages_per_row, int batch) {
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* kcode = sm + kTcKcode;
-  uint8_t* vcode = sm + kTcVcode;
-  uint32_t* sgn = reinterpret_cast<uint32_t*>(sm + kTcSign);   // [128 tokens][4] sign words
-  uint32_t* norms = reinterpret_cast<uint32_t*>(sm + kTcNorm);
-  uint16_t* scales = reinterpret_cast<uint16_t*>(sm + kTcScale);
-  uint64_t* bar_s = reinterpret_cast<uint64_t*>(sm + kTcBar);
-  uint64_t* bar_mma = bar_s + 1;
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_s + 2);
+  uint8_t* vcode = sm + kQbVcode;
+  uint64_t* bar_tab = reinterpret_cast<uint64_t*>(sm + kQbBar);
+  uint64_t* bar_rot = bar_tab + 1;
+  uint64_t* bar_qjl = bar_tab + 2;
+  uint64_t* bar_ld = bar_tab + 3;  // [2]: page loads into buffer 0 / 1
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 5);
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
   pdl_launch();
   if (tid == 0) {
-    mbar_init(bar_s, 1);
-    mbar_init(bar_mma, 1);
+    mbar_init(bar_tab, 1);
+    mbar_init(bar_rot, 1);
+    mbar_init(bar_qjl, 1);
+    mbar_init(bar_ld, 1);
+    mbar_init(bar_ld + 1, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    mbar_expect_tx(bar_s, 2u * D * D);
-    bulk_g2s(sm + kTcS, lv.S_sw, 2u * D * D, bar_s);
+    mbar_expect_tx(bar_tab, 4u * D * D);
+    bulk_g2s(sm + kQbHD, lv.HD_sw, 2u * D * D, bar_tab);
+    bulk_g2s(sm + kQbS, lv.S_sw, 2u * D * D, bar_tab);
   }
-  if (warp == 0) {  // 128 TMEM columns: the fp32 accumulator of one 128 x 128 page
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 128;\n" ::"r"(smem_u32(tslot))
+  if (warp == 0) {  // 512 TMEM columns: rotated K (0..127), rotated V (128..255), z = S r (256..383)
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
@@ -433,224 +501,280 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_quantize_bulk128(AppendArgs a
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  float Dv[4], cent[4], bnd[3];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) Dv[e] = lv.D[4 * lane + e];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) cent[i] = lv.cb[i];
-#pragma unroll
-  for (int i = 0; i < 3; ++i) bnd[i] = lv.cb[4 + i];
-  bool ok = __syncthreads_and(mbar_wait(bar_s, 0)) != 0;
-  const int vb = lv.vb, vhalf = 1 << (vb - 1);
-  const float inv_sqrt_d = rsqrtf((float)D);
-  const uint32_t s_addr = smem_u32(sm + kTcS), ahi_addr = smem_u32(sm + kTcAhi), alo_addr = smem_u32(sm + kTcAlo);
-  uint32_t mma_phase = 0;
+  const uint32_t hd_addr = smem_u32(sm + kQbHD), s_addr = smem_u32(sm + kQbS), buf0 = smem_u32(sm + kQbBuf);
   const int ntasks = batch * lv.Hkv * pages_per_row;
-  for (int task = blockIdx.x; ok && task < ntasks; task += gridDim.x) {
-    const int b = task / (lv.Hkv * pages_per_row), h = (task / pages_per_row) % lv.Hkv, j = task % pages_per_row;
-    int slot, L, Np, pg, valid;
-    if (!page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && tid == 0)) continue;  // CTA-uniform
-    // ---- per token (warp): key rotation, norm, Lloyd-Max code, residual -> A; value quantisation.
-    // The 16 tokens of a warp are handled in chunks of 8 whose K and V rows are loaded together. ----
-    for (int c0 = 0; c0 < kPage / (kTcThreads / 32); c0 += 8) {
-    float kx[8][4], vx[8][4];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = warp + (kTcThreads / 32) * (c0 + i);
-      if (t < valid) {
-        load4(a, 0, slot, b, h, pg * kPage + t, L, Np, 4 * lane, kx[i]);
-        load4(a, 1, slot, b, h, pg * kPage + t, L, Np, 4 * lane, vx[i]);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) kx[i][e] = vx[i][e] = 0.f;
-      }
+  int b, h, slot, L, Np, pg;
+  int cur = bulk128_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+  __syncthreads();  // barriers initialised
+  bool tma_cur = cur < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld);
+  bool ok = __syncthreads_and(mbar_wait(bar_tab, 0)) != 0;
+  uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;  // ph_ld: bit i = parity of the next wait on bar_ld[i]
+  // warp roles: key path (warps 0-7) or value path (8-15); in each, warp w covers TMEM lane quarter
+  // w % 4 (tokens 32 (w % 4) + lane) and column half (w % 8) / 4
+  const bool kpath = warp < 8;
+  const int pw = warp & 7, q4 = pw & 3, half = pw >> 2;
+  const int t = 32 * q4 + lane;
+  float* xs = reinterpret_cast<float*>(sm + kQbX);                  // [2 halves][128] partial |y'|^2
+  float* xr = xs + 256;                                             // [2][128] partial |r|^2
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][8] half-1 index words
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 6144);     // [128][4] half-1 sign words
+  while (ok && cur < ntasks) {
+    const int cslot = slot, chead = h, cpg = pg;
+    const int nxt = bulk128_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+    const uint32_t buf = buf0 + bufi * 65536u;
+    const bool tma_nxt =
+        nxt < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
+                                     bar_ld + (bufi ^ 1u));
+    if (tma_cur) {  // this page's rows have landed
+      ok = mbar_wait(bar_ld + bufi, (ph_ld >> bufi) & 1u);
+      ph_ld ^= 1u << bufi;
     }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int t = warp + (kTcThreads / 32) * (c0 + i);
-      float x[4], y[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = kx[i][e];
-      float ss = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) ss = fmaf(x[e], x[e], ss);
-      ss = warp_sum(ss);
-      const float n = sqrtf(ss);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) y[e] = x[e] * Dv[e];
-      warp_fwht<4>(y, lane);
-      const float scale = n > 0.f ? 1.0f / (n * sqrtf((float)D)) : 0.f;
-      float rr = 0.f, res[4];
-      uint32_t codes4 = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float yy = y[e] * scale;
-        const int idx = (yy > bnd[0]) + (yy > bnd[1]) + (yy > bnd[2]);
-        res[e] = yy - cent[idx];
-        rr = fmaf(res[e], res[e], rr);
-        codes4 |= (uint32_t)idx << (8 * e);
-      }
-      *reinterpret_cast<uint32_t*>(kcode + t * D + 4 * lane) = codes4;
-      rr = warp_sum(rr);
-      uint32_t hi[2], lo[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint16_t h0 = f32_to_bf16_rn(res[2 * e]), h1 = f32_to_bf16_rn(res[2 * e + 1]);
-        const uint16_t l0 = f32_to_bf16_rn(res[2 * e] - bf16_to_f32(h0));
-        const uint16_t l1 = f32_to_bf16_rn(res[2 * e + 1] - bf16_to_f32(h1));
-        hi[e] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-        lo[e] = (uint32_t)l0 | ((uint32_t)l1 << 16);
-      }
-      const uint32_t off = sw128_offset(t, 4 * lane);
-      *reinterpret_cast<uint2*>(sm + kTcAhi + off) = make_uint2(hi[0], hi[1]);
-      *reinterpret_cast<uint2*>(sm + kTcAlo + off) = make_uint2(lo[0], lo[1]);
-      if (lane == 0) {
-        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
-        norms[t] = (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) x[e] = vx[i][e] * Dv[e];
-      warp_fwht<4>(x, lane);
-      float am = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        x[e] *= inv_sqrt_d;
-        am = fmaxf(am, fabsf(x[e]));
-      }
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 2));
-      am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
-      const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
-      const __half sh = __float2half_rn(s32);
-      const float sv = __half2float(sh);
-      uint32_t vc4 = 0;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int code = vhalf;
-        if (sv > 0.f) {
-          const float qv = floorf(__fdiv_rn(x[e], sv));
-          code = (int)fminf(fmaxf(qv, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
-        }
-        vc4 |= (uint32_t)code << (8 * e);
-      }
-      *reinterpret_cast<uint32_t*>(vcode + t * D + 4 * lane) = vc4;
-      if ((lane & 7) == 0) scales[t * (D / 32) + (lane >> 3)] = __half_as_ushort(sh);
-    }
-    }
-    // ---- z = S r on the tensor cores ----
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    __syncthreads();
-    if (tid == 0) {
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    if (tid == 0) {  // rotation of K and V: D[t][i] = sum_j x[t][j] (H D)[i][j]
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tmem, umma_desc_sw128(ahi_addr + koff), umma_desc_sw128(s_addr + koff), kIdescBf16M128N128,
-                  ks > 0 ? 1u : 0u);
+        umma_bf16(tmem, umma_desc_sw128(buf + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128, ks > 0);
       }
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tmem, umma_desc_sw128(alo_addr + koff), umma_desc_sw128(s_addr + koff), kIdescBf16M128N128, 1u);
+        umma_bf16(tmem + 128, umma_desc_sw128(buf + 32768 + koff), umma_desc_sw128(hd_addr + koff),
+                  kIdescBf16M128N128, ks > 0);
       }
-      umma_commit(bar_mma);
+      umma_commit(bar_rot);
     }
-    ok = __syncthreads_and(mbar_wait(bar_mma, mma_phase)) != 0;
-    mma_phase ^= 1;
+    ok = __syncthreads_and(mbar_wait(bar_rot, ph_rot)) != 0;
+    ph_rot ^= 1;
     if (!ok) break;
     tc_fence_after();
-    {  // warp w: TMEM lanes 32(w%4).. (tokens), columns 64(w/4).. (projection rows)
-      const int q = warp & 3, ch = warp >> 2, t = 32 * q + lane;
+    uint8_t* page = lv.pages + (((size_t)cslot * lv.Hkv + chead) * lv.max_pages + cpg) * lv.page_bytes;
+    const PageLayout pl = page_layout(D, lv.vb);
+    const uint32_t lrow = tmem + ((uint32_t)(32 * q4) << 16);
+    bool ok_p = true;
+    if (kpath) {
+      // ---- keys, two threads per token (64 coordinates each): |y'|, y = y' / |y'|, index, residual ----
+      float ss4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lrow + 64 * half + 32 * cc, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ss4[i & 3] = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss4[i & 3]);
+      }
+      xs[half * 128 + t] = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
+      named_barrier(1, 256);
+      const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
+      const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
+      const float b0 = lv.cb[4], b1 = lv.cb[5], b2 = lv.cb[6];
+      const float c0 = lv.cb[0], c1 = lv.cb[1], c2 = lv.cb[2], c3 = lv.cb[3];
+      uint32_t whi[4] = {0u, 0u, 0u, 0u}, wlo[4] = {0u, 0u, 0u, 0u};
+      float rr4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lrow + 64 * half + 32 * cc, v);
+#pragma unroll
+        for (int oc = 0; oc < 4; ++oc) {  // 8 coordinates = one 16-byte chunk of the A rows
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            float res2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate 64 half + jl
+              const float yy = __uint_as_float(v[i]) * scale;
+              // index = #{boundaries below yy}: high bit = (yy > b1); low bit = yy above the outer
+              // boundary on its side of b1
+              const bool hb = yy > b1;
+              const bool lb = yy > (hb ? b2 : b0);
+              const float cv = hb ? (lb ? c3 : c2) : (lb ? c1 : c0);
+              const float res = yy - cv;
+              rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
+              res2[e] = res;
+              // bit of coordinate j = 64 half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
+              // 64 half adds 8 to 2 (j >> 4)
+              const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+              whi[cw] |= hb ? (1u << bit) : 0u;
+              wlo[cw] |= lb ? (1u << bit) : 0u;
+            }
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(res2[0], res2[1]);
+            const float2 hf2 = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(res2[0] - hf2.x, res2[1] - hf2.y);
+            hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+            lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
+          }
+          const uint32_t off = sw128_offset(t, 64 * half + 32 * cc + 8 * oc);
+          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+      xr[half * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+      if (half) {
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) {
+          xw[t * 8 + cw] = whi[cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
+          xw[t * 8 + 4 + cw] = wlo[cw] << 8;
+        }
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc_fence_before();
+      named_barrier(1, 256);
+      uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+      const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
+      if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo)
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32 + (ks >> 3) * 32768;
+          umma_bf16(tmem + 256, umma_desc_sw128(buf + koff), umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32),
+                    kIdescBf16M128N128, ks > 0);
+        }
+        umma_commit(bar_qjl);
+      }
+      if (!half) {  // planes 0-1, n and gamma of token t
+        const float n = nrot * rsqrtf((float)D);
+        const float rr = xr[t] + xr[128 + t];
+        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
+        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
+            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) {
+          kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
+          kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
+        }
+      }
+      ok_p = mbar_wait(bar_qjl, ph_qjl);
+      tc_fence_after();
+      uint32_t wsg[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t z[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(64 * ch + 32 * cc), z);
-        uint32_t bits = 0;
+        tmem_ld32(lrow + 256 + 64 * half + 32 * cc, z);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) bits |= (uint32_t)(__uint_as_float(z[i]) >= 0.f) << i;
-        sgn[t * 4 + 2 * ch + cc] = bits;
+        for (int i = 0; i < 32; ++i) {
+          const int jl = 32 * cc + i;
+          const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+          wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
+        }
       }
-    }
-    tc_fence_before();
-    __syncthreads();
-    // ---- pack the page (fragment-major layout) ----
-    uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
-    const PageLayout pl = page_layout(D, vb);
-    uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-    for (int w = tid; w < 8 * 3 * 32 * 2; w += kTcThreads) {
-      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3, tile = w / 192;
-      const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
-      uint32_t word = 0;
-      if (pi < 2) {
-        const uint8_t* kc = kcode + t * D + 2 * c;
+      if (half) {
 #pragma unroll
-        for (int sq = 0; sq < 8; ++sq)
+        for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
+      }
+      named_barrier(1, 256);
+      if (!half) {
 #pragma unroll
-          for (int sub = 0; sub < 2; ++sub)
+        for (int cw = 0; cw < 4; ++cw) kw[((tile * 3 + 2) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[t * 4 + cw];
+      }
+    } else {
+      // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
+      const int vhalf = 1 << (lv.vb - 1);
+      const float inv_sqrt_d = rsqrtf((float)D);
+      uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
+#pragma unroll 1
+      for (int gg = 0; gg < 2; ++gg) {
+        const int grp = 2 * half + gg;
+        uint32_t v[32];
+        tmem_ld32(lrow + 128 + 32 * grp, v);
+        float x[32], am4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int code = kc[16 * sq + 8 * sub + e];
-              word |= (uint32_t)((pi == 0 ? code >> 1 : code) & 1) << (2 * sq + sub + 16 * e);
-            }
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(v[i]) * inv_sqrt_d;
+          am4[i & 3] = fmaxf(am4[i & 3], fabsf(x[i]));
+        }
+        const float am = fmaxf(fmaxf(am4[0], am4[1]), fmaxf(am4[2], am4[3]));
+        const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
+        const __half sh = __float2half_rn(s32);
+        const float sv = __half2float(sh);
+        // floor(x / s) with the quotient rounded as an IEEE division: x * (1/s) is within a few ulps of
+        // it, so its floor is exact unless it lies within ~4 ulps of an integer; those (rare) elements
+        // take the correctly rounded division.
+        const float rcp = sv > 0.f ? __frcp_rn(sv) : 0.f;
+        float fq[32];
+        bool near = false;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float qv = x[i] * rcp;
+          fq[i] = floorf(qv);
+          const float fr = qv - fq[i], eps = fabsf(qv) * 4.8e-7f + 1e-30f;
+          near |= (fr < eps) | (fr > 1.f - eps);
+        }
+        if (near && sv > 0.f) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) fq[i] = floorf(__fdiv_rn(x[i], sv));
+        }
+        uint32_t cw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int code = sv > 0.f ? (int)fminf(fmaxf(fq[4 * k + e], (float)-vhalf), (float)(vhalf - 1)) + vhalf : vhalf;
+            w |= (uint32_t)code << (8 * e);
+          }
+          cw[k] = w;
+        }
+        // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
+      }
+      named_barrier(2, 256);
+      // ---- pack the value codes (fragment-major layout) ----
+      const int vt = tid - 256;
+      uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
+      if (lv.vb == 2) {
+        for (int w = vt; w < 4 * (D / 16) * 32; w += 256) {
+          const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
+          const int g = ln >> 2, c = ln & 3;
+          uint32_t word = 0;
+#pragma unroll
+          for (int kap = 0; kap < 2; ++kap)
+#pragma unroll
+            for (int rg = 0; rg < 4; ++rg)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+                word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
+              }
+          vw[w] = word;
+        }
       } else {
-#pragma unroll
-        for (int sq = 0; sq < 8; ++sq)
-#pragma unroll
-          for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int jj = 16 * sq + 8 * sub + 2 * c + e;
-              word |= ((sgn[t * 4 + (jj >> 5)] >> (jj & 31)) & 1u) << (2 * sq + sub + 16 * e);
-            }
-      }
-      kw[w] = word;
-    }
-    uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
-    for (int t = tid; t < kPage; t += kTcThreads) nw[t] = norms[t];
-    uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
-    if (vb == 2) {
-      for (int w = tid; w < 4 * (D / 16) * 32; w += kTcThreads) {
-        const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
-        const int g = ln >> 2, c = ln & 3;
-        uint32_t word = 0;
-#pragma unroll
-        for (int kap = 0; kap < 2; ++kap)
+        for (int w = vt; w < 4 * (D / 16) * 32 * 2; w += 256) {
+          const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
+          const int g = ln >> 2, c = ln & 3;
+          uint32_t word = 0;
 #pragma unroll
           for (int rg = 0; rg < 4; ++rg)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
-              word |= (uint32_t)vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
+              const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+              word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
             }
-        vw[w] = word;
-      }
-    } else {
-      for (int w = tid; w < 4 * (D / 16) * 32 * 2; w += kTcThreads) {
-        const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
-        const int g = ln >> 2, c = ln & 3;
-        uint32_t word = 0;
-#pragma unroll
-        for (int rg = 0; rg < 4; ++rg)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
-            word |= (uint32_t)vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
-          }
-        vw[w] = word;
+          vw[w] = word;
+        }
       }
     }
-    uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
-    for (int i = tid; i < kPage * (D / 32); i += kTcThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
-    __syncthreads();  // shared buffers are reused by the next page
+    ph_qjl ^= kpath ? 1u : 0u;
+    tc_fence_before();
+    ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, vcode and exchange may be reused
+    tc_fence_after();
+    cur = nxt;
+    tma_cur = tma_nxt;
+    bufi ^= 1u;
   }
+  if (ok && tma_cur) mbar_wait(bar_ld + bufi, (ph_ld >> bufi) & 1u);  // no copy in flight at exit
   if (!ok && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 128;\n" ::"r"(tmem) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
 }
 
-// Ring update after the quantise launch: write the new ring tail and the sequence state.
 // Dependents (the decode of this layer) are released only after the state is written: they read the
 // sequence state before their own griddepcontrol.wait to start fetching pages early.
 __global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
@@ -756,6 +880,27 @@ cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStrea
 }
 
 // Bulk appends of head_dim 128 use the tcgen05 kernel: one persistent CTA per SM over all pages.
+// Tensor map of k or v ([batch][max_new][Hkv][128] bf16) for 64 x 1 x 128 x 1 boxes, 128-byte swizzle.
+cudaError_t bulk128_tensor_map(const void* base, int batch, int max_new, int hkv, CUtensorMap* m) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[4] = {128, (cuuint64_t)hkv, (cuuint64_t)max_new, (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {256, (cuuint64_t)hkv * 256, (cuuint64_t)max_new * hkv * 256};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
@@ -765,7 +910,11 @@ cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, i
   }
   const int ntasks = batch * a.lv.Hkv * pages;
   const int grid = std::max(1, std::min(ntasks, sms));
-  return launch_pdl(k_quantize_bulk128, dim3(grid), dim3(kTcThreads), kTcSmem, s, a, pages, batch);
+  CUtensorMap tmk, tmv;
+  cudaError_t e = bulk128_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, &tmk);
+  if (e == cudaSuccess) e = bulk128_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, &tmv);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(k_quantize_bulk128, dim3(grid), dim3(kTcThreads), kTcSmem, s, tmk, tmv, a, pages, batch);
 }
 
 }  // namespace
@@ -786,7 +935,7 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
     return a.lv.d == 128 ? launch_append_small_d<128>(a, batch, smem, s) : launch_append_small_d<256>(a, batch, smem, s);
   }
   const int pages = (max_new + kPage - 1) / kPage;
-  cudaError_t e = (a.lv.d == 128 && max_new >= kPage)
+  cudaError_t e = (a.lv.d == 128 && max_new >= kPage && dt == 0)
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
                       : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;

@@ -137,3 +137,39 @@ def test_full_size_llama_layer_sampled():
         ref = oracle.decode_attention(_f64(q[0, h * G:(h + 1) * G]), keys, vals, _f64(rk[:R]), _f64(rv[:R]), D, S, c)
         for g in range(G):
             assert rel_l2(out[0, h * G + g], ref[g]) <= 2e-3
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2)])
+def test_bulk_append_onto_a_partial_ring(d, vb):
+    """Bulk appends (>= 128 tokens) onto sequences whose ring is partly full: the first page written
+    takes its leading tokens from the ring and the rest from the new input; later pages come from the
+    input only. Rows: ring of 72, 1 and 128 tokens before the second append."""
+    Hkv, G = 2, 4
+    first, second = [200, 129, 128], [300, 260, 130]
+    B = len(first)
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B, max_ctx=600,
+                 seed=17)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    seqs = [synth.kv_tokens(f + s_, Hkv, d, seed=300 + i, outliers=("random", 4, 10.0))
+            for i, (f, s_) in enumerate(zip(first, second))]
+    ids = _i32(list(range(B)))
+    for part, lens in ((0, first), (1, second)):
+        n = max(lens)
+        kb = torch.zeros(B, n, Hkv, d, dtype=torch.bfloat16)
+        vbuf = torch.zeros_like(kb)
+        for i in range(B):
+            lo = 0 if part == 0 else first[i]
+            kb[i, :lens[i]] = seqs[i][0][lo:lo + lens[i]]
+            vbuf[i, :lens[i]] = seqs[i][1][lo:lo + lens[i]]
+        cache.append(0, kb.to(DEV), vbuf.to(DEV), ids, _i32(lens))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    for i in range(B):
+        _check_sequence(cache, 0, i, seqs[i][0], seqs[i][1], tables)
+    q = synth.queries(B, Hkv * G, d, seed=17)
+    out = cache.decode(0, q.to(DEV), ids).cpu().numpy()
+    for i in range(B):
+        ref = _oracle_decode(cache, 0, i, q[i], tables)
+        for hq in range(Hkv * G):
+            assert rel_l2(out[i, hq], ref[hq]) <= 2e-3
