@@ -87,9 +87,15 @@ __host__ __device__ constexpr int decode_xbuf_floats() {
   return D == 256 ? decode_threads<D>() * 2 * 8 : 0;
 }
 
+// Split CTAs run `decode_streams` independent page streams of 4 token-group warps x (d/128) coordinate
+// halves: 3 streams (12 warps, one CTA per SM) for head_dim 128, 1 stream (8 warps) for head_dim 256.
+template <int D>
+__host__ __device__ constexpr int decode_streams() {
+  return D == 128 ? 3 : 1;
+}
 template <int D>
 __host__ __device__ constexpr int decode_threads() {
-  return 32 * 4 * (D / 128);  // 4 token groups x (d/128) coordinate halves
+  return decode_streams<D>() * 32 * 4 * (D / 128);
 }
 
 // =============================================================================================
@@ -122,7 +128,7 @@ struct SFrag {
 };
 template <int D>
 __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f) {
-  if (D == 128) {
+  if (D == 128 && (threadIdx.x >> 5) < D / 32) {  // warps that compute q_proj rows
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int m2 = 0; m2 < 2; ++m2)
@@ -183,7 +189,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     }
   }
   __syncthreads();
-  {  // q_proj rows 16 mt .. 16 mt + 15, mt = 2 warp + {0, 1}; B column n = head g (zero for g >= 4)
+  if (warp < MT / 2) {  // q_proj rows 16 mt .. 16 mt + 15, mt = 2 warp + {0, 1}; B column n = head g (zero for g >= 4)
     const bool col = g < kMaxG;
     const float lam = col ? red[g] : 0.f;
     const float* qrow = qr + (col ? g : 0) * D + 2 * c;
@@ -560,15 +566,17 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // Values: P is moved from C to B fragment layout with movmatrix and scaled per value group. Then
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
 template <int D, int VB, int STAGES>
-__global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
   constexpr int HALVES = D / 128;
   constexpr int NT = decode_threads<D>();
+  constexpr int NS = decode_streams<D>();
+  constexpr int SW = 4 * HALVES;  // warps per stream
   constexpr int NG = D / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerView& lv = a.lv;
   const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int tg = warp & 3, hf = warp >> 2;
+  const int stream = warp / SW, tg = warp & 3, hf = (warp % SW) >> 2;
   const int nsp = a.plan.n_splits;
   float* part = reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                          (((size_t)b * lv.Hkv + h) * (nsp + 1) + sp) * a.plan.part_stride);
@@ -600,18 +608,20 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
   }
   const PageLayout pl = page_layout(D, VB);
   const uint32_t PB = pl.bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint8_t* stage0 = smem + 128;
-  float* xbuf = reinterpret_cast<float*>(stage0 + (size_t)STAGES * PB);  // [NT][2 tiles][8] partial scores
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [stream][stage]
+  uint8_t* stage0 = smem + 128;                         // [stream][stage] pages
+  float* xbuf = reinterpret_cast<float*>(stage0 + (size_t)NS * STAGES * PB);  // [NT][2 tiles][8] partial scores
   const uint8_t* gpages = lv.pages + ((size_t)slot * lv.Hkv + h) * lv.max_pages * PB;
-  const int npg = pg1 - pg0;
+  const int npg = pg1 - pg0;  // stream st takes local pages st, st + NS, st + 2 NS, ...
   if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < NS * STAGES; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    for (int s = 0; s < STAGES && s < npg; ++s) {
-      mbar_expect_tx(&full[s], PB);
-      bulk_g2s(stage0 + (size_t)s * PB, gpages + (size_t)(pg0 + s) * PB, PB, &full[s]);
-    }
+    for (int st = 0; st < NS; ++st)
+      for (int s = 0; s < STAGES && st + NS * s < npg; ++s) {
+        mbar_expect_tx(&full[st * STAGES + s], PB);
+        bulk_g2s(stage0 + (size_t)(st * STAGES + s) * PB, gpages + (size_t)(pg0 + st + NS * s) * PB, PB,
+                 &full[st * STAGES + s]);
+      }
   }
   SFrag<D> sfrag;
   sfrag_prefetch<D>(lv, sfrag);
@@ -631,13 +641,12 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
   __syncthreads();
   bool timed_out = false;
 
-  for (int ip = 0; ip < npg; ++ip) {
-    const int s_ = ip % STAGES;
-    if (!mbar_wait(&full[s_], (ip / STAGES) & 1)) {
-      timed_out = true;
-      break;
-    }
-    const uint8_t* pg = stage0 + (size_t)s_ * PB;
+  for (int k = 0; stream + NS * k < npg; ++k) {
+    const int ip = stream + NS * k, s_ = k % STAGES;
+    // A wait that gives up marks the call and stops waiting; the loop still runs to its end so that
+    // every warp reaches the stream barriers (the page contents are then unspecified).
+    if (!timed_out && !mbar_wait(&full[stream * STAGES + s_], (k / STAGES) & 1)) timed_out = true;
+    const uint8_t* pg = stage0 + (size_t)(stream * STAGES + s_) * PB;
     const int valid = min(kPage, P - (pg0 + ip) * kPage);
     const uint2* kw2 = reinterpret_cast<const uint2*>(pg + pl.kbits_off);
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(pg + pl.norms_off);
@@ -794,18 +803,23 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
         O[mt][3] = fmaf(O[mt][3], alpha[1], acc[3]);
       }
     }
-    __syncthreads();  // every warp is done with stage s_ (and with xbuf)
-    if (tid == 0 && ip + STAGES < npg) {
-      mbar_expect_tx(&full[s_], PB);
-      bulk_g2s(stage0 + (size_t)s_ * PB, gpages + (size_t)(pg0 + ip + STAGES) * PB, PB, &full[s_]);
+    // every warp of the stream is done with stage s_ (and with xbuf)
+    if (NS == 1) __syncthreads();
+    else named_barrier(5 + stream, 32 * SW);
+    if ((tid % (32 * SW)) == 0 && ip + NS * STAGES < npg) {
+      mbar_expect_tx(&full[stream * STAGES + s_], PB);
+      bulk_g2s(stage0 + (size_t)(stream * STAGES + s_) * PB, gpages + (size_t)(pg0 + ip + NS * STAGES) * PB, PB,
+               &full[stream * STAGES + s_]);
     }
   }
   if (timed_out && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   // ---- merge the token groups' partials through shared memory ----
   __syncthreads();
-  float* wm = reinterpret_cast<float*>(stage0);  // [4 token groups][4 heads]
-  float* wl = wm + 16;                           // [4][4]
-  float* wo = wl + 16;                           // [4][4][D]
+  constexpr int NGRP = 4 * NS;                     // (stream, token group) partials
+  const int grp = 4 * stream + tg;
+  float* wm = reinterpret_cast<float*>(stage0);  // [NGRP][4 heads]
+  float* wl = wm + 4 * NGRP;                     // [NGRP][4]
+  float* wo = wl + 4 * NGRP;                     // [NGRP][4][D]
   {
     float l0 = l_acc[0], l1 = l_acc[1];
 #pragma unroll
@@ -814,19 +828,19 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
     if (hf == 0 && g == 0 && c < 2) {
-      wm[tg * 4 + 2 * c] = m_eff[0];
-      wm[tg * 4 + 2 * c + 1] = m_eff[1];
-      wl[tg * 4 + 2 * c] = l0;
-      wl[tg * 4 + 2 * c + 1] = l1;
+      wm[grp * 4 + 2 * c] = m_eff[0];
+      wm[grp * 4 + 2 * c + 1] = m_eff[1];
+      wl[grp * 4 + 2 * c] = l0;
+      wl[grp * 4 + 2 * c + 1] = l1;
     }
     if (c < 2) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         const int j0 = 128 * hf + 16 * mt + g;
-        wo[(tg * 4 + 2 * c) * D + j0] = O[mt][0];
-        wo[(tg * 4 + 2 * c + 1) * D + j0] = O[mt][1];
-        wo[(tg * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
-        wo[(tg * 4 + 2 * c + 1) * D + j0 + 8] = O[mt][3];
+        wo[(grp * 4 + 2 * c) * D + j0] = O[mt][0];
+        wo[(grp * 4 + 2 * c + 1) * D + j0] = O[mt][1];
+        wo[(grp * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
+        wo[(grp * 4 + 2 * c + 1) * D + j0 + 8] = O[mt][3];
       }
     }
   }
@@ -835,11 +849,11 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
     const int hd = i / D, j = i % D;
     float m = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) m = fmaxf(m, wm[w * 4 + hd]);
+    for (int w = 0; w < NGRP; ++w) m = fmaxf(m, wm[w * 4 + hd]);
     float o = 0.f, l = 0.f;
     if (m != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
+      for (int w = 0; w < NGRP; ++w) {
         const float mw = wm[w * 4 + hd];
         const float f = mw == -INFINITY ? 0.f : exp2f(mw - m);
         o += f * wo[(w * 4 + hd) * D + j];
@@ -856,7 +870,7 @@ __global__ void __launch_bounds__(decode_threads<D>()) k_decode(DecodeArgs a) {
 }
 
 template <int D, int VB>
-constexpr int decode_stages() {
+constexpr int decode_stages() {  // pages in flight per stream
   return D == 128 ? 4 : 3;
 }
 
@@ -864,9 +878,11 @@ template <int D, int VB>
 size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB);
   constexpr int NT = decode_threads<D>();
-  const size_t merge_bytes = sizeof(float) * (16 + 16 + 16 * D);
+  constexpr int NGRP = 4 * decode_streams<D>();
+  const size_t merge_bytes = sizeof(float) * (8 * NGRP + 4 * NGRP * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
-  size_t smem = 128 + (size_t)decode_stages<D, VB>() * pl.bytes + xbuf_bytes + prep_scratch_bytes<D>();
+  size_t smem = 128 + (size_t)decode_streams<D>() * decode_stages<D, VB>() * pl.bytes + xbuf_bytes +
+                prep_scratch_bytes<D>();
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_smem_bytes<D>());
   smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 8 * 1026));  // combine: split (m, l)

@@ -265,9 +265,9 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
   const int per_sm = ctx->host_only ? 2 : decode_resident_ctas(ctx);
   const int target = per_sm * sms;  // split-K CTAs that fit in one wave
-  // Small batches: one wave of (splits + ring) CTAs per (row, KV head). Large batches: about three
+  // Small batches: one wave of (splits + ring) CTAs per (row, KV head). Large batches: about six
   // waves, so that the tail of the last wave is short.
-  int splits = units * 2 <= target ? std::max(1, target / units - 1) : std::max(2, (3 * target + units - 1) / units);
+  int splits = units * 2 <= target ? std::max(1, target / units - 1) : std::max(2, (6 * target + units - 1) / units);
   splits = std::min(splits, max_pages);
   splits = std::min(splits, 1024);  // the combine keeps 4 weights per split in shared memory
   DecodePlan p;
