@@ -409,8 +409,8 @@ def bench_quantize(tqm, synth, dev, args, peak):
     gbs = bytes_pass / (ms * 1e-3) / 1e9
     return {"tok_s": T / (ms * 1e-3), "token_head_layers_per_s": T * Hkv * L_layers / (ms * 1e-3),
             "ms_per_pass": ms, "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K3/V{vb}",
-            "path": ("tcgen05 QJL projection (bf16 hi/lo split, TMEM accumulator) + CUDA-core rotation and codes"
-                     if d == 128 else "CUDA-core quantise kernel (fp32 FMA QJL projection)"),
+            "path": ("tcgen05 rotation (H diag(D)) and QJL projection (bf16 hi/lo) into TMEM, thread-per-token "
+                     "coding, TMA page loads" if d == 128 else "CUDA-core quantise kernel (fp32 FMA QJL projection)"),
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
 
 
