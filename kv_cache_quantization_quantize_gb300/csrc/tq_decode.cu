@@ -60,6 +60,19 @@ __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   return *reinterpret_cast<const uint32_t*>(&r);
 }
 
+// ld.global.cg (L2 only: data written by other CTAs of this grid) that the compiler cannot move above
+// a guard; __ldcg is a non-volatile asm and may be hoisted.
+__device__ __forceinline__ float ld_cg_f(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];\n" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float4 ld_cg_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];\n" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float2 half2_to_float2(uint32_t a) {
   return __half22float2(*reinterpret_cast<const __half2*>(&a));
 }
@@ -105,7 +118,8 @@ __host__ __device__ constexpr int decode_threads() {
 // Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
 template <int D>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
-  return sizeof(float) * (2 * kMaxG * D + 16);
+  // q_rot, q_proj [4][D] fp32; 16 scales; 16 offset sums; B fragments [3 D/16 items][32 lanes] uint2
+  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (3 * D / 16);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
@@ -134,7 +148,7 @@ __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f)
     for (int m2 = 0; m2 < 2; ++m2)
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) f.a[m2 % (D == 128 ? 2 : 1)][ks % (D == 128 ? D / 16 : 1)] =
-          __ldg(lv.S_frag + sfrag_idx(D, 2 * warp + m2, ks, lane));
+          lv.S_frag[sfrag_idx(D, 2 * warp + m2, ks, lane)];
   }
 }
 
@@ -156,7 +170,8 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   constexpr int MT = D / 16;
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, c = lane & 3, hf = warp >> 2;
+  const int g = lane >> 2, c = lane & 3;
+  const int hf = (warp % (4 * HALVES)) >> 2;  // coordinate half of this warp within its page stream
   const int G = lv.G;
   const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
   float* qr = ps;               // [4][D]
@@ -204,7 +219,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
 #pragma unroll
       for (int m2 = 0; m2 < 2; ++m2) {
         const uint4 A = D == 128 ? sf.a[m2 % (D == 128 ? 2 : 1)][ks % (D == 128 ? MT : 1)]
-                                 : __ldg(lv.S_frag + sfrag_idx(D, 2 * warp + m2, ks, lane));
+                                 : lv.S_frag[sfrag_idx(D, 2 * warp + m2, ks, lane)];
         mma_f16(acc[m2], A.x, A.y, A.z, A.w, h0, h1);
         mma_f16(acc[m2], A.x, A.y, A.z, A.w, l0, l1);
       }
@@ -222,46 +237,55 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     }
   }
   __syncthreads();
+  // B fragments: item (hv, pi, s) is computed by warp item % NW and shared through shared memory;
+  // red[16 + hd] / red[20 + hd] collect the offset sums of head hd
+  constexpr int NW = NT / 32, NITEMS = HALVES * 3 * 8;
+  float* sums = red + 16;
+  uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
+  if (tid < 8) sums[tid] = 0.f;
   const bool live = g < G;
   const float lam_m = live ? red[4 + 2 * g] : 0.f, lam_q = live ? red[4 + 2 * g + 1] : 0.f;
   const float* bm = qr + (live ? g : 0) * D;
   const float* bp = qp + (live ? g : 0) * D;
+  __syncthreads();
   float sum_m = 0.f, sum_q = 0.f;
-#pragma unroll
-  for (int hv = 0; hv < HALVES; ++hv) {
-#pragma unroll
-    for (int pi = 0; pi < 3; ++pi) {
-      const float w = (pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f) * (pi < 2 ? lam_m : lam_q);
-      const float* base = pi < 2 ? bm : bp;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
-        const float pre0 = key_prescale(2 * s), pre1 = key_prescale(2 * s + 1);
-        const float2 x0 = *reinterpret_cast<const float2*>(base + j0);
-        const float2 x1 = *reinterpret_cast<const float2*>(base + j1);
-        const uint32_t b0 = pack_half2(w * x0.x * pre0, w * x0.y * pre0);
-        const uint32_t b1 = pack_half2(w * x1.x * pre1, w * x1.y * pre1);
-        if (hv == hf) bq[pi][s] = make_uint2(b0, b1);
-        const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
-        const float v = (r0.x + r0.y) * (1.f / pre0) + (r1.x + r1.y) * (1.f / pre1);
-        if (pi < 2) sum_m += v;
-        else sum_q += v;
-      }
-    }
+  for (int item = warp; item < NITEMS; item += NW) {
+    const int s = item & 7, pi = (item >> 3) % 3, hv = item / 24;
+    const float w = (pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f) * (pi < 2 ? lam_m : lam_q);
+    const float* base = pi < 2 ? bm : bp;
+    const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
+    const float pre0 = key_prescale(2 * s), pre1 = key_prescale(2 * s + 1);
+    const float2 x0 = *reinterpret_cast<const float2*>(base + j0);
+    const float2 x1 = *reinterpret_cast<const float2*>(base + j1);
+    const uint32_t b0 = pack_half2(w * x0.x * pre0, w * x0.y * pre0);
+    const uint32_t b1 = pack_half2(w * x1.x * pre1, w * x1.y * pre1);
+    frag[item * 32 + lane] = make_uint2(b0, b1);
+    const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
+    const float v = (r0.x + r0.y) * (1.f / pre0) + (r1.x + r1.y) * (1.f / pre1);
+    if (pi < 2) sum_m += v;
+    else sum_q += v;
   }
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 1);
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
+  if (c == 0 && g < kMaxG) {
+    atomicAdd(&sums[g], sum_m);
+    atomicAdd(&sums[4 + g], sum_q);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int pi = 0; pi < 3; ++pi)
+#pragma unroll
+    for (int s = 0; s < 8; ++s) bq[pi][s] = frag[((hf * 3 + pi) * 8 + s) * 32 + lane];
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd; its sums live in lanes 4 hd ..
+  for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd
     const int hd = min(2 * c + i, kMaxG - 1);
-    const float sm_ = __shfl_sync(0xffffffffu, sum_m, 4 * hd), sq_ = __shfl_sync(0xffffffffu, sum_q, 4 * hd);
     um[i] = a.scale * kLog2e / red[4 + 2 * hd];
-    cm[i] = 0.5f * sm_;
+    cm[i] = 0.5f * sums[hd];
     uq[i] = a.scale * kLog2e * kappa / red[4 + 2 * hd + 1];
-    cq[i] = 0.5f * sq_;
+    cq[i] = 0.5f * sums[4 + hd];
   }
 }
 
@@ -429,11 +453,34 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float* red = sm;                      // [NW][4]
   float* fs = sm + 4 * NW;              // [nsp][4] split maxima, then split weights
   float* ls = fs + 4 * (nsp + 1);       // [nsp][4] split sums
+  // 0. warps 0..G-1 (query head = warp) start loading the outputs of the first 16 splits and the ring
+  //    partial now: they do not depend on the weights, so they share the round trip of the (m, l) loads
+  constexpr int PRE = D == 128 ? 16 : 8;
+  const int hdw = warp;
+  const bool merger = warp < lv.G;
+  const float* ob = base + 2 * kMaxG + hdw * D + 4 * lane;
+  const float* rp = base + nsp * stride;
+  float4 vpre[PRE][NE / 4], rvp[NE / 4];
+  float mrp = -INFINITY, lrp = 0.f;
+  if (merger) {
+#pragma unroll
+    for (int u = 0; u < PRE; ++u)
+#pragma unroll
+      for (int hf = 0; hf < NE / 4; ++hf) {
+        vpre[u][hf] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (u < nsp) vpre[u][hf] = ld_cg_f4(ob + u * stride + 128 * hf);
+      }
+#pragma unroll
+    for (int hf = 0; hf < NE / 4; ++hf)
+      rvp[hf] = ld_cg_f4(rp + 2 * kMaxG + hdw * D + 128 * hf + 4 * lane);
+    mrp = ld_cg_f(rp + hdw);
+    lrp = ld_cg_f(rp + kMaxG + hdw);
+  }
   // 1. one pass over the splits' (m, l): kept in shared memory; block-wide max per head
   float mloc[kMaxG] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
   for (int s = tid; s < nsp; s += NT) {
-    const float4 m4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride));
-    const float4 l4 = __ldcg(reinterpret_cast<const float4*>(base + s * stride + kMaxG));
+    const float4 m4 = ld_cg_f4(base + s * stride);
+    const float4 l4 = ld_cg_f4(base + s * stride + kMaxG);
     *reinterpret_cast<float4*>(fs + 4 * s) = m4;
     *reinterpret_cast<float4*>(ls + 4 * s) = l4;
     mloc[0] = fmaxf(mloc[0], m4.x);
@@ -474,19 +521,30 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float l = 0.f;
 #pragma unroll
   for (int w = 0; w < NW; ++w) l += red[w * 4 + hd];
-  // 3. weighted sum of the split outputs: 16 splits' loads in flight, two accumulator sets
+  // 3. weighted sum of the split outputs: the prefetched 16, then 16 splits' loads in flight at a time
   float o[NE], o2[NE];
 #pragma unroll
   for (int e = 0; e < NE; ++e) o[e] = o2[e] = 0.f;
-  const float* ob = base + 2 * kMaxG + hd * D + 4 * lane;
-  int s0 = 0;
+#pragma unroll
+  for (int u = 0; u < PRE; ++u) {
+    const float f = u < nsp ? fs[u * 4 + hd] : 0.f;
+    float* acc = (u & 1) ? o2 : o;
+#pragma unroll
+    for (int hf = 0; hf < NE / 4; ++hf) {
+      acc[4 * hf + 0] = fmaf(f, vpre[u][hf].x, acc[4 * hf + 0]);
+      acc[4 * hf + 1] = fmaf(f, vpre[u][hf].y, acc[4 * hf + 1]);
+      acc[4 * hf + 2] = fmaf(f, vpre[u][hf].z, acc[4 * hf + 2]);
+      acc[4 * hf + 3] = fmaf(f, vpre[u][hf].w, acc[4 * hf + 3]);
+    }
+  }
+  int s0 = PRE;
   for (; s0 + 16 <= nsp; s0 += 16) {  // empty splits hold weight 0 and O = 0
     float4 v[16][NE / 4];
 #pragma unroll
     for (int u = 0; u < 16; ++u)
 #pragma unroll
       for (int hf = 0; hf < NE / 4; ++hf)
-        v[u][hf] = __ldcg(reinterpret_cast<const float4*>(ob + (s0 + u) * stride + 128 * hf));
+        v[u][hf] = ld_cg_f4(ob + (s0 + u) * stride + 128 * hf);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const float f = fs[(s0 + u) * 4 + hd];
@@ -504,7 +562,7 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
     const float f = fs[s0 * 4 + hd];
 #pragma unroll
     for (int hf = 0; hf < NE / 4; ++hf) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(ob + s0 * stride + 128 * hf));
+      const float4 v = ld_cg_f4(ob + s0 * stride + 128 * hf);
       o[4 * hf + 0] = fmaf(f, v.x, o[4 * hf + 0]);
       o[4 * hf + 1] = fmaf(f, v.y, o[4 * hf + 1]);
       o[4 * hf + 2] = fmaf(f, v.z, o[4 * hf + 2]);
@@ -518,9 +576,8 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   const float rs = rsqrtf((float)D);
 #pragma unroll
   for (int e = 0; e < NE; ++e) o[e] *= rs * lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
-  const float* rp = base + nsp * stride;
   const float m = M[hd];
-  const float mr = __ldcg(rp + hd), lr = __ldcg(rp + kMaxG + hd);
+  const float mr = mrp, lr = lrp;
   const float mm = fmaxf(m, mr);
   const float fh = (m == -INFINITY) ? 0.f : exp2f(m - mm);
   const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mm);
@@ -529,7 +586,7 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float* out = a.out + ((size_t)b * lv.Hq + h * lv.G + hd) * D;
 #pragma unroll
   for (int hf = 0; hf < NE / 4; ++hf) {
-    const float4 rv = __ldcg(reinterpret_cast<const float4*>(rp + 2 * kMaxG + hd * D + 128 * hf + 4 * lane));
+    const float4 rv = rvp[hf];
     float4 r;
     r.x = (fh * o[4 * hf + 0] + fr * rv.x) * inv;
     r.y = (fh * o[4 * hf + 1] + fr * rv.y) * inv;
@@ -845,23 +902,29 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     }
   }
   __syncthreads();
-  for (int i = tid; i < kMaxG * D; i += NT) {
-    const int hd = i / D, j = i % D;
+  float* wf = wo + NGRP * 4 * D;  // [NGRP][4] group weights exp2(m_group - m)
+  if (tid < 4 * NGRP) {
+    const int hd = tid & 3, w = tid >> 2;
     float m = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NGRP; ++w) m = fmaxf(m, wm[w * 4 + hd]);
-    float o = 0.f, l = 0.f;
-    if (m != -INFINITY) {
+    for (int v = 0; v < NGRP; ++v) m = fmaxf(m, wm[v * 4 + hd]);
+    const float mw = wm[w * 4 + hd];
+    wf[w * 4 + hd] = (m == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - m);
+  }
+  __syncthreads();
+  for (int i = tid; i < kMaxG * D; i += NT) {
+    const int hd = i / D, j = i % D;
+    float o = 0.f;
 #pragma unroll
-      for (int w = 0; w < NGRP; ++w) {
-        const float mw = wm[w * 4 + hd];
-        const float f = mw == -INFINITY ? 0.f : exp2f(mw - m);
-        o += f * wo[(w * 4 + hd) * D + j];
-        l += f * wl[w * 4 + hd];
-      }
-    }
+    for (int w = 0; w < NGRP; ++w) o = fmaf(wf[w * 4 + hd], wo[(w * 4 + hd) * D + j], o);
     part[2 * kMaxG + hd * D + j] = o;
     if (j == 0) {
+      float m = -INFINITY, l = 0.f;
+#pragma unroll
+      for (int w = 0; w < NGRP; ++w) {
+        m = fmaxf(m, wm[w * 4 + hd]);
+        l = fmaf(wf[w * 4 + hd], wl[w * 4 + hd], l);
+      }
       part[hd] = m;
       part[kMaxG + hd] = l;
     }
@@ -879,7 +942,7 @@ size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB);
   constexpr int NT = decode_threads<D>();
   constexpr int NGRP = 4 * decode_streams<D>();
-  const size_t merge_bytes = sizeof(float) * (8 * NGRP + 4 * NGRP * D);
+  const size_t merge_bytes = sizeof(float) * (12 * NGRP + 4 * NGRP * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
   size_t smem = 128 + (size_t)decode_streams<D>() * decode_stages<D, VB>() * pl.bytes + xbuf_bytes +
                 prep_scratch_bytes<D>();
