@@ -452,6 +452,24 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
   return false;
 }
 
+// Rotation of the K and V tiles of one page (buffer at smem address buf) by the tensor cores:
+// D[t][i] = sum_j x[t][j] (H D)[i][j], K into TMEM columns [0, 128) of `tcol`, V into [128, 256).
+__device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar) {
+  tc_fence_after();
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+    umma_bf16(tcol, umma_desc_sw128(buf + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128, ks > 0);
+  }
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+    umma_bf16(tcol + 128, umma_desc_sw128(buf + 32768 + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128,
+              ks > 0);
+  }
+  umma_commit(bar);
+}
+
 // Next task (>= task, stepping by the grid) that has a page to write, or ntasks.
 __device__ __forceinline__ int bulk128_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, int& b,
                                             int& h, int& slot, int& L, int& Np, int& pg) {
@@ -473,26 +491,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* vcode = sm + kQbVcode;
   uint64_t* bar_tab = reinterpret_cast<uint64_t*>(sm + kQbBar);
-  uint64_t* bar_rot = bar_tab + 1;
-  uint64_t* bar_qjl = bar_tab + 2;
-  uint64_t* bar_ld = bar_tab + 3;  // [2]: page loads into buffer 0 / 1
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 5);
+  uint64_t* bar_qjl = bar_tab + 1;
+  uint64_t* bar_ld = bar_tab + 2;   // [2]: page loads into buffer 0 / 1
+  uint64_t* bar_rot = bar_tab + 4;  // [2]: rotations into TMEM half 0 / 1
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 6);
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
   pdl_launch();
   if (tid == 0) {
-    mbar_init(bar_tab, 1);
-    mbar_init(bar_rot, 1);
-    mbar_init(bar_qjl, 1);
-    mbar_init(bar_ld, 1);
-    mbar_init(bar_ld + 1, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(bar_tab + i, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(bar_tab, 4u * D * D);
     bulk_g2s(sm + kQbHD, lv.HD_sw, 2u * D * D, bar_tab);
     bulk_g2s(sm + kQbS, lv.S_sw, 2u * D * D, bar_tab);
   }
-  if (warp == 0) {  // 512 TMEM columns: rotated K (0..127), rotated V (128..255), z = S r (256..383)
+  if (warp == 0) {  // 512 TMEM columns: two halves of [rotated K (then z = S r) | rotated V], by page parity
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
@@ -507,8 +521,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int cur = bulk128_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
   bool tma_cur = cur < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld);
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   bool ok = __syncthreads_and(mbar_wait(bar_tab, 0)) != 0;
-  uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;  // ph_ld: bit i = parity of the next wait on bar_ld[i]
+  // parities of the next wait: bit i of ph_ld / ph_rot for buffer / TMEM half i
+  uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;
+  // The rotation of a page runs on the tensor cores while the previous page is coded: it is issued
+  // here for the first page and, for each later page, once the page before it has issued its QJL MMAs.
+  if (ok && cur < ntasks && tid == 0) {
+    if (tma_cur && !mbar_wait(bar_ld, 0)) ok = false;
+    if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot);
+  }
+  if (tma_cur) ph_ld ^= 1u;
+  ok = __syncthreads_and(ok) != 0;
   // warp roles: key path (warps 0-7) or value path (8-15); in each, warp w covers TMEM lane quarter
   // w % 4 (tokens 32 (w % 4) + lane) and column half (w % 8) / 4
   const bool kpath = warp < 8;
@@ -522,38 +546,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int cslot = slot, chead = h, cpg = pg;
     const int nxt = bulk128_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
     const uint32_t buf = buf0 + bufi * 65536u;
+    // the next page's rows stream into the other buffer while this page is coded
     const bool tma_nxt =
         nxt < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
                                      bar_ld + (bufi ^ 1u));
-    if (tma_cur) {  // this page's rows have landed
-      ok = mbar_wait(bar_ld + bufi, (ph_ld >> bufi) & 1u);
-      ph_ld ^= 1u << bufi;
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    if (tid == 0) {  // rotation of K and V: D[t][i] = sum_j x[t][j] (H D)[i][j]
-      tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tmem, umma_desc_sw128(buf + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128, ks > 0);
-      }
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(tmem + 128, umma_desc_sw128(buf + 32768 + koff), umma_desc_sw128(hd_addr + koff),
-                  kIdescBf16M128N128, ks > 0);
-      }
-      umma_commit(bar_rot);
-    }
-    ok = __syncthreads_and(mbar_wait(bar_rot, ph_rot)) != 0;
-    ph_rot ^= 1;
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied pages -> tensor cores
+    ok = __syncthreads_and(mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u)) != 0;
+    ph_rot ^= 1u << bufi;
     if (!ok) break;
     tc_fence_after();
     uint8_t* page = lv.pages + (((size_t)cslot * lv.Hkv + chead) * lv.max_pages + cpg) * lv.page_bytes;
     const PageLayout pl = page_layout(D, lv.vb);
-    const uint32_t lrow = tmem + ((uint32_t)(32 * q4) << 16);
+    const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
     if (kpath) {
       // ---- keys, two threads per token (64 coordinates each): |y'|, y = y' / |y'|, index, residual ----
@@ -625,15 +629,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_barrier(1, 256);
       uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
       const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
-      if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo)
+      if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
           const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32 + (ks >> 3) * 32768;
-          umma_bf16(tmem + 256, umma_desc_sw128(buf + koff), umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32),
-                    kIdescBf16M128N128, ks > 0);
+          umma_bf16(tmem + 256u * bufi, umma_desc_sw128(buf + koff),
+                    umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
         }
         umma_commit(bar_qjl);
+        // then the rotation of the next page into the other TMEM half (its page finished last iteration)
+        if (nxt < ntasks) {
+          bool landed = true;
+          if (tma_nxt) {
+            landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
+            if (!landed) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+          }
+          if (landed) bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u));
+        }
       }
       if (!half) {  // planes 0-1, n and gamma of token t
         const float n = nrot * rsqrtf((float)D);
@@ -653,7 +666,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         uint32_t z[32];
-        tmem_ld32(lrow + 256 + 64 * half + 32 * cc, z);
+        tmem_ld32(lrow + 64 * half + 32 * cc, z);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int jl = 32 * cc + i;
@@ -760,6 +773,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     ph_qjl ^= kpath ? 1u : 0u;
+    if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);  // waited on by thread 0 above
     tc_fence_before();
     ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, vcode and exchange may be reused
     tc_fence_after();
@@ -767,7 +781,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tma_cur = tma_nxt;
     bufi ^= 1u;
   }
-  if (ok && tma_cur) mbar_wait(bar_ld + bufi, (ph_ld >> bufi) & 1u);  // no copy in flight at exit
   if (!ok && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
