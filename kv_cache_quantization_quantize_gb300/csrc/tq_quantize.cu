@@ -88,11 +88,14 @@ __device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int
   return true;
 }
 
-// Quantises page pg of (row b, KV head h): its first `valid` tokens come from the ring (positions
-// below L) and then from the new input. Run by all kQThreads threads of the CTA.
+// Quantises the 32-token block q32 of page pg of (row b, KV head h): the page's first `valid` tokens
+// come from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
+// zero vectors. A 32-token block owns whole words of every page section, so four CTAs can write the
+// four blocks of one page independently. Run by all kQThreads threads of the CTA.
 template <int D>
 __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
-                                                  int valid, uint8_t* smem) {
+                                                  int valid, int q32, uint8_t* smem) {
+  const int t0 = 32 * q32, t1 = t0 + 32;
   constexpr int NE = D / 32;  // coordinates per lane
   uint32_t* st2 = reinterpret_cast<uint32_t*>(smem);                    // S^T as bf16 pairs [D][D/2]
   uint8_t* kcode = smem + 2 * D * D;                                    // [128][D]: idx | sign << 2
@@ -120,7 +123,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
   const int vb = lv.vb, vhalf = 1 << (vb - 1);
   const float inv_sqrt_d = rsqrtf((float)D);
   float* r = rbuf + warp * D;
-  for (int t = warp; t < kPage; t += kQThreads / 32) {
+  for (int t = t0 + warp; t < t1; t += kQThreads / 32) {
     const int pos = pg * kPage + t;
     float x[NE], y[NE];
     if (t < valid) {
@@ -235,7 +238,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   constexpr int HALVES = D / 128;
-  for (int w = tid; w < 8 * 3 * HALVES * 32 * 2; w += kQThreads) {
+  for (int w = (t0 / 16) * 192 * HALVES + tid; w < (t1 / 16) * 192 * HALVES; w += kQThreads) {
     const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % 3;
     const int tile = w / (192 * HALVES);
     const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
@@ -254,10 +257,10 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     kw[w] = word;
   }
   uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
-  for (int t = tid; t < kPage; t += kQThreads) nw[t] = norms[t];
+  for (int t = t0 + tid; t < t1; t += kQThreads) nw[t] = norms[t];
   uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
   if (vb == 2) {
-    for (int w = tid; w < 4 * (D / 16) * 32; w += kQThreads) {
+    for (int w = q32 * (D / 16) * 32 + tid; w < (q32 + 1) * (D / 16) * 32; w += kQThreads) {
       const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
       const int g = ln >> 2, c = ln & 3;
       uint32_t word = 0;
@@ -274,7 +277,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
       vw[w] = word;
     }
   } else {
-    for (int w = tid; w < 4 * (D / 16) * 32 * 2; w += kQThreads) {
+    for (int w = q32 * (D / 16) * 64 + tid; w < (q32 + 1) * (D / 16) * 64; w += kQThreads) {
       const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
       const int g = ln >> 2, c = ln & 3;
       uint32_t word = 0;
@@ -290,7 +293,8 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     }
   }
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
-  for (int i = tid; i < kPage * (D / 32); i += kQThreads) sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
+  for (int i = t0 * (D / 32) + tid; i < t1 * (D / 32); i += kQThreads)
+    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
 }
 
 template <int D>
@@ -300,23 +304,27 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
   pdl_launch();
   int slot, L, Np, pg, valid;
-  if (!page_task(a, b, blockIdx.z, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
-  quantize_page_cta<D>(a, b, h, slot, L, Np, pg, valid, smem);
+  const int j = blockIdx.z >> 2;  // 4 CTAs per page, one per 32-token block
+  if (!page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
+  quantize_page_cta<D>(a, b, h, slot, L, Np, pg, valid, blockIdx.z & 3, smem);
 }
 
-// Appends of fewer than 128 tokens per row in one launch: CTA (row b, KV head h) packs the page that
-// completes when the ring overflows (at most one), then writes head h's new ring rows. The last CTA
-// of the row to arrive publishes the new length. Dependents (the decode) are released only after
-// that, so they may read the state before their own stream wait.
+// Appends of fewer than 128 tokens per row in one launch. CTA (row b, KV head h, block q) codes
+// 32-token block q of the page that a ring overflow completes (if any). The last of the row's
+// 4 Hkv CTAs to arrive writes the new ring rows of every head (all CTAs have read the old ones by
+// then) and publishes the new length. Dependents (the decode) are released only after that, so they
+// may read the state before their own stream wait.
 template <int D>
 __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
-  const int b = blockIdx.x, h = blockIdx.y, tid = threadIdx.x;
+  __shared__ int s_last;
+  const int b = blockIdx.x, h = blockIdx.y, q32 = blockIdx.z, tid = threadIdx.x;
   pdl_wait();  // sequence state, ring and inputs come from earlier work on the stream
   const LayerView& lv = a.lv;
   const int slot = a.seq_ids[b];
+  const bool first = h == 0 && q32 == 0 && tid == 0;
   if (slot < 0 || slot >= lv.max_seqs) {
-    if (h == 0 && tid == 0) set_status(lv.status, TQ_DEV_ERR_SEQ_ID);
+    if (first) set_status(lv.status, TQ_DEV_ERR_SEQ_ID);
     return;
   }
   const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
@@ -324,42 +332,50 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   const int nn = a.n_new[b];
   const int L2 = L + nn;
   if (nn < 0 || nn > a.max_new || L2 > lv.max_ctx) {
-    if (h == 0 && tid == 0) set_status(lv.status, TQ_DEV_ERR_CAPACITY);
+    if (first) set_status(lv.status, TQ_DEV_ERR_CAPACITY);
     return;
   }
   const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
-  if (Np2 > Np) quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, smem);  // Np2 - Np == 128
-  __syncthreads();  // the page read the old ring rows of head h
-  const int p0 = max(L, Np2);
-  const int d = lv.d, q4 = d / 4;
-  const int n_items = (L2 - p0) * 2 * q4;  // (pos, which, quad) of head h
-  for (int it = tid; it < n_items; it += blockDim.x) {
-    const int quad = it % q4, which = (it / q4) & 1, pos = p0 + it / (2 * q4);
-    const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + h) * d + 4 * quad;
-    uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + h) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
-    const void* base = which ? a.v : a.k;
-    uint2 out;
-    if (a.dt == 0) {
-      out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
-    } else {
-      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
-      out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
-      out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
-    }
-    *reinterpret_cast<uint2*>(dst) = out;
-  }
-  __syncthreads();
+  if (Np2 > Np) quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, q32, smem);  // Np2 - Np == 128
+  __syncthreads();  // this CTA has read the old ring rows it needed
   if (tid == 0) {
     __threadfence();
     const int old = atomicAdd(lv.acnt + slot, 1);
-    if (old == lv.Hkv - 1) {  // every head of the row is done with the old state
+    s_last = old == 4 * lv.Hkv - 1;
+  }
+  __syncthreads();
+  if (s_last) {
+    const int p0 = max(L, Np2);
+    const int d = lv.d, q4 = d / 4;
+    const int n_items = (L2 - p0) * lv.Hkv * 2 * q4;  // (pos, head, which, quad)
+    for (int it = tid; it < n_items; it += blockDim.x) {
+      const int quad = it % q4;
+      int rest = it / q4;
+      const int which = rest & 1;
+      rest >>= 1;
+      const int hh = rest % lv.Hkv, pos = p0 + rest / lv.Hkv;
+      const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + hh) * d + 4 * quad;
+      uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + hh) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
+      const void* base = which ? a.v : a.k;
+      uint2 out;
+      if (a.dt == 0) {
+        out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
+      } else {
+        const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
+        out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
+        out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
+      }
+      *reinterpret_cast<uint2*>(dst) = out;
+    }
+    __syncthreads();
+    if (tid == 0) {
       lv.acnt[slot] = 0;
       lv.state[2 * slot] = L2;
       lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
       __threadfence();
     }
+    __syncthreads();
   }
-  __syncthreads();
   pdl_launch();
 }
 
@@ -872,7 +888,8 @@ cudaError_t launch_quantize_d(const AppendArgs& a, int batch, int pages, cudaStr
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  dim3 grid(batch, a.lv.Hkv, pages);
+  if (pages > 65535 / 4) return cudaErrorInvalidValue;  // grid z holds four 32-token CTAs per page
+  dim3 grid(batch, a.lv.Hkv, 4 * pages);
   return launch_pdl(k_quantize_pages<D>, grid, dim3(kQThreads), smem, s, a);
 }
 
@@ -884,7 +901,7 @@ cudaError_t launch_append_small_d(const AppendArgs& a, int batch, size_t smem, c
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(k_append_small<D>, dim3(batch, a.lv.Hkv), dim3(kQThreads), smem, s, a);
+  return launch_pdl(k_append_small<D>, dim3(batch, a.lv.Hkv, 4), dim3(kQThreads), smem, s, a);
 }
 
 cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
