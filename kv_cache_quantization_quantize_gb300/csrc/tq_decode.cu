@@ -102,6 +102,7 @@ __host__ __device__ constexpr int decode_xbuf_floats() {
 
 // Split CTAs run `decode_streams` independent page streams of 4 token-group warps x (d/128) coordinate
 // halves: 3 streams (12 warps, one CTA per SM) for head_dim 128, 1 stream (8 warps) for head_dim 256.
+// (Four streams of 16 warps measured slower at batch 1 and no faster at batch 32.)
 template <int D>
 __host__ __device__ constexpr int decode_streams() {
   return D == 128 ? 3 : 1;
@@ -163,15 +164,13 @@ __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f)
 // represented (rounded) operands, i.e. the +-1 offsets of the bit planes.
 template <int D, int NT>
 __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
-                                           uint2 (&bq)[3][8], float (&um)[2], float (&cm)[2], float (&uq)[2],
-                                           float (&cq)[2]) {
+                                           float (&um)[2], float (&cm)[2], float (&uq)[2], float (&cq)[2]) {
   constexpr int NE = D / 32;
   constexpr int HALVES = D / 128;
   constexpr int MT = D / 16;
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
-  const int hf = (warp % (4 * HALVES)) >> 2;  // coordinate half of this warp within its page stream
   const int G = lv.G;
   const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
   float* qr = ps;               // [4][D]
@@ -274,10 +273,6 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     atomicAdd(&sums[4 + g], sum_q);
   }
   __syncthreads();
-#pragma unroll
-  for (int pi = 0; pi < 3; ++pi)
-#pragma unroll
-    for (int s = 0; s < 8; ++s) bq[pi][s] = frag[((hf * 3 + pi) * 8 + s) * 32 + lane];
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
 #pragma unroll
   for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd
@@ -683,9 +678,12 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   SFrag<D> sfrag;
   sfrag_prefetch<D>(lv, sfrag);
   pdl_wait();  // earlier work on the stream (q, and the partials of any decode that shares ws) is done
-  uint2 bq[3][8];
   float um[2], cm[2], uq[2], cq[2];
-  query_prep<D, NT>(a, b, h, reinterpret_cast<float*>(xbuf + decode_xbuf_floats<D>()), sfrag, bq, um, cm, uq, cq);
+  float* ps = xbuf + decode_xbuf_floats<D>();
+  query_prep<D, NT>(a, b, h, ps, sfrag, um, cm, uq, cq);
+  // f16 B fragments of the key MMAs for this warp's coordinate half, [plane][k-step][lane] in shared
+  // memory (written by query_prep; read once per page and k-step, shared by both tiles)
+  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * 24 * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
   const int G = lv.G;
   bool colok[2];
@@ -724,13 +722,15 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
       const int q0 = s < 6 ? 2 * s : 2 * s - 4;
       const uint32_t m0 = 0x00010001u << q0, m1 = 0x00010001u << (q0 + 1);
 #pragma unroll
-      for (int pi = 0; pi < 3; ++pi)
+      for (int pi = 0; pi < 3; ++pi) {
+        const uint2 bv = bfr[(pi * 8 + s) * 32];
 #pragma unroll
         for (int kap = 0; kap < 2; ++kap) {
           const uint32_t x0 = s < 6 ? kwv[kap][pi].x : kwv[kap][pi].x >> 4;
           const uint32_t x1 = s < 6 ? kwv[kap][pi].y : kwv[kap][pi].y >> 4;
-          mma_f16(acc[kap][pi], x0 & m0, x1 & m0, x0 & m1, x1 & m1, bq[pi][s].x, bq[pi][s].y);
+          mma_f16(acc[kap][pi], x0 & m0, x1 & m0, x0 & m1, x1 & m1, bv.x, bv.y);
         }
+      }
     }
 #pragma unroll
     for (int kap = 0; kap < 2; ++kap) {
