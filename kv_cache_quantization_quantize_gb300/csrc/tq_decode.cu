@@ -433,90 +433,60 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
 
 // =============================================================================================
 // Combine: LSE merge of history splits (rotated basis) -> Pi^T -> exact merge with the ring split.
-// Run by the last CTA of a (row, KV head) to finish its partial; warp w merges query head w.
+// Run by the last CTA of a (row, KV head) to finish its partial. Warp w merges query head w on its
+// own (no block barrier): lanes take the splits' (m, l), the weights go through shared memory column w.
 // =============================================================================================
 template <int D, int NT>
 __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, float* sm) {
   constexpr int NE = D / 32;
-  constexpr int NW = NT / 32;
   const LayerView& lv = a.lv;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp >= lv.G) return;
+  const int hd = warp;  // query head; lane holds coordinates 4*lane+e (+128)
   const int nsp = a.plan.n_splits;
   const size_t stride = a.plan.part_stride / sizeof(float);
   const float* base = reinterpret_cast<const float*>(a.ws + a.plan.part_off +
                                                      ((size_t)b * lv.Hkv + h) * (nsp + 1) * a.plan.part_stride);
-  float* red = sm;                      // [NW][4]
-  float* fs = sm + 4 * NW;              // [nsp][4] split maxima, then split weights
-  float* ls = fs + 4 * (nsp + 1);       // [nsp][4] split sums
-  // 0. warps 0..G-1 (query head = warp) start loading the outputs of the first 16 splits and the ring
-  //    partial now: they do not depend on the weights, so they share the round trip of the (m, l) loads
-  constexpr int PRE = D == 128 ? 16 : 8;
-  const int hdw = warp;
-  const bool merger = warp < lv.G;
-  const float* ob = base + 2 * kMaxG + hdw * D + 4 * lane;
+  float* fs = sm;                   // [nsp][4] split maxima, then split weights (column hd is this warp's)
+  float* ls = fs + 4 * (nsp + 1);   // [nsp][4] split sums
+  // 0. the outputs of the first PRE splits and the ring partial do not depend on the weights: their
+  //    loads share the round trip of the (m, l) loads
+  constexpr int PRE = D == 128 ? 20 : 8;
+  const float* ob = base + 2 * kMaxG + hd * D + 4 * lane;
   const float* rp = base + nsp * stride;
   float4 vpre[PRE][NE / 4], rvp[NE / 4];
-  float mrp = -INFINITY, lrp = 0.f;
-  if (merger) {
 #pragma unroll
-    for (int u = 0; u < PRE; ++u)
+  for (int u = 0; u < PRE; ++u)
 #pragma unroll
-      for (int hf = 0; hf < NE / 4; ++hf) {
-        vpre[u][hf] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (u < nsp) vpre[u][hf] = ld_cg_f4(ob + u * stride + 128 * hf);
-      }
-#pragma unroll
-    for (int hf = 0; hf < NE / 4; ++hf)
-      rvp[hf] = ld_cg_f4(rp + 2 * kMaxG + hdw * D + 128 * hf + 4 * lane);
-    mrp = ld_cg_f(rp + hdw);
-    lrp = ld_cg_f(rp + kMaxG + hdw);
-  }
-  // 1. one pass over the splits' (m, l): kept in shared memory; block-wide max per head
-  float mloc[kMaxG] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-  for (int s = tid; s < nsp; s += NT) {
-    const float4 m4 = ld_cg_f4(base + s * stride);
-    const float4 l4 = ld_cg_f4(base + s * stride + kMaxG);
-    *reinterpret_cast<float4*>(fs + 4 * s) = m4;
-    *reinterpret_cast<float4*>(ls + 4 * s) = l4;
-    mloc[0] = fmaxf(mloc[0], m4.x);
-    mloc[1] = fmaxf(mloc[1], m4.y);
-    mloc[2] = fmaxf(mloc[2], m4.z);
-    mloc[3] = fmaxf(mloc[3], m4.w);
-  }
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) mloc[g] = warp_max(mloc[g]);
-  if (lane < kMaxG) red[warp * 4 + lane] = mloc[lane];
-  __syncthreads();
-  float M[kMaxG];
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) {
-    float m = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) m = fmaxf(m, red[w * 4 + g]);
-    M[g] = m;
-  }
-  __syncthreads();
-  // 2. per-split weights (in place of the maxima) and the weighted sum of l
-  float lloc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
-  for (int s = tid; s < nsp; s += NT) {
-#pragma unroll
-    for (int g = 0; g < kMaxG; ++g) {
-      const float mv = fs[4 * s + g];
-      const float f = mv == -INFINITY ? 0.f : exp2f(mv - M[g]);
-      fs[4 * s + g] = f;
-      lloc[g] = fmaf(f, ls[4 * s + g], lloc[g]);
+    for (int hf = 0; hf < NE / 4; ++hf) {
+      vpre[u][hf] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (u < nsp) vpre[u][hf] = ld_cg_f4(ob + u * stride + 128 * hf);
     }
+#pragma unroll
+  for (int hf = 0; hf < NE / 4; ++hf) rvp[hf] = ld_cg_f4(rp + 2 * kMaxG + hd * D + 128 * hf + 4 * lane);
+  const float mr = ld_cg_f(rp + hd), lr = ld_cg_f(rp + kMaxG + hd);
+  float dsg[NE];  // the rotation signs of this lane's coordinates (constant table)
+#pragma unroll
+  for (int e = 0; e < NE; ++e) dsg[e] = lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
+  // 1. the splits' (m, l) of this head across the lanes; maximum, weights and the weighted sum of l
+  float mloc = -INFINITY;
+  for (int s = lane; s < nsp; s += 32) {
+    const float mv = ld_cg_f(base + s * stride + hd), lv2 = ld_cg_f(base + s * stride + kMaxG + hd);
+    fs[4 * s + hd] = mv;
+    ls[4 * s + hd] = lv2;
+    mloc = fmaxf(mloc, mv);
   }
-#pragma unroll
-  for (int g = 0; g < kMaxG; ++g) lloc[g] = warp_sum(lloc[g]);
-  if (lane < kMaxG) red[warp * 4 + lane] = lloc[lane];
-  __syncthreads();
-  if (warp >= lv.G) return;
-  const int hd = warp;  // warps 0..G-1 merge query head = warp; lane holds coordinates 4*lane+e (+128)
-  float l = 0.f;
-#pragma unroll
-  for (int w = 0; w < NW; ++w) l += red[w * 4 + hd];
-  // 3. weighted sum of the split outputs: the prefetched 16, then 16 splits' loads in flight at a time
+  const float m = warp_max(mloc);
+  float lloc = 0.f;
+  for (int s = lane; s < nsp; s += 32) {
+    const float mv = fs[4 * s + hd];
+    const float f = mv == -INFINITY ? 0.f : exp2f(mv - m);
+    fs[4 * s + hd] = f;
+    lloc = fmaf(f, ls[4 * s + hd], lloc);
+  }
+  const float l = warp_sum(lloc);
+  __syncwarp();
+  // 2. weighted sum of the split outputs: the prefetched PRE, then 16 splits' loads in flight at a time
   float o[NE], o2[NE];
 #pragma unroll
   for (int e = 0; e < NE; ++e) o[e] = o2[e] = 0.f;
@@ -566,13 +536,11 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   }
 #pragma unroll
   for (int e = 0; e < NE; ++e) o[e] += o2[e];
-  // 4. Pi^T o = D * (H o) / sqrt(d), then the exact merge with the ring split
+  // 3. Pi^T o = D * (H o) / sqrt(d), then the exact merge with the ring split
   warp_fwht<NE>(o, lane);
   const float rs = rsqrtf((float)D);
 #pragma unroll
-  for (int e = 0; e < NE; ++e) o[e] *= rs * lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
-  const float m = M[hd];
-  const float mr = mrp, lr = lrp;
+  for (int e = 0; e < NE; ++e) o[e] *= rs * dsg[e];
   const float mm = fmaxf(m, mr);
   const float fh = (m == -INFINITY) ? 0.f : exp2f(m - mm);
   const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mm);
@@ -592,21 +560,22 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
 }
 
 // After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
-// merges all of them (threadfence reduction; no CTA waits on another).
+// merges all of them (an arrival counter; no CTA waits on another).
 template <int D, int NT>
 __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem) {
   __shared__ int s_last;
-  __syncthreads();
+  __syncthreads();  // every thread's part of the partial is written
   if (threadIdx.x == 0) {
-    __threadfence();
+    // acq_rel at gpu scope: releases this CTA's partial (ordered before by the barrier) and, in the
+    // last CTA, acquires every other CTA's
     int* cnt = reinterpret_cast<int*>(a.ws + a.plan.cnt_off) + b * a.lv.Hkv + h;
-    const int old = atomicAdd(cnt, 1);
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(cnt) : "memory");
     s_last = old == a.plan.n_splits;
     if (s_last) *cnt = 0;  // ready for the next call
   }
   __syncthreads();
   if (!s_last) return;
-  __threadfence();
   combine_unit<D, NT>(a, b, h, reinterpret_cast<float*>(smem + 128));
 }
 
