@@ -64,7 +64,11 @@ typedef struct tq_config {
   int32_t key_bits;    /* 3 */
   int32_t value_bits;  /* 2 or 4 ([Guide] §二 step 4) */
   int32_t value_group; /* 32 ([Guide] §二 step 4) */
-  int32_t ring_size;   /* 128: exact recent buffer ([Guide] §五.1 buffer_size=128) */
+  int32_t ring_size;   /* 128: hybrid mode, exact recent buffer ([Guide] §五.1 buffer_size=128);
+                        * 0: full_tq mode ([Guide] §三): every token is quantised by its append and decode
+                        * reads only packed tokens. The bf16 ring is still allocated, as a staging copy of
+                        * the current block: each append codes the 32-token blocks that hold its new tokens
+                        * (older tokens of such a block again, with identical codes) and publishes F = L - Np. */
   int32_t n_layers;
   int32_t n_kv_heads;
   int32_t n_q_heads;   /* multiple of n_kv_heads, with n_q_heads / n_kv_heads in {1, 2, 4} (GQA) */
@@ -118,7 +122,7 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
  *   - A row that would exceed max_ctx is skipped and sets TQ_DEV_ERR_CAPACITY.
  *   - Launches: for max_new < 128, one kernel (the page that an overflow completes, the ring rows and
  *     the new length); otherwise one quantize kernel over the pages to write, then one ring-update
- *     kernel. */
+ *     kernel (in full_tq mode followed by the two launches of tq_ring_flush). */
 tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
                              const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
                              tq_stream_t stream);

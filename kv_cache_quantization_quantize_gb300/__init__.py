@@ -14,10 +14,14 @@ from ._abi import TQConfig, TQError, check, load, TQ_BF16, TQ_F32
 __all__ = ["TQConfig", "TQError", "TurboQuantCache", "HostTables", "load", "config"]
 
 
-def config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0):
-    return TQConfig(head_dim=head_dim, key_bits=3, value_bits=value_bits, value_group=32, ring_size=128,
-                    n_layers=n_layers, n_kv_heads=n_kv_heads, n_q_heads=n_q_heads, max_seqs=max_seqs,
-                    max_ctx=max_ctx, seed=seed)
+def config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0,
+           mode="hybrid"):
+    """mode "hybrid": 128-token exact recent buffer; "full_tq": every token quantised (ring_size 0)."""
+    if mode not in ("hybrid", "full_tq"):
+        raise ValueError(f"mode {mode!r}: expected 'hybrid' or 'full_tq'")
+    return TQConfig(head_dim=head_dim, key_bits=3, value_bits=value_bits, value_group=32,
+                    ring_size=128 if mode == "hybrid" else 0, n_layers=n_layers, n_kv_heads=n_kv_heads,
+                    n_q_heads=n_q_heads, max_seqs=max_seqs, max_ctx=max_ctx, seed=seed)
 
 
 def _stream(stream=None):

@@ -72,7 +72,8 @@ tq_status validate(const tq_config* c) {
   if (c->value_bits != 2 && c->value_bits != 4)
     return fail(TQ_ERR_UNSUPPORTED, "value_bits %d: supported 2, 4", c->value_bits);
   if (c->value_group != 32) return fail(TQ_ERR_UNSUPPORTED, "value_group %d: supported 32", c->value_group);
-  if (c->ring_size != tq::kPage) return fail(TQ_ERR_UNSUPPORTED, "ring_size %d: supported 128", c->ring_size);
+  if (c->ring_size != tq::kPage && c->ring_size != 0)
+    return fail(TQ_ERR_UNSUPPORTED, "ring_size %d: supported 128 (hybrid) and 0 (full_tq)", c->ring_size);
   if (c->n_layers < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 || c->max_seqs < 1 || c->max_ctx < 1)
     return fail(TQ_ERR_INVALID_ARG, "n_layers, n_kv_heads, n_q_heads, max_seqs, max_ctx must be >= 1");
   if (c->n_q_heads % c->n_kv_heads != 0)

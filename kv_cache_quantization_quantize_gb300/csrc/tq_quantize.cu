@@ -26,6 +26,7 @@ struct AppendArgs {
   const int32_t* n_new;
   int max_new;
   int flush;  // 1: quantise the current ring block (tq_ring_flush)
+  int full;   // 1: full_tq mode (ring_size 0): every appended token is quantised by the append itself
 };
 
 // Load 4 consecutive coordinates of one token of the source stream (ring bf16 or input bf16/f32).
@@ -336,7 +337,20 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
     return;
   }
   const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
-  if (Np2 > Np) quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, q32, smem);  // Np2 - Np == 128
+  if (a.full) {
+    // full_tq: every 32-token block that holds a new token is coded again, its older tokens from the
+    // ring (pages hold each token's code, so they come out identical) and the new ones from the input;
+    // tokens past L2 are coded as zero vectors until they arrive. A page that this append enters is
+    // coded to its end, so that decode never reads a block that no append has written.
+    const int end_blk = Np2 >= L ? Np2 / 32 + 3 : (L2 - 1) / 32;
+    for (int blk = L / 32 + q32; blk <= end_blk; blk += 4) {
+      const int pg = blk / 4;
+      quantize_page_cta<D>(a, b, h, slot, L, Np, pg, min(kPage, L2 - pg * kPage), blk & 3, smem);
+      __syncthreads();  // shared memory is staged again by the next block
+    }
+  } else if (Np2 > Np) {
+    quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, q32, smem);  // Np2 - Np == 128
+  }
   __syncthreads();  // this CTA has read the old ring rows it needed
   if (tid == 0) {
     __threadfence();
@@ -371,7 +385,7 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
     if (tid == 0) {
       lv.acnt[slot] = 0;
       lv.state[2 * slot] = L2;
-      lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
+      lv.state[2 * slot + 1] = a.full ? L2 - Np2 : (Np2 > Np ? 0 : F);
       __threadfence();
     }
     __syncthreads();
@@ -960,6 +974,7 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.n_new = n_new;
   a.max_new = max_new;
   a.flush = 0;
+  a.full = ctx->cfg.ring_size == 0;
   if (max_new < kPage) {  // decode-sized appends: one launch (page on ring overflow + ring rows + state)
     const size_t smem = a.lv.d == 128 ? quantize_smem_bytes<128>() : quantize_smem_bytes<256>();
     return a.lv.d == 128 ? launch_append_small_d<128>(a, batch, smem, s) : launch_append_small_d<256>(a, batch, smem, s);
@@ -969,7 +984,9 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
                       : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_ring_update, dim3(batch), dim3(256), 0, s, a);
+  e = launch_pdl(k_ring_update, dim3(batch), dim3(256), 0, s, a);
+  if (e != cudaSuccess || !a.full) return e;
+  return launch_flush(ctx, layer, seq_ids, batch, s);  // full_tq: the partial page too
 }
 
 cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s) {
@@ -981,6 +998,7 @@ cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
   a.n_new = nullptr;
   a.max_new = 0;
   a.flush = 1;
+  a.full = 0;
   cudaError_t e = launch_quantize(a, batch, 1, s);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_ring_update, dim3(batch), dim3(32), 0, s, a);

@@ -137,9 +137,15 @@ def cos_sim_report(k, v, key_rec, val_rec, D, S, centroids):
 
 
 def history_split(L, ring=RING):
-    """(packed, ring) token counts of a sequence of length L: whole ring blocks are flushed when full."""
+    """(packed, ring) token counts of a sequence of length L: whole ring blocks are flushed when full.
+
+    ring = 0 is the full_tq mode of [Guide] §三 (read as: no exact recent buffer, every token is
+    quantised as it arrives), so all L tokens are packed.
+    """
     if L <= 0:
         return 0, 0
+    if ring == 0:
+        return L, 0
     packed = ring * ((L - 1) // ring)
     return packed, L - packed
 

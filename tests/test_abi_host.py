@@ -32,6 +32,7 @@ def test_library_exports_every_header_function():
     ("head_dim", 64, _abi.TQ_ERR_UNSUPPORTED), ("head_dim", 96, _abi.TQ_ERR_UNSUPPORTED),
     ("value_bits", 3, _abi.TQ_ERR_UNSUPPORTED), ("key_bits", 4, _abi.TQ_ERR_UNSUPPORTED),
     ("value_group", 64, _abi.TQ_ERR_UNSUPPORTED), ("ring_size", 64, _abi.TQ_ERR_UNSUPPORTED),
+    ("ring_size", -1, _abi.TQ_ERR_UNSUPPORTED),
     ("n_layers", 0, _abi.TQ_ERR_INVALID_ARG), ("n_q_heads", 12, _abi.TQ_ERR_UNSUPPORTED),
     ("n_q_heads", 9, _abi.TQ_ERR_INVALID_ARG), ("max_ctx", 0, _abi.TQ_ERR_INVALID_ARG),
 ])
@@ -44,6 +45,17 @@ def test_invalid_configs_rejected(field, value, status):
     assert lib.tq_init_codebooks(ctypes.byref(cfg), None, 0, None, ctypes.byref(ctx)) == status
     assert not ctx.value
     assert lib.tq_last_error()
+
+
+def test_full_tq_mode_config_is_accepted():
+    """ring_size 0 selects full_tq mode; the cache keeps the same layout (the ring is a staging copy)."""
+    lib = _abi.load()
+    hyb, full = tqm.config(), tqm.config(mode="full_tq")
+    assert full.ring_size == 0
+    assert lib.tq_tables_bytes(ctypes.byref(full)) == lib.tq_tables_bytes(ctypes.byref(hyb)) > 0
+    assert lib.tq_cache_bytes(ctypes.byref(full)) == lib.tq_cache_bytes(ctypes.byref(hyb)) > 0
+    with pytest.raises(ValueError):
+        tqm.config(mode="capture_only")
 
 
 def test_null_and_host_only_misuse_is_rejected():

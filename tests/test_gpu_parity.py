@@ -173,3 +173,34 @@ def test_bulk_append_onto_a_partial_ring(d, vb):
         ref = _oracle_decode(cache, 0, i, q[i], tables)
         for hq in range(Hkv * G):
             assert rel_l2(out[i, hq], ref[hq]) <= 2e-3
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4)])
+def test_full_tq_mode_appends_and_decode(d, vb):
+    """full_tq mode (ring_size 0, [Guide] §三): every appended token is quantised by its own append and
+    decode reads packed tokens only. A bulk prefill of 300 tokens, three single-token appends, then an
+    82-token append that completes a page and starts the next (303 -> 385). After every step all L
+    tokens are packed, the records equal the oracle's codes of every token, and decode matches the
+    oracle's attention over the packed tokens with no exact ring."""
+    Hkv, G, slot = 2, 4, 1
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
+                 max_ctx=640, seed=21, mode="full_tq")
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    k, v = synth.kv_tokens(400, Hkv, d, seed=21, outliers=("random", 4, 10.0))
+    q = synth.queries(1, Hkv * G, d, seed=21)
+    L = 0
+    for n in (300, 1, 1, 1, 82):
+        cache.append(0, k[None, L:L + n].to(DEV).contiguous(), v[None, L:L + n].to(DEV).contiguous(),
+                     _i32([slot]), _i32([n]))
+        L += n
+        torch.cuda.synchronize()
+        assert cache.check_status() == 0
+        Lg, F = cache.state(0, slot)
+        Np, R = oracle.history_split(L)
+        assert Lg == L and Np + F == L and oracle.history_split(L, 0) == (L, 0)
+        _check_sequence(cache, 0, slot, k[:L], v[:L], tables)
+        out = cache.decode(0, q.to(DEV), _i32([slot])).cpu().numpy()
+        ref = _oracle_decode(cache, 0, slot, q[0], tables)  # packed records only: the ring part is empty
+        for hq in range(Hkv * G):
+            assert rel_l2(out[0, hq], ref[hq]) <= 2e-3, (L, hq, rel_l2(out[0, hq], ref[hq]))

@@ -124,6 +124,8 @@ def test_history_split_ring_semantics():
     assert history_split(129) == (128, 1)
     assert history_split(1152) == (1024, 128)  # 1024 packed + 128-token ring
     assert history_split(32768) == (32640, 128)
+    # full_tq (ring 0): nothing stays exact
+    assert history_split(0, 0) == (0, 0) and history_split(1, 0) == (1, 0) and history_split(385, 0) == (385, 0)
 
 
 def test_cos_sim_report_pins():
