@@ -89,21 +89,38 @@ __device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int
   return true;
 }
 
-// Quantises the 32-token block q32 of page pg of (row b, KV head h): the page's first `valid` tokens
-// come from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
-// zero vectors. A 32-token block owns whole words of every page section, so four CTAs can write the
-// four blocks of one page independently. Run by all kQThreads threads of the CTA.
+// Shared-memory arrays of the CUDA-core quantiser: S^T (bf16 pairs), per-token key codes
+// (idx | sign << 2), value codes, {n, gamma} and value scales of a page, and one fp32 row per warp.
 template <int D>
-__device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
-                                                  int valid, int q32, uint8_t* smem) {
-  const int t0 = 32 * q32, t1 = t0 + 32;
+struct QSmem {
+  uint32_t* st2;     // [D][D/2]
+  uint8_t* kcode;    // [128][D]
+  uint8_t* vcode;    // [128][D]
+  uint32_t* norms;   // [128] n16 | gamma16 << 16
+  uint16_t* scales;  // [128][D/32]
+  float* rbuf;       // [8 warps][D]
+  __device__ explicit QSmem(uint8_t* smem)
+      : st2(reinterpret_cast<uint32_t*>(smem)),
+        kcode(smem + 2 * D * D),
+        vcode(kcode + kPage * D),
+        norms(reinterpret_cast<uint32_t*>(vcode + kPage * D)),
+        scales(reinterpret_cast<uint16_t*>(norms + kPage)),
+        rbuf(reinterpret_cast<float*>(scales + kPage * (D / 32))) {}
+};
+
+// Codes tokens [t_begin, t_end) of page pg of (row b, KV head h) into the shared-memory arrays, one
+// warp per token, after staging S^T (bf16) in shared memory. The page's first `valid` tokens come
+// from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
+// zero vectors. Run by all kQThreads threads of the CTA; ends with a block barrier.
+template <int D>
+__device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
+                                            int valid, int t_begin, int t_end, const QSmem<D>& sm) {
   constexpr int NE = D / 32;  // coordinates per lane
-  uint32_t* st2 = reinterpret_cast<uint32_t*>(smem);                    // S^T as bf16 pairs [D][D/2]
-  uint8_t* kcode = smem + 2 * D * D;                                    // [128][D]: idx | sign << 2
-  uint8_t* vcode = kcode + kPage * D;                                   // [128][D]
-  uint32_t* norms = reinterpret_cast<uint32_t*>(vcode + kPage * D);     // [128] n16 | gamma16 << 16
-  uint16_t* scales = reinterpret_cast<uint16_t*>(norms + kPage);        // [128][D/32]
-  float* rbuf = reinterpret_cast<float*>(scales + kPage * (D / 32));    // [8 warps][D]
+  uint32_t* st2 = sm.st2;
+  uint8_t* kcode = sm.kcode;
+  uint8_t* vcode = sm.vcode;
+  uint32_t* norms = sm.norms;
+  uint16_t* scales = sm.scales;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const LayerView& lv = a.lv;
   // stage S^T (bf16) in shared memory
@@ -123,8 +140,8 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
 
   const int vb = lv.vb, vhalf = 1 << (vb - 1);
   const float inv_sqrt_d = rsqrtf((float)D);
-  float* r = rbuf + warp * D;
-  for (int t = t0 + warp; t < t1; t += kQThreads / 32) {
+  float* r = sm.rbuf + warp * D;
+  for (int t = t_begin + warp; t < t_end; t += kQThreads / 32) {
     const int pos = pg * kPage + t;
     float x[NE], y[NE];
     if (t < valid) {
@@ -233,6 +250,25 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     }
   }
   __syncthreads();
+}
+
+// Quantises the 32-token block q32 of page pg of (row b, KV head h): the page's first `valid` tokens
+// come from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
+// zero vectors. A 32-token block owns whole words of every page section, so four CTAs can write the
+// four blocks of one page independently. Run by all kQThreads threads of the CTA.
+template <int D>
+__device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
+                                                  int valid, int q32, uint8_t* smem) {
+  const int t0 = 32 * q32, t1 = t0 + 32;
+  const QSmem<D> sm(smem);
+  code_tokens<D>(a, b, h, slot, L, Np, pg, valid, t0, t1, sm);
+  uint8_t* kcode = sm.kcode;
+  uint8_t* vcode = sm.vcode;
+  uint32_t* norms = sm.norms;
+  uint16_t* scales = sm.scales;
+  const int tid = threadIdx.x;
+  const LayerView& lv = a.lv;
+  const int vb = lv.vb;
 
   // ---- pack the page (fragment-major layout) ----
   uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
@@ -298,6 +334,87 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
 }
 
+// full_tq appends: codes tokens [t_lo, t_hi) of page pg (page-relative, one 32-token block at most)
+// and writes only their bits. Key words, {n, gamma} and value scales belong to one token each; a value
+// word holds the codes of 8 tokens of its block, so it is read, the new tokens' fields replaced, and
+// written back (one thread per word: this CTA is the block's only writer). Run by all kQThreads threads.
+template <int D>
+__device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np,
+                                                    int pg, int t_lo, int t_hi, uint8_t* smem) {
+  constexpr int HALVES = D / 128;
+  const QSmem<D> sm(smem);
+  code_tokens<D>(a, b, h, slot, L, Np, pg, t_hi, t_lo, t_hi, sm);
+  const int tid = threadIdx.x;
+  const LayerView& lv = a.lv;
+  const int vb = lv.vb, ntok = t_hi - t_lo;
+  uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
+  const PageLayout pl = page_layout(D, vb);
+  uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+  for (int i = tid; i < ntok * 12 * HALVES; i += kQThreads) {  // (token, plane, half, c)
+    const int c = i & 3, hf = (i >> 2) % HALVES, pi = (i / (4 * HALVES)) % 3, t = t_lo + i / (12 * HALVES);
+    const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
+    const uint8_t* kc = sm.kcode + t * D + 128 * hf + 2 * c;
+    uint32_t word = 0;
+#pragma unroll
+    for (int sq = 0; sq < 8; ++sq)
+#pragma unroll
+      for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int code = kc[16 * sq + 8 * sub + e];
+          const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
+          word |= (uint32_t)bit << (2 * sq + sub + 16 * e);
+        }
+    kw[((((tile * 3 + pi) * HALVES + hf) * 32) + 4 * g + c) * 2 + r] = word;
+  }
+  uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
+  for (int t = t_lo + tid; t < t_hi; t += kQThreads) nw[t] = sm.norms[t];
+  uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
+  const int blk = t_lo >> 5;
+  if (vb == 2) {
+    for (int w = blk * (D / 16) * 32 + tid; w < (blk + 1) * (D / 16) * 32; w += kQThreads) {
+      const int ln = w & 31, mt = (w >> 5) % (D / 16);
+      const int g = ln >> 2, c = ln & 3;
+      uint32_t mask = 0, bits = 0;
+#pragma unroll
+      for (int kap = 0; kap < 2; ++kap)
+#pragma unroll
+        for (int rg = 0; rg < 4; ++rg)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+            if (t >= t_lo && t < t_hi) {
+              const int sh = 16 * e + 2 * vfield2(kap, rg);
+              mask |= 3u << sh;
+              bits |= (uint32_t)sm.vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << sh;
+            }
+          }
+      if (mask) vw[w] = (vw[w] & ~mask) | bits;
+    }
+  } else {
+    for (int w = blk * (D / 16) * 64 + tid; w < (blk + 1) * (D / 16) * 64; w += kQThreads) {
+      const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16);
+      const int g = ln >> 2, c = ln & 3;
+      uint32_t mask = 0, bits = 0;
+#pragma unroll
+      for (int rg = 0; rg < 4; ++rg)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
+          if (t >= t_lo && t < t_hi) {
+            const int sh = 16 * e + 4 * vfield4(rg);
+            mask |= 15u << sh;
+            bits |= (uint32_t)sm.vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << sh;
+          }
+        }
+      if (mask) vw[w] = (vw[w] & ~mask) | bits;
+    }
+  }
+  uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
+  for (int i = t_lo * (D / 32) + tid; i < t_hi * (D / 32); i += kQThreads)
+    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = sm.scales[i];
+}
+
 template <int D>
 __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -338,14 +455,20 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   }
   const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
   if (a.full) {
-    // full_tq: every 32-token block that holds a new token is coded again, its older tokens from the
-    // ring (pages hold each token's code, so they come out identical) and the new ones from the input;
-    // tokens past L2 are coded as zero vectors until they arrive. A page that this append enters is
-    // coded to its end, so that decode never reads a block that no append has written.
-    const int end_blk = Np2 >= L ? Np2 / 32 + 3 : (L2 - 1) / 32;
+    // full_tq: the new tokens are coded into the page that holds them. A page that this append enters
+    // is coded whole (its tokens past L2 as zero vectors until they arrive), so that decode never reads
+    // a block that no append has written; in an older page only the new tokens' bits are written.
+    const bool entered = Np2 >= L;
+    const int end_blk = entered ? Np2 / 32 + 3 : (L2 - 1) / 32;
     for (int blk = L / 32 + q32; blk <= end_blk; blk += 4) {
       const int pg = blk / 4;
-      quantize_page_cta<D>(a, b, h, slot, L, Np, pg, min(kPage, L2 - pg * kPage), blk & 3, smem);
+      if (entered && pg * kPage == Np2) {
+        quantize_page_cta<D>(a, b, h, slot, L, Np, pg, min(kPage, L2 - pg * kPage), blk & 3, smem);
+      } else {
+        const int base = pg * kPage;
+        quantize_new_tokens<D>(a, b, h, slot, L, Np, pg, max(L, 32 * blk) - base, min(L2, 32 * blk + 32) - base,
+                               smem);
+      }
       __syncthreads();  // shared memory is staged again by the next block
     }
   } else if (Np2 > Np) {
