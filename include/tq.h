@@ -56,6 +56,8 @@ typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 #define TQ_DEV_ERR_SEQ_ID 0x2u   /* a sequence id outside [0, max_seqs); the row was skipped */
 #define TQ_DEV_ERR_SPLITS 0x4u   /* decode saw more packed pages than its grid covers (max_ctx_hint too small) */
 #define TQ_DEV_ERR_TIMEOUT 0x8u  /* a bounded wait on a bulk copy gave up; that split was dropped */
+#define TQ_DEV_ERR_BLOCK 0x10u   /* paged cache: a page that an append or decode touched has no valid block in
+                                  * the block table; the append skipped it, the decode result is undefined */
 
 /* Configuration. The key is 3 bits per coordinate: a 2-bit Lloyd-Max code plus 1 QJL sign bit
  * ([Guide] §二 steps 2-3; §五.1 key_bits=3). */
@@ -75,6 +77,13 @@ typedef struct tq_config {
   int32_t max_seqs;    /* number of sequence slots in the cache */
   int32_t max_ctx;     /* maximum tokens per sequence (packed + ring) */
   uint64_t seed;       /* seeds the rotation signs D and the QJL matrix S (SplitMix64) */
+  int32_t n_blocks;    /* 0: every (layer, slot, KV head) owns max_pages = ceil(max_ctx / 128) contiguous
+                        * pages. > 0: paged cache ([Guide] §七: the engine's KV cache lives in paged blocks). Each layer
+                        * holds a pool of n_blocks blocks; a block is one 128-token page of every KV head. The
+                        * int32 block table [max_seqs][max_pages] (in the cache buffer, see
+                        * tq_block_table_offset) maps (slot, page) to a block; the caller fills it before an
+                        * append or decode touches the page, with ids in [0, n_blocks) and no block shared by
+                        * two live pages. It is the same table for every layer. */
 } tq_config;
 
 typedef struct tq_ctx tq_ctx; /* opaque host object owned by the library */
@@ -83,7 +92,8 @@ typedef struct tq_ctx tq_ctx; /* opaque host object owned by the library */
 size_t tq_tables_bytes(const tq_config* cfg);
 
 /* Bytes of the device cache buffer for `cfg`; 0 if invalid. Layout, in order:
- *   - packed pages [layer][slot][kv_head][page][page_bytes];
+ *   - packed pages [layer][slot][kv_head][page][page_bytes], or for a paged cache (n_blocks > 0)
+ *     [layer][block][kv_head][page_bytes];
  *   - bf16 ring K and V [layer][slot][kv_head][ring][d];
  *   - int32 state [layer][slot][2]: total length L and flushed ring prefix F;
  *   - the int32 device status word. */
@@ -206,8 +216,14 @@ const char* tq_last_error(void);
 
 /* ---- Host-only inspection helpers (tests and tools; no device work) ---- */
 
-/* Byte offset, inside the cache buffer, of one packed page of (layer, slot, kv_head, page). */
+/* Byte offset, inside the cache buffer, of one packed page of (layer, slot, kv_head, page); (size_t)-1
+ * for a paged cache (the page's block comes from the device block table). */
 size_t tq_page_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int page);
+/* Paged cache: byte offset of the page of (layer, block, kv_head); (size_t)-1 when not paged. */
+size_t tq_block_page_offset(const tq_ctx* ctx, int layer, int block, int kv_head);
+/* Paged cache: byte offset of the int32 block table [max_seqs][max_pages] inside the cache buffer
+ * (tq_cache_bind sets every entry to -1, "no block"); (size_t)-1 when not paged. */
+size_t tq_block_table_offset(const tq_ctx* ctx);
 /* Byte offsets of the ring K (which = 0) / V (which = 1) block of (layer, slot, kv_head). */
 size_t tq_ring_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int which);
 /* Byte offset of the int32 pair {L, F} of (layer, slot), and of the status word. */

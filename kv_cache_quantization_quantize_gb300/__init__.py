@@ -15,13 +15,14 @@ __all__ = ["TQConfig", "TQError", "TurboQuantCache", "HostTables", "load", "conf
 
 
 def config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0,
-           mode="hybrid"):
-    """mode "hybrid": 128-token exact recent buffer; "full_tq": every token quantised (ring_size 0)."""
+           mode="hybrid", n_blocks=0):
+    """mode "hybrid": 128-token exact recent buffer; "full_tq": every token quantised (ring_size 0).
+    n_blocks > 0: paged cache with a pool of n_blocks 128-token blocks per layer (see block_table)."""
     if mode not in ("hybrid", "full_tq"):
         raise ValueError(f"mode {mode!r}: expected 'hybrid' or 'full_tq'")
     return TQConfig(head_dim=head_dim, key_bits=3, value_bits=value_bits, value_group=32,
                     ring_size=128 if mode == "hybrid" else 0, n_layers=n_layers, n_kv_heads=n_kv_heads,
-                    n_q_heads=n_q_heads, max_seqs=max_seqs, max_ctx=max_ctx, seed=seed)
+                    n_q_heads=n_q_heads, max_seqs=max_seqs, max_ctx=max_ctx, seed=seed, n_blocks=n_blocks)
 
 
 def _stream(stream=None):
@@ -166,8 +167,23 @@ class TurboQuantCache(HostTables):
         off = self.lib.tq_state_offset(self.ctx, layer, slot)
         return tuple(int(x) for x in self.cache_buf[off:off + 8].view(torch.int32).cpu())
 
+    @property
+    def block_table(self):
+        """Paged cache: the int32 block table [max_seqs, max_pages] (a view of the cache buffer, -1 = no
+        block). The caller maps every page an append or decode will touch, once for all layers."""
+        if self.cfg.n_blocks <= 0:
+            return None
+        off = self.lib.tq_block_table_offset(self.ctx)
+        max_pages = (self.cfg.max_ctx + 127) // 128
+        n = self.cfg.max_seqs * max_pages
+        return self.cache_buf[off:off + 4 * n].view(torch.int32).view(self.cfg.max_seqs, max_pages)
+
     def page(self, layer, slot, head, page):
-        off = self.lib.tq_page_offset(self.ctx, layer, slot, head, page)
+        if self.cfg.n_blocks > 0:
+            blk = int(self.block_table[slot, page])
+            off = self.lib.tq_block_page_offset(self.ctx, layer, blk, head)
+        else:
+            off = self.lib.tq_page_offset(self.ctx, layer, slot, head, page)
         return self.cache_buf[off:off + self.page_bytes()].cpu().numpy()
 
     def ring(self, layer, slot, head):

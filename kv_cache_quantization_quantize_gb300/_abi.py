@@ -9,7 +9,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "tq.h")
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CAPACITY, TQ_ERR_CUDA, TQ_ERR_DEVICE = range(6)
 TQ_BF16, TQ_F32 = 0, 1
-TQ_DEV_ERR_CAPACITY, TQ_DEV_ERR_SEQ_ID, TQ_DEV_ERR_SPLITS, TQ_DEV_ERR_TIMEOUT = 0x1, 0x2, 0x4, 0x8
+TQ_DEV_ERR_CAPACITY, TQ_DEV_ERR_SEQ_ID, TQ_DEV_ERR_SPLITS, TQ_DEV_ERR_TIMEOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8, 0x10
 
 c_int, c_size_t, c_void_p, c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
 
@@ -19,7 +19,7 @@ class TQConfig(ctypes.Structure):
         ("head_dim", ctypes.c_int32), ("key_bits", ctypes.c_int32), ("value_bits", ctypes.c_int32),
         ("value_group", ctypes.c_int32), ("ring_size", ctypes.c_int32), ("n_layers", ctypes.c_int32),
         ("n_kv_heads", ctypes.c_int32), ("n_q_heads", ctypes.c_int32), ("max_seqs", ctypes.c_int32),
-        ("max_ctx", ctypes.c_int32), ("seed", ctypes.c_uint64),
+        ("max_ctx", ctypes.c_int32), ("seed", ctypes.c_uint64), ("n_blocks", ctypes.c_int32),
     ]
 
 
@@ -44,6 +44,8 @@ _SIGS = {
     "tq_destroy": (None, [c_void_p]),
     "tq_last_error": (ctypes.c_char_p, []),
     "tq_page_offset": (c_size_t, [c_void_p, c_int, c_int, c_int, c_int]),
+    "tq_block_page_offset": (c_size_t, [c_void_p, c_int, c_int, c_int]),
+    "tq_block_table_offset": (c_size_t, [c_void_p]),
     "tq_ring_offset": (c_size_t, [c_void_p, c_int, c_int, c_int, c_int]),
     "tq_state_offset": (c_size_t, [c_void_p, c_int, c_int]),
     "tq_status_offset": (c_size_t, [c_void_p]),

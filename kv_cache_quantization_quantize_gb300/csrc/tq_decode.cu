@@ -85,6 +85,21 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 
+// Issues the bulk copy of packed page pg of (slot, KV head h) into a stage and its mbarrier. A paged
+// cache page without a block reports TQ_DEV_ERR_BLOCK and completes the phase with a plain arrival
+// (the stage keeps stale bytes: the call's result is then undefined, and nothing waits forever).
+__device__ __forceinline__ void issue_page(const LayerView& lv, int slot, int h, int pg, uint8_t* stage, uint32_t bytes,
+                                           uint64_t* bar) {
+  const uint8_t* src = page_addr(lv, slot, h, pg);
+  if (src) {
+    mbar_expect_tx(bar, bytes);
+    bulk_g2s(stage, src, bytes, bar);
+  } else {
+    set_status(lv.status, TQ_DEV_ERR_BLOCK);
+    mbar_arrive(bar);
+  }
+}
+
 __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L, int& Np, int& P) {
   L = lv.state[2 * slot];
   const int F = lv.state[2 * slot + 1];
@@ -119,8 +134,9 @@ __host__ __device__ constexpr int decode_threads() {
 // Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
 template <int D>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
-  // q_rot, q_proj [4][D] fp32; 16 scales; 16 offset sums; B fragments [3 D/16 items][32 lanes] uint2
-  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (3 * D / 16);
+  // q_rot, q_proj [4][D] fp32; 32 floats of scales; B fragments [3 D/16 items][32 lanes] uint2;
+  // per-warp offset sums [warps][8]
+  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (3 * D / 16) + sizeof(float) * 8 * (decode_threads<D>() / 32);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
@@ -237,11 +253,11 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   }
   __syncthreads();
   // B fragments: item (hv, pi, s) is computed by warp item % NW and shared through shared memory;
-  // red[16 + hd] / red[20 + hd] collect the offset sums of head hd
+  // wsum[w][hd] / wsum[w][4 + hd] hold warp w's offset sums of head hd, added in a fixed order below
+  // (the same constants in every split CTA and every call)
   constexpr int NW = NT / 32, NITEMS = HALVES * 3 * 8;
-  float* sums = red + 16;
   uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
-  if (tid < 8) sums[tid] = 0.f;
+  float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][8]
   const bool live = g < G;
   const float lam_m = live ? red[4 + 2 * g] : 0.f, lam_q = live ? red[4 + 2 * g + 1] : 0.f;
   const float* bm = qr + (live ? g : 0) * D;
@@ -269,18 +285,23 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
   if (c == 0 && g < kMaxG) {
-    atomicAdd(&sums[g], sum_m);
-    atomicAdd(&sums[4 + g], sum_q);
+    wsum[warp * 8 + g] = sum_m;
+    wsum[warp * 8 + 4 + g] = sum_q;
   }
   __syncthreads();
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
 #pragma unroll
   for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd
     const int hd = min(2 * c + i, kMaxG - 1);
+    float sm = 0.f, sq = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      sm += wsum[w * 8 + hd];
+      sq += wsum[w * 8 + 4 + hd];
+    }
     um[i] = a.scale * kLog2e / red[4 + 2 * hd];
-    cm[i] = 0.5f * sums[hd];
+    cm[i] = 0.5f * sm;
     uq[i] = a.scale * kLog2e * kappa / red[4 + 2 * hd + 1];
-    cq[i] = 0.5f * sums[4 + hd];
+    cq[i] = 0.5f * sq;
   }
 }
 
@@ -586,7 +607,7 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // exchange partial sums through shared memory.
 // Values: P is moved from C to B fragment layout with movmatrix and scaled per value group. Then
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
-template <int D, int VB, int STAGES>
+template <int D, int VB, int STAGES, bool PAGED>
 __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
   constexpr int HALVES = D / 128;
   constexpr int NT = decode_threads<D>();
@@ -632,6 +653,9 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [stream][stage]
   uint8_t* stage0 = smem + 128;                         // [stream][stage] pages
   float* xbuf = reinterpret_cast<float*>(stage0 + (size_t)NS * STAGES * PB);  // [NT][2 tiles][8] partial scores
+  // contiguous cache: the pages of (slot, h) follow each other; a paged cache maps every page through the
+  // block table (a separate instantiation: the lookup inside the page loop costs the contiguous kernel
+  // about 20 % if it is only branched around)
   const uint8_t* gpages = lv.pages + ((size_t)slot * lv.Hkv + h) * lv.max_pages * PB;
   const int npg = pg1 - pg0;  // stream st takes local pages st, st + NS, st + 2 NS, ...
   if (tid == 0) {
@@ -639,9 +663,13 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (int st = 0; st < NS; ++st)
       for (int s = 0; s < STAGES && st + NS * s < npg; ++s) {
-        mbar_expect_tx(&full[st * STAGES + s], PB);
-        bulk_g2s(stage0 + (size_t)(st * STAGES + s) * PB, gpages + (size_t)(pg0 + st + NS * s) * PB, PB,
-                 &full[st * STAGES + s]);
+        if (PAGED) {
+          issue_page(lv, slot, h, pg0 + st + NS * s, stage0 + (size_t)(st * STAGES + s) * PB, PB, &full[st * STAGES + s]);
+        } else {
+          mbar_expect_tx(&full[st * STAGES + s], PB);
+          bulk_g2s(stage0 + (size_t)(st * STAGES + s) * PB, gpages + (size_t)(pg0 + st + NS * s) * PB, PB,
+                   &full[st * STAGES + s]);
+        }
       }
   }
   SFrag<D> sfrag;
@@ -833,9 +861,14 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     if (NS == 1) __syncthreads();
     else named_barrier(5 + stream, 32 * SW);
     if ((tid % (32 * SW)) == 0 && ip + NS * STAGES < npg) {
-      mbar_expect_tx(&full[stream * STAGES + s_], PB);
-      bulk_g2s(stage0 + (size_t)(stream * STAGES + s_) * PB, gpages + (size_t)(pg0 + ip + NS * STAGES) * PB, PB,
-               &full[stream * STAGES + s_]);
+      if (PAGED) {
+        issue_page(lv, slot, h, pg0 + ip + NS * STAGES, stage0 + (size_t)(stream * STAGES + s_) * PB, PB,
+                   &full[stream * STAGES + s_]);
+      } else {
+        mbar_expect_tx(&full[stream * STAGES + s_], PB);
+        bulk_g2s(stage0 + (size_t)(stream * STAGES + s_) * PB, gpages + (size_t)(pg0 + ip + NS * STAGES) * PB, PB,
+                 &full[stream * STAGES + s_]);
+      }
     }
   }
   if (timed_out && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
@@ -928,12 +961,14 @@ int decode_setup() {
   if (resident == 0) {
     constexpr int STAGES = decode_stages<D, VB>();
     const size_t smem = decode_smem_bytes<D, VB>();
-    if (cudaFuncSetAttribute(k_decode<D, VB, STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(k_decode<D, VB, STAGES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(k_decode<D, VB, STAGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
       return -1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES>, decode_threads<D>(), smem) !=
-            cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES, false>, decode_threads<D>(),
+                                                      smem) != cudaSuccess ||
         n < 1)
       n = 1;
     resident = n;
@@ -951,8 +986,9 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
-    cudaError_t e = launch_pdl(k_decode<D, VB, STAGES>, dim3(a.plan.n_splits + 1, a.lv.Hkv, batch),
-                               dim3(decode_threads<D>()), smem, s, a);
+    const dim3 grid(a.plan.n_splits + 1, a.lv.Hkv, batch);
+    cudaError_t e = a.lv.btab ? launch_pdl(k_decode<D, VB, STAGES, true>, grid, dim3(decode_threads<D>()), smem, s, a)
+                              : launch_pdl(k_decode<D, VB, STAGES, false>, grid, dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;  // phase 2 (combine) runs inside phase 1's last CTA of every (row, KV head)

@@ -63,6 +63,16 @@ __device__ __forceinline__ void warp_fwht(float (&x)[NE], int lane) {
 
 __device__ __forceinline__ void set_status(uint32_t* status, uint32_t bit) { atomicOr(status, bit); }
 
+// Address of packed page pg of (slot, KV head h) in layer view lv. A paged cache maps (slot, pg)
+// through the block table; an entry outside [0, n_blocks) gives nullptr (the caller skips the page
+// and reports TQ_DEV_ERR_BLOCK).
+__device__ __forceinline__ uint8_t* page_addr(const LayerView& lv, int slot, int h, int pg) {
+  if (!lv.btab) return lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
+  const int blk = lv.btab[(size_t)slot * lv.max_pages + pg];
+  if (blk < 0 || blk >= lv.n_blocks) return nullptr;
+  return lv.pages + ((size_t)blk * lv.Hkv + h) * lv.page_bytes;
+}
+
 // Barrier `id` (1..15) over the first `threads` threads that reach it (a multiple of 32).
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
@@ -84,6 +94,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Plain arrival (no transaction bytes): completes a phase whose copy was not issued.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Bounded wait on an mbarrier phase: returns false after ~2^22 polls (seconds), never hangs.

@@ -81,6 +81,7 @@ tq_status validate(const tq_config* c) {
   const int G = c->n_q_heads / c->n_kv_heads;
   if (G != 1 && G != 2 && G != 4) return fail(TQ_ERR_UNSUPPORTED, "GQA group %d: supported 1, 2, 4", G);
   if (c->max_ctx > (1 << 24)) return fail(TQ_ERR_UNSUPPORTED, "max_ctx %d above 2^24", c->max_ctx);
+  if (c->n_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "n_blocks %d < 0", c->n_blocks);
   return TQ_OK;
 }
 
@@ -203,11 +204,14 @@ void compute_offsets(tq_ctx* ctx) {
   ctx->to = tq::table_offsets(c.head_dim);
   ctx->max_pages = (c.max_ctx + tq::kPage - 1) / tq::kPage;
   const size_t units = (size_t)c.n_layers * c.max_seqs * c.n_kv_heads;
+  const size_t page_units = c.n_blocks > 0 ? (size_t)c.n_layers * c.n_blocks * c.n_kv_heads : units * ctx->max_pages;
   ctx->pages_off = 0;
-  ctx->ring_off = align_up(units * ctx->max_pages * ctx->pl.bytes, 256);
+  ctx->ring_off = align_up(page_units * ctx->pl.bytes, 256);
   ctx->state_off = align_up(ctx->ring_off + units * ring_elems(c) * 2, 256);
   ctx->acnt_off = align_up(ctx->state_off + (size_t)c.n_layers * c.max_seqs * 8, 256);
-  ctx->status_off = align_up(ctx->acnt_off + (size_t)c.n_layers * c.max_seqs * 4, 256);
+  ctx->btab_off = align_up(ctx->acnt_off + (size_t)c.n_layers * c.max_seqs * 4, 256);
+  const size_t btab_bytes = c.n_blocks > 0 ? (size_t)c.max_seqs * ctx->max_pages * 4 : 0;
+  ctx->status_off = align_up(ctx->btab_off + btab_bytes, 256);
   ctx->total_bytes = ctx->status_off + 256;
 }
 
@@ -250,7 +254,14 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   v.HD_sw = reinterpret_cast<const uint16_t*>(tb + ctx->to.HD_sw);
   uint8_t* cb = static_cast<uint8_t*>(ctx->d_cache);
   const size_t units_per_layer = (size_t)c.max_seqs * c.n_kv_heads;
-  v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
+  if (c.n_blocks > 0) {
+    v.pages = cb + ctx->pages_off + (size_t)layer * c.n_blocks * c.n_kv_heads * ctx->pl.bytes;
+    v.btab = reinterpret_cast<const int32_t*>(cb + ctx->btab_off);
+  } else {
+    v.pages = cb + ctx->pages_off + (size_t)layer * units_per_layer * ctx->max_pages * ctx->pl.bytes;
+    v.btab = nullptr;
+  }
+  v.n_blocks = c.n_blocks;
   v.ring = reinterpret_cast<uint16_t*>(cb + ctx->ring_off) + (size_t)layer * units_per_layer * ring_elems(c);
   v.state = reinterpret_cast<int32_t*>(cb + ctx->state_off) + (size_t)layer * c.max_seqs * 2;
   v.acnt = reinterpret_cast<int32_t*>(cb + ctx->acnt_off) + (size_t)layer * c.max_seqs;
@@ -432,6 +443,10 @@ tq_status tq_cache_bind(tq_ctx* ctx, void* d_cache, size_t cache_bytes, tq_strea
   uint8_t* base = static_cast<uint8_t*>(d_cache);
   cudaError_t e = cudaMemsetAsync(base + ctx->state_off, 0, ctx->total_bytes - ctx->state_off, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(state)");
+  if (ctx->cfg.n_blocks > 0) {  // block table: every entry -1 ("no block")
+    e = cudaMemsetAsync(base + ctx->btab_off, 0xFF, (size_t)ctx->cfg.max_seqs * ctx->max_pages * 4, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(block table)");
+  }
   ctx->d_cache = d_cache;
   ctx->cache_bytes = cache_bytes;
   return ok();
@@ -554,9 +569,18 @@ void tq_destroy(tq_ctx* ctx) { delete ctx; }
 
 size_t tq_page_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int page) {
   const tq_config& c = ctx->cfg;
+  if (c.n_blocks > 0) return (size_t)-1;
   return ctx->pages_off +
          ((((size_t)layer * c.max_seqs + slot) * c.n_kv_heads + kv_head) * ctx->max_pages + page) * ctx->pl.bytes;
 }
+
+size_t tq_block_page_offset(const tq_ctx* ctx, int layer, int block, int kv_head) {
+  const tq_config& c = ctx->cfg;
+  if (c.n_blocks <= 0) return (size_t)-1;
+  return ctx->pages_off + ((((size_t)layer * c.n_blocks + block) * c.n_kv_heads) + kv_head) * ctx->pl.bytes;
+}
+
+size_t tq_block_table_offset(const tq_ctx* ctx) { return ctx->cfg.n_blocks > 0 ? ctx->btab_off : (size_t)-1; }
 
 size_t tq_ring_offset(const tq_ctx* ctx, int layer, int slot, int kv_head, int which) {
   const tq_config& c = ctx->cfg;

@@ -132,7 +132,7 @@ struct tq_ctx {
   void* d_tables = nullptr;
   void* d_cache = nullptr;
   size_t cache_bytes = 0;
-  size_t pages_off = 0, ring_off = 0, state_off = 0, acnt_off = 0, status_off = 0, total_bytes = 0;
+  size_t pages_off = 0, ring_off = 0, state_off = 0, acnt_off = 0, btab_off = 0, status_off = 0, total_bytes = 0;
   std::vector<float> D;
   std::vector<uint16_t> S;  // bf16 bits, row-major
   double cent[4] = {0, 0, 0, 0};
@@ -152,7 +152,9 @@ struct LayerView {
   const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128)
   const uint4* S_frag;   // S in f16 m16n8k16 A fragments (sfrag_idx)
   const uint16_t* HD_sw;  // H diag(D) in the tcgen05 swizzled K-major layout (head_dim 128)
-  uint8_t* pages;      // this layer: [slot][head][page][page_bytes]
+  uint8_t* pages;      // this layer: [slot][head][page][page_bytes], or paged: [block][head][page_bytes]
+  const int32_t* btab; // paged cache: block table [slot][max_pages] (all layers); nullptr: contiguous
+  int n_blocks;        // paged cache: blocks per layer
   uint16_t* ring;      // this layer: [slot][head][2][128][d] bf16
   int32_t* state;      // this layer: [slot][2] = {L, F}
   int32_t* acnt;       // this layer: [slot] arrival counters of the small-append kernel (left at zero)

@@ -271,7 +271,11 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
   const int vb = lv.vb;
 
   // ---- pack the page (fragment-major layout) ----
-  uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
+  uint8_t* page = page_addr(lv, slot, h, pg);
+  if (!page) {  // paged cache without a block for this page: nothing is written
+    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
+    return;
+  }
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   constexpr int HALVES = D / 128;
@@ -347,7 +351,11 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
   const int tid = threadIdx.x;
   const LayerView& lv = a.lv;
   const int vb = lv.vb, ntok = t_hi - t_lo;
-  uint8_t* page = lv.pages + (((size_t)slot * lv.Hkv + h) * lv.max_pages + pg) * lv.page_bytes;
+  uint8_t* page = page_addr(lv, slot, h, pg);
+  if (!page) {  // paged cache without a block for this page: nothing is written
+    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
+    return;
+  }
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   for (int i = tid; i < ntok * 12 * HALVES; i += kQThreads) {  // (token, plane, half, c)
@@ -708,7 +716,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     ph_rot ^= 1u << bufi;
     if (!ok) break;
     tc_fence_after();
-    uint8_t* page = lv.pages + (((size_t)cslot * lv.Hkv + chead) * lv.max_pages + cpg) * lv.page_bytes;
+    uint8_t* page = page_addr(lv, cslot, chead, cpg);
+    const bool wr = page != nullptr;  // paged cache without a block for this page: code it, write nothing
+    if (!wr && tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
     const PageLayout pl = page_layout(D, lv.vb);
     const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
@@ -805,12 +815,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float n = nrot * rsqrtf((float)D);
         const float rr = xr[t] + xr[128 + t];
         const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
-        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
-            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+        if (wr) {
+          reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
+              (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) {
-          kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
-          kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
+          for (int cw = 0; cw < 4; ++cw) {
+            kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
+            kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
+          }
         }
       }
       ok_p = mbar_wait(bar_qjl, ph_qjl);
@@ -834,7 +846,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_barrier(1, 256);
       if (!half) {
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) kw[((tile * 3 + 2) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[t * 4 + cw];
+        for (int cw = 0; cw < 4 && wr; ++cw) kw[((tile * 3 + 2) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[t * 4 + cw];
       }
     } else {
       // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
@@ -887,7 +899,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
         *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
         *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
+        if (wr) sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
       }
       named_barrier(2, 256);
       // ---- pack the value codes (fragment-major layout) ----
@@ -907,7 +919,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
                 word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
               }
-          vw[w] = word;
+          if (wr) vw[w] = word;
         }
       } else {
         for (int w = vt; w < 4 * (D / 16) * 32 * 2; w += 256) {
@@ -921,7 +933,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
               word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
             }
-          vw[w] = word;
+          if (wr) vw[w] = word;
         }
       }
     }

@@ -58,6 +58,27 @@ def test_full_tq_mode_config_is_accepted():
         tqm.config(mode="capture_only")
 
 
+def test_paged_cache_layout():
+    """n_blocks > 0: the pages section is a per-layer pool of n_blocks blocks (every KV head of a 128-token
+    page), followed by the ring, the state and the int32 block table [max_seqs][max_pages]."""
+    lib = _abi.load()
+    flat = tqm.config(n_layers=2, n_kv_heads=2, n_q_heads=8, max_seqs=64, max_ctx=8192)
+    paged = tqm.config(n_layers=2, n_kv_heads=2, n_q_heads=8, max_seqs=64, max_ctx=8192, n_blocks=100)
+    page = lib.tq_page_bytes(ctypes.byref(flat))
+    cf, cp = lib.tq_cache_bytes(ctypes.byref(flat)), lib.tq_cache_bytes(ctypes.byref(paged))
+    pool_flat, pool_paged = 2 * 64 * 2 * 64 * page, 2 * 100 * 2 * page
+    assert cf - cp >= pool_flat - pool_paged - 64 * 64 * 4 - 1024
+    bad = tqm.config(n_blocks=-1)
+    ctx = ctypes.c_void_p()
+    assert lib.tq_init_codebooks(ctypes.byref(bad), None, 0, None, ctypes.byref(ctx)) == _abi.TQ_ERR_INVALID_ARG
+    h = tqm.HostTables(paged)
+    assert lib.tq_page_offset(h.ctx, 0, 0, 0, 0) == ctypes.c_size_t(-1).value
+    assert lib.tq_block_page_offset(h.ctx, 1, 3, 1) == ((1 * 100 + 3) * 2 + 1) * page
+    assert lib.tq_block_table_offset(h.ctx) < cp
+    hf = tqm.HostTables(flat)
+    assert lib.tq_block_table_offset(hf.ctx) == ctypes.c_size_t(-1).value
+
+
 def test_null_and_host_only_misuse_is_rejected():
     lib = _abi.load()
     assert lib.tq_init_codebooks(None, None, 0, None, None) == _abi.TQ_ERR_INVALID_ARG

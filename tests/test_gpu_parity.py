@@ -204,3 +204,64 @@ def test_full_tq_mode_appends_and_decode(d, vb):
         ref = _oracle_decode(cache, 0, slot, q[0], tables)  # packed records only: the ring part is empty
         for hq in range(Hkv * G):
             assert rel_l2(out[0, hq], ref[hq]) <= 2e-3, (L, hq, rel_l2(out[0, hq], ref[hq]))
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4)])
+def test_paged_cache_scrambled_block_table(d, vb):
+    """Paged cache (n_blocks > 0): three sequences (300, 129 and 1000 tokens, then two single-token
+    appends) share one pool of 24 blocks through a scrambled block table. Their pages are byte-identical
+    to those of the contiguous layout fed the same inputs, decode outputs are identical, and both match
+    the oracle. A page with no block is reported on the status word without a fault."""
+    Hkv, G, extra = 2, 4, 2
+    lens, slots = [300, 129, 1000], [2, 0, 1]
+    B, max_ctx = len(lens), 1100
+    common = dict(head_dim=d, value_bits=vb, n_layers=2, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=3,
+                  max_ctx=max_ctx, seed=5)
+    paged = TurboQuantCache(config(n_blocks=24, **common))
+    flat = TurboQuantCache(config(**common))
+    perm = torch.randperm(24, generator=torch.Generator().manual_seed(3))
+    bt, nxt = paged.block_table, 0
+    for s_, L in zip(slots, lens):
+        for pg in range((L + extra + 127) // 128):
+            bt[s_, pg] = int(perm[nxt])
+            nxt += 1
+    tables = _oracle_tables(paged)
+    seqs = [synth.kv_tokens(L + extra, Hkv, d, seed=500 + i, outliers=("random", 4, 10.0)) for i, L in enumerate(lens)]
+    kb = torch.zeros(B, max(lens), Hkv, d, dtype=torch.bfloat16)
+    vbuf = torch.zeros_like(kb)
+    for i, L in enumerate(lens):
+        kb[i, :L] = seqs[i][0][:L]
+        vbuf[i, :L] = seqs[i][1][:L]
+    layer = 1
+    for cache in (paged, flat):
+        cache.append(layer, kb.to(DEV), vbuf.to(DEV), _i32(slots), _i32(lens))
+        for s in range(extra):
+            kd = torch.stack([seqs[i][0][L + s] for i, L in enumerate(lens)])[:, None].contiguous()
+            vd = torch.stack([seqs[i][1][L + s] for i, L in enumerate(lens)])[:, None].contiguous()
+            cache.append(layer, kd.to(DEV), vd.to(DEV), _i32(slots), _i32([1] * B))
+    torch.cuda.synchronize()
+    assert paged.check_status() == 0 and flat.check_status() == 0
+    for i, s_ in enumerate(slots):
+        assert paged.state(layer, s_) == flat.state(layer, s_)
+        Lt, F = paged.state(layer, s_)
+        P = oracle.history_split(Lt)[0] + F
+        for h in range(Hkv):
+            for pg in range((P + 127) // 128):
+                assert np.array_equal(paged.page(layer, s_, h, pg), flat.page(layer, s_, h, pg)), (i, h, pg)
+        _check_sequence(paged, layer, s_, seqs[i][0], seqs[i][1], tables)
+    q = synth.queries(B, Hkv * G, d, seed=6)
+    out_p = paged.decode(layer, q.to(DEV), _i32(slots)).cpu().numpy()
+    out_f = flat.decode(layer, q.to(DEV), _i32(slots)).cpu().numpy()
+    assert np.array_equal(out_p, out_f)
+    for i, s_ in enumerate(slots):
+        ref = _oracle_decode(paged, layer, s_, q[i], tables)
+        for hq in range(Hkv * G):
+            assert rel_l2(out_p[i, hq], ref[hq]) <= 2e-3
+    # a page whose block is missing: reported, no fault; the append that would write one skips it
+    bt[slots[0], 0] = -1
+    paged.decode(layer, q.to(DEV), _i32(slots))
+    assert paged.check_status() & 0x10
+    bt[slots[1], 2] = -1
+    k1 = torch.zeros(1, 260, Hkv, d, dtype=torch.bfloat16, device=DEV)
+    paged.append(layer, k1, k1, _i32([slots[1]]), _i32([260]))  # 131 -> 391 tokens: writes pages 1 and 2
+    assert paged.check_status() & 0x10
