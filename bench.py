@@ -201,10 +201,15 @@ def run_ours(args):
     extra = 1 + W + K + (n_e2e_warm + K) + K + 8  # tokens appended after prefill by all passes
     max_ctx = ctx + extra
     full = args.mode == "full_tq"
+    paged = args.layout == "paged"
+    max_pages = (max_ctx + 127) // 128
     cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=B,
-                     max_ctx=max_ctx, seed=1, mode=args.mode)
+                     max_ctx=max_ctx, seed=1, mode=args.mode, n_blocks=B * max_pages if paged else 0)
     cache = tqm.TurboQuantCache(cfg, device=dev)
     ids = torch.arange(B, dtype=torch.int32, device=dev)
+    if paged:  # every page of every row mapped to a block of a seeded permutation of the pool
+        perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
+        cache.block_table.copy_(perm.view(B, max_pages).to(dev))
     L0 = ctx - W - 2  # after the eager step and the W warm-up replays the first timed step attends ctx tokens
     n0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
     for l in range(L_layers):
@@ -308,7 +313,7 @@ def run_ours(args):
     kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
     kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
-    traffic = None if full else profiled_traffic()  # the committed ncu summary is of the hybrid step
+    traffic = None if full or paged else profiled_traffic()  # the committed ncu summary is of the hybrid step
 
     # ---- end to end through the public API with pinned host buffers ----
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
@@ -354,7 +359,7 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
-        "config": bench_config(world, args.mode),
+        "config": dict(bench_config(world, args.mode), **({"layout": "paged (scrambled block table)"} if paged else {})),
         "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * hbm_gbs / peak,
         "roofline": {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
@@ -370,7 +375,7 @@ def run_ours(args):
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not full:  # the oracle sample is of the hybrid step
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged:  # the oracle sample: hybrid step
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -382,9 +387,14 @@ def run_ours(args):
 def bench_quantize(tqm, synth, dev, args, peak):
     import torch
     T, Hkv, L_layers, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["layers"], PREFILL["d"], PREFILL["vb"]
+    paged = getattr(args, "layout", "contiguous") == "paged"
+    max_pages = (T + 127) // 128
     cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=4 * Hkv, max_seqs=1,
-                     max_ctx=T, seed=PREFILL["seed"])
+                     max_ctx=T, seed=PREFILL["seed"], n_blocks=max_pages if paged else 0)
     qc = tqm.TurboQuantCache(cfg, device=dev)
+    if paged:
+        perm = torch.randperm(max_pages, generator=torch.Generator().manual_seed(12)).to(torch.int32)
+        qc.block_table.copy_(perm.view(1, max_pages).to(dev))
     k, v = synth.kv_tokens(T, Hkv, d, seed=PREFILL["seed"], outliers=WL["outliers"], device=dev)
     k, v = k[None].contiguous(), v[None].contiguous()
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -549,6 +559,8 @@ def main():
     p.add_argument("--skip-quantize", action="store_true")
     p.add_argument("--mode", default="hybrid", choices=["hybrid", "full_tq"],
                    help="full_tq: no exact recent buffer, every token quantised on append")
+    p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
+                   help="paged: the packed pages live in a block pool addressed through a scrambled block table")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",

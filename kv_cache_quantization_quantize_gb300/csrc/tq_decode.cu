@@ -85,21 +85,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 
-// Issues the bulk copy of packed page pg of (slot, KV head h) into a stage and its mbarrier. A paged
-// cache page without a block reports TQ_DEV_ERR_BLOCK and completes the phase with a plain arrival
-// (the stage keeps stale bytes: the call's result is then undefined, and nothing waits forever).
-__device__ __forceinline__ void issue_page(const LayerView& lv, int slot, int h, int pg, uint8_t* stage, uint32_t bytes,
-                                           uint64_t* bar) {
-  const uint8_t* src = page_addr(lv, slot, h, pg);
-  if (src) {
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(stage, src, bytes, bar);
-  } else {
-    set_status(lv.status, TQ_DEV_ERR_BLOCK);
-    mbar_arrive(bar);
-  }
-}
-
 __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L, int& Np, int& P) {
   L = lv.state[2 * slot];
   const int F = lv.state[2 * slot + 1];
@@ -663,8 +648,13 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (int st = 0; st < NS; ++st)
       for (int s = 0; s < STAGES && st + NS * s < npg; ++s) {
-        if (PAGED) {
-          issue_page(lv, slot, h, pg0 + st + NS * s, stage0 + (size_t)(st * STAGES + s) * PB, PB, &full[st * STAGES + s]);
+        if (PAGED) {  // a page without a block reads block 0 and is reported after the loop
+          const int blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + st + NS * s];
+          const bool okb = (unsigned)blk < (unsigned)lv.n_blocks;
+          if (!okb) set_status(lv.status, TQ_DEV_ERR_BLOCK);
+          mbar_expect_tx(&full[st * STAGES + s], PB);
+          bulk_g2s(stage0 + (size_t)(st * STAGES + s) * PB, lv.pages + ((size_t)(okb ? blk : 0) * lv.Hkv + h) * PB, PB,
+                   &full[st * STAGES + s]);
         } else {
           mbar_expect_tx(&full[st * STAGES + s], PB);
           bulk_g2s(stage0 + (size_t)(st * STAGES + s) * PB, gpages + (size_t)(pg0 + st + NS * s) * PB, PB,
@@ -692,6 +682,10 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   float m_eff[2] = {-INFINITY, -INFINITY}, l_acc[2] = {0.f, 0.f};
   __syncthreads();
   bool timed_out = false;
+  bool bad_block = false;  // paged cache: a page without a block was read as block 0
+  int next_blk = 0;        // paged cache: block of the page this stream's issuing thread copies next
+  if (PAGED && (tid % (32 * SW)) == 0 && stream + NS * STAGES < npg)
+    next_blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + stream + NS * STAGES];
 
   for (int k = 0; stream + NS * k < npg; ++k) {
     const int ip = stream + NS * k, s_ = k % STAGES;
@@ -861,9 +855,14 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     if (NS == 1) __syncthreads();
     else named_barrier(5 + stream, 32 * SW);
     if ((tid % (32 * SW)) == 0 && ip + NS * STAGES < npg) {
-      if (PAGED) {
-        issue_page(lv, slot, h, pg0 + ip + NS * STAGES, stage0 + (size_t)(stream * STAGES + s_) * PB, PB,
-                   &full[stream * STAGES + s_]);
+      if (PAGED) {  // branch-free: a page without a block reads block 0 and is reported after the loop
+        const int blk = next_blk;  // loaded one page earlier, off this warp's critical path
+        if (ip + NS + NS * STAGES < npg) next_blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + ip + NS + NS * STAGES];
+        const bool okb = (unsigned)blk < (unsigned)lv.n_blocks;
+        bad_block |= !okb;
+        mbar_expect_tx(&full[stream * STAGES + s_], PB);
+        bulk_g2s(stage0 + (size_t)(stream * STAGES + s_) * PB, lv.pages + ((size_t)(okb ? blk : 0) * lv.Hkv + h) * PB,
+                 PB, &full[stream * STAGES + s_]);
       } else {
         mbar_expect_tx(&full[stream * STAGES + s_], PB);
         bulk_g2s(stage0 + (size_t)(stream * STAGES + s_) * PB, gpages + (size_t)(pg0 + ip + NS * STAGES) * PB, PB,
@@ -872,6 +871,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     }
   }
   if (timed_out && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  if (PAGED && bad_block) set_status(lv.status, TQ_DEV_ERR_BLOCK);
   // ---- merge the token groups' partials through shared memory ----
   __syncthreads();
   constexpr int NGRP = 4 * NS;                     // (stream, token group) partials
