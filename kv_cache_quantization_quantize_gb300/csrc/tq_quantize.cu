@@ -435,10 +435,37 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   quantize_page_cta<D>(a, b, h, slot, L, Np, pg, valid, blockIdx.z & 3, smem);
 }
 
+// Writes the ring rows of positions [p0, L2) of row b (every KV head, K and V) from the new input,
+// whose first token is position L; the ring then starts at position Np2. Run by all threads of a CTA.
+__device__ __forceinline__ void write_ring_rows(const AppendArgs& a, int b, int slot, int L, int Np2, int p0, int L2) {
+  const LayerView& lv = a.lv;
+  const int d = lv.d, q4 = d / 4;
+  const int n_items = (L2 - p0) * lv.Hkv * 2 * q4;  // (pos, head, which, quad)
+  for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+    const int quad = it % q4;
+    int rest = it / q4;
+    const int which = rest & 1;
+    rest >>= 1;
+    const int hh = rest % lv.Hkv, pos = p0 + rest / lv.Hkv;
+    const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + hh) * d + 4 * quad;
+    uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + hh) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
+    const void* base = which ? a.v : a.k;
+    uint2 out;
+    if (a.dt == 0) {
+      out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
+    } else {
+      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
+      out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
+      out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
+    }
+    *reinterpret_cast<uint2*>(dst) = out;
+  }
+}
+
 // Appends of fewer than 128 tokens per row in one launch. CTA (row b, KV head h, block q) codes
 // 32-token block q of the page that a ring overflow completes (if any). The last of the row's
 // 4 Hkv CTAs to arrive writes the new ring rows of every head (all CTAs have read the old ones by
-// then) and publishes the new length. Dependents (the decode) are released only after that, so they
+// then) and publishes the new length; without an overflow CTA (b, 0, 0) does that alone. Dependents (the decode) are released only after that, so they
 // may read the state before their own stream wait.
 template <int D>
 __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
@@ -462,6 +489,21 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
     return;
   }
   const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
+  if (!a.full && Np2 == Np) {
+    // no page to code (the common decode step): nothing reads the old ring rows, so CTA (b, 0, 0)
+    // writes every head's new rows and the length on its own and the others leave at once
+    if (h == 0 && q32 == 0) {
+      write_ring_rows(a, b, slot, L, Np2, L, L2);
+      __syncthreads();
+      if (tid == 0) {
+        lv.state[2 * slot] = L2;
+        __threadfence();
+      }
+      __syncthreads();
+    }
+    pdl_launch();
+    return;
+  }
   if (a.full) {
     // full_tq: the new tokens are coded into the page that holds them. A page that this append enters
     // is coded whole (its tokens past L2 as zero vectors until they arrive), so that decode never reads
@@ -490,28 +532,7 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   }
   __syncthreads();
   if (s_last) {
-    const int p0 = max(L, Np2);
-    const int d = lv.d, q4 = d / 4;
-    const int n_items = (L2 - p0) * lv.Hkv * 2 * q4;  // (pos, head, which, quad)
-    for (int it = tid; it < n_items; it += blockDim.x) {
-      const int quad = it % q4;
-      int rest = it / q4;
-      const int which = rest & 1;
-      rest >>= 1;
-      const int hh = rest % lv.Hkv, pos = p0 + rest / lv.Hkv;
-      const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + hh) * d + 4 * quad;
-      uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + hh) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
-      const void* base = which ? a.v : a.k;
-      uint2 out;
-      if (a.dt == 0) {
-        out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
-      } else {
-        const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
-        out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
-        out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
-      }
-      *reinterpret_cast<uint2*>(dst) = out;
-    }
+    write_ring_rows(a, b, slot, L, Np2, max(L, Np2), L2);
     __syncthreads();
     if (tid == 0) {
       lv.acnt[slot] = 0;
