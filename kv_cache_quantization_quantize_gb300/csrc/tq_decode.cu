@@ -770,22 +770,21 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
       mx[col] = m;
     }
-    float smax = 0.f;
-    for (int i = lane; i < 16 * NG; i += 32) {
-      const float2 sv = half2_to_float2(vsc[16 * tg * NG + i]);
-      smax = fmaxf(smax, fmaxf(sv.x, sv.y));
-    }
-    smax = warp_max(smax);
-    int e2 = 0;
-    frexpf(smax, &e2);
+    // largest value scale of this warp's tokens: the scales are finite non-negative f16, so their bit
+    // patterns order like their values (one warp max-reduction on the bits)
+    uint32_t smax_bits = 0;
+    for (int i = lane; i < 16 * NG; i += 32) smax_bits = __vmaxu2(smax_bits, vsc[16 * tg * NG + i]);
+    smax_bits = __reduce_max_sync(0xffffffffu, max(smax_bits & 0xffffu, smax_bits >> 16));
+    // e2 = exponent of smax as frexp gives it (biased f16 exponent - 14; <= 0 for subnormals and zero).
     // p * 2^(24-pos) <= 2^(15 - max(e2, 0)) keeps both P (packed before the scale) and P * s below 2^15
-    const float E = smax > 0.f ? (float)(9 + max(e2, 0)) : 9.f;
-    float alpha[2];
+    const float E = (float)(9 + max((int)((smax_bits >> 10) & 31u) - 14, 0));
+    float alpha[2], m_use[2];  // m_use: m_eff, or 0 while a column has seen no token (then every x is -inf)
 #pragma unroll
     for (int col = 0; col < 2; ++col) {
       const float m_new = fmaxf(m_eff[col], mx[col] + E);
       alpha[col] = (m_new == -INFINITY) ? 1.f : exp2f(m_eff[col] - m_new);
       m_eff[col] = m_new;
+      m_use[col] = m_new == -INFINITY ? 0.f : m_new;
       l_acc[col] *= alpha[col];
     }
     uint32_t pb[2][2];  // B fragments of P (no value scale yet): [k-step][tokens 0-7 / 8-15]
@@ -795,8 +794,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = i >> 1, col = i & 1;
-        const float x = sc[kap][i];
-        const float pn = x == -INFINITY ? 0.f : exp2f(x - m_eff[col]);
+        const float pn = exp2f(sc[kap][i] - m_use[col]);  // exp2(-inf) = 0
         l_acc[col] += pn;
         const int pos = VB == 2 ? vpos2(kap, row) : vpos4(row);
         pv[i] = pn * (float)(1u << (24 - pos));
