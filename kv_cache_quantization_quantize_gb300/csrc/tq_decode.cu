@@ -672,10 +672,15 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   // memory (written by query_prep; read once per page and k-step, shared by both tiles)
   const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * 24 * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
-  const int G = lv.G;
-  bool colok[2];
+  // score = n (um (am - cm) + uq gamma (aq - cq)) as n fma(gamma, fma(uq, aq, -uq cq), fma(um, am, -um cm)).
+  // Columns of heads >= G (and 4..7) carry zero query operands: their scores are finite and their
+  // outputs are never merged, so only tokens past the end of a partial page need masking.
+  float umcm[2], uqcq[2];
 #pragma unroll
-  for (int i = 0; i < 2; ++i) colok[i] = 2 * c + i < G;
+  for (int i = 0; i < 2; ++i) {
+    umcm[i] = um[i] * cm[i];
+    uqcq[i] = uq[i] * cq[i];
+  }
   float O[8][4];
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
@@ -756,8 +761,12 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int row = i >> 1, col = i & 1;
-        const bool ok = (row ? t1 : t0) < valid && colok[col];
-        sc[kap][i] = ok ? nv[row] * fmaf(um[col], am[i] - cm[col], uq[col] * gv[row] * (aq[i] - cq[col])) : -INFINITY;
+        sc[kap][i] = nv[row] * fmaf(gv[row], fmaf(uq[col], aq[i], -uqcq[col]), fmaf(um[col], am[i], -umcm[col]));
+      }
+      if (valid < kPage) {  // the last page of a sequence: tokens past its end take no weight
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (((i >> 1) ? t1 : t0) >= valid) sc[kap][i] = -INFINITY;
       }
     }
     // ---- online softmax (exp2 units); m_eff also keeps p * s * 2^(24 - pos) inside f16 range ----
