@@ -551,10 +551,11 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
 //     K-major tiles) while the current page is coded.
 //   - Rotation: y' = (H diag(D)) x for all 128 tokens of K and of V as two M = N = 128, K = 128 MMAs
 //     (the +-1 entries are exact in bf16, products are exact, fp32 accumulation) into TMEM.
-//   - Warps 0-3 code the keys thread-per-token from TMEM: norm, Lloyd-Max index, residual, bf16
-//     hi + lo split of the residual (written over the consumed K tile), then the QJL projection
-//     z = S r as 16 more MMAs (|r - hi - lo| <= 2^-18 |r|) and the signs of z.
-//   - Warps 4-7 code the values thread-per-token: groups of 32, fp16 scale, mid-rise codes.
+//   - Warps 0-7 code the keys, two threads per token row, from TMEM: norm, Lloyd-Max index,
+//     residual, bf16 hi + lo split of the residual (written over the consumed K tile); then thread 0
+//     issues the QJL projection z = S r as 16 more MMAs (|r - hi - lo| <= 2^-18 |r|).
+//   - Warps 8-15 code the values the same way (groups of 32, fp16 scale, mid-rise codes) and then
+//     take the signs of z, so the key warps need not wait for the projection.
 //   - Key words, norms and value scales go to the page straight from registers; value codes are
 //     staged in shared memory for the fragment-major value layout.
 // =============================================================================================
@@ -846,29 +847,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
-      ok_p = mbar_wait(bar_qjl, ph_qjl);
-      tc_fence_after();
-      uint32_t wsg[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t z[32];
-        tmem_ld32(lrow + 64 * half + 32 * cc, z);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int jl = 32 * cc + i;
-          const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
-          wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
-        }
-      }
-      if (half) {
-#pragma unroll
-        for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
-      }
-      named_barrier(1, 256);
-      if (!half) {
-#pragma unroll
-        for (int cw = 0; cw < 4 && wr; ++cw) kw[((tile * 3 + 2) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[t * 4 + cw];
-      }
+      // the QJL signs are read by the value warps (their path is the shorter one)
     } else {
       // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
       const int vhalf = 1 << (lv.vb - 1);
@@ -957,8 +936,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (wr) vw[w] = word;
         }
       }
+      // ---- the QJL signs of this page's keys, once the key warps' projection MMAs complete ----
+      ok_p = mbar_wait(bar_qjl, ph_qjl);
+      tc_fence_after();
+      uint32_t wsg[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t z[32];
+        tmem_ld32(lrow + 64 * half + 32 * cc, z);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int jl = 32 * cc + i;
+          const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+          wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
+        }
+      }
+      if (half) {
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
+      }
+      named_barrier(2, 256);
+      if (!half && wr) {
+        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+        const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) kw[((ktile * 3 + 2) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
+      }
     }
-    ph_qjl ^= kpath ? 1u : 0u;
+    ph_qjl ^= kpath ? 0u : 1u;
     if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);  // waited on by thread 0 above
     tc_fence_before();
     ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, vcode and exchange may be reused
