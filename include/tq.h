@@ -62,7 +62,7 @@ typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 /* Configuration. The key is 3 bits per coordinate: a 2-bit Lloyd-Max code plus 1 QJL sign bit
  * ([Guide] §二 steps 2-3; §五.1 key_bits=3). */
 typedef struct tq_config {
-  int32_t head_dim;    /* d: 128 or 256 */
+  int32_t head_dim;    /* d: 64, 128 or 256 */
   int32_t key_bits;    /* 3 */
   int32_t value_bits;  /* 2 or 4 ([Guide] §二 step 4) */
   int32_t value_group; /* 32 ([Guide] §二 step 4) */

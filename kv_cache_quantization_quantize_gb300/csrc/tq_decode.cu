@@ -73,6 +73,42 @@ __device__ __forceinline__ float4 ld_cg_f4(const float* p) {
   return v;
 }
 
+__device__ __forceinline__ float2 ld_cg_f2(const float* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];\n" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+// This lane's D / 32 values of a d-row in the lane_coord layout (L2 loads / plain stores).
+template <int D>
+__device__ __forceinline__ void ld_cg_row(const float* row, int lane, float (&x)[D / 32]) {
+  if (D == 64) {
+    const float2 v = ld_cg_f2(row + 2 * lane);
+    x[0] = v.x;
+    x[D / 32 - 1] = v.y;
+  } else {
+#pragma unroll
+    for (int hf = 0; hf < D / 128; ++hf) {
+      const float4 v = ld_cg_f4(row + 128 * hf + 4 * lane);
+      x[(4 * hf) % (D / 32)] = v.x;
+      x[(4 * hf + 1) % (D / 32)] = v.y;
+      x[(4 * hf + 2) % (D / 32)] = v.z;
+      x[(4 * hf + 3) % (D / 32)] = v.w;
+    }
+  }
+}
+template <int D>
+__device__ __forceinline__ void st_row(float* row, int lane, const float (&x)[D / 32]) {
+  if (D == 64) {
+    *reinterpret_cast<float2*>(row + 2 * lane) = make_float2(x[0], x[D / 32 - 1]);
+  } else {
+#pragma unroll
+    for (int hf = 0; hf < D / 128; ++hf)
+      *reinterpret_cast<float4*>(row + 128 * hf + 4 * lane) =
+          make_float4(x[(4 * hf) % (D / 32)], x[(4 * hf + 1) % (D / 32)], x[(4 * hf + 2) % (D / 32)],
+                      x[(4 * hf + 3) % (D / 32)]);
+  }
+}
+
 __device__ __forceinline__ float2 half2_to_float2(uint32_t a) {
   return __half22float2(*reinterpret_cast<const __half2*>(&a));
 }
@@ -105,11 +141,16 @@ __host__ __device__ constexpr int decode_xbuf_floats() {
 // (Four streams of 16 warps measured slower at batch 1 and no faster at batch 32.)
 template <int D>
 __host__ __device__ constexpr int decode_streams() {
-  return D == 128 ? 3 : 1;
+  return D <= 128 ? 3 : 1;
+}
+// Coordinates of one warp (a 128-coordinate half, or all 64) and key-MMA k-steps per warp.
+template <int D>
+__host__ __device__ constexpr int warp_coords() {
+  return D < 128 ? D : 128;
 }
 template <int D>
 __host__ __device__ constexpr int decode_threads() {
-  return decode_streams<D>() * 32 * 4 * (D / 128);
+  return decode_streams<D>() * 32 * 4 * (D / warp_coords<D>());
 }
 
 // =============================================================================================
@@ -167,7 +208,7 @@ template <int D, int NT>
 __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
                                            float (&um)[2], float (&cm)[2], float (&uq)[2], float (&cq)[2]) {
   constexpr int NE = D / 32;
-  constexpr int HALVES = D / 128;
+  constexpr int HALVES = D / warp_coords<D>();
   constexpr int MT = D / 16;
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -181,7 +222,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     float x[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
-      const int j = (e >> 2) * 128 + 4 * lane + (e & 3);
+      const int j = lane_coord<D>(e, lane);
       const float qv = warp < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + warp) * D + j]) : 0.f;
       x[e] = qv * lv.D[j];
     }
@@ -191,7 +232,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       const float v = x[e] * rs;
-      qr[warp * D + (e >> 2) * 128 + 4 * lane + (e & 3)] = v;
+      qr[warp * D + lane_coord<D>(e, lane)] = v;
       mx = fmaxf(mx, fabsf(v));
     }
     mx = warp_max(mx);
@@ -240,7 +281,8 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   // B fragments: item (hv, pi, s) is computed by warp item % NW and shared through shared memory;
   // wsum[w][hd] / wsum[w][4 + hd] hold warp w's offset sums of head hd, added in a fixed order below
   // (the same constants in every split CTA and every call)
-  constexpr int NW = NT / 32, NITEMS = HALVES * 3 * 8;
+  constexpr int KS = warp_coords<D>() / 16;  // key-MMA k-steps per warp
+  constexpr int NW = NT / 32, NITEMS = HALVES * 3 * KS;
   uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
   float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][8]
   const bool live = g < G;
@@ -250,7 +292,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   __syncthreads();
   float sum_m = 0.f, sum_q = 0.f;
   for (int item = warp; item < NITEMS; item += NW) {
-    const int s = item & 7, pi = (item >> 3) % 3, hv = item / 24;
+    const int s = item % KS, pi = (item / KS) % 3, hv = item / (3 * KS);
     const float w = (pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f) * (pi < 2 ? lam_m : lam_q);
     const float* base = pi < 2 ? bm : bp;
     const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
@@ -297,7 +339,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
 // in flight together), then [128][4] scores, the softmax statistics and q as fp32 [4][D].
 template <int D>
 __host__ __device__ constexpr bool ring_kv_together() {
-  return D == 128;
+  return D <= 128;
 }
 template <int D>
 __host__ __device__ constexpr size_t ring_smem_bytes() {
@@ -457,23 +499,24 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float* ls = fs + 4 * (nsp + 1);   // [nsp][4] split sums
   // 0. the outputs of the first PRE splits and the ring partial do not depend on the weights: their
   //    loads share the round trip of the (m, l) loads
-  constexpr int PRE = D == 128 ? 20 : 8;
-  const float* ob = base + 2 * kMaxG + hd * D + 4 * lane;
+  constexpr int PRE = D == 128 ? 20 : D == 64 ? 24 : 8;
+  const float* ob = base + 2 * kMaxG + hd * D;
   const float* rp = base + nsp * stride;
-  float4 vpre[PRE][NE / 4], rvp[NE / 4];
+  float vpre[PRE][NE], rvp[NE];
 #pragma unroll
-  for (int u = 0; u < PRE; ++u)
+  for (int u = 0; u < PRE; ++u) {
+    if (u < nsp) {
+      ld_cg_row<D>(ob + u * stride, lane, vpre[u]);
+    } else {
 #pragma unroll
-    for (int hf = 0; hf < NE / 4; ++hf) {
-      vpre[u][hf] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (u < nsp) vpre[u][hf] = ld_cg_f4(ob + u * stride + 128 * hf);
+      for (int e = 0; e < NE; ++e) vpre[u][e] = 0.f;
     }
-#pragma unroll
-  for (int hf = 0; hf < NE / 4; ++hf) rvp[hf] = ld_cg_f4(rp + 2 * kMaxG + hd * D + 128 * hf + 4 * lane);
+  }
+  ld_cg_row<D>(rp + 2 * kMaxG + hd * D, lane, rvp);
   const float mr = ld_cg_f(rp + hd), lr = ld_cg_f(rp + kMaxG + hd);
   float dsg[NE];  // the rotation signs of this lane's coordinates (constant table)
 #pragma unroll
-  for (int e = 0; e < NE; ++e) dsg[e] = lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
+  for (int e = 0; e < NE; ++e) dsg[e] = lv.D[lane_coord<D>(e, lane)];
   // 1. the splits' (m, l) of this head across the lanes; maximum, weights and the weighted sum of l
   float mloc = -INFINITY;
   for (int s = lane; s < nsp; s += 32) {
@@ -501,44 +544,27 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
     const float f = u < nsp ? fs[u * 4 + hd] : 0.f;
     float* acc = (u & 1) ? o2 : o;
 #pragma unroll
-    for (int hf = 0; hf < NE / 4; ++hf) {
-      acc[4 * hf + 0] = fmaf(f, vpre[u][hf].x, acc[4 * hf + 0]);
-      acc[4 * hf + 1] = fmaf(f, vpre[u][hf].y, acc[4 * hf + 1]);
-      acc[4 * hf + 2] = fmaf(f, vpre[u][hf].z, acc[4 * hf + 2]);
-      acc[4 * hf + 3] = fmaf(f, vpre[u][hf].w, acc[4 * hf + 3]);
-    }
+    for (int e = 0; e < NE; ++e) acc[e] = fmaf(f, vpre[u][e], acc[e]);
   }
   int s0 = PRE;
   for (; s0 + 16 <= nsp; s0 += 16) {  // empty splits hold weight 0 and O = 0
-    float4 v[16][NE / 4];
+    float v[16][NE];
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
-#pragma unroll
-      for (int hf = 0; hf < NE / 4; ++hf)
-        v[u][hf] = ld_cg_f4(ob + (s0 + u) * stride + 128 * hf);
+    for (int u = 0; u < 16; ++u) ld_cg_row<D>(ob + (s0 + u) * stride, lane, v[u]);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
       const float f = fs[(s0 + u) * 4 + hd];
       float* acc = (u & 1) ? o2 : o;
 #pragma unroll
-      for (int hf = 0; hf < NE / 4; ++hf) {
-        acc[4 * hf + 0] = fmaf(f, v[u][hf].x, acc[4 * hf + 0]);
-        acc[4 * hf + 1] = fmaf(f, v[u][hf].y, acc[4 * hf + 1]);
-        acc[4 * hf + 2] = fmaf(f, v[u][hf].z, acc[4 * hf + 2]);
-        acc[4 * hf + 3] = fmaf(f, v[u][hf].w, acc[4 * hf + 3]);
-      }
+      for (int e = 0; e < NE; ++e) acc[e] = fmaf(f, v[u][e], acc[e]);
     }
   }
   for (; s0 < nsp; ++s0) {
     const float f = fs[s0 * 4 + hd];
+    float v[NE];
+    ld_cg_row<D>(ob + s0 * stride, lane, v);
 #pragma unroll
-    for (int hf = 0; hf < NE / 4; ++hf) {
-      const float4 v = ld_cg_f4(ob + s0 * stride + 128 * hf);
-      o[4 * hf + 0] = fmaf(f, v.x, o[4 * hf + 0]);
-      o[4 * hf + 1] = fmaf(f, v.y, o[4 * hf + 1]);
-      o[4 * hf + 2] = fmaf(f, v.z, o[4 * hf + 2]);
-      o[4 * hf + 3] = fmaf(f, v.w, o[4 * hf + 3]);
-    }
+    for (int e = 0; e < NE; ++e) o[e] = fmaf(f, v[e], o[e]);
   }
 #pragma unroll
   for (int e = 0; e < NE; ++e) o[e] += o2[e];
@@ -552,17 +578,10 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   const float fr = (mr == -INFINITY) ? 0.f : exp2f(mr - mm);
   const float den = fh * l + fr * lr;
   const float inv = den > 0.f ? 1.f / den : 0.f;
-  float* out = a.out + ((size_t)b * lv.Hq + h * lv.G + hd) * D;
+  float r[NE];
 #pragma unroll
-  for (int hf = 0; hf < NE / 4; ++hf) {
-    const float4 rv = rvp[hf];
-    float4 r;
-    r.x = (fh * o[4 * hf + 0] + fr * rv.x) * inv;
-    r.y = (fh * o[4 * hf + 1] + fr * rv.y) * inv;
-    r.z = (fh * o[4 * hf + 2] + fr * rv.z) * inv;
-    r.w = (fh * o[4 * hf + 3] + fr * rv.w) * inv;
-    *reinterpret_cast<float4*>(out + 128 * hf + 4 * lane) = r;
-  }
+  for (int e = 0; e < NE; ++e) r[e] = (fh * o[e] + fr * rvp[e]) * inv;
+  st_row<D>(a.out + ((size_t)b * lv.Hq + h * lv.G + hd) * D, lane, r);
 }
 
 // After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
@@ -594,7 +613,10 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
 template <int D, int VB, int STAGES, bool PAGED>
 __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
-  constexpr int HALVES = D / 128;
+  constexpr int CW = warp_coords<D>();  // coordinates per warp
+  constexpr int HALVES = D / CW;
+  constexpr int KS = CW / 16;           // key-MMA k-steps per warp
+  constexpr int QG = CW / 32;           // value groups per warp
   constexpr int NT = decode_threads<D>();
   constexpr int NS = decode_streams<D>();
   constexpr int SW = 4 * HALVES;  // warps per stream
@@ -670,7 +692,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   query_prep<D, NT>(a, b, h, ps, sfrag, um, cm, uq, cq);
   // f16 B fragments of the key MMAs for this warp's coordinate half, [plane][k-step][lane] in shared
   // memory (written by query_prep; read once per page and k-step, shared by both tiles)
-  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * 24 * 32 + lane;
+  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * 3 * KS * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
   // score = n (um (am - cm) + uq gamma (aq - cq)) as n fma(gamma, fma(uq, aq, -uq cq), fma(um, am, -um cm)).
   // Columns of heads >= G (and 4..7) carry zero query operands: their scores are finite and their
@@ -681,9 +703,9 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     umcm[i] = um[i] * cm[i];
     uqcq[i] = uq[i] * cq[i];
   }
-  float O[8][4];
+  float O[2 * QG][4];
 #pragma unroll
-  for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
+  for (int mt = 0; mt < 2 * QG; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
   float m_eff[2] = {-INFINITY, -INFINITY}, l_acc[2] = {0.f, 0.f};
   __syncthreads();
   bool timed_out = false;
@@ -711,15 +733,20 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
 #pragma unroll
       for (int pi = 0; pi < 3; ++pi) {
         acc[kap][pi][0] = acc[kap][pi][1] = acc[kap][pi][2] = acc[kap][pi][3] = 0.f;
-        kwv[kap][pi] = kw2[(((2 * tg + kap) * 3 + pi) * HALVES + hf) * 32 + lane];
+        if (D == 64) {  // both tiles in one word; the odd tile 8 bit positions higher
+          const uint2 wv = kw2[(tg * 3 + pi) * 32 + lane];
+          kwv[kap][pi] = kap ? make_uint2(wv.x >> 8, wv.y >> 8) : wv;
+        } else {
+          kwv[kap][pi] = kw2[(((2 * tg + kap) * 3 + pi) * HALVES + hf) * 32 + lane];
+        }
       }
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
+    for (int s = 0; s < KS; ++s) {
       const int q0 = s < 6 ? 2 * s : 2 * s - 4;
       const uint32_t m0 = 0x00010001u << q0, m1 = 0x00010001u << (q0 + 1);
 #pragma unroll
       for (int pi = 0; pi < 3; ++pi) {
-        const uint2 bv = bfr[(pi * 8 + s) * 32];
+        const uint2 bv = bfr[(pi * KS + s) * 32];
 #pragma unroll
         for (int kap = 0; kap < 2; ++kap) {
           const uint32_t x0 = s < 6 ? kwv[kap][pi].x : kwv[kap][pi].x >> 4;
@@ -823,8 +850,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     constexpr uint32_t kOff10 = voff_pattern(kVmax, VB == 2 ? vpos2(1, 0) : vpos4(0));
     constexpr uint32_t kOff11 = voff_pattern(kVmax, VB == 2 ? vpos2(1, 1) : vpos4(1));
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int gq = 4 * hf + q;
+    for (int q = 0; q < QG; ++q) {
+      const int gq = QG * hf + q;
       uint32_t bf[2][2];
 #pragma unroll
       for (int kap = 0; kap < 2; ++kap) {
@@ -839,7 +866,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
       for (int i = 0; i < 4; ++i) coff[i] *= 0.5f;
 #pragma unroll
       for (int mh = 0; mh < 2; ++mh) {
-        const int mt = 2 * q + mh, mtg = 8 * hf + mt;
+        const int mt = 2 * q + mh, mtg = 2 * QG * hf + mt;
         float acc[4] = {coff[0], coff[1], coff[2], coff[3]};
         if (VB == 2) {
           const uint32_t w = vw[(tg * (D / 16) + mtg) * 32 + lane];
@@ -901,8 +928,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     }
     if (c < 2) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int j0 = 128 * hf + 16 * mt + g;
+      for (int mt = 0; mt < 2 * QG; ++mt) {
+        const int j0 = CW * hf + 16 * mt + g;
         wo[(grp * 4 + 2 * c) * D + j0] = O[mt][0];
         wo[(grp * 4 + 2 * c + 1) * D + j0] = O[mt][1];
         wo[(grp * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
@@ -943,7 +970,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
 
 template <int D, int VB>
 constexpr int decode_stages() {  // pages in flight per stream
-  return D == 128 ? 4 : 3;
+  return D <= 128 ? 4 : 3;
 }
 
 template <int D, int VB>
@@ -1006,7 +1033,9 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
 int decode_resident_ctas(const tq_ctx* ctx) {
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
   int n;
-  if (d == 128 && vb == 2) n = decode_setup<128, 2>();
+  if (d == 64 && vb == 2) n = decode_setup<64, 2>();
+  else if (d == 64 && vb == 4) n = decode_setup<64, 4>();
+  else if (d == 128 && vb == 2) n = decode_setup<128, 2>();
   else if (d == 128 && vb == 4) n = decode_setup<128, 4>();
   else if (d == 256 && vb == 2) n = decode_setup<256, 2>();
   else n = decode_setup<256, 4>();
@@ -1024,6 +1053,8 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.ws = static_cast<uint8_t*>(ws);
   a.plan = plan;
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
+  if (d == 64 && vb == 2) return launch_decode_dv<64, 2>(a, batch, phase, s);
+  if (d == 64 && vb == 4) return launch_decode_dv<64, 4>(a, batch, phase, s);
   if (d == 128 && vb == 2) return launch_decode_dv<128, 2>(a, batch, phase, s);
   if (d == 128 && vb == 4) return launch_decode_dv<128, 4>(a, batch, phase, s);
   if (d == 256 && vb == 2) return launch_decode_dv<256, 2>(a, batch, phase, s);

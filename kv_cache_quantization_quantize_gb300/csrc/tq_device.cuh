@@ -28,19 +28,31 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Unnormalised Walsh-Hadamard transform (Sylvester order) of a d-vector spread over one warp.
-// Lane l holds coordinates 4l + e (e = 0..3) in x[e] and, for d = 256, 128 + 4l + e in x[4 + e].
-// Coordinate bits 0-1 (and 7) are butterflied in registers; bits 2-6 across lanes with shuffles.
+// Coordinate that lane `lane` holds in x[e] when a d-vector is spread over one warp (NE = d / 32
+// values per lane): 4 lane + e (+ 128 for e >= 4) for d >= 128, and 2 lane + e for d = 64.
+template <int D>
+__device__ __forceinline__ int lane_coord(int e, int lane) {
+  return D == 64 ? 2 * lane + e : (e >> 2) * 128 + 4 * lane + (e & 3);
+}
+
+// Unnormalised Walsh-Hadamard transform (Sylvester order) of a d-vector spread over one warp in the
+// lane_coord layout. The coordinate bits held in registers (bits 0-1 and, for d = 256, bit 7; bit 0
+// for d = 64) are butterflied in registers, the lane bits across lanes with shuffles.
 template <int NE>
 __device__ __forceinline__ void warp_fwht(float (&x)[NE], int lane) {
 #pragma unroll
-  for (int base = 0; base < NE; base += 4) {
+  for (int base = 0; base + 3 < NE; base += 4) {
     float a0 = x[base + 0] + x[base + 1], a1 = x[base + 0] - x[base + 1];
     float a2 = x[base + 2] + x[base + 3], a3 = x[base + 2] - x[base + 3];
     x[base + 0] = a0 + a2;
     x[base + 2] = a0 - a2;
     x[base + 1] = a1 + a3;
     x[base + 3] = a1 - a3;
+  }
+  if (NE == 2) {  // head_dim 64: lane holds coordinates 2 lane + {0, 1}
+    const float a = x[0], b = x[1];
+    x[0] = a + b;
+    x[1] = a - b;
   }
   if (NE == 8) {
 #pragma unroll

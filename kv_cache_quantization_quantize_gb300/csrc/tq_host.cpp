@@ -66,8 +66,8 @@ uint16_t bf16_to_f16_rne(uint16_t b) {
 
 tq_status validate(const tq_config* c) {
   if (!c) return fail(TQ_ERR_INVALID_ARG, "cfg is NULL");
-  if (c->head_dim != 128 && c->head_dim != 256)
-    return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: supported 128, 256", c->head_dim);
+  if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
+    return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: supported 64, 128, 256", c->head_dim);
   if (c->key_bits != 3) return fail(TQ_ERR_UNSUPPORTED, "key_bits %d: supported 3 (2-bit Lloyd-Max + 1-bit QJL)", c->key_bits);
   if (c->value_bits != 2 && c->value_bits != 4)
     return fail(TQ_ERR_UNSUPPORTED, "value_bits %d: supported 2, 4", c->value_bits);

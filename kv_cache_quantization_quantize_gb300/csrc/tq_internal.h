@@ -55,10 +55,18 @@ TQ_HD PageLayout page_layout(int d, int vb) {
 // 128*half + 16s + 8sub + 2c + e, with pair index q = 2s + sub. Masking bits q and q + 16 of a word
 // gives the f16 pair of m16n8k16 operand A (rows = tokens, k = coordinates). For q < 12 each half is
 // exactly 2^(q-24) when set; pairs 12..15 are shifted down by 4 first.
+// head_dim 64 has 4 pair indices per tile, so one word holds both tiles of a 32-token group: KBITS is
+// [group 4][plane 3][lane 32][row 2] u32 and the odd tile sits 8 bit positions higher (the decoder
+// shifts it down by 8 first).
 TQ_HD void kbit_loc(int d, int t, int j, int pi, int& word, int& bit) {
   const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
   const int half = j >> 7, jj = j & 127;
   const int s = jj >> 4, sub = (jj >> 3) & 1, c = (jj >> 1) & 3, e = jj & 1;
+  if (d == 64) {
+    word = (((tile >> 1) * 3 + pi) * 32 + 4 * g + c) * 2 + r;
+    bit = 2 * s + sub + 8 * (tile & 1) + 16 * e;
+    return;
+  }
   word = ((((tile * 3 + pi) * (d >> 7) + half) * 32) + 4 * g + c) * 2 + r;
   bit = 2 * s + sub + 16 * e;
 }

@@ -29,6 +29,28 @@ struct AppendArgs {
   int full;   // 1: full_tq mode (ring_size 0): every appended token is quantised by the append itself
 };
 
+// Load 2 consecutive coordinates of one token of the source stream (ring bf16 or input bf16/f32).
+__device__ __forceinline__ void load2(const AppendArgs& a, int which, int slot, int b, int h, int pos, int L, int Np,
+                                      int j, float (&o)[2]) {
+  const int d = a.lv.d;
+  uint32_t u;
+  if (pos < L) {  // still in the ring: ring index pos - Np
+    u = *reinterpret_cast<const uint32_t*>(a.lv.ring + ((((size_t)slot * a.lv.Hkv + h) * 2 + which) * kPage + (pos - Np)) * d + j);
+  } else {
+    const size_t off = (((size_t)b * a.max_new + (pos - L)) * a.lv.Hkv + h) * d + j;
+    const void* base = which ? a.v : a.k;
+    if (a.dt != 0) {
+      const float2 f = *reinterpret_cast<const float2*>(static_cast<const float*>(base) + off);
+      o[0] = f.x;
+      o[1] = f.y;
+      return;
+    }
+    u = *reinterpret_cast<const uint32_t*>(static_cast<const uint16_t*>(base) + off);
+  }
+  o[0] = __uint_as_float(u << 16);
+  o[1] = __uint_as_float(u & 0xffff0000u);
+}
+
 // Load 4 consecutive coordinates of one token of the source stream (ring bf16 or input bf16/f32).
 __device__ __forceinline__ void load4(const AppendArgs& a, int which, int slot, int b, int h, int pos, int L, int Np,
                                       int j, float (&o)[4]) {
@@ -89,6 +111,42 @@ __device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int
   return true;
 }
 
+// Bits of plane pi of one token's key codes kc (coordinates 16 sq + 8 sub + 2c + e of a 128-coordinate
+// half, sq < nsq) at bit 2 sq + sub + 16 e (+ shift) of a KBITS word (see kbit_loc).
+__device__ __forceinline__ uint32_t kbits_field(const uint8_t* kc, int pi, int nsq, int shift) {
+  uint32_t word = 0;
+  for (int sq = 0; sq < nsq; ++sq)
+#pragma unroll
+    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int code = kc[16 * sq + 8 * sub + e];
+        const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
+        word |= (uint32_t)bit << (2 * sq + sub + 16 * e + shift);
+      }
+  return word;
+}
+
+// One token of the source stream in the lane_coord layout (D / 32 values per lane).
+template <int D>
+__device__ __forceinline__ void load_token(const AppendArgs& a, int which, int slot, int b, int h, int pos, int L,
+                                           int Np, int lane, float (&x)[D / 32]) {
+  if (D == 64) {
+    float o[2];
+    load2(a, which, slot, b, h, pos, L, Np, 2 * lane, o);
+    x[0] = o[0];
+    x[D / 32 - 1] = o[1];
+  } else {
+#pragma unroll
+    for (int hh = 0; hh < D / 128; ++hh) {
+      float o[4];
+      load4(a, which, slot, b, h, pos, L, Np, 128 * hh + 4 * lane, o);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) x[(4 * hh + e) % (D / 32)] = o[e];
+    }
+  }
+}
+
 // Shared-memory arrays of the CUDA-core quantiser: S^T (bf16 pairs), per-token key codes
 // (idx | sign << 2), value codes, {n, gamma} and value scales of a page, and one fp32 row per warp.
 template <int D>
@@ -131,7 +189,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
   }
   float Dv[NE], cent[4], bnd[3];
 #pragma unroll
-  for (int e = 0; e < NE; ++e) Dv[e] = lv.D[(e >> 2) * 128 + 4 * lane + (e & 3)];
+  for (int e = 0; e < NE; ++e) Dv[e] = lv.D[lane_coord<D>(e, lane)];
 #pragma unroll
   for (int i = 0; i < 4; ++i) cent[i] = lv.cb[i];
 #pragma unroll
@@ -145,13 +203,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
     const int pos = pg * kPage + t;
     float x[NE], y[NE];
     if (t < valid) {
-#pragma unroll
-      for (int hh = 0; hh < NE / 4; ++hh) {
-        float o[4];
-        load4(a, 0, slot, b, h, pos, L, Np, 128 * hh + 4 * lane, o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[4 * hh + e] = o[e];
-      }
+      load_token<D>(a, 0, slot, b, h, pos, L, Np, lane, x);
     } else {
 #pragma unroll
       for (int e = 0; e < NE; ++e) x[e] = 0.f;
@@ -174,7 +226,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
       const int idx = (yy > bnd[0]) + (yy > bnd[1]) + (yy > bnd[2]);
       const float res = yy - cent[idx];
       rr = fmaf(res, res, rr);
-      const int j = (e >> 2) * 128 + 4 * lane + (e & 3);
+      const int j = lane_coord<D>(e, lane);
       r[j] = res;
       kc[j] = (uint8_t)idx;
     }
@@ -210,21 +262,40 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
     }
     // ---- value: v' = Pi v, symmetric mid-rise groups of 32, fp16 scale ----
     if (t < valid) {
+      load_token<D>(a, 1, slot, b, h, pos, L, Np, lane, x);
 #pragma unroll
-      for (int hh = 0; hh < NE / 4; ++hh) {
-        float o[4];
-        load4(a, 1, slot, b, h, pos, L, Np, 128 * hh + 4 * lane, o);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) x[4 * hh + e] = o[e] * Dv[4 * hh + e];
-      }
+      for (int e = 0; e < NE; ++e) x[e] *= Dv[e];
     } else {
 #pragma unroll
       for (int e = 0; e < NE; ++e) x[e] = 0.f;
     }
     warp_fwht<NE>(x, lane);
     uint8_t* vc = vcode + t * D;
+    if (D == 64) {  // a group of 32 coordinates is 16 lanes x 2
+      float am = 0.f;
 #pragma unroll
-    for (int hh = 0; hh < NE / 4; ++hh) {
+      for (int e = 0; e < NE; ++e) {
+        x[e] *= inv_sqrt_d;
+        am = fmaxf(am, fabsf(x[e]));
+      }
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+      const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
+      const __half sh = __float2half_rn(s32);
+      const float s = __half2float(sh);
+#pragma unroll
+      for (int e = 0; e < NE; ++e) {
+        int code = vhalf;
+        if (s > 0.f) {
+          const float qv = floorf(__fdiv_rn(x[e], s));
+          code = (int)fminf(fmaxf(qv, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
+        }
+        vc[lane_coord<D>(e, lane)] = (uint8_t)code;
+      }
+      if ((lane & 15) == 0) scales[t * (D / 32) + (lane >> 4)] = __half_as_ushort(sh);
+    }
+#pragma unroll
+    for (int hh = 0; hh < (D == 64 ? 0 : NE / 4); ++hh) {
       float am = 0.f;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -278,8 +349,18 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
   }
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-  constexpr int HALVES = D / 128;
-  for (int w = (t0 / 16) * 192 * HALVES + tid; w < (t1 / 16) * 192 * HALVES; w += kQThreads) {
+  constexpr int HALVES = D >= 128 ? D / 128 : 1;  // 128-coordinate halves (the head_dim 64 words are below)
+  if (D == 64) {  // one word holds both 16-token tiles of the block: [group][plane][lane][row]
+    for (int w = q32 * 192 + tid; w < (q32 + 1) * 192; w += kQThreads) {
+      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3;
+      uint32_t word = 0;
+#pragma unroll
+      for (int kap = 0; kap < 2; ++kap)
+        word |= kbits_field(kcode + (32 * q32 + 16 * kap + (ln >> 2) + 8 * r) * D + 2 * (ln & 3), pi, 4, 8 * kap);
+      kw[w] = word;
+    }
+  }
+  for (int w = (t0 / 16) * 192 * HALVES + tid; D >= 128 && w < (t1 / 16) * 192 * HALVES; w += kQThreads) {
     const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % 3;
     const int tile = w / (192 * HALVES);
     const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
@@ -345,7 +426,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
 template <int D>
 __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np,
                                                     int pg, int t_lo, int t_hi, uint8_t* smem) {
-  constexpr int HALVES = D / 128;
+  constexpr int HALVES = D >= 128 ? D / 128 : 1;  // 128-coordinate halves (head_dim 64: see below)
   const QSmem<D> sm(smem);
   code_tokens<D>(a, b, h, slot, L, Np, pg, t_hi, t_lo, t_hi, sm);
   const int tid = threadIdx.x;
@@ -358,7 +439,23 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
   }
   const PageLayout pl = page_layout(D, vb);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-  for (int i = tid; i < ntok * 12 * HALVES; i += kQThreads) {  // (token, plane, half, c)
+  if (D == 64) {  // a word holds two tokens (both tiles of the block): replace the new tokens' fields
+    const int grp = t_lo >> 5;
+    for (int w = grp * 192 + tid; w < (grp + 1) * 192; w += kQThreads) {
+      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3;
+      uint32_t mask = 0, bits = 0;
+#pragma unroll
+      for (int kap = 0; kap < 2; ++kap) {
+        const int t = 32 * grp + 16 * kap + (ln >> 2) + 8 * r;
+        if (t >= t_lo && t < t_hi) {
+          mask |= 0x00FF00FFu << (8 * kap);
+          bits |= kbits_field(sm.kcode + t * D + 2 * (ln & 3), pi, 4, 8 * kap);
+        }
+      }
+      if (mask) kw[w] = (kw[w] & ~mask) | bits;
+    }
+  }
+  for (int i = tid; D >= 128 && i < ntok * 12 * HALVES; i += kQThreads) {  // (token, plane, half, c)
     const int c = i & 3, hf = (i >> 2) % HALVES, pi = (i / (4 * HALVES)) % 3, t = t_lo + i / (12 * HALVES);
     const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
     const uint8_t* kc = sm.kcode + t * D + 128 * hf + 2 * c;
@@ -1080,6 +1177,7 @@ cudaError_t launch_append_small_d(const AppendArgs& a, int batch, size_t smem, c
 }
 
 cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
+  if (a.lv.d == 64) return launch_quantize_d<64>(a, batch, pages, s);
   if (a.lv.d == 128) return launch_quantize_d<128>(a, batch, pages, s);
   return launch_quantize_d<256>(a, batch, pages, s);
 }
@@ -1137,8 +1235,9 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.flush = 0;
   a.full = ctx->cfg.ring_size == 0;
   if (max_new < kPage) {  // decode-sized appends: one launch (page on ring overflow + ring rows + state)
-    const size_t smem = a.lv.d == 128 ? quantize_smem_bytes<128>() : quantize_smem_bytes<256>();
-    return a.lv.d == 128 ? launch_append_small_d<128>(a, batch, smem, s) : launch_append_small_d<256>(a, batch, smem, s);
+    if (a.lv.d == 64) return launch_append_small_d<64>(a, batch, quantize_smem_bytes<64>(), s);
+    if (a.lv.d == 128) return launch_append_small_d<128>(a, batch, quantize_smem_bytes<128>(), s);
+    return launch_append_small_d<256>(a, batch, quantize_smem_bytes<256>(), s);
   }
   const int pages = (max_new + kPage - 1) / kPage;
   cudaError_t e = (a.lv.d == 128 && max_new >= kPage && dt == 0)

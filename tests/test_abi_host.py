@@ -29,7 +29,7 @@ def test_library_exports_every_header_function():
 
 
 @pytest.mark.parametrize("field,value,status", [
-    ("head_dim", 64, _abi.TQ_ERR_UNSUPPORTED), ("head_dim", 96, _abi.TQ_ERR_UNSUPPORTED),
+    ("head_dim", 32, _abi.TQ_ERR_UNSUPPORTED), ("head_dim", 96, _abi.TQ_ERR_UNSUPPORTED),
     ("value_bits", 3, _abi.TQ_ERR_UNSUPPORTED), ("key_bits", 4, _abi.TQ_ERR_UNSUPPORTED),
     ("value_group", 64, _abi.TQ_ERR_UNSUPPORTED), ("ring_size", 64, _abi.TQ_ERR_UNSUPPORTED),
     ("ring_size", -1, _abi.TQ_ERR_UNSUPPORTED),
@@ -90,7 +90,7 @@ def test_null_and_host_only_misuse_is_rejected():
     assert lib.tq_ring_flush(h.ctx, 0, None, 1, None) == _abi.TQ_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("seed", [0, 1, 12345])
 def test_tables_match_oracle_bitwise(d, seed):
     h = tqm.HostTables(tqm.config(head_dim=d, seed=seed))
@@ -106,7 +106,8 @@ def test_tables_match_oracle_bitwise(d, seed):
     assert np.array_equal(c.astype(np.float32), np.array(g["centroids"]).astype(np.float32))
 
 
-@pytest.mark.parametrize("d,vb,expect", [(128, 2, 92), (128, 4, 124), (256, 2, 180), (256, 4, 244)])
+@pytest.mark.parametrize("d,vb,expect", [(64, 2, 48), (64, 4, 64), (128, 2, 92), (128, 4, 124), (256, 2, 180),
+                                         (256, 4, 244)])
 def test_page_bytes_equal_canonical_records(d, vb, expect):
     h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
     assert h.key_record_bytes() + h.value_record_bytes() == expect
@@ -119,7 +120,7 @@ def _random_records(h, n, rng):
     return kr, vr
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2), (256, 4)])
+@pytest.mark.parametrize("d,vb", [(64, 2), (64, 4), (128, 2), (128, 4), (256, 2), (256, 4)])
 def test_records_page_round_trip(d, vb):
     h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
     rng = np.random.default_rng(d + vb)
@@ -140,7 +141,7 @@ def _unpack(rec, bits, d):
     return ((b[:, :, None] >> sh) & ((1 << bits) - 1)).reshape(rec.shape[0], d)
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2), (256, 4)])
+@pytest.mark.parametrize("d,vb", [(64, 2), (64, 4), (128, 2), (128, 4), (256, 2), (256, 4)])
 def test_decoder_operand_extraction_matches_records(d, vb):
     """Emulate, on the CPU, how the decode kernel cuts mma.sync operands out of a page.
 
@@ -158,15 +159,20 @@ def test_decoder_operand_extraction_matches_records(d, vb):
     codes = _unpack(vr, vb, d)
     planes = [(idx >> 1) & 1, idx & 1, sign]
     kw = page[:3 * 128 * d // 8].view(np.uint32)
-    halves = d // 128
+    halves = max(1, d // 128)
     for tile in range(8):
         for pi in range(3):
             for hf in range(halves):
                 for lane in range(32):
                     g, c = lane >> 2, lane & 3
-                    base = (((tile * 3 + pi) * halves + hf) * 32 + lane) * 2
-                    w0, w1 = int(kw[base]), int(kw[base + 1])  # rows g and g + 8 of the tile
-                    for s_ in range(8):
+                    if d == 64:  # both tiles of a 32-token group share a word; the odd one 8 positions up
+                        base = (((tile >> 1) * 3 + pi) * 32 + lane) * 2
+                        sh = 8 * (tile & 1)
+                    else:
+                        base = (((tile * 3 + pi) * halves + hf) * 32 + lane) * 2
+                        sh = 0
+                    w0, w1 = int(kw[base]) >> sh, int(kw[base + 1]) >> sh  # rows g and g + 8 of the tile
+                    for s_ in range(min(8, d // 16)):
                         if s_ < 6:
                             x0, x1, q0 = w0, w1, 2 * s_
                         else:

@@ -37,7 +37,8 @@ def test_tiny_single_head_config():
     assert cache.check_status() == 0
 
 
-@pytest.mark.parametrize("d,vb,G", [(128, 2, 4), (128, 4, 4), (256, 2, 4), (256, 4, 2), (128, 2, 1)])
+@pytest.mark.parametrize("d,vb,G", [(128, 2, 4), (128, 4, 4), (256, 2, 4), (256, 4, 2), (128, 2, 1), (64, 2, 4),
+                                    (64, 4, 2)])
 def test_ragged_batch_appends_and_decode(d, vb, G):
     """Ragged lengths across several tiles and a ragged tail: 1, 127, 128, 129, 300, 1000 tokens,
     built by a prefill append and then single-token decode appends (ring overflow and flush)."""
@@ -139,7 +140,7 @@ def test_full_size_llama_layer_sampled():
             assert rel_l2(out[0, h * G + g], ref[g]) <= 2e-3
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2)])
+@pytest.mark.parametrize("d,vb", [(128, 2), (128, 4), (256, 2), (64, 4)])
 def test_bulk_append_onto_a_partial_ring(d, vb):
     """Bulk appends (>= 128 tokens) onto sequences whose ring is partly full: the first page written
     takes its leading tokens from the ring and the rest from the new input; later pages come from the
@@ -175,7 +176,7 @@ def test_bulk_append_onto_a_partial_ring(d, vb):
             assert rel_l2(out[i, hq], ref[hq]) <= 2e-3
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4)])
+@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4), (64, 2)])
 def test_full_tq_mode_appends_and_decode(d, vb):
     """full_tq mode (ring_size 0, [Guide] §三): every appended token is quantised by its own append and
     decode reads packed tokens only. A bulk prefill of 300 tokens, three single-token appends, then an
@@ -206,7 +207,7 @@ def test_full_tq_mode_appends_and_decode(d, vb):
             assert rel_l2(out[0, hq], ref[hq]) <= 2e-3, (L, hq, rel_l2(out[0, hq], ref[hq]))
 
 
-@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4)])
+@pytest.mark.parametrize("d,vb", [(128, 2), (256, 4), (64, 4)])
 def test_paged_cache_scrambled_block_table(d, vb):
     """Paged cache (n_blocks > 0): three sequences (300, 129 and 1000 tokens, then two single-token
     appends) share one pool of 24 blocks through a scrambled block table. Their pages are byte-identical
