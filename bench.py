@@ -313,7 +313,8 @@ def run_ours(args):
     kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
     kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
-    traffic = None if full or paged else profiled_traffic()  # the committed ncu summary is of the hybrid step
+    # the committed ncu summary is of the default (hybrid, contiguous, head_dim 128) step
+    traffic = None if full or paged or d != 128 else profiled_traffic()
 
     # ---- end to end through the public API with pinned host buffers ----
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
@@ -375,7 +376,7 @@ def run_ours(args):
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged:  # the oracle sample: hybrid step
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged and d == 128:  # oracle sample
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -559,6 +560,8 @@ def main():
     p.add_argument("--skip-quantize", action="store_true")
     p.add_argument("--mode", default="hybrid", choices=["hybrid", "full_tq"],
                    help="full_tq: no exact recent buffer, every token quantised on append")
+    p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
+                   help="the same decode and prefill shapes with another head_dim (synthetic variants)")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
                    help="paged: the packed pages live in a block pool addressed through a scrambled block table")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -566,6 +569,10 @@ def main():
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
                    help="only run one layer of the prefill quantisation PASSES times (for profilers)")
     args = p.parse_args()
+    if args.head_dim != 128:
+        WL.update(d=args.head_dim, name=f"llama3.1-8b-shaped decode with head_dim {args.head_dim}, batch 1, "
+                                        f"context 32768, K3/V2")
+        PREFILL.update(d=args.head_dim)
     if args.warmup < 3:
         args.warmup = 3
     if args.profile_quantize:
