@@ -147,46 +147,59 @@ __device__ __forceinline__ void load_token(const AppendArgs& a, int which, int s
   }
 }
 
-// Shared-memory arrays of the CUDA-core quantiser: S^T (bf16 pairs), per-token key codes
-// (idx | sign << 2), value codes, {n, gamma} and value scales of a page, and one fp32 row per warp.
+// Shared-memory arrays of the CUDA-core quantiser: per-token key codes (idx | sign << 2), value codes,
+// {n, gamma} and value scales of a page, and the f16 hi / lo split of the residuals of one 32-token
+// block (rows padded by 8 halves: conflict-free B-fragment reads).
+template <int D>
+constexpr int kRStride = D + 8;
 template <int D>
 struct QSmem {
-  uint32_t* st2;     // [D][D/2]
   uint8_t* kcode;    // [128][D]
   uint8_t* vcode;    // [128][D]
   uint32_t* norms;   // [128] n16 | gamma16 << 16
   uint16_t* scales;  // [128][D/32]
-  float* rbuf;       // [8 warps][D]
+  __half* rh;        // [32][kRStride] residual * 2^8, f16
+  __half* rl;        // [32][kRStride] residual * 2^8 - rh, f16
   __device__ explicit QSmem(uint8_t* smem)
-      : st2(reinterpret_cast<uint32_t*>(smem)),
-        kcode(smem + 2 * D * D),
+      : kcode(smem),
         vcode(kcode + kPage * D),
         norms(reinterpret_cast<uint32_t*>(vcode + kPage * D)),
         scales(reinterpret_cast<uint16_t*>(norms + kPage)),
-        rbuf(reinterpret_cast<float*>(scales + kPage * (D / 32))) {}
+        rh(reinterpret_cast<__half*>(scales + kPage * (D / 32))),
+        rl(rh + 32 * kRStride<D>) {}
 };
+template <int D>
+constexpr size_t quantize_smem_bytes_d() {
+  return 2 * kPage * D + 4 * kPage + 2 * kPage * (D / 32) + 2 * 2 * 32 * kRStride<D>;
+}
 
-// Codes tokens [t_begin, t_end) of page pg of (row b, KV head h) into the shared-memory arrays, one
-// warp per token, after staging S^T (bf16) in shared memory. The page's first `valid` tokens come
-// from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
-// zero vectors. Run by all kQThreads threads of the CTA; ends with a block barrier.
+// D += A B, m16n8k16, f16 operands, f32 accumulate.
+__device__ __forceinline__ void mma_f16_acc(float (&c)[4], const uint4& a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w), "r"(b0), "r"(b1));
+}
+
+// Codes tokens [t_begin, t_end) of page pg of (row b, KV head h), all inside one 32-token block, into
+// the shared-memory arrays: one warp per token for the norm, rotation, index, residual and value
+// codes, then the QJL projection z = S r of the whole block as one f16 mma.sync GEMM (A = S from the
+// f16 fragment table, B = the residuals scaled by 2^8 and split into f16 hi + lo; the scale leaves the
+// signs unchanged). The page's first `valid` tokens come from the ring (positions below L) and then
+// from the new input; tokens past `valid` are coded as zero vectors. Run by all kQThreads threads of
+// the CTA; ends with a block barrier.
 template <int D>
 __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
                                             int valid, int t_begin, int t_end, const QSmem<D>& sm) {
   constexpr int NE = D / 32;  // coordinates per lane
-  uint32_t* st2 = sm.st2;
+  constexpr int RS = kRStride<D>;
   uint8_t* kcode = sm.kcode;
   uint8_t* vcode = sm.vcode;
   uint32_t* norms = sm.norms;
   uint16_t* scales = sm.scales;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tb = t_begin & ~31;  // the block's first token
   const LayerView& lv = a.lv;
-  // stage S^T (bf16) in shared memory
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(lv.St);
-    uint4* dst = reinterpret_cast<uint4*>(st2);
-    for (int i = tid; i < D * D / 8; i += kQThreads) dst[i] = src[i];
-  }
   float Dv[NE], cent[4], bnd[3];
 #pragma unroll
   for (int e = 0; e < NE; ++e) Dv[e] = lv.D[lane_coord<D>(e, lane)];
@@ -194,11 +207,9 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
   for (int i = 0; i < 4; ++i) cent[i] = lv.cb[i];
 #pragma unroll
   for (int i = 0; i < 3; ++i) bnd[i] = lv.cb[4 + i];
-  __syncthreads();
 
   const int vb = lv.vb, vhalf = 1 << (vb - 1);
   const float inv_sqrt_d = rsqrtf((float)D);
-  float* r = sm.rbuf + warp * D;
   for (int t = t_begin + warp; t < t_end; t += kQThreads / 32) {
     const int pos = pg * kPage + t;
     float x[NE], y[NE];
@@ -227,35 +238,14 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
       const float res = yy - cent[idx];
       rr = fmaf(res, res, rr);
       const int j = lane_coord<D>(e, lane);
-      r[j] = res;
+      const float rs = res * 256.f;
+      const __half hi = __float2half_rn(rs);
+      sm.rh[(t - tb) * RS + j] = hi;
+      sm.rl[(t - tb) * RS + j] = __float2half_rn(rs - __half2float(hi));
       kc[j] = (uint8_t)idx;
     }
     rr = warp_sum(rr);
     const float gamma = sqrtf(rr);
-    __syncwarp();
-    // ---- QJL: z = S r; lane owns rows 2l, 2l+1 (+64m) ----
-    {
-      constexpr int NR = D / 64;  // row pairs per lane
-      float z0[NR], z1[NR];
-#pragma unroll
-      for (int m = 0; m < NR; ++m) z0[m] = z1[m] = 0.f;
-      for (int jj = 0; jj < D; ++jj) {
-        const float rj = r[jj];
-#pragma unroll
-        for (int m = 0; m < NR; ++m) {
-          const uint32_t s = st2[jj * (D / 2) + lane + 32 * m];
-          z0[m] = fmaf(__uint_as_float(s << 16), rj, z0[m]);
-          z1[m] = fmaf(__uint_as_float(s & 0xffff0000u), rj, z1[m]);
-        }
-      }
-      __syncwarp();
-#pragma unroll
-      for (int m = 0; m < NR; ++m) {
-        const int i0 = 2 * lane + 64 * m;
-        kc[i0] = (uint8_t)(kc[i0] | ((z0[m] >= 0.f) << 2));
-        kc[i0 + 1] = (uint8_t)(kc[i0 + 1] | ((z1[m] >= 0.f) << 2));
-      }
-    }
     if (lane == 0) {
       const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(gamma);
       norms[t] = (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
@@ -318,6 +308,36 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
         vc[128 * hh + 4 * lane + e] = (uint8_t)code;
       }
       if ((lane & 7) == 0) scales[t * (D / 32) + 4 * hh + (lane >> 3)] = __half_as_ushort(sh);
+    }
+  }
+  __syncthreads();
+  // ---- QJL: Z^T = S R^T for the block; warp task = one 16-row m-tile of S x NTW 8-token n-tiles ----
+  {
+    constexpr int MTS = D / 16, NTW = D >= 128 ? 4 : 2;
+    const int g = lane >> 2, c = lane & 3;
+    for (int u = warp; u < MTS * (4 / NTW); u += kQThreads / 32) {
+      const int mt = u % MTS, nt0 = (u / MTS) * NTW;
+      float z[NTW][4];
+#pragma unroll
+      for (int n = 0; n < NTW; ++n) z[n][0] = z[n][1] = z[n][2] = z[n][3] = 0.f;
+      for (int ks = 0; ks < D / 16; ++ks) {
+        const uint4 A = lv.S_frag[sfrag_idx(D, mt, ks, lane)];
+#pragma unroll
+        for (int n = 0; n < NTW; ++n) {
+          const int row = (8 * (nt0 + n) + g) * RS + 16 * ks + 2 * c;
+          mma_f16_acc(z[n], A, *reinterpret_cast<const uint32_t*>(sm.rh + row),
+                      *reinterpret_cast<const uint32_t*>(sm.rh + row + 8));
+          mma_f16_acc(z[n], A, *reinterpret_cast<const uint32_t*>(sm.rl + row),
+                      *reinterpret_cast<const uint32_t*>(sm.rl + row + 8));
+        }
+      }
+#pragma unroll
+      for (int n = 0; n < NTW; ++n)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int t = tb + 8 * (nt0 + n) + 2 * c + (i & 1), row = 16 * mt + g + 8 * (i >> 1);
+          if (t >= t_begin && t < t_end) kcode[t * D + row] = (uint8_t)(kcode[t * D + row] | ((z[n][i] >= 0.f) << 2));
+        }
     }
   }
   __syncthreads();
@@ -1148,7 +1168,7 @@ __global__ void k_reset(int32_t* state_base, int n_layers, int max_seqs, int lay
 
 template <int D>
 size_t quantize_smem_bytes() {
-  return 2 * D * D + 2 * kPage * D + 4 * kPage + 2 * kPage * (D / 32) + 4 * 8 * D;
+  return quantize_smem_bytes_d<D>();
 }
 
 template <int D>
