@@ -184,6 +184,24 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream);
 
+/* tq_prefill_attention: attention of a prefill chunk over the cache of one layer. The chunk's tokens
+ * must already be appended (tq_quantize_append); row b's queries are its sequence's last d_n_q[b]
+ * tokens. Query i of the row (position L - n_q + i) attends causally to every position up to its own,
+ * through the same estimator as tq_decode_attention: packed tokens through their codes, ring tokens
+ * exactly ([Guide] §七: prefill attention; here over the packed history).
+ *   - q: device bf16 [batch][q_per_row][n_q_heads][d]; out: device f32 of the same shape. Queries
+ *     i >= d_n_q[b] of a row are padding: their outputs are zero.
+ *   - d_n_q[b] in [0, q_per_row] and at most the row's length; d_seq_ids as for decode.
+ *   - d_workspace: at least tq_prefill_workspace_bytes(ctx, batch, q_per_row, max_ctx_hint) bytes,
+ *     256-byte aligned; its arrival counters are zeroed by every call (one memset).
+ *   - batch * q_per_row <= 65535.
+ *   - Launches: the memset and one split-K decode kernel over batch * q_per_row query rows (the
+ *     rows of one sequence read the same pages, mostly from L2). */
+size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint);
+tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                               const int32_t* d_n_q, int batch, int q_per_row, float softmax_scale,
+                               void* d_workspace, size_t workspace_bytes, int max_ctx_hint, tq_stream_t stream);
+
 /* tq_decode_attention_noalloc: the same decode step as tq_decode_attention, for callers that cannot
  * allocate device memory when they decode. Examples: code on a path where cudaMalloc's implicit
  * synchronisation is forbidden, or a host runtime that owns all device memory and only hands over the

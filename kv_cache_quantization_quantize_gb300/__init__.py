@@ -145,6 +145,24 @@ class TurboQuantCache(HostTables):
                                            float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint, _stream(stream)))
         return out
 
+    def prefill_workspace(self, batch, q_per_row, max_ctx_hint=0):
+        n = self.lib.tq_prefill_workspace_bytes(self.ctx, batch, q_per_row, max_ctx_hint)
+        return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
+
+    def prefill(self, layer, q, seq_ids, n_q, softmax_scale=0.0, out=None, max_ctx_hint=0, workspace=None,
+                stream=None):
+        """Chunk attention after its append: q [batch, q_per_row, n_q_heads, d] bf16 (a row's last n_q[b]
+        tokens; the rest padding) -> out [batch, q_per_row, n_q_heads, d] f32, causal over the cache."""
+        assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous() and q.dim() == 4
+        batch, qpr = q.shape[0], q.shape[1]
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        ws = workspace if workspace is not None else self.prefill_workspace(batch, qpr, max_ctx_hint)
+        check(self.lib.tq_prefill_attention(self.ctx, layer, _ptr(q), _ptr(out), _ptr(seq_ids), _ptr(n_q), batch, qpr,
+                                            float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint,
+                                            _stream(stream)))
+        return out
+
     def decode_phase(self, phase, layer, q, seq_ids, out, softmax_scale=0.0, max_ctx_hint=0, workspace=None,
                      stream=None):
         """One phase (0 prep, 1 splits, 2 combine) of decode(); the three in order equal decode()."""

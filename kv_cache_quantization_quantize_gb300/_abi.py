@@ -36,6 +36,9 @@ _SIGS = {
     "tq_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int]),
     "tq_decode_attention": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p, c_size_t,
                                     c_int, c_void_p]),
+    "tq_prefill_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int, c_int]),
+    "tq_prefill_attention": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_float,
+                                     c_void_p, c_size_t, c_int, c_void_p]),
     "tq_decode_phase": (c_int, [c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p,
                                 c_size_t, c_int, c_void_p]),
     "tq_decode_attention_noalloc": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_int,

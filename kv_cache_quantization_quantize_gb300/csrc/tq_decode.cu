@@ -29,6 +29,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct DecodeArgs {
   LayerView lv;
+  int qpr;              // queries per cache row: 1 for decode; > 1 for prefill (row b = batch row b / qpr)
+  const int32_t* n_q;   // prefill: queries of each batch row (its last n_q tokens); nullptr for decode
   const uint16_t* q;  // bf16 [B][Hq][D]
   float* out;         // [B][Hq][D]
   const int32_t* seq_ids;
@@ -126,6 +128,16 @@ __device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L
   const int F = lv.state[2 * slot + 1];
   Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
   P = Np + F;
+}
+
+// Cache slot of (virtual) row b, and the number of the sequence's tokens it attends to: all L for
+// decode; for query i of a prefill chunk of n_q queries (the sequence's last n_q tokens) the first
+// L - (n_q - 1 - i), i.e. every position up to its own (causal); 0 for padding rows (i >= n_q).
+__device__ __forceinline__ int row_slot(const DecodeArgs& a, int b) { return a.seq_ids[a.qpr > 1 ? b / a.qpr : b]; }
+__device__ __forceinline__ int row_len(const DecodeArgs& a, int b, int L) {
+  if (a.qpr <= 1) return L;
+  const int i = b % a.qpr, nq = a.n_q[b / a.qpr];
+  return i < nq ? max(0, L - (nq - 1 - i)) : 0;
 }
 
 template <int D>
@@ -362,7 +374,8 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L, Np, P;
   seq_packed(lv, slot, L, Np, P);
-  const int F = P - Np, R = L - Np, n = R - F;
+  const int Lq = row_len(a, b, L);  // ring tokens are positions P .. Lq - 1
+  const int F = P - Np, n = Lq - P;
   if (n <= 0) {
     write_empty_partial(part, D, tid, NT);
     return;
@@ -630,7 +643,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   float* part = reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                          (((size_t)b * lv.Hkv + h) * (nsp + 1) + sp) * a.plan.part_stride);
   pdl_launch();
-  const int slot = a.seq_ids[b];
+  const int slot = row_slot(a, b);
   if (slot < 0 || slot >= lv.max_seqs) {
     pdl_wait();
     write_empty_partial(part, D, tid, NT);
@@ -645,6 +658,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   }
   int L, Np, P;
   seq_packed(lv, slot, L, Np, P);
+  P = min(P, row_len(a, b, L));  // a prefill query sees the packed tokens before its own position
   const int n_pages = (P + kPage - 1) / kPage;
   const int pps = a.plan.pages_per_split;
   if (sp == 0 && tid == 0 && n_pages > nsp * pps) set_status(lv.status, TQ_DEV_ERR_SPLITS);
@@ -1043,9 +1057,12 @@ int decode_resident_ctas(const tq_ctx* ctx) {
 }
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
-                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s) {
+                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
+                          const int32_t* n_q) {
   DecodeArgs a;
   a.lv = layer_view(ctx, layer);
+  a.qpr = qpr;
+  a.n_q = n_q;
   a.q = static_cast<const uint16_t*>(q);
   a.out = out;
   a.seq_ids = seq_ids;

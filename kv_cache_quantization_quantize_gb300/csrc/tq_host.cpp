@@ -269,7 +269,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   return v;
 }
 
-DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows) {
   const tq_config& c = ctx->cfg;
   const int hint = (max_ctx_hint <= 0 || max_ctx_hint > c.max_ctx) ? c.max_ctx : max_ctx_hint;
   const int max_pages = std::max(1, (hint + kPage - 1) / kPage);
@@ -289,7 +289,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   // The arrival counters sit at a fixed place (offset 0, sized for max_seqs rows), so that calls with
   // other batch sizes or hints on the same workspace find them where the last call left them (zero).
   p.cnt_off = 0;
-  p.part_off = align_up(sizeof(int32_t) * (size_t)c.max_seqs * c.n_kv_heads, 256);
+  p.part_off = align_up(sizeof(int32_t) * (size_t)std::max(c.max_seqs, cnt_rows) * c.n_kv_heads, 256);
   p.part_stride = align_up((size_t)(2 * kMaxG + kMaxG * d) * sizeof(float), 16);
   p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
   return p;
@@ -510,6 +510,40 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint) {
 static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                                int max_ctx_hint, tq_stream_t stream);
+
+size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
+  if (!ctx || batch < 1 || q_per_row < 1 || (long long)batch * q_per_row > 65535) return 0;
+  const int rows = batch * q_per_row;
+  return tq::decode_plan(ctx, rows, max_ctx_hint, rows).bytes;
+}
+
+tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
+                               const int32_t* d_n_q, int batch, int q_per_row, float softmax_scale,
+                               void* d_workspace, size_t workspace_bytes, int max_ctx_hint, tq_stream_t stream) {
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (batch < 0 || q_per_row < 1) return fail(TQ_ERR_INVALID_ARG, "batch %d / q_per_row %d", batch, q_per_row);
+  if (batch == 0) return ok();
+  if ((long long)batch * q_per_row > 65535) return fail(TQ_ERR_CAPACITY, "batch * q_per_row above 65535");
+  if (!q || !out || !d_seq_ids || !d_n_q || !d_workspace)
+    return fail(TQ_ERR_INVALID_ARG, "NULL q/out/d_seq_ids/d_n_q/d_workspace");
+  if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
+  const int rows = batch * q_per_row;
+  const tq::DecodePlan plan = tq::decode_plan(ctx, rows, max_ctx_hint, rows);
+  if (workspace_bytes < plan.bytes)
+    return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+  cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, rows, scale, d_workspace, plan, 0,
+                                    (cudaStream_t)stream, q_per_row, d_n_q);  // zero the counters
+  if (e == cudaSuccess)
+    e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, rows, scale, d_workspace, plan, 1, (cudaStream_t)stream,
+                          q_per_row, d_n_q);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "prefill attention kernels");
+}
 
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,

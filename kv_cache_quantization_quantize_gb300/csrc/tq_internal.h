@@ -180,7 +180,8 @@ struct DecodePlan {
                                  // max_seqs rows (left at zero by every call)
   size_t bytes;
 };
-DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint);
+// cnt_rows: rows the arrival counters have room for (at least max_seqs; prefill rows per query).
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows = 0);
 
 // Split-K decode CTAs resident per SM for ctx's (head_dim, value_bits); sets kernel attributes once.
 int decode_resident_ctas(const tq_ctx* ctx);
@@ -196,6 +197,7 @@ cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
 cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
 // phase -1 = all three phases; 0 = prep, 1 = splits, 2 = combine.
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
-                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s);
+                          int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr = 1,
+                          const int32_t* n_q = nullptr);
 
 }  // namespace tq

@@ -32,7 +32,7 @@ from .quant import (
     pack_key_records, unpack_key_records, pack_value_records, unpack_value_records,
     key_record_bytes, value_record_bytes, history_split, cos_sim_report,
 )
-from .attention import decode_attention, estimated_scores, qjl_inner_product_estimate
+from .attention import decode_attention, estimated_scores, prefill_attention, qjl_inner_product_estimate
 from .memory import kv_bytes_dense, kv_bytes_turboquant, kv_bytes_bits_per_element
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -76,3 +76,39 @@ def decode_attention(q, keys, values, ring_k, ring_v, D, S, centroids, softmax_s
     p = np.exp(s)
     p /= np.sum(p, axis=1, keepdims=True)
     return p @ v
+
+
+def prefill_attention(q, keys, values, ring_k, ring_v, L, D, S, centroids, softmax_scale=None):
+    """Causal attention of a chunk's queries over one KV head's cache after the chunk's append.
+
+    q [n_q, G, d]: the sequence's last n_q tokens, so query i sits at position p_i = L - n_q + i.
+    keys / values: records of the P packed tokens (positions 0 .. P-1); ring_k / ring_v [L - P, d]: the
+    exact tokens at positions P .. L-1. Query i attends to every position <= p_i with the decode
+    estimator (packed tokens through their codes, ring tokens exactly). Written as one masked score
+    matrix per head: s[i, t] over all L positions, -inf where t > p_i. Returns [n_q, G, d].
+    """
+    q = np.asarray(q, dtype=np.float64)
+    n_q, G, d = q.shape
+    scale = 1.0 / np.sqrt(d) if softmax_scale is None else float(softmax_scale)
+    Pi = rotation_matrix(D)
+    P = 0 if keys is None else keys.idx.shape[0]
+    ring_k = np.asarray(ring_k, dtype=np.float64).reshape(-1, d)
+    ring_v = np.asarray(ring_v, dtype=np.float64).reshape(-1, d)
+    assert P + ring_k.shape[0] == L and n_q <= L
+    vals = np.concatenate([dequantize_values(values, D) if P else np.zeros((0, d)), ring_v], axis=0)  # [L, d]
+    pos = L - n_q + np.arange(n_q)
+    out = np.zeros((n_q, G, d))
+    for g in range(G):
+        qg = q[:, g, :]                                             # [n_q, d]
+        parts = []
+        if P:
+            q_rot = qg @ Pi.T
+            parts.append(estimated_scores(q_rot, q_rot @ np.asarray(S, dtype=np.float64).T, keys, centroids))
+        parts.append(qg @ ring_k.T)
+        s = scale * np.concatenate(parts, axis=1)                   # [n_q, L]
+        s = np.where(np.arange(L)[None, :] <= pos[:, None], s, -np.inf)
+        s = s - np.max(s, axis=1, keepdims=True)
+        p = np.exp(s)
+        p /= np.sum(p, axis=1, keepdims=True)
+        out[:, g, :] = p @ vals
+    return out

@@ -266,3 +266,53 @@ def test_paged_cache_scrambled_block_table(d, vb):
     k1 = torch.zeros(1, 260, Hkv, d, dtype=torch.bfloat16, device=DEV)
     paged.append(layer, k1, k1, _i32([slots[1]]), _i32([260]))  # 131 -> 391 tokens: writes pages 1 and 2
     assert paged.check_status() & 0x10
+
+
+@pytest.mark.parametrize("d,vb", [(128, 2), (64, 4), (256, 2)])
+def test_prefill_chunk_attention(d, vb):
+    """Chunked prefill: histories of 300 and 129 tokens, then chunks of 200 and 37 tokens appended in
+    one call (the second row padded to 200 queries). Every chunk query attends causally over the cache
+    after the append (packed tokens through their codes, ring tokens exactly), as the oracle's masked
+    prefill attention gives it on the device's own records and ring; padding queries output zeros."""
+    Hkv, G = 2, 4
+    hist, chunk, slots = [300, 129], [200, 37], [1, 0]
+    B, Tq = len(hist), max(chunk)
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2, max_ctx=640,
+                 seed=13)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    seqs = [synth.kv_tokens(h_ + c_, Hkv, d, seed=700 + i, outliers=("random", 4, 10.0))
+            for i, (h_, c_) in enumerate(zip(hist, chunk))]
+    ids = _i32(slots)
+    for lo, lens in ((None, hist), (hist, chunk)):
+        n = max(lens)
+        kb = torch.zeros(B, n, Hkv, d, dtype=torch.bfloat16)
+        vbuf = torch.zeros_like(kb)
+        for i in range(B):
+            o = 0 if lo is None else lo[i]
+            kb[i, :lens[i]] = seqs[i][0][o:o + lens[i]]
+            vbuf[i, :lens[i]] = seqs[i][1][o:o + lens[i]]
+        cache.append(0, kb.to(DEV), vbuf.to(DEV), ids, _i32(lens))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    q = synth.queries(B * Tq, Hkv * G, d, seed=14).view(B, Tq, Hkv * G, d).contiguous()
+    out = cache.prefill(0, q.to(DEV), ids, _i32(chunk)).cpu().numpy()
+    assert cache.check_status() == 0
+    D, S, c, t = tables
+    for i, s_ in enumerate(slots):
+        L, F = cache.state(0, s_)
+        assert L == hist[i] + chunk[i]
+        Np, R = oracle.history_split(L)
+        P = Np + F
+        nq = chunk[i]
+        assert np.all(out[i, nq:] == 0)
+        for h in range(Hkv):
+            kr, vr = cache.records(0, s_, h, P)
+            keys = oracle.unpack_key_records(kr, d)
+            vals = oracle.unpack_value_records(vr, d, vb)
+            rk, rv = cache.ring(0, s_, h)
+            qh = _f64(q[i, :nq, h * G:(h + 1) * G])
+            ref = oracle.prefill_attention(qh, keys, vals, _f64(rk[F:R]), _f64(rv[F:R]), L, D, S, c)
+            for j in range(nq):
+                for g in range(G):
+                    assert rel_l2(out[i, j, h * G + g], ref[j, g]) <= 2e-3, (i, j, h, g)
