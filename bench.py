@@ -431,6 +431,52 @@ def bench_quantize(tqm, synth, dev, args, peak):
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
 
 
+def bench_prefill(args):
+    """Prefill attention of one chunk over the cache: the Llama-3.1-8B shape (8 KV heads, 32 q heads,
+    d=128, K3/V2), one sequence of 32768 tokens whose last `args.prefill_chunk` tokens are the chunk,
+    all 32 layers. Prints one JSON line (query tokens/s); it is not the bench line of the decode step."""
+    import torch
+    import kv_cache_quantization_quantize_gb300 as tqm
+    from kv_cache_quantization_quantize_gb300 import synth
+    dev = torch.device("cuda", 0)
+    L_layers, Hq, Hkv, d, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["ctx"], WL["vb"]
+    Tq = args.prefill_chunk
+    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=1,
+                     max_ctx=ctx, seed=1)
+    cache = tqm.TurboQuantCache(cfg, device=dev)
+    ids = torch.zeros(1, dtype=torch.int32, device=dev)
+    for l in range(L_layers):
+        k, v = synth.kv_tokens(ctx, Hkv, d, seed=1000 + l, outliers=WL["outliers"], device=dev)
+        cache.append(l, k[None].contiguous(), v[None].contiguous(), ids, torch.full((1,), ctx, dtype=torch.int32,
+                                                                                     device=dev))
+        del k, v
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(9)
+    q = torch.randn((L_layers, 1, Tq, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    out = torch.empty((L_layers, 1, Tq, Hq, d), dtype=torch.float32, device=dev)
+    nq = torch.full((1,), Tq, dtype=torch.int32, device=dev)
+    ws = cache.prefill_workspace(1, Tq, ctx)
+    for l in range(L_layers):
+        cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
+    torch.cuda.synchronize()
+    reps = max(1, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        for l in range(L_layers):
+            cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    status = cache.check_status()
+    print(json.dumps({"metric": "prefill attention query tokens/s (all layers)", "value": Tq / (ms * 1e-3),
+                      "unit": "query-tok/s", "ms_per_chunk": ms, "ms_per_layer": ms / L_layers,
+                      "config": {"workload": f"{WL['name']}: prefill chunk of {Tq} queries at the end of a "
+                                             f"{ctx}-token sequence", "layers": L_layers},
+                      "path": "one split-K decode launch over chunk-query rows (causal length per row)",
+                      "device_status": status}), flush=True)
+
+
 def profile_quantize(passes):
     """A small quantise-only run for profilers: one layer of the prefill workload, `passes` times.
 
@@ -560,6 +606,8 @@ def main():
     p.add_argument("--skip-quantize", action="store_true")
     p.add_argument("--mode", default="hybrid", choices=["hybrid", "full_tq"],
                    help="full_tq: no exact recent buffer, every token quantised on append")
+    p.add_argument("--prefill-chunk", type=int, default=0, metavar="TQ",
+                   help="time prefill attention of a TQ-token chunk instead (one JSON line of its own)")
     p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
                    help="the same decode and prefill shapes with another head_dim (synthetic variants)")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
@@ -577,6 +625,8 @@ def main():
         args.warmup = 3
     if args.profile_quantize:
         profile_quantize(args.profile_quantize)
+    elif args.prefill_chunk:
+        bench_prefill(args)
     elif args.oracle_sample:
         oracle_sample_main(args.oracle_sample)
     elif args.impl == "reference":
