@@ -19,6 +19,8 @@ Sources, cited by page title and section throughout:
 Readings of points the pages leave open are listed with each function.
 
 Parity status:
+* The comparison codecs (``codecs``: KIVI 2-bit, Bonsai 1-bit, [Overview] §核心技术解析) are pinned
+  by ``tests/test_oracle_codecs.py``.
 * Every function here is pinned by a ``-m "not gpu"`` test in ``tests/test_oracle_*.py``, except
   the key figure of ``cos_sim_report``. Its page figure (key cos_sim of about 1.000000, [Guide] §六) names no quantity
   that can be reproduced. It is **parity unpinned** and is only reported.
@@ -35,4 +37,5 @@ from .quant import (
 from .attention import decode_attention, estimated_scores, prefill_attention, qjl_inner_product_estimate
 from .memory import kv_bytes_dense, kv_bytes_turboquant, kv_bytes_bits_per_element
 
+from .codecs import bonsai1_dequantize, bonsai1_quantize, kivi2_dequantize, kivi2_quantize
 __all__ = [n for n in dir() if not n.startswith("_")]
