@@ -477,6 +477,60 @@ def bench_prefill(args):
                       "device_status": status}), flush=True)
 
 
+def bench_codec(args):
+    """Comparison codec (KIVI 2-bit or Bonsai 1-bit) over the whole 32K-token KV cache of the
+    Llama-3.1-8B shape: 32 layers x 8 KV heads x 128, one quantise launch per layer (K and V together),
+    then one dequantise launch per layer. Every layer has its own input (134 MB, above L2). Prints one
+    JSON line (tokens/s of quantisation; HBM fraction per launch); it is not the bench line of the decode
+    step."""
+    import torch
+    from kv_cache_quantization_quantize_gb300 import codecs, synth
+    dev = torch.device("cuda", 0)
+    L_layers, Hkv, d, T = args.codec_layers or WL["layers"], WL["hkv"], WL["d"], WL["ctx"]
+    peak, peak_kind = measured_peaks()
+    kv = [synth.kv_tokens(T, Hkv, d, seed=2000 + l, outliers=WL["outliers"], device=dev) for l in range(L_layers)]
+    deq_out = tuple(torch.empty(T, Hkv, d, dtype=torch.bfloat16, device=dev) for _ in range(2))
+    if args.codec == "kivi2":
+        outs = [codecs.kivi2_alloc(T, Hkv, d, dev) for _ in range(L_layers)]
+        quant = lambda l: codecs.kivi2_quantize(kv[l][0], kv[l][1], out=outs[l])
+        dequant = lambda l: codecs.kivi2_dequantize(outs[l], T, Hkv, d, out=deq_out)
+    else:
+        outs = [codecs.bonsai1_alloc(T * Hkv, d, dev) for _ in range(L_layers)]
+        quant = lambda l: codecs.bonsai1_quantize(kv[l][0], kv[l][1], out=outs[l])
+        dequant = lambda l: codecs.bonsai1_dequantize(outs[l], T, Hkv, d, out=deq_out)
+    code_bytes = sum(t.numel() * t.element_size() for t in outs[0].values())
+    in_bytes = 2 * T * Hkv * d * 2
+
+    def timed(fn):
+        for _ in range(max(3, args.warmup)):
+            for l in range(L_layers):
+                fn(l)
+        torch.cuda.synchronize()
+        reps = max(1, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            for l in range(L_layers):
+                fn(l)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    mq, md = timed(quant), timed(dequant)
+    per = lambda ms: (in_bytes + code_bytes) / (ms * 1e-3 / L_layers) / 1e9
+    print(json.dumps({
+        "metric": f"{args.codec} KV quantisation tokens/s (all layers)", "value": T / (mq * 1e-3), "unit": "tok/s",
+        "ms_per_pass": mq, "us_per_launch": 1e3 * mq / L_layers,
+        "roofline": {"bound": "hbm", "achieved": per(mq), "peak": peak, "unit": "GB/s", "frac": per(mq) / peak,
+                     "peak_kind": peak_kind, "bytes_per_launch": in_bytes + code_bytes},
+        "dequantize": {"ms_per_pass": md, "us_per_launch": 1e3 * md / L_layers, "achieved_gbs": per(md),
+                       "frac": per(md) / peak},
+        "stored_bytes_all_layers": code_bytes * L_layers,
+        "config": {"workload": f"{args.codec} over the KV cache of {WL['name'].split(',')[0]}: {T} tokens x {Hkv} KV "
+                               f"heads x {L_layers} layers, d={d}, bf16 in", "l2": "each layer's input exceeds L2"},
+    }), flush=True)
+
+
 def profile_quantize(passes):
     """A small quantise-only run for profilers: one layer of the prefill workload, `passes` times.
 
@@ -612,6 +666,9 @@ def main():
                    help="the same decode and prefill shapes with another head_dim (synthetic variants)")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
                    help="paged: the packed pages live in a block pool addressed through a scrambled block table")
+    p.add_argument("--codec", default="", choices=["", "kivi2", "bonsai1"],
+                   help="time a comparison codec over the 32K-token KV cache instead (one JSON line of its own)")
+    p.add_argument("--codec-layers", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
@@ -627,6 +684,8 @@ def main():
         profile_quantize(args.profile_quantize)
     elif args.prefill_chunk:
         bench_prefill(args)
+    elif args.codec:
+        bench_codec(args)
     elif args.oracle_sample:
         oracle_sample_main(args.oracle_sample)
     elif args.impl == "reference":

@@ -232,6 +232,90 @@ void tq_destroy(tq_ctx* ctx);
 /* Thread-local description of the last error (empty string if none). */
 const char* tq_last_error(void);
 
+/* ---- Comparison codecs (stateless; no context) ----
+ * KIVI 2-bit and Bonsai 1-bit, the two other KV codecs of the TurboQuant-vLLM overview
+ * (§核心技术解析, sizes in §性能表现与实测数据). The overview names the schemes but not their parameters.
+ * These entry points take the plainest reading that gives its table's sizes (KIVI 2-bit 1,024 MB,
+ * Bonsai 1-bit 288 MB for Llama-3.1-8B at 32K tokens).
+ *
+ * Inputs are bf16 K and V laid out [n_tokens][n_heads][head_dim] (row-major, device). Groups never
+ * cross a head. Every pointer is a device pointer owned by the caller, and every call is asynchronous
+ * on `stream`. Returns TQ_ERR_INVALID_ARG for bad sizes, NULL outputs or misaligned pointers; nothing
+ * is launched then. Values at or beyond the fp16 range (|x| >= 65504) are outside the codecs' domain.
+ * Codes are undefined there.
+ *
+ * KIVI 2-bit ([Overview] §KIVI非对称量化):
+ *   - Keys are grouped per channel over 16 consecutive tokens; values per token over 16 consecutive
+ *     channels.
+ *   - Per group: zero z = fp16(min) and scale s = fp16((max - min) / 3), with the difference and
+ *     quotient in fp32.
+ *   - code = clamp(rint((x - z) * (1/s)), 0, 3), each step in fp32 round-to-nearest-even; code 0 if
+ *     s = 0.
+ *   - Reconstruction: x_hat = z + code * s.
+ *   Layouts, with C = n_heads * head_dim:
+ *   - k_codes  uint32 [n_tokens/16][C]: word (g, c) holds tokens 16g..16g+15 of channel c; token 16g+t
+ *     is at bits 2t..2t+1.
+ *   - k_scale, k_zero  fp16 bits [n_tokens/16][C].
+ *   - v_codes  uint32 [n_tokens][C/16]: channel 16j+i is at bits 2i..2i+1 of word (t, j).
+ *   - v_scale, v_zero  fp16 bits [n_tokens][C/16].
+ *   Requirements:
+ *   - head_dim is a multiple of 16. When keys are given, n_tokens is a multiple of 16.
+ *   - k and v are 16-byte aligned; k_codes is 8-byte aligned; k_scale, k_zero and v_codes are 4-byte
+ *     aligned.
+ *   - k or v may be NULL to skip that tensor; its outputs are then unused.
+ *   One launch codes both tensors. */
+tq_status tq_kivi2_quantize(const void* k, const void* v, int n_tokens, int n_heads, int head_dim,
+                            uint32_t* k_codes, uint16_t* k_scale, uint16_t* k_zero, uint32_t* v_codes,
+                            uint16_t* v_scale, uint16_t* v_zero, tq_stream_t stream);
+/* Inverse of tq_kivi2_quantize. It writes bf16 x_hat = z + code * s (computed in fp32, rounded to
+ * nearest even) to k_out and v_out, in the input layout. Either output may be NULL. Alignment is the
+ * same as for tq_kivi2_quantize, with k_out and v_out 16-byte aligned. */
+tq_status tq_kivi2_dequantize(const uint32_t* k_codes, const uint16_t* k_scale, const uint16_t* k_zero,
+                              const uint32_t* v_codes, const uint16_t* v_scale, const uint16_t* v_zero,
+                              int n_tokens, int n_heads, int head_dim, void* k_out, void* v_out,
+                              tq_stream_t stream);
+/* Bonsai 1-bit Q1_0_g128 ([Overview] §Bonsai 1-bit). Each of the n_rows rows (a token's head vector)
+ * splits into groups of 128 channels.
+ *   - bit = 1 where x >= 0.
+ *   - scale = fp16(mean |x|) of the group, the least-squares scale for fixed signs. The sum runs in
+ *     fp32 in a fixed order, so it can sit one fp16 ulp from the exact mean.
+ *   - Reconstruction: x_hat = +scale or -scale.
+ *   Layouts:
+ *   - bits  uint32 [n_rows][head_dim/32]: channel 32w+b is at bit b of word w.
+ *   - scale  fp16 bits [n_rows][head_dim/128].
+ *   Requirements:
+ *   - head_dim is a multiple of 128.
+ *   - k and v are 16-byte aligned; bits are 4-byte aligned.
+ *   - Either input may be NULL.
+ *   One launch codes both tensors. The fp16 residual cache of recent tokens that the overview pairs
+ *   with this codec is the ring of the hybrid mode above; it is not part of these calls. */
+tq_status tq_bonsai1_quantize(const void* k, const void* v, int64_t n_rows, int head_dim, uint32_t* k_bits,
+                              uint16_t* k_scale, uint32_t* v_bits, uint16_t* v_scale, tq_stream_t stream);
+/* Inverse of tq_bonsai1_quantize: bf16 +-scale per channel into k_out and v_out (16-byte aligned;
+ * either may be NULL). */
+tq_status tq_bonsai1_dequantize(const uint32_t* k_bits, const uint16_t* k_scale, const uint32_t* v_bits,
+                                const uint16_t* v_scale, int64_t n_rows, int head_dim, void* k_out, void* v_out,
+                                tq_stream_t stream);
+
+/* Stored K + V bytes of a cache of n_tokens tokens in n_layers layers of n_kv_heads heads under each
+ * codec. These are the codes and their parameters only, with no ring and no alignment padding. The
+ * rows of the overview's table in §性能表现与实测数据 are:
+ *   - FP16: 2 bytes per element.
+ *   - KIVI 2-bit: 2 bits plus fp16 scale and zero per 16 elements.
+ *   - Bonsai 1-bit: 1 bit plus an fp16 scale per 128 elements.
+ * This library's own records are:
+ *   - key: d/4 + d/8 + 4 bytes;
+ *   - value: d/4 (2-bit) or d/2 (4-bit), plus d/16 bytes.
+ * Returns 0 for an unknown codec, bad sizes, or a head_dim that the codec does not accept. */
+typedef enum tq_codec {
+  TQ_CODEC_FP16 = 0,
+  TQ_CODEC_KIVI2 = 1,
+  TQ_CODEC_BONSAI1 = 2,
+  TQ_CODEC_TQ_K3V2 = 3,
+  TQ_CODEC_TQ_K3V4 = 4
+} tq_codec;
+size_t tq_codec_kv_bytes(int codec, int n_layers, int n_kv_heads, int head_dim, int64_t n_tokens);
+
 /* ---- Host-only inspection helpers (tests and tools; no device work) ---- */
 
 /* Byte offset, inside the cache buffer, of one packed page of (layer, slot, kv_head, page); (size_t)-1

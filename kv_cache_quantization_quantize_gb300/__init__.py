@@ -10,8 +10,9 @@ import torch
 
 from . import _abi
 from ._abi import TQConfig, TQError, check, load, TQ_BF16, TQ_F32
+from . import codecs
 
-__all__ = ["TQConfig", "TQError", "TurboQuantCache", "HostTables", "load", "config"]
+__all__ = ["TQConfig", "TQError", "TurboQuantCache", "HostTables", "load", "config", "codecs"]
 
 
 def config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0,

@@ -9,6 +9,7 @@ HEADER = os.path.join(os.path.dirname(_PKG), "include", "tq.h")
 
 TQ_OK, TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED, TQ_ERR_CAPACITY, TQ_ERR_CUDA, TQ_ERR_DEVICE = range(6)
 TQ_BF16, TQ_F32 = 0, 1
+TQ_CODEC_FP16, TQ_CODEC_KIVI2, TQ_CODEC_BONSAI1, TQ_CODEC_TQ_K3V2, TQ_CODEC_TQ_K3V4 = range(5)
 TQ_DEV_ERR_CAPACITY, TQ_DEV_ERR_SEQ_ID, TQ_DEV_ERR_SPLITS, TQ_DEV_ERR_TIMEOUT, TQ_DEV_ERR_BLOCK = 0x1, 0x2, 0x4, 0x8, 0x10
 
 c_int, c_size_t, c_void_p, c_float = ctypes.c_int, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_float
@@ -55,6 +56,11 @@ _SIGS = {
     "tq_page_to_records": (c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p]),
     "tq_records_to_page": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_void_p]),
     "tq_get_tables": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "tq_kivi2_quantize": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int] + [c_void_p] * 7),
+    "tq_kivi2_dequantize": (c_int, [c_void_p] * 6 + [c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]),
+    "tq_bonsai1_quantize": (c_int, [c_void_p, c_void_p, ctypes.c_int64, c_int] + [c_void_p] * 5),
+    "tq_bonsai1_dequantize": (c_int, [c_void_p] * 4 + [ctypes.c_int64, c_int, c_void_p, c_void_p, c_void_p]),
+    "tq_codec_kv_bytes": (c_size_t, [c_int, c_int, c_int, c_int, ctypes.c_int64]),
 }
 
 _lib = None

@@ -217,3 +217,46 @@ def test_decoder_operand_extraction_matches_records(d, vb):
                             t = 32 * blk + 16 * kap + 8 * hiT + 2 * c + e
                             j = 16 * mt + 8 * rowhi + g
                             assert val == codes[t, j] * 2.0 ** (pos - 24)
+
+
+def test_codec_kv_bytes_reproduce_the_overview_table():
+    """tq_codec_kv_bytes against the KV sizes the overview prints for Llama-3.1-8B at 32K tokens."""
+    from kv_cache_quantization_quantize_gb300 import codecs
+    g = json.load(open(os.path.join(GOLDEN, "memory_figures.json")))["llama31_8b_32k"]
+    sh = g["shape"]
+    MiB = 1 << 20
+    args = (sh["layers"], sh["kv_heads"], sh["head_dim"], sh["seq_len"])
+    assert codecs.codec_kv_bytes("fp16", *args) == g["fp16_MB"] * MiB
+    assert codecs.codec_kv_bytes("kivi2", *args) == g["kivi_2bit_MB"] * MiB
+    assert codecs.codec_kv_bytes("bonsai1", *args) == g["bonsai_1bit_g128_MB"] * MiB
+    # this library's records: key d/4 + d/8 + 4 bytes, value d/4 (2-bit) or d/2 (4-bit) + d/16 bytes
+    h = tqm.HostTables(tqm.config(head_dim=128, value_bits=2))
+    per = h.key_record_bytes() + h.value_record_bytes()
+    assert codecs.codec_kv_bytes("turboquant_k3v2", *args) == per * 32 * 8 * 32768 == 736 * MiB
+    assert codecs.codec_kv_bytes("turboquant_k3v4", *args) == 992 * MiB
+    lib = _abi.load()
+    assert lib.tq_codec_kv_bytes(_abi.TQ_CODEC_BONSAI1, 1, 1, 64, 16) == 0  # head_dim not a multiple of 128
+    assert lib.tq_codec_kv_bytes(_abi.TQ_CODEC_KIVI2, 1, 1, 24, 16) == 0
+    assert lib.tq_codec_kv_bytes(99, 1, 1, 128, 16) == 0
+    assert lib.tq_codec_kv_bytes(_abi.TQ_CODEC_FP16, 0, 1, 128, 16) == 0
+
+
+def test_codec_entry_points_validate_before_launching():
+    """Bad sizes and misaligned pointers are rejected on the host (no device work is attempted);
+    an empty input returns TQ_OK without a launch."""
+    lib = _abi.load()
+    P = ctypes.c_void_p
+    a16, mis = P(1 << 20), P((1 << 20) + 2)
+    outs = [a16] * 6
+    assert lib.tq_kivi2_quantize(a16, a16, 32, 2, 24, *outs, None) == _abi.TQ_ERR_INVALID_ARG      # d % 16
+    assert lib.tq_kivi2_quantize(a16, None, 40, 2, 64, *outs, None) == _abi.TQ_ERR_INVALID_ARG     # keys: T % 16
+    assert lib.tq_kivi2_quantize(mis, None, 32, 2, 64, *outs, None) == _abi.TQ_ERR_INVALID_ARG     # k alignment
+    assert lib.tq_kivi2_quantize(a16, None, 32, 2, 64, None, a16, a16, None, None, None, None) \
+        == _abi.TQ_ERR_INVALID_ARG                                                                  # NULL output
+    assert lib.tq_kivi2_quantize(a16, a16, 0, 2, 64, *outs, None) == _abi.TQ_OK                    # empty
+    assert lib.tq_kivi2_dequantize(*outs, 32, 2, 64, mis, None, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_bonsai1_quantize(a16, a16, 4, 64, a16, a16, a16, a16, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_bonsai1_quantize(a16, mis, 4, 128, a16, a16, a16, a16, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_bonsai1_quantize(a16, None, -1, 128, a16, a16, None, None, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_bonsai1_quantize(a16, a16, 0, 128, a16, a16, a16, a16, None) == _abi.TQ_OK
+    assert lib.tq_bonsai1_dequantize(a16, a16, a16, a16, 4, 128, mis, None, None) == _abi.TQ_ERR_INVALID_ARG
