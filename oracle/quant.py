@@ -3,7 +3,9 @@
 Steps, following [Guide] §二 (rotate -> Lloyd-Max -> QJL residual sign -> value group quantisation
 -> bit packing). The magnitude/direction split follows [Overview] §核心技术解析 (PolarQuant).
 
-Key k in R^d (3 bits/coordinate = 2-bit Lloyd-Max + 1-bit QJL, [Guide] §二 and §五 key_bits=3):
+Key k in R^d (key_bits per coordinate = (key_bits - 1)-bit Lloyd-Max + 1-bit QJL, [Guide] §二 and §五:
+key_bits=3 is the configuration the guide runs; key_bits=4 is the 4-bit TurboQuant row of [Overview]
+§性能表现与实测数据, read as a 3-bit Lloyd-Max index plus the QJL sign):
   n = ||k||_2;  y = Pi (k / n)  (y = 0 when n = 0);
   idx_j = #{ i : t_i < y_j }  (t = Lloyd-Max boundaries; the comparison is taken in fp32);
   r = y - c[idx];  gamma = ||r||_2;  z = S r;  sign_j = 1 if fp32(z_j) >= 0 else 0;
@@ -21,8 +23,10 @@ Readings (the pages are silent; the plainest reading is used):
 * decisions (code index, sign, floor) are taken in fp32, the kernel's precision.
 
 Canonical record bytes (bit packing, [Guide] §二 step 5: four 2-bit values per byte):
-  element j of a b-bit array sits at bit b*(j mod 8/b) of byte floor(j*b/8) (little-endian in the byte);
-  key record   = idx (2 bits) | sign (1 bit) | n (fp16 LE) | gamma (fp16 LE)  -> d/4 + d/8 + 4 bytes;
+  a b-bit array is a little-endian bit stream: element j holds bits b*j .. b*j + b - 1, bit i of the
+  stream is bit i mod 8 of byte floor(i/8) (for b = 1, 2, 4: bit b*(j mod 8/b) of byte floor(j*b/8));
+  key record   = idx (key_bits-1 bits) | sign (1 bit) | n (fp16 LE) | gamma (fp16 LE)
+                 -> d*(key_bits-1)/8 + d/8 + 4 bytes (52 B at d=128, key_bits 3; 68 B at key_bits 4);
   value record = codes (b bits) | scales (fp16 LE, d/32 of them)            -> d*b/8 + d/16 bytes.
 """
 
@@ -43,6 +47,7 @@ class KeyRecords:
     sign: np.ndarray   # uint8 [T, d], 1 = projection >= 0
     norm: np.ndarray   # float16 [T]
     gamma: np.ndarray  # float16 [T]
+    mse_bits: int = KEY_MSE_BITS  # bits of idx (key_bits - 1)
 
 
 @dataclass
@@ -57,7 +62,8 @@ def _fp16_via_fp32(x):
 
 
 def quantize_keys(k, D, S, centroids, boundaries):
-    """Key records for k [T, d] (fp64 values). S is the QJL matrix [d, d], D the rotation signs."""
+    """Key records for k [T, d] (fp64 values). S is the QJL matrix [d, d], D the rotation signs. The
+    index width follows the codebook: 4 centroids -> 2 bits (key_bits 3), 8 -> 3 bits (key_bits 4)."""
     k = np.atleast_2d(np.asarray(k, dtype=np.float64))
     Pi = rotation_matrix(D)
     n = np.sqrt(np.sum(k * k, axis=1))
@@ -70,7 +76,9 @@ def quantize_keys(k, D, S, centroids, boundaries):
     gamma = np.sqrt(np.sum(r * r, axis=1))
     z = r @ np.asarray(S, dtype=np.float64).T
     sign = (z.astype(np.float32) >= 0).astype(np.uint8)
-    return KeyRecords(idx=idx, sign=sign, norm=_fp16_via_fp32(n), gamma=_fp16_via_fp32(gamma))
+    mse_bits = int(np.log2(len(centroids)))
+    assert 1 << mse_bits == len(centroids)
+    return KeyRecords(idx=idx, sign=sign, norm=_fp16_via_fp32(n), gamma=_fp16_via_fp32(gamma), mse_bits=mse_bits)
 
 
 def quantize_values(v, D, bits, group=VALUE_GROUP):
@@ -151,24 +159,22 @@ def history_split(L, ring=RING):
 
 
 def _pack_bits(a, bits):
+    """[T, d] values of `bits` bits -> [T, d*bits/8] bytes, as a little-endian bit stream."""
     a = np.asarray(a, dtype=np.uint8)
     T, d = a.shape
-    per = 8 // bits
-    a = a.reshape(T, d // per, per).astype(np.uint16)
-    shifts = (np.arange(per) * bits).astype(np.uint16)
-    return np.bitwise_or.reduce(a << shifts, axis=2).astype(np.uint8)
+    assert (d * bits) % 8 == 0
+    stream = (a[:, :, None] >> np.arange(bits, dtype=np.uint8)) & 1  # [T, d, bits]: bit i of element j
+    return np.packbits(stream.reshape(T, d * bits), axis=1, bitorder="little")
 
 
 def _unpack_bits(b, bits, d):
     b = np.asarray(b, dtype=np.uint8)
-    per = 8 // bits
-    shifts = (np.arange(per) * bits).astype(np.uint8)
-    out = (b[:, :, None] >> shifts) & ((1 << bits) - 1)
-    return out.reshape(b.shape[0], d).astype(np.uint8)
+    stream = np.unpackbits(b, axis=1, bitorder="little")[:, :d * bits].reshape(b.shape[0], d, bits)
+    return np.sum(stream.astype(np.uint16) << np.arange(bits, dtype=np.uint16), axis=2).astype(np.uint8)
 
 
-def key_record_bytes(d):
-    return d * KEY_MSE_BITS // 8 + d // 8 + 4
+def key_record_bytes(d, key_bits=KEY_MSE_BITS + 1):
+    return d * (key_bits - 1) // 8 + d // 8 + 4
 
 
 def value_record_bytes(d, bits, group=VALUE_GROUP):
@@ -178,18 +184,20 @@ def value_record_bytes(d, bits, group=VALUE_GROUP):
 def pack_key_records(rec):
     T, d = rec.idx.shape
     return np.concatenate([
-        _pack_bits(rec.idx, KEY_MSE_BITS), _pack_bits(rec.sign, 1),
+        _pack_bits(rec.idx, rec.mse_bits), _pack_bits(rec.sign, 1),
         rec.norm.astype("<f2").view(np.uint8).reshape(T, 2),
         rec.gamma.astype("<f2").view(np.uint8).reshape(T, 2)], axis=1)
 
 
-def unpack_key_records(buf, d):
+def unpack_key_records(buf, d, key_bits=KEY_MSE_BITS + 1):
     buf = np.asarray(buf, dtype=np.uint8)
     T = buf.shape[0]
-    o1 = d * KEY_MSE_BITS // 8
+    mb = key_bits - 1
+    o1 = d * mb // 8
     o2 = o1 + d // 8
     return KeyRecords(
-        idx=_unpack_bits(buf[:, :o1], KEY_MSE_BITS, d),
+        mse_bits=mb,
+        idx=_unpack_bits(buf[:, :o1], mb, d),
         sign=_unpack_bits(buf[:, o1:o2], 1, d),
         norm=np.ascontiguousarray(buf[:, o2:o2 + 2]).view("<f2").reshape(T).astype(np.float16),
         gamma=np.ascontiguousarray(buf[:, o2 + 2:o2 + 4]).view("<f2").reshape(T).astype(np.float16))

@@ -13,15 +13,16 @@ from oracle import (decode_attention, dequantize_keys, dequantize_values, gaussi
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
-@pytest.mark.parametrize("d", [64, 128, 256])
-def test_qjl_estimator_unbiased_over_seeds(d):
-    """Mean estimator error over 10^4 independent Gaussian S is 0 within 3 sigma (fixed q, k)."""
+@pytest.mark.parametrize("d,mse_bits", [(64, 2), (128, 2), (256, 2), (128, 3)])
+def test_qjl_estimator_unbiased_over_seeds(d, mse_bits):
+    """Mean estimator error over 10^4 independent Gaussian S is 0 within 3 sigma (fixed q, k); also for the
+    3-bit index of key_bits 4."""
     rng = np.random.default_rng(100 + d)
     q = rng.standard_normal(d)
     k = rng.standard_normal(d)
     k[1] *= 6.0
     D = rademacher_signs(4, d)
-    c, t = lloyd_max_codebook(d, 2)
+    c, t = lloyd_max_codebook(d, mse_bits)
     truth = float(q @ k)
     n_trials = 10000
     err = np.empty(n_trials)
@@ -72,12 +73,12 @@ def test_all_ring_context_is_exact_attention(d):
     assert np.allclose(out, _sdpa(q, rk, rv, 1 / np.sqrt(d)), atol=1e-13)
 
 
-@pytest.mark.parametrize("vbits", [2, 4])
-def test_hybrid_attention_equals_attention_on_dequantised_cache(vbits):
+@pytest.mark.parametrize("vbits,mse_bits", [(2, 2), (4, 2), (4, 3)])
+def test_hybrid_attention_equals_attention_on_dequantised_cache(vbits, mse_bits):
     d = 128
     rng = np.random.default_rng(vbits)
     D, S = rademacher_signs(5, d), gaussian_matrix_bf16(5, d)
-    c, t = lloyd_max_codebook(d, 2)
+    c, t = lloyd_max_codebook(d, mse_bits)
     kp, vp = rng.standard_normal((200, d)), rng.standard_normal((200, d))
     rk, rv = rng.standard_normal((17, d)), rng.standard_normal((17, d))
     q = rng.standard_normal((4, d)) * 2.0

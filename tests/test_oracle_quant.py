@@ -31,6 +31,11 @@ def test_pack_unpack_exhaustive(bits):
 
 
 def test_pack_bit_order_little_endian():
+    # 3-bit stream, worked by hand: element j at bits 3j..3j+2, bit i of the stream = bit i % 8 of byte i // 8
+    # [1, 2, 7, 0, 5, 3, 6, 4] sets stream bits 0 | 4 | 6 7 8 | - | 12 14 | 15 16 | 19 20 | 23
+    assert list(_pack_bits(np.array([[1, 2, 7, 0, 5, 3, 6, 4]], np.uint8), 3)[0]) == [0xD1, 0xD1, 0x99]
+    rnd = np.random.default_rng(3).integers(0, 8, size=(5, 64), dtype=np.uint8)
+    assert np.array_equal(_unpack_bits(_pack_bits(rnd, 3), 3, 64), rnd)
     assert _pack_bits(np.array([[0, 1, 2, 3]], np.uint8), 2)[0, 0] == 0b11100100
     assert _pack_bits(np.array([[1, 0, 0, 0, 0, 0, 0, 1]], np.uint8), 1)[0, 0] == 0b10000001
     assert _pack_bits(np.array([[0x3, 0xA]], np.uint8), 4)[0, 0] == 0xA3
@@ -41,19 +46,22 @@ def test_record_sizes_and_golden_constants():
     assert g["key_bits"] == 2 + g["qjl_bits_per_dim"]
     assert g["values_per_byte_at_2bit"] == 8 // 2
     assert key_record_bytes(128) == 52 and key_record_bytes(256) == 100
+    assert key_record_bytes(128, 4) == 68 and key_record_bytes(64, 4) == 36 and key_record_bytes(256, 4) == 132
     assert value_record_bytes(128, 2) == 40 and value_record_bytes(128, 4) == 72
     assert value_record_bytes(256, 2) == 80 and value_record_bytes(256, 4) == 144
 
 
+@pytest.mark.parametrize("key_bits", [3, 4])
 @pytest.mark.parametrize("d", [64, 128, 256])
-def test_key_records(d):
+def test_key_records(d, key_bits):
     rng = np.random.default_rng(d)
     k = rng.standard_normal((64, d))
     k[:, 3] *= 8.0
     k[5] = 0.0
     D, S = rademacher_signs(1, d), gaussian_matrix_bf16(1, d)
-    c, t = lloyd_max_codebook(d, 2)
+    c, t = lloyd_max_codebook(d, key_bits - 1)
     rec = quantize_keys(k, D, S, c, t)
+    assert rec.mse_bits == key_bits - 1 and rec.idx.max() == 2 ** (key_bits - 1) - 1
     n = np.linalg.norm(k, axis=1)
     assert np.array_equal(rec.norm, n.astype(np.float32).astype(np.float16))
     y = _rotate(k, D) / np.where(n > 0, n, 1)[:, None]
@@ -68,8 +76,8 @@ def test_key_records(d):
     assert np.allclose(np.sum(pm * z, axis=1), np.sum(np.abs(z), axis=1), rtol=1e-12)
     # round trip through the canonical bytes
     buf = pack_key_records(rec)
-    assert buf.shape == (64, key_record_bytes(d))
-    back = unpack_key_records(buf, d)
+    assert buf.shape == (64, key_record_bytes(d, key_bits))
+    back = unpack_key_records(buf, d, key_bits)
     for f in ("idx", "sign", "norm", "gamma"):
         assert np.array_equal(getattr(back, f), getattr(rec, f))
 
