@@ -39,8 +39,8 @@ if ROOT not in sys.path:
 METRIC = "decode attn context-tok/s & packed-KV HBM GB/s (% of 8 TB/s); quantize tok/s"
 UNIT = "context-tok/s"
 WL = dict(name="llama3.1-8b-shaped decode, batch 1, context 32768, K3/V2",
-          layers=32, hq=32, hkv=8, d=128, batch=1, ctx=32768, vb=2, outliers=("random", 4, 10.0))
-PREFILL = dict(tokens=65536, hkv=8, layers=32, d=128, vb=2, seed=4)
+          layers=32, hq=32, hkv=8, d=128, batch=1, ctx=32768, vb=2, kb=3, outliers=("random", 4, 10.0))
+PREFILL = dict(tokens=65536, hkv=8, layers=32, d=128, vb=2, kb=3, seed=4)
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -132,7 +132,7 @@ def aggregate_over_ranks(ms, units, world, device):
 
 def bench_config(world, mode="hybrid"):
     cfg = {"workload": WL["name"], "layers": WL["layers"], "q_heads": WL["hq"], "kv_heads": WL["hkv"],
-           "head_dim": WL["d"], "batch_per_gpu": WL["batch"], "context": WL["ctx"], "value_bits": WL["vb"],
+           "head_dim": WL["d"], "batch_per_gpu": WL["batch"], "context": WL["ctx"], "key_bits": WL["kb"], "value_bits": WL["vb"],
            "ring": 128, "l2": "inputs larger than L2 (~785 MB of packed records per step vs 129 MB L2)",
            "parallelism": "replicas" if world > 1 else "single GPU",
            "step": "append 1 token + hybrid decode attention, all 32 layers, one CUDA graph replay"}
@@ -203,7 +203,8 @@ def run_ours(args):
     full = args.mode == "full_tq"
     paged = args.layout == "paged"
     max_pages = (max_ctx + 127) // 128
-    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=B,
+    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
+                     max_seqs=B,
                      max_ctx=max_ctx, seed=1, mode=args.mode, n_blocks=B * max_pages if paged else 0)
     cache = tqm.TurboQuantCache(cfg, device=dev)
     ids = torch.arange(B, dtype=torch.int32, device=dev)
@@ -281,7 +282,7 @@ def run_ours(args):
     ms_per_step = t_max / K
 
     # algorithmic bytes per step: packed K3/V2 records + ring (K,V bf16) + q + out, all layers
-    rec = (d // 4 + d // 8 + 4) + (d * vb // 8 + d // 16)
+    rec = (d * (WL["kb"] - 1) // 8 + d // 8 + 4) + (d * vb // 8 + d // 16)
     Lmid = L_first + (K - 1) / 2.0
     packed = Lmid if full else 128 * ((Lmid - 1) // 128)
     ring = Lmid - packed
@@ -314,7 +315,7 @@ def run_ours(args):
     kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
     # the committed ncu summary is of the default (hybrid, contiguous, head_dim 128) step
-    traffic = None if full or paged or d != 128 else profiled_traffic()
+    traffic = None if full or paged or d != 128 or WL["kb"] != 3 else profiled_traffic()
 
     # ---- end to end through the public API with pinned host buffers ----
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
@@ -376,7 +377,8 @@ def run_ours(args):
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged and d == 128:  # oracle sample
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged and d == 128
+            and WL["kb"] == 3):  # oracle sample
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -390,7 +392,8 @@ def bench_quantize(tqm, synth, dev, args, peak):
     T, Hkv, L_layers, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["layers"], PREFILL["d"], PREFILL["vb"]
     paged = getattr(args, "layout", "contiguous") == "paged"
     max_pages = (T + 127) // 128
-    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=4 * Hkv, max_seqs=1,
+    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=PREFILL["kb"], n_layers=L_layers, n_kv_heads=Hkv,
+                     n_q_heads=4 * Hkv, max_seqs=1,
                      max_ctx=T, seed=PREFILL["seed"], n_blocks=max_pages if paged else 0)
     qc = tqm.TurboQuantCache(cfg, device=dev)
     if paged:
@@ -419,7 +422,7 @@ def bench_quantize(tqm, synth, dev, args, peak):
     ms = e0.elapsed_time(e1) / reps
     if qc.check_status():
         raise RuntimeError("device status after quantise")
-    rec = (d // 4 + d // 8 + 4) + (d * vb // 8 + d // 16)
+    rec = (d * (WL["kb"] - 1) // 8 + d // 8 + 4) + (d * vb // 8 + d // 16)
     packed = 128 * ((T - 1) // 128)
     ring = T - packed
     bytes_pass = L_layers * Hkv * (T * d * 2 * 2 + packed * rec + ring * d * 2 * 2)
@@ -441,7 +444,8 @@ def bench_prefill(args):
     dev = torch.device("cuda", 0)
     L_layers, Hq, Hkv, d, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["ctx"], WL["vb"]
     Tq = args.prefill_chunk
-    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq, max_seqs=1,
+    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
+                     max_seqs=1,
                      max_ctx=ctx, seed=1)
     cache = tqm.TurboQuantCache(cfg, device=dev)
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -664,6 +668,8 @@ def main():
                    help="time prefill attention of a TQ-token chunk instead (one JSON line of its own)")
     p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
                    help="the same decode and prefill shapes with another head_dim (synthetic variants)")
+    p.add_argument("--key-bits", type=int, default=3, choices=[3, 4],
+                   help="4: 3-bit Lloyd-Max index + QJL sign with 4-bit values (the 4-bit configuration)")
     p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
                    help="paged: the packed pages live in a block pool addressed through a scrambled block table")
     p.add_argument("--codec", default="", choices=["", "kivi2", "bonsai1"],
@@ -678,6 +684,9 @@ def main():
         WL.update(d=args.head_dim, name=f"llama3.1-8b-shaped decode with head_dim {args.head_dim}, batch 1, "
                                         f"context 32768, K3/V2")
         PREFILL.update(d=args.head_dim)
+    if args.key_bits == 4:
+        WL.update(kb=4, vb=4, name=WL["name"].replace("K3/V2", "K4/V4"))
+        PREFILL.update(kb=4, vb=4)
     if args.warmup < 3:
         args.warmup = 3
     if args.profile_quantize:

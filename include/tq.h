@@ -59,11 +59,13 @@ typedef enum tq_dtype { TQ_BF16 = 0, TQ_F32 = 1 } tq_dtype;
 #define TQ_DEV_ERR_BLOCK 0x10u   /* paged cache: a page that an append or decode touched has no valid block in
                                   * the block table; the append skipped it, the decode result is undefined */
 
-/* Configuration. The key is 3 bits per coordinate: a 2-bit Lloyd-Max code plus 1 QJL sign bit
- * ([Guide] §二 steps 2-3; §五.1 key_bits=3). */
+/* Configuration. The key has key_bits bits per coordinate: a (key_bits - 1)-bit Lloyd-Max code plus 1 QJL
+ * sign bit ([Guide] §二 steps 2-3; §五.1 key_bits=3). key_bits 4 is the 4-bit TurboQuant row of the
+ * overview's table (§性能表现与实测数据), read as a 3-bit code plus the sign; it is served with
+ * value_bits 4. */
 typedef struct tq_config {
   int32_t head_dim;    /* d: 64, 128 or 256 */
-  int32_t key_bits;    /* 3 */
+  int32_t key_bits;    /* 3, or 4 with value_bits 4 (TQ_ERR_UNSUPPORTED otherwise) */
   int32_t value_bits;  /* 2 or 4 ([Guide] §二 step 4) */
   int32_t value_group; /* 32 ([Guide] §二 step 4) */
   int32_t ring_size;   /* 128: hybrid mode, exact recent buffer ([Guide] §五.1 buffer_size=128);
@@ -334,9 +336,10 @@ size_t tq_status_offset(const tq_ctx* ctx);
 
 /* Converts the first n_tokens of one packed page (a host copy of tq_page_bytes bytes) into canonical
  * records ([Guide] §二 step 5 bit packing, little-endian within bytes):
- *   - key record = idx (2 bits/coord) | QJL sign (1 bit/coord, 1 = projection >= 0) | fp16 n | fp16 gamma;
+ *   - key record = idx (key_bits - 1 bits/coord, a little-endian bit stream: bit i of coordinate j is bit
+ *     (key_bits - 1) j + i of the stream) | QJL sign (1 bit/coord, 1 = projection >= 0) | fp16 n | fp16 gamma;
  *   - value record = codes (value_bits/coord) | fp16 scale per 32 coords.
- * out_keys holds n_tokens * (d/4 + d/8 + 4) bytes; out_values holds n_tokens * (d*vb/8 + d/16). */
+ * out_keys holds n_tokens * (d*(key_bits-1)/8 + d/8 + 4) bytes; out_values holds n_tokens * (d*vb/8 + d/16). */
 tq_status tq_page_to_records(const tq_ctx* ctx, const void* h_page, int n_tokens, uint8_t* out_keys,
                              uint8_t* out_values);
 /* Inverse of tq_page_to_records (host): builds a page from canonical records (unused tokens zero). */
@@ -346,8 +349,8 @@ tq_status tq_records_to_page(const tq_ctx* ctx, const uint8_t* keys, const uint8
 /* Host copies of the tables this context uploaded:
  *   - D: float[d] (+-1);
  *   - S_bf16: uint16[d*d], row-major bf16 bits;
- *   - centroids: double[4];
- *   - boundaries: double[3].
+ *   - centroids: double[2^(key_bits-1)] (4 or 8);
+ *   - boundaries: double[2^(key_bits-1) - 1] (3 or 7).
  * Any pointer may be NULL. */
 tq_status tq_get_tables(const tq_ctx* ctx, float* D, uint16_t* S_bf16, double* centroids, double* boundaries);
 

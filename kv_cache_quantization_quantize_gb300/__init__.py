@@ -16,12 +16,13 @@ __all__ = ["TQConfig", "TQError", "TurboQuantCache", "HostTables", "load", "conf
 
 
 def config(head_dim=128, value_bits=2, n_layers=1, n_kv_heads=1, n_q_heads=1, max_seqs=1, max_ctx=1152, seed=0,
-           mode="hybrid", n_blocks=0):
+           mode="hybrid", n_blocks=0, key_bits=3):
     """mode "hybrid": 128-token exact recent buffer; "full_tq": every token quantised (ring_size 0).
-    n_blocks > 0: paged cache with a pool of n_blocks 128-token blocks per layer (see block_table)."""
+    n_blocks > 0: paged cache with a pool of n_blocks 128-token blocks per layer (see block_table).
+    key_bits 3: 2-bit Lloyd-Max index + QJL sign; key_bits 4 (with value_bits 4): 3-bit index + sign."""
     if mode not in ("hybrid", "full_tq"):
         raise ValueError(f"mode {mode!r}: expected 'hybrid' or 'full_tq'")
-    return TQConfig(head_dim=head_dim, key_bits=3, value_bits=value_bits, value_group=32,
+    return TQConfig(head_dim=head_dim, key_bits=key_bits, value_bits=value_bits, value_group=32,
                     ring_size=128 if mode == "hybrid" else 0, n_layers=n_layers, n_kv_heads=n_kv_heads,
                     n_q_heads=n_q_heads, max_seqs=max_seqs, max_ctx=max_ctx, seed=seed, n_blocks=n_blocks)
 
@@ -53,8 +54,9 @@ class HostTables:
         d = self.cfg.head_dim
         D = np.zeros(d, np.float32)
         S = np.zeros(d * d, np.uint16)
-        c = np.zeros(4, np.float64)
-        t = np.zeros(3, np.float64)
+        nlev = 1 << (self.cfg.key_bits - 1)
+        c = np.zeros(nlev, np.float64)
+        t = np.zeros(nlev - 1, np.float64)
         check(self.lib.tq_get_tables(self.ctx, D.ctypes.data, S.ctypes.data, c.ctypes.data, t.ctypes.data))
         return D, S.reshape(d, d), c, t
 
@@ -63,7 +65,7 @@ class HostTables:
 
     def key_record_bytes(self):
         d = self.cfg.head_dim
-        return d // 4 + d // 8 + 4
+        return d * (self.cfg.key_bits - 1) // 8 + d // 8 + 4
 
     def value_record_bytes(self):
         d = self.cfg.head_dim

@@ -3,9 +3,11 @@
 //
 // Scores. For a packed token (n, idx, gamma, sign) and query head q:
 //   s = scale * n * ( <Pi q, c[idx]> + sqrt(pi/2)/d * gamma * <S Pi q, 2 sign - 1> )  ([Guide] §二, TurboQuantProd).
-// The 2-bit codebook is odd-symmetric, so c[idx] = alpha*(2 b_hi - 1) + beta*(2 b_lo - 1), with
-// alpha = (c2+c3)/2 and beta = (c3-c2)/2. Each score is therefore a sum of three bit-plane dot
-// products on f16 tensor cores (mma.sync m16n8k16):
+// The codebook is odd-symmetric, so c[idx] is a weighted sum of +-1 bit planes:
+//   - 2-bit index (key_bits 3): c = alpha (2 b1 - 1) + beta (2 b0 - 1), alpha = (c2+c3)/2, beta = (c3-c2)/2;
+//   - 3-bit index (key_bits 4): c = A s2 + B t1 + C t0 + E s2 t1 t0 (s, t = 2 bit - 1), the last plane
+//     being b2 ^ b1 ^ b0, with A, B, C, E fitted exactly to c4..c7.
+// Each score is therefore a sum of bit-plane dot products (3 or 5) on f16 tensor cores (mma.sync m16n8k16):
 //   - A = key bits masked straight out of the packed words. Bits 0..11 of an f16 half are exactly
 //     2^(q-24) when set, and 0 otherwise.
 //   - B = the query, prescaled by 2^(24-q), for up to 4 heads.
@@ -169,12 +171,23 @@ __host__ __device__ constexpr int decode_threads() {
 // Query prep: q_rot = Pi q, q_proj = S q_rot; f16 operands of the three key bit-plane MMAs
 // =============================================================================================
 
+// B-operand planes of the key MMAs:
+//   key_bits 3: index planes 0, 1 and the QJL sign plane 2.
+//   key_bits 4: index planes 0-3 (3 = parity plane), the QJL sign plane 4, and plane 5, the f16
+//     rounding remainder of plane 0's operand (the largest weight), multiplied against plane 0's bits.
+//     Without plane 5 the f16 rounding of four index operands adds about 1.2x the score error of the
+//     2-bit index.
+__host__ __device__ constexpr int key_bplanes(int kb) { return kb == 3 ? 3 : 6; }
+// B plane that carries the QJL operand.
+__host__ __device__ constexpr int key_qjl_plane(int kb) { return kb == 3 ? 2 : 4; }
+
 // Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
-template <int D>
+template <int D, int KB>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
-  // q_rot, q_proj [4][D] fp32; 32 floats of scales; B fragments [3 D/16 items][32 lanes] uint2;
+  // q_rot, q_proj [4][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes] uint2;
   // per-warp offset sums [warps][8]
-  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (3 * D / 16) + sizeof(float) * 8 * (decode_threads<D>() / 32);
+  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (key_bplanes(KB) * D / 16) +
+         sizeof(float) * 8 * (decode_threads<D>() / 32);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
@@ -216,9 +229,10 @@ __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f)
 // (f16 max 65504), from bounds: max|w x_j| 2^24 with max|q_proj| <= max_i sum_j |S_ij| * max|q_rot|.
 // um / uq undo lambda (and apply the softmax scale in log2 units); cm / cq are half the sums of the
 // represented (rounded) operands, i.e. the +-1 offsets of the bit planes.
-template <int D, int NT>
+template <int D, int NT, int KB>
 __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
                                            float (&um)[2], float (&cm)[2], float (&uq)[2], float (&cq)[2]) {
+  constexpr int NBP = key_bplanes(KB), QP = key_qjl_plane(KB), NMW = KB == 3 ? 2 : 4;  // B planes; QJL plane; weights
   constexpr int NE = D / 32;
   constexpr int HALVES = D / warp_coords<D>();
   constexpr int MT = D / 16;
@@ -226,7 +240,9 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
   const int G = lv.G;
-  const float alpha2 = 2.f * lv.cb[8], beta2 = 2.f * lv.cb[9];
+  float wmax = 0.f;  // largest |2 w| of the index planes
+#pragma unroll
+  for (int p = 0; p < NMW; ++p) wmax = fmaxf(wmax, fabsf(2.f * lv.cb[kCbW + p]));
   float* qr = ps;               // [4][D]
   float* qp = qr + kMaxG * D;   // [4][D]
   float* red = qp + kMaxG * D;  // [hd]: projection lambda; [4 + 2 hd + {0, 1}]: operand lambdas
@@ -251,7 +267,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     if (lane == 0) {
       const float big = 16777216.f;  // 2^24, the largest bit-plane prescale
       red[warp] = mx > 0.f ? exp2f(floorf(log2f(16384.f / mx))) : 1.f;
-      const float bm = fmaxf(alpha2, beta2) * mx * big, bp = 2.f * lv.cb[10] * mx * big;
+      const float bm = wmax * mx * big, bp = 2.f * lv.cb[kCbSmax] * mx * big;
       red[4 + 2 * warp + 0] = bm > 0.f ? exp2f(floorf(log2f(32768.f / bm))) : 1.f;
       red[4 + 2 * warp + 1] = bp > 0.f ? exp2f(floorf(log2f(32768.f / bp))) : 1.f;
     }
@@ -294,7 +310,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   // wsum[w][hd] / wsum[w][4 + hd] hold warp w's offset sums of head hd, added in a fixed order below
   // (the same constants in every split CTA and every call)
   constexpr int KS = warp_coords<D>() / 16;  // key-MMA k-steps per warp
-  constexpr int NW = NT / 32, NITEMS = HALVES * 3 * KS;
+  constexpr int NW = NT / 32, NITEMS = HALVES * NBP * KS;
   uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
   float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][8]
   const bool live = g < G;
@@ -304,20 +320,29 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   __syncthreads();
   float sum_m = 0.f, sum_q = 0.f;
   for (int item = warp; item < NITEMS; item += NW) {
-    const int s = item % KS, pi = (item / KS) % 3, hv = item / (3 * KS);
-    const float w = (pi == 0 ? alpha2 : pi == 1 ? beta2 : 2.f) * (pi < 2 ? lam_m : lam_q);
-    const float* base = pi < 2 ? bm : bp;
+    const int s = item % KS, pi = (item / KS) % NBP, hv = item / (NBP * KS);
+    const bool qjl = pi == QP, rem = pi == 5;  // rem: remainder plane of plane 0 (key_bits 4)
+    const float w = qjl ? 2.f * lam_q : 2.f * lv.cb[kCbW + (rem ? 0 : pi)] * lam_m;
+    const float* base = qjl ? bp : bm;
     const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
     const float pre0 = key_prescale(2 * s), pre1 = key_prescale(2 * s + 1);
     const float2 x0 = *reinterpret_cast<const float2*>(base + j0);
     const float2 x1 = *reinterpret_cast<const float2*>(base + j1);
-    const uint32_t b0 = pack_half2(w * x0.x * pre0, w * x0.y * pre0);
-    const uint32_t b1 = pack_half2(w * x1.x * pre1, w * x1.y * pre1);
+    float v4[4] = {w * x0.x * pre0, w * x0.y * pre0, w * x1.x * pre1, w * x1.y * pre1};
+    if (rem) {  // what the f16 operand of plane 0 left out
+      const float2 h0 = half2_to_float2(pack_half2(v4[0], v4[1])), h1 = half2_to_float2(pack_half2(v4[2], v4[3]));
+      v4[0] -= h0.x;
+      v4[1] -= h0.y;
+      v4[2] -= h1.x;
+      v4[3] -= h1.y;
+    }
+    const uint32_t b0 = pack_half2(v4[0], v4[1]);
+    const uint32_t b1 = pack_half2(v4[2], v4[3]);
     frag[item * 32 + lane] = make_uint2(b0, b1);
     const float2 r0 = half2_to_float2(b0), r1 = half2_to_float2(b1);
     const float v = (r0.x + r0.y) * (1.f / pre0) + (r1.x + r1.y) * (1.f / pre1);
-    if (pi < 2) sum_m += v;
-    else sum_q += v;
+    if (qjl) sum_q += v;
+    else sum_m += v;
   }
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 1);
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
@@ -624,8 +649,9 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // exchange partial sums through shared memory.
 // Values: P is moved from C to B fragment layout with movmatrix and scaled per value group. Then
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
-template <int D, int VB, int STAGES, bool PAGED>
+template <int D, int VB, int STAGES, bool PAGED, int KB>
 __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
+  constexpr int NBP = key_bplanes(KB);  // B planes of the key MMAs (stored planes: KB)
   constexpr int CW = warp_coords<D>();  // coordinates per warp
   constexpr int HALVES = D / CW;
   constexpr int KS = CW / 16;           // key-MMA k-steps per warp
@@ -669,7 +695,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     finish_unit<D, NT>(a, b, h, smem);
     return;
   }
-  const PageLayout pl = page_layout(D, VB);
+  const PageLayout pl = page_layout(D, VB, KB);
   const uint32_t PB = pl.bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);  // [stream][stage]
   uint8_t* stage0 = smem + 128;                         // [stream][stage] pages
@@ -703,10 +729,10 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   pdl_wait();  // earlier work on the stream (q, and the partials of any decode that shares ws) is done
   float um[2], cm[2], uq[2], cq[2];
   float* ps = xbuf + decode_xbuf_floats<D>();
-  query_prep<D, NT>(a, b, h, ps, sfrag, um, cm, uq, cq);
+  query_prep<D, NT, KB>(a, b, h, ps, sfrag, um, cm, uq, cq);
   // f16 B fragments of the key MMAs for this warp's coordinate half, [plane][k-step][lane] in shared
   // memory (written by query_prep; read once per page and k-step, shared by both tiles)
-  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * 3 * KS * 32 + lane;
+  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * NBP * KS * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
   // score = n (um (am - cm) + uq gamma (aq - cq)) as n fma(gamma, fma(uq, aq, -uq cq), fma(um, am, -um cm)).
   // Columns of heads >= G (and 4..7) carry zero query operands: their scores are finite and their
@@ -739,33 +765,45 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(pg + pl.norms_off);
     const uint32_t* vsc = reinterpret_cast<const uint32_t*>(pg + pl.vscale_off);  // [token pair][group] f16x2
     float sc[2][4];
-    // six independent MMA chains: (tile, plane); both tiles' words are loaded up front
+    // six independent MMA chains: (tile, chain); both tiles' words are loaded up front. With a 3-bit
+    // index the four index planes share two chains (planes 0-1 and 2-3) and the parity plane's
+    // words are formed once per page.
+    constexpr int NKW = KB == 3 ? 3 : 5;  // key words per tile: the stored planes (+ the parity plane)
     float acc[2][3][4];
-    uint2 kwv[2][3];
+    uint2 kwv[2][NKW];
 #pragma unroll
-    for (int kap = 0; kap < 2; ++kap)
+    for (int kap = 0; kap < 2; ++kap) {
 #pragma unroll
-      for (int pi = 0; pi < 3; ++pi) {
-        acc[kap][pi][0] = acc[kap][pi][1] = acc[kap][pi][2] = acc[kap][pi][3] = 0.f;
+      for (int ch = 0; ch < 3; ++ch) acc[kap][ch][0] = acc[kap][ch][1] = acc[kap][ch][2] = acc[kap][ch][3] = 0.f;
+#pragma unroll
+      for (int pi = 0; pi < KB; ++pi) {
+        uint2 wv;
         if (D == 64) {  // both tiles in one word; the odd tile 8 bit positions higher
-          const uint2 wv = kw2[(tg * 3 + pi) * 32 + lane];
-          kwv[kap][pi] = kap ? make_uint2(wv.x >> 8, wv.y >> 8) : wv;
+          wv = kw2[(tg * KB + pi) * 32 + lane];
+          if (kap) wv = make_uint2(wv.x >> 8, wv.y >> 8);
         } else {
-          kwv[kap][pi] = kw2[(((2 * tg + kap) * 3 + pi) * HALVES + hf) * 32 + lane];
+          wv = kw2[(((2 * tg + kap) * KB + pi) * HALVES + hf) * 32 + lane];
         }
+        kwv[kap][pi == KB - 1 ? NKW - 1 : pi] = wv;  // the sign plane is the last word
       }
+      if (KB == 4)
+        kwv[kap][3] = make_uint2(kwv[kap][0].x ^ kwv[kap][1].x ^ kwv[kap][2].x, kwv[kap][0].y ^ kwv[kap][1].y ^ kwv[kap][2].y);
+    }
 #pragma unroll
     for (int s = 0; s < KS; ++s) {
       const int q0 = s < 6 ? 2 * s : 2 * s - 4;
       const uint32_t m0 = 0x00010001u << q0, m1 = 0x00010001u << (q0 + 1);
 #pragma unroll
-      for (int pi = 0; pi < 3; ++pi) {
+      for (int pi = 0; pi < NBP; ++pi) {
         const uint2 bv = bfr[(pi * KS + s) * 32];
+        // chains: key_bits 3 one per plane; key_bits 4 {0, 1, 5}, {2, 3}, {4}
+        const int ch = KB == 3 ? pi : (pi == 4 ? 2 : (pi == 2 || pi == 3) ? 1 : 0);
+        const int wi = pi == 5 ? 0 : pi;  // the remainder plane multiplies plane 0's bits
 #pragma unroll
         for (int kap = 0; kap < 2; ++kap) {
-          const uint32_t x0 = s < 6 ? kwv[kap][pi].x : kwv[kap][pi].x >> 4;
-          const uint32_t x1 = s < 6 ? kwv[kap][pi].y : kwv[kap][pi].y >> 4;
-          mma_f16(acc[kap][pi], x0 & m0, x1 & m0, x0 & m1, x1 & m1, bv.x, bv.y);
+          const uint32_t x0 = s < 6 ? kwv[kap][wi].x : kwv[kap][wi].x >> 4;
+          const uint32_t x1 = s < 6 ? kwv[kap][wi].y : kwv[kap][wi].y >> 4;
+          mma_f16(acc[kap][ch], x0 & m0, x1 & m0, x0 & m1, x1 & m1, bv.x, bv.y);
         }
       }
     }
@@ -987,15 +1025,15 @@ constexpr int decode_stages() {  // pages in flight per stream
   return D <= 128 ? 4 : 3;
 }
 
-template <int D, int VB>
+template <int D, int VB, int KB>
 size_t decode_smem_bytes() {
-  const PageLayout pl = page_layout(D, VB);
+  const PageLayout pl = page_layout(D, VB, KB);
   constexpr int NT = decode_threads<D>();
   constexpr int NGRP = 4 * decode_streams<D>();
   const size_t merge_bytes = sizeof(float) * (12 * NGRP + 4 * NGRP * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
   size_t smem = 128 + (size_t)decode_streams<D>() * decode_stages<D, VB>() * pl.bytes + xbuf_bytes +
-                prep_scratch_bytes<D>();
+                prep_scratch_bytes<D, KB>();
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_smem_bytes<D>());
   smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 8 * 1026));  // combine: split (m, l)
@@ -1003,19 +1041,19 @@ size_t decode_smem_bytes() {
 }
 
 // Sets the kernels' shared-memory attributes once and returns resident split-K CTAs per SM.
-template <int D, int VB>
+template <int D, int VB, int KB>
 int decode_setup() {
   static int resident = 0;  // set once, outside any stream capture that follows
   if (resident == 0) {
     constexpr int STAGES = decode_stages<D, VB>();
-    const size_t smem = decode_smem_bytes<D, VB>();
-    if (cudaFuncSetAttribute(k_decode<D, VB, STAGES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const size_t smem = decode_smem_bytes<D, VB, KB>();
+    if (cudaFuncSetAttribute(k_decode<D, VB, STAGES, false, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
-        cudaFuncSetAttribute(k_decode<D, VB, STAGES, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(k_decode<D, VB, STAGES, true, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess)
       return -1;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES, false>, decode_threads<D>(),
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES, false, KB>, decode_threads<D>(),
                                                       smem) != cudaSuccess ||
         n < 1)
       n = 1;
@@ -1024,19 +1062,20 @@ int decode_setup() {
   return resident;
 }
 
-template <int D, int VB>
+template <int D, int VB, int KB>
 cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s) {
   constexpr int STAGES = decode_stages<D, VB>();
-  if (decode_setup<D, VB>() < 0) return cudaErrorInvalidValue;
-  const size_t smem = decode_smem_bytes<D, VB>();
+  if (decode_setup<D, VB, KB>() < 0) return cudaErrorInvalidValue;
+  const size_t smem = decode_smem_bytes<D, VB, KB>();
   if (phase == 0) {  // zero the arrival counters (every decode call leaves them at zero)
     cudaError_t e = cudaMemsetAsync(a.ws + a.plan.cnt_off, 0, sizeof(int32_t) * (size_t)batch * a.lv.Hkv, s);
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
     const dim3 grid(a.plan.n_splits + 1, a.lv.Hkv, batch);
-    cudaError_t e = a.lv.btab ? launch_pdl(k_decode<D, VB, STAGES, true>, grid, dim3(decode_threads<D>()), smem, s, a)
-                              : launch_pdl(k_decode<D, VB, STAGES, false>, grid, dim3(decode_threads<D>()), smem, s, a);
+    cudaError_t e = a.lv.btab
+                        ? launch_pdl(k_decode<D, VB, STAGES, true, KB>, grid, dim3(decode_threads<D>()), smem, s, a)
+                        : launch_pdl(k_decode<D, VB, STAGES, false, KB>, grid, dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;  // phase 2 (combine) runs inside phase 1's last CTA of every (row, KV head)
@@ -1044,15 +1083,17 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
 
 }  // namespace
 
+// key_bits 4 is served with value_bits 4 (validated on the host).
 int decode_resident_ctas(const tq_ctx* ctx) {
-  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   int n;
-  if (d == 64 && vb == 2) n = decode_setup<64, 2>();
-  else if (d == 64 && vb == 4) n = decode_setup<64, 4>();
-  else if (d == 128 && vb == 2) n = decode_setup<128, 2>();
-  else if (d == 128 && vb == 4) n = decode_setup<128, 4>();
-  else if (d == 256 && vb == 2) n = decode_setup<256, 2>();
-  else n = decode_setup<256, 4>();
+  if (kb == 4) n = d == 64 ? decode_setup<64, 4, 4>() : d == 128 ? decode_setup<128, 4, 4>() : decode_setup<256, 4, 4>();
+  else if (d == 64 && vb == 2) n = decode_setup<64, 2, 3>();
+  else if (d == 64 && vb == 4) n = decode_setup<64, 4, 3>();
+  else if (d == 128 && vb == 2) n = decode_setup<128, 2, 3>();
+  else if (d == 128 && vb == 4) n = decode_setup<128, 4, 3>();
+  else if (d == 256 && vb == 2) n = decode_setup<256, 2, 3>();
+  else n = decode_setup<256, 4, 3>();
   return n > 0 ? n : 1;
 }
 
@@ -1069,13 +1110,18 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.scale = scale;
   a.ws = static_cast<uint8_t*>(ws);
   a.plan = plan;
-  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits;
-  if (d == 64 && vb == 2) return launch_decode_dv<64, 2>(a, batch, phase, s);
-  if (d == 64 && vb == 4) return launch_decode_dv<64, 4>(a, batch, phase, s);
-  if (d == 128 && vb == 2) return launch_decode_dv<128, 2>(a, batch, phase, s);
-  if (d == 128 && vb == 4) return launch_decode_dv<128, 4>(a, batch, phase, s);
-  if (d == 256 && vb == 2) return launch_decode_dv<256, 2>(a, batch, phase, s);
-  return launch_decode_dv<256, 4>(a, batch, phase, s);
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
+  if (kb == 4) {
+    if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s);
+    if (d == 128) return launch_decode_dv<128, 4, 4>(a, batch, phase, s);
+    return launch_decode_dv<256, 4, 4>(a, batch, phase, s);
+  }
+  if (d == 64 && vb == 2) return launch_decode_dv<64, 2, 3>(a, batch, phase, s);
+  if (d == 64 && vb == 4) return launch_decode_dv<64, 4, 3>(a, batch, phase, s);
+  if (d == 128 && vb == 2) return launch_decode_dv<128, 2, 3>(a, batch, phase, s);
+  if (d == 128 && vb == 4) return launch_decode_dv<128, 4, 3>(a, batch, phase, s);
+  if (d == 256 && vb == 2) return launch_decode_dv<256, 2, 3>(a, batch, phase, s);
+  return launch_decode_dv<256, 4, 3>(a, batch, phase, s);
 }
 
 }  // namespace tq

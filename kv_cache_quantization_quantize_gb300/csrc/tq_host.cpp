@@ -68,7 +68,9 @@ tq_status validate(const tq_config* c) {
   if (!c) return fail(TQ_ERR_INVALID_ARG, "cfg is NULL");
   if (c->head_dim != 64 && c->head_dim != 128 && c->head_dim != 256)
     return fail(TQ_ERR_UNSUPPORTED, "head_dim %d: supported 64, 128, 256", c->head_dim);
-  if (c->key_bits != 3) return fail(TQ_ERR_UNSUPPORTED, "key_bits %d: supported 3 (2-bit Lloyd-Max + 1-bit QJL)", c->key_bits);
+  if (c->key_bits != 3 && c->key_bits != 4)
+    return fail(TQ_ERR_UNSUPPORTED, "key_bits %d: supported 3 and 4 ((key_bits-1)-bit Lloyd-Max + 1-bit QJL)",
+                c->key_bits);
   if (c->value_bits != 2 && c->value_bits != 4)
     return fail(TQ_ERR_UNSUPPORTED, "value_bits %d: supported 2, 4", c->value_bits);
   if (c->value_group != 32) return fail(TQ_ERR_UNSUPPORTED, "value_group %d: supported 32", c->value_group);
@@ -82,6 +84,8 @@ tq_status validate(const tq_config* c) {
   if (G != 1 && G != 2 && G != 4) return fail(TQ_ERR_UNSUPPORTED, "GQA group %d: supported 1, 2, 4", G);
   if (c->max_ctx > (1 << 24)) return fail(TQ_ERR_UNSUPPORTED, "max_ctx %d above 2^24", c->max_ctx);
   if (c->n_blocks < 0) return fail(TQ_ERR_INVALID_ARG, "n_blocks %d < 0", c->n_blocks);
+  if (c->key_bits == 4 && c->value_bits != 4)
+    return fail(TQ_ERR_UNSUPPORTED, "key_bits 4 is served with value_bits 4 (the 4-bit configuration)");
   return TQ_OK;
 }
 
@@ -200,7 +204,7 @@ size_t ring_elems(const tq_config& c) { return (size_t)2 * tq::kPage * c.head_di
 
 void compute_offsets(tq_ctx* ctx) {
   const tq_config& c = ctx->cfg;
-  ctx->pl = tq::page_layout(c.head_dim, c.value_bits);
+  ctx->pl = tq::page_layout(c.head_dim, c.value_bits, c.key_bits);
   ctx->to = tq::table_offsets(c.head_dim);
   ctx->max_pages = (c.max_ctx + tq::kPage - 1) / tq::kPage;
   const size_t units = (size_t)c.n_layers * c.max_seqs * c.n_kv_heads;
@@ -237,6 +241,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   LayerView v;
   v.d = c.head_dim;
   v.vb = c.value_bits;
+  v.kb = c.key_bits;
   v.G = c.n_q_heads / c.n_kv_heads;
   v.Hkv = c.n_kv_heads;
   v.Hq = c.n_q_heads;
@@ -323,7 +328,7 @@ size_t tq_tables_bytes(const tq_config* cfg) {
 
 size_t tq_page_bytes(const tq_config* cfg) {
   if (validate(cfg) != TQ_OK) return 0;
-  return tq::page_layout(cfg->head_dim, cfg->value_bits).bytes;
+  return tq::page_layout(cfg->head_dim, cfg->value_bits, cfg->key_bits).bytes;
 }
 
 size_t tq_cache_bytes(const tq_config* cfg) {
@@ -361,7 +366,7 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
     const double g = std::sqrt(-2.0 * std::log(u1)) * std::cos(6.283185307179586476925286766559 * u2);
     ctx->S[k] = bf16_rne_bits(g);
   }
-  lloyd_max(d, 2, ctx->cent, ctx->bnd);
+  lloyd_max(d, cfg->key_bits - 1, ctx->cent, ctx->bnd);
   if (!d_tables) {  // host-only context: inspection helpers only
     ctx->host_only = true;
     *out = ctx;
@@ -382,18 +387,27 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
   for (int i = 0; i < d; ++i)
     for (int j = 0; j < d; ++j) st_h[(size_t)j * d + i] = ctx->S[(size_t)i * d + j];
   float cb[tq::kCbFloats] = {0};
-  for (int i = 0; i < 4; ++i) cb[i] = (float)ctx->cent[i];
-  for (int i = 0; i < 3; ++i) cb[4 + i] = (float)ctx->bnd[i];
-  cb[8] = (float)(0.5 * (ctx->cent[2] + ctx->cent[3]));
-  cb[9] = (float)(0.5 * (ctx->cent[3] - ctx->cent[2]));
-  {  // cb[10]: max_i sum_j |S_ij| (rounded up), a bound on |(S x)_i| / max|x|
+  const int nlev = 1 << (cfg->key_bits - 1);
+  for (int i = 0; i < nlev; ++i) cb[tq::kCbCent + i] = (float)ctx->cent[i];
+  for (int i = 0; i < nlev - 1; ++i) cb[tq::kCbBnd + i] = (float)ctx->bnd[i];
+  const double* c = ctx->cent;
+  if (nlev == 4) {  // c[idx] = w0 (2 b1 - 1) + w1 (2 b0 - 1)
+    cb[tq::kCbW + 0] = (float)(0.5 * (c[2] + c[3]));
+    cb[tq::kCbW + 1] = (float)(0.5 * (c[3] - c[2]));
+  } else {  // c[idx] = A s2 + B t1 + C t0 + E s2 t1 t0 (s, t = 2 bit - 1), fitted to c4..c7 exactly
+    cb[tq::kCbW + 0] = (float)(0.25 * (c[4] + c[5] + c[6] + c[7]));
+    cb[tq::kCbW + 1] = (float)(0.25 * (-c[4] - c[5] + c[6] + c[7]));
+    cb[tq::kCbW + 2] = (float)(0.25 * (-c[4] + c[5] - c[6] + c[7]));
+    cb[tq::kCbW + 3] = (float)(0.25 * (c[4] - c[5] - c[6] + c[7]));
+  }
+  {  // cb[kCbSmax]: max_i sum_j |S_ij| (rounded up), a bound on |(S x)_i| / max|x|
     double m = 0.0;
     for (int i = 0; i < d; ++i) {
       double r = 0.0;
       for (int j = 0; j < d; ++j) r += std::fabs((double)bf16_to_float(ctx->S[(size_t)i * d + j]));
       m = std::max(m, r);
     }
-    cb[10] = (float)(m * (1.0 + 1e-6));
+    cb[tq::kCbSmax] = (float)(m * (1.0 + 1e-6));
   }
   std::memcpy(host.data() + ctx->to.cb, cb, sizeof(cb));
   if (d == 128) {
@@ -637,28 +651,32 @@ tq_status tq_page_to_records(const tq_ctx* ctx, const void* h_page, int n_tokens
   const uint8_t* pg = static_cast<const uint8_t*>(h_page);
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(pg + pl.kbits_off);
   const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + pl.vbits_off);
-  const size_t krec = d / 4 + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
+  const int kb = ctx->cfg.key_bits, mb = kb - 1;  // planes; index bits
+  const size_t kidx = (size_t)d * mb / 8, krec = kidx + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
   for (int t = 0; t < n_tokens; ++t) {
     uint8_t* kr = out_keys + t * krec;
     uint8_t* vr = out_values + t * vrec;
     std::memset(kr, 0, krec);
     std::memset(vr, 0, vrec);
     for (int j = 0; j < d; ++j) {
-      int w, b;
-      tq::kbit_loc(d, t, j, 0, w, b);
-      const int hi = (kw[w] >> b) & 1;
-      tq::kbit_loc(d, t, j, 1, w, b);
-      const int lo = (kw[w] >> b) & 1;
-      tq::kbit_loc(d, t, j, 2, w, b);
+      int w, b, idx = 0;
+      for (int pi = 0; pi < mb; ++pi) {  // index bits, highest first
+        tq::kbit_loc(d, kb, t, j, pi, w, b);
+        idx = 2 * idx + (int)((kw[w] >> b) & 1);
+      }
+      tq::kbit_loc(d, kb, t, j, mb, w, b);
       const int sg = (kw[w] >> b) & 1;
-      kr[j / 4] |= (uint8_t)((2 * hi + lo) << (2 * (j % 4)));
-      kr[d / 4 + j / 8] |= (uint8_t)(sg << (j % 8));
+      for (int i = 0; i < mb; ++i) {  // little-endian bit stream: index bit i of element j at stream bit mb j + i
+        const int sb = mb * j + i;
+        kr[sb / 8] |= (uint8_t)(((idx >> i) & 1) << (sb % 8));
+      }
+      kr[kidx + j / 8] |= (uint8_t)(sg << (j % 8));
       tq::vcode_loc(d, vb, t, j, w, b);
       const int code = (vw[w] >> b) & ((1 << vb) - 1);
       const int per = 8 / vb;
       vr[j / per] |= (uint8_t)(code << (vb * (j % per)));
     }
-    std::memcpy(kr + d / 4 + d / 8, pg + pl.norms_off + 4 * t, 4);
+    std::memcpy(kr + kidx + d / 8, pg + pl.norms_off + 4 * t, 4);
     for (int q = 0; q < d / 32; ++q)
       std::memcpy(vr + (size_t)d * vb / 8 + 2 * q, pg + pl.vscale_off + 2 * (size_t)tq::vscale_idx(d, t, q), 2);
   }
@@ -675,26 +693,31 @@ tq_status tq_records_to_page(const tq_ctx* ctx, const uint8_t* keys, const uint8
   std::memset(pg, 0, pl.bytes);
   uint32_t* kw = reinterpret_cast<uint32_t*>(pg + pl.kbits_off);
   uint32_t* vw = reinterpret_cast<uint32_t*>(pg + pl.vbits_off);
-  const size_t krec = d / 4 + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
+  const int kb = ctx->cfg.key_bits, mb = kb - 1;
+  const size_t kidx = (size_t)d * mb / 8, krec = kidx + d / 8 + 4, vrec = (size_t)d * vb / 8 + d / 16;
   for (int t = 0; t < n_tokens; ++t) {
     const uint8_t* kr = keys + t * krec;
     const uint8_t* vr = values + t * vrec;
     for (int j = 0; j < d; ++j) {
-      const int idx = (kr[j / 4] >> (2 * (j % 4))) & 3;
-      const int sg = (kr[d / 4 + j / 8] >> (j % 8)) & 1;
+      int idx = 0;
+      for (int i = 0; i < mb; ++i) {
+        const int sb = mb * j + i;
+        idx |= ((kr[sb / 8] >> (sb % 8)) & 1) << i;
+      }
+      const int sg = (kr[kidx + j / 8] >> (j % 8)) & 1;
       int w, b;
-      tq::kbit_loc(d, t, j, 0, w, b);
-      kw[w] |= (uint32_t)(idx >> 1) << b;
-      tq::kbit_loc(d, t, j, 1, w, b);
-      kw[w] |= (uint32_t)(idx & 1) << b;
-      tq::kbit_loc(d, t, j, 2, w, b);
+      for (int pi = 0; pi < mb; ++pi) {
+        tq::kbit_loc(d, kb, t, j, pi, w, b);
+        kw[w] |= (uint32_t)((idx >> (mb - 1 - pi)) & 1) << b;
+      }
+      tq::kbit_loc(d, kb, t, j, mb, w, b);
       kw[w] |= (uint32_t)sg << b;
       const int per = 8 / vb;
       const int code = (vr[j / per] >> (vb * (j % per))) & ((1 << vb) - 1);
       tq::vcode_loc(d, vb, t, j, w, b);
       vw[w] |= (uint32_t)code << b;
     }
-    std::memcpy(pg + pl.norms_off + 4 * t, kr + d / 4 + d / 8, 4);
+    std::memcpy(pg + pl.norms_off + 4 * t, kr + kidx + d / 8, 4);
     for (int q = 0; q < d / 32; ++q)
       std::memcpy(pg + pl.vscale_off + 2 * (size_t)tq::vscale_idx(d, t, q), vr + (size_t)d * vb / 8 + 2 * q, 2);
   }
@@ -706,8 +729,9 @@ tq_status tq_get_tables(const tq_ctx* ctx, float* D, uint16_t* S_bf16, double* c
   const int d = ctx->cfg.head_dim;
   if (D) std::memcpy(D, ctx->D.data(), sizeof(float) * d);
   if (S_bf16) std::memcpy(S_bf16, ctx->S.data(), 2ull * d * d);
-  if (centroids) std::memcpy(centroids, ctx->cent, sizeof(ctx->cent));
-  if (boundaries) std::memcpy(boundaries, ctx->bnd, sizeof(ctx->bnd));
+  const int nlev = 1 << (ctx->cfg.key_bits - 1);
+  if (centroids) std::memcpy(centroids, ctx->cent, sizeof(double) * nlev);
+  if (boundaries) std::memcpy(boundaries, ctx->bnd, sizeof(double) * (nlev - 1));
   return ok();
 }
 

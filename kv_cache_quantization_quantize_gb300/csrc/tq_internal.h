@@ -24,52 +24,58 @@ constexpr int kMaxG = 4;    // query heads per KV head served by one decode CTA 
 // ---------------------------------------------------------------------------------------------
 // Packed page of 128 tokens of one KV head. The layout is fragment-major: the decode kernel's
 // mma.sync operand registers are cut out of it with one LOP3 per 2 elements. Sections:
-//   KBITS  [tile 8][plane 3][half d/128][lane 32][row 2] u32 (see kbit_loc).
-//          Planes: 0 = high bit of the Lloyd-Max index, 1 = low bit, 2 = QJL sign (1 = z >= 0).
+//   KBITS  [tile 8][plane kb][half d/128][lane 32][row 2] u32 (see kbit_loc), kb = key_bits planes:
+//          planes 0 .. kb-2 = the Lloyd-Max index bits from the highest down, plane kb-1 = QJL sign
+//          (1 = z >= 0).
 //   NORMS  [token 128] {fp16 n, fp16 gamma}.
 //   VBITS  2-bit: [block 4][m-tile d/16][lane 32] u32; 4-bit: [block 4][m-tile d/16][lane 32][2] u32.
 //   VSCALE [token/2 64][group d/32][token&1 2] fp16 (pairs of consecutive tokens per group).
-// Per token: K (3*d/8 + 4 B) + V (d*vb/8 + d/16 B); d=128, V2 -> 92 B, identical to the canonical
+// Per token: K (kb*d/8 + 4 B) + V (d*vb/8 + d/16 B); d=128, K3/V2 -> 92 B, identical to the canonical
 // record size. A page is therefore the canonical records in another order.
 // ---------------------------------------------------------------------------------------------
 struct PageLayout {
-  int d, vb;
+  int d, vb, kb;
   uint32_t kbits_off, norms_off, vbits_off, vscale_off, bytes;
 };
 
-TQ_HD PageLayout page_layout(int d, int vb) {
+TQ_HD PageLayout page_layout(int d, int vb, int kb) {
   PageLayout p;
   p.d = d;
   p.vb = vb;
+  p.kb = kb;
   p.kbits_off = 0;
-  p.norms_off = p.kbits_off + 3u * kPage * d / 8;
+  p.norms_off = p.kbits_off + (uint32_t)kb * kPage * d / 8;
   p.vbits_off = p.norms_off + 4u * kPage;
   p.vscale_off = p.vbits_off + (uint32_t)kPage * d * vb / 8;
   p.bytes = p.vscale_off + 2u * kPage * (d / 32);
   return p;
 }
 
-// Location of the key bit of (token t, coordinate j, plane pi) in KBITS: u32 word index and bit.
-// KBITS is [tile 8][plane 3][half d/128][lane 32][row 2] u32. Tile = 16 tokens, row r = token bit 3,
+// Location of the key bit of (token t, coordinate j, plane pi) in KBITS of a page with kb planes: u32
+// word index and bit. KBITS is [tile 8][plane kb][half d/128][lane 32][row 2] u32. Tile = 16 tokens, row r = token bit 3,
 // lane = 4g + c with g = token bits 0-2. Bit q + 16e of a word holds coordinate
 // 128*half + 16s + 8sub + 2c + e, with pair index q = 2s + sub. Masking bits q and q + 16 of a word
 // gives the f16 pair of m16n8k16 operand A (rows = tokens, k = coordinates). For q < 12 each half is
 // exactly 2^(q-24) when set; pairs 12..15 are shifted down by 4 first.
 // head_dim 64 has 4 pair indices per tile, so one word holds both tiles of a 32-token group: KBITS is
-// [group 4][plane 3][lane 32][row 2] u32 and the odd tile sits 8 bit positions higher (the decoder
+// [group 4][plane kb][lane 32][row 2] u32 and the odd tile sits 8 bit positions higher (the decoder
 // shifts it down by 8 first).
-TQ_HD void kbit_loc(int d, int t, int j, int pi, int& word, int& bit) {
+TQ_HD void kbit_loc(int d, int kb, int t, int j, int pi, int& word, int& bit) {
   const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
   const int half = j >> 7, jj = j & 127;
   const int s = jj >> 4, sub = (jj >> 3) & 1, c = (jj >> 1) & 3, e = jj & 1;
   if (d == 64) {
-    word = (((tile >> 1) * 3 + pi) * 32 + 4 * g + c) * 2 + r;
+    word = (((tile >> 1) * kb + pi) * 32 + 4 * g + c) * 2 + r;
     bit = 2 * s + sub + 8 * (tile & 1) + 16 * e;
     return;
   }
-  word = ((((tile * 3 + pi) * (d >> 7) + half) * 32) + 4 * g + c) * 2 + r;
+  word = ((((tile * kb + pi) * (d >> 7) + half) * 32) + 4 * g + c) * 2 + r;
   bit = 2 * s + sub + 16 * e;
 }
+// Bit of plane pi in a per-coordinate key code (idx | sign << (kb - 1)): index bits from the highest
+// down, then the sign.
+TQ_HD int plane_bit(int code, int pi, int kb) { return (code >> (pi < kb - 1 ? kb - 2 - pi : kb - 1)) & 1; }
+
 // Effective bit position (after the decoder's shift) of pair index q.
 TQ_HD int kpair_pos(int q) { return q < 12 ? q : q - 4; }
 
@@ -123,9 +129,16 @@ struct TableOffsets {
 TQ_HD int sfrag_idx(int d, int mt, int ks, int lane) { return (mt * (d / 16) + ks) * 32 + lane; }
 TableOffsets table_offsets(int d);
 
-// Codebook block: cb[0..3] centroids, cb[4..6] boundaries, cb[8] alpha=(c2+c3)/2, cb[9] beta=(c3-c2)/2,
-// cb[10] = max_i sum_j |S_ij| (rounded up).
-constexpr int kCbFloats = 16;
+// Codebook block (floats). The index has kb - 1 bits, L = 2^(kb-1) levels.
+//   cb[kCbCent ..]: the L centroids.
+//   cb[kCbBnd ..]: the L - 1 boundaries.
+//   cb[kCbW ..]: the weights of the +-1 index planes. The codebook is odd-symmetric, so
+//     c[idx] = sum_p w_p (2 bit_p - 1), where the planes are:
+//     - 2 bits: the high and low bit, with w = (c2 + c3)/2 and (c3 - c2)/2;
+//     - 3 bits: b2, b1, b0 and b2^b1^b0, with w = A, B, C, E. These fit the upper levels c4..c7:
+//       c = A + B t1 + C t0 + E t1 t0, where t = 2 bit - 1. The lower half follows by symmetry.
+//   cb[kCbSmax]: max_i sum_j |S_ij| (rounded up).
+constexpr int kCbCent = 0, kCbBnd = 8, kCbW = 16, kCbSmax = 20, kCbFloats = 32;
 
 }  // namespace tq
 
@@ -143,15 +156,15 @@ struct tq_ctx {
   size_t pages_off = 0, ring_off = 0, state_off = 0, acnt_off = 0, btab_off = 0, status_off = 0, total_bytes = 0;
   std::vector<float> D;
   std::vector<uint16_t> S;  // bf16 bits, row-major
-  double cent[4] = {0, 0, 0, 0};
-  double bnd[3] = {0, 0, 0};
+  double cent[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 2^(key_bits-1) used
+  double bnd[7] = {0, 0, 0, 0, 0, 0, 0};
 };
 
 namespace tq {
 
 // Pointers and sizes for one layer, passed to kernels by value.
 struct LayerView {
-  int d, vb, G, Hkv, Hq, max_seqs, max_ctx, max_pages;
+  int d, vb, kb, G, Hkv, Hq, max_seqs, max_ctx, max_pages;
   uint32_t page_bytes;
   const float* D;
   const uint16_t* S;   // bf16 [d][d]

@@ -113,16 +113,14 @@ __device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int
 
 // Bits of plane pi of one token's key codes kc (coordinates 16 sq + 8 sub + 2c + e of a 128-coordinate
 // half, sq < nsq) at bit 2 sq + sub + 16 e (+ shift) of a KBITS word (see kbit_loc).
-__device__ __forceinline__ uint32_t kbits_field(const uint8_t* kc, int pi, int nsq, int shift) {
+__device__ __forceinline__ uint32_t kbits_field(const uint8_t* kc, int pi, int kb, int nsq, int shift) {
   uint32_t word = 0;
   for (int sq = 0; sq < nsq; ++sq)
 #pragma unroll
     for (int sub = 0; sub < 2; ++sub)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int code = kc[16 * sq + 8 * sub + e];
-        const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
-        word |= (uint32_t)bit << (2 * sq + sub + 16 * e + shift);
+        word |= (uint32_t)plane_bit(kc[16 * sq + 8 * sub + e], pi, kb) << (2 * sq + sub + 16 * e + shift);
       }
   return word;
 }
@@ -147,7 +145,7 @@ __device__ __forceinline__ void load_token(const AppendArgs& a, int which, int s
   }
 }
 
-// Shared-memory arrays of the CUDA-core quantiser: per-token key codes (idx | sign << 2), value codes,
+// Shared-memory arrays of the CUDA-core quantiser: per-token key codes (idx | sign << (kb - 1)), value codes,
 // {n, gamma} and value scales of a page, and the f16 hi / lo split of the residuals of one 32-token
 // block (rows padded by 8 halves: conflict-free B-fragment reads).
 template <int D>
@@ -187,8 +185,8 @@ __device__ __forceinline__ void mma_f16_acc(float (&c)[4], const uint4& a, uint3
 // f16 fragment table, B = the residuals scaled by 2^8 and split into f16 hi + lo; the scale leaves the
 // signs unchanged). The page's first `valid` tokens come from the ring (positions below L) and then
 // from the new input; tokens past `valid` are coded as zero vectors. Run by all kQThreads threads of
-// the CTA; ends with a block barrier.
-template <int D>
+// the CTA; ends with a block barrier. KB = key bits: a (KB - 1)-bit Lloyd-Max index plus the sign.
+template <int D, int KB>
 __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
                                             int valid, int t_begin, int t_end, const QSmem<D>& sm) {
   constexpr int NE = D / 32;  // coordinates per lane
@@ -200,13 +198,14 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int tb = t_begin & ~31;  // the block's first token
   const LayerView& lv = a.lv;
-  float Dv[NE], cent[4], bnd[3];
+  constexpr int NL = 1 << (KB - 1);  // Lloyd-Max levels
+  float Dv[NE], cent[NL], bnd[NL - 1];
 #pragma unroll
   for (int e = 0; e < NE; ++e) Dv[e] = lv.D[lane_coord<D>(e, lane)];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) cent[i] = lv.cb[i];
+  for (int i = 0; i < NL; ++i) cent[i] = lv.cb[kCbCent + i];
 #pragma unroll
-  for (int i = 0; i < 3; ++i) bnd[i] = lv.cb[4 + i];
+  for (int i = 0; i < NL - 1; ++i) bnd[i] = lv.cb[kCbBnd + i];
 
   const int vb = lv.vb, vhalf = 1 << (vb - 1);
   const float inv_sqrt_d = rsqrtf((float)D);
@@ -234,8 +233,23 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       const float yy = y[e] * scale;
-      const int idx = (yy > bnd[0]) + (yy > bnd[1]) + (yy > bnd[2]);
-      const float res = yy - cent[idx];
+      // index = #{boundaries below yy} by binary search over the sorted boundaries
+      int idx;
+      float cv;
+      if (KB == 3) {
+        const bool hb = yy > bnd[1];
+        const bool lb = yy > (hb ? bnd[2] : bnd[0]);
+        idx = 2 * hb + lb;
+        cv = hb ? (lb ? cent[3] : cent[2]) : (lb ? cent[1] : cent[0]);
+      } else {
+        const bool b2 = yy > bnd[3];
+        const bool b1 = yy > (b2 ? bnd[5] : bnd[1]);
+        const bool b0 = yy > (b2 ? (b1 ? bnd[6] : bnd[4]) : (b1 ? bnd[2] : bnd[0]));
+        idx = 4 * b2 + 2 * b1 + b0;
+        cv = b2 ? (b1 ? (b0 ? cent[7] : cent[6]) : (b0 ? cent[5] : cent[4]))
+                : (b1 ? (b0 ? cent[3] : cent[2]) : (b0 ? cent[1] : cent[0]));
+      }
+      const float res = yy - cv;
       rr = fmaf(res, res, rr);
       const int j = lane_coord<D>(e, lane);
       const float rs = res * 256.f;
@@ -336,7 +350,8 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int t = tb + 8 * (nt0 + n) + 2 * c + (i & 1), row = 16 * mt + g + 8 * (i >> 1);
-          if (t >= t_begin && t < t_end) kcode[t * D + row] = (uint8_t)(kcode[t * D + row] | ((z[n][i] >= 0.f) << 2));
+          if (t >= t_begin && t < t_end)
+            kcode[t * D + row] = (uint8_t)(kcode[t * D + row] | ((z[n][i] >= 0.f) << (KB - 1)));
         }
     }
   }
@@ -347,12 +362,12 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
 // come from the ring (positions below L) and then from the new input; tokens past `valid` are coded as
 // zero vectors. A 32-token block owns whole words of every page section, so four CTAs can write the
 // four blocks of one page independently. Run by all kQThreads threads of the CTA.
-template <int D>
+template <int D, int KB>
 __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, int h, int slot, int L, int Np, int pg,
                                                   int valid, int q32, uint8_t* smem) {
   const int t0 = 32 * q32, t1 = t0 + 32;
   const QSmem<D> sm(smem);
-  code_tokens<D>(a, b, h, slot, L, Np, pg, valid, t0, t1, sm);
+  code_tokens<D, KB>(a, b, h, slot, L, Np, pg, valid, t0, t1, sm);
   uint8_t* kcode = sm.kcode;
   uint8_t* vcode = sm.vcode;
   uint32_t* norms = sm.norms;
@@ -367,36 +382,25 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
     return;
   }
-  const PageLayout pl = page_layout(D, vb);
+  const PageLayout pl = page_layout(D, vb, KB);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   constexpr int HALVES = D >= 128 ? D / 128 : 1;  // 128-coordinate halves (the head_dim 64 words are below)
+  constexpr int WT = 64 * KB;                      // KBITS words of a tile per half (a 32-token group at d=64)
   if (D == 64) {  // one word holds both 16-token tiles of the block: [group][plane][lane][row]
-    for (int w = q32 * 192 + tid; w < (q32 + 1) * 192; w += kQThreads) {
-      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3;
+    for (int w = q32 * WT + tid; w < (q32 + 1) * WT; w += kQThreads) {
+      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % KB;
       uint32_t word = 0;
 #pragma unroll
       for (int kap = 0; kap < 2; ++kap)
-        word |= kbits_field(kcode + (32 * q32 + 16 * kap + (ln >> 2) + 8 * r) * D + 2 * (ln & 3), pi, 4, 8 * kap);
+        word |= kbits_field(kcode + (32 * q32 + 16 * kap + (ln >> 2) + 8 * r) * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
       kw[w] = word;
     }
   }
-  for (int w = (t0 / 16) * 192 * HALVES + tid; D >= 128 && w < (t1 / 16) * 192 * HALVES; w += kQThreads) {
-    const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % 3;
-    const int tile = w / (192 * HALVES);
+  for (int w = (t0 / 16) * WT * HALVES + tid; D >= 128 && w < (t1 / 16) * WT * HALVES; w += kQThreads) {
+    const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % KB;
+    const int tile = w / (WT * HALVES);
     const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
-    const uint8_t* kc = kcode + t * D + 128 * hf + 2 * c;
-    uint32_t word = 0;
-#pragma unroll
-    for (int sq = 0; sq < 8; ++sq)
-#pragma unroll
-      for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int code = kc[16 * sq + 8 * sub + e];
-          const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
-          word |= (uint32_t)bit << (2 * sq + sub + 16 * e);
-        }
-    kw[w] = word;
+    kw[w] = kbits_field(kcode + t * D + 128 * hf + 2 * c, pi, KB, 8, 0);
   }
   uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
   for (int t = t0 + tid; t < t1; t += kQThreads) nw[t] = norms[t];
@@ -443,12 +447,12 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
 // and writes only their bits. Key words, {n, gamma} and value scales belong to one token each; a value
 // word holds the codes of 8 tokens of its block, so it is read, the new tokens' fields replaced, and
 // written back (one thread per word: this CTA is the block's only writer). Run by all kQThreads threads.
-template <int D>
+template <int D, int KB>
 __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, int h, int slot, int L, int Np,
                                                     int pg, int t_lo, int t_hi, uint8_t* smem) {
   constexpr int HALVES = D >= 128 ? D / 128 : 1;  // 128-coordinate halves (head_dim 64: see below)
   const QSmem<D> sm(smem);
-  code_tokens<D>(a, b, h, slot, L, Np, pg, t_hi, t_lo, t_hi, sm);
+  code_tokens<D, KB>(a, b, h, slot, L, Np, pg, t_hi, t_lo, t_hi, sm);
   const int tid = threadIdx.x;
   const LayerView& lv = a.lv;
   const int vb = lv.vb, ntok = t_hi - t_lo;
@@ -457,40 +461,29 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
     return;
   }
-  const PageLayout pl = page_layout(D, vb);
+  const PageLayout pl = page_layout(D, vb, KB);
   uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
   if (D == 64) {  // a word holds two tokens (both tiles of the block): replace the new tokens' fields
     const int grp = t_lo >> 5;
-    for (int w = grp * 192 + tid; w < (grp + 1) * 192; w += kQThreads) {
-      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % 3;
+    for (int w = grp * 64 * KB + tid; w < (grp + 1) * 64 * KB; w += kQThreads) {
+      const int r = w & 1, ln = (w >> 1) & 31, pi = (w >> 6) % KB;
       uint32_t mask = 0, bits = 0;
 #pragma unroll
       for (int kap = 0; kap < 2; ++kap) {
         const int t = 32 * grp + 16 * kap + (ln >> 2) + 8 * r;
         if (t >= t_lo && t < t_hi) {
           mask |= 0x00FF00FFu << (8 * kap);
-          bits |= kbits_field(sm.kcode + t * D + 2 * (ln & 3), pi, 4, 8 * kap);
+          bits |= kbits_field(sm.kcode + t * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
         }
       }
       if (mask) kw[w] = (kw[w] & ~mask) | bits;
     }
   }
-  for (int i = tid; D >= 128 && i < ntok * 12 * HALVES; i += kQThreads) {  // (token, plane, half, c)
-    const int c = i & 3, hf = (i >> 2) % HALVES, pi = (i / (4 * HALVES)) % 3, t = t_lo + i / (12 * HALVES);
+  for (int i = tid; D >= 128 && i < ntok * 4 * KB * HALVES; i += kQThreads) {  // (token, plane, half, c)
+    const int c = i & 3, hf = (i >> 2) % HALVES, pi = (i / (4 * HALVES)) % KB, t = t_lo + i / (4 * KB * HALVES);
     const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
-    const uint8_t* kc = sm.kcode + t * D + 128 * hf + 2 * c;
-    uint32_t word = 0;
-#pragma unroll
-    for (int sq = 0; sq < 8; ++sq)
-#pragma unroll
-      for (int sub = 0; sub < 2; ++sub)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int code = kc[16 * sq + 8 * sub + e];
-          const int bit = pi == 0 ? (code >> 1) & 1 : pi == 1 ? code & 1 : (code >> 2) & 1;
-          word |= (uint32_t)bit << (2 * sq + sub + 16 * e);
-        }
-    kw[((((tile * 3 + pi) * HALVES + hf) * 32) + 4 * g + c) * 2 + r] = word;
+    kw[((((tile * KB + pi) * HALVES + hf) * 32) + 4 * g + c) * 2 + r] =
+        kbits_field(sm.kcode + t * D + 128 * hf + 2 * c, pi, KB, 8, 0);
   }
   uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
   for (int t = t_lo + tid; t < t_hi; t += kQThreads) nw[t] = sm.norms[t];
@@ -540,7 +533,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
     sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = sm.scales[i];
 }
 
-template <int D>
+template <int D, int KB>
 __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int b = blockIdx.x, h = blockIdx.y;
@@ -549,7 +542,7 @@ __global__ void __launch_bounds__(kQThreads) k_quantize_pages(AppendArgs a) {
   int slot, L, Np, pg, valid;
   const int j = blockIdx.z >> 2;  // 4 CTAs per page, one per 32-token block
   if (!page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && blockIdx.z == 0 && threadIdx.x == 0)) return;
-  quantize_page_cta<D>(a, b, h, slot, L, Np, pg, valid, blockIdx.z & 3, smem);
+  quantize_page_cta<D, KB>(a, b, h, slot, L, Np, pg, valid, blockIdx.z & 3, smem);
 }
 
 // Writes the ring rows of positions [p0, L2) of row b (every KV head, K and V) from the new input,
@@ -584,7 +577,7 @@ __device__ __forceinline__ void write_ring_rows(const AppendArgs& a, int b, int 
 // 4 Hkv CTAs to arrive writes the new ring rows of every head (all CTAs have read the old ones by
 // then) and publishes the new length; without an overflow CTA (b, 0, 0) does that alone. Dependents (the decode) are released only after that, so they
 // may read the state before their own stream wait.
-template <int D>
+template <int D, int KB>
 __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
@@ -630,16 +623,16 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
     for (int blk = L / 32 + q32; blk <= end_blk; blk += 4) {
       const int pg = blk / 4;
       if (entered && pg * kPage == Np2) {
-        quantize_page_cta<D>(a, b, h, slot, L, Np, pg, min(kPage, L2 - pg * kPage), blk & 3, smem);
+        quantize_page_cta<D, KB>(a, b, h, slot, L, Np, pg, min(kPage, L2 - pg * kPage), blk & 3, smem);
       } else {
         const int base = pg * kPage;
-        quantize_new_tokens<D>(a, b, h, slot, L, Np, pg, max(L, 32 * blk) - base, min(L2, 32 * blk + 32) - base,
-                               smem);
+        quantize_new_tokens<D, KB>(a, b, h, slot, L, Np, pg, max(L, 32 * blk) - base,
+                                   min(L2, 32 * blk + 32) - base, smem);
       }
       __syncthreads();  // shared memory is staged again by the next block
     }
   } else if (Np2 > Np) {
-    quantize_page_cta<D>(a, b, h, slot, L, Np, Np / kPage, kPage, q32, smem);  // Np2 - Np == 128
+    quantize_page_cta<D, KB>(a, b, h, slot, L, Np, Np / kPage, kPage, q32, smem);  // Np2 - Np == 128
   }
   __syncthreads();  // this CTA has read the old ring rows it needed
   if (tid == 0) {
@@ -858,7 +851,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* page = page_addr(lv, cslot, chead, cpg);
     const bool wr = page != nullptr;  // paged cache without a block for this page: code it, write nothing
     if (!wr && tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
-    const PageLayout pl = page_layout(D, lv.vb);
+    const PageLayout pl = page_layout(D, lv.vb, 3);  // this kernel serves key_bits 3
     const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
     if (kpath) {
@@ -875,8 +868,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_barrier(1, 256);
       const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
       const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
-      const float b0 = lv.cb[4], b1 = lv.cb[5], b2 = lv.cb[6];
-      const float c0 = lv.cb[0], c1 = lv.cb[1], c2 = lv.cb[2], c3 = lv.cb[3];
+      const float b0 = lv.cb[kCbBnd], b1 = lv.cb[kCbBnd + 1], b2 = lv.cb[kCbBnd + 2];
+      const float c0 = lv.cb[kCbCent], c1 = lv.cb[kCbCent + 1], c2 = lv.cb[kCbCent + 2], c3 = lv.cb[kCbCent + 3];
       uint32_t whi[4] = {0u, 0u, 0u, 0u}, wlo[4] = {0u, 0u, 0u, 0u};
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -1171,35 +1164,45 @@ size_t quantize_smem_bytes() {
   return quantize_smem_bytes_d<D>();
 }
 
-template <int D>
-cudaError_t launch_quantize_d(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
+template <int D, int KB>
+cudaError_t launch_quantize_dk(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
   const size_t smem = quantize_smem_bytes<D>();
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_pages<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_pages<D, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (pages > 65535 / 4) return cudaErrorInvalidValue;  // grid z holds four 32-token CTAs per page
   dim3 grid(batch, a.lv.Hkv, 4 * pages);
-  return launch_pdl(k_quantize_pages<D>, grid, dim3(kQThreads), smem, s, a);
+  return launch_pdl(k_quantize_pages<D, KB>, grid, dim3(kQThreads), smem, s, a);
 }
 
-template <int D>
-cudaError_t launch_append_small_d(const AppendArgs& a, int batch, size_t smem, cudaStream_t s) {
+template <int D, int KB>
+cudaError_t launch_append_small_dk(const AppendArgs& a, int batch, cudaStream_t s) {
+  const size_t smem = quantize_smem_bytes<D>();
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_append_small<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(k_append_small<D, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  return launch_pdl(k_append_small<D>, dim3(batch, a.lv.Hkv, 4), dim3(kQThreads), smem, s, a);
+  return launch_pdl(k_append_small<D, KB>, dim3(batch, a.lv.Hkv, 4), dim3(kQThreads), smem, s, a);
 }
 
 cudaError_t launch_quantize(const AppendArgs& a, int batch, int pages, cudaStream_t s) {
-  if (a.lv.d == 64) return launch_quantize_d<64>(a, batch, pages, s);
-  if (a.lv.d == 128) return launch_quantize_d<128>(a, batch, pages, s);
-  return launch_quantize_d<256>(a, batch, pages, s);
+  const bool k4 = a.lv.kb == 4;
+  if (a.lv.d == 64) return k4 ? launch_quantize_dk<64, 4>(a, batch, pages, s) : launch_quantize_dk<64, 3>(a, batch, pages, s);
+  if (a.lv.d == 128)
+    return k4 ? launch_quantize_dk<128, 4>(a, batch, pages, s) : launch_quantize_dk<128, 3>(a, batch, pages, s);
+  return k4 ? launch_quantize_dk<256, 4>(a, batch, pages, s) : launch_quantize_dk<256, 3>(a, batch, pages, s);
+}
+
+cudaError_t launch_append_small(const AppendArgs& a, int batch, cudaStream_t s) {
+  const bool k4 = a.lv.kb == 4;
+  if (a.lv.d == 64) return k4 ? launch_append_small_dk<64, 4>(a, batch, s) : launch_append_small_dk<64, 3>(a, batch, s);
+  if (a.lv.d == 128) return k4 ? launch_append_small_dk<128, 4>(a, batch, s) : launch_append_small_dk<128, 3>(a, batch, s);
+  return k4 ? launch_append_small_dk<256, 4>(a, batch, s) : launch_append_small_dk<256, 3>(a, batch, s);
 }
 
 // Bulk appends of head_dim 128 use the tcgen05 kernel: one persistent CTA per SM over all pages.
@@ -1254,13 +1257,10 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.max_new = max_new;
   a.flush = 0;
   a.full = ctx->cfg.ring_size == 0;
-  if (max_new < kPage) {  // decode-sized appends: one launch (page on ring overflow + ring rows + state)
-    if (a.lv.d == 64) return launch_append_small_d<64>(a, batch, quantize_smem_bytes<64>(), s);
-    if (a.lv.d == 128) return launch_append_small_d<128>(a, batch, quantize_smem_bytes<128>(), s);
-    return launch_append_small_d<256>(a, batch, quantize_smem_bytes<256>(), s);
-  }
+  if (max_new < kPage) return launch_append_small(a, batch, s);  // page on ring overflow + ring rows + state
   const int pages = (max_new + kPage - 1) / kPage;
-  cudaError_t e = (a.lv.d == 128 && max_new >= kPage && dt == 0)
+  // the tcgen05 bulk coder serves head_dim 128 with key_bits 3; other shapes use the CUDA-core coder
+  cudaError_t e = (a.lv.d == 128 && a.lv.kb == 3 && max_new >= kPage && dt == 0)
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
                       : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;

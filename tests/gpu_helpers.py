@@ -35,7 +35,7 @@ def check_sequence(cache, layer, slot, k_all, v_all, tables, heads=None):
     for h in (range(k_all.shape[1]) if heads is None else heads):
         kr, vr = cache.records(layer, slot, h, P)
         if P:
-            kk = oracle.unpack_key_records(kr, cache.cfg.head_dim)
+            kk = oracle.unpack_key_records(kr, cache.cfg.head_dim, cache.cfg.key_bits)
             vv = oracle.unpack_value_records(vr, cache.cfg.head_dim, cache.cfg.value_bits)
             stats.append(check_key_records(kk, f64(k_all[:P, h]), D, S, c, t))
             stats.append(check_value_records(vv, f64(v_all[:P, h]), D, cache.cfg.value_bits))
@@ -56,7 +56,7 @@ def oracle_decode(cache, layer, slot, q_row, tables, scale=None):
     out = np.zeros((cfg.n_q_heads, cfg.head_dim))
     for h in range(cfg.n_kv_heads):
         kr, vr = cache.records(layer, slot, h, P)
-        keys = oracle.unpack_key_records(kr, cfg.head_dim) if P else None
+        keys = oracle.unpack_key_records(kr, cfg.head_dim, cfg.key_bits) if P else None
         vals = oracle.unpack_value_records(vr, cfg.head_dim, cfg.value_bits) if P else None
         rk, rv = cache.ring(layer, slot, h)
         out[h * G:(h + 1) * G] = oracle.decode_attention(

@@ -35,6 +35,7 @@ def test_library_exports_every_header_function():
     ("ring_size", -1, _abi.TQ_ERR_UNSUPPORTED),
     ("n_layers", 0, _abi.TQ_ERR_INVALID_ARG), ("n_q_heads", 12, _abi.TQ_ERR_UNSUPPORTED),
     ("n_q_heads", 9, _abi.TQ_ERR_INVALID_ARG), ("max_ctx", 0, _abi.TQ_ERR_INVALID_ARG),
+    ("key_bits", 5, _abi.TQ_ERR_UNSUPPORTED), ("key_bits", 2, _abi.TQ_ERR_UNSUPPORTED),
 ])
 def test_invalid_configs_rejected(field, value, status):
     lib = _abi.load()
@@ -45,6 +46,16 @@ def test_invalid_configs_rejected(field, value, status):
     assert lib.tq_init_codebooks(ctypes.byref(cfg), None, 0, None, ctypes.byref(ctx)) == status
     assert not ctx.value
     assert lib.tq_last_error()
+
+
+def test_key_bits_4_needs_value_bits_4():
+    lib = _abi.load()
+    ctx = ctypes.c_void_p()
+    cfg = tqm.config(key_bits=4, value_bits=2)
+    assert lib.tq_init_codebooks(ctypes.byref(cfg), None, 0, None, ctypes.byref(ctx)) == _abi.TQ_ERR_UNSUPPORTED
+    cfg = tqm.config(key_bits=4, value_bits=4)
+    assert lib.tq_init_codebooks(ctypes.byref(cfg), None, 0, None, ctypes.byref(ctx)) == _abi.TQ_OK
+    lib.tq_destroy(ctx)
 
 
 def test_full_tq_mode_config_is_accepted():
@@ -102,14 +113,27 @@ def test_tables_match_oracle_bitwise(d, seed):
     assert np.allclose(c, g["centroids"], rtol=0, atol=1e-13)
     assert np.allclose(t, g["boundaries"], rtol=0, atol=1e-13)
     assert t[1] == 0.0 and np.array_equal(c, -c[::-1])
+    # key_bits 4: the 3-bit codebook
+    h4 = tqm.HostTables(tqm.config(head_dim=d, seed=seed, key_bits=4, value_bits=4))
+    _, _, c4, t4 = h4.tables()
+    g4 = json.load(open(os.path.join(GOLDEN, "codebooks.json")))["codebooks"][f"d{d}_b3"]
+    assert c4.shape == (8,) and t4.shape == (7,)
+    # both are Lloyd iterations stopped near the fixed point (8 cells converge more slowly than 4)
+    assert np.allclose(c4, g4["centroids"], rtol=0, atol=5e-13)
+    assert np.allclose(t4, g4["boundaries"], rtol=0, atol=5e-13)
+    assert t4[3] == 0.0 and np.array_equal(c4, -c4[::-1])
+    # the fp32 values the kernels use agree exactly
+    assert np.array_equal(c4.astype(np.float32), np.array(g4["centroids"]).astype(np.float32))
+    assert np.array_equal(t4.astype(np.float32), np.array(g4["boundaries"]).astype(np.float32))
     # the fp32 values the kernels use agree exactly
     assert np.array_equal(c.astype(np.float32), np.array(g["centroids"]).astype(np.float32))
 
 
-@pytest.mark.parametrize("d,vb,expect", [(64, 2, 48), (64, 4, 64), (128, 2, 92), (128, 4, 124), (256, 2, 180),
-                                         (256, 4, 244)])
-def test_page_bytes_equal_canonical_records(d, vb, expect):
-    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+@pytest.mark.parametrize("d,vb,kb,expect", [(64, 2, 3, 48), (64, 4, 3, 64), (128, 2, 3, 92), (128, 4, 3, 124),
+                                            (256, 2, 3, 180), (256, 4, 3, 244), (64, 4, 4, 72), (128, 4, 4, 140),
+                                            (256, 4, 4, 276)])
+def test_page_bytes_equal_canonical_records(d, vb, kb, expect):
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb, key_bits=kb))
     assert h.key_record_bytes() + h.value_record_bytes() == expect
     assert h.page_bytes() == 128 * expect
 
@@ -120,9 +144,10 @@ def _random_records(h, n, rng):
     return kr, vr
 
 
-@pytest.mark.parametrize("d,vb", [(64, 2), (64, 4), (128, 2), (128, 4), (256, 2), (256, 4)])
-def test_records_page_round_trip(d, vb):
-    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+@pytest.mark.parametrize("d,vb,kb", [(64, 2, 3), (64, 4, 3), (128, 2, 3), (128, 4, 3), (256, 2, 3), (256, 4, 3),
+                                     (64, 4, 4), (128, 4, 4), (256, 4, 4)])
+def test_records_page_round_trip(d, vb, kb):
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb, key_bits=kb))
     rng = np.random.default_rng(d + vb)
     kr, vr = _random_records(h, 128, rng)
     page = h.records_to_page(kr, vr)
@@ -141,37 +166,46 @@ def _unpack(rec, bits, d):
     return ((b[:, :, None] >> sh) & ((1 << bits) - 1)).reshape(rec.shape[0], d)
 
 
-@pytest.mark.parametrize("d,vb", [(64, 2), (64, 4), (128, 2), (128, 4), (256, 2), (256, 4)])
-def test_decoder_operand_extraction_matches_records(d, vb):
+@pytest.mark.parametrize("d,vb,kb", [(64, 2, 3), (64, 4, 3), (128, 2, 3), (128, 4, 3), (256, 2, 3), (256, 4, 3),
+                                     (64, 4, 4), (128, 4, 4), (256, 4, 4)])
+def test_decoder_operand_extraction_matches_records(d, vb, kb):
     """Emulate, on the CPU, how the decode kernel cuts mma.sync operands out of a page.
 
     Key side (f16 m16n8k16, A operand, rows = tokens, k = coordinates): every f16 half must be 0, or
     2^(q-24) for the bit position q it was masked from, exactly when the bit-plane value is 1.
     Value side (f16 m16n8k16, A operand): every f16 half must equal code * 2^(pos - 24) for the
     position that the B operand is prescaled with.
+    With a 3-bit index (key_bits 4) the decoder also forms the parity plane b2 ^ b1 ^ b0 by XOR of the
+    three index-plane words before masking; that plane is checked as a fifth.
     """
-    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb))
+    from oracle.quant import _unpack_bits
+    h = tqm.HostTables(tqm.config(head_dim=d, value_bits=vb, key_bits=kb))
     rng = np.random.default_rng(7)
     kr, vr = _random_records(h, 128, rng)
     page = h.records_to_page(kr, vr)
-    idx = _unpack(kr, 2, d)
-    sign = _unpack(kr[:, d // 4:], 1, d)
+    mb = kb - 1
+    idx = _unpack_bits(kr[:, :d * mb // 8], mb, d)
+    sign = _unpack(kr[:, d * mb // 8:], 1, d)
     codes = _unpack(vr, vb, d)
-    planes = [(idx >> 1) & 1, idx & 1, sign]
-    kw = page[:3 * 128 * d // 8].view(np.uint32)
+    planes = [(idx >> (mb - 1 - p)) & 1 for p in range(mb)] + [sign]
+    if kb == 4:
+        planes.append(((idx >> 2) ^ (idx >> 1) ^ idx) & 1)
+    kw = page[:kb * 128 * d // 8].view(np.uint32)
     halves = max(1, d // 128)
+
+    def word(tile, pi, hf, lane, row):
+        if pi == kb:  # the parity plane: XOR of the index-plane words
+            return word(tile, 0, hf, lane, row) ^ word(tile, 1, hf, lane, row) ^ word(tile, 2, hf, lane, row)
+        if d == 64:  # both tiles of a 32-token group share a word; the odd one 8 positions up
+            return int(kw[(((tile >> 1) * kb + pi) * 32 + lane) * 2 + row]) >> (8 * (tile & 1))
+        return int(kw[(((tile * kb + pi) * halves + hf) * 32 + lane) * 2 + row])
+
     for tile in range(8):
-        for pi in range(3):
+        for pi in range(len(planes)):
             for hf in range(halves):
                 for lane in range(32):
                     g, c = lane >> 2, lane & 3
-                    if d == 64:  # both tiles of a 32-token group share a word; the odd one 8 positions up
-                        base = (((tile >> 1) * 3 + pi) * 32 + lane) * 2
-                        sh = 8 * (tile & 1)
-                    else:
-                        base = (((tile * 3 + pi) * halves + hf) * 32 + lane) * 2
-                        sh = 0
-                    w0, w1 = int(kw[base]) >> sh, int(kw[base + 1]) >> sh  # rows g and g + 8 of the tile
+                    w0, w1 = word(tile, pi, hf, lane, 0), word(tile, pi, hf, lane, 1)  # rows g and g + 8 of the tile
                     for s_ in range(min(8, d // 16)):
                         if s_ < 6:
                             x0, x1, q0 = w0, w1, 2 * s_
@@ -189,7 +223,7 @@ def test_decoder_operand_extraction_matches_records(d, vb):
                                 qeff = q0 + (r >> 1)
                                 expect = 2.0 ** (qeff - 24) if planes[pi][t, j] else 0.0
                                 assert val == expect
-    off = 3 * 128 * d // 8 + 4 * 128
+    off = kb * 128 * d // 8 + 4 * 128
     vw = page[off:off + 128 * d * vb // 8].view(np.uint32)
     nmt = d // 16
     pos2 = {(0, 0): 0, (0, 1): 4, (1, 0): 6, (1, 1): 8}
