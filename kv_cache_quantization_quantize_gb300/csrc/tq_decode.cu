@@ -172,21 +172,23 @@ __host__ __device__ constexpr int decode_threads() {
 // =============================================================================================
 
 // B-operand planes of the key MMAs:
-//   key_bits 3: index planes 0, 1 and the QJL sign plane 2.
-//   key_bits 4: index planes 0-3 (3 = parity plane), the QJL sign plane 4, and plane 5, the f16
-//     rounding remainder of plane 0's operand (the largest weight), multiplied against plane 0's bits.
-//     Without plane 5 the f16 rounding of four index operands adds about 1.2x the score error of the
-//     2-bit index.
-__host__ __device__ constexpr int key_bplanes(int kb) { return kb == 3 ? 3 : 6; }
-// B plane that carries the QJL operand.
+//   key_bits 3: index planes 0, 1 and the QJL sign plane 2; at head_dim 64 also plane 3, the f16
+//     rounding remainder of plane 0's operand, multiplied against plane 0's bits (with 64 coordinates
+//     the rounding error of the operands weighs most).
+//   key_bits 4: index planes 0-3 (3 = parity plane), the QJL sign plane 4, and plane 5, the remainder
+//     of plane 0 (the largest weight). Without it the f16 rounding of four index operands adds about
+//     1.2x the score error of the 2-bit index.
+__host__ __device__ constexpr int key_bplanes(int kb, int d) { return kb == 3 ? (d == 64 ? 4 : 3) : 6; }
+// B plane that carries the QJL operand, and the remainder plane of plane 0 (-1: none).
 __host__ __device__ constexpr int key_qjl_plane(int kb) { return kb == 3 ? 2 : 4; }
+__host__ __device__ constexpr int key_rem_plane(int kb, int d) { return kb == 3 ? (d == 64 ? 3 : -1) : 5; }
 
 // Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
 template <int D, int KB>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
   // q_rot, q_proj [4][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes] uint2;
   // per-warp offset sums [warps][8]
-  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (key_bplanes(KB) * D / 16) +
+  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (key_bplanes(KB, D) * D / 16) +
          sizeof(float) * 8 * (decode_threads<D>() / 32);
 }
 
@@ -232,7 +234,8 @@ __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f)
 template <int D, int NT, int KB>
 __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
                                            float (&um)[2], float (&cm)[2], float (&uq)[2], float (&cq)[2]) {
-  constexpr int NBP = key_bplanes(KB), QP = key_qjl_plane(KB), NMW = KB == 3 ? 2 : 4;  // B planes; QJL plane; weights
+  constexpr int NBP = key_bplanes(KB, D), QP = key_qjl_plane(KB), RP = key_rem_plane(KB, D);
+  constexpr int NMW = KB == 3 ? 2 : 4;  // index-plane weights
   constexpr int NE = D / 32;
   constexpr int HALVES = D / warp_coords<D>();
   constexpr int MT = D / 16;
@@ -321,7 +324,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   float sum_m = 0.f, sum_q = 0.f;
   for (int item = warp; item < NITEMS; item += NW) {
     const int s = item % KS, pi = (item / KS) % NBP, hv = item / (NBP * KS);
-    const bool qjl = pi == QP, rem = pi == 5;  // rem: remainder plane of plane 0 (key_bits 4)
+    const bool qjl = pi == QP, rem = pi == RP;  // rem: remainder plane of plane 0
     const float w = qjl ? 2.f * lam_q : 2.f * lv.cb[kCbW + (rem ? 0 : pi)] * lam_m;
     const float* base = qjl ? bp : bm;
     const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
@@ -651,7 +654,8 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
 template <int D, int VB, int STAGES, bool PAGED, int KB>
 __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
-  constexpr int NBP = key_bplanes(KB);  // B planes of the key MMAs (stored planes: KB)
+  constexpr int NBP = key_bplanes(KB, D);  // B planes of the key MMAs (stored planes: KB)
+  constexpr int RP = key_rem_plane(KB, D);
   constexpr int CW = warp_coords<D>();  // coordinates per warp
   constexpr int HALVES = D / CW;
   constexpr int KS = CW / 16;           // key-MMA k-steps per warp
@@ -796,9 +800,9 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
 #pragma unroll
       for (int pi = 0; pi < NBP; ++pi) {
         const uint2 bv = bfr[(pi * KS + s) * 32];
-        // chains: key_bits 3 one per plane; key_bits 4 {0, 1, 5}, {2, 3}, {4}
-        const int ch = KB == 3 ? pi : (pi == 4 ? 2 : (pi == 2 || pi == 3) ? 1 : 0);
-        const int wi = pi == 5 ? 0 : pi;  // the remainder plane multiplies plane 0's bits
+        // chains: key_bits 3 one per plane (the remainder joins plane 0); key_bits 4 {0, 1, 5}, {2, 3}, {4}
+        const int ch = KB == 3 ? (pi == RP ? 0 : pi) : (pi == 4 ? 2 : (pi == 2 || pi == 3) ? 1 : 0);
+        const int wi = pi == RP ? 0 : pi;  // the remainder plane multiplies plane 0's bits
 #pragma unroll
         for (int kap = 0; kap < 2; ++kap) {
           const uint32_t x0 = s < 6 ? kwv[kap][wi].x : kwv[kap][wi].x >> 4;
