@@ -710,12 +710,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // copies (tensor [batch][max_new][Hkv][128], box 64 x 1 x 128 x 1, 128-byte swizzle) that complete on
 // `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
 // all threads (at most one page per row and append).
+// The copy is made by the nthr threads whose index relative to `first` is in [0, nthr).
 __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
-                                             uint64_t* bar) {
+                                             uint64_t* bar, int first, int nthr) {
   constexpr int D = 128;
+  const int rel = (int)threadIdx.x - first;
+  if (rel < 0 || rel >= nthr) return pg * kPage >= L;
   if (pg * kPage >= L) {
-    if (threadIdx.x == 0) {
+    if (rel == 0) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_expect_tx(bar, 4u * 16384u);
       const int z = pg * kPage - L;
@@ -731,7 +734,7 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
     }
     return true;
   }
-  for (int q = threadIdx.x; q < 2 * kPage * (D / 8); q += kTcThreads) {
+  for (int q = rel; q < 2 * kPage * (D / 8); q += nthr) {
     const int which = q >> 11, t = (q >> 4) & 127, c = q & 15;
     const int pos = pg * kPage + t;
     const uint16_t* src;
@@ -784,7 +787,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* vcode = sm + kQbVcode;
   uint64_t* bar_tab = reinterpret_cast<uint64_t*>(sm + kQbBar);
-  uint64_t* bar_qjl = bar_tab + 1;
+  // QJL projections of pages in buffers 0 / 1: two barriers, so that a projection can never complete
+  // twice before the value warps wait for it
+  auto bar_qjl2 = [bar_tab](uint32_t i) { return i ? bar_tab + 7 : bar_tab + 1; };
   uint64_t* bar_ld = bar_tab + 2;   // [2]: page loads into buffer 0 / 1
   uint64_t* bar_rot = bar_tab + 4;  // [2]: rotations into TMEM half 0 / 1
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 6);
@@ -793,7 +798,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   pdl_wait();
   pdl_launch();
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(bar_tab + i, 1);
+    for (int i = 0; i < 8; ++i)
+      if (i != 6) mbar_init(bar_tab + i, 1);  // slot 6 holds the TMEM address
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(bar_tab, 4u * D * D);
     bulk_g2s(sm + kQbHD, lv.HD_sw, 2u * D * D, bar_tab);
@@ -813,13 +819,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int b, h, slot, L, Np, pg;
   int cur = bulk128_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
-  bool tma_cur = cur < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld);
+  bool tma_cur = cur < ntasks &&
+                 bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, 0, kTcThreads);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   bool ok = __syncthreads_and(mbar_wait(bar_tab, 0)) != 0;
   // parities of the next wait: bit i of ph_ld / ph_rot for buffer / TMEM half i
   uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;
-  // The rotation of a page runs on the tensor cores while the previous page is coded: it is issued
-  // here for the first page and, for each later page, once the page before it has issued its QJL MMAs.
+  // Pipeline. Page i lives in smem buffer i % 2 and TMEM half i % 2.
+  //   - The key warps code page i and issue its QJL MMAs.
+  //   - The value warps first take the QJL signs of page i - 1 (its MMAs ran during the end of iteration
+  //     i - 1), which frees buffer and TMEM half (i + 1) % 2. They then start the copy of page i + 1,
+  //     code the values of page i, and issue the rotation of page i + 1.
+  // So no warp waits on the tensor cores inside an iteration: the rotation of page i + 1 and the
+  // projection of page i run while the values of page i are packed. The first page's rotation is
+  // issued here.
   if (ok && cur < ntasks && tid == 0) {
     if (tma_cur && !mbar_wait(bar_ld, 0)) ok = false;
     if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot);
@@ -835,15 +848,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* xr = xs + 256;                                             // [2][128] partial |r|^2
   uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][8] half-1 index words
   uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 6144);     // [128][4] half-1 sign words
+  const PageLayout pl = page_layout(D, lv.vb, 3);  // this kernel serves key_bits 3
+  uint8_t* prev_page = nullptr;  // page whose QJL signs are still to be written (its MMAs are in flight)
+  bool prev = false;
+  // QJL signs of the page in TMEM half `hb` (value warps): wait for its projection, threshold z = S r,
+  // write the sign plane. Returns false if the wait gave up.
+  auto qjl_signs = [&](uint32_t hb, uint8_t* page) -> bool {
+    const bool w_ok = mbar_wait(bar_qjl2(hb), (ph_qjl >> hb) & 1u);
+    ph_qjl ^= 1u << hb;
+    tc_fence_after();
+    const uint32_t prow = tmem + 256u * hb + ((uint32_t)(32 * q4) << 16);
+    uint32_t wsg[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t z[32];
+      tmem_ld32(prow + 64 * half + 32 * cc, z);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int jl = 32 * cc + i;
+        const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+        wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
+      }
+    }
+    if (half) {
+#pragma unroll
+      for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
+    }
+    tc_fence_before();
+    named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
+    if (!half && page) {
+      uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+      const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
+#pragma unroll
+      for (int cw = 0; cw < 4; ++cw) kw[((ktile * 3 + 2) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
+    }
+    return w_ok;
+  };
   while (ok && cur < ntasks) {
     const int cslot = slot, chead = h, cpg = pg;
     const int nxt = bulk128_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
-    const uint32_t buf = buf0 + bufi * 65536u;
-    // the next page's rows stream into the other buffer while this page is coded
-    const bool tma_nxt =
-        nxt < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
-                                     bar_ld + (bufi ^ 1u));
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied pages -> tensor cores
     ok = __syncthreads_and(mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u)) != 0;
     ph_rot ^= 1u << bufi;
     if (!ok) break;
@@ -851,7 +894,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* page = page_addr(lv, cslot, chead, cpg);
     const bool wr = page != nullptr;  // paged cache without a block for this page: code it, write nothing
     if (!wr && tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
-    const PageLayout pl = page_layout(D, lv.vb, 3);  // this kernel serves key_bits 3
     const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
     if (kpath) {
@@ -922,8 +964,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
       named_barrier(1, 256);
-      uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-      const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
+      const uint32_t buf = buf0 + bufi * 65536u;
       if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
         tc_fence_after();
 #pragma unroll
@@ -932,33 +973,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           umma_bf16(tmem + 256u * bufi, umma_desc_sw128(buf + koff),
                     umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
         }
-        umma_commit(bar_qjl);
-        // then the rotation of the next page into the other TMEM half (its page finished last iteration)
-        if (nxt < ntasks) {
-          bool landed = true;
-          if (tma_nxt) {
-            landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
-            if (!landed) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
-          }
-          if (landed) bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u));
-        }
+        umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
       }
-      if (!half) {  // planes 0-1, n and gamma of token t
+      if (!half && wr) {  // planes 0-1, n and gamma of token t
         const float n = nrot * rsqrtf((float)D);
         const float rr = xr[t] + xr[128 + t];
         const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
-        if (wr) {
-          reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
-              (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+        const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
+        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
+            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
 #pragma unroll
-          for (int cw = 0; cw < 4; ++cw) {
-            kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
-            kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
-          }
+        for (int cw = 0; cw < 4; ++cw) {
+          kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
+          kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
         }
       }
-      // the QJL signs are read by the value warps (their path is the shorter one)
     } else {
+      // ---- the previous page's QJL signs; this frees buffer and TMEM half bufi ^ 1 ----
+      if (prev) ok_p = qjl_signs(bufi ^ 1u, prev_page);
+      // ---- start the copy of the next page into buffer bufi ^ 1 ----
+      bool tma_nxt = false;
+      if (nxt < ntasks)
+        tma_nxt = bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
+                               bar_ld + (bufi ^ 1u), 256, 256);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
       // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
       const int vhalf = 1 << (lv.vb - 1);
       const float inv_sqrt_d = rsqrtf((float)D);
@@ -1011,7 +1050,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
         if (wr) sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
       }
-      named_barrier(2, 256);
+      tc_fence_before();
+      named_barrier(2, 256);  // value codes staged; V columns of this half read; next page's rows copied
+      if (tid == 256 && nxt < ntasks) {  // rotation of the next page into TMEM half bufi ^ 1
+        tc_fence_after();
+        bool landed = true;
+        if (tma_nxt) {
+          landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
+          if (!landed) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+        }
+        if (landed) bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u));
+        else ok_p = false;
+      }
+      if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);
       // ---- pack the value codes (fragment-major layout) ----
       const int vt = tid - 256;
       uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
@@ -1046,103 +1097,91 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (wr) vw[w] = word;
         }
       }
-      // ---- the QJL signs of this page's keys, once the key warps' projection MMAs complete ----
-      ok_p = mbar_wait(bar_qjl, ph_qjl);
-      tc_fence_after();
-      uint32_t wsg[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t z[32];
-        tmem_ld32(lrow + 64 * half + 32 * cc, z);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int jl = 32 * cc + i;
-          const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
-          wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
-        }
-      }
-      if (half) {
-#pragma unroll
-        for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
-      }
-      named_barrier(2, 256);
-      if (!half && wr) {
-        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-        const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
-#pragma unroll
-        for (int cw = 0; cw < 4; ++cw) kw[((ktile * 3 + 2) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
-      }
     }
-    ph_qjl ^= kpath ? 0u : 1u;
-    if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);  // waited on by thread 0 above
     tc_fence_before();
     ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, vcode and exchange may be reused
     tc_fence_after();
+    prev = true;
+    prev_page = page;
     cur = nxt;
-    tma_cur = tma_nxt;
     bufi ^= 1u;
   }
-  if (!ok && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  // the last page's QJL signs (its projection was issued in the final iteration)
+  if (ok && prev && !kpath && !qjl_signs(bufi ^ 1u, prev_page)) ok = false;
+  if (!ok && (tid == 0 || tid == 256)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
 }
 
-// Dependents (the decode of this layer) are released only after the state is written: they read the
-// sequence state before their own griddepcontrol.wait to start fetching pages early.
-__global__ void __launch_bounds__(256) k_ring_update(AppendArgs a) {
+// Ring rows of a bulk append: the tokens past the last full page, [batch][pos][Hkv][K|V][d] items of
+// 4 elements, spread over gridDim.y blocks per row. It reads the state before k_ring_update writes it.
+__global__ void __launch_bounds__(256) k_ring_rows(AppendArgs a) {
   const int b = blockIdx.x;
   pdl_wait();  // the quantise launch has read the old ring and state
   const LayerView& lv = a.lv;
   const int slot = a.seq_ids[b];
-  if (slot < 0 || slot >= lv.max_seqs) return;
-  const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
-  const int Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
-  if (a.flush) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      lv.state[2 * slot + 1] = L - Np;
-      __threadfence();
+  if (slot >= 0 && slot < lv.max_seqs) {
+    const int L = lv.state[2 * slot];
+    const int nn = a.n_new[b];
+    const int L2 = L + nn;
+    if (nn >= 0 && nn <= a.max_new && L2 <= lv.max_ctx) {
+      const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
+      const int p0 = max(L, Np2);
+      const int d = lv.d, q4 = d / 4;
+      const int n_items = (L2 - p0) * lv.Hkv * 2 * q4;  // (pos, head, which, quad)
+      for (int it = blockIdx.y * blockDim.x + threadIdx.x; it < n_items; it += gridDim.y * blockDim.x) {
+        const int quad = it % q4;
+        int rest = it / q4;
+        const int which = rest % 2;
+        rest /= 2;
+        const int hh = rest % lv.Hkv;
+        const int pos = p0 + rest / lv.Hkv;
+        const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + hh) * d + 4 * quad;
+        uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + hh) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
+        const void* base = which ? a.v : a.k;
+        uint2 out;
+        if (a.dt == 0) {
+          out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
+        } else {
+          const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
+          out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
+          out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
+        }
+        *reinterpret_cast<uint2*>(dst) = out;
+      }
     }
-    __syncthreads();
-    pdl_launch();
-    return;
-  }
-  const int nn = a.n_new[b];
-  const int L2 = L + nn;
-  if (nn < 0 || nn > a.max_new || L2 > lv.max_ctx) return;
-  const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
-  const int p0 = max(L, Np2);
-  const int d = lv.d, q4 = d / 4;
-  const int n_items = (L2 - p0) * lv.Hkv * 2 * q4;  // (pos, head, which, quad)
-  for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
-    const int quad = it % q4;
-    int rest = it / q4;
-    const int which = rest % 2;
-    rest /= 2;
-    const int hh = rest % lv.Hkv;
-    const int pos = p0 + rest / lv.Hkv;
-    const size_t src = (((size_t)b * a.max_new + (pos - L)) * lv.Hkv + hh) * d + 4 * quad;
-    uint16_t* dst = lv.ring + ((((size_t)slot * lv.Hkv + hh) * 2 + which) * kPage + (pos - Np2)) * d + 4 * quad;
-    const void* base = which ? a.v : a.k;
-    uint2 out;
-    if (a.dt == 0) {
-      out = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + src);
-    } else {
-      const float4 f = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + src);
-      out.x = (uint32_t)f32_to_bf16_rn(f.x) | ((uint32_t)f32_to_bf16_rn(f.y) << 16);
-      out.y = (uint32_t)f32_to_bf16_rn(f.z) | ((uint32_t)f32_to_bf16_rn(f.w) << 16);
-    }
-    *reinterpret_cast<uint2*>(dst) = out;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    lv.state[2 * slot] = L2;
-    lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
+  pdl_launch();
+}
+
+// Sequence state after an append (a.flush = 0, after k_ring_rows) or a ring flush (a.flush = 1).
+// Dependents (the decode of this layer) are released only after the state is written: they read the
+// sequence state before their own griddepcontrol.wait to start fetching pages early.
+__global__ void __launch_bounds__(32) k_ring_update(AppendArgs a) {
+  const int b = blockIdx.x;
+  pdl_wait();  // the ring rows are written and the quantise launch has read the old state
+  const LayerView& lv = a.lv;
+  const int slot = a.seq_ids[b];
+  if (threadIdx.x == 0 && slot >= 0 && slot < lv.max_seqs) {
+    const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
+    const int Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+    if (a.flush) {
+      lv.state[2 * slot + 1] = L - Np;
+    } else {
+      const int nn = a.n_new[b];
+      const int L2 = L + nn;
+      if (nn >= 0 && nn <= a.max_new && L2 <= lv.max_ctx) {
+        const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
+        lv.state[2 * slot] = L2;
+        lv.state[2 * slot + 1] = Np2 > Np ? 0 : F;
+      }
+    }
     __threadfence();
   }
-  __syncthreads();
+  __syncwarp();
   pdl_launch();
 }
 
@@ -1264,7 +1303,10 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
                       : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(k_ring_update, dim3(batch), dim3(256), 0, s, a);
+  // ring rows: up to 128 tokens x Hkv x (K, V) x d / 4 items per row, about 4 items per thread
+  const int row_items = kPage * a.lv.Hkv * 2 * (a.lv.d / 4);
+  e = launch_pdl(k_ring_rows, dim3(batch, (row_items + 1023) / 1024), dim3(256), 0, s, a);
+  if (e == cudaSuccess) e = launch_pdl(k_ring_update, dim3(batch), dim3(32), 0, s, a);
   if (e != cudaSuccess || !a.full) return e;
   return launch_flush(ctx, layer, seq_ids, batch, s);  // full_tq: the partial page too
 }
