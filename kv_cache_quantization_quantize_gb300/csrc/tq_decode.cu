@@ -672,16 +672,20 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   const int nsp = a.plan.n_splits;
   float* part = reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                          (((size_t)b * lv.Hkv + h) * (nsp + 1) + sp) * a.plan.part_stride);
-  pdl_launch();
+  // Every kernel of this library starts its dependents only after its own stream wait, so what this
+  // kernel reads before its wait (q, seq_ids, the tables, the packed pages and count) was complete
+  // before the previous kernel's dependents started.
   const int slot = row_slot(a, b);
   if (slot < 0 || slot >= lv.max_seqs) {
     pdl_wait();
+    pdl_launch();
     write_empty_partial(part, D, tid, NT);
     finish_unit<D, NT>(a, b, h, smem);
     return;
   }
   if (sp == nsp) {
     pdl_wait();
+    pdl_launch();
     ring_split<D, NT>(a, b, h, slot, part, smem);
     finish_unit<D, NT>(a, b, h, smem);
     return;
@@ -695,6 +699,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   const int pg0 = sp * pps, pg1 = min(n_pages, pg0 + pps);
   if (pg0 >= pg1) {
     pdl_wait();
+    pdl_launch();
     write_empty_partial(part, D, tid, NT);
     finish_unit<D, NT>(a, b, h, smem);
     return;
@@ -730,10 +735,11 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   }
   SFrag<D> sfrag;
   sfrag_prefetch<D>(lv, sfrag);
-  pdl_wait();  // earlier work on the stream (q, and the partials of any decode that shares ws) is done
   float um[2], cm[2], uq[2], cq[2];
   float* ps = xbuf + decode_xbuf_floats<D>();
-  query_prep<D, NT, KB>(a, b, h, ps, sfrag, um, cm, uq, cq);
+  query_prep<D, NT, KB>(a, b, h, ps, sfrag, um, cm, uq, cq);  // shared memory only
+  pdl_wait();  // the partials and counters of any decode that shares ws are no longer in use
+  pdl_launch();
   // f16 B fragments of the key MMAs for this warp's coordinate half, [plane][k-step][lane] in shared
   // memory (written by query_prep; read once per page and k-step, shared by both tiles)
   const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * NBP * KS * 32 + lane;

@@ -575,8 +575,10 @@ __device__ __forceinline__ void write_ring_rows(const AppendArgs& a, int b, int 
 // Appends of fewer than 128 tokens per row in one launch. CTA (row b, KV head h, block q) codes
 // 32-token block q of the page that a ring overflow completes (if any). The last of the row's
 // 4 Hkv CTAs to arrive writes the new ring rows of every head (all CTAs have read the old ones by
-// then) and publishes the new length; without an overflow CTA (b, 0, 0) does that alone. Dependents (the decode) are released only after that, so they
-// may read the state before their own stream wait.
+// then) and publishes the new length; without an overflow CTA (b, 0, 0) does that alone. When a page
+// is coded (or in full_tq mode), dependents (the decode) are released only after that, so they may
+// read the state before their own stream wait; without one they are released at once, since the
+// packed count they read then is the same before and after this append.
 template <int D, int KB>
 __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -601,7 +603,10 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
   const int Np2 = L2 > 0 ? kPage * ((L2 - 1) / kPage) : 0;
   if (!a.full && Np2 == Np) {
     // no page to code (the common decode step): nothing reads the old ring rows, so CTA (b, 0, 0)
-    // writes every head's new rows and the length on its own and the others leave at once
+    // writes every head's new rows and the length on its own and the others leave at once.
+    // Dependents are released first: the packed count (what a decode split reads before its own
+    // stream wait) does not change here, and a decode's ring split waits for this grid to finish.
+    pdl_launch();
     if (h == 0 && q32 == 0) {
       write_ring_rows(a, b, slot, L, Np2, L, L2);
       __syncthreads();
@@ -611,7 +616,6 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
       }
       __syncthreads();
     }
-    pdl_launch();
     return;
   }
   if (a.full) {
