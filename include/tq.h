@@ -19,6 +19,12 @@
  *     device memory; it allocates only its small host-side context.
  *   - Work is enqueued asynchronously on the caller's CUDA stream `stream`. Calls on one layer must
  *     be ordered by the caller (same stream, or events).
+ *   - Kernels are launched with programmatic dependent launch: a kernel may start, and read its
+ *     inputs (q, k, v, seq_ids, n_new, the tables, the packed pages), as soon as the previous kernel
+ *     on the stream releases its dependents. Every kernel of this library does that only after it
+ *     has itself waited for its own predecessor. A caller kernel that releases dependents early
+ *     (griddepcontrol.launch_dependents) must have finished writing those inputs first; kernels that
+ *     do not use that instruction, and copies, need no care.
  *   - Every argument is validated on the host before any launch. A bad argument returns
  *     TQ_ERR_INVALID_ARG and an unsupported shape returns TQ_ERR_UNSUPPORTED; nothing is launched
  *     in either case. A launch failure returns TQ_ERR_CUDA. tq_last_error() gives the reason
