@@ -38,8 +38,24 @@ if ROOT not in sys.path:
 
 METRIC = "decode attn context-tok/s & packed-KV HBM GB/s (% of 8 TB/s); quantize tok/s"
 UNIT = "context-tok/s"
-WL = dict(name="llama3.1-8b-shaped decode, batch 1, context 32768, K3/V2",
-          layers=32, hq=32, hkv=8, d=128, batch=1, ctx=32768, vb=2, kb=3, outliers=("random", 4, 10.0))
+# Decode workloads (--workload). `ctx` is the context of every row at the first timed step; `lens`
+# draws ragged per-row contexts uniform in [lo, hi] instead; inputs are seeded per layer with
+# seed * 1000 + layer.
+WORKLOADS = {
+    "llama8b": dict(name="llama3.1-8b-shaped decode, batch 1, context 32768, K3/V2", layers=32, hq=32, hkv=8,
+                    d=128, batch=1, ctx=32768, lens=None, vb=2, kb=3, outliers=("random", 4, 10.0), dist="normal",
+                    seed=1),
+    "batched": dict(name="llama3.1-8b-shaped batched decode, batch 16, ragged context U[4096, 8192], K3/V4",
+                    layers=32, hq=32, hkv=8, d=128, batch=16, ctx=8192, lens=(4096, 8192), vb=4, kb=3,
+                    outliers=None, dist="normal", seed=2),
+    "d256": dict(name="head_dim 256 decode, 16 layers, batch 4, context 16384, Student-t nu=5, K3/V2", layers=16,
+                 hq=32, hkv=8, d=256, batch=4, ctx=16384, lens=None, vb=2, kb=3, outliers=None, dist="student_t5",
+                 seed=3),
+    "long": dict(name="long-context decode, batch 32, context 131072, K3/V2 (about 99 GB of packed cache)", layers=32,
+                 hq=32, hkv=8, d=128, batch=32, ctx=131072, lens=None, vb=2, kb=3, outliers=("random", 4, 10.0),
+                 dist="normal", seed=4),
+}
+WL = dict(WORKLOADS["llama8b"])
 PREFILL = dict(tokens=65536, hkv=8, layers=32, d=128, vb=2, kb=3, seed=4)
 NOMINAL_HBM_GBS = 8000.0
 
@@ -130,12 +146,14 @@ def aggregate_over_ranks(ms, units, world, device):
     return t_max, units * world / (t_max * 1e-3)
 
 
-def bench_config(world, mode="hybrid"):
+def bench_config(world, mode="hybrid", step_mb=785):
     cfg = {"workload": WL["name"], "layers": WL["layers"], "q_heads": WL["hq"], "kv_heads": WL["hkv"],
            "head_dim": WL["d"], "batch_per_gpu": WL["batch"], "context": WL["ctx"], "key_bits": WL["kb"], "value_bits": WL["vb"],
-           "ring": 128, "l2": "inputs larger than L2 (~785 MB of packed records per step vs 129 MB L2)",
+           "ring": 128, "l2": f"inputs larger than L2 (~{step_mb:.0f} MB of packed records per step vs 129 MB L2)",
            "parallelism": "replicas" if world > 1 else "single GPU",
-           "step": "append 1 token + hybrid decode attention, all 32 layers, one CUDA graph replay"}
+           "step": f"append 1 token + hybrid decode attention, all {WL['layers']} layers, one CUDA graph replay"}
+    if WL["lens"] is not None:
+        cfg.update(context=f"ragged, uniform in [{WL['lens'][0]}, {WL['lens'][1]}] (seed {WL['seed']})")
     if mode == "full_tq":
         cfg.update(workload=WL["name"] + ", full_tq mode", ring=0, mode="full_tq",
                    step="append 1 token (quantised at once) + decode over packed tokens only, all 32 layers, "
@@ -199,7 +217,10 @@ def run_ours(args):
     L_layers, Hq, Hkv, d, B, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["batch"], WL["ctx"], WL["vb"]
     n_e2e_warm = 2
     extra = 1 + W + K + (n_e2e_warm + K) + K + 8  # tokens appended after prefill by all passes
-    max_ctx = ctx + extra
+    # context of each row at the first timed step
+    lens = (synth.ragged_lengths(B, WL["lens"][0], WL["lens"][1], seed=WL["seed"]) if WL["lens"] is not None
+            else [ctx] * B)
+    max_ctx = max(lens) + extra
     full = args.mode == "full_tq"
     paged = args.layout == "paged"
     max_pages = (max_ctx + 127) // 128
@@ -211,11 +232,13 @@ def run_ours(args):
     if paged:  # every page of every row mapped to a block of a seeded permutation of the pool
         perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
         cache.block_table.copy_(perm.view(B, max_pages).to(dev))
-    L0 = ctx - W - 2  # after the eager step and the W warm-up replays the first timed step attends ctx tokens
-    n0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
+    # after the eager step and the W warm-up replays, the first timed step of row b attends lens[b] tokens
+    L0 = [n - W - 2 for n in lens]
     for l in range(L_layers):
-        k, v = synth.kv_tokens(L0, Hkv, d, seed=1000 + l, outliers=WL["outliers"], device=dev)
-        cache.append(l, k[None].expand(B, -1, -1, -1).contiguous(), v[None].expand(B, -1, -1, -1).contiguous(), ids, n0)
+        k, v = synth.kv_tokens(max(L0), Hkv, d, seed=WL["seed"] * 1000 + l, dist=WL["dist"], outliers=WL["outliers"],
+                               device=dev)
+        for b in range(B):  # one row per call: rows share the layer's tokens, each with its own length
+            cache.append(l, k[None], v[None], ids[b:b + 1], torch.full((1,), L0[b], dtype=torch.int32, device=dev))
         del k, v
     torch.cuda.synchronize()
     if cache.check_status():
@@ -257,7 +280,7 @@ def run_ours(args):
     for _ in range(W):
         g.replay()
     torch.cuda.synchronize()
-    L_first = cache.state(0, 0)[0] + 1
+    L_first = [cache.state(0, b)[0] + 1 for b in range(B)]
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -276,17 +299,19 @@ def run_ours(args):
     sampler.stop()
     clocks = sampler.summary(t_host0, t_host1)
     status = cache.check_status()
-    ctx_tokens = sum(B * (L_first + i) for i in range(K))  # each step attends its full context
+    ctx_tokens = sum(Lb + i for Lb in L_first for i in range(K))  # each step attends every row's full context
     # max over ranks of the timed region; whole-job throughput
     t_max, value = aggregate_over_ranks(ms, ctx_tokens, world, dev)
     ms_per_step = t_max / K
 
     # algorithmic bytes per step: packed K3/V2 records + ring (K,V bf16) + q + out, all layers
     rec = (d * (WL["kb"] - 1) // 8 + d // 8 + 4) + (d * vb // 8 + d // 16)
-    Lmid = L_first + (K - 1) / 2.0
-    packed = Lmid if full else 128 * ((Lmid - 1) // 128)
-    ring = Lmid - packed
-    step_bytes = L_layers * B * (Hkv * (packed * rec + ring * d * 2 * 2) + Hq * d * (2 + 4))
+    step_bytes = 0.0
+    for Lb in L_first:
+        Lmid = Lb + (K - 1) / 2.0
+        packed = Lmid if full else 128 * ((Lmid - 1) // 128)
+        ring = Lmid - packed
+        step_bytes += L_layers * (Hkv * (packed * rec + ring * d * 2 * 2) + Hq * d * (2 + 4))
     hbm_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = measured_peaks()
 
@@ -301,9 +326,12 @@ def run_ours(args):
     for _ in range(3):
         g2.replay()
     torch.cuda.synchronize()
-    Lk, Fk = cache.state(0, 0)
-    packed_k = 128 * ((Lk - 1) // 128) + Fk
-    ring_k = Lk - packed_k
+    kern_bytes = 0
+    for b in range(B):
+        Lk, Fk = cache.state(0, b)
+        packed_k = 128 * ((Lk - 1) // 128) + Fk
+        ring_k = Lk - packed_k
+        kern_bytes += Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     reps = max(K, 10)
     e0.record()
@@ -312,10 +340,9 @@ def run_ours(args):
     e1.record()
     torch.cuda.synchronize()
     kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
-    kern_bytes = B * (Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4))
     kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
     # the committed ncu summary is of the default (hybrid, contiguous, head_dim 128) step
-    traffic = None if full or paged or d != 128 or WL["kb"] != 3 else profiled_traffic()
+    traffic = None if full or paged or WL["name"] != WORKLOADS["llama8b"]["name"] else profiled_traffic()
 
     # ---- end to end through the public API with pinned host buffers ----
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
@@ -339,7 +366,7 @@ def run_ours(args):
     for _ in range(n_e2e_warm):
         e2e_step()
     torch.cuda.synchronize()
-    L_e2e = cache.state(0, 0)[0] + 1
+    L_e2e = [cache.state(0, b)[0] + 1 for b in range(B)]
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(s)
     for _ in range(K):
@@ -347,7 +374,7 @@ def run_ours(args):
     f1.record(s)
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1)
-    e2e_value = sum(B * (L_e2e + i) for i in range(K)) * world / (e2e_ms * 1e-3)
+    e2e_value = sum(Lb + i for Lb in L_e2e for i in range(K)) * world / (e2e_ms * 1e-3)
     if cache.check_status():
         status |= 1 << 16
 
@@ -361,7 +388,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
-        "config": dict(bench_config(world, args.mode), **({"layout": "paged (scrambled block table)"} if paged else {})),
+        "config": dict(bench_config(world, args.mode, step_bytes / 1e6),
+                       **({"layout": "paged (scrambled block table)"} if paged else {})),
         "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
         "pct_of_measured_hbm": 100.0 * hbm_gbs / peak,
         "roofline": {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
@@ -377,8 +405,8 @@ def run_ours(args):
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
-    if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged and d == 128
-            and WL["kb"] == 3):  # oracle sample
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged
+            and WL["name"] == WORKLOADS["llama8b"]["name"]):  # oracle sample
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -666,6 +694,10 @@ def main():
                    help="full_tq: no exact recent buffer, every token quantised on append")
     p.add_argument("--prefill-chunk", type=int, default=0, metavar="TQ",
                    help="time prefill attention of a TQ-token chunk instead (one JSON line of its own)")
+    p.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS),
+                   help="decode workload of the step: llama8b (batch 1, 32K), batched (batch 16, ragged 4K-8K, V4), "
+                        "d256 (head_dim 256, batch 4, 16K), long (batch 32, 128K)")
+    p.add_argument("--value-bits", type=int, default=0, choices=[0, 2, 4], help="override the workload's value bits")
     p.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
                    help="the same decode and prefill shapes with another head_dim (synthetic variants)")
     p.add_argument("--key-bits", type=int, default=3, choices=[3, 4],
@@ -680,6 +712,11 @@ def main():
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
                    help="only run one layer of the prefill quantisation PASSES times (for profilers)")
     args = p.parse_args()
+    if args.workload != "llama8b":
+        WL.update(WORKLOADS[args.workload])
+        args.skip_quantize = True  # the prefill quantise line belongs to the default run
+    if args.value_bits:
+        WL.update(vb=args.value_bits, name=WL["name"].replace(f"/V{WL['vb']}", f"/V{args.value_bits}"))
     if args.head_dim != 128:
         WL.update(d=args.head_dim, name=f"llama3.1-8b-shaped decode with head_dim {args.head_dim}, batch 1, "
                                         f"context 32768, K3/V2")

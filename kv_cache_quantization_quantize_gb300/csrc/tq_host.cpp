@@ -282,13 +282,33 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
   const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
   const int per_sm = ctx->host_only ? 2 : decode_resident_ctas(ctx);
   const int target = per_sm * sms;  // split-K CTAs that fit in one wave
-  // Small batches: one wave of (splits + ring) CTAs per (row, KV head). Large batches: about six
-  // waves, so that the tail of the last wave is short.
-  int splits = units * 2 <= target ? std::max(1, target / units - 1) : std::max(2, (6 * target + units - 1) / units);
-  splits = std::min(splits, max_pages);
-  splits = std::min(splits, 1024);  // the combine keeps 4 weights per split in shared memory
+  // Splits per (row, KV head): the fewest whose estimated time is within 3 % of the least, with every
+  // row taken at the hint's length. Time = waves x (page rounds of a split + the fixed cost of a split
+  // CTA: query prep, merge of its streams, arrival). A split CTA runs 3 page streams at head_dim <= 128
+  // and one at 256; its fixed cost is about 2.5 page rounds (batch-1 trace: 2.5 us query prep and
+  // 2.7 us merge and arrival against 2.1 us per page round). The ring CTA of a (row, KV head) is short:
+  // it counts as that fixed cost's share of a wave slot.
+  const int ns = c.head_dim <= 128 ? 3 : 1;
+  const double fixed_rounds = 2.5;
+  const int max_splits = std::min(max_pages, 1024);  // the combine keeps 4 weights per split in shared memory
+  auto cost_of = [&](int pps) {
+    const int n = (max_pages + pps - 1) / pps;
+    const double rounds = (double)((pps + ns - 1) / ns);
+    const double slots = (double)units * (n + fixed_rounds / (rounds + fixed_rounds));
+    return std::ceil(slots / target - 1e-9) * (rounds + fixed_rounds);
+  };
+  double best_cost = cost_of(max_pages);
+  for (int s = 2; s <= max_splits; ++s) best_cost = std::min(best_cost, cost_of((max_pages + s - 1) / s));
+  int best_pps = max_pages;
+  for (int s = 1; s <= max_splits; ++s) {
+    const int pps = (max_pages + s - 1) / s;
+    if (cost_of(pps) <= 1.03 * best_cost) {
+      best_pps = pps;
+      break;
+    }
+  }
   DecodePlan p;
-  p.pages_per_split = (max_pages + splits - 1) / splits;
+  p.pages_per_split = best_pps;
   p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
   const int d = c.head_dim;
   // The arrival counters sit at a fixed place (offset 0, sized for max_seqs rows), so that calls with
