@@ -625,21 +625,33 @@ def oracle_unit_step(st):
     return oracle.decode_attention(st["q"], st["keys"], st["vals"], st["rk"], st["rv"], st["D"], st["S"], st["c"])
 
 
-def cpu_baseline(args):
-    """Times the oracle in a child process so that its thread count is known."""
-    cores = os.cpu_count() or 1
+def _oracle_child(threads):
+    """Runs the oracle sample in a child process limited to `threads` BLAS/OpenMP threads."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[var] = str(cores)
+        env[var] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "150"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def cpu_baseline(args):
+    """Times the oracle in child processes so that their thread counts are known: all host cores (the
+    reported value) and one thread."""
+    cores = os.cpu_count() or 1
     try:
-        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "150"], env=env,
-                           capture_output=True, text=True, timeout=600)
-        res = json.loads(r.stdout.strip().splitlines()[-1])
+        res = _oracle_child(cores)
     except Exception as e:  # report, do not fail the GPU line
         return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": f"failed: {e}"}
-    return {"value": res["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
+    line = {"value": res["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": res["sample"], "seconds": res["seconds"]}
+    try:
+        one = _oracle_child(1)
+        line["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1, "seconds": one["seconds"]}
+    except Exception as e:
+        line["single_thread"] = {"value": None, "note": f"failed: {e}"}
+    return line
 
 
 def oracle_sample_main(reps):
