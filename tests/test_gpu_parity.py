@@ -85,6 +85,62 @@ def test_ragged_batch_appends_and_decode(d, vb, G, kbits):
     assert torch.all(out0 == 0)
 
 
+@pytest.mark.parametrize("d,vb", [(128, 2), (64, 4), (256, 2)])
+def test_append_then_decode_back_to_back(d, vb):
+    """The decode step as a server issues it: on every layer a one-token append is followed at once by
+    the decode, with no synchronisation in between, while different rows cross a 128-token page
+    boundary (a page is coded) on different steps. Every decode output is checked against the oracle
+    on the cache as that decode saw it."""
+    Hkv, G, n_layers, steps = 2, 4, 3, 4
+    lens = [126, 127, 128, 255, 256, 383]
+    B = len(lens)
+    cfg = config(head_dim=d, value_bits=vb, n_layers=n_layers, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B,
+                 max_ctx=400, seed=21)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    slots = list(range(B))
+    max_new = max(lens)
+    seqs = {}
+    for layer in range(n_layers):
+        kb = torch.zeros(B, max_new, Hkv, d, dtype=torch.bfloat16)
+        vbuf = torch.zeros_like(kb)
+        for i, L in enumerate(lens):
+            k, v = synth.kv_tokens(L + steps, Hkv, d, seed=300 + 10 * layer + i)
+            seqs[layer, i] = (k, v)
+            kb[i, :L], vbuf[i, :L] = k[:L], v[:L]
+        cache.append(layer, kb.to(DEV), vbuf.to(DEV), _i32(slots), _i32(lens))
+    ones, ids = _i32([1] * B), _i32(slots)
+    ws = cache.workspace(B)
+    outs = torch.empty((n_layers, B, Hkv * G, d), dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    worst = 0.0
+    for s in range(steps):
+        qs = [synth.queries(B, Hkv * G, d, seed=40 + 7 * s + layer) for layer in range(n_layers)]
+        # every input of the step is on the device first, so that nothing but the library's own
+        # kernels runs between an append and its decode
+        kds = [torch.stack([seqs[layer, i][0][L + s] for i, L in enumerate(lens)])[:, None].contiguous().to(DEV)
+               for layer in range(n_layers)]
+        vds = [torch.stack([seqs[layer, i][1][L + s] for i, L in enumerate(lens)])[:, None].contiguous().to(DEV)
+               for layer in range(n_layers)]
+        qd = [q.to(DEV) for q in qs]
+        torch.cuda.synchronize()
+        for layer in range(n_layers):
+            cache.append(layer, kds[layer], vds[layer], ids, ones)
+            cache.decode(layer, qd[layer], ids, out=outs[layer], workspace=ws)
+        torch.cuda.synchronize()
+        assert cache.check_status() == 0
+        for layer in range(n_layers):
+            out = outs[layer].cpu().numpy()
+            for i in range(B):
+                assert cache.state(layer, i)[0] == lens[i] + s + 1
+                ref = _oracle_decode(cache, layer, i, qs[layer][i], tables)
+                for hq in range(Hkv * G):
+                    err = rel_l2(out[i, hq], ref[hq])
+                    worst = max(worst, err)
+                    assert err <= 2e-3, (s, layer, i, hq, err)
+    print(f"back-to-back append + decode d={d} V{vb}: worst rel-L2 {worst:.2e}")
+
+
 def test_ring_flush_then_decode_and_overflow():
     d, vb, G, Hkv = 128, 2, 4, 2
     cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
