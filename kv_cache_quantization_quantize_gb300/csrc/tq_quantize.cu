@@ -145,30 +145,31 @@ __device__ __forceinline__ void load_token(const AppendArgs& a, int which, int s
   }
 }
 
-// Shared-memory arrays of the CUDA-core quantiser: per-token key codes (idx | sign << (kb - 1)), value codes,
-// {n, gamma} and value scales of a page, and the f16 hi / lo split of the residuals of one 32-token
-// block (rows padded by 8 halves: conflict-free B-fragment reads).
+// Shared-memory arrays of the CUDA-core quantiser for one 32-token block (a CTA codes one block at a
+// time; row i is the block's token i): key codes (idx | sign << (kb - 1)), value codes, {n, gamma},
+// value scales, and the f16 hi / lo split of the residuals (rows padded by 8 halves: conflict-free
+// B-fragment reads).
 template <int D>
 constexpr int kRStride = D + 8;
 template <int D>
 struct QSmem {
-  uint8_t* kcode;    // [128][D]
-  uint8_t* vcode;    // [128][D]
-  uint32_t* norms;   // [128] n16 | gamma16 << 16
-  uint16_t* scales;  // [128][D/32]
+  uint8_t* kcode;    // [32][D]
+  uint8_t* vcode;    // [32][D]
+  uint32_t* norms;   // [32] n16 | gamma16 << 16
+  uint16_t* scales;  // [32][D/32]
   __half* rh;        // [32][kRStride] residual * 2^8, f16
   __half* rl;        // [32][kRStride] residual * 2^8 - rh, f16
   __device__ explicit QSmem(uint8_t* smem)
       : kcode(smem),
-        vcode(kcode + kPage * D),
-        norms(reinterpret_cast<uint32_t*>(vcode + kPage * D)),
-        scales(reinterpret_cast<uint16_t*>(norms + kPage)),
-        rh(reinterpret_cast<__half*>(scales + kPage * (D / 32))),
+        vcode(kcode + 32 * D),
+        norms(reinterpret_cast<uint32_t*>(vcode + 32 * D)),
+        scales(reinterpret_cast<uint16_t*>(norms + 32)),
+        rh(reinterpret_cast<__half*>(scales + 32 * (D / 32))),
         rl(rh + 32 * kRStride<D>) {}
 };
 template <int D>
 constexpr size_t quantize_smem_bytes_d() {
-  return 2 * kPage * D + 4 * kPage + 2 * kPage * (D / 32) + 2 * 2 * 32 * kRStride<D>;
+  return 2 * 32 * D + 4 * 32 + 2 * 32 * (D / 32) + 2 * 2 * 32 * kRStride<D>;
 }
 
 // D += A B, m16n8k16, f16 operands, f32 accumulate.
@@ -229,7 +230,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
     warp_fwht<NE>(y, lane);
     const float scale = n > 0.f ? 1.0f / (n * sqrtf((float)D)) : 0.f;
     float rr = 0.f;
-    uint8_t* kc = kcode + t * D;
+    uint8_t* kc = kcode + (t - tb) * D;
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       const float yy = y[e] * scale;
@@ -262,7 +263,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
     const float gamma = sqrtf(rr);
     if (lane == 0) {
       const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(gamma);
-      norms[t] = (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+      norms[t - tb] = (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
     }
     // ---- value: v' = Pi v, symmetric mid-rise groups of 32, fp16 scale ----
     if (t < valid) {
@@ -274,7 +275,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
       for (int e = 0; e < NE; ++e) x[e] = 0.f;
     }
     warp_fwht<NE>(x, lane);
-    uint8_t* vc = vcode + t * D;
+    uint8_t* vc = vcode + (t - tb) * D;
     if (D == 64) {  // a group of 32 coordinates is 16 lanes x 2
       float am = 0.f;
 #pragma unroll
@@ -296,7 +297,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
         }
         vc[lane_coord<D>(e, lane)] = (uint8_t)code;
       }
-      if ((lane & 15) == 0) scales[t * (D / 32) + (lane >> 4)] = __half_as_ushort(sh);
+      if ((lane & 15) == 0) scales[(t - tb) * (D / 32) + (lane >> 4)] = __half_as_ushort(sh);
     }
 #pragma unroll
     for (int hh = 0; hh < (D == 64 ? 0 : NE / 4); ++hh) {
@@ -321,7 +322,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
         }
         vc[128 * hh + 4 * lane + e] = (uint8_t)code;
       }
-      if ((lane & 7) == 0) scales[t * (D / 32) + 4 * hh + (lane >> 3)] = __half_as_ushort(sh);
+      if ((lane & 7) == 0) scales[(t - tb) * (D / 32) + 4 * hh + (lane >> 3)] = __half_as_ushort(sh);
     }
   }
   __syncthreads();
@@ -351,7 +352,7 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
         for (int i = 0; i < 4; ++i) {
           const int t = tb + 8 * (nt0 + n) + 2 * c + (i & 1), row = 16 * mt + g + 8 * (i >> 1);
           if (t >= t_begin && t < t_end)
-            kcode[t * D + row] = (uint8_t)(kcode[t * D + row] | ((z[n][i] >= 0.f) << (KB - 1)));
+            kcode[(t - tb) * D + row] = (uint8_t)(kcode[(t - tb) * D + row] | ((z[n][i] >= 0.f) << (KB - 1)));
         }
     }
   }
@@ -392,7 +393,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
       uint32_t word = 0;
 #pragma unroll
       for (int kap = 0; kap < 2; ++kap)
-        word |= kbits_field(kcode + (32 * q32 + 16 * kap + (ln >> 2) + 8 * r) * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
+        word |= kbits_field(kcode + (16 * kap + (ln >> 2) + 8 * r) * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
       kw[w] = word;
     }
   }
@@ -400,10 +401,10 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
     const int r = w & 1, ln = (w >> 1) & 31, hf = (w >> 6) % HALVES, pi = (w / (64 * HALVES)) % KB;
     const int tile = w / (WT * HALVES);
     const int t = 16 * tile + (ln >> 2) + 8 * r, c = ln & 3;
-    kw[w] = kbits_field(kcode + t * D + 128 * hf + 2 * c, pi, KB, 8, 0);
+    kw[w] = kbits_field(kcode + (t - t0) * D + 128 * hf + 2 * c, pi, KB, 8, 0);
   }
   uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
-  for (int t = t0 + tid; t < t1; t += kQThreads) nw[t] = norms[t];
+  for (int t = t0 + tid; t < t1; t += kQThreads) nw[t] = norms[t - t0];
   uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
   if (vb == 2) {
     for (int w = q32 * (D / 16) * 32 + tid; w < (q32 + 1) * (D / 16) * 32; w += kQThreads) {
@@ -418,7 +419,7 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
           for (int e = 0; e < 2; ++e) {
             const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
             const int j = 16 * mt + 8 * (rg & 1) + g;
-            word |= (uint32_t)vcode[t * D + j] << (16 * e + 2 * vfield2(kap, rg));
+            word |= (uint32_t)vcode[(t - t0) * D + j] << (16 * e + 2 * vfield2(kap, rg));
           }
       vw[w] = word;
     }
@@ -433,14 +434,14 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
         for (int e = 0; e < 2; ++e) {
           const int t = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
           const int j = 16 * mt + 8 * (rg & 1) + g;
-          word |= (uint32_t)vcode[t * D + j] << (16 * e + 4 * vfield4(rg));
+          word |= (uint32_t)vcode[(t - t0) * D + j] << (16 * e + 4 * vfield4(rg));
         }
       vw[w] = word;
     }
   }
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
   for (int i = t0 * (D / 32) + tid; i < t1 * (D / 32); i += kQThreads)
-    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i];
+    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i - t0 * (D / 32)];
 }
 
 // full_tq appends: codes tokens [t_lo, t_hi) of page pg (page-relative, one 32-token block at most)
@@ -456,6 +457,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
   const int tid = threadIdx.x;
   const LayerView& lv = a.lv;
   const int vb = lv.vb, ntok = t_hi - t_lo;
+  const int tb = t_lo & ~31;  // the block's first token (row 0 of the shared-memory arrays)
   uint8_t* page = page_addr(lv, slot, h, pg);
   if (!page) {  // paged cache without a block for this page: nothing is written
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
@@ -473,7 +475,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
         const int t = 32 * grp + 16 * kap + (ln >> 2) + 8 * r;
         if (t >= t_lo && t < t_hi) {
           mask |= 0x00FF00FFu << (8 * kap);
-          bits |= kbits_field(sm.kcode + t * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
+          bits |= kbits_field(sm.kcode + (t - tb) * D + 2 * (ln & 3), pi, KB, 4, 8 * kap);
         }
       }
       if (mask) kw[w] = (kw[w] & ~mask) | bits;
@@ -483,10 +485,10 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
     const int c = i & 3, hf = (i >> 2) % HALVES, pi = (i / (4 * HALVES)) % KB, t = t_lo + i / (4 * KB * HALVES);
     const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
     kw[((((tile * KB + pi) * HALVES + hf) * 32) + 4 * g + c) * 2 + r] =
-        kbits_field(sm.kcode + t * D + 128 * hf + 2 * c, pi, KB, 8, 0);
+        kbits_field(sm.kcode + (t - tb) * D + 128 * hf + 2 * c, pi, KB, 8, 0);
   }
   uint32_t* nw = reinterpret_cast<uint32_t*>(page + pl.norms_off);
-  for (int t = t_lo + tid; t < t_hi; t += kQThreads) nw[t] = sm.norms[t];
+  for (int t = t_lo + tid; t < t_hi; t += kQThreads) nw[t] = sm.norms[t - tb];
   uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
   const int blk = t_lo >> 5;
   if (vb == 2) {
@@ -504,7 +506,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
             if (t >= t_lo && t < t_hi) {
               const int sh = 16 * e + 2 * vfield2(kap, rg);
               mask |= 3u << sh;
-              bits |= (uint32_t)sm.vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << sh;
+              bits |= (uint32_t)sm.vcode[(t - tb) * D + 16 * mt + 8 * (rg & 1) + g] << sh;
             }
           }
       if (mask) vw[w] = (vw[w] & ~mask) | bits;
@@ -522,7 +524,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
           if (t >= t_lo && t < t_hi) {
             const int sh = 16 * e + 4 * vfield4(rg);
             mask |= 15u << sh;
-            bits |= (uint32_t)sm.vcode[t * D + 16 * mt + 8 * (rg & 1) + g] << sh;
+            bits |= (uint32_t)sm.vcode[(t - tb) * D + 16 * mt + 8 * (rg & 1) + g] << sh;
           }
         }
       if (mask) vw[w] = (vw[w] & ~mask) | bits;
@@ -530,7 +532,7 @@ __device__ __forceinline__ void quantize_new_tokens(const AppendArgs& a, int b, 
   }
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
   for (int i = t_lo * (D / 32) + tid; i < t_hi * (D / 32); i += kQThreads)
-    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = sm.scales[i];
+    sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = sm.scales[i - tb * (D / 32)];
 }
 
 template <int D, int KB>
