@@ -183,13 +183,20 @@ __host__ __device__ constexpr int key_bplanes(int kb, int d) { return kb == 3 ? 
 __host__ __device__ constexpr int key_qjl_plane(int kb) { return kb == 3 ? 2 : 4; }
 __host__ __device__ constexpr int key_rem_plane(int kb, int d) { return kb == 3 ? (d == 64 ? 3 : -1) : 5; }
 
-// Bytes of a split CTA's query-prep scratch: q_rot and q_proj as fp32 [4][D], 16 floats of scales.
-template <int D, int KB>
+// Query columns of a split CTA: the 8 B columns of the MMAs carry the kMaxG heads of QP query rows
+// (QP = 1 for decode; 2 for prefill, whose chunk queries of one sequence share the key operands).
+template <int QP>
+__host__ __device__ constexpr int qcols() {
+  return kMaxG * QP;
+}
+
+// Bytes of a split CTA's query-prep scratch.
+template <int D, int KB, int QP = 1>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
-  // q_rot, q_proj [4][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes] uint2;
-  // per-warp offset sums [warps][8]
-  return sizeof(float) * (2 * kMaxG * D + 32) + 8 * 32 * (key_bplanes(KB, D) * D / 16) +
-         sizeof(float) * 8 * (decode_threads<D>() / 32);
+  // q_rot, q_proj [columns][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes]
+  // uint2; per-warp offset sums [warps][2 columns]
+  return sizeof(float) * (2 * qcols<QP>() * D + 32) + 8 * 32 * (key_bplanes(KB, D) * D / 16) +
+         sizeof(float) * 2 * qcols<QP>() * (decode_threads<D>() / 32);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
@@ -231,10 +238,13 @@ __device__ __forceinline__ void sfrag_prefetch(const LayerView& lv, SFrag<D>& f)
 // (f16 max 65504), from bounds: max|w x_j| 2^24 with max|q_proj| <= max_i sum_j |S_ij| * max|q_rot|.
 // um / uq undo lambda (and apply the softmax scale in log2 units); cm / cq are half the sums of the
 // represented (rounded) operands, i.e. the +-1 offsets of the bit planes.
-template <int D, int NT, int KB>
+// With QP = 2 the CTA's row b covers the query rows 2b and 2b + 1 of one sequence: B column n is head
+// n % 4 of query n / 4.
+template <int D, int NT, int KB, int QP = 1>
 __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, float* ps, const SFrag<D>& sf,
                                            float (&um)[2], float (&cm)[2], float (&uq)[2], float (&cq)[2]) {
-  constexpr int NBP = key_bplanes(KB, D), QP = key_qjl_plane(KB), RP = key_rem_plane(KB, D);
+  constexpr int NCOL = qcols<QP>();
+  constexpr int NBP = key_bplanes(KB, D), QJP = key_qjl_plane(KB), RP = key_rem_plane(KB, D);
   constexpr int NMW = KB == 3 ? 2 : 4;  // index-plane weights
   constexpr int NE = D / 32;
   constexpr int HALVES = D / warp_coords<D>();
@@ -246,15 +256,16 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   float wmax = 0.f;  // largest |2 w| of the index planes
 #pragma unroll
   for (int p = 0; p < NMW; ++p) wmax = fmaxf(wmax, fabsf(2.f * lv.cb[kCbW + p]));
-  float* qr = ps;               // [4][D]
-  float* qp = qr + kMaxG * D;   // [4][D]
-  float* red = qp + kMaxG * D;  // [hd]: projection lambda; [4 + 2 hd + {0, 1}]: operand lambdas
-  if (warp < kMaxG) {           // q_rot: warp w rotates head w (zero rows for heads >= G)
+  float* qr = ps;              // [NCOL][D]
+  float* qp = qr + NCOL * D;   // [NCOL][D]
+  float* red = qp + NCOL * D;  // [col]: projection lambda; [NCOL + 2 col + {0, 1}]: operand lambdas
+  if (warp < NCOL) {           // q_rot: warp w rotates column w (zero rows for heads >= G)
+    const int hw = warp % kMaxG, vrow = QP * b + warp / kMaxG;
     float x[NE];
 #pragma unroll
     for (int e = 0; e < NE; ++e) {
       const int j = lane_coord<D>(e, lane);
-      const float qv = warp < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + warp) * D + j]) : 0.f;
+      const float qv = hw < G ? bf16_to_f32(a.q[((size_t)vrow * lv.Hq + h * G + hw) * D + j]) : 0.f;
       x[e] = qv * lv.D[j];
     }
     warp_fwht<NE>(x, lane);
@@ -271,13 +282,13 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
       const float big = 16777216.f;  // 2^24, the largest bit-plane prescale
       red[warp] = mx > 0.f ? exp2f(floorf(log2f(16384.f / mx))) : 1.f;
       const float bm = wmax * mx * big, bp = 2.f * lv.cb[kCbSmax] * mx * big;
-      red[4 + 2 * warp + 0] = bm > 0.f ? exp2f(floorf(log2f(32768.f / bm))) : 1.f;
-      red[4 + 2 * warp + 1] = bp > 0.f ? exp2f(floorf(log2f(32768.f / bp))) : 1.f;
+      red[NCOL + 2 * warp + 0] = bm > 0.f ? exp2f(floorf(log2f(32768.f / bm))) : 1.f;
+      red[NCOL + 2 * warp + 1] = bp > 0.f ? exp2f(floorf(log2f(32768.f / bp))) : 1.f;
     }
   }
   __syncthreads();
-  if (warp < MT / 2) {  // q_proj rows 16 mt .. 16 mt + 15, mt = 2 warp + {0, 1}; B column n = head g (zero for g >= 4)
-    const bool col = g < kMaxG;
+  if (warp < MT / 2) {  // q_proj rows 16 mt .. 16 mt + 15, mt = 2 warp + {0, 1}; B column n = column g (zero for g >= NCOL)
+    const bool col = g < NCOL;
     const float lam = col ? red[g] : 0.f;
     const float* qrow = qr + (col ? g : 0) * D + 2 * c;
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
@@ -296,7 +307,7 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
         mma_f16(acc[m2], A.x, A.y, A.z, A.w, l0, l1);
       }
     }
-    if (2 * c < kMaxG) {  // C columns 2c, 2c + 1 are heads
+    if (2 * c < NCOL) {  // C columns 2c, 2c + 1 are query columns
       const float i0 = 1.f / red[2 * c], i1 = 1.f / red[2 * c + 1];
 #pragma unroll
       for (int m2 = 0; m2 < 2; ++m2) {
@@ -315,16 +326,16 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   constexpr int KS = warp_coords<D>() / 16;  // key-MMA k-steps per warp
   constexpr int NW = NT / 32, NITEMS = HALVES * NBP * KS;
   uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
-  float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][8]
-  const bool live = g < G;
-  const float lam_m = live ? red[4 + 2 * g] : 0.f, lam_q = live ? red[4 + 2 * g + 1] : 0.f;
+  float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][2 NCOL]
+  const bool live = g < NCOL && g % kMaxG < G;
+  const float lam_m = live ? red[NCOL + 2 * g] : 0.f, lam_q = live ? red[NCOL + 2 * g + 1] : 0.f;
   const float* bm = qr + (live ? g : 0) * D;
   const float* bp = qp + (live ? g : 0) * D;
   __syncthreads();
   float sum_m = 0.f, sum_q = 0.f;
   for (int item = warp; item < NITEMS; item += NW) {
     const int s = item % KS, pi = (item / KS) % NBP, hv = item / (NBP * KS);
-    const bool qjl = pi == QP, rem = pi == RP;  // rem: remainder plane of plane 0
+    const bool qjl = pi == QJP, rem = pi == RP;  // rem: remainder plane of plane 0
     const float w = qjl ? 2.f * lam_q : 2.f * lv.cb[kCbW + (rem ? 0 : pi)] * lam_m;
     const float* base = qjl ? bp : bm;
     const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
@@ -351,23 +362,23 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
-  if (c == 0 && g < kMaxG) {
-    wsum[warp * 8 + g] = sum_m;
-    wsum[warp * 8 + 4 + g] = sum_q;
+  if (c == 0 && g < NCOL) {
+    wsum[warp * 2 * NCOL + g] = sum_m;
+    wsum[warp * 2 * NCOL + NCOL + g] = sum_q;
   }
   __syncthreads();
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is head hd
-    const int hd = min(2 * c + i, kMaxG - 1);
+  for (int i = 0; i < 2; ++i) {  // C-fragment column 2c + i is query column hd
+    const int hd = min(2 * c + i, NCOL - 1);
     float sm = 0.f, sq = 0.f;
     for (int w = 0; w < NW; ++w) {
-      sm += wsum[w * 8 + hd];
-      sq += wsum[w * 8 + 4 + hd];
+      sm += wsum[w * 2 * NCOL + hd];
+      sq += wsum[w * 2 * NCOL + NCOL + hd];
     }
-    um[i] = a.scale * kLog2e / red[4 + 2 * hd];
+    um[i] = a.scale * kLog2e / red[NCOL + 2 * hd];
     cm[i] = 0.5f * sm;
-    uq[i] = a.scale * kLog2e * kappa / red[4 + 2 * hd + 1];
+    uq[i] = a.scale * kLog2e * kappa / red[NCOL + 2 * hd + 1];
     cq[i] = 0.5f * sq;
   }
 }
@@ -381,39 +392,45 @@ template <int D>
 __host__ __device__ constexpr bool ring_kv_together() {
   return D <= 128;
 }
-template <int D>
+template <int D, int QP = 1>
 __host__ __device__ constexpr size_t ring_smem_bytes() {
-  return 128 + (ring_kv_together<D>() ? 2 : 1) * 2 * kPage * D + kPage * kMaxG * 4 + 64 + kMaxG * D * 4;
+  return 128 + (ring_kv_together<D>() ? 2 : 1) * 2 * kPage * D + kPage * qcols<QP>() * 4 + 16 * qcols<QP>() +
+         qcols<QP>() * D * 4;
 }
 
-__device__ __forceinline__ void write_empty_partial(float* part, int D, int tid, int nt) {
-  for (int i = tid; i < 2 * kMaxG + kMaxG * D; i += nt) part[i] = i < kMaxG ? -INFINITY : 0.f;
+// A partial of `ncol` query columns: m [ncol], l [ncol], o [ncol][D].
+__device__ __forceinline__ void write_empty_partial(float* part, int D, int tid, int nt, int ncol = kMaxG) {
+  for (int i = tid; i < 2 * ncol + ncol * D; i += nt) part[i] = i < ncol ? -INFINITY : 0.f;
 }
 
 // Exact attention over the unflushed ring tokens [F, R) of one (row, KV head). K and V rows are
 // bulk-copied into shared memory (together for head_dim 128). Scores are thread-per-token: thread t
 // walks its K row in 16-byte chunks starting at chunk t, so the 8 lanes of each quarter-warp read
 // 8 different bank groups. P.V is thread-per-coordinate.
-template <int D, int NT>
+// With QP = 2 the CTA's query rows 2b, 2b + 1 see n0 and n1 ring tokens (causal; a padding row sees
+// none): the columns of each query take no weight from ring tokens past its own count.
+template <int D, int NT, int QP = 1>
 __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
   constexpr int NC = D / 8;  // 16-byte chunks per row
+  constexpr int NCOL = qcols<QP>();
   constexpr bool KV = ring_kv_together<D>();
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L, Np, P;
   seq_packed(lv, slot, L, Np, P);
-  const int Lq = row_len(a, b, L);  // ring tokens are positions P .. Lq - 1
-  const int F = P - Np, n = Lq - P;
+  // ring tokens are positions P .. Lq - 1 of each query row
+  const int n0 = row_len(a, QP * b, L) - P, n1 = QP == 1 ? n0 : row_len(a, QP * b + 1, L) - P;
+  const int F = P - Np, n = max(n0, n1);
   if (n <= 0) {
-    write_empty_partial(part, D, tid, NT);
+    write_empty_partial(part, D, tid, NT, NCOL);
     return;
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
   const uint16_t* krows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16
   const uint16_t* vrows = KV ? krows + (size_t)kPage * D : krows;             // [n][D] bf16
-  float* sc = reinterpret_cast<float*>(smem_raw + 128 + (KV ? 2 : 1) * 2 * kPage * D);  // [128][4]
-  float* red = sc + kPage * kMaxG;                                                       // [4][2]
-  float* qs = red + 16;                                                                  // [4][D]
+  float* sc = reinterpret_cast<float*>(smem_raw + 128 + (KV ? 2 : 1) * 2 * kPage * D);  // [128][NCOL]
+  float* red = sc + kPage * NCOL;                                                        // [NCOL][2] (+ pad)
+  float* qs = red + 4 * NCOL;                                                            // [NCOL][D]
   const uint16_t* rk = lv.ring + (((size_t)slot * lv.Hkv + h) * 2) * kPage * D + (size_t)F * D;
   const uint16_t* rv = rk + (size_t)kPage * D;
   const uint32_t bytes = (uint32_t)n * D * 2;
@@ -429,16 +446,18 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     }
   }
   const int G = lv.G;
-  for (int i = tid; i < kMaxG * D; i += NT) {
-    const int g = i / D;
-    qs[i] = g < G ? bf16_to_f32(a.q[((size_t)b * lv.Hq + h * G + g) * D + (i % D)]) : 0.f;
+  for (int i = tid; i < NCOL * D; i += NT) {
+    const int g = (i / D) % kMaxG, vrow = QP * b + i / (kMaxG * D);
+    qs[i] = g < G ? bf16_to_f32(a.q[((size_t)vrow * lv.Hq + h * G + g) * D + (i % D)]) : 0.f;
   }
   __syncthreads();
   bool ok = mbar_wait(bar, 0);
   const float s2 = a.scale * kLog2e;
   if (ok) {
     for (int t = tid; t < n; t += NT) {
-      float acc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+      float acc[NCOL];
+#pragma unroll
+      for (int g = 0; g < NCOL; ++g) acc[g] = 0.f;
       const uint16_t* row = krows + (size_t)t * D;
 #pragma unroll 4
       for (int i = 0; i < NC; ++i) {
@@ -449,14 +468,17 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
                             __uint_as_float(u.z << 16), __uint_as_float(u.z & 0xffff0000u),
                             __uint_as_float(u.w << 16), __uint_as_float(u.w & 0xffff0000u)};
 #pragma unroll
-        for (int g = 0; g < kMaxG; ++g) {
+        for (int g = 0; g < NCOL; ++g) {
           const float4 q0 = *reinterpret_cast<const float4*>(qs + g * D + 8 * ci);
           const float4 q1 = *reinterpret_cast<const float4*>(qs + g * D + 8 * ci + 4);
           acc[g] = fmaf(q0.x, k[0], fmaf(q0.y, k[1], fmaf(q0.z, k[2], fmaf(q0.w, k[3], acc[g]))));
           acc[g] = fmaf(q1.x, k[4], fmaf(q1.y, k[5], fmaf(q1.z, k[6], fmaf(q1.w, k[7], acc[g]))));
         }
       }
-      *reinterpret_cast<float4*>(sc + t * kMaxG) = make_float4(acc[0] * s2, acc[1] * s2, acc[2] * s2, acc[3] * s2);
+#pragma unroll
+      for (int g4 = 0; g4 < NCOL; g4 += 4)
+        *reinterpret_cast<float4*>(sc + t * NCOL + g4) =
+            make_float4(acc[g4] * s2, acc[g4 + 1] * s2, acc[g4 + 2] * s2, acc[g4 + 3] * s2);
     }
   }
   __syncthreads();  // every K row has been read
@@ -465,16 +487,18 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     mbar_expect_tx(bar, bytes);
     bulk_g2s(smem_raw + 128, rv, bytes, bar);
   }
-  if (warp < kMaxG) {  // softmax statistics: warp g reduces head g
+  if (warp < NCOL) {  // softmax statistics: warp g reduces column g over its query's ring tokens
+    const int nw = warp < kMaxG ? n0 : n1;
     float m = -INFINITY;
-    for (int t = lane; t < n; t += 32) m = fmaxf(m, sc[t * kMaxG + warp]);
+    for (int t = lane; t < nw; t += 32) m = fmaxf(m, sc[t * NCOL + warp]);
     m = warp_max(m);
     float l = 0.f;
-    for (int t = lane; t < n; t += 32) {
-      const float p = exp2f(sc[t * kMaxG + warp] - m);
-      sc[t * kMaxG + warp] = p;
+    for (int t = lane; t < nw; t += 32) {
+      const float p = exp2f(sc[t * NCOL + warp] - m);
+      sc[t * NCOL + warp] = p;
       l += p;
     }
+    for (int t = max(nw, 0) + lane; t < n; t += 32) sc[t * NCOL + warp] = 0.f;  // past this query's position
     l = warp_sum(l);
     if (lane == 0) {
       red[2 * warp] = m;
@@ -485,38 +509,46 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
   ok = ok && mbar_wait(KV ? bar + 1 : bar, KV ? 0 : 1);
   if (!ok) {
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
-    write_empty_partial(part, D, tid, NT);
+    write_empty_partial(part, D, tid, NT, NCOL);
     return;
   }
   for (int j = tid; j < D; j += NT) {
-    float o[2][kMaxG] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float o[2][NCOL];
+#pragma unroll
+    for (int g = 0; g < NCOL; ++g) o[0][g] = o[1][g] = 0.f;
     int t = 0;
 #pragma unroll 4
     for (; t + 1 < n; t += 2) {  // two independent accumulator sets
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        const float4 p = *reinterpret_cast<const float4*>(sc + (t + u) * kMaxG);
         const float vv = bf16_to_f32(vrows[(size_t)(t + u) * D + j]);
-        o[u][0] = fmaf(p.x, vv, o[u][0]);
-        o[u][1] = fmaf(p.y, vv, o[u][1]);
-        o[u][2] = fmaf(p.z, vv, o[u][2]);
-        o[u][3] = fmaf(p.w, vv, o[u][3]);
+#pragma unroll
+        for (int g4 = 0; g4 < NCOL; g4 += 4) {
+          const float4 p = *reinterpret_cast<const float4*>(sc + (t + u) * NCOL + g4);
+          o[u][g4] = fmaf(p.x, vv, o[u][g4]);
+          o[u][g4 + 1] = fmaf(p.y, vv, o[u][g4 + 1]);
+          o[u][g4 + 2] = fmaf(p.z, vv, o[u][g4 + 2]);
+          o[u][g4 + 3] = fmaf(p.w, vv, o[u][g4 + 3]);
+        }
       }
     }
     if (t < n) {
-      const float4 p = *reinterpret_cast<const float4*>(sc + t * kMaxG);
       const float vv = bf16_to_f32(vrows[(size_t)t * D + j]);
-      o[0][0] = fmaf(p.x, vv, o[0][0]);
-      o[0][1] = fmaf(p.y, vv, o[0][1]);
-      o[0][2] = fmaf(p.z, vv, o[0][2]);
-      o[0][3] = fmaf(p.w, vv, o[0][3]);
+#pragma unroll
+      for (int g4 = 0; g4 < NCOL; g4 += 4) {
+        const float4 p = *reinterpret_cast<const float4*>(sc + t * NCOL + g4);
+        o[0][g4] = fmaf(p.x, vv, o[0][g4]);
+        o[0][g4 + 1] = fmaf(p.y, vv, o[0][g4 + 1]);
+        o[0][g4 + 2] = fmaf(p.z, vv, o[0][g4 + 2]);
+        o[0][g4 + 3] = fmaf(p.w, vv, o[0][g4 + 3]);
+      }
     }
 #pragma unroll
-    for (int g = 0; g < kMaxG; ++g) part[2 * kMaxG + g * D + j] = o[0][g] + o[1][g];
+    for (int g = 0; g < NCOL; ++g) part[2 * NCOL + g * D + j] = o[0][g] + o[1][g];
   }
-  if (tid < kMaxG) {
+  if (tid < NCOL) {
     part[tid] = red[2 * tid];
-    part[kMaxG + tid] = red[2 * tid + 1];
+    part[NCOL + tid] = red[2 * tid + 1];
   }
 }
 
@@ -525,23 +557,24 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
 // Run by the last CTA of a (row, KV head) to finish its partial. Warp w merges query head w on its
 // own (no block barrier): lanes take the splits' (m, l), the weights go through shared memory column w.
 // =============================================================================================
-template <int D, int NT>
+template <int D, int NT, int QP = 1>
 __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, float* sm) {
   constexpr int NE = D / 32;
+  constexpr int NCOL = qcols<QP>();
   const LayerView& lv = a.lv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp >= lv.G) return;
-  const int hd = warp;  // query head; lane holds coordinates 4*lane+e (+128)
+  if (warp >= NCOL || warp % kMaxG >= lv.G) return;
+  const int hd = warp;  // query column (head hd % 4 of query row QP b + hd / 4); lane holds coordinates 4*lane+e (+128)
   const int nsp = a.plan.n_splits;
   const size_t stride = a.plan.part_stride / sizeof(float);
   const float* base = reinterpret_cast<const float*>(a.ws + a.plan.part_off +
                                                      ((size_t)b * lv.Hkv + h) * (nsp + 1) * a.plan.part_stride);
-  float* fs = sm;                   // [nsp][4] split maxima, then split weights (column hd is this warp's)
-  float* ls = fs + 4 * (nsp + 1);   // [nsp][4] split sums
+  float* fs = sm;                      // [nsp][NCOL] split maxima, then split weights (column hd is this warp's)
+  float* ls = fs + NCOL * (nsp + 1);   // [nsp][NCOL] split sums
   // 0. the outputs of the first PRE splits and the ring partial do not depend on the weights: their
   //    loads share the round trip of the (m, l) loads
   constexpr int PRE = D == 128 ? 20 : D == 64 ? 24 : 8;
-  const float* ob = base + 2 * kMaxG + hd * D;
+  const float* ob = base + 2 * NCOL + hd * D;
   const float* rp = base + nsp * stride;
   float vpre[PRE][NE], rvp[NE];
 #pragma unroll
@@ -553,26 +586,26 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
       for (int e = 0; e < NE; ++e) vpre[u][e] = 0.f;
     }
   }
-  ld_cg_row<D>(rp + 2 * kMaxG + hd * D, lane, rvp);
-  const float mr = ld_cg_f(rp + hd), lr = ld_cg_f(rp + kMaxG + hd);
+  ld_cg_row<D>(rp + 2 * NCOL + hd * D, lane, rvp);
+  const float mr = ld_cg_f(rp + hd), lr = ld_cg_f(rp + NCOL + hd);
   float dsg[NE];  // the rotation signs of this lane's coordinates (constant table)
 #pragma unroll
   for (int e = 0; e < NE; ++e) dsg[e] = lv.D[lane_coord<D>(e, lane)];
   // 1. the splits' (m, l) of this head across the lanes; maximum, weights and the weighted sum of l
   float mloc = -INFINITY;
   for (int s = lane; s < nsp; s += 32) {
-    const float mv = ld_cg_f(base + s * stride + hd), lv2 = ld_cg_f(base + s * stride + kMaxG + hd);
-    fs[4 * s + hd] = mv;
-    ls[4 * s + hd] = lv2;
+    const float mv = ld_cg_f(base + s * stride + hd), lv2 = ld_cg_f(base + s * stride + NCOL + hd);
+    fs[NCOL * s + hd] = mv;
+    ls[NCOL * s + hd] = lv2;
     mloc = fmaxf(mloc, mv);
   }
   const float m = warp_max(mloc);
   float lloc = 0.f;
   for (int s = lane; s < nsp; s += 32) {
-    const float mv = fs[4 * s + hd];
+    const float mv = fs[NCOL * s + hd];
     const float f = mv == -INFINITY ? 0.f : exp2f(mv - m);
-    fs[4 * s + hd] = f;
-    lloc = fmaf(f, ls[4 * s + hd], lloc);
+    fs[NCOL * s + hd] = f;
+    lloc = fmaf(f, ls[NCOL * s + hd], lloc);
   }
   const float l = warp_sum(lloc);
   __syncwarp();
@@ -582,7 +615,7 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   for (int e = 0; e < NE; ++e) o[e] = o2[e] = 0.f;
 #pragma unroll
   for (int u = 0; u < PRE; ++u) {
-    const float f = u < nsp ? fs[u * 4 + hd] : 0.f;
+    const float f = u < nsp ? fs[u * NCOL + hd] : 0.f;
     float* acc = (u & 1) ? o2 : o;
 #pragma unroll
     for (int e = 0; e < NE; ++e) acc[e] = fmaf(f, vpre[u][e], acc[e]);
@@ -594,14 +627,14 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
     for (int u = 0; u < 16; ++u) ld_cg_row<D>(ob + (s0 + u) * stride, lane, v[u]);
 #pragma unroll
     for (int u = 0; u < 16; ++u) {
-      const float f = fs[(s0 + u) * 4 + hd];
+      const float f = fs[(s0 + u) * NCOL + hd];
       float* acc = (u & 1) ? o2 : o;
 #pragma unroll
       for (int e = 0; e < NE; ++e) acc[e] = fmaf(f, v[u][e], acc[e]);
     }
   }
   for (; s0 < nsp; ++s0) {
-    const float f = fs[s0 * 4 + hd];
+    const float f = fs[s0 * NCOL + hd];
     float v[NE];
     ld_cg_row<D>(ob + s0 * stride, lane, v);
 #pragma unroll
@@ -622,12 +655,12 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   float r[NE];
 #pragma unroll
   for (int e = 0; e < NE; ++e) r[e] = (fh * o[e] + fr * rvp[e]) * inv;
-  st_row<D>(a.out + ((size_t)b * lv.Hq + h * lv.G + hd) * D, lane, r);
+  st_row<D>(a.out + ((size_t)(QP * b + hd / kMaxG) * lv.Hq + h * lv.G + hd % kMaxG) * D, lane, r);
 }
 
 // After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
 // merges all of them (an arrival counter; no CTA waits on another).
-template <int D, int NT>
+template <int D, int NT, int QP = 1>
 __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem) {
   __shared__ int s_last;
   __syncthreads();  // every thread's part of the partial is written
@@ -642,7 +675,7 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
   }
   __syncthreads();
   if (!s_last) return;
-  combine_unit<D, NT>(a, b, h, reinterpret_cast<float*>(smem + 128));
+  combine_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
 }
 
 // Split-K decode CTA: 4 token groups x (d/128) coordinate halves of warps. Warp (tg, hf) owns
@@ -652,8 +685,11 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // exchange partial sums through shared memory.
 // Values: P is moved from C to B fragment layout with movmatrix and scaled per value group. Then
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
-template <int D, int VB, int STAGES, bool PAGED, int KB>
+// QP = 2 (prefill): the CTA's row b is the query rows 2b and 2b + 1 of one sequence, in the 8 B
+// columns; each lane's two C columns belong to query c / 2.
+template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1>
 __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
+  constexpr int NCOL = qcols<QP>();
   constexpr int NBP = key_bplanes(KB, D);  // B planes of the key MMAs (stored planes: KB)
   constexpr int RP = key_rem_plane(KB, D);
   constexpr int CW = warp_coords<D>();  // coordinates per warp
@@ -675,24 +711,27 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   // Every kernel of this library starts its dependents only after its own stream wait, so what this
   // kernel reads before its wait (q, seq_ids, the tables, the packed pages and count) was complete
   // before the previous kernel's dependents started.
-  const int slot = row_slot(a, b);
+  const int slot = row_slot(a, QP * b);
   if (slot < 0 || slot >= lv.max_seqs) {
     pdl_wait();
     pdl_launch();
-    write_empty_partial(part, D, tid, NT);
-    finish_unit<D, NT>(a, b, h, smem);
+    write_empty_partial(part, D, tid, NT, NCOL);
+    finish_unit<D, NT, QP>(a, b, h, smem);
     return;
   }
   if (sp == nsp) {
     pdl_wait();
     pdl_launch();
-    ring_split<D, NT>(a, b, h, slot, part, smem);
-    finish_unit<D, NT>(a, b, h, smem);
+    ring_split<D, NT, QP>(a, b, h, slot, part, smem);
+    finish_unit<D, NT, QP>(a, b, h, smem);
     return;
   }
   int L, Np, P;
   seq_packed(lv, slot, L, Np, P);
-  P = min(P, row_len(a, b, L));  // a prefill query sees the packed tokens before its own position
+  // a prefill query sees the packed tokens before its own position; Pq: this lane's query
+  const int P0 = min(P, row_len(a, QP * b, L)), P1 = QP == 1 ? P0 : min(P, row_len(a, QP * b + 1, L));
+  const int Pq = (QP == 1 || (lane & 3) < 2) ? P0 : P1;
+  P = max(P0, P1);
   const int n_pages = (P + kPage - 1) / kPage;
   const int pps = a.plan.pages_per_split;
   if (sp == 0 && tid == 0 && n_pages > nsp * pps) set_status(lv.status, TQ_DEV_ERR_SPLITS);
@@ -700,8 +739,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   if (pg0 >= pg1) {
     pdl_wait();
     pdl_launch();
-    write_empty_partial(part, D, tid, NT);
-    finish_unit<D, NT>(a, b, h, smem);
+    write_empty_partial(part, D, tid, NT, NCOL);
+    finish_unit<D, NT, QP>(a, b, h, smem);
     return;
   }
   const PageLayout pl = page_layout(D, VB, KB);
@@ -737,12 +776,12 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   sfrag_prefetch<D>(lv, sfrag);
   float um[2], cm[2], uq[2], cq[2];
   float* ps = xbuf + decode_xbuf_floats<D>();
-  query_prep<D, NT, KB>(a, b, h, ps, sfrag, um, cm, uq, cq);  // shared memory only
+  query_prep<D, NT, KB, QP>(a, b, h, ps, sfrag, um, cm, uq, cq);  // shared memory only
   pdl_wait();  // the partials and counters of any decode that shares ws are no longer in use
   pdl_launch();
   // f16 B fragments of the key MMAs for this warp's coordinate half, [plane][k-step][lane] in shared
   // memory (written by query_prep; read once per page and k-step, shared by both tiles)
-  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * kMaxG * D + 32) + hf * NBP * KS * 32 + lane;
+  const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * NCOL * D + 32) + hf * NBP * KS * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
   // score = n (um (am - cm) + uq gamma (aq - cq)) as n fma(gamma, fma(uq, aq, -uq cq), fma(um, am, -um cm)).
   // Columns of heads >= G (and 4..7) carry zero query operands: their scores are finite and their
@@ -770,7 +809,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
     // every warp reaches the stream barriers (the page contents are then unspecified).
     if (!timed_out && !mbar_wait(&full[stream * STAGES + s_], (k / STAGES) & 1)) timed_out = true;
     const uint8_t* pg = stage0 + (size_t)(stream * STAGES + s_) * PB;
-    const int valid = min(kPage, P - (pg0 + ip) * kPage);
+    const int valid = min(kPage, Pq - (pg0 + ip) * kPage);  // tokens of this page that this lane's query sees
     const uint2* kw2 = reinterpret_cast<const uint2*>(pg + pl.kbits_off);
     const uint32_t* nrm = reinterpret_cast<const uint32_t*>(pg + pl.norms_off);
     const uint32_t* vsc = reinterpret_cast<const uint32_t*>(pg + pl.vscale_off);  // [token pair][group] f16x2
@@ -972,9 +1011,9 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   __syncthreads();
   constexpr int NGRP = 4 * NS;                     // (stream, token group) partials
   const int grp = 4 * stream + tg;
-  float* wm = reinterpret_cast<float*>(stage0);  // [NGRP][4 heads]
-  float* wl = wm + 4 * NGRP;                     // [NGRP][4]
-  float* wo = wl + 4 * NGRP;                     // [NGRP][4][D]
+  float* wm = reinterpret_cast<float*>(stage0);  // [NGRP][NCOL query columns]
+  float* wl = wm + NCOL * NGRP;                  // [NGRP][NCOL]
+  float* wo = wl + NCOL * NGRP;                  // [NGRP][NCOL][D]
   {
     float l0 = l_acc[0], l1 = l_acc[1];
 #pragma unroll
@@ -982,52 +1021,52 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
-    if (hf == 0 && g == 0 && c < 2) {
-      wm[grp * 4 + 2 * c] = m_eff[0];
-      wm[grp * 4 + 2 * c + 1] = m_eff[1];
-      wl[grp * 4 + 2 * c] = l0;
-      wl[grp * 4 + 2 * c + 1] = l1;
+    if (hf == 0 && g == 0 && 2 * c < NCOL) {
+      wm[grp * NCOL + 2 * c] = m_eff[0];
+      wm[grp * NCOL + 2 * c + 1] = m_eff[1];
+      wl[grp * NCOL + 2 * c] = l0;
+      wl[grp * NCOL + 2 * c + 1] = l1;
     }
-    if (c < 2) {
+    if (2 * c < NCOL) {
 #pragma unroll
       for (int mt = 0; mt < 2 * QG; ++mt) {
         const int j0 = CW * hf + 16 * mt + g;
-        wo[(grp * 4 + 2 * c) * D + j0] = O[mt][0];
-        wo[(grp * 4 + 2 * c + 1) * D + j0] = O[mt][1];
-        wo[(grp * 4 + 2 * c) * D + j0 + 8] = O[mt][2];
-        wo[(grp * 4 + 2 * c + 1) * D + j0 + 8] = O[mt][3];
+        wo[(grp * NCOL + 2 * c) * D + j0] = O[mt][0];
+        wo[(grp * NCOL + 2 * c + 1) * D + j0] = O[mt][1];
+        wo[(grp * NCOL + 2 * c) * D + j0 + 8] = O[mt][2];
+        wo[(grp * NCOL + 2 * c + 1) * D + j0 + 8] = O[mt][3];
       }
     }
   }
   __syncthreads();
-  float* wf = wo + NGRP * 4 * D;  // [NGRP][4] group weights exp2(m_group - m)
-  if (tid < 4 * NGRP) {
-    const int hd = tid & 3, w = tid >> 2;
+  float* wf = wo + NGRP * NCOL * D;  // [NGRP][NCOL] group weights exp2(m_group - m)
+  if (tid < NCOL * NGRP) {
+    const int hd = tid % NCOL, w = tid / NCOL;
     float m = -INFINITY;
 #pragma unroll
-    for (int v = 0; v < NGRP; ++v) m = fmaxf(m, wm[v * 4 + hd]);
-    const float mw = wm[w * 4 + hd];
-    wf[w * 4 + hd] = (m == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - m);
+    for (int v = 0; v < NGRP; ++v) m = fmaxf(m, wm[v * NCOL + hd]);
+    const float mw = wm[w * NCOL + hd];
+    wf[w * NCOL + hd] = (m == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - m);
   }
   __syncthreads();
-  for (int i = tid; i < kMaxG * D; i += NT) {
+  for (int i = tid; i < NCOL * D; i += NT) {
     const int hd = i / D, j = i % D;
     float o = 0.f;
 #pragma unroll
-    for (int w = 0; w < NGRP; ++w) o = fmaf(wf[w * 4 + hd], wo[(w * 4 + hd) * D + j], o);
-    part[2 * kMaxG + hd * D + j] = o;
+    for (int w = 0; w < NGRP; ++w) o = fmaf(wf[w * NCOL + hd], wo[(w * NCOL + hd) * D + j], o);
+    part[2 * NCOL + hd * D + j] = o;
     if (j == 0) {
       float m = -INFINITY, l = 0.f;
 #pragma unroll
       for (int w = 0; w < NGRP; ++w) {
-        m = fmaxf(m, wm[w * 4 + hd]);
-        l = fmaf(wf[w * 4 + hd], wl[w * 4 + hd], l);
+        m = fmaxf(m, wm[w * NCOL + hd]);
+        l = fmaf(wf[w * NCOL + hd], wl[w * NCOL + hd], l);
       }
       part[hd] = m;
-      part[kMaxG + hd] = l;
+      part[NCOL + hd] = l;
     }
   }
-  finish_unit<D, NT>(a, b, h, smem);
+  finish_unit<D, NT, QP>(a, b, h, smem);
 }
 
 template <int D, int VB>
@@ -1035,18 +1074,19 @@ constexpr int decode_stages() {  // pages in flight per stream
   return D <= 128 ? 4 : 3;
 }
 
-template <int D, int VB, int KB>
+template <int D, int VB, int KB, int QP = 1>
 size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB, KB);
   constexpr int NT = decode_threads<D>();
   constexpr int NGRP = 4 * decode_streams<D>();
-  const size_t merge_bytes = sizeof(float) * (12 * NGRP + 4 * NGRP * D);
+  constexpr int NCOL = qcols<QP>();
+  const size_t merge_bytes = sizeof(float) * (3 * NGRP * NCOL + NGRP * NCOL * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
   size_t smem = 128 + (size_t)decode_streams<D>() * decode_stages<D, VB>() * pl.bytes + xbuf_bytes +
-                prep_scratch_bytes<D, KB>();
+                prep_scratch_bytes<D, KB, QP>();
   smem = std::max(smem, 128 + merge_bytes);
-  smem = std::max(smem, ring_smem_bytes<D>());
-  smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 8 * 1026));  // combine: split (m, l)
+  smem = std::max(smem, ring_smem_bytes<D, QP>());
+  smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 2 * NCOL * 1026));  // combine: split (m, l)
   return smem;
 }
 
@@ -1072,26 +1112,50 @@ int decode_setup() {
   return resident;
 }
 
+// qp = 2: prefill query pairs (contiguous cache); `batch` is then the number of CTA rows (pairs).
 template <int D, int VB, int KB>
-cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s) {
+cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s, int qp) {
   constexpr int STAGES = decode_stages<D, VB>();
   if (decode_setup<D, VB, KB>() < 0) return cudaErrorInvalidValue;
-  const size_t smem = decode_smem_bytes<D, VB, KB>();
+  const size_t smem = qp == 2 ? decode_smem_bytes<D, VB, KB, 2>() : decode_smem_bytes<D, VB, KB>();
+  if (qp == 2) {  // query pairs (prefill): attribute set once, outside any stream capture that follows
+    static bool pair_attr = false;
+    if (!pair_attr) {
+      if (smem > kMaxSmemPerCta) return cudaErrorInvalidValue;
+      cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, STAGES, false, KB, 2>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      pair_attr = true;
+    }
+  }
   if (phase == 0) {  // zero the arrival counters (every decode call leaves them at zero)
     cudaError_t e = cudaMemsetAsync(a.ws + a.plan.cnt_off, 0, sizeof(int32_t) * (size_t)batch * a.lv.Hkv, s);
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
     const dim3 grid(a.plan.n_splits + 1, a.lv.Hkv, batch);
-    cudaError_t e = a.lv.btab
-                        ? launch_pdl(k_decode<D, VB, STAGES, true, KB>, grid, dim3(decode_threads<D>()), smem, s, a)
-                        : launch_pdl(k_decode<D, VB, STAGES, false, KB>, grid, dim3(decode_threads<D>()), smem, s, a);
+    cudaError_t e =
+        qp == 2 ? launch_pdl(k_decode<D, VB, STAGES, false, KB, 2>, grid, dim3(decode_threads<D>()), smem, s, a)
+        : a.lv.btab ? launch_pdl(k_decode<D, VB, STAGES, true, KB>, grid, dim3(decode_threads<D>()), smem, s, a)
+                    : launch_pdl(k_decode<D, VB, STAGES, false, KB>, grid, dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;  // phase 2 (combine) runs inside phase 1's last CTA of every (row, KV head)
 }
 
 }  // namespace
+
+// True when the query-pair (prefill) kernel of ctx's shape fits the per-CTA shared memory.
+bool decode_pairs_fit(const tq_ctx* ctx) {
+  const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
+  size_t b;
+  if (kb == 4) b = d == 64 ? decode_smem_bytes<64, 4, 4, 2>() : d == 128 ? decode_smem_bytes<128, 4, 4, 2>()
+                                                                          : decode_smem_bytes<256, 4, 4, 2>();
+  else if (d == 64) b = vb == 2 ? decode_smem_bytes<64, 2, 3, 2>() : decode_smem_bytes<64, 4, 3, 2>();
+  else if (d == 128) b = vb == 2 ? decode_smem_bytes<128, 2, 3, 2>() : decode_smem_bytes<128, 4, 3, 2>();
+  else b = vb == 2 ? decode_smem_bytes<256, 2, 3, 2>() : decode_smem_bytes<256, 4, 3, 2>();
+  return b <= kMaxSmemPerCta;
+}
 
 // key_bits 4 is served with value_bits 4 (validated on the host).
 int decode_resident_ctas(const tq_ctx* ctx) {
@@ -1109,7 +1173,8 @@ int decode_resident_ctas(const tq_ctx* ctx) {
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
-                          const int32_t* n_q) {
+                          const int32_t* n_q, int qp) {
+  if (qp == 2 && (qpr % 2 != 0 || ctx->cfg.n_blocks > 0)) return cudaErrorInvalidValue;
   DecodeArgs a;
   a.lv = layer_view(ctx, layer);
   a.qpr = qpr;
@@ -1122,16 +1187,16 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.plan = plan;
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   if (kb == 4) {
-    if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s);
-    if (d == 128) return launch_decode_dv<128, 4, 4>(a, batch, phase, s);
-    return launch_decode_dv<256, 4, 4>(a, batch, phase, s);
+    if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);
+    if (d == 128) return launch_decode_dv<128, 4, 4>(a, batch, phase, s, qp);
+    return launch_decode_dv<256, 4, 4>(a, batch, phase, s, qp);
   }
-  if (d == 64 && vb == 2) return launch_decode_dv<64, 2, 3>(a, batch, phase, s);
-  if (d == 64 && vb == 4) return launch_decode_dv<64, 4, 3>(a, batch, phase, s);
-  if (d == 128 && vb == 2) return launch_decode_dv<128, 2, 3>(a, batch, phase, s);
-  if (d == 128 && vb == 4) return launch_decode_dv<128, 4, 3>(a, batch, phase, s);
-  if (d == 256 && vb == 2) return launch_decode_dv<256, 2, 3>(a, batch, phase, s);
-  return launch_decode_dv<256, 4, 3>(a, batch, phase, s);
+  if (d == 64 && vb == 2) return launch_decode_dv<64, 2, 3>(a, batch, phase, s, qp);
+  if (d == 64 && vb == 4) return launch_decode_dv<64, 4, 3>(a, batch, phase, s, qp);
+  if (d == 128 && vb == 2) return launch_decode_dv<128, 2, 3>(a, batch, phase, s, qp);
+  if (d == 128 && vb == 4) return launch_decode_dv<128, 4, 3>(a, batch, phase, s, qp);
+  if (d == 256 && vb == 2) return launch_decode_dv<256, 2, 3>(a, batch, phase, s, qp);
+  return launch_decode_dv<256, 4, 3>(a, batch, phase, s, qp);
 }
 
 }  // namespace tq

@@ -274,7 +274,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer) {
   return v;
 }
 
-DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows) {
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows, int ncol) {
   const tq_config& c = ctx->cfg;
   const int hint = (max_ctx_hint <= 0 || max_ctx_hint > c.max_ctx) ? c.max_ctx : max_ctx_hint;
   const int max_pages = std::max(1, (hint + kPage - 1) / kPage);
@@ -315,7 +315,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
   // other batch sizes or hints on the same workspace find them where the last call left them (zero).
   p.cnt_off = 0;
   p.part_off = align_up(sizeof(int32_t) * (size_t)std::max(c.max_seqs, cnt_rows) * c.n_kv_heads, 256);
-  p.part_stride = align_up((size_t)(2 * kMaxG + kMaxG * d) * sizeof(float), 16);
+  p.part_stride = align_up((size_t)(2 * ncol + ncol * d) * sizeof(float), 16);  // m, l [ncol], o [ncol][d]
   p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
   return p;
 }
@@ -545,10 +545,17 @@ static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q,
                                int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                                int max_ctx_hint, tq_stream_t stream);
 
+// Query rows per prefill CTA: two (that share the key operands of their sequence) when a row's chunk
+// has an even number of query slots, the cache is contiguous and the pair kernel's shared memory fits
+// (head_dim 128 with 4-bit keys does not), else one.
+static int prefill_qp(const tq_ctx* ctx, int q_per_row) {
+  return q_per_row % 2 == 0 && ctx->cfg.n_blocks == 0 && tq::decode_pairs_fit(ctx) ? 2 : 1;
+}
+
 size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
   if (!ctx || batch < 1 || q_per_row < 1 || (long long)batch * q_per_row > 65535) return 0;
-  const int rows = batch * q_per_row;
-  return tq::decode_plan(ctx, rows, max_ctx_hint, rows).bytes;
+  const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;
+  return tq::decode_plan(ctx, cta_rows, max_ctx_hint, cta_rows, tq::kMaxG * qp).bytes;
 }
 
 tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
@@ -566,16 +573,16 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
     return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
-  const int rows = batch * q_per_row;
-  const tq::DecodePlan plan = tq::decode_plan(ctx, rows, max_ctx_hint, rows);
+  const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;
+  const tq::DecodePlan plan = tq::decode_plan(ctx, cta_rows, max_ctx_hint, cta_rows, tq::kMaxG * qp);
   if (workspace_bytes < plan.bytes)
     return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
-  cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, rows, scale, d_workspace, plan, 0,
-                                    (cudaStream_t)stream, q_per_row, d_n_q);  // zero the counters
+  cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, cta_rows, scale, d_workspace, plan, 0,
+                                    (cudaStream_t)stream, q_per_row, d_n_q, qp);  // zero the counters
   if (e == cudaSuccess)
-    e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, rows, scale, d_workspace, plan, 1, (cudaStream_t)stream,
-                          q_per_row, d_n_q);
+    e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, cta_rows, scale, d_workspace, plan, 1, (cudaStream_t)stream,
+                          q_per_row, d_n_q, qp);
   return e == cudaSuccess ? ok() : cuda_fail(e, "prefill attention kernels");
 }
 

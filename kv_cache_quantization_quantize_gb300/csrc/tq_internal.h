@@ -194,10 +194,14 @@ struct DecodePlan {
   size_t bytes;
 };
 // cnt_rows: rows the arrival counters have room for (at least max_seqs; prefill rows per query).
-DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows = 0);
+DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows = 0, int ncol = kMaxG);
 
 // Split-K decode CTAs resident per SM for ctx's (head_dim, value_bits); sets kernel attributes once.
 int decode_resident_ctas(const tq_ctx* ctx);
+// Largest dynamic shared memory of one CTA on sm_103 (227 KB).
+constexpr size_t kMaxSmemPerCta = 232448;
+// True when the query-pair (prefill) decode kernel of ctx's shape fits kMaxSmemPerCta.
+bool decode_pairs_fit(const tq_ctx* ctx);
 
 // Records `msg` as the thread-local last error and returns `st` (for entry points outside tq_host.cpp).
 tq_status set_error(tq_status st, const char* msg);
@@ -211,6 +215,6 @@ cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
 // phase -1 = all three phases; 0 = prep, 1 = splits, 2 = combine.
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr = 1,
-                          const int32_t* n_q = nullptr);
+                          const int32_t* n_q = nullptr, int qp = 1);
 
 }  // namespace tq
