@@ -206,8 +206,7 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *   - Launches: the memset and one split-K decode kernel over batch * q_per_row query rows (the
  *     rows of one sequence read the same pages, mostly from L2). With an even q_per_row and a
  *     contiguous cache, each CTA takes two adjacent query rows of a sequence in the MMAs' 8 query
- *     columns, so they share the expanded key bits (not at head_dim 128 with key_bits 4, whose pair
- *     kernel would exceed the shared memory of a CTA). The workspace size depends on this choice;
+ *     columns, so they share the expanded key bits. The workspace size depends on this choice;
  *     tq_prefill_workspace_bytes makes the same one. */
 size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint);
 tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,

@@ -1074,7 +1074,7 @@ constexpr int decode_stages() {  // pages in flight per stream
   return D <= 128 ? 4 : 3;
 }
 
-template <int D, int VB, int KB, int QP = 1>
+template <int D, int VB, int KB, int QP = 1, int STAGES = decode_stages<D, VB>()>
 size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB, KB);
   constexpr int NT = decode_threads<D>();
@@ -1082,7 +1082,7 @@ size_t decode_smem_bytes() {
   constexpr int NCOL = qcols<QP>();
   const size_t merge_bytes = sizeof(float) * (3 * NGRP * NCOL + NGRP * NCOL * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
-  size_t smem = 128 + (size_t)decode_streams<D>() * decode_stages<D, VB>() * pl.bytes + xbuf_bytes +
+  size_t smem = 128 + (size_t)decode_streams<D>() * STAGES * pl.bytes + xbuf_bytes +
                 prep_scratch_bytes<D, KB, QP>();
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_smem_bytes<D, QP>());
@@ -1112,17 +1112,30 @@ int decode_setup() {
   return resident;
 }
 
+// Pages in flight per stream of the query-pair (prefill) kernel: the decode's count, or one fewer
+// where the pair kernel's shared memory would not fit (head_dim 128 with key_bits 4).
+template <int D, int VB, int KB>
+constexpr int pair_stages() {
+  constexpr int S = decode_stages<D, VB>();
+  constexpr size_t page_bytes = (size_t)KB * kPage * D / 8 + 4 * kPage + (size_t)kPage * D * VB / 8 + 2 * kPage * (D / 32);
+  return 128 + (size_t)decode_streams<D>() * S * page_bytes + sizeof(float) * decode_xbuf_floats<D>() +
+                     prep_scratch_bytes<D, KB, 2>() <= kMaxSmemPerCta
+             ? S
+             : S - 1;
+}
+
 // qp = 2: prefill query pairs (contiguous cache); `batch` is then the number of CTA rows (pairs).
 template <int D, int VB, int KB>
 cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStream_t s, int qp) {
   constexpr int STAGES = decode_stages<D, VB>();
   if (decode_setup<D, VB, KB>() < 0) return cudaErrorInvalidValue;
-  const size_t smem = qp == 2 ? decode_smem_bytes<D, VB, KB, 2>() : decode_smem_bytes<D, VB, KB>();
+  constexpr int PSTAGES = pair_stages<D, VB, KB>();
+  const size_t smem = qp == 2 ? decode_smem_bytes<D, VB, KB, 2, PSTAGES>() : decode_smem_bytes<D, VB, KB>();
   if (qp == 2) {  // query pairs (prefill): attribute set once, outside any stream capture that follows
     static bool pair_attr = false;
     if (!pair_attr) {
       if (smem > kMaxSmemPerCta) return cudaErrorInvalidValue;
-      cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, STAGES, false, KB, 2>,
+      cudaError_t e = cudaFuncSetAttribute(k_decode<D, VB, PSTAGES, false, KB, 2>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       pair_attr = true;
@@ -1135,7 +1148,7 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
   if (phase < 0 || phase == 1) {
     const dim3 grid(a.plan.n_splits + 1, a.lv.Hkv, batch);
     cudaError_t e =
-        qp == 2 ? launch_pdl(k_decode<D, VB, STAGES, false, KB, 2>, grid, dim3(decode_threads<D>()), smem, s, a)
+        qp == 2 ? launch_pdl(k_decode<D, VB, PSTAGES, false, KB, 2>, grid, dim3(decode_threads<D>()), smem, s, a)
         : a.lv.btab ? launch_pdl(k_decode<D, VB, STAGES, true, KB>, grid, dim3(decode_threads<D>()), smem, s, a)
                     : launch_pdl(k_decode<D, VB, STAGES, false, KB>, grid, dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
@@ -1149,11 +1162,19 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
 bool decode_pairs_fit(const tq_ctx* ctx) {
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   size_t b;
-  if (kb == 4) b = d == 64 ? decode_smem_bytes<64, 4, 4, 2>() : d == 128 ? decode_smem_bytes<128, 4, 4, 2>()
-                                                                          : decode_smem_bytes<256, 4, 4, 2>();
-  else if (d == 64) b = vb == 2 ? decode_smem_bytes<64, 2, 3, 2>() : decode_smem_bytes<64, 4, 3, 2>();
-  else if (d == 128) b = vb == 2 ? decode_smem_bytes<128, 2, 3, 2>() : decode_smem_bytes<128, 4, 3, 2>();
-  else b = vb == 2 ? decode_smem_bytes<256, 2, 3, 2>() : decode_smem_bytes<256, 4, 3, 2>();
+  if (kb == 4)
+    b = d == 64    ? decode_smem_bytes<64, 4, 4, 2, pair_stages<64, 4, 4>()>()
+        : d == 128 ? decode_smem_bytes<128, 4, 4, 2, pair_stages<128, 4, 4>()>()
+                   : decode_smem_bytes<256, 4, 4, 2, pair_stages<256, 4, 4>()>();
+  else if (d == 64)
+    b = vb == 2 ? decode_smem_bytes<64, 2, 3, 2, pair_stages<64, 2, 3>()>()
+                : decode_smem_bytes<64, 4, 3, 2, pair_stages<64, 4, 3>()>();
+  else if (d == 128)
+    b = vb == 2 ? decode_smem_bytes<128, 2, 3, 2, pair_stages<128, 2, 3>()>()
+                : decode_smem_bytes<128, 4, 3, 2, pair_stages<128, 4, 3>()>();
+  else
+    b = vb == 2 ? decode_smem_bytes<256, 2, 3, 2, pair_stages<256, 2, 3>()>()
+                : decode_smem_bytes<256, 4, 3, 2, pair_stages<256, 4, 3>()>();
   return b <= kMaxSmemPerCta;
 }
 

@@ -547,7 +547,8 @@ static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q,
 
 // Query rows per prefill CTA: two (that share the key operands of their sequence) when a row's chunk
 // has an even number of query slots, the cache is contiguous and the pair kernel's shared memory fits
-// (head_dim 128 with 4-bit keys does not), else one.
+// (it does for every supported shape, with one page stage fewer at head_dim 128 and key_bits 4), else
+// one.
 static int prefill_qp(const tq_ctx* ctx, int q_per_row) {
   return q_per_row % 2 == 0 && ctx->cfg.n_blocks == 0 && tq::decode_pairs_fit(ctx) ? 2 : 1;
 }
