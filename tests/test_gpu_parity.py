@@ -329,14 +329,20 @@ def test_paged_cache_scrambled_block_table(d, vb, kbits):
     assert paged.check_status() & 0x10
 
 
-@pytest.mark.parametrize("d,vb,kbits", [(128, 2, 3), (64, 4, 3), (256, 2, 3), (128, 4, 4)])
-def test_prefill_chunk_attention(d, vb, kbits):
-    """Chunked prefill: histories of 300 and 129 tokens, then chunks of 200 and 37 tokens appended in
-    one call (the second row padded to 200 queries). Every chunk query attends causally over the cache
-    after the append (packed tokens through their codes, ring tokens exactly), as the oracle's masked
-    prefill attention gives it on the device's own records and ring; padding queries output zeros."""
-    Hkv, G = 2, 4
-    hist, chunk, slots = [300, 129], [200, 37], [1, 0]
+@pytest.mark.parametrize("d,vb,kbits,chunk,G", [(128, 2, 3, (200, 37), 4), (64, 4, 3, (200, 37), 4),
+                                                (256, 2, 3, (200, 37), 4), (128, 4, 4, (200, 37), 4),
+                                                (128, 2, 3, (199, 36), 4), (128, 4, 3, (200, 37), 2),
+                                                (256, 4, 4, (199, 36), 2)])
+def test_prefill_chunk_attention(d, vb, kbits, chunk, G):
+    """Chunked prefill: histories of 300 and 129 tokens, then chunks of chunk[0] and chunk[1] tokens
+    appended in one call (the second row padded to chunk[0] queries). Every chunk query attends causally
+    over the cache after the append (packed tokens through their codes, ring tokens exactly), as the
+    oracle's masked prefill attention gives it on the device's own records and ring; padding queries
+    output zeros. An even number of query slots per row takes two query rows per CTA (their causal
+    lengths differ inside a CTA, and a query next to a padding query shares its CTA); an odd number
+    takes one."""
+    Hkv = 2
+    hist, chunk, slots = [300, 129], list(chunk), [1, 0]
     B, Tq = len(hist), max(chunk)
     cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2, max_ctx=640,
                  seed=13, key_bits=kbits)
@@ -380,4 +386,4 @@ def test_prefill_chunk_attention(d, vb, kbits):
                     err = rel_l2(out[i, j, h * G + g], ref[j, g])
                     worst = max(worst, err)
                     assert err <= 2e-3, (i, j, h, g, err)
-    print(f"prefill d={d} V{vb} K{kbits}: worst rel-L2 {worst:.2e}")
+    print(f"prefill d={d} V{vb} K{kbits} q_per_row {Tq} G{G}: worst rel-L2 {worst:.2e}")
