@@ -166,12 +166,17 @@ DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_llama8b_b1_ctx32k.md")
 
 
 def decode_source_digest():
-    """sha256 over the sources that make up the decode kernel (ties ncu counters to a kernel version)."""
+    """sha256 over the code of the sources that make up the decode kernel, with comments and whitespace
+    removed (ties ncu counters to a kernel version; an edit of a comment keeps them)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in DECODE_SOURCES:
-        with open(os.path.join(ROOT, "kv_cache_quantization_quantize_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "kv_cache_quantization_quantize_gb300", "csrc", name), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                 # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

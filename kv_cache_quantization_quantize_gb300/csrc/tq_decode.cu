@@ -784,8 +784,9 @@ __global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a)
   const uint2* bfr = reinterpret_cast<const uint2*>(ps + 2 * NCOL * D + 32) + hf * NBP * KS * 32 + lane;
   const int g = lane >> 2, c = lane & 3;
   // score = n (um (am - cm) + uq gamma (aq - cq)) as n fma(gamma, fma(uq, aq, -uq cq), fma(um, am, -um cm)).
-  // Columns of heads >= G (and 4..7) carry zero query operands: their scores are finite and their
-  // outputs are never merged, so only tokens past the end of a partial page need masking.
+  // Columns of heads >= G (and, for decode, columns 4..7) carry zero query operands: their scores are
+  // finite and their outputs are never merged, so only tokens past the end of the tokens this lane's
+  // query sees need masking (a partial last page, or a prefill query's causal end).
   float umcm[2], uqcq[2];
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
