@@ -687,8 +687,10 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
 // P.V runs on m16n8k16 with A = code fields (f16 subnormals code * 2^(pos-24)).
 // QP = 2 (prefill): the CTA's row b is the query rows 2b and 2b + 1 of one sequence, in the 8 B
 // columns; each lane's two C columns belong to query c / 2.
+// head_dim 256 with 2-bit values runs two CTAs per SM (128 registers, 104 KB of shared memory each);
+// its other shapes need more than half of an SM's shared memory and keep one.
 template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1>
-__global__ void __launch_bounds__(decode_threads<D>(), 1) k_decode(DecodeArgs a) {
+__global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 : 1) k_decode(DecodeArgs a) {
   constexpr int NCOL = qcols<QP>();
   constexpr int NBP = key_bplanes(KB, D);  // B planes of the key MMAs (stored planes: KB)
   constexpr int RP = key_rem_plane(KB, D);
