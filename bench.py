@@ -411,7 +411,7 @@ def run_ours(args):
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged
-            and WL["name"] == WORKLOADS["llama8b"]["name"]):  # oracle sample
+            and WL["kb"] == 3 and args.head_dim == 128):  # oracle sample of this workload
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -609,7 +609,7 @@ def oracle_sample_setup():
     import oracle
     from kv_cache_quantization_quantize_gb300 import synth
     d, ctx, Hkv = WL["d"], WL["ctx"], WL["hkv"]
-    k, v = synth.kv_tokens(ctx, Hkv, d, seed=1000, outliers=WL["outliers"])
+    k, v = synth.kv_tokens(ctx, Hkv, d, seed=1000, dist=WL["dist"], outliers=WL["outliers"])
     k = k[:, 0].double().numpy()
     v = v[:, 0].double().numpy()
     D = oracle.rademacher_signs(1, d)
@@ -630,14 +630,27 @@ def oracle_unit_step(st):
     return oracle.decode_attention(st["q"], st["keys"], st["vals"], st["rk"], st["rv"], st["D"], st["S"], st["c"])
 
 
-def _oracle_child(threads):
+def oracle_units():
+    """(layer, KV head, row) units of one decode step; the oracle times one and extrapolates."""
+    return WL["layers"] * WL["hkv"] * WL["batch"]
+
+
+def oracle_sample_reps():
+    """Timed oracle steps: 150 at 32K context, fewer at longer contexts (a bounded sample)."""
+    return max(10, 150 * 32768 // WL["ctx"])
+
+
+def _oracle_child(threads, args):
     """Runs the oracle sample in a child process limited to `threads` BLAS/OpenMP threads."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", "150"], env=env,
-                       capture_output=True, text=True, timeout=600)
+    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(oracle_sample_reps()),
+           "--workload", args.workload]
+    if args.value_bits:
+        cmd += ["--value-bits", str(args.value_bits)]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
@@ -646,13 +659,13 @@ def cpu_baseline(args):
     reported value) and one thread."""
     cores = os.cpu_count() or 1
     try:
-        res = _oracle_child(cores)
+        res = _oracle_child(cores, args)
     except Exception as e:  # report, do not fail the GPU line
         return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": f"failed: {e}"}
     line = {"value": res["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": res["sample"], "seconds": res["seconds"]}
     try:
-        one = _oracle_child(1)
+        one = _oracle_child(1, args)
         line["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1, "seconds": one["seconds"]}
     except Exception as e:
         line["single_thread"] = {"value": None, "note": f"failed: {e}"}
@@ -666,12 +679,13 @@ def oracle_sample_main(reps):
     for _ in range(reps):
         oracle_unit_step(st)
     dt = (time.perf_counter() - t0) / reps
-    units = WL["layers"] * WL["hkv"]
-    step_s = dt * units  # extrapolated linearly to all layers and KV heads
+    units = oracle_units()
+    step_s = dt * units  # extrapolated linearly to all layers, KV heads and rows
     value = WL["batch"] * WL["ctx"] / step_s
     print(json.dumps({"value": value, "seconds": dt * reps,
-                      "sample": f"{reps} decode steps of 1 layer x 1 KV head (4 query heads, {WL['ctx']} context) "
-                                f"timed; extrapolated linearly x{units} (32 layers x 8 KV heads)"}))
+                      "sample": f"{reps} decode steps of 1 layer x 1 KV head x 1 row ({WL['hq'] // WL['hkv']} query "
+                                f"heads, {WL['ctx']} context, head_dim {WL['d']}) timed; extrapolated linearly x{units} "
+                                f"({WL['layers']} layers x {WL['hkv']} KV heads x {WL['batch']} rows)"}))
 
 
 def run_reference(args):
@@ -686,7 +700,7 @@ def run_reference(args):
     for _ in range(args.steps):
         oracle_unit_step(st)
     dt = (time.perf_counter() - t0) / max(args.steps, 1)
-    units = WL["layers"] * WL["hkv"]
+    units = oracle_units()
     value = WL["batch"] * WL["ctx"] / (dt * units)
     cores = os.cpu_count() or 1
     sample = (f"each step = 1 layer x 1 KV head (4 query heads) of the {WL['ctx']}-token decode step, "
