@@ -714,6 +714,11 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   // kernel reads before its wait (q, seq_ids, the tables, the packed pages and count) was complete
   // before the previous kernel's dependents started.
   const int slot = row_slot(a, QP * b);
+  // The sequence state is read below before the stream wait. A decode row's packed count does not
+  // depend on the length that an append which codes no page may still be writing (such an append
+  // releases its dependents early). A prefill query's causal length does; a prefill launch never
+  // overlaps an append, because tq_prefill_attention zeroes the arrival counters with a memset right
+  // before this kernel, and a memset waits for the whole preceding kernel.
   if (slot < 0 || slot >= lv.max_seqs) {
     pdl_wait();
     pdl_launch();

@@ -579,6 +579,9 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
   if (workspace_bytes < plan.bytes)
     return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+  // Phase 0 zeroes the arrival counters with a memset. It also keeps the prefill kernel from
+  // overlapping a preceding append (a memset waits for the whole kernel before it), which the kernel
+  // relies on: it reads the sequence lengths, which fix every query's causal extent, before its wait.
   cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, cta_rows, scale, d_workspace, plan, 0,
                                     (cudaStream_t)stream, q_per_row, d_n_q, qp);  // zero the counters
   if (e == cudaSuccess)
