@@ -225,12 +225,25 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
  *     that device current. Make that first call before any stream capture.
  *   - Every call shares the one array, whose contents persist between calls. The only entries that
- *     must start at zero are the arrival counters: the array is zero-filled when the library loads and
- *     every call leaves the counters at zero; everything else a call reads, it writes first. Calls that
- *     overlap on the GPU (on different streams, or from different host threads) race on it and give
- *     wrong results; order them. */
+ *     must start at zero are the arrival counters: 16384 of them, one per (row, KV head), in a fixed
+ *     region at the start of the array for every context (so batch x n_kv_heads <= 16384, else
+ *     TQ_ERR_CAPACITY); the split partials follow that region. The array is zero-filled when the library
+ *     loads and every call leaves the counters at zero; everything else a call reads, it writes first, so
+ *     calls on contexts of different shapes may alternate. Calls that overlap on the GPU (on different
+ *     streams, or from different host threads) race on it and give wrong results; order them. */
 tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                       int batch, float softmax_scale, int max_ctx_hint, tq_stream_t stream);
+
+/* Test hook for the bounded waits of the decode kernels (not part of the decode itself). stage >= 0 makes
+ * every following tq_decode_attention / tq_decode_phase / tq_decode_attention_noalloc launch at head_dim 128
+ * leave one page stage without its copy: in the first split CTA of row 0, KV head 0, the first page stream issues neither
+ * the copy nor the expected-byte count of page stage `stage` (0 .. stages - 1; a stage the kernel does not
+ * have is ignored), and its wait on that stage gives up after `polls` polls (1 .. 2^22). The kernel then
+ * sets TQ_DEV_ERR_TIMEOUT, waits (bounded) for every copy it did issue, and returns; that unit's output is
+ * unspecified, every other unit's is exact, and the workspace stays usable. Nothing faults or hangs.
+ * stage = -1 turns the hook off (the default). Returns TQ_ERR_INVALID_ARG for values out of range.
+ * Process-wide; set it only while no other thread launches decodes. */
+tq_status tq_debug_decode_wait_fault(int stage, int polls);
 
 /* Synchronises `stream` and reads the device status word. It returns TQ_OK if the word is zero.
  * Otherwise it returns TQ_ERR_DEVICE and stores the word in *word (if non-NULL). `clear` != 0

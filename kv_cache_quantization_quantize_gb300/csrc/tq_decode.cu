@@ -16,6 +16,7 @@
 // P' = p * s * 2^(24-pos). The mid-rise offset (2^(b-1) - 1/2) * sum(P') is removed at the end of
 // the split, using the same f16 weights.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdio>
 #include <mutex>
@@ -29,6 +30,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// Wait-timeout test hook (tq_debug_decode_wait_fault), read by every decode launch.
+std::atomic<int> g_fault_stage{-1};
+std::atomic<int> g_fault_polls{0};
+
 struct DecodeArgs {
   LayerView lv;
   int qpr;              // queries per cache row: 1 for decode; > 1 for prefill (row b = batch row b / qpr)
@@ -39,6 +44,11 @@ struct DecodeArgs {
   float scale;
   uint8_t* ws;
   DecodePlan plan;
+  // Wait-timeout test hook (tq_debug_decode_wait_fault): >= 0 makes the first split CTA of (row 0, KV head 0)
+  // leave page stage `fault_stage` of its first page stream without a copy; its wait on that stage gives up
+  // after `fault_polls` polls. -1 in normal use.
+  int fault_stage;
+  uint32_t fault_polls;
 };
 
 __device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -172,16 +182,18 @@ __host__ __device__ constexpr int decode_threads() {
 // =============================================================================================
 
 // B-operand planes of the key MMAs:
-//   key_bits 3: index planes 0, 1 and the QJL sign plane 2; at head_dim 64 also plane 3, the f16
-//     rounding remainder of plane 0's operand, multiplied against plane 0's bits (with 64 coordinates
-//     the rounding error of the operands weighs most).
+//   key_bits 3: index planes 0, 1 and the QJL sign plane 2; at head_dim 64 and 128 also plane 3, the f16
+//     rounding remainder of plane 0's operand, multiplied against plane 0's bits. The f16 rounding of
+//     the query operands is the largest error of the estimate; the remainder roughly halves it (at
+//     head_dim 128 it took an early prefill query over 1025 tokens with x10 key outliers from 2.6e-3 to
+//     inside the 2e-3 attention bound).
 //   key_bits 4: index planes 0-3 (3 = parity plane), the QJL sign plane 4, and plane 5, the remainder
 //     of plane 0 (the largest weight). Without it the f16 rounding of four index operands adds about
 //     1.2x the score error of the 2-bit index.
-__host__ __device__ constexpr int key_bplanes(int kb, int d) { return kb == 3 ? (d == 64 ? 4 : 3) : 6; }
+__host__ __device__ constexpr int key_bplanes(int kb, int d) { return kb == 3 ? (d <= 128 ? 4 : 3) : 6; }
 // B plane that carries the QJL operand, and the remainder plane of plane 0 (-1: none).
 __host__ __device__ constexpr int key_qjl_plane(int kb) { return kb == 3 ? 2 : 4; }
-__host__ __device__ constexpr int key_rem_plane(int kb, int d) { return kb == 3 ? (d == 64 ? 3 : -1) : 5; }
+__host__ __device__ constexpr int key_rem_plane(int kb, int d) { return kb == 3 ? (d <= 128 ? 3 : -1) : 5; }
 
 // Query columns of a split CTA: the 8 B columns of the MMAs carry the kMaxG heads of QP query rows
 // (QP = 1 for decode; 2 for prefill, whose chunk queries of one sequence share the key operands).
@@ -409,8 +421,10 @@ __device__ __forceinline__ void write_empty_partial(float* part, int D, int tid,
 // 8 different bank groups. P.V is thread-per-coordinate.
 // With QP = 2 the CTA's query rows 2b, 2b + 1 see n0 and n1 ring tokens (causal; a padding row sees
 // none): the columns of each query take no weight from ring tokens past its own count.
+// Returns false when a copy into shared memory may still be in flight (a wait gave up and so did the
+// bounded drain after it): the CTA must then not reuse its shared memory.
 template <int D, int NT, int QP = 1>
-__device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
+__device__ __noinline__ bool ring_split(const DecodeArgs& a, int b, int h, int slot, float* part, uint8_t* smem_raw) {
   constexpr int NC = D / 8;  // 16-byte chunks per row
   constexpr int NCOL = qcols<QP>();
   constexpr bool KV = ring_kv_together<D>();
@@ -423,7 +437,7 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
   const int F = P - Np, n = max(n0, n1);
   if (n <= 0) {
     write_empty_partial(part, D, tid, NT, NCOL);
-    return;
+    return true;
   }
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
   const uint16_t* krows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16
@@ -450,10 +464,10 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     const int g = (i / D) % kMaxG, vrow = QP * b + i / (kMaxG * D);
     qs[i] = g < G ? bf16_to_f32(a.q[((size_t)vrow * lv.Hq + h * G + g) * D + (i % D)]) : 0.f;
   }
-  __syncthreads();
-  bool ok = mbar_wait(bar, 0);
+  // every thread agrees on whether the K rows landed (the V copy below depends on it)
+  const bool ok_k = __syncthreads_and(mbar_wait(bar, 0)) != 0;
   const float s2 = a.scale * kLog2e;
-  if (ok) {
+  if (ok_k) {
     for (int t = tid; t < n; t += NT) {
       float acc[NCOL];
 #pragma unroll
@@ -482,7 +496,7 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     }
   }
   __syncthreads();  // every K row has been read
-  if (!KV && tid == 0 && ok) {
+  if (!KV && tid == 0 && ok_k) {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     mbar_expect_tx(bar, bytes);
     bulk_g2s(smem_raw + 128, rv, bytes, bar);
@@ -506,11 +520,19 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     }
   }
   __syncthreads();
-  ok = ok && mbar_wait(KV ? bar + 1 : bar, KV ? 0 : 1);
-  if (!ok) {
-    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  const bool ok_v = __syncthreads_and(ok_k && mbar_wait(KV ? bar + 1 : bar, KV ? 0 : 1)) != 0;
+  if (!ok_v) {
+    // a wait gave up: thread 0 waits (bounded) for the copies that were issued and not seen to land -
+    // K (if its wait failed) and V (issued with K, or after K landed) - so that none lands later
+    bool drained = true;
+    if (tid == 0) {
+      set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+      if (!ok_k) drained = mbar_wait(bar, 0);
+      if (KV) drained = mbar_wait(bar + 1, 0) && drained;
+      else if (ok_k) drained = mbar_wait(bar, 1) && drained;
+    }
     write_empty_partial(part, D, tid, NT, NCOL);
-    return;
+    return __syncthreads_and(drained) != 0;
   }
   for (int j = tid; j < D; j += NT) {
     float o[2][NCOL];
@@ -550,6 +572,7 @@ __device__ __noinline__ void ring_split(const DecodeArgs& a, int b, int h, int s
     part[tid] = red[2 * tid];
     part[NCOL + tid] = red[2 * tid + 1];
   }
+  return true;
 }
 
 // =============================================================================================
@@ -658,10 +681,25 @@ __device__ __noinline__ void combine_unit(const DecodeArgs& a, int b, int h, flo
   st_row<D>(a.out + ((size_t)(QP * b + hd / kMaxG) * lv.Hq + h * lv.G + hd % kMaxG) * D, lane, r);
 }
 
+// Zero outputs of the query columns of (row b, KV head h): the result of a unit whose last CTA cannot
+// use its shared memory (a copy into it may still be in flight after a wait gave up; the call has
+// TQ_DEV_ERR_TIMEOUT set and its result is unspecified).
+template <int D, int NT, int QP>
+__device__ __forceinline__ void zero_unit_out(const DecodeArgs& a, int b, int h) {
+  constexpr int NCOL = qcols<QP>();
+  const LayerView& lv = a.lv;
+  for (int i = threadIdx.x; i < NCOL * D; i += NT) {
+    const int col = i / D;
+    if (col % kMaxG < lv.G)
+      a.out[((size_t)(QP * b + col / kMaxG) * lv.Hq + h * lv.G + col % kMaxG) * D + i % D] = 0.f;
+  }
+}
+
 // After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
-// merges all of them (an arrival counter; no CTA waits on another).
+// merges all of them (an arrival counter; no CTA waits on another). smem_ok = false: this CTA's shared
+// memory may still receive a copy, so a last CTA writes zeros instead of combining.
 template <int D, int NT, int QP = 1>
-__device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem) {
+__device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem, bool smem_ok = true) {
   __shared__ int s_last;
   __syncthreads();  // every thread's part of the partial is written
   if (threadIdx.x == 0) {
@@ -675,6 +713,10 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
   }
   __syncthreads();
   if (!s_last) return;
+  if (!smem_ok) {
+    zero_unit_out<D, NT, QP>(a, b, h);
+    return;
+  }
   combine_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
 }
 
@@ -729,8 +771,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   if (sp == nsp) {
     pdl_wait();
     pdl_launch();
-    ring_split<D, NT, QP>(a, b, h, slot, part, smem);
-    finish_unit<D, NT, QP>(a, b, h, smem);
+    const bool smem_ok = ring_split<D, NT, QP>(a, b, h, slot, part, smem);
+    finish_unit<D, NT, QP>(a, b, h, smem, smem_ok);
     return;
   }
   int L, Np, P;
@@ -760,11 +802,16 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   // about 20 % if it is only branched around)
   const uint8_t* gpages = lv.pages + ((size_t)slot * lv.Hkv + h) * lv.max_pages * PB;
   const int npg = pg1 - pg0;  // stream st takes local pages st, st + NS, st + 2 NS, ...
+  // wait-timeout test hook (head_dim 128 kernels): this CTA's stream 0 gets no copy (and no expect_tx) for
+  // page stage fault_k
+  const int fault_k =
+      (D == 128 && a.fault_stage >= 0 && a.fault_stage < STAGES && sp == 0 && h == 0 && b == 0) ? a.fault_stage : -1;
   if (tid == 0) {
     for (int s = 0; s < NS * STAGES; ++s) mbar_init(&full[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     for (int st = 0; st < NS; ++st)
       for (int s = 0; s < STAGES && st + NS * s < npg; ++s) {
+        if (st == 0 && s == fault_k) continue;
         if (PAGED) {  // a page without a block reads block 0 and is reported after the loop
           const int blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + st + NS * s];
           const bool okb = (unsigned)blk < (unsigned)lv.n_blocks;
@@ -805,17 +852,22 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   for (int mt = 0; mt < 2 * QG; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.f;
   float m_eff[2] = {-INFINITY, -INFINITY}, l_acc[2] = {0.f, 0.f};
   __syncthreads();
-  bool timed_out = false;
+  // kt: the first page (loop index k) whose wait this thread gave up on, or -1. A wait that gives up
+  // marks the call (TQ_DEV_ERR_TIMEOUT); this thread then waits no more, and a stream whose issuing
+  // thread gave up issues no more copies. The loop still runs to its end so that every warp reaches the
+  // stream barriers (the page contents are then unspecified).
+  int kt = -1;
+  const bool issuer = (tid % (32 * SW)) == 0;  // the thread that issues this stream's copies
   bool bad_block = false;  // paged cache: a page without a block was read as block 0
   int next_blk = 0;        // paged cache: block of the page this stream's issuing thread copies next
-  if (PAGED && (tid % (32 * SW)) == 0 && stream + NS * STAGES < npg)
+  if (PAGED && issuer && stream + NS * STAGES < npg)
     next_blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + stream + NS * STAGES];
 
   for (int k = 0; stream + NS * k < npg; ++k) {
     const int ip = stream + NS * k, s_ = k % STAGES;
-    // A wait that gives up marks the call and stops waiting; the loop still runs to its end so that
-    // every warp reaches the stream barriers (the page contents are then unspecified).
-    if (!timed_out && !mbar_wait(&full[stream * STAGES + s_], (k / STAGES) & 1)) timed_out = true;
+    if (kt < 0 && !mbar_wait(&full[stream * STAGES + s_], (k / STAGES) & 1,
+                             stream == 0 && k == fault_k ? a.fault_polls : kWaitPolls))
+      kt = k;
     const uint8_t* pg = stage0 + (size_t)(stream * STAGES + s_) * PB;
     const int valid = min(kPage, Pq - (pg0 + ip) * kPage);  // tokens of this page that this lane's query sees
     const uint2* kw2 = reinterpret_cast<const uint2*>(pg + pl.kbits_off);
@@ -997,7 +1049,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
     // every warp of the stream is done with stage s_ (and with xbuf)
     if (NS == 1) __syncthreads();
     else named_barrier(5 + stream, 32 * SW);
-    if ((tid % (32 * SW)) == 0 && ip + NS * STAGES < npg) {
+    if (issuer && kt < 0 && ip + NS * STAGES < npg) {
       if (PAGED) {  // branch-free: a page without a block reads block 0 and is reported after the loop
         const int blk = next_blk;  // loaded one page earlier, off this warp's critical path
         if (ip + NS + NS * STAGES < npg) next_blk = lv.btab[(size_t)slot * lv.max_pages + pg0 + ip + NS + NS * STAGES];
@@ -1013,8 +1065,25 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
       }
     }
   }
-  if (timed_out && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   if (PAGED && bad_block) set_status(lv.status, TQ_DEV_ERR_BLOCK);
+  if (__syncthreads_or(kt >= 0)) {
+    // A wait gave up. Each stream's issuing thread waits (bounded) for the copies it issued that it has
+    // not seen land: its refills stopped at its first failed wait kt, so they are pages kt .. kt + STAGES - 1
+    // of the stream (the hook's page was never issued). Only then may the stages be reused below, or the
+    // CTA exit. If such a copy still does not land, the CTA leaves its shared memory alone.
+    bool drained = true;
+    if (issuer && kt >= 0) {
+      const int nk = (npg - stream + NS - 1) / NS;
+      for (int j = kt; j < kt + STAGES && j < nk; ++j)
+        if (!(stream == 0 && j == fault_k)) drained = mbar_wait(&full[stream * STAGES + j % STAGES], (j / STAGES) & 1) && drained;
+    }
+    if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+    if (!__syncthreads_and(drained)) {
+      write_empty_partial(part, D, tid, NT, NCOL);
+      finish_unit<D, NT, QP>(a, b, h, smem, false);
+      return;
+    }
+  }
   // ---- merge the token groups' partials through shared memory ----
   __syncthreads();
   constexpr int NGRP = 4 * NS;                     // (stream, token group) partials
@@ -1214,6 +1283,8 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.scale = scale;
   a.ws = static_cast<uint8_t*>(ws);
   a.plan = plan;
+  a.fault_stage = g_fault_stage.load();
+  a.fault_polls = (uint32_t)g_fault_polls.load();
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   if (kb == 4) {
     if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);
@@ -1246,6 +1317,11 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB, held by every device that loads libtq
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+// The arrival counters sit in a fixed region at the start of the array, one per (row, KV head), and the
+// split partials start right after it, whatever the context. Calls on contexts of different shapes
+// therefore never place one context's partials over another's counters (the workspace plan of a
+// context sizes its counter region by that context's max_seqs x n_kv_heads).
+constexpr size_t kNoAllocCounters = 16384;
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
@@ -1285,7 +1361,14 @@ extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const v
     return tq::set_error(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
   if (!(softmax_scale == softmax_scale)) return tq::set_error(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
   if (ctx->device >= tq::kMaxDevices) return tq::set_error(TQ_ERR_UNSUPPORTED, "device index >= 64");
-  const tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
+  if ((size_t)batch * ctx->cfg.n_kv_heads > tq::kNoAllocCounters)
+    return tq::set_error(TQ_ERR_CAPACITY, "batch x n_kv_heads exceeds the 16384 arrival counters of the built-in "
+                                          "scratch of tq_decode_attention_noalloc");
+  tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
+  plan.cnt_off = 0;
+  plan.part_off = tq::kNoAllocCounters * sizeof(int32_t);
+  plan.bytes = (plan.part_off + plan.part_stride * (size_t)batch * ctx->cfg.n_kv_heads * (plan.n_splits + 1) + 255) /
+               256 * 256;
   if (plan.bytes > tq::kNoAllocScratchBytes) {
     char msg[200];
     snprintf(msg, sizeof(msg),
@@ -1300,5 +1383,14 @@ extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const v
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
   e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, scratch, plan, -1, (cudaStream_t)stream);
   if (e != cudaSuccess) return tq::set_error(TQ_ERR_CUDA, cudaGetErrorString(e));
+  return tq::set_error(TQ_OK, "");
+}
+
+extern "C" tq_status tq_debug_decode_wait_fault(int stage, int polls) {
+  if (stage < -1 || stage > 3) return tq::set_error(TQ_ERR_INVALID_ARG, "stage must be -1 (off) or 0..3");
+  if (stage >= 0 && (polls < 1 || polls > (int)tq::kWaitPolls))
+    return tq::set_error(TQ_ERR_INVALID_ARG, "polls must be in [1, 2^22]");
+  tq::g_fault_polls.store(stage >= 0 ? polls : 0);
+  tq::g_fault_stage.store(stage);
   return tq::set_error(TQ_OK, "");
 }

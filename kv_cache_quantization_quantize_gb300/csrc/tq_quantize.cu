@@ -679,7 +679,9 @@ constexpr int kTcThreads = 512;  // warps 0-7 keys, 8-15 values; two warps (colu
 constexpr uint32_t kQbHD = 0, kQbS = 32768, kQbBuf = 65536;  // 2 x [K tile 32 KB | V tile 32 KB]
 constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 value codes
 constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
-constexpr uint32_t kQbBar = kQbX + 2048 + 4096 + 2048, kQbEnd = kQbBar + 64;
+// mbarriers [8] (slot 6 holds the TMEM address), then the arming and completion counts of each barrier
+// ([8] + [8] u32, see bulk128_drain)
+constexpr uint32_t kQbBar = kQbX + 2048 + 4096 + 2048, kQbEnd = kQbBar + 128;
 constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -717,9 +719,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 // `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
 // all threads (at most one page per row and append).
 // The copy is made by the nthr threads whose index relative to `first` is in [0, nthr).
+// `armed` counts the copies armed on `bar` (see bulk128_drain).
 __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
-                                             uint64_t* bar, int first, int nthr) {
+                                             uint64_t* bar, uint32_t* armed, int first, int nthr) {
   constexpr int D = 128;
   const int rel = (int)threadIdx.x - first;
   if (rel < 0 || rel >= nthr) return pg * kPage >= L;
@@ -727,6 +730,7 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
     if (rel == 0) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_expect_tx(bar, 4u * 16384u);
+      ++*armed;
       const int z = pg * kPage - L;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -756,7 +760,8 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
 
 // Rotation of the K and V tiles of one page (buffer at smem address buf) by the tensor cores:
 // D[t][i] = sum_j x[t][j] (H D)[i][j], K into TMEM columns [0, 128) of `tcol`, V into [128, 256).
-__device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar) {
+__device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar,
+                                               uint32_t* armed) {
   tc_fence_after();
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
@@ -770,6 +775,27 @@ __device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint
               ks > 0);
   }
   umma_commit(bar);
+  ++*armed;
+}
+
+// After the page loop of k_quantize_bulk128 (thread 0): every copy or MMA batch armed on one of the
+// CTA's barriers and not seen complete by the thread that counts it is waited for (bounded), so that
+// nothing lands in shared memory or TMEM after the CTA frees them. armed / done: per barrier, the
+// phases armed and the phases seen complete. In a run without a failed wait the counts are equal.
+// Returns false if a wait gives up here too.
+__device__ __forceinline__ bool bulk128_drain(uint64_t* bars, uint32_t* armed, uint32_t* done) {
+  bool ok = true;
+  for (int i = 0; i < 8; ++i) {
+    if (i == 6) continue;  // the TMEM address slot
+    while (done[i] < armed[i]) {
+      if (!mbar_wait(bars + i, done[i] & 1u)) {
+        ok = false;
+        break;
+      }
+      ++done[i];
+    }
+  }
+  return ok;
 }
 
 // Next task (>= task, stepping by the grid) that has a page to write, or ntasks.
@@ -799,15 +825,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_ld = bar_tab + 2;   // [2]: page loads into buffer 0 / 1
   uint64_t* bar_rot = bar_tab + 4;  // [2]: rotations into TMEM half 0 / 1
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 6);
+  // phases armed on barrier i and seen complete by the thread that counts it: barrier 0 (tables) and the
+  // rotations by thread 0; the page loads by the thread that waits for them (0 for the first, 256
+  // after); the QJL projections by thread 256
+  uint32_t* armed = reinterpret_cast<uint32_t*>(bar_tab + 8);
+  uint32_t* done = armed + 8;
+  auto qjl_idx = [](uint32_t i) { return i ? 7 : 1; };
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
   pdl_launch();
   if (tid == 0) {
+    for (int i = 0; i < 16; ++i) armed[i] = 0u;  // armed[8], done[8]
     for (int i = 0; i < 8; ++i)
       if (i != 6) mbar_init(bar_tab + i, 1);  // slot 6 holds the TMEM address
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(bar_tab, 4u * D * D);
+    armed[0] = 1u;
     bulk_g2s(sm + kQbHD, lv.HD_sw, 2u * D * D, bar_tab);
     bulk_g2s(sm + kQbS, lv.S_sw, 2u * D * D, bar_tab);
   }
@@ -826,9 +860,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   int cur = bulk128_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
   bool tma_cur = cur < ntasks &&
-                 bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, 0, kTcThreads);
+                 bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0, kTcThreads);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-  bool ok = __syncthreads_and(mbar_wait(bar_tab, 0)) != 0;
+  const bool tab_ok = mbar_wait(bar_tab, 0);
+  if (tid == 0 && tab_ok) ++done[0];
+  bool ok = __syncthreads_and(tab_ok) != 0;
   // parities of the next wait: bit i of ph_ld / ph_rot for buffer / TMEM half i
   uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;
   // Pipeline. Page i lives in smem buffer i % 2 and TMEM half i % 2.
@@ -840,8 +876,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // projection of page i run while the values of page i are packed. The first page's rotation is
   // issued here.
   if (ok && cur < ntasks && tid == 0) {
-    if (tma_cur && !mbar_wait(bar_ld, 0)) ok = false;
-    if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot);
+    if (tma_cur) {
+      if (mbar_wait(bar_ld, 0)) ++done[2];
+      else ok = false;
+    }
+    if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot, armed + 4);
   }
   if (tma_cur) ph_ld ^= 1u;
   ok = __syncthreads_and(ok) != 0;
@@ -861,6 +900,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // write the sign plane. Returns false if the wait gave up.
   auto qjl_signs = [&](uint32_t hb, uint8_t* page) -> bool {
     const bool w_ok = mbar_wait(bar_qjl2(hb), (ph_qjl >> hb) & 1u);
+    if (tid == 256 && w_ok) ++done[qjl_idx(hb)];
     ph_qjl ^= 1u << hb;
     tc_fence_after();
     const uint32_t prow = tmem + 256u * hb + ((uint32_t)(32 * q4) << 16);
@@ -893,7 +933,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   while (ok && cur < ntasks) {
     const int cslot = slot, chead = h, cpg = pg;
     const int nxt = bulk128_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
-    ok = __syncthreads_and(mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u)) != 0;
+    const bool rot_ok = mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u);
+    if (tid == 0 && rot_ok) ++done[4 + bufi];
+    ok = __syncthreads_and(rot_ok) != 0;
     ph_rot ^= 1u << bufi;
     if (!ok) break;
     tc_fence_after();
@@ -980,6 +1022,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
         }
         umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
+        ++armed[qjl_idx(bufi)];
       }
       if (!half && wr) {  // planes 0-1, n and gamma of token t
         const float n = nrot * rsqrtf((float)D);
@@ -1002,7 +1045,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool tma_nxt = false;
       if (nxt < ntasks)
         tma_nxt = bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
-                               bar_ld + (bufi ^ 1u), 256, 256);
+                               bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 256);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
       // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
       const int vhalf = 1 << (lv.vb - 1);
@@ -1063,9 +1106,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         bool landed = true;
         if (tma_nxt) {
           landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
-          if (!landed) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+          if (landed) ++done[2 + (bufi ^ 1u)];
+          else set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
         }
-        if (landed) bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u));
+        if (landed)
+          bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u),
+                         armed + 4 + (bufi ^ 1u));
         else ok_p = false;
       }
       if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);
@@ -1116,6 +1162,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (ok && prev && !kpath && !qjl_signs(bufi ^ 1u, prev_page)) ok = false;
   if (!ok && (tid == 0 || tid == 256)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
+  __syncthreads();  // every count is final
+  // copies or MMAs still pending after a failed wait are waited for before shared memory and TMEM are
+  // given up; a no-op after a run without one
+  if (tid == 0 && !bulk128_drain(bar_tab, armed, done)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   __syncthreads();
   tc_fence_after();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");

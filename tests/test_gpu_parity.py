@@ -141,10 +141,7 @@ def test_append_then_decode_back_to_back(d, vb):
     print(f"back-to-back append + decode d={d} V{vb}: worst rel-L2 {worst:.2e}")
 
 
-@pytest.mark.xfail(strict=False, reason="precision margin, not correctness: at d=128 V2 query 1 of the chunk "
-                   "(1026 tokens, x10 key outliers) measured rel-L2 2.59e-3 against the 2e-3 bound; the f16 "
-                   "rounding of the query operands is the error source (d=64 carries a remainder plane for it)")
-@pytest.mark.parametrize("d,vb", [(128, 2), (64, 4)])
+@pytest.mark.parametrize("d,vb", [(128, 2), (64, 4), (256, 2)])
 def test_prefill_right_after_a_small_append(d, vb):
     """A chunk of fewer than 128 tokens that codes no page (the small-append kernel releases the next
     launch as it starts), followed at once by its prefill attention: every query's causal length comes
@@ -436,3 +433,54 @@ def test_prefill_chunk_attention(d, vb, kbits, chunk, G):
                     worst = max(worst, err)
                     assert err <= 2e-3, (i, j, h, g, err)
     print(f"prefill d={d} V{vb} K{kbits} q_per_row {Tq} G{G}: worst rel-L2 {worst:.2e}")
+
+
+def test_decode_wait_timeout_is_reported_and_the_workspace_stays_usable():
+    """Bounded waits: a test hook makes one page stage of the first split CTA of (row 0, KV head 0) get
+    neither its copy nor its expected-byte count, and its wait give up after a few polls. The call returns,
+    the status word carries TQ_DEV_ERR_TIMEOUT, every other (row, KV head) is exact, and the next decode on
+    the same workspace (hook off) matches the oracle everywhere: the kernel waited for the copies it had
+    issued and left its arrival counters at zero. Nothing faults or hangs: the abandoned stage has no copy
+    in flight."""
+    from kv_cache_quantization_quantize_gb300 import _abi
+    d, vb, Hkv, G = 128, 2, 2, 4
+    # 32 rows of 900-993 tokens (7 packed pages each): the decode plan then gives one split of 8 pages per
+    # (row, KV head), so the first page stream of a split CTA reads pages 0, 3 and 6 through stages 0-2
+    lens = [900 + 3 * i for i in range(32)]
+    B = len(lens)
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B, max_ctx=1024,
+                 seed=31)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    kb = torch.zeros(B, max(lens), Hkv, d, dtype=torch.bfloat16)
+    vbuf = torch.zeros_like(kb)
+    for i, L in enumerate(lens):
+        kk, vv = synth.kv_tokens(L, Hkv, d, seed=900 + i)
+        kb[i, :L], vbuf[i, :L] = kk, vv
+    ids = _i32(list(range(B)))
+    cache.append(0, kb.to(DEV), vbuf.to(DEV), ids, _i32(lens))
+    q = synth.queries(B, Hkv * G, d, seed=32)
+    ws = cache.workspace(B)
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    lib = _abi.load()
+    refs = [_oracle_decode(cache, 0, i, q[i], tables) for i in range(B)]
+    for stage in (0, 2):
+        assert lib.tq_debug_decode_wait_fault(stage, 8) == _abi.TQ_OK
+        try:
+            out = cache.decode(0, q.to(DEV), ids, workspace=ws).cpu().numpy()
+        finally:
+            assert lib.tq_debug_decode_wait_fault(-1, 0) == _abi.TQ_OK
+        assert cache.check_status() & _abi.TQ_DEV_ERR_TIMEOUT
+        for i in range(B):
+            for hq in range(Hkv * G):
+                if i == 0 and hq < G:
+                    continue  # the unit whose wait gave up: unspecified
+                assert rel_l2(out[i, hq], refs[i][hq]) <= 2e-3, (stage, i, hq)
+        out = cache.decode(0, q.to(DEV), ids, workspace=ws).cpu().numpy()
+        assert cache.check_status() == 0
+        for i in range(B):
+            for hq in range(Hkv * G):
+                assert rel_l2(out[i, hq], refs[i][hq]) <= 2e-3, ("after", stage, i, hq)
+    assert lib.tq_debug_decode_wait_fault(7, 8) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_decode_wait_fault(0, 0) == _abi.TQ_ERR_INVALID_ARG

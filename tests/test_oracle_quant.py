@@ -158,3 +158,29 @@ def test_cos_sim_report_pins():
     expect = np.sqrt(1.0 - d * mse_distortion(d, c, t))  # per-coordinate distortion x d = unit-vector D
     assert abs(rep["key_cos_mse"] - expect) < 3e-3, (rep, expect)
     assert rep["key_cos_qjl"] < rep["key_cos_mse"]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_dequantized_key_inner_product_is_unbiased(d):
+    """The QJL term makes the key estimate unbiased ([Guide] §二 step 3): for a unit vector y and
+    y_hat = c[idx] + sqrt(pi/2)/d * gamma * S^T sign(S r), E_S <y, y_hat> = <y, c> + <c, r> + gamma^2 =
+    ||c + r||^2 = 1, since E[sign(s.r) s] = sqrt(2/pi) r / ||r|| for s ~ N(0, I). Over 2000 independent S
+    (one unit key each, through dequantize_keys with n = 1) the mean of <k, k_hat> must be 1 within 3
+    standard errors. A wrong constant in the QJL term (e.g. sqrt(2/pi)/d: mean ~0.96) or a flipped sign
+    (mean ~0.77) fails, and so does leaving the term out (mean 1 - D ~ 0.88)."""
+    from oracle import dequantize_keys, gaussian_matrix_bf16, lloyd_max_codebook
+    c, t = lloyd_max_codebook(d, 2)
+    D = rademacher_signs(3, d)
+    rng = np.random.default_rng(d)
+    vals = []
+    for seed in range(2000):
+        S = gaussian_matrix_bf16(10_000 + seed, d)
+        k = rng.standard_normal((1, d))
+        k /= np.linalg.norm(k)
+        rec = quantize_keys(k, D, S, c, t)
+        rec.norm[:] = np.float16(1.0)  # exact unit norm, so <k, k_hat> = <y, y_hat>
+        vals.append(float(np.sum(k * dequantize_keys(rec, D, S, c, with_qjl=True))))
+    vals = np.asarray(vals)
+    se = vals.std(ddof=1) / np.sqrt(len(vals))
+    assert abs(vals.mean() - 1.0) <= 3 * se + 2e-3, (vals.mean(), se)  # 2e-3: fp16 gamma and bf16 S
+    assert se < 0.01

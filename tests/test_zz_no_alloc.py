@@ -81,3 +81,41 @@ def test_noalloc_rejects_scratch_above_its_limit():
     assert "exceeds" in msg and str(4 << 20) in msg
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)  # nothing was launched
+
+
+def _cache_with_history(max_seqs, lens, Hkv, d, seed):
+    cfg = config(head_dim=d, value_bits=2, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * 4, max_seqs=max_seqs,
+                 max_ctx=1200, seed=seed)
+    cache = TurboQuantCache(cfg)
+    B = len(lens)
+    k = torch.zeros(B, max(lens), Hkv, d, dtype=torch.bfloat16)
+    v = torch.zeros_like(k)
+    for i, L in enumerate(lens):
+        kk, vv = synth.kv_tokens(L, Hkv, d, seed=seed * 10 + i, outliers=("random", 4, 10.0))
+        k[i, :L], v[i, :L] = kk, vv
+    ids = torch.arange(B, dtype=torch.int32, device=DEV)
+    cache.append(0, k.to(DEV), v.to(DEV), ids, torch.tensor(lens, dtype=torch.int32, device=DEV))
+    q = synth.queries(B, Hkv * 4, d, seed=seed).to(DEV)
+    return cache, ids, q
+
+
+def test_noalloc_alternating_contexts_of_different_shapes():
+    """The one scratch array serves every context. Calls alternate between a context with one sequence
+    slot and one with sixteen (8 KV heads each): the small context's partials must never land on the
+    large context's arrival counters. Both match the workspace decode on every call."""
+    d, Hkv = 128, 8
+    big, ids_b, q_b = _cache_with_history(16, [300 + 37 * i for i in range(16)], Hkv, d, seed=5)
+    small, ids_s, q_s = _cache_with_history(1, [900], Hkv, d, seed=6)
+    ref_b = big.decode(0, q_b, ids_b)
+    ref_s = small.decode(0, q_s, ids_s)
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for cache, q, ids, ref in ((big, q_b, ids_b, ref_b), (small, q_s, ids_s, ref_s), (big, q_b, ids_b, ref_b)):
+            out = torch.full_like(ref, float("nan"))
+            assert _noalloc(cache, 0, q, out, ids) == _abi.TQ_OK, _abi.load().tq_last_error()
+            torch.cuda.synchronize()
+            assert torch.isfinite(out).all()
+            for i in range(q.shape[0]):
+                for h in range(q.shape[1]):
+                    assert _rel_l2(out[i, h], ref[i, h]) <= 2e-3
+    assert big.check_status() == 0 and small.check_status() == 0
