@@ -70,9 +70,70 @@ def measured_peaks():
 
 
 # --------------------------------------------------------------------------------------------
-# nvidia-smi clock sampler (runs during warm-up and the timed region)
+# clocks during the timed region: NVML read-only queries polled every millisecond (nvidia-smi's
+# sampling period is longer than a short timed region); nvidia-smi as a fallback
 # --------------------------------------------------------------------------------------------
-class ClockSampler:
+class NvmlClocks:
+    """Polls SM clock, power and the clock-event reasons of one GPU through NVML (read-only queries)."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid, period_s=0.001):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) != 0:
+            raise RuntimeError(f"no NVML device {uuid}")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value)
+        self.period = period_s
+        self.samples = []
+        self._stop = threading.Event()
+        self.thread = None
+
+    def _one(self):
+        ct = self.ct
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ct.byref(mw))
+        self.reasons_fn(self.h, ct.byref(rs))
+        return time.time(), float(mhz.value), mw.value / 1000.0, int(rs.value)
+
+    def _run(self):
+        while not self._stop.is_set():
+            self.samples.append(self._one())
+            time.sleep(self.period)
+
+    def start(self):
+        self.thread = threading.Thread(target=self._run, daemon=True)
+        self.thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [x for x in self.samples if t0 <= x[0] <= t1]
+        window = "timed"
+        if not inside:
+            inside, window = self.samples[-3:], "after the timed region (no sample inside it)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0, "source": "nvml"}
+        reasons = sorted({name for x in inside for bit, name in self.REASONS.items() if x[3] & bit})
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(x[1] for x in inside), "power_w_max": max(x[2] for x in inside),
+                "reasons": reasons, "samples": len(inside), "window": window, "source": "nvml, 1 ms polling"}
+
+
+class SmiClocks:
+    """nvidia-smi sampler (fallback when NVML cannot be loaded)."""
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -128,7 +189,18 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for s in inside for i in range(4) if s[5 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside), "window": window}
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(inside), "window": window,
+                "source": "nvidia-smi"}
+
+
+def clock_sampler(dev):
+    import torch
+    uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    try:
+        return NvmlClocks(uuid)
+    except Exception:
+        return SmiClocks(uuid)
 
 
 # --------------------------------------------------------------------------------------------
@@ -146,18 +218,51 @@ def aggregate_over_ranks(ms, units, world, device):
     return t_max, units * world / (t_max * 1e-3)
 
 
-def bench_config(world, mode="hybrid", step_mb=785):
-    cfg = {"workload": WL["name"], "layers": WL["layers"], "q_heads": WL["hq"], "kv_heads": WL["hkv"],
-           "head_dim": WL["d"], "batch_per_gpu": WL["batch"], "context": WL["ctx"], "key_bits": WL["kb"], "value_bits": WL["vb"],
-           "ring": 128, "l2": f"inputs larger than L2 (~{step_mb:.0f} MB of packed records per step vs 129 MB L2)",
-           "parallelism": "replicas" if world > 1 else "single GPU",
-           "step": f"append 1 token + hybrid decode attention, all {WL['layers']} layers, one CUDA graph replay"}
-    if WL["lens"] is not None:
-        cfg.update(context=f"ragged, uniform in [{WL['lens'][0]}, {WL['lens'][1]}] (seed {WL['seed']})")
+def record_bytes(wl):
+    """Canonical key + value record bytes of one token and KV head."""
+    d = wl["d"]
+    return (d * (wl["kb"] - 1) // 8 + d // 8 + 4) + (d * wl["vb"] // 8 + d // 16)
+
+
+def nominal_step_bytes(wl, mode="hybrid"):
+    """Algorithmic bytes of one decode step at the workload's nominal contexts (packed records + ring +
+    q + out, all layers); a description of the workload, identical in both arms."""
+    lens = (synth_lengths(wl) if wl["lens"] is not None else [wl["ctx"]] * wl["batch"])
+    total = 0
+    for L in lens:
+        packed = L if mode == "full_tq" else 128 * ((L - 1) // 128)
+        total += wl["layers"] * (wl["hkv"] * (packed * record_bytes(wl) + (L - packed) * wl["d"] * 4)
+                                 + wl["hq"] * wl["d"] * 6)
+    return total
+
+
+def synth_lengths(wl):
+    from kv_cache_quantization_quantize_gb300 import synth
+    return synth.ragged_lengths(wl["batch"], wl["lens"][0], wl["lens"][1], seed=wl["seed"])
+
+
+def workload_config(wl, mode="hybrid"):
+    cfg = {"workload": wl["name"], "layers": wl["layers"], "q_heads": wl["hq"], "kv_heads": wl["hkv"],
+           "head_dim": wl["d"], "batch_per_gpu": wl["batch"], "context": wl["ctx"], "key_bits": wl["kb"],
+           "value_bits": wl["vb"], "ring": 128,
+           "l2": f"inputs larger than L2 ({nominal_step_bytes(wl, mode) / 1e6:.0f} MB of packed records per step vs "
+                 f"129 MB L2)",
+           "step": f"append 1 token + hybrid decode attention, all {wl['layers']} layers"}
+    if wl["lens"] is not None:
+        cfg.update(context=f"ragged, uniform in [{wl['lens'][0]}, {wl['lens'][1]}] (seed {wl['seed']})")
     if mode == "full_tq":
-        cfg.update(workload=WL["name"] + ", full_tq mode", ring=0, mode="full_tq",
-                   step="append 1 token (quantised at once) + decode over packed tokens only, all 32 layers, "
-                        "one CUDA graph replay")
+        cfg.update(workload=wl["name"] + ", full_tq mode", ring=0, mode="full_tq",
+                   step=f"append 1 token (quantised at once) + decode over packed tokens only, all {wl['layers']} "
+                        "layers")
+    return cfg
+
+
+def bench_config(world, mode="hybrid", layout="contiguous"):
+    """The `config` of the JSON line. It depends on the workload and flags only, so both arms print the
+    same one."""
+    cfg = dict(workload_config(WL, mode), parallelism="replicas" if world > 1 else "single GPU")
+    if layout == "paged":
+        cfg["layout"] = "paged (scrambled block table)"
     return cfg
 
 
@@ -201,6 +306,210 @@ def profiled_traffic(path=DECODE_PROFILE):
         return None
 
 
+def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
+    """One decode workload: prefill the cache, capture the step (append 1 token + decode, every layer) as
+    a CUDA graph, time K replays after W warm-up replays, and time the split-K kernel alone. With
+    `headline`, also the two end-to-end figures (graph replay and eager per-layer API calls, both with
+    pinned-host copies inside the timed region)."""
+    import torch
+    import torch.distributed as dist
+    L_layers, Hq, Hkv, d, B, ctx, vb = wl["layers"], wl["hq"], wl["hkv"], wl["d"], wl["batch"], wl["ctx"], wl["vb"]
+    n_e2e_warm = 2
+    # tokens appended after prefill by all passes (eager step, warm-up, timed, both e2e passes)
+    extra = 1 + W + K + (2 * (n_e2e_warm + K) if headline else 0) + 8
+    lens = synth_lengths(wl) if wl["lens"] is not None else [ctx] * B  # context of each row at the first timed step
+    max_ctx = max(lens) + extra
+    full = args.mode == "full_tq"
+    paged = args.layout == "paged" and headline
+    max_pages = (max_ctx + 127) // 128
+    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=wl["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
+                     max_seqs=B, max_ctx=max_ctx, seed=1, mode=args.mode if headline else "hybrid",
+                     n_blocks=B * max_pages if paged else 0)
+    cache = tqm.TurboQuantCache(cfg, device=dev)
+    ids = torch.arange(B, dtype=torch.int32, device=dev)
+    if paged:  # every page of every row mapped to a block of a seeded permutation of the pool
+        perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
+        cache.block_table.copy_(perm.view(B, max_pages).to(dev))
+    # after the eager step and the W warm-up replays, the first timed step of row b attends lens[b] tokens
+    L0 = [n - W - 2 for n in lens]
+    for l in range(L_layers):
+        k, v = synth.kv_tokens(max(L0), Hkv, d, seed=wl["seed"] * 1000 + l, dist=wl["dist"], outliers=wl["outliers"],
+                               device=dev)
+        for b in range(B):  # one row per call: rows share the layer's tokens, each with its own length
+            cache.append(l, k[None], v[None], ids[b:b + 1], torch.full((1,), L0[b], dtype=torch.int32, device=dev))
+        del k, v
+    torch.cuda.synchronize()
+    if cache.check_status():
+        raise RuntimeError("device status after prefill")
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    knew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    vnew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
+    qs = torch.randn((L_layers, B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
+    outs = torch.empty((L_layers, B, Hq, d), dtype=torch.float32, device=dev)
+    ones = torch.ones(B, dtype=torch.int32, device=dev)
+    ws = cache.workspace(B, max_ctx)
+    s = torch.cuda.Stream(device=dev)
+
+    def step():
+        for l in range(L_layers):
+            cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
+            cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        step()  # eager: sets kernel attributes before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    launches_per_step = L_layers * 2  # small append + split-K decode (query prep and combine inside) per layer
+
+    sampler = clock_sampler(dev)
+    sampler.start()
+    time.sleep(0.05)
+    with torch.cuda.stream(s):
+        for _ in range(W):
+            g.replay()
+    torch.cuda.synchronize()
+    L_first = [cache.state(0, b)[0] + 1 for b in range(B)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host0 = time.time()
+    ev0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(K):
+            g.replay()
+    ev1.record(s)
+    ev1.synchronize()
+    t_host1 = time.time()
+    torch.cuda.synchronize()
+    ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        dist.barrier()
+    sampler.stop()
+    clocks = sampler.summary(t_host0, t_host1)
+    status = cache.check_status()
+    ctx_tokens = sum(Lb + i for Lb in L_first for i in range(K))  # each step attends every row's full context
+    t_max, value = aggregate_over_ranks(ms, ctx_tokens, world, dev)  # max over ranks; whole-job throughput
+    ms_per_step = t_max / K
+
+    # algorithmic bytes per step: packed records + ring (K,V bf16) + q + out, all layers
+    rec = record_bytes(wl)
+    step_bytes = 0.0
+    for Lb in L_first:
+        Lmid = Lb + (K - 1) / 2.0
+        packed = Lmid if full else 128 * ((Lmid - 1) // 128)
+        ring = Lmid - packed
+        step_bytes += L_layers * (Hkv * (packed * rec + ring * d * 2 * 2) + Hq * d * (2 + 4))
+    hbm_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+
+    # ---- the split-K kernel alone: a graph of its per-layer launches ----
+    for l in range(L_layers):
+        cache.decode_phase(0, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=s):
+        for l in range(L_layers):
+            cache.decode_phase(1, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            g2.replay()
+    torch.cuda.synchronize()
+    kern_bytes = 0
+    for b in range(B):
+        Lk, Fk = cache.state(0, b)
+        packed_k = 128 * ((Lk - 1) // 128) + Fk
+        ring_k = Lk - packed_k
+        kern_bytes += Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(K, 10)
+    e0.record(s)
+    with torch.cuda.stream(s):
+        for _ in range(reps):
+            g2.replay()
+    e1.record(s)
+    torch.cuda.synchronize()
+    kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
+    kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
+    roof = {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
+            "achieved": kern_gbs, "peak": peak, "unit": "GB/s", "frac": kern_gbs / peak, "peak_kind": peak_kind,
+            "bytes_per_launch": kern_bytes, "us_per_launch": kern_us, "frac_of_8TBps": kern_gbs / NOMINAL_HBM_GBS}
+    res = {"workload": wl["name"], "value": value, "unit": UNIT, "ms_per_step": ms_per_step, "steps": K,
+           "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
+           "pct_of_measured_hbm": 100.0 * hbm_gbs / peak, "step_bytes": step_bytes, "roofline": roof,
+           "clocks": clocks, "gpu_launches": launches_per_step * K, "device_status": status}
+    del g2
+    if headline:
+        res.update(measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_e2e_warm, world, B,
+                               L_layers))
+    del g
+    del cache, knew, vnew, qs, outs, ws
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_warm, world, B, L_layers):
+    """The step end to end with host buffers: every step copies q, k and v from pinned host memory to the
+    device and the outputs back, inside the timed region. `e2e` replays the captured graph between the
+    copies; `e2e_api` calls tq_quantize_append and tq_decode_attention per layer through the Python
+    binding (ctypes -> C ABI), with no graph."""
+    import torch
+    hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
+    hk = torch.empty(knew.shape, dtype=knew.dtype, pin_memory=True)
+    hv = torch.empty(vnew.shape, dtype=vnew.dtype, pin_memory=True)
+    ho = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
+    hq.copy_(qs)
+    hk.copy_(knew)
+    hv.copy_(vnew)
+    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
+    d2h = ho.numel() * 4
+
+    def graph_step():
+        with torch.cuda.stream(s):
+            qs.copy_(hq, non_blocking=True)
+            knew.copy_(hk, non_blocking=True)
+            vnew.copy_(hv, non_blocking=True)
+            g.replay()
+            ho.copy_(outs, non_blocking=True)
+
+    def api_step():
+        with torch.cuda.stream(s):
+            qs.copy_(hq, non_blocking=True)
+            knew.copy_(hk, non_blocking=True)
+            vnew.copy_(hv, non_blocking=True)
+            for l in range(L_layers):
+                cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
+                cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+            ho.copy_(outs, non_blocking=True)
+
+    out = {}
+    for key, fn, launches in (("e2e", graph_step, "one CUDA graph replay"),
+                              ("e2e_api", api_step, "per-layer tq_quantize_append + tq_decode_attention calls")):
+        for _ in range(n_warm):
+            fn()
+        torch.cuda.synchronize()
+        L0 = [cache.state(0, b)[0] + 1 for b in range(B)]
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(s)
+        for _ in range(K):
+            fn()
+        f1.record(s)
+        torch.cuda.synchronize()
+        e_ms = f0.elapsed_time(f1)
+        out[key] = {"value": sum(Lb + i for Lb in L0 for i in range(K)) * world / (e_ms * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e_ms / K,
+                    "launch": launches}
+        if cache.check_status():
+            out[key]["device_status"] = "non-zero"
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -219,199 +528,43 @@ def run_ours(args):
     from kv_cache_quantization_quantize_gb300 import synth
 
     K, W = args.steps, args.warmup
-    L_layers, Hq, Hkv, d, B, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["batch"], WL["ctx"], WL["vb"]
-    n_e2e_warm = 2
-    extra = 1 + W + K + (n_e2e_warm + K) + K + 8  # tokens appended after prefill by all passes
-    # context of each row at the first timed step
-    lens = (synth.ragged_lengths(B, WL["lens"][0], WL["lens"][1], seed=WL["seed"]) if WL["lens"] is not None
-            else [ctx] * B)
-    max_ctx = max(lens) + extra
-    full = args.mode == "full_tq"
-    paged = args.layout == "paged"
-    max_pages = (max_ctx + 127) // 128
-    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
-                     max_seqs=B,
-                     max_ctx=max_ctx, seed=1, mode=args.mode, n_blocks=B * max_pages if paged else 0)
-    cache = tqm.TurboQuantCache(cfg, device=dev)
-    ids = torch.arange(B, dtype=torch.int32, device=dev)
-    if paged:  # every page of every row mapped to a block of a seeded permutation of the pool
-        perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
-        cache.block_table.copy_(perm.view(B, max_pages).to(dev))
-    # after the eager step and the W warm-up replays, the first timed step of row b attends lens[b] tokens
-    L0 = [n - W - 2 for n in lens]
-    for l in range(L_layers):
-        k, v = synth.kv_tokens(max(L0), Hkv, d, seed=WL["seed"] * 1000 + l, dist=WL["dist"], outliers=WL["outliers"],
-                               device=dev)
-        for b in range(B):  # one row per call: rows share the layer's tokens, each with its own length
-            cache.append(l, k[None], v[None], ids[b:b + 1], torch.full((1,), L0[b], dtype=torch.int32, device=dev))
-        del k, v
-    torch.cuda.synchronize()
-    if cache.check_status():
-        raise RuntimeError("device status after prefill")
-    gen = torch.Generator(device=dev)
-    gen.manual_seed(7)
-    knew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
-    vnew = torch.randn((L_layers, B, 1, Hkv, d), generator=gen, device=dev).to(torch.bfloat16)
-    qs = torch.randn((L_layers, B, Hq, d), generator=gen, device=dev).to(torch.bfloat16)
-    outs = torch.empty((L_layers, B, Hq, d), dtype=torch.float32, device=dev)
-    ones = torch.ones(B, dtype=torch.int32, device=dev)
-    ws = cache.workspace(B, max_ctx)
-
-    def step():
-        for l in range(L_layers):
-            cache.append(l, knew[l], vnew[l], ids, ones)
-            cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws)
-
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        step()  # eager: sets kernel attributes before capture
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=s):
-        step()
-    launches_per_step = L_layers * 2  # small append + split-K decode (query prep and combine inside) per layer
-
-    gpu_id = local
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
-    except Exception:
-        pass
-    sampler = ClockSampler(gpu_id)
-    sampler.start()
-    time.sleep(0.3)
-    for _ in range(W):
-        g.replay()
-    torch.cuda.synchronize()
-    L_first = [cache.state(0, b)[0] + 1 for b in range(B)]
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    t_host0 = time.time()
-    ev0.record()
-    for _ in range(K):
-        g.replay()
-    ev1.record()
-    torch.cuda.synchronize()
-    t_host1 = time.time()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        dist.barrier()
-    time.sleep(0.2)
-    sampler.stop()
-    clocks = sampler.summary(t_host0, t_host1)
-    status = cache.check_status()
-    ctx_tokens = sum(Lb + i for Lb in L_first for i in range(K))  # each step attends every row's full context
-    # max over ranks of the timed region; whole-job throughput
-    t_max, value = aggregate_over_ranks(ms, ctx_tokens, world, dev)
-    ms_per_step = t_max / K
-
-    # algorithmic bytes per step: packed K3/V2 records + ring (K,V bf16) + q + out, all layers
-    rec = (d * (WL["kb"] - 1) // 8 + d // 8 + 4) + (d * vb // 8 + d // 16)
-    step_bytes = 0.0
-    for Lb in L_first:
-        Lmid = Lb + (K - 1) / 2.0
-        packed = Lmid if full else 128 * ((Lmid - 1) // 128)
-        ring = Lmid - packed
-        step_bytes += L_layers * (Hkv * (packed * rec + ring * d * 2 * 2) + Hq * d * (2 + 4))
-    hbm_gbs = step_bytes / (ms_per_step * 1e-3) / 1e9
-    peak, peak_kind = measured_peaks()
-
-    # ---- roofline of the split-K kernel alone: graph of its 32 per-layer launches ----
-    for l in range(L_layers):
-        cache.decode_phase(0, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws)
-    torch.cuda.synchronize()
-    g2 = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g2, stream=s):
-        for l in range(L_layers):
-            cache.decode_phase(1, l, qs[l], ids, outs[l], max_ctx_hint=max_ctx, workspace=ws)
-    for _ in range(3):
-        g2.replay()
-    torch.cuda.synchronize()
-    kern_bytes = 0
-    for b in range(B):
-        Lk, Fk = cache.state(0, b)
-        packed_k = 128 * ((Lk - 1) // 128) + Fk
-        ring_k = Lk - packed_k
-        kern_bytes += Hkv * (packed_k * rec + ring_k * d * 2 * 2) + Hq * d * (2 + 4)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(K, 10)
-    e0.record()
-    for _ in range(reps):
-        g2.replay()
-    e1.record()
-    torch.cuda.synchronize()
-    kern_us = e0.elapsed_time(e1) * 1e3 / (reps * L_layers)
-    kern_gbs = kern_bytes / (kern_us * 1e-6) / 1e9
-    # the committed ncu summary is of the default (hybrid, contiguous, head_dim 128) step
+    head = measure_decode(tqm, synth, dev, WL, args, K, W, world, headline=True)
+    full, paged = args.mode == "full_tq", args.layout == "paged"
     traffic = None if full or paged or WL["name"] != WORKLOADS["llama8b"]["name"] else profiled_traffic()
+    head["roofline"]["traffic"] = traffic
+    peak, _ = measured_peaks()
 
-    # ---- end to end through the public API with pinned host buffers ----
-    hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
-    hk = torch.empty(knew.shape, dtype=knew.dtype, pin_memory=True)
-    hv = torch.empty(vnew.shape, dtype=vnew.dtype, pin_memory=True)
-    ho = torch.empty(outs.shape, dtype=outs.dtype, pin_memory=True)
-    hq.copy_(qs)
-    hk.copy_(knew)
-    hv.copy_(vnew)
-    h2d = hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2
-    d2h = ho.numel() * 4
-
-    def e2e_step():
-        with torch.cuda.stream(s):
-            qs.copy_(hq, non_blocking=True)
-            knew.copy_(hk, non_blocking=True)
-            vnew.copy_(hv, non_blocking=True)
-            g.replay()
-            ho.copy_(outs, non_blocking=True)
-
-    for _ in range(n_e2e_warm):
-        e2e_step()
-    torch.cuda.synchronize()
-    L_e2e = [cache.state(0, b)[0] + 1 for b in range(B)]
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(s)
-    for _ in range(K):
-        e2e_step()
-    f1.record(s)
-    torch.cuda.synchronize()
-    e2e_ms = f0.elapsed_time(f1)
-    e2e_value = sum(Lb + i for Lb in L_e2e for i in range(K)) * world / (e2e_ms * 1e-3)
-    if cache.check_status():
-        status |= 1 << 16
-
-    # ---- bulk prefill quantise (tok/s over all layers and heads) ----
     quant = None
     if not args.skip_quantize:
-        del g, g2
         quant = bench_quantize(tqm, synth, dev, args, peak)
+    # the other decode workloads, each with its own cache (freed after it), as nested records
+    nested = {}
+    if args.nested and WL["name"] == WORKLOADS["llama8b"]["name"] and not full and not paged:
+        for name, over in (("batched", {}), ("d256", {}), ("d256_v4", {"vb": 4}), ("long", {})):
+            wl = dict(WORKLOADS[name.split("_")[0]], **over)
+            if over:
+                wl["name"] = wl["name"].replace("K3/V2", f"K3/V{over['vb']}")
+            r = measure_decode(tqm, synth, dev, wl, args, max(10, min(K, 50)), W, world, headline=False)
+            r["config"] = workload_config(wl)
+            nested[name] = r
 
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
-        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16 tensor-core products, f32 accumulate and softmax", "data": "synthetic",
-        "config": dict(bench_config(world, args.mode, step_bytes / 1e6),
-                       **({"layout": "paged (scrambled block table)"} if paged else {})),
-        "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
-        "pct_of_measured_hbm": 100.0 * hbm_gbs / peak,
-        "roofline": {"kernel": "k_decode (split-K decode over packed pages + ring split)", "bound": "hbm",
-                     "achieved": kern_gbs, "peak": peak, "unit": "GB/s", "frac": kern_gbs / peak,
-                     "peak_kind": peak_kind, "traffic": traffic, "bytes_per_launch": kern_bytes,
-                     "us_per_launch": kern_us, "frac_of_8TBps": kern_gbs / NOMINAL_HBM_GBS},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms / K},
-        "gpu_launches": launches_per_step * K,
-        "clocks": clocks,
-        "device_status": status,
+        "config": bench_config(world, args.mode, args.layout),
+        "hbm_gbs": head["hbm_gbs"], "pct_of_8TBps": head["pct_of_8TBps"],
+        "pct_of_measured_hbm": head["pct_of_measured_hbm"],
+        "roofline": head["roofline"], "e2e": head["e2e"], "e2e_api": head["e2e_api"],
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "device_status": head["device_status"],
     }
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
         line["quantize"] = quant
+    if nested:
+        line["workloads"] = nested
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged
-            and WL["kb"] == 3 and args.head_dim == 128):  # oracle sample of this workload
+            and WL["kb"] == 3 and args.head_dim == 128):  # the oracle on this workload
         line["cpu_baseline"] = cpu_baseline(args)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -442,16 +595,21 @@ def bench_quantize(tqm, synth, dev, args, peak):
         for l in range(L_layers):
             qc.append(l, k, v, ids, nn)
 
-    for _ in range(2):
+    for _ in range(3):
         one_pass()
     torch.cuda.synchronize()
-    reps = max(1, min(args.steps, 5))
+    reps = 20
+    sampler = clock_sampler(dev)
+    sampler.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
     e0.record()
     for _ in range(reps):
         one_pass()
     e1.record()
-    torch.cuda.synchronize()
+    e1.synchronize()
+    t1 = time.time()
+    sampler.stop()
     ms = e0.elapsed_time(e1) / reps
     if qc.check_status():
         raise RuntimeError("device status after quantise")
@@ -461,9 +619,10 @@ def bench_quantize(tqm, synth, dev, args, peak):
     bytes_pass = L_layers * Hkv * (T * d * 2 * 2 + packed * rec + ring * d * 2 * 2)
     gbs = bytes_pass / (ms * 1e-3) / 1e9
     return {"tok_s": T / (ms * 1e-3), "token_head_layers_per_s": T * Hkv * L_layers / (ms * 1e-3),
-            "ms_per_pass": ms, "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K3/V{vb}",
+            "ms_per_pass": ms, "passes": reps, "clocks": sampler.summary(t0, t1), "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K3/V{vb}",
             "path": ("tcgen05 rotation (H diag(D)) and QJL projection (bf16 hi/lo) into TMEM, thread-per-token "
-                     "coding, TMA page loads" if d == 128 else "CUDA-core quantise kernel (fp32 FMA QJL projection)"),
+                     "coding, TMA page loads" if d == 128 and PREFILL["kb"] == 3 else
+                     "CUDA-core quantise kernel (QJL projection as an f16 mma.sync GEMM per 32-token block)"),
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
 
 
@@ -603,23 +762,28 @@ def profile_quantize(passes):
 # --------------------------------------------------------------------------------------------
 # oracle timing (cpu_baseline leg and --impl reference)
 # --------------------------------------------------------------------------------------------
-def oracle_sample_setup():
-    """Packed records + ring of one (layer 0, KV head 0) unit of the workload, built by the oracle."""
+def oracle_unit_setup(k, v):
+    """Packed records + ring of one (layer, KV head) unit, built by the oracle from that unit's fp64 K and V
+    [ctx, d] (the unit's context), with the new decode token taken as the last one."""
     import numpy as np
     import oracle
-    from kv_cache_quantization_quantize_gb300 import synth
-    d, ctx, Hkv = WL["d"], WL["ctx"], WL["hkv"]
-    k, v = synth.kv_tokens(ctx, Hkv, d, seed=1000, dist=WL["dist"], outliers=WL["outliers"])
-    k = k[:, 0].double().numpy()
-    v = v[:, 0].double().numpy()
+    d, ctx, Hkv = WL["d"], k.shape[0], WL["hkv"]
     D = oracle.rademacher_signs(1, d)
     S = oracle.gaussian_matrix_bf16(1, d)
-    c, t = oracle.lloyd_max_codebook(d, 2)
+    c, t = oracle.lloyd_max_codebook(d, WL["kb"] - 1)
     Np, R = oracle.history_split(ctx)
     keys = oracle.quantize_keys(k[:Np], D, S, c, t)
     vals = oracle.quantize_values(v[:Np], D, WL["vb"])
     q = np.random.default_rng(0).standard_normal((WL["hq"] // Hkv, d))
     return dict(keys=keys, vals=vals, rk=k[Np:], rv=v[Np:], q=q, D=D, S=S, c=c, t=t, k_new=k[-1:], v_new=v[-1:])
+
+
+def oracle_sample_setup():
+    """Records + ring of one (layer 0, KV head 0) unit of the workload."""
+    from kv_cache_quantization_quantize_gb300 import synth
+    k, v = synth.kv_tokens(WL["ctx"], WL["hkv"], WL["d"], seed=WL["seed"] * 1000, dist=WL["dist"],
+                           outliers=WL["outliers"])
+    return oracle_unit_setup(k[:, 0].double().numpy(), v[:, 0].double().numpy())
 
 
 def oracle_unit_step(st):
@@ -640,33 +804,37 @@ def oracle_sample_reps():
     return max(10, 150 * 32768 // WL["ctx"])
 
 
-def _oracle_child(threads, args):
-    """Runs the oracle sample in a child process limited to `threads` BLAS/OpenMP threads."""
+def _oracle_child(threads, args, mode="--oracle-sample", arg=None):
+    """Runs an oracle timing in a child process limited to `threads` BLAS/OpenMP threads."""
     env = dict(os.environ)
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         env[var] = str(threads)
     env["CUDA_VISIBLE_DEVICES"] = ""
-    cmd = [sys.executable, os.path.abspath(__file__), "--oracle-sample", str(oracle_sample_reps()),
+    cmd = [sys.executable, os.path.abspath(__file__), mode, str(arg if arg is not None else oracle_sample_reps()),
            "--workload", args.workload]
     if args.value_bits:
         cmd += ["--value-bits", str(args.value_bits)]
-    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=900)
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def cpu_baseline(args):
-    """Times the oracle in child processes so that their thread counts are known: all host cores (the
-    reported value) and one thread."""
+    """Times the oracle in child processes so that their thread counts are known. On the batch-1 32K
+    workload the all-core figure is one full decode step (every layer and KV head, each with its own
+    records); elsewhere, and on one thread, a sample of one (layer, KV head, row) unit extrapolated over
+    the step's units."""
     cores = os.cpu_count() or 1
+    full = WL["name"] == WORKLOADS["llama8b"]["name"]
     try:
-        res = _oracle_child(cores, args)
+        res = _oracle_child(cores, args, "--oracle-full-step", 1) if full else _oracle_child(cores, args)
     except Exception as e:  # report, do not fail the GPU line
         return {"value": None, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": f"failed: {e}"}
     line = {"value": res["value"], "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": res["sample"], "seconds": res["seconds"]}
     try:
         one = _oracle_child(1, args)
-        line["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1, "seconds": one["seconds"]}
+        line["single_thread"] = {"value": one["value"], "unit": UNIT, "cores": 1, "seconds": one["seconds"],
+                                 "sample": one["sample"]}
     except Exception as e:
         line["single_thread"] = {"value": None, "note": f"failed: {e}"}
     return line
@@ -686,6 +854,31 @@ def oracle_sample_main(reps):
                       "sample": f"{reps} decode steps of 1 layer x 1 KV head x 1 row ({WL['hq'] // WL['hkv']} query "
                                 f"heads, {WL['ctx']} context, head_dim {WL['d']}) timed; extrapolated linearly x{units} "
                                 f"({WL['layers']} layers x {WL['hkv']} KV heads x {WL['batch']} rows)"}))
+
+
+def oracle_full_step_main(steps):
+    """Whole decode steps of the batch-1 workload by the oracle: the records of every (layer, KV head) are
+    built first (untimed, per-layer inputs seeded like the GPU arm's), then `steps` steps are timed, each
+    quantising every unit's new token and attending over every unit's own records and ring."""
+    from kv_cache_quantization_quantize_gb300 import synth
+    units = []
+    for l in range(WL["layers"]):
+        k, v = synth.kv_tokens(WL["ctx"], WL["hkv"], WL["d"], seed=WL["seed"] * 1000 + l, dist=WL["dist"],
+                               outliers=WL["outliers"])
+        k, v = k.double().numpy(), v.double().numpy()
+        for h in range(WL["hkv"]):
+            units.append(oracle_unit_setup(k[:, h].copy(), v[:, h].copy()))
+        del k, v
+    oracle_unit_step(units[0])  # warm
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        for st in units:
+            oracle_unit_step(st)
+    dt = (time.perf_counter() - t0) / steps
+    print(json.dumps({"value": WL["batch"] * WL["ctx"] / dt, "seconds": dt * steps,
+                      "sample": f"{steps} full decode step(s): {WL['layers']} layers x {WL['hkv']} KV heads, each "
+                                f"with its own records ({WL['ctx']} context, {WL['hq'] // WL['hkv']} query heads, "
+                                f"head_dim {WL['d']}); not extrapolated"}))
 
 
 def run_reference(args):
@@ -708,7 +901,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * units * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": bench_config(world),
+            "config": bench_config(world, args.mode, args.layout),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -717,7 +910,7 @@ def run_reference(args):
 def main():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--steps", type=int, default=1400, help="timed decode steps (1400: about 1 s at batch 1)")
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--skip-quantize", action="store_true")
@@ -739,7 +932,10 @@ def main():
                    help="time a comparison codec over the 32K-token KV cache instead (one JSON line of its own)")
     p.add_argument("--codec-layers", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-nested", dest="nested", action="store_false",
+                   help="skip the nested records of the other decode workloads (batched, d256, d256_v4, long)")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
+    p.add_argument("--oracle-full-step", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
                    help="only run one layer of the prefill quantisation PASSES times (for profilers)")
     args = p.parse_args()
@@ -765,6 +961,8 @@ def main():
         bench_codec(args)
     elif args.oracle_sample:
         oracle_sample_main(args.oracle_sample)
+    elif args.oracle_full_step:
+        oracle_full_step_main(args.oracle_full_step)
     elif args.impl == "reference":
         run_reference(args)
     else:

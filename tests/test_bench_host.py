@@ -51,3 +51,22 @@ def test_oracle_units_and_sample_size(monkeypatch):
     monkeypatch.setattr(bench, "WL", dict(bench.WORKLOADS["llama8b"]))
     assert bench.oracle_units() == 32 * 8
     assert bench.oracle_sample_reps() == 150
+
+
+def test_config_depends_on_the_workload_only(monkeypatch):
+    """Both arms print bench_config(): it must not depend on anything measured."""
+    monkeypatch.setattr(bench, "WL", dict(bench.WORKLOADS["llama8b"]))
+    a = bench.bench_config(1)
+    b = bench.bench_config(1, "hybrid", "contiguous")
+    assert a == b
+    # 32 layers x (8 KV heads x (32640 packed x 92 B + 128 ring x 512 B) + 32 q heads x 128 x 6 B)
+    assert bench.nominal_step_bytes(bench.WL) == 32 * (8 * (32640 * 92 + 128 * 512) + 32 * 128 * 6)
+    assert "786 MB" in a["l2"]
+    assert bench.bench_config(1, layout="paged")["layout"].startswith("paged")
+
+
+def test_record_bytes_of_the_workloads():
+    assert bench.record_bytes(bench.WORKLOADS["llama8b"]) == 52 + 40
+    assert bench.record_bytes(bench.WORKLOADS["batched"]) == 52 + 72
+    assert bench.record_bytes(bench.WORKLOADS["d256"]) == 100 + 80
+    assert bench.record_bytes(dict(bench.WORKLOADS["llama8b"], kb=4, vb=4)) == 68 + 72
