@@ -19,7 +19,9 @@
 #include <atomic>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
+#include <string>
 
 #include <cuda_runtime.h>
 
@@ -77,14 +79,14 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
     pdl_wait();
     pdl_launch();
     write_empty_partial(part, D, tid, NT, NCOL);
-    finish_unit<D, NT, QP>(a, b, h, smem);
+    finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
     return;
   }
   if (sp == nsp) {
     pdl_wait();
     pdl_launch();
     const bool smem_ok = ring_split<D, NT, QP>(a, b, h, slot, part, smem);
-    finish_unit<D, NT, QP>(a, b, h, smem, smem_ok);
+    finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128), smem_ok);
     return;
   }
   int L, Np, P;
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
     pdl_wait();
     pdl_launch();
     write_empty_partial(part, D, tid, NT, NCOL);
-    finish_unit<D, NT, QP>(a, b, h, smem);
+    finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
     return;
   }
   const PageLayout pl = page_layout(D, VB, KB);
@@ -392,7 +394,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
     if (tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
     if (!__syncthreads_and(drained)) {
       write_empty_partial(part, D, tid, NT, NCOL);
-      finish_unit<D, NT, QP>(a, b, h, smem, false);
+      finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128), false);
       return;
     }
   }
@@ -455,7 +457,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
       part[NCOL + hd] = l;
     }
   }
-  finish_unit<D, NT, QP>(a, b, h, smem);
+  finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
 }
 
 template <int D, int VB>
@@ -581,6 +583,16 @@ int decode_resident_ctas(const tq_ctx* ctx) {
   return n > 0 ? n : 1;
 }
 
+// The tcgen05 decoder serves decode (one query per row) at head_dim 128 with key_bits 3; TQ_DECODE_KERNEL=mma
+// in the environment selects the f16 mma.sync decoder there as well (comparisons, measurements).
+static bool tc_decoder_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("TQ_DECODE_KERNEL");
+    return !(v && std::string(v) == "mma");
+  }();
+  return on;
+}
+
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
                           const int32_t* n_q, int qp) {
@@ -598,6 +610,7 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.fault_stage = g_fault_stage.load();
   a.fault_polls = (uint32_t)g_fault_polls.load();
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
+  if (d == 128 && kb == 3 && qpr == 1 && qp == 1 && tc_decoder_enabled()) return launch_decode_tc(a, batch, phase, s);
   if (kb == 4) {
     if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);
     if (d == 128) return launch_decode_dv<128, 4, 4>(a, batch, phase, s, qp);

@@ -704,10 +704,11 @@ __device__ __forceinline__ void zero_unit_out(const DecodeArgs& a, int b, int h)
 }
 
 // After this CTA's partial is written: the last of the (n_splits + 1) CTAs of the (row, KV head)
-// merges all of them (an arrival counter; no CTA waits on another). smem_ok = false: this CTA's shared
-// memory may still receive a copy, so a last CTA writes zeros instead of combining.
+// merges all of them (an arrival counter; no CTA waits on another), with `scratch` (shared memory, room
+// for 4 (NT/32) + 2 NCOL 1026 floats) as its working space. smem_ok = false: this CTA's shared memory may
+// still receive a copy, so a last CTA writes zeros instead of combining.
 template <int D, int NT, int QP = 1>
-__device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint8_t* smem, bool smem_ok = true) {
+__device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, float* scratch, bool smem_ok = true) {
   __shared__ int s_last;
   __syncthreads();  // every thread's part of the partial is written
   if (threadIdx.x == 0) {
@@ -725,7 +726,7 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, uint
     zero_unit_out<D, NT, QP>(a, b, h);
     return;
   }
-  combine_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128));
+  combine_unit<D, NT, QP>(a, b, h, scratch);
 }
 
 }  // namespace
