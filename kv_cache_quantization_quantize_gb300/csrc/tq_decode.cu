@@ -19,9 +19,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdio>
-#include <cstdlib>
 #include <mutex>
-#include <string>
 
 #include <cuda_runtime.h>
 
@@ -48,8 +46,9 @@ std::atomic<int> g_fault_polls{0};
 template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1>
 __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 : 1) k_decode(DecodeArgs a) {
   constexpr int NCOL = qcols<QP>();
-  constexpr int NBP = key_bplanes(KB, D);  // B planes of the key MMAs (stored planes: KB)
+  constexpr int NBP = key_loop_planes(KB, D, QP);  // B planes the key MMAs run (stored planes: KB)
   constexpr int RP = key_rem_plane(KB, D);
+  constexpr bool REMN = key_rem_in_n(KB, D, QP);   // the remainder sits in columns 4..7 of plane 0
   constexpr int CW = warp_coords<D>();  // coordinates per warp
   constexpr int HALVES = D / CW;
   constexpr int KS = CW / 16;           // key-MMA k-steps per warp
@@ -238,6 +237,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
       for (int i = 0; i < 4; ++i) {
         am[i] = acc[kap][0][i] + acc[kap][1][i];
         aq[i] = acc[kap][2][i];
+        // column h + 4 (lanes c ^ 2) holds the remainder part of head h
+        if (REMN) am[i] += __shfl_xor_sync(0xffffffffu, am[i], 2);
       }
       if (HALVES == 2) {  // add the partner half's partial sums
         float* mine = xbuf + ((size_t)tid * 2 + kap) * 8;
@@ -583,16 +584,6 @@ int decode_resident_ctas(const tq_ctx* ctx) {
   return n > 0 ? n : 1;
 }
 
-// The tcgen05 decoder serves decode (one query per row) at head_dim 128 with key_bits 3; TQ_DECODE_KERNEL=mma
-// in the environment selects the f16 mma.sync decoder there as well (comparisons, measurements).
-static bool tc_decoder_enabled() {
-  static const bool on = [] {
-    const char* v = std::getenv("TQ_DECODE_KERNEL");
-    return !(v && std::string(v) == "mma");
-  }();
-  return on;
-}
-
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
                           const int32_t* n_q, int qp) {
@@ -610,7 +601,6 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.fault_stage = g_fault_stage.load();
   a.fault_polls = (uint32_t)g_fault_polls.load();
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
-  if (d == 128 && kb == 3 && qpr == 1 && qp == 1 && tc_decoder_enabled()) return launch_decode_tc(a, batch, phase, s);
   if (kb == 4) {
     if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);
     if (d == 128) return launch_decode_dv<128, 4, 4>(a, batch, phase, s, qp);

@@ -1,6 +1,5 @@
-// Shared device code of the decode kernels: arguments, MMA helpers, query rotation and projection, the
-// exact ring split, the cross-split combine and the arrival protocol. Included by tq_decode.cu (the f16
-// mma.sync bit-plane decoder) and tq_decode_tc.cu (the tcgen05 key-score decoder).
+// Device code of the decode kernels that is not their page loop: arguments, MMA helpers, query rotation and
+// projection, the exact ring split, the cross-split combine and the arrival protocol.
 #pragma once
 
 #include <cmath>
@@ -27,13 +26,6 @@ struct DecodeArgs {
   int fault_stage;
   uint32_t fault_polls;
 };
-
-// Split-K decode at head_dim 128 with key_bits 3 on the tcgen05 decoder (tq_decode_tc.cu): one launch of
-// a decode (qpr 1) over `batch` rows. phase as for launch_decode. Returns cudaErrorNotSupported for
-// shapes it does not serve.
-cudaError_t launch_decode_tc(const DecodeArgs& a, int batch, int phase, cudaStream_t s);
-// Resident CTAs per SM of the tcgen05 decoder (sets its kernel attributes once); < 0 on failure.
-int decode_tc_setup(int vb, bool paged);
 
 namespace {
 
@@ -181,6 +173,13 @@ __host__ __device__ constexpr int key_bplanes(int kb, int d) { return kb == 3 ? 
 // B plane that carries the QJL operand, and the remainder plane of plane 0 (-1: none).
 __host__ __device__ constexpr int key_qjl_plane(int kb) { return kb == 3 ? 2 : 4; }
 __host__ __device__ constexpr int key_rem_plane(int kb, int d) { return kb == 3 ? (d <= 128 ? 3 : -1) : 5; }
+// With one query row per CTA (decode), B columns 4..7 of the MMAs are free: the remainder plane then rides in
+// plane 0's MMAs as columns 4..7 (column 4 + h = the remainder of head h), and the epilogue adds column
+// 4 + h to column h. No MMA, mask or load is spent on it. B planes that the page loop runs:
+__host__ __device__ constexpr bool key_rem_in_n(int kb, int d, int qp) { return qp == 1 && key_rem_plane(kb, d) >= 0; }
+__host__ __device__ constexpr int key_loop_planes(int kb, int d, int qp) {
+  return key_bplanes(kb, d) - (key_rem_in_n(kb, d, qp) ? 1 : 0);
+}
 
 // Query columns of a split CTA: the 8 B columns of the MMAs carry the kMaxG heads of QP query rows
 // (QP = 1 for decode; 2 for prefill, whose chunk queries of one sequence share the key operands).
@@ -193,9 +192,9 @@ __host__ __device__ constexpr int qcols() {
 template <int D, int KB, int QP = 1>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
   // q_rot, q_proj [columns][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes]
-  // uint2; per-warp offset sums [warps][2 columns]
+  // uint2; per-warp offset sums [warps][2][8 B columns]
   return sizeof(float) * (2 * qcols<QP>() * D + 32) + 8 * 32 * (key_bplanes(KB, D) * D / 16) +
-         sizeof(float) * 2 * qcols<QP>() * (decode_threads<D>() / 32);
+         sizeof(float) * 2 * 8 * (decode_threads<D>() / 32);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).
@@ -341,22 +340,30 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   }
   __syncthreads();
   // B fragments: item (hv, pi, s) is computed by warp item % NW and shared through shared memory;
-  // wsum[w][hd] / wsum[w][4 + hd] hold warp w's offset sums of head hd, added in a fixed order below
+  // wsum[w][n] / wsum[w][8 + n] hold warp w's offset sums of B column n, added in a fixed order below
   // (the same constants in every split CTA and every call)
   constexpr int KS = warp_coords<D>() / 16;  // key-MMA k-steps per warp
-  constexpr int NW = NT / 32, NITEMS = HALVES * NBP * KS;
+  constexpr bool REMN = key_rem_in_n(KB, D, QP);  // the remainder rides in columns 4..7 of plane 0
+  constexpr int NBPL = key_loop_planes(KB, D, QP);
+  constexpr int NW = NT / 32, NITEMS = HALVES * NBPL * KS;
   uint2* frag = reinterpret_cast<uint2*>(red + 32);  // [NITEMS][32]
-  float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][2 NCOL]
-  const bool live = g < NCOL && g % kMaxG < G;
-  const float lam_m = live ? red[NCOL + 2 * g] : 0.f, lam_q = live ? red[NCOL + 2 * g + 1] : 0.f;
-  const float* bm = qr + (live ? g : 0) * D;
-  const float* bp = qp + (live ? g : 0) * D;
+  float* wsum = reinterpret_cast<float*>(frag + NITEMS * 32);  // [NW][2][8]
+  const bool rem_lane = REMN && g >= kMaxG;  // B column g carries the remainder of head g - 4
+  const int hsrc = rem_lane ? g - kMaxG : g;
+  const bool live = hsrc < NCOL && hsrc % kMaxG < G;
+  const float lam_m = live ? red[NCOL + 2 * hsrc] : 0.f, lam_q = live ? red[NCOL + 2 * hsrc + 1] : 0.f;
+  const float* bm = qr + (live ? hsrc : 0) * D;
+  const float* bp = qp + (live ? hsrc : 0) * D;
   __syncthreads();
   float sum_m = 0.f, sum_q = 0.f;
   for (int item = warp; item < NITEMS; item += NW) {
-    const int s = item % KS, pi = (item / KS) % NBP, hv = item / (NBP * KS);
-    const bool qjl = pi == QJP, rem = pi == RP;  // rem: remainder plane of plane 0
-    const float w = qjl ? 2.f * lam_q : 2.f * lv.cb[kCbW + (rem ? 0 : pi)] * lam_m;
+    const int s = item % KS, pi = (item / KS) % NBPL, hv = item / (NBPL * KS);
+    const bool qjl = pi == QJP;
+    // rem: this lane's operand is the remainder of plane 0 (a remainder plane, or columns 4..7 of plane 0)
+    const bool rem = REMN ? (rem_lane && pi == 0) : pi == RP;
+    const float w = (rem_lane && pi != 0) ? 0.f
+                    : qjl                 ? 2.f * lam_q
+                                          : 2.f * lv.cb[kCbW + (rem ? 0 : pi)] * lam_m;
     const float* base = qjl ? bp : bm;
     const int j0 = 128 * hv + 16 * s + 2 * c, j1 = j0 + 8;
     const float pre0 = key_prescale(2 * s), pre1 = key_prescale(2 * s + 1);
@@ -382,9 +389,9 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
   sum_m += __shfl_xor_sync(0xffffffffu, sum_m, 2);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 1);
   sum_q += __shfl_xor_sync(0xffffffffu, sum_q, 2);
-  if (c == 0 && g < NCOL) {
-    wsum[warp * 2 * NCOL + g] = sum_m;
-    wsum[warp * 2 * NCOL + NCOL + g] = sum_q;
+  if (c == 0) {
+    wsum[warp * 16 + g] = sum_m;
+    wsum[warp * 16 + 8 + g] = sum_q;
   }
   __syncthreads();
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
@@ -393,8 +400,8 @@ __device__ __forceinline__ void query_prep(const DecodeArgs& a, int b, int h, fl
     const int hd = min(2 * c + i, NCOL - 1);
     float sm = 0.f, sq = 0.f;
     for (int w = 0; w < NW; ++w) {
-      sm += wsum[w * 2 * NCOL + hd];
-      sq += wsum[w * 2 * NCOL + NCOL + hd];
+      sm += wsum[w * 16 + hd] + (REMN ? wsum[w * 16 + kMaxG + hd] : 0.f);
+      sq += wsum[w * 16 + 8 + hd];
     }
     um[i] = a.scale * kLog2e / red[NCOL + 2 * hd];
     cm[i] = 0.5f * sm;
