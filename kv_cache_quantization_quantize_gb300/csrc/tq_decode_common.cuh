@@ -193,7 +193,7 @@ template <int D, int KB, int QP = 1>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
   // q_rot, q_proj [columns][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes]
   // uint2; per-warp offset sums [warps][2][8 B columns]
-  return sizeof(float) * (2 * qcols<QP>() * D + 32) + 8 * 32 * (key_bplanes(KB, D) * D / 16) +
+  return sizeof(float) * (2 * qcols<QP>() * D + 32) + 8 * 32 * (key_loop_planes(KB, D, QP) * D / 16) +
          sizeof(float) * 2 * 8 * (decode_threads<D>() / 32);
 }
 
