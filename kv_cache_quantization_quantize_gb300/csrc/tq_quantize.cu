@@ -1066,33 +1066,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
         const __half sh = __float2half_rn(s32);
         const float sv = __half2float(sh);
-        // floor(x / s) with the quotient rounded as an IEEE division: x * (1/s) is within a few ulps of
-        // it, so its floor is exact unless it lies within ~4 ulps of an integer; those (rare) elements
-        // take the correctly rounded division.
-        const float rcp = sv > 0.f ? __frcp_rn(sv) : 0.f;
-        float fq[32];
-        bool near = false;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float qv = x[i] * rcp;
-          fq[i] = floorf(qv);
-          const float fr = qv - fq[i], eps = fabsf(qv) * 4.8e-7f + 1e-30f;
-          near |= (fr < eps) | (fr > 1.f - eps);
-        }
-        if (near && sv > 0.f) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) fq[i] = floorf(__fdiv_rn(x[i], sv));
-        }
         uint32_t cw[8];
+        if (lv.vb == 2) {
+          // code = clamp(floor(fl(x / s)), -2, 1) + 2 = [fl(x/s) >= -1] + [fl(x/s) >= 0] + [fl(x/s) >= 1], and
+          // for s > 0: fl(x/s) >= -1  <=>  x/s >= -(1 + 2^-24)  <=>  x + s >= -s 2^-24 (ties round to the even
+          // -1); fl(x/s) >= 1  <=>  x - s >= -s 2^-25; fl(x/s) >= 0  <=>  x >= 0. x + s and x - s are exact
+          // where the comparison is close (Sterbenz), so no division is needed.
+          const float t_lo = -sv * 5.9604644775390625e-8f, t_hi = -sv * 2.98023223876953125e-8f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint32_t w = 0;
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w = 0;
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int code = sv > 0.f ? (int)fminf(fmaxf(fq[4 * k + e], (float)-vhalf), (float)(vhalf - 1)) + vhalf : vhalf;
-            w |= (uint32_t)code << (8 * e);
+            for (int e = 0; e < 4; ++e) {
+              const float xv = x[4 * k + e];
+              const uint32_t code = (uint32_t)(xv + sv >= t_lo) + (uint32_t)(xv >= 0.f) + (uint32_t)(xv - sv >= t_hi);
+              w |= code << (8 * e);
+            }
+            cw[k] = sv > 0.f ? w : 0x02020202u;  // a zero group: every code 2
           }
-          cw[k] = w;
+        } else {
+          // floor(x / s) with the quotient rounded as an IEEE division: x * (1/s) is within a few ulps of
+          // it, so its floor is exact unless it lies within ~4 ulps of an integer; those (rare) elements
+          // take the correctly rounded division.
+          const float rcp = sv > 0.f ? __frcp_rn(sv) : 0.f;
+          float fq[32];
+          bool near = false;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float qv = x[i] * rcp;
+            fq[i] = floorf(qv);
+            const float fr = qv - fq[i], eps = fabsf(qv) * 4.8e-7f + 1e-30f;
+            near |= (fr < eps) | (fr > 1.f - eps);
+          }
+          if (near && sv > 0.f) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) fq[i] = floorf(__fdiv_rn(x[i], sv));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int code = sv > 0.f ? (int)fminf(fmaxf(fq[4 * k + e], (float)-vhalf), (float)(vhalf - 1)) + vhalf : vhalf;
+              w |= (uint32_t)code << (8 * e);
+            }
+            cw[k] = w;
+          }
         }
         // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
         *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
