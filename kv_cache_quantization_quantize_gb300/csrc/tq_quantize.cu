@@ -675,10 +675,10 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
 //   - Key words, norms and value scales go to the page straight from registers; value codes are
 //     staged in shared memory for the fragment-major value layout.
 // =============================================================================================
-constexpr int kTcThreads = 512;  // 16 warps; four threads (32-coordinate chunks) per token row
+constexpr int kTcThreads = 512;  // warps 0-7 keys, 8-15 values; two warps (column halves) per token row
 constexpr uint32_t kQbHD = 0, kQbS = 32768, kQbBuf = 65536;  // 2 x [K tile 32 KB | V tile 32 KB]
 constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 value codes
-constexpr uint32_t kQbX = kQbVcode + 16384;                   // chunk exchange of the norms (see below)
+constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
 // mbarriers [8] (slot 6 holds the TMEM address), then the arming and completion counts of each barrier
 // ([8] + [8] u32, see bulk128_drain)
 constexpr uint32_t kQbBar = kQbX + 2048 + 4096 + 2048, kQbEnd = kQbBar + 128;
@@ -865,16 +865,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool tab_ok = mbar_wait(bar_tab, 0);
   if (tid == 0 && tab_ok) ++done[0];
   bool ok = __syncthreads_and(tab_ok) != 0;
-  // parities of the next wait: bit i of ph_ld / ph_rot / ph_qjl for buffer / TMEM half i
+  // parities of the next wait: bit i of ph_ld / ph_rot for buffer / TMEM half i
   uint32_t ph_rot = 0, ph_qjl = 0, bufi = 0, ph_ld = 0;
-  // Pipeline. Page i lives in smem buffer i % 2 and TMEM half i % 2; all 16 warps take every phase, so
-  // each phase has four warps per SM sub-partition to hide its latencies:
-  //   1. the QJL signs of page i - 1 (its projection ran during the value phase of iteration i - 1);
-  //      that frees smem buffer and TMEM half (i + 1) % 2, and the copy of page i + 1 starts;
-  //   2. the keys of page i: norms, Lloyd-Max index, residual (bf16 hi + lo over the consumed K tile);
-  //      then thread 0 issues the QJL projection of page i and, page i + 1 having landed, its rotation;
-  //   3. the values of page i, while the tensor cores run those two.
-  // The first page's rotation is issued here.
+  // Pipeline. Page i lives in smem buffer i % 2 and TMEM half i % 2.
+  //   - The key warps code page i and issue its QJL MMAs.
+  //   - The value warps first take the QJL signs of page i - 1 (its MMAs ran during the end of iteration
+  //     i - 1), which frees buffer and TMEM half (i + 1) % 2. They then start the copy of page i + 1,
+  //     code the values of page i, and issue the rotation of page i + 1.
+  // So no warp waits on the tensor cores inside an iteration: the rotation of page i + 1 and the
+  // projection of page i run while the values of page i are packed. The first page's rotation is
+  // issued here.
   if (ok && cur < ntasks && tid == 0) {
     if (tma_cur) {
       if (mbar_wait(bar_ld, 0)) ++done[2];
@@ -884,43 +884,49 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (tma_cur) ph_ld ^= 1u;
   ok = __syncthreads_and(ok) != 0;
-  // thread (token t, chunk cq): TMEM lane t = 32 (warp % 4) + lane, coordinates 32 cq .. 32 cq + 31 of the
-  // token's K and V rows (the four threads of a token sit in warps w, w + 4, w + 8, w + 12)
-  const int t = 32 * (warp & 3) + lane, cq = warp >> 2;
-  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-  float* xs = reinterpret_cast<float*>(sm + kQbX);  // [4 chunks][128] partial |y'|^2
-  float* xr = xs + 512;                             // [4][128] partial |r|^2
-  // partial words of the four chunks of a token, in the value-code staging area (free outside the value
-  // phase): index planes [4 cq][128 t][8] (hi 0-3, lo 4-7), sign plane [4 cq][128 t][4]
-  uint32_t* xw = reinterpret_cast<uint32_t*>(vcode);
+  // warp roles: key path (warps 0-7) or value path (8-15); in each, warp w covers TMEM lane quarter
+  // w % 4 (tokens 32 (w % 4) + lane) and column half (w % 8) / 4
+  const bool kpath = warp < 8;
+  const int pw = warp & 7, q4 = pw & 3, half = pw >> 2;
+  const int t = 32 * q4 + lane;
+  float* xs = reinterpret_cast<float*>(sm + kQbX);                  // [2 halves][128] partial |y'|^2
+  float* xr = xs + 256;                                             // [2][128] partial |r|^2
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][8] half-1 index words
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 6144);     // [128][4] half-1 sign words
   const PageLayout pl = page_layout(D, lv.vb, 3);  // this kernel serves key_bits 3
   uint8_t* prev_page = nullptr;  // page whose QJL signs are still to be written (its MMAs are in flight)
   bool prev = false;
-  // Bits of coordinate 32 cq + i in a token's key words: word (i >> 1) & 3, bit 2 (i >> 4) + ((i >> 3) & 1) +
-  // 16 (i & 1) + 4 cq (the shift by 4 cq is applied to whole words).
-  // QJL signs of the page in TMEM half `hb`: wait for its projection, threshold z = S r, write the sign
-  // plane (thread (t, cq) writes word cq). Returns false if the wait gave up. Ends with a block barrier.
+  // QJL signs of the page in TMEM half `hb` (value warps): wait for its projection, threshold z = S r,
+  // write the sign plane. Returns false if the wait gave up.
   auto qjl_signs = [&](uint32_t hb, uint8_t* page) -> bool {
     const bool w_ok = mbar_wait(bar_qjl2(hb), (ph_qjl >> hb) & 1u);
-    if (tid == 0 && w_ok) ++done[qjl_idx(hb)];
+    if (tid == 256 && w_ok) ++done[qjl_idx(hb)];
     ph_qjl ^= 1u << hb;
     tc_fence_after();
-    uint32_t z[32];
-    tmem_ld32(tmem + 256u * hb + lane_off + 32 * cq, z);
-    tc_fence_before();
+    const uint32_t prow = tmem + 256u * hb + ((uint32_t)(32 * q4) << 16);
     uint32_t wsg[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
-      wsg[(i >> 1) & 3] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << (2 * (i >> 4) + ((i >> 3) & 1) + 16 * (i & 1))) : 0u;
+    for (int cc = 0; cc < 2; ++cc) {
+      uint32_t z[32];
+      tmem_ld32(prow + 64 * half + 32 * cc, z);
 #pragma unroll
-    for (int cw = 0; cw < 4; ++cw) xw[(cq * 128 + t) * 4 + cw] = wsg[cw] << (4 * cq);
-    __syncthreads();  // every thread has read z (the half may be rotated into next) and written its bits
-    if (page) {
+      for (int i = 0; i < 32; ++i) {
+        const int jl = 32 * cc + i;
+        const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+        wsg[cw] |= (__uint_as_float(z[i]) >= 0.f) ? (1u << bit) : 0u;
+      }
+    }
+    if (half) {
+#pragma unroll
+      for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
+    }
+    tc_fence_before();
+    named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
+    if (!half && page) {
       uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
       const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
-      const uint32_t wv = xw[(0 * 128 + t) * 4 + cq] | xw[(1 * 128 + t) * 4 + cq] | xw[(2 * 128 + t) * 4 + cq] |
-                          xw[(3 * 128 + t) * 4 + cq];
-      kw[((ktile * 3 + 2) * 32 + 4 * kg + cq) * 2 + kr] = wv;
+#pragma unroll
+      for (int cw = 0; cw < 4; ++cw) kw[((ktile * 3 + 2) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
     }
     return w_ok;
   };
@@ -936,88 +942,186 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* page = page_addr(lv, cslot, chead, cpg);
     const bool wr = page != nullptr;  // paged cache without a block for this page: code it, write nothing
     if (!wr && tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
-    const uint32_t lrow = tmem + 256u * bufi + lane_off;
+    const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
-    // ---- 1. the previous page's QJL signs; then the copy of the next page into buffer bufi ^ 1 ----
-    if (prev) ok_p = qjl_signs(bufi ^ 1u, prev_page);
-    bool tma_nxt = false;
-    if (nxt < ntasks)
-      tma_nxt = bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
-                             bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 0, kTcThreads);
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
-    // ---- 2. keys: |y'|, y = y' / |y'|, index, residual ----
-    uint32_t v[32];
-    tmem_ld32(lrow + 32 * cq, v);
-    {
+    if (kpath) {
+      // ---- keys, two threads per token (64 coordinates each): |y'|, y = y' / |y'|, index, residual ----
       float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ss4[i & 3] = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss4[i & 3]);
-      xs[cq * 128 + t] = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
-    }
-    __syncthreads();  // partial norms in place; the signs' partial words have been read
-    const float nrot = sqrtf((xs[t] + xs[128 + t]) + (xs[256 + t] + xs[384 + t]));  // = sqrt(d) |k|
-    const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
-    {
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lrow + 64 * half + 32 * cc, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ss4[i & 3] = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss4[i & 3]);
+      }
+      xs[half * 128 + t] = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
+      named_barrier(1, 256);
+      const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
+      const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
       const float b0 = lv.cb[kCbBnd], b1 = lv.cb[kCbBnd + 1], b2 = lv.cb[kCbBnd + 2];
       const float c0 = lv.cb[kCbCent], c1 = lv.cb[kCbCent + 1], c2 = lv.cb[kCbCent + 2], c3 = lv.cb[kCbCent + 3];
       uint32_t whi[4] = {0u, 0u, 0u, 0u}, wlo[4] = {0u, 0u, 0u, 0u};
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int oc = 0; oc < 4; ++oc) {  // 8 coordinates = one 16-byte chunk of the A rows
-        uint32_t hi[4], lo[4];
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t v[32];
+        tmem_ld32(lrow + 64 * half + 32 * cc, v);
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          float res2[2];
+        for (int oc = 0; oc < 4; ++oc) {  // 8 coordinates = one 16-byte chunk of the A rows
+          uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int i = 8 * oc + 2 * e2 + e;  // coordinate 32 cq + i
-            const float yy = __uint_as_float(v[i]) * scale;
-            // index = #{boundaries below yy}: high bit = (yy > b1); low bit = yy above the outer
-            // boundary on its side of b1
-            const bool hb = yy > b1;
-            const bool lb = yy > (hb ? b2 : b0);
-            const float cv = hb ? (lb ? c3 : c2) : (lb ? c1 : c0);
-            const float res = yy - cv;
-            rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
-            res2[e] = res;
-            const int cw = (i >> 1) & 3, bit = 2 * (i >> 4) + ((i >> 3) & 1) + 16 * (i & 1);
-            whi[cw] |= hb ? (1u << bit) : 0u;
-            wlo[cw] |= lb ? (1u << bit) : 0u;
+          for (int e2 = 0; e2 < 4; ++e2) {
+            float res2[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate 64 half + jl
+              const float yy = __uint_as_float(v[i]) * scale;
+              // index = #{boundaries below yy}: high bit = (yy > b1); low bit = yy above the outer
+              // boundary on its side of b1
+              const bool hb = yy > b1;
+              const bool lb = yy > (hb ? b2 : b0);
+              const float cv = hb ? (lb ? c3 : c2) : (lb ? c1 : c0);
+              const float res = yy - cv;
+              rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
+              res2[e] = res;
+              // bit of coordinate j = 64 half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
+              // 64 half adds 8 to 2 (j >> 4)
+              const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+              whi[cw] |= hb ? (1u << bit) : 0u;
+              wlo[cw] |= lb ? (1u << bit) : 0u;
+            }
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(res2[0], res2[1]);
+            const float2 hf2 = __bfloat1622float2(h2);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(res2[0] - hf2.x, res2[1] - hf2.y);
+            hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
+            lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
           }
-          const __nv_bfloat162 h2 = __floats2bfloat162_rn(res2[0], res2[1]);
-          const float2 hf2 = __bfloat1622float2(h2);
-          const __nv_bfloat162 l2 = __floats2bfloat162_rn(res2[0] - hf2.x, res2[1] - hf2.y);
-          hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
-          lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
+          const uint32_t off = sw128_offset(t, 64 * half + 32 * cc + 8 * oc);
+          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
-        const uint32_t off = sw128_offset(t, 32 * cq + 8 * oc);
-        *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       }
-      xr[cq * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+      xr[half * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+      if (half) {
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) {
-        xw[(cq * 128 + t) * 8 + cw] = whi[cw] << (4 * cq);
-        xw[(cq * 128 + t) * 8 + 4 + cw] = wlo[cw] << (4 * cq);
+        for (int cw = 0; cw < 4; ++cw) {
+          xw[t * 8 + cw] = whi[cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
+          xw[t * 8 + 4 + cw] = wlo[cw] << 8;
+        }
       }
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // residual tile -> tensor cores
-    tc_fence_before();
-    __syncthreads();  // residuals, partial |r|^2 and partial words in place; the K columns have been read
-    if (tid == 0) {
-      // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
-      tc_fence_after();
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc_fence_before();
+      named_barrier(1, 256);
       const uint32_t buf = buf0 + bufi * 65536u;
+      if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
+        tc_fence_after();
 #pragma unroll
-      for (int ks = 0; ks < 16; ++ks) {
-        const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32 + (ks >> 3) * 32768;
-        umma_bf16(tmem + 256u * bufi, umma_desc_sw128(buf + koff),
-                  umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
+        for (int ks = 0; ks < 16; ++ks) {
+          const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32 + (ks >> 3) * 32768;
+          umma_bf16(tmem + 256u * bufi, umma_desc_sw128(buf + koff),
+                    umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
+        }
+        umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
+        ++armed[qjl_idx(bufi)];
       }
-      umma_commit(bar_qjl2(bufi));  // waited for by the signs of the next iteration (or after the loop)
-      ++armed[qjl_idx(bufi)];
-      // rotation of the next page into TMEM half bufi ^ 1 (its z was read by the signs above)
-      if (nxt < ntasks) {
+      if (!half && wr) {  // planes 0-1, n and gamma of token t
+        const float n = nrot * rsqrtf((float)D);
+        const float rr = xr[t] + xr[128 + t];
+        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
+        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+        const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
+        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
+            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) {
+          kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
+          kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
+        }
+      }
+    } else {
+      // ---- the previous page's QJL signs; this frees buffer and TMEM half bufi ^ 1 ----
+      if (prev) ok_p = qjl_signs(bufi ^ 1u, prev_page);
+      // ---- start the copy of the next page into buffer bufi ^ 1 ----
+      bool tma_nxt = false;
+      if (nxt < ntasks)
+        tma_nxt = bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
+                               bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 256);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
+      // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
+      const int vhalf = 1 << (lv.vb - 1);
+      const float inv_sqrt_d = rsqrtf((float)D);
+      uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
+#pragma unroll 1
+      for (int gg = 0; gg < 2; ++gg) {
+        const int grp = 2 * half + gg;
+        uint32_t v[32];
+        tmem_ld32(lrow + 128 + 32 * grp, v);
+        float x[32], am4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = __uint_as_float(v[i]) * inv_sqrt_d;
+          am4[i & 3] = fmaxf(am4[i & 3], fabsf(x[i]));
+        }
+        const float am = fmaxf(fmaxf(am4[0], am4[1]), fmaxf(am4[2], am4[3]));
+        const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
+        const __half sh = __float2half_rn(s32);
+        const float sv = __half2float(sh);
+        uint32_t cw[8];
+        if (lv.vb == 2) {
+          // code = clamp(floor(fl(x / s)), -2, 1) + 2 = [fl(x/s) >= -1] + [fl(x/s) >= 0] + [fl(x/s) >= 1], and
+          // for s > 0: fl(x/s) >= -1  <=>  x/s >= -(1 + 2^-24)  <=>  x + s >= -s 2^-24 (ties round to the even
+          // -1); fl(x/s) >= 1  <=>  x - s >= -s 2^-25; fl(x/s) >= 0  <=>  x >= 0. x + s and x - s are exact
+          // where the comparison is close (Sterbenz), so no division is needed.
+          const float t_lo = -sv * 5.9604644775390625e-8f, t_hi = -sv * 2.98023223876953125e-8f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float xv = x[4 * k + e];
+              const uint32_t code = (uint32_t)(xv + sv >= t_lo) + (uint32_t)(xv >= 0.f) + (uint32_t)(xv - sv >= t_hi);
+              w |= code << (8 * e);
+            }
+            cw[k] = sv > 0.f ? w : 0x02020202u;  // a zero group: every code 2
+          }
+        } else {
+          // floor(x / s) with the quotient rounded as an IEEE division: x * (1/s) is within a few ulps of
+          // it, so its floor is exact unless it lies within ~4 ulps of an integer; those (rare) elements
+          // take the correctly rounded division.
+          const float rcp = sv > 0.f ? __frcp_rn(sv) : 0.f;
+          float fq[32];
+          bool near = false;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float qv = x[i] * rcp;
+            fq[i] = floorf(qv);
+            const float fr = qv - fq[i], eps = fabsf(qv) * 4.8e-7f + 1e-30f;
+            near |= (fr < eps) | (fr > 1.f - eps);
+          }
+          if (near && sv > 0.f) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) fq[i] = floorf(__fdiv_rn(x[i], sv));
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint32_t w = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int code = sv > 0.f ? (int)fminf(fmaxf(fq[4 * k + e], (float)-vhalf), (float)(vhalf - 1)) + vhalf : vhalf;
+              w |= (uint32_t)code << (8 * e);
+            }
+            cw[k] = w;
+          }
+        }
+        // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        if (wr) sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
+      }
+      tc_fence_before();
+      named_barrier(2, 256);  // value codes staged; V columns of this half read; next page's rows copied
+      if (tid == 256 && nxt < ntasks) {  // rotation of the next page into TMEM half bufi ^ 1
+        tc_fence_after();
         bool landed = true;
         if (tma_nxt) {
           landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
@@ -1029,103 +1133,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          armed + 4 + (bufi ^ 1u));
         else ok_p = false;
       }
-    }
-    if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);
-    if (wr) {  // thread (t, cq) writes index words cq of both planes; chunk 0 also n and gamma
-      uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-      const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
-      uint32_t whi = 0u, wlo = 0u;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        whi |= xw[(c4 * 128 + t) * 8 + cq];
-        wlo |= xw[(c4 * 128 + t) * 8 + 4 + cq];
-      }
-      kw[((tile * 3 + 0) * 32 + 4 * g + cq) * 2 + r] = whi;
-      kw[((tile * 3 + 1) * 32 + 4 * g + cq) * 2 + r] = wlo;
-      if (cq == 0) {
-        const float n = nrot * rsqrtf((float)D);
-        const float rr = (xr[t] + xr[128 + t]) + (xr[256 + t] + xr[384 + t]);
-        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
-        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
-            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
-      }
-    }
-    // ---- 3. values: group cq of token t (32 coordinates): fp16 scale, mid-rise codes ----
-    {
-      const int vhalf = 1 << (lv.vb - 1);
-      const float inv_sqrt_d = rsqrtf((float)D);
-      uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
-      tmem_ld32(lrow + 128 + 32 * cq, v);
-      float x[32], am4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = __uint_as_float(v[i]) * inv_sqrt_d;
-        am4[i & 3] = fmaxf(am4[i & 3], fabsf(x[i]));
-      }
-      const float am = fmaxf(fmaxf(am4[0], am4[1]), fmaxf(am4[2], am4[3]));
-      const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
-      const __half sh = __float2half_rn(s32);
-      const float sv = __half2float(sh);
-      uint32_t cw[8];
-      if (lv.vb == 2) {
-        // code = clamp(floor(fl(x / s)), -2, 1) + 2 = [fl(x/s) >= -1] + [fl(x/s) >= 0] + [fl(x/s) >= 1], and
-        // for s > 0: fl(x/s) >= -1  <=>  x/s >= -(1 + 2^-24)  <=>  x + s >= -s 2^-24 (ties round to the even
-        // -1); fl(x/s) >= 1  <=>  x - s >= -s 2^-25; fl(x/s) >= 0  <=>  x >= 0. x + s and x - s are exact
-        // where the comparison is close (Sterbenz), so no division is needed.
-        const float t_lo = -sv * 5.9604644775390625e-8f, t_hi = -sv * 2.98023223876953125e-8f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint32_t w = 0;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float xv = x[4 * k + e];
-            const uint32_t code = (uint32_t)(xv + sv >= t_lo) + (uint32_t)(xv >= 0.f) + (uint32_t)(xv - sv >= t_hi);
-            w |= code << (8 * e);
-          }
-          cw[k] = sv > 0.f ? w : 0x02020202u;  // a zero group: every code 2
-        }
-      } else {
-        // floor(x / s) with the quotient rounded as an IEEE division: x * (1/s) is within a few ulps of
-        // it, so its floor is exact unless it lies within ~4 ulps of an integer; those (rare) elements
-        // take the correctly rounded division.
-        const float rcp = sv > 0.f ? __frcp_rn(sv) : 0.f;
-        float fq[32];
-        bool near = false;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float qv = x[i] * rcp;
-          fq[i] = floorf(qv);
-          const float fr = qv - fq[i], eps = fabsf(qv) * 4.8e-7f + 1e-30f;
-          near |= (fr < eps) | (fr > 1.f - eps);
-        }
-        if (near && sv > 0.f) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) fq[i] = floorf(__fdiv_rn(x[i], sv));
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint32_t w = 0;
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int code = sv > 0.f ? (int)fminf(fmaxf(fq[4 * k + e], (float)-vhalf), (float)(vhalf - 1)) + vhalf : vhalf;
-            w |= (uint32_t)code << (8 * e);
-          }
-          cw[k] = w;
-        }
-      }
-      if (wr) sw[vscale_idx(D, t, cq)] = __half_as_ushort(sh);
-      tc_fence_before();
-      __syncthreads();  // the partial index words have been read: the staging area takes the value codes
-      // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
-      *reinterpret_cast<uint4*>(vcode + t * D + (((2 * cq) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-      *reinterpret_cast<uint4*>(vcode + t * D + (((2 * cq + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-    }
-    __syncthreads();  // value codes staged
-    // ---- pack the value codes (fragment-major layout) ----
-    {
+      if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);
+      // ---- pack the value codes (fragment-major layout) ----
+      const int vt = tid - 256;
       uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
       if (lv.vb == 2) {
-        for (int w = tid; w < 4 * (D / 16) * 32; w += kTcThreads) {
+        for (int w = vt; w < 4 * (D / 16) * 32; w += 256) {
           const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
           const int g = ln >> 2, c = ln & 3;
           uint32_t word = 0;
@@ -1141,7 +1154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (wr) vw[w] = word;
         }
       } else {
-        for (int w = tid; w < 4 * (D / 16) * 32 * 2; w += kTcThreads) {
+        for (int w = vt; w < 4 * (D / 16) * 32 * 2; w += 256) {
           const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
           const int g = ln >> 2, c = ln & 3;
           uint32_t word = 0;
@@ -1157,16 +1170,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     tc_fence_before();
-    ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, staging and exchange may be reused
+    ok = __syncthreads_and(ok_p) != 0;  // the page is done; its buffer, vcode and exchange may be reused
     tc_fence_after();
     prev = true;
-    prev_page = wr ? page : nullptr;
+    prev_page = page;
     cur = nxt;
     bufi ^= 1u;
   }
   // the last page's QJL signs (its projection was issued in the final iteration)
-  if (ok && prev && !qjl_signs(bufi ^ 1u, prev_page)) ok = false;
-  if (!ok && tid == 0) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  if (ok && prev && !kpath && !qjl_signs(bufi ^ 1u, prev_page)) ok = false;
+  if (!ok && (tid == 0 || tid == 256)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();  // every count is final
   // copies or MMAs still pending after a failed wait are waited for before shared memory and TMEM are
