@@ -681,7 +681,7 @@ constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 v
 constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
 // mbarriers [8] (slot 6 holds the TMEM address), then the arming and completion counts of each barrier
 // ([8] + [8] u32, see bulk128_drain)
-constexpr uint32_t kQbBar = kQbX + 2048 + 4096 + 2048, kQbEnd = kQbBar + 128;
+constexpr uint32_t kQbBar = kQbX + 2048 + 6144 + 2048, kQbEnd = kQbBar + 128;
 constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -811,10 +811,13 @@ __device__ __forceinline__ int bulk128_next(const AppendArgs& a, int task, int n
   return ntasks;
 }
 
+// KB = key bits: 3 (2-bit Lloyd-Max index + sign) or 4 (3-bit index + sign, served with 4-bit values).
+template <int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_quantize_bulk128(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AppendArgs a,
                        int pages_per_row, int batch) {
   constexpr int D = 128;
+  constexpr int MB = KB - 1;  // index bits = index planes
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* vcode = sm + kQbVcode;
@@ -891,9 +894,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int t = 32 * q4 + lane;
   float* xs = reinterpret_cast<float*>(sm + kQbX);                  // [2 halves][128] partial |y'|^2
   float* xr = xs + 256;                                             // [2][128] partial |r|^2
-  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][8] half-1 index words
-  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 6144);     // [128][4] half-1 sign words
-  const PageLayout pl = page_layout(D, lv.vb, 3);  // this kernel serves key_bits 3
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][4 MB] half-1 index words
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 8192);     // [128][4] half-1 sign words
+  const PageLayout pl = page_layout(D, lv.vb, KB);
   uint8_t* prev_page = nullptr;  // page whose QJL signs are still to be written (its MMAs are in flight)
   bool prev = false;
   // QJL signs of the page in TMEM half `hb` (value warps): wait for its projection, threshold z = S r,
@@ -926,7 +929,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
       const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) kw[((ktile * 3 + 2) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
+      for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
     }
     return w_ok;
   };
@@ -958,9 +961,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_barrier(1, 256);
       const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
       const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
-      const float b0 = lv.cb[kCbBnd], b1 = lv.cb[kCbBnd + 1], b2 = lv.cb[kCbBnd + 2];
-      const float c0 = lv.cb[kCbCent], c1 = lv.cb[kCbCent + 1], c2 = lv.cb[kCbCent + 2], c3 = lv.cb[kCbCent + 3];
-      uint32_t whi[4] = {0u, 0u, 0u, 0u}, wlo[4] = {0u, 0u, 0u, 0u};
+      constexpr int NL = 1 << MB;  // Lloyd-Max levels
+      float cent[NL], bnd[NL - 1];
+#pragma unroll
+      for (int i = 0; i < NL; ++i) cent[i] = lv.cb[kCbCent + i];
+#pragma unroll
+      for (int i = 0; i < NL - 1; ++i) bnd[i] = lv.cb[kCbBnd + i];
+      uint32_t wix[MB][4];  // index planes, highest bit first
+#pragma unroll
+      for (int p = 0; p < MB; ++p) wix[p][0] = wix[p][1] = wix[p][2] = wix[p][3] = 0u;
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
@@ -976,19 +985,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int e = 0; e < 2; ++e) {
               const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate 64 half + jl
               const float yy = __uint_as_float(v[i]) * scale;
-              // index = #{boundaries below yy}: high bit = (yy > b1); low bit = yy above the outer
-              // boundary on its side of b1
-              const bool hb = yy > b1;
-              const bool lb = yy > (hb ? b2 : b0);
-              const float cv = hb ? (lb ? c3 : c2) : (lb ? c1 : c0);
+              // index = #{boundaries below yy}, by binary search over the sorted boundaries
+              bool ib[MB];
+              float cv;
+              if constexpr (MB == 2) {
+                ib[0] = yy > bnd[1];
+                ib[1] = yy > (ib[0] ? bnd[2] : bnd[0]);
+                cv = ib[0] ? (ib[1] ? cent[3] : cent[2]) : (ib[1] ? cent[1] : cent[0]);
+              } else {
+                ib[0] = yy > bnd[3];
+                ib[1] = yy > (ib[0] ? bnd[5] : bnd[1]);
+                ib[2] = yy > (ib[0] ? (ib[1] ? bnd[6] : bnd[4]) : (ib[1] ? bnd[2] : bnd[0]));
+                cv = ib[0] ? (ib[1] ? (ib[2] ? cent[7] : cent[6]) : (ib[2] ? cent[5] : cent[4]))
+                           : (ib[1] ? (ib[2] ? cent[3] : cent[2]) : (ib[2] ? cent[1] : cent[0]));
+              }
               const float res = yy - cv;
               rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
               res2[e] = res;
               // bit of coordinate j = 64 half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
               // 64 half adds 8 to 2 (j >> 4)
               const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
-              whi[cw] |= hb ? (1u << bit) : 0u;
-              wlo[cw] |= lb ? (1u << bit) : 0u;
+#pragma unroll
+              for (int p = 0; p < MB; ++p) wix[p][cw] |= ib[p] ? (1u << bit) : 0u;
             }
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(res2[0], res2[1]);
             const float2 hf2 = __bfloat1622float2(h2);
@@ -1004,10 +1022,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       xr[half * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
       if (half) {
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) {
-          xw[t * 8 + cw] = whi[cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
-          xw[t * 8 + 4 + cw] = wlo[cw] << 8;
-        }
+        for (int p = 0; p < MB; ++p)
+#pragma unroll
+          for (int cw = 0; cw < 4; ++cw) xw[t * 4 * MB + 4 * p + cw] = wix[p][cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
@@ -1033,10 +1050,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
             (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) {
-          kw[((tile * 3 + 0) * 32 + 4 * g + cw) * 2 + r] = whi[cw] | xw[t * 8 + cw];
-          kw[((tile * 3 + 1) * 32 + 4 * g + cw) * 2 + r] = wlo[cw] | xw[t * 8 + 4 + cw];
-        }
+        for (int p = 0; p < MB; ++p)
+#pragma unroll
+          for (int cw = 0; cw < 4; ++cw)
+            kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[t * 4 * MB + 4 * p + cw];
       }
     } else {
       // ---- the previous page's QJL signs; this frees buffer and TMEM half bufi ^ 1 ----
@@ -1341,10 +1358,11 @@ cudaError_t bulk128_tensor_map(const void* base, int batch, int max_new, int hkv
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+template <int KB>
+cudaError_t launch_quantize_bulk128_k(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk128, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk128<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1354,7 +1372,11 @@ cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, i
   cudaError_t e = bulk128_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, &tmk);
   if (e == cudaSuccess) e = bulk128_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, &tmv);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_quantize_bulk128, dim3(grid), dim3(kTcThreads), kTcSmem, s, tmk, tmv, a, pages, batch);
+  return launch_pdl(k_quantize_bulk128<KB>, dim3(grid), dim3(kTcThreads), kTcSmem, s, tmk, tmv, a, pages, batch);
+}
+cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+  return a.lv.kb == 4 ? launch_quantize_bulk128_k<4>(a, batch, pages, sms, s)
+                      : launch_quantize_bulk128_k<3>(a, batch, pages, sms, s);
 }
 
 }  // namespace
@@ -1373,8 +1395,8 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.full = ctx->cfg.ring_size == 0;
   if (max_new < kPage) return launch_append_small(a, batch, s);  // page on ring overflow + ring rows + state
   const int pages = (max_new + kPage - 1) / kPage;
-  // the tcgen05 bulk coder serves head_dim 128 with key_bits 3; other shapes use the CUDA-core coder
-  cudaError_t e = (a.lv.d == 128 && a.lv.kb == 3 && max_new >= kPage && dt == 0)
+  // the tcgen05 bulk coder serves head_dim 128 (key_bits 3 and 4); other shapes use the CUDA-core coder
+  cudaError_t e = (a.lv.d == 128 && max_new >= kPage && dt == 0)
                       ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
                       : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
