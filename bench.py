@@ -263,10 +263,12 @@ def bench_config(world, mode="hybrid", layout="contiguous"):
     cfg = dict(workload_config(WL, mode), parallelism="replicas" if world > 1 else "single GPU")
     if layout == "paged":
         cfg["layout"] = "paged (scrambled block table)"
+    elif layout == "paged-ordered":
+        cfg["layout"] = "paged (block table in allocation order)"
     return cfg
 
 
-DECODE_SOURCES = ("tq_decode.cu", "tq_device.cuh", "tq_internal.h")
+DECODE_SOURCES = ("tq_decode.cu", "tq_decode_common.cuh", "tq_device.cuh", "tq_internal.h")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_llama8b_b1_ctx32k.md")
 
 
@@ -320,15 +322,18 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     lens = synth_lengths(wl) if wl["lens"] is not None else [ctx] * B  # context of each row at the first timed step
     max_ctx = max(lens) + extra
     full = args.mode == "full_tq"
-    paged = args.layout == "paged" and headline
+    paged = args.layout.startswith("paged") and headline
     max_pages = (max_ctx + 127) // 128
     cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=wl["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
                      max_seqs=B, max_ctx=max_ctx, seed=1, mode=args.mode if headline else "hybrid",
                      n_blocks=B * max_pages if paged else 0)
     cache = tqm.TurboQuantCache(cfg, device=dev)
     ids = torch.arange(B, dtype=torch.int32, device=dev)
-    if paged:  # every page of every row mapped to a block of a seeded permutation of the pool
-        perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
+    if paged:  # every page of every row mapped to a block of a seeded permutation of the pool (or in order)
+        if args.layout == "paged":
+            perm = torch.randperm(B * max_pages, generator=torch.Generator().manual_seed(11)).to(torch.int32)
+        else:
+            perm = torch.arange(B * max_pages, dtype=torch.int32)
         cache.block_table.copy_(perm.view(B, max_pages).to(dev))
     # after the eager step and the W warm-up replays, the first timed step of row b attends lens[b] tokens
     L0 = [n - W - 2 for n in lens]
@@ -529,7 +534,7 @@ def run_ours(args):
 
     K, W = args.steps, args.warmup
     head = measure_decode(tqm, synth, dev, WL, args, K, W, world, headline=True)
-    full, paged = args.mode == "full_tq", args.layout == "paged"
+    full, paged = args.mode == "full_tq", args.layout.startswith("paged")
     traffic = None if full or paged or WL["name"] != WORKLOADS["llama8b"]["name"] else profiled_traffic()
     head["roofline"]["traffic"] = traffic
     peak, _ = measured_peaks()
@@ -576,14 +581,16 @@ def run_ours(args):
 def bench_quantize(tqm, synth, dev, args, peak):
     import torch
     T, Hkv, L_layers, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["layers"], PREFILL["d"], PREFILL["vb"]
-    paged = getattr(args, "layout", "contiguous") == "paged"
+    layout = getattr(args, "layout", "contiguous")
+    paged = layout.startswith("paged")
     max_pages = (T + 127) // 128
     cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=PREFILL["kb"], n_layers=L_layers, n_kv_heads=Hkv,
                      n_q_heads=4 * Hkv, max_seqs=1,
                      max_ctx=T, seed=PREFILL["seed"], n_blocks=max_pages if paged else 0)
     qc = tqm.TurboQuantCache(cfg, device=dev)
     if paged:
-        perm = torch.randperm(max_pages, generator=torch.Generator().manual_seed(12)).to(torch.int32)
+        perm = (torch.randperm(max_pages, generator=torch.Generator().manual_seed(12)).to(torch.int32)
+                if layout == "paged" else torch.arange(max_pages, dtype=torch.int32))
         qc.block_table.copy_(perm.view(1, max_pages).to(dev))
     k, v = synth.kv_tokens(T, Hkv, d, seed=PREFILL["seed"], outliers=WL["outliers"], device=dev)
     k, v = k[None].contiguous(), v[None].contiguous()
@@ -926,8 +933,9 @@ def main():
                    help="the same decode and prefill shapes with another head_dim (synthetic variants)")
     p.add_argument("--key-bits", type=int, default=3, choices=[3, 4],
                    help="4: 3-bit Lloyd-Max index + QJL sign with 4-bit values (the 4-bit configuration)")
-    p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged"],
-                   help="paged: the packed pages live in a block pool addressed through a scrambled block table")
+    p.add_argument("--layout", default="contiguous", choices=["contiguous", "paged", "paged-ordered"],
+                   help="paged: the packed pages live in a block pool addressed through a scrambled block table; "
+                        "paged-ordered: the same pool with every row's blocks in allocation order")
     p.add_argument("--codec", default="", choices=["", "kivi2", "bonsai1"],
                    help="time a comparison codec over the 32K-token KV cache instead (one JSON line of its own)")
     p.add_argument("--codec-layers", type=int, default=0, help=argparse.SUPPRESS)

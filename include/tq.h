@@ -178,16 +178,15 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
                               int max_ctx_hint, tq_stream_t stream);
 
 /* tq_decode_phase: launches one phase of tq_decode_attention with the same arguments, for callers that
- * interleave the phases with other work or time them one by one. The three phases run in order on
- * one workspace:
+ * interleave the phases with other work or time them one by one. The two phases run in order on one
+ * workspace:
  *   0 = zero the workspace's arrival counters (a memset; needed once before the first phase-1 call
  *       on a workspace that was not zero-filled);
  *   1 = split-K decode over packed pages (each split CTA prepares the query: rotation, projection,
  *       f16 operands of the key bit-plane MMAs) plus the exact ring split. The last CTA of every
- *       (row, KV head) also runs the combine: log-sum-exp merge, inverse rotation, ring merge -> out;
- *   2 = nothing (accepted for callers written against separate prep and combine phases).
- * Phase 1 leaves the counters at zero, so calling 0, 1, 2 or just 1 on a zeroed workspace is
- * equivalent to one tq_decode_attention call. */
+ *       (row, KV head) also runs the combine: log-sum-exp merge, inverse rotation, ring merge -> out.
+ * Any other phase returns TQ_ERR_INVALID_ARG. Phase 1 leaves the counters at zero, so calling 0 and
+ * then 1, or just 1 on a zeroed workspace, is equivalent to one tq_decode_attention call. */
 tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream);

@@ -168,7 +168,8 @@ class TurboQuantCache(HostTables):
 
     def decode_phase(self, phase, layer, q, seq_ids, out, softmax_scale=0.0, max_ctx_hint=0, workspace=None,
                      stream=None):
-        """One phase (0 prep, 1 splits, 2 combine) of decode(); the three in order equal decode()."""
+        """One phase of decode(): 0 zeroes the workspace's arrival counters, 1 runs the decode launch (its
+        last CTA per (row, KV head) combines). 0 then 1 equals decode()."""
         batch = q.shape[0]
         ws = workspace if workspace is not None else self.workspace(batch, max_ctx_hint)
         check(self.lib.tq_decode_phase(self.ctx, phase, layer, _ptr(q), _ptr(out), _ptr(seq_ids), batch,

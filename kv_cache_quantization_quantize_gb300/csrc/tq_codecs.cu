@@ -328,6 +328,7 @@ extern "C" size_t tq_codec_kv_bytes(int codec, int n_layers, int n_kv_heads, int
 extern "C" tq_status tq_kivi2_quantize(const void* k, const void* v, int n_tokens, int n_heads, int head_dim,
                                        uint32_t* k_codes, uint16_t* k_scale, uint16_t* k_zero, uint32_t* v_codes,
                                        uint16_t* v_scale, uint16_t* v_zero, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_kivi2_quantize");
   using namespace tq;
   if (n_tokens < 0 || n_heads < 1 || head_dim < 16 || head_dim % kKiviGroup)
     return set_error(TQ_ERR_INVALID_ARG, "kivi2: n_tokens >= 0, n_heads >= 1, head_dim a multiple of 16 >= 16");
@@ -367,6 +368,7 @@ extern "C" tq_status tq_kivi2_dequantize(const uint32_t* k_codes, const uint16_t
                                          const uint32_t* v_codes, const uint16_t* v_scale, const uint16_t* v_zero,
                                          int n_tokens, int n_heads, int head_dim, void* k_out, void* v_out,
                                          tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_kivi2_dequantize");
   using namespace tq;
   if (n_tokens < 0 || n_heads < 1 || head_dim < 16 || head_dim % kKiviGroup)
     return set_error(TQ_ERR_INVALID_ARG, "kivi2: n_tokens >= 0, n_heads >= 1, head_dim a multiple of 16 >= 16");
@@ -403,6 +405,7 @@ extern "C" tq_status tq_kivi2_dequantize(const uint32_t* k_codes, const uint16_t
 
 extern "C" tq_status tq_bonsai1_quantize(const void* k, const void* v, int64_t n_rows, int head_dim, uint32_t* k_bits,
                                          uint16_t* k_scale, uint32_t* v_bits, uint16_t* v_scale, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_bonsai1_quantize");
   using namespace tq;
   if (n_rows < 0 || head_dim < kBonsaiGroup || head_dim % kBonsaiGroup)
     return set_error(TQ_ERR_INVALID_ARG, "bonsai1: n_rows >= 0 and head_dim a multiple of 128");
@@ -433,6 +436,7 @@ extern "C" tq_status tq_bonsai1_quantize(const void* k, const void* v, int64_t n
 extern "C" tq_status tq_bonsai1_dequantize(const uint32_t* k_bits, const uint16_t* k_scale, const uint32_t* v_bits,
                                            const uint16_t* v_scale, int64_t n_rows, int head_dim, void* k_out,
                                            void* v_out, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_bonsai1_dequantize");
   using namespace tq;
   if (n_rows < 0 || head_dim < kBonsaiGroup || head_dim % kBonsaiGroup)
     return set_error(TQ_ERR_INVALID_ARG, "bonsai1: n_rows >= 0 and head_dim a multiple of 128");

@@ -545,7 +545,7 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
                     : launch_pdl(k_decode<D, VB, STAGES, false, KB>, grid, dim3(decode_threads<D>()), smem, s, a);
     if (e != cudaSuccess) return e;
   }
-  return cudaSuccess;  // phase 2 (combine) runs inside phase 1's last CTA of every (row, KV head)
+  return cudaSuccess;  // the combine runs inside phase 1's last CTA of every (row, KV head)
 }
 
 }  // namespace
@@ -666,6 +666,7 @@ cudaError_t noalloc_scratch(void** out) {
 extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, float* out,
                                                  const int32_t* d_seq_ids, int batch, float softmax_scale,
                                                  int max_ctx_hint, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_attention_noalloc");
   tq_status st = tq::check_layer_ready(ctx, layer);
   if (st != TQ_OK) return st;
   if (batch < 0) return tq::set_error(TQ_ERR_INVALID_ARG, "batch is negative");

@@ -361,6 +361,7 @@ size_t tq_cache_bytes(const tq_config* cfg) {
 
 tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_bytes, tq_stream_t stream,
                             tq_ctx** out) {
+  const tq::NvtxRange nvtx_range("tq_init_codebooks");
   if (!out) return fail(TQ_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
   tq_status st = validate(cfg);
@@ -469,6 +470,7 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
 }
 
 tq_status tq_cache_bind(tq_ctx* ctx, void* d_cache, size_t cache_bytes, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_cache_bind");
   if (!ctx || !d_cache) return fail(TQ_ERR_INVALID_ARG, "ctx or d_cache is NULL");
   if (ctx->host_only) return fail(TQ_ERR_INVALID_ARG, "host-only context (created without d_tables)");
   if (cache_bytes < ctx->total_bytes)
@@ -494,6 +496,7 @@ static tq_status check_ready(const tq_ctx* ctx, int layer) {
 }
 
 tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_reset_seqs");
   if (!ctx) return fail(TQ_ERR_INVALID_ARG, "ctx is NULL");
   if (layer != -1) {
     tq_status st = check_ready(ctx, layer);
@@ -510,6 +513,7 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
 tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
                              const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
                              tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_quantize_append");
   tq_status st = check_ready(ctx, layer);
   if (st != TQ_OK) return st;
   if (dt != TQ_BF16 && dt != TQ_F32) return fail(TQ_ERR_INVALID_ARG, "dtype %d", (int)dt);
@@ -526,6 +530,7 @@ tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* 
 }
 
 tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_ring_flush");
   tq_status st = check_ready(ctx, layer);
   if (st != TQ_OK) return st;
   if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d negative", batch);
@@ -562,6 +567,7 @@ size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, i
 tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                const int32_t* d_n_q, int batch, int q_per_row, float softmax_scale,
                                void* d_workspace, size_t workspace_bytes, int max_ctx_hint, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_prefill_attention");
   tq_status st = check_ready(ctx, layer);
   if (st != TQ_OK) return st;
   if (batch < 0 || q_per_row < 1) return fail(TQ_ERR_INVALID_ARG, "batch %d / q_per_row %d", batch, q_per_row);
@@ -593,6 +599,7 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_attention");
   return decode_common(ctx, -1, layer, q, out, d_seq_ids, batch, softmax_scale, d_workspace, workspace_bytes,
                        max_ctx_hint, stream);
 }
@@ -600,7 +607,8 @@ tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out,
 tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                           int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                           int max_ctx_hint, tq_stream_t stream) {
-  if (phase < 0 || phase > 2) return fail(TQ_ERR_INVALID_ARG, "phase %d not in {0, 1, 2}", phase);
+  const tq::NvtxRange nvtx_range("tq_decode_phase");
+  if (phase < 0 || phase > 1) return fail(TQ_ERR_INVALID_ARG, "phase %d not in {0, 1}", phase);
   return decode_common(ctx, phase, layer, q, out, d_seq_ids, batch, softmax_scale, d_workspace, workspace_bytes,
                        max_ctx_hint, stream);
 }

@@ -7,6 +7,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "tq.h"
 
@@ -17,6 +18,15 @@
 #endif
 
 namespace tq {
+
+// NVTX range named after the C-ABI call it covers (Nsight Systems timelines, ncu --nvtx filters). With
+// no tool attached the push and pop are a load and a branch each.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr int kPage = 128;  // tokens per packed page = ring capacity ([Guide] §五.1 buffer_size=128)
 constexpr int kMaxG = 4;    // query heads per KV head served by one decode CTA (GQA <= 4)
