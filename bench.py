@@ -356,10 +356,16 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     ws = cache.workspace(B, max_ctx)
     s = torch.cuda.Stream(device=dev)
 
+    fused = getattr(args, "step_call", "fused") == "fused"
+
     def step():
         for l in range(L_layers):
-            cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
-            cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+            if fused:  # the one-token append and the decode in one launch
+                cache.decode_step(l, knew[l, :, 0], vnew[l, :, 0], qs[l], ids, out=outs[l], max_ctx_hint=max_ctx,
+                                  workspace=ws, stream=s)
+            else:
+                cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
+                cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
 
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -369,7 +375,9 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         step()
-    launches_per_step = L_layers * 2  # small append + split-K decode (query prep and combine inside) per layer
+    # per layer: the fused step kernel, or the small append and the split-K decode (query prep and combine
+    # inside the decode either way)
+    launches_per_step = L_layers * (1 if fused and not full else 2)  # full_tq: tq_decode_step runs both
 
     sampler = clock_sampler(dev)
     sampler.start()
@@ -447,11 +455,13 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     res = {"workload": wl["name"], "value": value, "unit": UNIT, "ms_per_step": ms_per_step, "steps": K,
            "hbm_gbs": hbm_gbs, "pct_of_8TBps": 100.0 * hbm_gbs / NOMINAL_HBM_GBS,
            "pct_of_measured_hbm": 100.0 * hbm_gbs / peak, "step_bytes": step_bytes, "roofline": roof,
-           "clocks": clocks, "gpu_launches": launches_per_step * K, "device_status": status}
+           "clocks": clocks, "gpu_launches": launches_per_step * K, "device_status": status,
+           "step_call": "tq_decode_step (append + decode in one launch per layer)" if fused
+           else "tq_quantize_append + tq_decode_attention (two launches per layer)"}
     del g2
     if headline:
         res.update(measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_e2e_warm, world, B,
-                               L_layers))
+                               L_layers, fused))
     del g
     del cache, knew, vnew, qs, outs, ws
     torch.cuda.synchronize()
@@ -459,11 +469,11 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     return res
 
 
-def measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_warm, world, B, L_layers):
+def measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_warm, world, B, L_layers, fused):
     """The step end to end with host buffers: every step copies q, k and v from pinned host memory to the
     device and the outputs back, inside the timed region. `e2e` replays the captured graph between the
-    copies; `e2e_api` calls tq_quantize_append and tq_decode_attention per layer through the Python
-    binding (ctypes -> C ABI), with no graph."""
+    copies; `e2e_api` calls the step's entry points per layer through the Python binding (ctypes -> C
+    ABI), with no graph: tq_decode_step, or tq_quantize_append and tq_decode_attention."""
     import torch
     hq = torch.empty(qs.shape, dtype=qs.dtype, pin_memory=True)
     hk = torch.empty(knew.shape, dtype=knew.dtype, pin_memory=True)
@@ -489,13 +499,18 @@ def measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_
             knew.copy_(hk, non_blocking=True)
             vnew.copy_(hv, non_blocking=True)
             for l in range(L_layers):
-                cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
-                cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
+                if fused:
+                    cache.decode_step(l, knew[l, :, 0], vnew[l, :, 0], qs[l], ids, out=outs[l], max_ctx_hint=max_ctx,
+                                      workspace=ws, stream=s)
+                else:
+                    cache.append(l, knew[l], vnew[l], ids, ones, stream=s)
+                    cache.decode(l, qs[l], ids, out=outs[l], max_ctx_hint=max_ctx, workspace=ws, stream=s)
             ho.copy_(outs, non_blocking=True)
 
     out = {}
     for key, fn, launches in (("e2e", graph_step, "one CUDA graph replay"),
-                              ("e2e_api", api_step, "per-layer tq_quantize_append + tq_decode_attention calls")):
+                              ("e2e_api", api_step, "per-layer tq_decode_step calls" if fused
+                               else "per-layer tq_quantize_append + tq_decode_attention calls")):
         for _ in range(n_warm):
             fn()
         torch.cuda.synchronize()
@@ -562,6 +577,7 @@ def run_ours(args):
         "pct_of_measured_hbm": head["pct_of_measured_hbm"],
         "roofline": head["roofline"], "e2e": head["e2e"], "e2e_api": head["e2e_api"],
         "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "device_status": head["device_status"],
+        "step_call": head["step_call"],
     }
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]
@@ -921,6 +937,9 @@ def main():
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--skip-quantize", action="store_true")
+    p.add_argument("--step-call", default="fused", choices=["fused", "separate"],
+                   help="fused: tq_decode_step (one launch per layer); separate: tq_quantize_append + "
+                        "tq_decode_attention")
     p.add_argument("--mode", default="hybrid", choices=["hybrid", "full_tq"],
                    help="full_tq: no exact recent buffer, every token quantised on append")
     p.add_argument("--prefill-chunk", type=int, default=0, metavar="TQ",

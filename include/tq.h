@@ -133,13 +133,15 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
  *     d_n_new[b] tokens.
  *   - d_seq_ids[b]: the cache slot of row b. d_n_new[b] is in [0, max_new].
  *   - Ring semantics: the ring holds the last R = L - 128*floor((L-1)/128) tokens of a length-L
- *     sequence. When an append overflows the ring, every complete 128-token block is quantised
- *     into the packed history. So a sequence is 128*floor((L-1)/128) packed tokens + R ring tokens.
+ *     sequence, so decode reads 128*floor((L-1)/128) packed tokens + R ring tokens. An append
+ *     quantises every 128-token block it completes into its packed page at once, including the
+ *     block that fills the ring to R = 128 (decode keeps reading those from the ring until the next
+ *     token starts a new ring block); so the pages of all blocks below 128*floor(L/128) are written.
  *   - f32 inputs enter the ring rounded to bf16. Blocks that never pass through the ring are
  *     quantised from the f32 values.
  *   - A row that would exceed max_ctx is skipped and sets TQ_DEV_ERR_CAPACITY.
- *   - Launches: for max_new < 128, one kernel (the page that an overflow completes, the ring rows and
- *     the new length); otherwise one quantize kernel over the pages to write, then one ring-update
+ *   - Launches: for max_new < 128, one kernel (the page of a block the append completes, the ring rows
+ *     and the new length); otherwise one quantize kernel over the pages to write, then one ring-update
  *     kernel (in full_tq mode followed by the two launches of tq_ring_flush). */
 tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
                              const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
@@ -149,12 +151,13 @@ tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* 
  * the residual cache into the main cache", [Overview] §核心技术解析, Bonsai residual cache).
  *   - Afterwards decode treats all L tokens as packed.
  *   - The bf16 copies stay in the ring until the block is complete, and that block is re-quantised
- *     with identical codes when it overflows. Quantisation is per token, so the codes do not change.
+ *     with identical codes when it completes. Quantisation is per token, so the codes do not change.
  *   - Rows with an empty ring are unchanged. */
 tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream);
 
 /* Bytes of the decode workspace for `batch` rows and a longest sequence of `max_ctx_hint` tokens
- * (0 = cfg.max_ctx). */
+ * (0 = cfg.max_ctx). The same workspace serves tq_decode_attention, tq_decode_phase and
+ * tq_decode_step. */
 size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
 
 /* tq_decode_attention: one decode step of hybrid attention for one layer ([Guide] §五.1 and §七).
@@ -166,9 +169,9 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
  *     over the packed history, and exact dot products over the ring.
  *   - One softmax runs over both.
  *   - d_workspace: at least tq_workspace_bytes(ctx, batch, max_ctx_hint) bytes, 256-byte aligned,
- *     scratch owned by the caller. It holds per-(row, KV head) arrival counters that must be zero
- *     before the first call on a workspace (zero-fill it once, or run tq_decode_phase 0); every call
- *     leaves them at zero again.
+ *     scratch owned by the caller. It starts with per-(row, KV head) and per-row arrival counters
+ *     that must be zero before the first call on a workspace (zero-fill it once); every call leaves
+ *     them at zero again.
  *   - max_ctx_hint: an upper bound on every row's length (0 = cfg.max_ctx). It only sizes the grid;
  *     a row longer than the hint sets TQ_DEV_ERR_SPLITS.
  *   - Launches: one split-K decode kernel (+ the ring split). Every split CTA rotates and projects
@@ -176,6 +179,26 @@ size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint);
 tq_status tq_decode_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                               int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                               int max_ctx_hint, tq_stream_t stream);
+
+/* tq_decode_step: one decode step of one layer in one launch: appends one new token to every row
+ * and attends q over the sequence that includes it. The results, the cache contents and the sequence
+ * state are identical to tq_quantize_append with d_n_new[b] = 1 followed by tq_decode_attention, in
+ * one kernel instead of two ([Guide] §五.1 ring buffer, §三 hybrid decode, §二 pipeline).
+ *   - k_new, v_new: device [batch][n_kv_heads][d] of dtype dt (bf16 or f32), aligned to 4 elements.
+ *   - q, out, d_seq_ids, softmax_scale, d_workspace, workspace_bytes: as tq_decode_attention.
+ *     max_ctx_hint must cover every row's length after its new token.
+ *   - The ring split of each (row, KV head) takes the new token from k_new / v_new, attends to it and
+ *     writes it into the ring. When the token fills the ring to 128, that CTA also codes the 128
+ *     ring tokens into their packed page (the next step then starts a new ring block over it). The
+ *     last (row, KV head) of a row to finish publishes the row's new length.
+ *   - A row already at max_ctx gets no token (TQ_DEV_ERR_CAPACITY) and is decoded as it stands; an
+ *     invalid slot sets TQ_DEV_ERR_SEQ_ID.
+ *   - A launch of this library that directly follows a decode step of the same layer on the same
+ *     stream reads the sequence state only after its stream wait (the step publishes it at its end).
+ *   - full_tq contexts (ring_size 0) run it as the append and decode launches. */
+tq_status tq_decode_step(tq_ctx* ctx, int layer, const void* k_new, const void* v_new, tq_dtype dt, const void* q,
+                         float* out, const int32_t* d_seq_ids, int batch, float softmax_scale, void* d_workspace,
+                         size_t workspace_bytes, int max_ctx_hint, tq_stream_t stream);
 
 /* tq_decode_phase: launches one phase of tq_decode_attention with the same arguments, for callers that
  * interleave the phases with other work or time them one by one. The two phases run in order on one

@@ -148,6 +148,24 @@ class TurboQuantCache(HostTables):
                                            float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint, _stream(stream)))
         return out
 
+    def decode_step(self, layer, k_new, v_new, q, seq_ids, softmax_scale=0.0, out=None, max_ctx_hint=0,
+                    workspace=None, stream=None):
+        """One decode step in one launch: appends k_new, v_new [batch, n_kv_heads, d] (bf16/f32, one token
+        per row) and returns the attention of q [batch, n_q_heads, d] bf16 over the sequence with it (f32).
+        Equal to append(..., n_new=1) followed by decode()."""
+        assert q.is_cuda and q.dtype == torch.bfloat16 and q.is_contiguous()
+        assert k_new.is_cuda and k_new.is_contiguous() and v_new.is_contiguous() and k_new.shape == v_new.shape
+        assert k_new.dtype == v_new.dtype and k_new.dtype in (torch.bfloat16, torch.float32)
+        dt = TQ_BF16 if k_new.dtype == torch.bfloat16 else TQ_F32
+        batch = q.shape[0]
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        ws = workspace if workspace is not None else self.workspace(batch, max_ctx_hint)
+        check(self.lib.tq_decode_step(self.ctx, layer, _ptr(k_new), _ptr(v_new), dt, _ptr(q), _ptr(out), _ptr(seq_ids),
+                                      batch, float(softmax_scale), _ptr(ws), ws.numel(), max_ctx_hint,
+                                      _stream(stream)))
+        return out
+
     def prefill_workspace(self, batch, q_per_row, max_ctx_hint=0):
         n = self.lib.tq_prefill_workspace_bytes(self.ctx, batch, q_per_row, max_ctx_hint)
         return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)

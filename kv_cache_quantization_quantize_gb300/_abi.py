@@ -37,6 +37,8 @@ _SIGS = {
     "tq_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int]),
     "tq_decode_attention": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p, c_size_t,
                                     c_int, c_void_p]),
+    "tq_decode_step": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float,
+                               c_void_p, c_size_t, c_int, c_void_p]),
     "tq_prefill_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int, c_int]),
     "tq_prefill_attention": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_float,
                                      c_void_p, c_size_t, c_int, c_void_p]),

@@ -24,6 +24,7 @@
 #include <cuda_runtime.h>
 
 #include "tq_decode_common.cuh"
+#include "tq_quantize_common.cuh"
 
 namespace tq {
 namespace {
@@ -43,6 +44,29 @@ std::atomic<int> g_fault_polls{0};
 // columns; each lane's two C columns belong to query c / 2.
 // head_dim 256 with 2-bit values runs two CTAs per SM (128 registers, 104 KB of shared memory each);
 // its other shapes need more than half of an SM's shared memory and keep one.
+// Decode step: the new token has filled the ring of (row b, KV head h) to 128 tokens (L, the length
+// with it, is a multiple of 128). The ring CTA codes those 128 tokens into their packed page now, so
+// that the step whose token starts the next ring block finds every block below it coded (appends keep
+// the same rule). The tokens are the ring rows before the new one and the new token from the input.
+template <int D, int KB, int NT>
+__device__ __noinline__ void step_code_block(const DecodeArgs& a, int b, int h, int slot, int L, uint8_t* smem) {
+  AppendArgs ap;
+  ap.lv = a.lv;
+  ap.k = a.k_new;
+  ap.v = a.v_new;
+  ap.dt = a.new_dt;
+  ap.seq_ids = a.seq_ids;
+  ap.n_new = nullptr;
+  ap.max_new = 1;
+  ap.flush = 0;
+  ap.full = 0;
+  const int Np = L - kPage;  // the ring's first position
+  for (int q32 = 0; q32 < 4; ++q32) {
+    __syncthreads();  // shared memory is free: the ring split and combine, or the previous block, are done
+    quantize_page_cta<D, KB, NT>(ap, b, h, slot, L - 1, Np, Np / kPage, kPage, q32, smem);
+  }
+}
+
 template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1>
 __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 : 1) k_decode(DecodeArgs a) {
   constexpr int NCOL = qcols<QP>();
@@ -63,6 +87,7 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int stream = warp / SW, tg = warp & 3, hf = (warp % SW) >> 2;
   const int nsp = a.plan.n_splits;
+  if (a.late_state) pdl_wait();  // the previous launch was a decode step of this layer: see DecodeArgs
   float* part = reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                          (((size_t)b * lv.Hkv + h) * (nsp + 1) + sp) * a.plan.part_stride);
   // Every kernel of this library starts its dependents only after its own stream wait, so what this
@@ -84,12 +109,17 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   if (sp == nsp) {
     pdl_wait();
     pdl_launch();
+    int L1 = 0, Np1, P1;
+    bool stepped = false;
+    if (QP == 1 && a.k_new) seq_view(a, slot, L1, Np1, P1, stepped);  // before this unit can finish
     const bool smem_ok = ring_split<D, NT, QP>(a, b, h, slot, part, smem);
     finish_unit<D, NT, QP>(a, b, h, reinterpret_cast<float*>(smem + 128), smem_ok);
+    if (QP == 1 && stepped && smem_ok && L1 % kPage == 0) step_code_block<D, KB, NT>(a, b, h, slot, L1, smem + 128);
     return;
   }
   int L, Np, P;
-  seq_packed(lv, slot, L, Np, P);
+  bool stepped;
+  seq_view(a, slot, L, Np, P, stepped);
   // a prefill query sees the packed tokens before its own position; Pq: this lane's query
   const int P0 = min(P, row_len(a, QP * b, L)), P1 = QP == 1 ? P0 : min(P, row_len(a, QP * b + 1, L));
   const int Pq = (QP == 1 || (lane & 3) < 2) ? P0 : P1;
@@ -586,7 +616,7 @@ int decode_resident_ctas(const tq_ctx* ctx) {
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
-                          const int32_t* n_q, int qp) {
+                          const int32_t* n_q, int qp, const void* k_new, const void* v_new, int new_dt, int late_state) {
   if (qp == 2 && (qpr % 2 != 0 || ctx->cfg.n_blocks > 0)) return cudaErrorInvalidValue;
   DecodeArgs a;
   a.lv = layer_view(ctx, layer);
@@ -600,6 +630,10 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.plan = plan;
   a.fault_stage = g_fault_stage.load();
   a.fault_polls = (uint32_t)g_fault_polls.load();
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.new_dt = new_dt;
+  a.late_state = late_state;
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   if (kb == 4) {
     if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);
@@ -682,6 +716,7 @@ extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const v
                                           "scratch of tq_decode_attention_noalloc");
   tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
   plan.cnt_off = 0;
+  plan.row_cnt_off = 0;  // no decode step runs on this scratch
   plan.part_off = tq::kNoAllocCounters * sizeof(int32_t);
   plan.bytes = (plan.part_off + plan.part_stride * (size_t)batch * ctx->cfg.n_kv_heads * (plan.n_splits + 1) + 255) /
                256 * 256;
@@ -697,7 +732,8 @@ extern "C" tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const v
   cudaError_t e = tq::noalloc_scratch(&scratch);
   if (e != cudaSuccess) return tq::set_error(TQ_ERR_CUDA, cudaGetErrorString(e));
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
-  e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, scratch, plan, -1, (cudaStream_t)stream);
+  e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, scratch, plan, -1, (cudaStream_t)stream, 1,
+                        nullptr, 1, nullptr, nullptr, 0, tq::step_follows(ctx, layer, (cudaStream_t)stream) ? 1 : 0);
   if (e != cudaSuccess) return tq::set_error(TQ_ERR_CUDA, cudaGetErrorString(e));
   return tq::set_error(TQ_OK, "");
 }

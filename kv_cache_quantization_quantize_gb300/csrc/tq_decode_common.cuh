@@ -25,6 +25,15 @@ struct DecodeArgs {
   // after `fault_polls` polls. -1 in normal use.
   int fault_stage;
   uint32_t fault_polls;
+  // Decode step (tq_decode_step): one new token per row, k_new / v_new [B][Hkv][D] (bf16, or fp32 when
+  // new_dt = 1), is appended by this launch and attended to. nullptr for a plain decode.
+  const void* k_new;
+  const void* v_new;
+  int new_dt;
+  // 1: the previous launch on the stream was a decode step of this layer, which changes the sequence
+  // state and may code a page after it released its dependents; this launch then reads the state and
+  // pages only after its stream wait.
+  int late_state;
 };
 
 namespace {
@@ -114,11 +123,28 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
 }
 
 
-__device__ __forceinline__ void seq_packed(const LayerView& lv, int slot, int& L, int& Np, int& P) {
+// The sequence as a decode CTA sees it: L tokens, of which the first Np lie in packed blocks before
+// the ring and P = Np + F are read packed (F: ring tokens a flush coded). In a decode step the row is
+// seen with its new token (stepped; a row already at max_ctx takes none and is decoded as it stands).
+// Every CTA of a row reads the state before any of them can change it (the row's length is published
+// by the last (row, KV head) unit to finish, see row_arrive).
+__device__ __forceinline__ void seq_view(const DecodeArgs& a, int slot, int& L, int& Np, int& P, bool& stepped) {
+  const LayerView& lv = a.lv;
   L = lv.state[2 * slot];
-  const int F = lv.state[2 * slot + 1];
+  int F = lv.state[2 * slot + 1];
+  const int Np0 = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+  stepped = a.k_new != nullptr && L < lv.max_ctx;
+  if (stepped) ++L;
   Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+  if (Np != Np0) F = 0;  // the new token starts a new ring block
   P = Np + F;
+}
+
+// One element of the step's new token (K: which = 0, V: 1) as bf16 bits, as an append stores it.
+__device__ __forceinline__ uint16_t new_token_elem(const DecodeArgs& a, int which, int b, int h, int j) {
+  const size_t i = ((size_t)b * a.lv.Hkv + h) * a.lv.d + j;
+  const void* base = which ? a.v_new : a.k_new;
+  return a.new_dt ? f32_to_bf16_rn(static_cast<const float*>(base)[i]) : static_cast<const uint16_t*>(base)[i];
 }
 
 // Cache slot of (virtual) row b, and the number of the sequence's tokens it attends to: all L for
@@ -446,7 +472,8 @@ __device__ __noinline__ bool ring_split(const DecodeArgs& a, int b, int h, int s
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int L, Np, P;
-  seq_packed(lv, slot, L, Np, P);
+  bool stepped;
+  seq_view(a, slot, L, Np, P, stepped);
   // ring tokens are positions P .. Lq - 1 of each query row
   const int n0 = row_len(a, QP * b, L) - P, n1 = QP == 1 ? n0 : row_len(a, QP * b + 1, L) - P;
   const int F = P - Np, n = max(n0, n1);
@@ -454,6 +481,9 @@ __device__ __noinline__ bool ring_split(const DecodeArgs& a, int b, int h, int s
     write_empty_partial(part, D, tid, NT, NCOL);
     return true;
   }
+  // a decode step's new token is ring row n - 1: it comes from the input (and is written to the ring
+  // here); the rows before it come from the ring
+  const int nm = stepped ? n - 1 : n;
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem_raw);
   const uint16_t* krows = reinterpret_cast<const uint16_t*>(smem_raw + 128);  // [n][D] bf16
   const uint16_t* vrows = KV ? krows + (size_t)kPage * D : krows;             // [n][D] bf16
@@ -462,16 +492,35 @@ __device__ __noinline__ bool ring_split(const DecodeArgs& a, int b, int h, int s
   float* qs = red + 4 * NCOL;                                                            // [NCOL][D]
   const uint16_t* rk = lv.ring + (((size_t)slot * lv.Hkv + h) * 2) * kPage * D + (size_t)F * D;
   const uint16_t* rv = rk + (size_t)kPage * D;
-  const uint32_t bytes = (uint32_t)n * D * 2;
+  const uint32_t bytes = (uint32_t)nm * D * 2;
   if (tid == 0) {
     mbar_init(bar, 1);
     if (KV) mbar_init(bar + 1, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(smem_raw + 128, rk, bytes, bar);
+    if (bytes) {
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_raw + 128, rk, bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
     if (KV) {
-      mbar_expect_tx(bar + 1, bytes);
-      bulk_g2s(smem_raw + 128 + 2 * kPage * D, rv, bytes, bar + 1);
+      if (bytes) {
+        mbar_expect_tx(bar + 1, bytes);
+        bulk_g2s(smem_raw + 128 + 2 * kPage * D, rv, bytes, bar + 1);
+      } else {
+        mbar_arrive(bar + 1);
+      }
+    }
+  }
+  if (QP == 1 && stepped) {  // the new token: shared-memory row nm (V later when it shares K's rows) and the ring
+    uint16_t* kr = reinterpret_cast<uint16_t*>(smem_raw + 128) + (size_t)nm * D;
+    uint16_t* gk = lv.ring + ((((size_t)slot * lv.Hkv + h) * 2) * kPage + F + nm) * D;
+    for (int j = tid; j < D; j += NT) {
+      const uint16_t kv = new_token_elem(a, 0, b, h, j), vv = new_token_elem(a, 1, b, h, j);
+      kr[j] = kv;
+      gk[j] = kv;
+      gk[(size_t)kPage * D + j] = vv;
+      if (KV) kr[(size_t)kPage * D + j] = vv;  // the V rows follow the K rows
     }
   }
   const int G = lv.G;
@@ -513,8 +562,16 @@ __device__ __noinline__ bool ring_split(const DecodeArgs& a, int b, int h, int s
   __syncthreads();  // every K row has been read
   if (!KV && tid == 0 && ok_k) {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(smem_raw + 128, rv, bytes, bar);
+    if (bytes) {
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_raw + 128, rv, bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+  }
+  if (!KV && QP == 1 && stepped) {  // the new token's V row, where its K row was
+    uint16_t* vr = reinterpret_cast<uint16_t*>(smem_raw + 128) + (size_t)nm * D;
+    for (int j = tid; j < D; j += NT) vr[j] = new_token_elem(a, 1, b, h, j);
   }
   if (warp < NCOL) {  // softmax statistics: warp g reduces column g over its query's ring tokens
     const int nw = warp < kMaxG ? n0 : n1;
@@ -714,6 +771,33 @@ __device__ __forceinline__ void zero_unit_out(const DecodeArgs& a, int b, int h)
 // merges all of them (an arrival counter; no CTA waits on another), with `scratch` (shared memory, room
 // for 4 (NT/32) + 2 NCOL 1026 floats) as its working space. smem_ok = false: this CTA's shared memory may
 // still receive a copy, so a last CTA writes zeros instead of combining.
+// Decode step: the last (row, KV head) unit of a row to finish publishes the row's new length (and a
+// new ring block's F = 0). Every CTA of the row has read the old state by then: a unit finishes only
+// after all of its CTAs arrived, and they read the state before arriving. The per-row counters follow
+// the per-unit ones in the workspace and are left at zero.
+__device__ __noinline__ void row_arrive(const DecodeArgs& a, int b) {
+  if (threadIdx.x != 0) return;
+  int* rc = reinterpret_cast<int*>(a.ws + a.plan.row_cnt_off) + b;
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(rc) : "memory");
+  if (old != a.lv.Hkv - 1) return;
+  *rc = 0;
+  const LayerView& lv = a.lv;
+  const int slot = a.seq_ids[b];
+  if (slot < 0 || slot >= lv.max_seqs) {
+    set_status(lv.status, TQ_DEV_ERR_SEQ_ID);
+    return;
+  }
+  const int L = lv.state[2 * slot];
+  if (L >= lv.max_ctx) {
+    set_status(lv.status, TQ_DEV_ERR_CAPACITY);
+    return;
+  }
+  const int Np = L > 0 ? kPage * ((L - 1) / kPage) : 0, Np2 = kPage * (L / kPage);
+  lv.state[2 * slot] = L + 1;
+  if (Np2 != Np) lv.state[2 * slot + 1] = 0;
+}
+
 template <int D, int NT, int QP = 1>
 __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, float* scratch, bool smem_ok = true) {
   __shared__ int s_last;
@@ -729,11 +813,9 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, floa
   }
   __syncthreads();
   if (!s_last) return;
-  if (!smem_ok) {
-    zero_unit_out<D, NT, QP>(a, b, h);
-    return;
-  }
-  combine_unit<D, NT, QP>(a, b, h, scratch);
+  if (!smem_ok) zero_unit_out<D, NT, QP>(a, b, h);
+  else combine_unit<D, NT, QP>(a, b, h, scratch);
+  if (QP == 1 && a.k_new) row_arrive(a, b);
 }
 
 }  // namespace

@@ -313,8 +313,10 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
   const int d = c.head_dim;
   // The arrival counters sit at a fixed place (offset 0, sized for max_seqs rows), so that calls with
   // other batch sizes or hints on the same workspace find them where the last call left them (zero).
+  const size_t rows = (size_t)std::max(c.max_seqs, cnt_rows);
   p.cnt_off = 0;
-  p.part_off = align_up(sizeof(int32_t) * (size_t)std::max(c.max_seqs, cnt_rows) * c.n_kv_heads, 256);
+  p.row_cnt_off = sizeof(int32_t) * rows * c.n_kv_heads;  // then one counter per row (decode step)
+  p.part_off = align_up(p.row_cnt_off + sizeof(int32_t) * rows, 256);
   p.part_stride = align_up((size_t)(2 * ncol + ncol * d) * sizeof(float), 16);  // m, l [ncol], o [ncol][d]
   p.bytes = align_up(p.part_off + p.part_stride * (size_t)units * (p.n_splits + 1), 256);
   return p;
@@ -323,6 +325,17 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
 tq_status set_error(tq_status st, const char* msg) {
   g_last_error = msg ? msg : "";
   return st;
+}
+
+bool step_follows(tq_ctx* ctx, int layer, cudaStream_t s) {
+  const bool follows = ctx->step_layer >= 0 && ctx->step_layer == layer && ctx->step_stream == (void*)s;
+  ctx->step_layer = -1;
+  return follows;
+}
+
+void record_step(tq_ctx* ctx, int layer, cudaStream_t s) {
+  ctx->step_layer = layer;
+  ctx->step_stream = (void*)s;
 }
 
 tq_status check_layer_ready(const tq_ctx* ctx, int layer) {
@@ -506,6 +519,7 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
   }
   if (batch < 0 || (batch > 0 && !d_seq_ids)) return fail(TQ_ERR_INVALID_ARG, "bad batch / d_seq_ids");
   if (batch == 0) return ok();
+  tq::step_follows(ctx, layer, (cudaStream_t)stream);  // a plain launch: it waits for the whole step
   cudaError_t e = tq::launch_reset(ctx, layer, d_seq_ids, batch, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "reset kernel");
 }
@@ -525,6 +539,7 @@ tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* 
   const size_t esz = dt == TQ_BF16 ? 2 : 4;
   if (reinterpret_cast<uintptr_t>(k) % (esz * 4) || reinterpret_cast<uintptr_t>(v) % (esz * 4))
     return fail(TQ_ERR_INVALID_ARG, "k/v must be %zu-byte aligned", esz * 4);
+  tq::step_follows(ctx, layer, (cudaStream_t)stream);  // the append kernels read the state after their wait
   cudaError_t e = tq::launch_append(ctx, layer, k, v, (int)dt, d_seq_ids, d_n_new, batch, max_new, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "append kernels");
 }
@@ -537,6 +552,7 @@ tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
   if (batch == 0) return ok();
   if (!d_seq_ids) return fail(TQ_ERR_INVALID_ARG, "d_seq_ids is NULL");
   if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  tq::step_follows(ctx, layer, (cudaStream_t)stream);  // the flush kernels read the state after their wait
   cudaError_t e = tq::launch_flush(ctx, layer, d_seq_ids, batch, (cudaStream_t)stream);
   return e == cudaSuccess ? ok() : cuda_fail(e, "flush kernel");
 }
@@ -588,6 +604,7 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
   // Phase 0 zeroes the arrival counters with a memset. It also keeps the prefill kernel from
   // overlapping a preceding append (a memset waits for the whole kernel before it), which the kernel
   // relies on: it reads the sequence lengths, which fix every query's causal extent, before its wait.
+  tq::step_follows(ctx, layer, (cudaStream_t)stream);  // the counter memset waits for the whole step
   cudaError_t e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, cta_rows, scale, d_workspace, plan, 0,
                                     (cudaStream_t)stream, q_per_row, d_n_q, qp);  // zero the counters
   if (e == cudaSuccess)
@@ -613,6 +630,44 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
                        max_ctx_hint, stream);
 }
 
+tq_status tq_decode_step(tq_ctx* ctx, int layer, const void* k_new, const void* v_new, tq_dtype dt, const void* q,
+                         float* out, const int32_t* d_seq_ids, int batch, float softmax_scale, void* d_workspace,
+                         size_t workspace_bytes, int max_ctx_hint, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_decode_step");
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  if (dt != TQ_BF16 && dt != TQ_F32) return fail(TQ_ERR_INVALID_ARG, "dtype %d", (int)dt);
+  if (batch < 0) return fail(TQ_ERR_INVALID_ARG, "batch %d negative", batch);
+  if (batch == 0) return ok();
+  if (!k_new || !v_new || !q || !out || !d_seq_ids || !d_workspace)
+    return fail(TQ_ERR_INVALID_ARG, "NULL k_new/v_new/q/out/d_seq_ids/d_workspace");
+  if (batch > ctx->cfg.max_seqs) return fail(TQ_ERR_CAPACITY, "batch %d > max_seqs %d", batch, ctx->cfg.max_seqs);
+  const size_t esz = dt == TQ_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(k_new) % (esz * 4) || reinterpret_cast<uintptr_t>(v_new) % (esz * 4))
+    return fail(TQ_ERR_INVALID_ARG, "k_new/v_new must be %zu-byte aligned", esz * 4);
+  if (reinterpret_cast<uintptr_t>(q) % 16 || reinterpret_cast<uintptr_t>(out) % 16)
+    return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
+  if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
+  const tq::DecodePlan plan = tq::decode_plan(ctx, batch, max_ctx_hint);
+  if (workspace_bytes < plan.bytes)
+    return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+  const cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  if (ctx->cfg.ring_size == 0) {  // full_tq: the append codes the token into its page, then the decode
+    tq::step_follows(ctx, layer, s);
+    e = tq::launch_append(ctx, layer, k_new, v_new, (int)dt, d_seq_ids, nullptr, batch, 1, s);
+    if (e == cudaSuccess) e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, -1, s);
+  } else {
+    const int late = tq::step_follows(ctx, layer, s) ? 1 : 0;
+    e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, -1, s, 1, nullptr, 1, k_new,
+                          v_new, (int)dt, late);
+    if (e == cudaSuccess) tq::record_step(ctx, layer, s);
+  }
+  return e == cudaSuccess ? ok() : cuda_fail(e, "decode step kernels");
+}
+
 static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                int batch, float softmax_scale, void* d_workspace, size_t workspace_bytes,
                                int max_ctx_hint, tq_stream_t stream) {
@@ -631,7 +686,8 @@ static tq_status decode_common(tq_ctx* ctx, int phase, int layer, const void* q,
     return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
   cudaError_t e =
-      tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, phase, (cudaStream_t)stream);
+      tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch, scale, d_workspace, plan, phase, (cudaStream_t)stream, 1,
+                        nullptr, 1, nullptr, nullptr, 0, tq::step_follows(ctx, layer, (cudaStream_t)stream) ? 1 : 0);
   return e == cudaSuccess ? ok() : cuda_fail(e, "decode kernels");
 }
 

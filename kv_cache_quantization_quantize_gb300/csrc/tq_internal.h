@@ -168,6 +168,9 @@ struct tq_ctx {
   std::vector<uint16_t> S;  // bf16 bits, row-major
   double cent[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // 2^(key_bits-1) used
   double bnd[7] = {0, 0, 0, 0, 0, 0, 0};
+  // the last launch of this context, if it was a decode step: its layer (-1: none) and stream
+  int step_layer = -1;
+  void* step_stream = nullptr;
 };
 
 namespace tq {
@@ -201,6 +204,7 @@ struct DecodePlan {
   size_t part_off, part_stride;  // per (row, kv head, split) partial
   size_t cnt_off;                // per (row, kv head) int32 arrival counters at offset 0, room for
                                  // max_seqs rows (left at zero by every call)
+  size_t row_cnt_off;            // per row int32 counters of the decode step's units (left at zero)
   size_t bytes;
 };
 // cnt_rows: rows the arrival counters have room for (at least max_seqs; prefill rows per query).
@@ -222,9 +226,17 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
                           const int32_t* seq_ids, const int32_t* n_new, int batch, int max_new, cudaStream_t s);
 cudaError_t launch_flush(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
 cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, int batch, cudaStream_t s);
-// phase -1 = all three phases; 0 = prep, 1 = splits, 2 = combine.
+// phase -1 = the whole decode; 0 = zero the arrival counters, 1 = the decode launch. k_new / v_new
+// (one token per row, dtype new_dt): a decode step that appends them in the same launch.
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr = 1,
-                          const int32_t* n_q = nullptr, int qp = 1);
+                          const int32_t* n_q = nullptr, int qp = 1, const void* k_new = nullptr,
+                          const void* v_new = nullptr, int new_dt = 0, int late_state = 0);
+// Decode launches read a row's state (and the pages it implies) before their stream wait. That is safe
+// after every launch of this library except a decode step of the same layer on the same stream (it
+// publishes the state at its end). step_follows() says whether the last launch of ctx on stream s was
+// such a step (and forgets it); every launching entry point calls it, tq_decode_step then records itself.
+bool step_follows(tq_ctx* ctx, int layer, cudaStream_t s);
+void record_step(tq_ctx* ctx, int layer, cudaStream_t s);
 
 }  // namespace tq
