@@ -659,6 +659,11 @@ def bench_prefill(args):
     dev = torch.device("cuda", 0)
     L_layers, Hq, Hkv, d, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["ctx"], WL["vb"]
     Tq = args.prefill_chunk
+    from kv_cache_quantization_quantize_gb300 import _abi, build as _build
+    _build.build()
+    force_cc = getattr(args, "prefill_path", "auto") == "cuda-core"
+    _abi.load().tq_debug_prefill_path(1 if force_cc else 0)
+    tc = not force_cc and d == 128 and WL["kb"] == 3 and Hq == 4 * Hkv
     cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
                      max_seqs=1,
                      max_ctx=ctx, seed=1)
@@ -692,7 +697,9 @@ def bench_prefill(args):
                       "unit": "query-tok/s", "ms_per_chunk": ms, "ms_per_layer": ms / L_layers,
                       "config": {"workload": f"{WL['name']}: prefill chunk of {Tq} queries at the end of a "
                                              f"{ctx}-token sequence", "layers": L_layers},
-                      "path": "one split-K decode launch over chunk-query rows (causal length per row)",
+                      "path": ("tcgen05: tiles of 32 queries x 4 heads, key planes and values expanded once per page "
+                               "and tile, scores and P.V into TMEM; then a ring-only decode launch") if tc
+                      else "one split-K decode launch over chunk-query rows (causal length per row)",
                       "device_status": status}), flush=True)
 
 
@@ -942,6 +949,8 @@ def main():
                         "tq_decode_attention")
     p.add_argument("--mode", default="hybrid", choices=["hybrid", "full_tq"],
                    help="full_tq: no exact recent buffer, every token quantised on append")
+    p.add_argument("--prefill-path", default="auto", choices=["auto", "cuda-core"],
+                   help="with --prefill-chunk: cuda-core forces the decode-kernel path where tcgen05 applies")
     p.add_argument("--prefill-chunk", type=int, default=0, metavar="TQ",
                    help="time prefill attention of a TQ-token chunk instead (one JSON line of its own)")
     p.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS),

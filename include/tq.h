@@ -225,11 +225,16 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *   - d_workspace: at least tq_prefill_workspace_bytes(ctx, batch, q_per_row, max_ctx_hint) bytes,
  *     256-byte aligned; its arrival counters are zeroed by every call (one memset).
  *   - batch * q_per_row <= 65535.
- *   - Launches: the memset and one split-K decode kernel over batch * q_per_row query rows (the
+ *   - Launches, head_dim 128 with key_bits 3 and 4 query heads per KV head: a tcgen05 kernel over
+ *     tiles of 128 query rows (32 queries x the 4 query heads of one KV head) that expands each page's
+ *     key bits and values once per tile and computes scores and P.V on the tensor cores into TMEM,
+ *     writing one partial per (query, KV head, history split); then a decode launch that runs only
+ *     the exact ring split of each (query, KV head) and combines.
+ *   - Other shapes: the memset and one split-K decode kernel over batch * q_per_row query rows (the
  *     rows of one sequence read the same pages, mostly from L2). With an even q_per_row and a
  *     contiguous cache, each CTA takes two adjacent query rows of a sequence in the MMAs' 8 query
- *     columns, so they share the expanded key bits. The workspace size depends on this choice;
- *     tq_prefill_workspace_bytes makes the same one. */
+ *     columns, so they share the expanded key bits.
+ *   - The workspace size depends on these choices; tq_prefill_workspace_bytes makes the same ones. */
 size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint);
 tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
                                const int32_t* d_n_q, int batch, int q_per_row, float softmax_scale,
@@ -266,6 +271,12 @@ tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, flo
  * stage = -1 turns the hook off (the default). Returns TQ_ERR_INVALID_ARG for values out of range.
  * Process-wide; set it only while no other thread launches decodes. */
 tq_status tq_debug_decode_wait_fault(int stage, int polls);
+
+/* Test hook for the two prefill paths (not part of the prefill itself): mode 1 makes every following
+ * tq_prefill_attention (and tq_prefill_workspace_bytes) take the CUDA-core decode-kernel path even where
+ * the tcgen05 path applies; mode 0 (the default) chooses automatically. Returns TQ_ERR_INVALID_ARG for
+ * other values. Process-wide; set it only while no other thread calls the prefill. */
+tq_status tq_debug_prefill_path(int mode);
 
 /* Synchronises `stream` and reads the device status word. It returns TQ_OK if the word is zero.
  * Otherwise it returns TQ_ERR_DEVICE and stores the word in *word (if non-NULL). `clear` != 0

@@ -1,6 +1,7 @@
 // Host side of libtq: argument validation, tables (codebook, rotation signs, QJL matrix), cache
 // layout, canonical record conversion and the C ABI entry points.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -574,10 +575,31 @@ static int prefill_qp(const tq_ctx* ctx, int q_per_row) {
   return q_per_row % 2 == 0 && ctx->cfg.n_blocks == 0 && tq::decode_pairs_fit(ctx) ? 2 : 1;
 }
 
+static std::atomic<int> g_prefill_path{0};  // tq_debug_prefill_path: 1 forces the CUDA-core path
+
+static bool prefill_tc(const tq_ctx* ctx) { return g_prefill_path.load() == 0 && tq::prefill_tc_eligible(ctx); }
+
+// Workspace plan of the tcgen05 prefill: one query per row (4 columns), n_splits history partials from the
+// tensor-core kernel and the ring partial.
+static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
+  const int rows = batch * q_per_row;
+  tq::DecodePlan p = tq::decode_plan(ctx, rows, max_ctx_hint, rows, tq::kMaxG);
+  p.n_splits = tq::prefill_tc_splits(ctx, batch, q_per_row, max_ctx_hint);
+  p.bytes = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * (p.n_splits + 1), 256);
+  return p;
+}
+
 size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
   if (!ctx || batch < 1 || q_per_row < 1 || (long long)batch * q_per_row > 65535) return 0;
+  if (prefill_tc(ctx)) return prefill_tc_plan(ctx, batch, q_per_row, max_ctx_hint).bytes;
   const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;
   return tq::decode_plan(ctx, cta_rows, max_ctx_hint, cta_rows, tq::kMaxG * qp).bytes;
+}
+
+tq_status tq_debug_prefill_path(int mode) {
+  if (mode != 0 && mode != 1) return fail(TQ_ERR_INVALID_ARG, "prefill path mode %d not in {0, 1}", mode);
+  g_prefill_path.store(mode);
+  return ok();
 }
 
 tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* d_seq_ids,
@@ -596,6 +618,21 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
     return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
+  if (prefill_tc(ctx)) {
+    const tq::DecodePlan plan = prefill_tc_plan(ctx, batch, q_per_row, max_ctx_hint);
+    if (workspace_bytes < plan.bytes)
+      return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
+    const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
+    const cudaStream_t s = (cudaStream_t)stream;
+    // Both kernels read the sequence state after their stream wait; the ring-only decode launch needs no
+    // arrival counters (each of its CTAs is the only one of its unit).
+    tq::step_follows(ctx, layer, s);
+    cudaError_t e = tq::launch_prefill_tc(ctx, layer, q, d_seq_ids, d_n_q, batch, q_per_row, scale, d_workspace, plan, s);
+    if (e == cudaSuccess)
+      e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch * q_per_row, scale, d_workspace, plan, 1, s, q_per_row,
+                            d_n_q, 1, nullptr, nullptr, 0, 0, 1);
+    return e == cudaSuccess ? ok() : cuda_fail(e, "prefill attention kernels");
+  }
   const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;
   const tq::DecodePlan plan = tq::decode_plan(ctx, cta_rows, max_ctx_hint, cta_rows, tq::kMaxG * qp);
   if (workspace_bytes < plan.bytes)

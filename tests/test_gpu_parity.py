@@ -384,15 +384,59 @@ def test_prefill_chunk_attention(d, vb, kbits, chunk, G):
     appended in one call (the second row padded to chunk[0] queries). Every chunk query attends causally
     over the cache after the append (packed tokens through their codes, ring tokens exactly), as the
     oracle's masked prefill attention gives it on the device's own records and ring; padding queries
-    output zeros. An even number of query slots per row takes two query rows per CTA (their causal
-    lengths differ inside a CTA, and a query next to a padding query shares its CTA); an odd number
-    takes one."""
+    output zeros. head_dim 128 with key_bits 3 and G 4 takes the tcgen05 path (tiles of 32 queries x 4
+    heads); elsewhere an even number of query slots per row takes two query rows per CTA (their causal
+    lengths differ inside a CTA, and a query next to a padding query shares its CTA), an odd number one."""
+    _prefill_chunk_case(d, vb, kbits, chunk, G, [300, 129])
+
+
+@pytest.fixture
+def cuda_core_prefill():
+    """Every prefill of the test takes the CUDA-core (decode kernel) path, also where tcgen05 applies."""
+    from kv_cache_quantization_quantize_gb300 import _abi
+    lib = _abi.load()
+    assert lib.tq_debug_prefill_path(1) == _abi.TQ_OK
+    yield
+    assert lib.tq_debug_prefill_path(0) == _abi.TQ_OK
+
+
+@pytest.mark.parametrize("vb,chunk", [(2, (200, 37)), (2, (199, 36)), (4, (200, 37))])
+def test_prefill_chunk_attention_cuda_core_path(cuda_core_prefill, vb, chunk):
+    """The shapes that take the tcgen05 prefill by default (head_dim 128, key_bits 3, G 4), forced onto the
+    CUDA-core path: both paths stay covered."""
+    _prefill_chunk_case(128, vb, 3, chunk, 4, [300, 129])
+
+
+@pytest.mark.parametrize("vb,paged", [(2, False), (4, False), (2, True)])
+def test_prefill_tcgen05_long_history(vb, paged):
+    """The tcgen05 prefill over several pages per split and several tiles per row: histories of 1500 and
+    700 tokens, chunks of 256 and 64 queries (8 tiles of 32 queries per row, the second row mostly
+    padding), x10 key outliers; contiguous and paged caches. Checked against the oracle, and against
+    the CUDA-core path on the same cache."""
+    out_tc = _prefill_chunk_case(128, vb, 3, (256, 64), 4, [1500, 700], paged=paged, max_ctx=1792)
+    from kv_cache_quantization_quantize_gb300 import _abi
+    lib = _abi.load()
+    assert lib.tq_debug_prefill_path(1) == _abi.TQ_OK
+    try:
+        out_cc = _prefill_chunk_case(128, vb, 3, (256, 64), 4, [1500, 700], paged=paged, max_ctx=1792)
+    finally:
+        assert lib.tq_debug_prefill_path(0) == _abi.TQ_OK
+    diff = max(rel_l2(out_tc[i, j, hq], out_cc[i, j, hq]) for i in range(2) for j in range(64) for hq in range(8))
+    assert diff <= 2e-3, diff
+    print(f"tcgen05 against CUDA-core prefill: worst rel-L2 {diff:.2e}")
+
+
+def _prefill_chunk_case(d, vb, kbits, chunk, G, hist, paged=False, max_ctx=640):
     Hkv = 2
-    hist, chunk, slots = [300, 129], list(chunk), [1, 0]
+    hist, chunk, slots = list(hist), list(chunk), [1, 0]
     B, Tq = len(hist), max(chunk)
-    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2, max_ctx=640,
-                 seed=13, key_bits=kbits)
+    max_pages = (max_ctx + 127) // 128
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
+                 max_ctx=max_ctx, seed=13, key_bits=kbits, n_blocks=2 * max_pages if paged else 0)
     cache = TurboQuantCache(cfg)
+    if paged:
+        perm = torch.randperm(2 * max_pages, generator=torch.Generator().manual_seed(3)).to(torch.int32)
+        cache.block_table.copy_(perm.view(2, max_pages).to(DEV))
     tables = _oracle_tables(cache)
     seqs = [synth.kv_tokens(h_ + c_, Hkv, d, seed=700 + i, outliers=("random", 4, 10.0))
             for i, (h_, c_) in enumerate(zip(hist, chunk))]
@@ -432,7 +476,8 @@ def test_prefill_chunk_attention(d, vb, kbits, chunk, G):
                     err = rel_l2(out[i, j, h * G + g], ref[j, g])
                     worst = max(worst, err)
                     assert err <= 2e-3, (i, j, h, g, err)
-    print(f"prefill d={d} V{vb} K{kbits} q_per_row {Tq} G{G}: worst rel-L2 {worst:.2e}")
+    print(f"prefill d={d} V{vb} K{kbits} q_per_row {Tq} G{G} paged={paged}: worst rel-L2 {worst:.2e}")
+    return out
 
 
 def test_decode_wait_timeout_is_reported_and_the_workspace_stays_usable():
