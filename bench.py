@@ -663,7 +663,7 @@ def bench_prefill(args):
     _build.build()
     force_cc = getattr(args, "prefill_path", "auto") == "cuda-core"
     _abi.load().tq_debug_prefill_path(1 if force_cc else 0)
-    tc = not force_cc and d == 128 and WL["kb"] == 3 and Hq == 4 * Hkv
+    tc = not force_cc and d == 128 and WL["kb"] == 3 and Hq == 4 * Hkv and Tq >= 32
     cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
                      max_seqs=1,
                      max_ctx=ctx, seed=1)

@@ -225,7 +225,7 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *   - d_workspace: at least tq_prefill_workspace_bytes(ctx, batch, q_per_row, max_ctx_hint) bytes,
  *     256-byte aligned; its arrival counters are zeroed by every call (one memset).
  *   - batch * q_per_row <= 65535.
- *   - Launches, head_dim 128 with key_bits 3 and 4 query heads per KV head: a tcgen05 kernel over
+ *   - Launches, head_dim 128 with key_bits 3, 4 query heads per KV head and q_per_row >= 32: a tcgen05 kernel over
  *     tiles of 128 query rows (32 queries x the 4 query heads of one KV head) that expands each page's
  *     key bits and values once per tile and computes scores and P.V on the tensor cores into TMEM,
  *     writing one partial per (query, KV head, history split); then a decode launch that runs only

@@ -577,7 +577,11 @@ static int prefill_qp(const tq_ctx* ctx, int q_per_row) {
 
 static std::atomic<int> g_prefill_path{0};  // tq_debug_prefill_path: 1 forces the CUDA-core path
 
-static bool prefill_tc(const tq_ctx* ctx) { return g_prefill_path.load() == 0 && tq::prefill_tc_eligible(ctx); }
+// The tcgen05 path fills 128-row tiles with 32 queries; chunks of fewer queries per row take the decode
+// kernel, whose CTAs hold one or two query rows.
+static bool prefill_tc(const tq_ctx* ctx, int q_per_row) {
+  return g_prefill_path.load() == 0 && q_per_row >= 32 && tq::prefill_tc_eligible(ctx);
+}
 
 // Workspace plan of the tcgen05 prefill: one query per row (4 columns), n_splits history partials from the
 // tensor-core kernel and the ring partial.
@@ -591,7 +595,7 @@ static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_ro
 
 size_t tq_prefill_workspace_bytes(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
   if (!ctx || batch < 1 || q_per_row < 1 || (long long)batch * q_per_row > 65535) return 0;
-  if (prefill_tc(ctx)) return prefill_tc_plan(ctx, batch, q_per_row, max_ctx_hint).bytes;
+  if (prefill_tc(ctx, q_per_row)) return prefill_tc_plan(ctx, batch, q_per_row, max_ctx_hint).bytes;
   const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;
   return tq::decode_plan(ctx, cta_rows, max_ctx_hint, cta_rows, tq::kMaxG * qp).bytes;
 }
@@ -618,7 +622,7 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
     return fail(TQ_ERR_INVALID_ARG, "q/out must be 16-byte aligned");
   if (reinterpret_cast<uintptr_t>(d_workspace) % 256) return fail(TQ_ERR_INVALID_ARG, "workspace not 256-byte aligned");
   if (!(softmax_scale == softmax_scale)) return fail(TQ_ERR_INVALID_ARG, "softmax_scale is NaN");
-  if (prefill_tc(ctx)) {
+  if (prefill_tc(ctx, q_per_row)) {
     const tq::DecodePlan plan = prefill_tc_plan(ctx, batch, q_per_row, max_ctx_hint);
     if (workspace_bytes < plan.bytes)
       return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);

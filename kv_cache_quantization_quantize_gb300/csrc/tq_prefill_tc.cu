@@ -10,11 +10,13 @@
 //
 // Scores, with the odd-symmetric 2-bit codebook c[idx] = a_h (2 h - 1) + a_l (2 l - 1) and the QJL
 // sign s = 2 sigma - 1, are one fp32 accumulator in TMEM:
-//   S[r][t] = A_hi . B_h + A_lo . B_h + A_hi . B_l + A_qp . B_s
-//     A_hi + A_lo = lambda a_h q_rot (f16 hi + remainder), A_qp = lambda kappa (S q_rot) (f16),
-//     B_h = +-1, B_l = +-rho (rho = a_l / a_h in f16), B_s = +-gamma_t (gamma_t is stored as f16),
+//   S[r][t] = A_hi . B_h + A_lo . B_h + A_l . B_l + A_qp . B_s
+//     A_hi + A_lo = lambda a_h q_rot (f16 hi + remainder), A_l = lambda a_l q_rot, A_qp = lambda kappa
+//     (S q_rot) (f16), B_h = B_l = +-1, B_s = +-gamma_t (gamma_t is stored as f16, so exactly),
 // so S = lambda (<q_rot, c[idx_t]> + kappa gamma_t <S q_rot, s_t>) up to the f16 rounding of the l and
-// QJL operands (as in the decode kernel), and the logit is S n_t scale / lambda. lambda, a power of two
+// QJL operands (as in the decode kernel), and the logit is S n_t scale / lambda. The MMAs run in three
+// groups (h, l, QJL) with a commit each, so the QJL plane and the values are expanded while the
+// remaining groups run. lambda, a power of two
 // per tile, keeps the operands inside the f16 range. P (f16) and the dequantised values V^T =
 // s_g (code - offset) (f16) feed the P.V MMA into a second TMEM accumulator; the softmax rescales it
 // lazily (only when a row maximum grows by more than 2^8).
@@ -27,13 +29,15 @@
 namespace tq {
 namespace {
 
-constexpr int kPtThreads = 256;  // 8 warps: warp w covers TMEM lanes 32 (w % 4).. and column half w / 4
-constexpr float kPtLog2e = 1.4426950408889634f;
-// shared memory (offsets from a 1024-byte aligned base): three A tiles, three B tiles, two page stages
-constexpr uint32_t kPtAhi = 0, kPtAlo = 32768, kPtAqp = 65536;
-constexpr uint32_t kPtB0 = 98304, kPtB1 = 131072, kPtB2 = 163840, kPtStg = 196608;
-// after the stages: per-token logit factors [128], row exchange [2][128], block maximum [8], barriers [8]
-constexpr uint32_t kPtTail = 128 * 4 + 256 * 4 + 8 * 4 + 8 * 8;
+constexpr int kPtThreads = 512;  // 16 warps: warp w covers TMEM lanes 32 (w % 4).. and column quarter w / 4
+constexpr int kPtQ = kPtThreads / 128;  // column quarters: 32 columns (and 32 coordinates of a row) per thread
+// shared memory (offsets from a 1024-byte aligned base): four A tiles, two B tiles, two page stages
+constexpr uint32_t kPtAhi = 0, kPtAlo = 32768, kPtAl = 65536, kPtAqp = 98304;
+constexpr uint32_t kPtBX = 131072, kPtBY = 163840, kPtStg = 196608;
+// after the stages: per-token logit factors [128], row exchange [4][128], block maximum [16], barriers [10]
+constexpr uint32_t kPtTail = 128 * 4 + 512 * 4 + 16 * 4 + 10 * 8;
+// barriers: S table, projection, page stages 0 / 1, MMA groups h, l, sigma, P.V
+enum { kBarTab = 0, kBarProj = 1, kBarPg = 2, kBarH = 4, kBarL = 5, kBarSg = 6, kBarO = 7, kNumBars = 8 };
 
 struct PrefillTcArgs {
   LayerView lv;
@@ -61,9 +65,19 @@ __device__ __forceinline__ const uint8_t* pt_page(const LayerView& lv, int slot,
   return p;
 }
 
-// One bounded mbarrier wait that every thread of the CTA agrees on.
+// One bounded mbarrier wait that every thread of the CTA agrees on. Thread 0 alone polls; the others
+// wait at the block barrier, which keeps 500 pollers off the shared-memory pipe that the tensor cores
+// read their operands through (the try_wait acquire of thread 0 and the barrier make the completed
+// copy or MMA results visible to every thread).
 __device__ __forceinline__ bool pt_wait_all(uint64_t* bar, uint32_t parity) {
-  return __syncthreads_and(mbar_wait(bar, parity)) != 0;
+  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity) : true) != 0;
+}
+
+// 2^x (the PTX approximate base-2 exponential; 2^-inf = 0).
+__device__ __forceinline__ float pt_ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // Pairs of f16 (512 + code) from a value word: the code field at bit `pos` (and pos + 16) moved to
@@ -72,6 +86,34 @@ template <int VB>
 __device__ __forceinline__ uint32_t code_pair_512(uint32_t w, int pos) {
   constexpr uint32_t mask = VB == 2 ? 0x00030003u : 0x000F000Fu;
   return (((w >> pos) & mask) << 1) | 0x60006000u;
+}
+
+// One +-c plane of a page into a B tile: token tk's 32 coordinates of quarter hv (4 chunks of 8), from its
+// four KBITS words of plane p; a set bit gives +c, a clear one -c (c in both f16 halves of `cst`).
+__device__ __forceinline__ void pt_expand_plane(const uint32_t* kw, int p, int tk, int hv, uint32_t cst, uint8_t* tile) {
+  constexpr int KB = 3;
+  const int tl = tk >> 4, g8 = tk & 7, rr = (tk >> 3) & 1;
+  uint32_t w[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) w[c] = kw[((tl * KB + p) * 32 + 4 * g8 + c) * 2 + rr];
+#pragma unroll
+  for (int mm = 0; mm < 4; ++mm) {
+    const int m = 4 * hv + mm;  // page bit m (and m + 16) holds coordinates 8 m + 2 c (+ 1)
+    uint32_t u4[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) u4[c] = (~(w[c] << (15 - m)) & 0x80008000u) | cst;
+    *reinterpret_cast<uint4*>(tile + sw128_offset(tk, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+  }
+}
+
+// Issues 8 MMAs (K = 128) of an f16 A tile against an f16 B tile into TMEM column t_d.
+__device__ __forceinline__ void pt_mma_k128(uint32_t t_d, uint32_t a_addr, uint32_t b_addr, bool accumulate_first) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
+    umma_bf16(t_d, umma_desc_sw128(a_addr + koff), umma_desc_sw128(b_addr + koff), kIdescF16M128N128,
+              (accumulate_first || ks > 0) ? 1u : 0u);
+  }
 }
 
 template <int VB>
@@ -88,13 +130,16 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const uint32_t PB = pl.bytes, PBS = (pl.bytes + 127) / 128 * 128;
   uint8_t* stg = sm + kPtStg;
   float* ns = reinterpret_cast<float*>(stg + 2 * PBS);  // [128] logit factor n_t scale log2e / lambda
-  float* xrow = ns + 128;                                 // [2][128] row maxima / sums of the two halves
-  float* bmax = xrow + 256;                               // [8] per-warp operand maxima
-  uint64_t* bars = reinterpret_cast<uint64_t*>(bmax + 8);  // 0 S table, 1 projection, 2-3 pages, 4 S, 5 O
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 6);
-  // this thread's query row (TMEM lane) and column half
+  float* xrow = ns + 128;                                 // [4][128] row maxima / sums of the four quarters
+  float* bmax = xrow + 512;                               // [16] per-warp operand maxima
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bmax + 16);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  // this thread's query row (TMEM lane) and column quarter: columns 32 ch .. 32 ch + 31
   const int r = 32 * (warp & 3) + lane, ch = warp >> 2;
   const int qi = r >> 2, g = r & 3, qidx = 32 * tile + qi;
+  // expansion roles: token / coordinate tk = tid % 128 and quarter hv = tid / 128 (a warp's 32 threads write
+  // 32 consecutive rows of a tile at the same chunk: conflict-free under the 128-byte swizzle)
+  const int tk = tid & 127, hv = tid >> 7;
   pdl_wait();  // sequence state, pages and queries come from earlier work on the stream
   pdl_launch();
   const int slot = a.seq_ids[b], nq = a.n_q[b];
@@ -112,6 +157,8 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const int pps = (npg_tile + S - 1) / S;
   const int pg0 = min(npg_tile, split * pps), pg1 = min(npg_tile, pg0 + pps), n = pg1 - pg0;
   const int vis_r = vis(qidx);
+  // pages below this warp's smallest causal extent need no mask
+  const int vis_w = __reduce_min_sync(0xffffffffu, (unsigned)vis_r);
   const bool row_out = qidx < a.qpr;  // a virtual row of the launch (padding rows get an empty partial)
   float* part = row_out ? reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                                    ((((size_t)b * a.qpr + qidx) * lv.Hkv + h) * (S + 1) + split) *
@@ -119,7 +166,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
                         : nullptr;
   if (n == 0) {  // nothing visible in this split: empty partials (m = -inf, l = 0, o = 0)
     if (row_out) {
-      for (int j = 64 * ch; j < 64 * ch + 64; ++j) part[2 * kMaxG + g * D + j] = 0.f;
+      for (int j = 32 * ch; j < 32 * ch + 32; ++j) part[2 * kMaxG + g * D + j] = 0.f;
       if (ch == 0) {
         part[g] = -INFINITY;
         part[kMaxG + g] = 0.f;
@@ -130,12 +177,12 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 
   // ---- setup: barriers, TMEM (256 columns: S at 0, O at 128), the S table for the projection ----
   if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    mbar_expect_tx(&bars[0], 2u * D * D);
-    bulk_g2s(sm + kPtB2, lv.S_sw, 2u * D * D, &bars[0]);
-    mbar_expect_tx(&bars[2], PB);  // the first page
-    bulk_g2s(stg, pt_page(lv, slot, h, pg0), PB, &bars[2]);
+    mbar_expect_tx(&bars[kBarTab], 2u * D * D);
+    bulk_g2s(sm + kPtAl, lv.S_sw, 2u * D * D, &bars[kBarTab]);  // A_l's place until the projection is done
+    mbar_expect_tx(&bars[kBarPg], PB);                         // the first page
+    bulk_g2s(stg, pt_page(lv, slot, h, pg0), PB, &bars[kBarPg]);
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(smem_u32(tslot))
@@ -143,10 +190,10 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
   // ---- query rows: q_rot = Pi q (warp-per-row FWHT), bf16 hi / lo for the projection, fp32 copy ----
-  float* qr = reinterpret_cast<float*>(sm + kPtB0);  // [128][128] fp32 q_rot (B0 and B1 until the pages)
+  float* qr = reinterpret_cast<float*>(sm + kPtBX);  // [128][128] fp32 q_rot (the B tiles until the pages)
   const float rs = rsqrtf((float)D);
   float amax = 0.f;
-  for (int rr = warp; rr < 128; rr += 8) {
+  for (int rr = warp; rr < 128; rr += kPtThreads / 32) {
     const int i = 32 * tile + (rr >> 2), gg = rr & 3;
     float x[4];
 #pragma unroll
@@ -181,207 +228,154 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tslot, t_s = tmem, t_o = tmem + 128;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  // phases armed on each barrier (a copy or an MMA batch that completes it) and seen complete, kept
-  // alike by every thread, for the drain after a wait that gave up
-  uint32_t armed[6] = {1, 0, 1, 0, 0, 0}, seen[6] = {0, 0, 0, 0, 0, 0};
-  bool ok = pt_wait_all(&bars[0], 0);  // S table landed
-  if (ok) ++seen[0];
-  if (ok) ++armed[1];
-  if (ok && tid == 0) {  // projection q_proj = S q_rot into TMEM columns [0, 128): A = q_rot hi, lo (bf16)
-    tc_fence_after();
-#pragma unroll
-    for (int ks = 0; ks < 16; ++ks) {
-      const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32;
-      umma_bf16(t_s, umma_desc_sw128(smem_u32(sm + (ks < 8 ? kPtAhi : kPtAlo)) + koff),
-                umma_desc_sw128(smem_u32(sm + kPtB2) + koff), kIdescBf16M128N128, ks > 0);
+  const uint32_t a_hi = smem_u32(sm + kPtAhi), a_lo = smem_u32(sm + kPtAlo), a_l = smem_u32(sm + kPtAl),
+                 a_qp = smem_u32(sm + kPtAqp), b_x = smem_u32(sm + kPtBX), b_y = smem_u32(sm + kPtBY);
+  // per barrier, kept alike by every thread: the parity of the next phase to wait for (bit i of par) and
+  // the phases armed (a copy or an MMA batch that completes it) but not seen complete (2 bits i of pend),
+  // for the drain after a wait that gave up. Armed now: the S table and the first page.
+  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (1u << (2 * kBarPg));
+  auto arm = [&](int i) { pend += 1u << (2 * i); };
+  auto wait_bar = [&](int i) {  // waits for the oldest armed phase of barrier i not seen yet
+    const bool w = pt_wait_all(&bars[i], (par >> i) & 1u);
+    if (w) {
+      par ^= 1u << i;
+      pend -= 1u << (2 * i);
     }
-    umma_commit(&bars[1]);
-  }
-  ok = ok && pt_wait_all(&bars[1], 0);
-  if (ok) ++seen[1];
-  tc_fence_after();
-  // operand scale lambda: the largest of |a_h q_rot| and |kappa q_proj| maps to [2^12, 2^13)
-  const float a_h = lv.cb[kCbW + 0], a_l = lv.cb[kCbW + 1];
-  const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
-  uint32_t qpv[2][32];
+    return w;
+  };
+  bool ok = wait_bar(kBarTab);  // S table landed
+  if (ok) {  // projection q_proj = S q_rot into TMEM columns [0, 128): A = q_rot hi, lo (bf16)
+    if (tid == 0) {
+      tc_fence_after();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) qpv[0][i] = qpv[1][i] = 0u;
-  if (ok) {
-    tmem_ld32(t_s + lane_base + 64 * ch, qpv[0]);
-    tmem_ld32(t_s + lane_base + 64 * ch + 32, qpv[1]);
+      for (int ks = 0; ks < 16; ++ks) {
+        const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32;
+        umma_bf16(t_s, umma_desc_sw128((ks < 8 ? a_hi : a_lo) + koff), umma_desc_sw128(a_l + koff),
+                  kIdescBf16M128N128, ks > 0);
+      }
+      umma_commit(&bars[kBarProj]);
+    }
+    arm(kBarProj);
+    ok = wait_bar(kBarProj);
   }
+  tc_fence_after();
+  // operand scale lambda: the largest of |a_h q_rot|, |a_l q_rot| and |kappa q_proj| maps to [2^12, 2^13)
+  const float w_h = lv.cb[kCbW + 0], w_l = lv.cb[kCbW + 1];
+  const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
+  uint32_t qpv[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) qpv[i] = 0u;
+  if (ok) tmem_ld32(t_s + lane_base + 32 * ch, qpv);
   float pmax = 0.f;
 #pragma unroll
-  for (int u = 0; u < 2; ++u)
-#pragma unroll
-    for (int i = 0; i < 32; ++i) pmax = fmaxf(pmax, fabsf(__uint_as_float(qpv[u][i])));
-  const float wmax = warp_max(fmaxf(fabsf(a_h) * amax, kappa * pmax));
+  for (int i = 0; i < 32; ++i) pmax = fmaxf(pmax, fabsf(__uint_as_float(qpv[i])));
+  const float wmax = warp_max(fmaxf(fmaxf(fabsf(w_h), fabsf(w_l)) * amax, kappa * pmax));
   if (lane == 0) bmax[warp] = wmax;
-  __syncthreads();
+  __syncthreads();  // also: every projection MMA has read A_hi, A_lo and the S table (waited above)
   float tmax = 0.f;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) tmax = fmaxf(tmax, bmax[w]);
+  for (int w = 0; w < kPtThreads / 32; ++w) tmax = fmaxf(tmax, bmax[w]);
   const float lam = tmax > 0.f ? exp2f(floorf(log2f(4096.f / tmax))) : 1.f;
-  // A_qp = lambda kappa q_proj (f16); A_hi / A_lo = f16 hi / remainder of lambda a_h q_rot
+  // A_qp = lambda kappa q_proj; A_hi / A_lo = f16 hi / remainder of lambda a_h q_rot; A_l = lambda a_l q_rot
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
+  for (int m = 0; m < 4; ++m) {
     uint32_t u4[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const int j = 8 * m + 2 * c;
-      const __half2 hv = __floats2half2_rn(lam * kappa * __uint_as_float(qpv[j >> 5][j & 31]),
-                                           lam * kappa * __uint_as_float(qpv[(j + 1) >> 5][(j + 1) & 31]));
-      u4[c] = *reinterpret_cast<const uint32_t*>(&hv);
+      const __half2 hv2 = __floats2half2_rn(lam * kappa * __uint_as_float(qpv[j]), lam * kappa * __uint_as_float(qpv[j + 1]));
+      u4[c] = *reinterpret_cast<const uint32_t*>(&hv2);
     }
-    *reinterpret_cast<uint4*>(sm + kPtAqp + sw128_offset(r, 64 * ch + 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+    *reinterpret_cast<uint4*>(sm + kPtAqp + sw128_offset(r, 32 * ch + 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
   }
 #pragma unroll
-  for (int m = 0; m < 8; ++m) {
-    uint32_t hi4[4], lo4[4];
+  for (int m = 0; m < 4; ++m) {
+    uint32_t hi4[4], lo4[4], l4[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      const int j = 64 * ch + 8 * m + 2 * c;
-      const float x0 = lam * a_h * qr[r * D + j], x1 = lam * a_h * qr[r * D + j + 1];
+      const int j = 32 * ch + 8 * m + 2 * c;
+      const float q0 = qr[r * D + j], q1 = qr[r * D + j + 1];
+      const float x0 = lam * w_h * q0, x1 = lam * w_h * q1;
       const __half2 hi = __floats2half2_rn(x0, x1);
       const float2 hf = __half22float2(hi);
       const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+      const __half2 lp = __floats2half2_rn(lam * w_l * q0, lam * w_l * q1);
       hi4[c] = *reinterpret_cast<const uint32_t*>(&hi);
       lo4[c] = *reinterpret_cast<const uint32_t*>(&lo);
+      l4[c] = *reinterpret_cast<const uint32_t*>(&lp);
     }
-    *reinterpret_cast<uint4*>(sm + kPtAhi + sw128_offset(r, 64 * ch + 8 * m)) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
-    *reinterpret_cast<uint4*>(sm + kPtAlo + sw128_offset(r, 64 * ch + 8 * m)) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+    const uint32_t off = sw128_offset(r, 32 * ch + 8 * m);
+    *reinterpret_cast<uint4*>(sm + kPtAhi + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
+    *reinterpret_cast<uint4*>(sm + kPtAlo + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+    *reinterpret_cast<uint4*>(sm + kPtAl + off) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
   }
-  // constants of the B planes: +-1, +-rho (f16), and the per-token +-gamma (below)
-  const __half rho_h = __float2half_rn(a_l / a_h);
-  const uint32_t c_h = 0x3C003C00u, c_l = (uint32_t)__half_as_ushort(rho_h) * 0x00010001u;
-  const float logit = a.scale * kPtLog2e / lam;
+  const float logit = a.scale * 1.4426950408889634f / lam;  // S n_t logit = score in log2 units
   constexpr float kVoff = VB == 2 ? 513.5f : 519.5f;  // 512 + the mid-rise offset 2^(VB-1) - 1/2
   const __half2 voff2 = __floats2half2_rn(kVoff, kVoff);
   float m_used = -INFINITY, l_loc = 0.f;
   for (int k = 0; k < n && ok; ++k) {
     const int pg = pg0 + k, buf = k & 1;
-    uint8_t* page = stg + buf * PBS;
-    if (k + 1 < n) {  // next page into the other stage (its last reader finished at the barrier below)
+    const uint8_t* page = stg + buf * PBS;
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
+    if (k + 1 < n) {  // next page into the other stage (its last reader finished before the barriers below)
       if (tid == 0) {
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        mbar_expect_tx(&bars[2 + (buf ^ 1)], PB);
-        bulk_g2s(stg + (buf ^ 1) * PBS, pt_page(lv, slot, h, pg + 1), PB, &bars[2 + (buf ^ 1)]);
+        mbar_expect_tx(&bars[kBarPg + (buf ^ 1)], PB);
+        bulk_g2s(stg + (buf ^ 1) * PBS, pt_page(lv, slot, h, pg + 1), PB, &bars[kBarPg + (buf ^ 1)]);
       }
-      ++armed[2 + (buf ^ 1)];
+      arm(kBarPg + (buf ^ 1));
     }
-    ok = pt_wait_all(&bars[2 + buf], (k >> 1) & 1);
-    if (ok) ++seen[2 + buf];
-    if (ok && k > 0) {  // the previous P.V MMAs have read B0 and B1
-      ok = pt_wait_all(&bars[5], (k - 1) & 1);
-      if (ok) ++seen[5];
-    }
+    ok = wait_bar(kBarPg + buf);
+    if (ok && k > 0) ok = wait_bar(kBarO);  // the previous P.V MMAs have read BX and BY
     if (!ok) break;
     tc_fence_after();
-    // ---- key planes: token tk, coordinate chunks 8 hv .. 8 hv + 7 ----
+    // ---- h and l planes (+-1, +-1 with the weights in A), per-token logit factors ----
     {
-      const int tk = tid >> 1, hv = tid & 1;
-      const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
       const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
-      const uint32_t c_s = (nw >> 16) * 0x00010001u;  // gamma_t in both halves
       if (hv == 0) ns[tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu))) * logit;
-      const int tl = tk >> 4, g8 = tk & 7, rr = (tk >> 3) & 1;
-#pragma unroll
-      for (int p = 0; p < KB; ++p) {
-        uint32_t w[4];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) w[c] = kw[((tl * KB + p) * 32 + 4 * g8 + c) * 2 + rr];
-        const uint32_t cst = p == 0 ? c_h : p == 1 ? c_l : c_s;
-        uint8_t* base = sm + (p == 0 ? kPtB0 : p == 1 ? kPtB1 : kPtB2);
-#pragma unroll
-        for (int mm = 0; mm < 8; ++mm) {
-          const int m = 8 * hv + mm;
-          uint32_t u4[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) u4[c] = (~(w[c] << (15 - m)) & 0x80008000u) | cst;  // bit 1 -> +, 0 -> -
-          *reinterpret_cast<uint4*>(base + sw128_offset(tk, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
-        }
-      }
+      pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, sm + kPtBX);
+      pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, sm + kPtBY);
     }
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // S = A_hi B_h + A_lo B_h + A_hi B_l + A_qp B_s
+    if (tid == 0) {  // S = A_hi B_h + A_lo B_h (commit h), + A_l B_l (commit l)
       tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 32; ++ks) {
-        const int blkk = ks >> 3, kk = ks & 7;
-        const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-        const uint32_t aoff = blkk == 0 || blkk == 2 ? kPtAhi : blkk == 1 ? kPtAlo : kPtAqp;
-        const uint32_t boff = blkk <= 1 ? kPtB0 : blkk == 2 ? kPtB1 : kPtB2;
-        umma_bf16(t_s, umma_desc_sw128(smem_u32(sm + aoff) + koff), umma_desc_sw128(smem_u32(sm + boff) + koff),
-                  kIdescF16M128N128, ks > 0);
-      }
-      umma_commit(&bars[4]);
+      pt_mma_k128(t_s, a_hi, b_x, false);
+      pt_mma_k128(t_s, a_lo, b_x, true);
+      umma_commit(&bars[kBarH]);
+      pt_mma_k128(t_s, a_l, b_y, true);
+      umma_commit(&bars[kBarL]);
     }
-    ++armed[4];
-    ok = pt_wait_all(&bars[4], k & 1);
+    arm(kBarH);
+    arm(kBarL);
+    // ---- the QJL plane (+-gamma_t) into BX once the h MMAs have read it ----
+    ok = wait_bar(kBarH);
     if (!ok) break;
-    ++seen[4];
-    tc_fence_after();
-    // ---- softmax of row r over tokens 64 ch .. 64 ch + 63 ----
-    uint32_t sv[2][32];
-    tmem_ld32(t_s + lane_base + 64 * ch, sv[0]);
-    tmem_ld32(t_s + lane_base + 64 * ch + 32, sv[1]);
-    float mx = -INFINITY;
-#pragma unroll
-    for (int u = 0; u < 2; ++u)
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int t = 64 * ch + 32 * u + i;
-        const float s = pg * kPage + t < vis_r ? __uint_as_float(sv[u][i]) * ns[t] : -INFINITY;
-        sv[u][i] = __float_as_uint(s);
-        mx = fmaxf(mx, s);
-      }
-    xrow[128 * ch + r] = mx;
-    __syncthreads();
-    mx = fmaxf(mx, xrow[128 * (ch ^ 1) + r]);
-    // the row maximum grew by more than 2^8: move to the new maximum (O and l scaled by alpha). The TMEM
-    // loads and stores are warp-wide, so a warp rescales when any of its rows needs it (alpha = 1 for the rest)
-    const bool grow = mx > m_used + 8.f;
-    const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : exp2f(m_used - mx));
-    if (__any_sync(0xffffffffu, grow && k > 0)) {
-      uint32_t ov[32];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        tmem_ld32(t_o + lane_base + 64 * ch + 32 * u, ov);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-        tmem_st32(t_o + lane_base + 64 * ch + 32 * u, ov);
-      }
-    }
-    if (grow) {
-      l_loc *= alpha;
-      m_used = mx;
-    }
-#pragma unroll
-    for (int mm = 0; mm < 8; ++mm) {
-      uint32_t u4[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = 8 * mm + 2 * c;
-        const float s0 = __uint_as_float(sv[i >> 5][i & 31]), s1 = __uint_as_float(sv[(i + 1) >> 5][(i + 1) & 31]);
-        const float p0 = m_used == -INFINITY ? 0.f : exp2f(s0 - m_used);
-        const float p1 = m_used == -INFINITY ? 0.f : exp2f(s1 - m_used);
-        l_loc += p0 + p1;
-        const __half2 ph = __floats2half2_rn(p0, p1);
-        u4[c] = *reinterpret_cast<const uint32_t*>(&ph);
-      }
-      *reinterpret_cast<uint4*>(sm + kPtB0 + sw128_offset(r, 64 * ch + 8 * mm)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
-    }
-    // ---- values: V^T[coordinate j][token] = s_g (code - offset), tokens 64 th .. 64 th + 63 ----
     {
-      const int j = tid >> 1, th = tid & 1;
+      const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
+      pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, sm + kPtBX);
+    }
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // S += A_qp B_s
+      tc_fence_after();
+      pt_mma_k128(t_s, a_qp, b_x, true);
+      umma_commit(&bars[kBarSg]);
+    }
+    arm(kBarSg);
+    // ---- values into BY once the l MMAs have read it: V^T[j][token] = s_g (code - offset) ----
+    ok = wait_bar(kBarL);
+    if (!ok) break;
+    {
+      const int j = tk, th = hv;
       const int mt = j >> 4, g8 = j & 7, rowhi = (j >> 3) & 1, grp = j >> 5;
       const uint32_t* vw = reinterpret_cast<const uint32_t*>(page + pl.vbits_off);
       const uint32_t* vsc = reinterpret_cast<const uint32_t*>(page + pl.vscale_off);  // [token pair][group] f16x2
 #pragma unroll
-      for (int mm = 0; mm < 8; ++mm) {
-        const int m = 8 * th + mm, blk = m >> 2, kap = (m >> 1) & 1, hiT = m & 1, rr = rowhi + 2 * hiT;
+      for (int mm = 0; mm < 4; ++mm) {
+        const int m = 4 * th + mm, blk = m >> 2, kap = (m >> 1) & 1, hiT = m & 1, rr = rowhi + 2 * hiT;
         uint32_t u4[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -397,57 +391,103 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
                                     *reinterpret_cast<const __half2*>(&s2));
           u4[c] = *reinterpret_cast<const uint32_t*>(&v);
         }
-        *reinterpret_cast<uint4*>(sm + kPtB1 + sw128_offset(j, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+        *reinterpret_cast<uint4*>(sm + kPtBY + sw128_offset(j, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
       }
+    }
+    // ---- softmax of row r over tokens 32 ch .. 32 ch + 31 ----
+    ok = wait_bar(kBarSg);
+    if (!ok) break;
+    tc_fence_after();
+    uint32_t sv[32];
+    tmem_ld32(t_s + lane_base + 32 * ch, sv);
+    const bool full = pg * kPage + kPage <= vis_w;  // every token of the page is visible to the whole warp
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4) {
+      const float4 f = *reinterpret_cast<const float4*>(ns + 32 * ch + 4 * i4);
+      const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * i4 + e, t = 32 * ch + i;
+        float s = __uint_as_float(sv[i]) * fv[e];
+        if (!full && pg * kPage + t >= vis_r) s = -INFINITY;
+        sv[i] = __float_as_uint(s);
+        mx = fmaxf(mx, s);
+      }
+    }
+    xrow[128 * ch + r] = mx;
+    __syncthreads();
+#pragma unroll
+    for (int q = 1; q < kPtQ; ++q) mx = fmaxf(mx, xrow[128 * ((ch + q) % kPtQ) + r]);
+    // the row maximum grew by more than 2^8: move to the new maximum (O and l scaled by alpha). The TMEM
+    // loads and stores are warp-wide, so a warp rescales when any of its rows needs it (alpha = 1 for the rest)
+    const bool grow = mx > m_used + 8.f;
+    const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : pt_ex2(m_used - mx));
+    if (__any_sync(0xffffffffu, grow && k > 0)) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + lane_base + 32 * ch, ov);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+      tmem_st32(t_o + lane_base + 32 * ch, ov);
+    }
+    if (grow) {
+      l_loc *= alpha;
+      m_used = mx;
+    }
+    const float mref = m_used == -INFINITY ? 0.f : m_used;  // every s is -inf while nothing is visible
+#pragma unroll
+    for (int mm = 0; mm < 4; ++mm) {
+      uint32_t u4[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = 8 * mm + 2 * c;
+        const float p0 = pt_ex2(__uint_as_float(sv[i]) - mref), p1 = pt_ex2(__uint_as_float(sv[i + 1]) - mref);
+        l_loc += p0 + p1;
+        const __half2 ph = __floats2half2_rn(p0, p1);
+        u4[c] = *reinterpret_cast<const uint32_t*>(&ph);
+      }
+      *reinterpret_cast<uint4*>(sm + kPtBX + sw128_offset(r, 32 * ch + 8 * mm)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
     }
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // O += P V: A = P [rows x tokens] (B0), B = V^T [coordinates x tokens] (B1)
+    if (tid == 0) {  // O += P V: A = P [rows x tokens] (BX), B = V^T [coordinates x tokens] (BY)
       tc_fence_after();
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(t_o, umma_desc_sw128(smem_u32(sm + kPtB0) + koff), umma_desc_sw128(smem_u32(sm + kPtB1) + koff),
-                  kIdescF16M128N128, (k > 0 || ks > 0) ? 1u : 0u);
-      }
-      umma_commit(&bars[5]);
+      pt_mma_k128(t_o, b_x, b_y, k > 0);
+      umma_commit(&bars[kBarO]);
     }
-    ++armed[5];
+    arm(kBarO);
   }
-  if (ok && armed[5] > seen[5]) {
-    ok = pt_wait_all(&bars[5], (armed[5] - 1) & 1);
-    if (ok) ++seen[5];
-  }
+  if (ok && ((pend >> (2 * kBarO)) & 3u)) ok = wait_bar(kBarO);
   tc_fence_after();
   // ---- the partial of row r: m (log2 units), l, o (rotated basis, relative to m) ----
+  __syncthreads();  // every thread has read the row maxima above
   xrow[128 * ch + r] = l_loc;
   __syncthreads();
-  const float l_row = l_loc + xrow[128 * (ch ^ 1) + r];
-  const bool has = ok && m_used != -INFINITY;  // this row saw a token
+  float l_row = 0.f;
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
+  for (int q = 0; q < kPtQ; ++q) l_row += xrow[128 * q + r];
+  const bool has = ok && m_used != -INFINITY;  // this row saw a token
+  {
     uint32_t ov[32];
-    if (ok) tmem_ld32(t_o + lane_base + 64 * ch + 32 * u, ov);  // warp-wide (ok is the same in every thread)
+    if (ok) tmem_ld32(t_o + lane_base + 32 * ch, ov);  // warp-wide (ok is the same in every thread)
 #pragma unroll
     for (int i4 = 0; i4 < 8 && row_out; ++i4)
-      *reinterpret_cast<float4*>(part + 2 * kMaxG + g * D + 64 * ch + 32 * u + 4 * i4) =
+      *reinterpret_cast<float4*>(part + 2 * kMaxG + g * D + 32 * ch + 4 * i4) =
           has ? make_float4(__uint_as_float(ov[4 * i4]), __uint_as_float(ov[4 * i4 + 1]),
                             __uint_as_float(ov[4 * i4 + 2]), __uint_as_float(ov[4 * i4 + 3]))
               : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  if (row_out) {
-    if (ch == 0) {
-      part[g] = has ? m_used : -INFINITY;
-      part[kMaxG + g] = has ? l_row : 0.f;
-    }
+  if (row_out && ch == 0) {
+    part[g] = has ? m_used : -INFINITY;
+    part[kMaxG + g] = has ? l_row : 0.f;
   }
   if (!ok && tid == 0) {
     // a wait gave up: nothing more is issued; wait (bounded) for every armed phase not seen complete - the
     // MMA batches before TMEM is freed, the copies before the CTA leaves its shared memory
     set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
-    for (int i = 0; i < 6; ++i)
-      for (uint32_t ph = seen[i]; ph < armed[i]; ++ph) mbar_wait(&bars[i], ph & 1);
+    for (int i = 0; i < kNumBars; ++i)
+      for (uint32_t c = 0, ph = (par >> i) & 1u; c < ((pend >> (2 * i)) & 3u); ++c, ph ^= 1u) mbar_wait(&bars[i], ph);
   }
   tc_fence_before();
   __syncthreads();
