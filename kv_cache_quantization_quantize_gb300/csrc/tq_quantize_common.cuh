@@ -142,6 +142,25 @@ constexpr size_t quantize_smem_bytes_d() {
   return 2 * 32 * D + 4 * 32 + 2 * 32 * (D / 32) + 2 * 2 * 32 * kRStride<D>;
 }
 
+// Mid-rise value code clamp(floor(fl(x / s)), -2^(vb-1), 2^(vb-1) - 1) + 2^(vb-1) for a scale s > 0 (the
+// decision of an IEEE division rounded to nearest), without a division on the common path:
+//   2 bits: three comparisons. fl(x / s) >= -1 exactly when x / s >= -(1 + 2^-24) (the midpoint below -1
+//     rounds to the even -1), i.e. x + s >= -s 2^-24; fl(x / s) >= 0 exactly when x >= 0; fl(x / s) >= 1
+//     exactly when x / s >= 1 - 2^-25, i.e. x - s >= -s 2^-25. Near those points x + s and x - s are exact
+//     (Sterbenz), and away from them rounding cannot change the comparison.
+//   4 bits: the floor of x * (1 / s), which lies within a few ulps of the rounded quotient, so it is
+//     exact unless the product is within 4 ulps of an integer; those take the division.
+__device__ __forceinline__ int value_code(float x, float s, float rcp, int vb) {
+  if (vb == 2)
+    return (int)(x + s >= -s * 5.9604644775390625e-8f) + (int)(x >= 0.f) + (int)(x - s >= -s * 2.98023223876953125e-8f);
+  const int vhalf = 1 << (vb - 1);
+  const float qv = x * rcp;
+  float fq = floorf(qv);
+  const float fr = qv - fq, eps = fabsf(qv) * 4.8e-7f + 1e-30f;
+  if (fr < eps || fr > 1.f - eps) fq = floorf(__fdiv_rn(x, s));
+  return (int)fminf(fmaxf(fq, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
+}
+
 // D += A B, m16n8k16, f16 operands, f32 accumulate.
 __device__ __forceinline__ void mma_f16_acc(float (&c)[4], const uint4& a, uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -257,16 +276,10 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
       for (int o = 1; o < 16; o <<= 1) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
       const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
       const __half sh = __float2half_rn(s32);
-      const float s = __half2float(sh);
+      const float s = __half2float(sh), rcp = s > 0.f ? __frcp_rn(s) : 0.f;
 #pragma unroll
-      for (int e = 0; e < NE; ++e) {
-        int code = vhalf;
-        if (s > 0.f) {
-          const float qv = floorf(__fdiv_rn(x[e], s));
-          code = (int)fminf(fmaxf(qv, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
-        }
-        vc[lane_coord<D>(e, lane)] = (uint8_t)code;
-      }
+      for (int e = 0; e < NE; ++e)
+        vc[lane_coord<D>(e, lane)] = (uint8_t)(s > 0.f ? value_code(x[e], s, rcp, vb) : vhalf);
       if ((lane & 15) == 0) scales[(t - tb) * (D / 32) + (lane >> 4)] = __half_as_ushort(sh);
     }
 #pragma unroll
@@ -282,16 +295,10 @@ __device__ __forceinline__ void code_tokens(const AppendArgs& a, int b, int h, i
       am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 4));
       const float s32 = fminf(__fdiv_rn(am, (float)vhalf - 0.5f), 65504.f);
       const __half sh = __float2half_rn(s32);
-      const float s = __half2float(sh);
+      const float s = __half2float(sh), rcp = s > 0.f ? __frcp_rn(s) : 0.f;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int code = vhalf;
-        if (s > 0.f) {
-          const float qv = floorf(__fdiv_rn(x[4 * hh + e], s));
-          code = (int)fminf(fmaxf(qv, (float)-vhalf), (float)(vhalf - 1)) + vhalf;
-        }
-        vc[128 * hh + 4 * lane + e] = (uint8_t)code;
-      }
+      for (int e = 0; e < 4; ++e)
+        vc[128 * hh + 4 * lane + e] = (uint8_t)(s > 0.f ? value_code(x[4 * hh + e], s, rcp, vb) : vhalf);
       if ((lane & 7) == 0) scales[(t - tb) * (D / 32) + 4 * hh + (lane >> 3)] = __half_as_ushort(sh);
     }
   }
