@@ -645,6 +645,9 @@ def bench_quantize(tqm, synth, dev, args, peak):
             "ms_per_pass": ms, "passes": reps, "clocks": sampler.summary(t0, t1), "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K{PREFILL['kb']}/V{vb}",
             "path": ("tcgen05 rotation (H diag(D)) and QJL projection (bf16 hi/lo) into TMEM, thread-per-token "
                      "coding, TMA page loads" if d == 128 else
+                     "tcgen05 rotation (two 128-point H diag(D_i) products, butterfly on CUDA cores) and QJL "
+                     "projection (bf16 hi/lo, S streamed in 32-row chunks) into TMEM, thread-per-token coding, "
+                     "TMA page loads" if d == 256 else
                      "CUDA-core quantise kernel (QJL projection as an f16 mma.sync GEMM per 32-token block)"),
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
 

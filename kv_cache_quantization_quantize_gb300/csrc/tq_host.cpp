@@ -231,8 +231,9 @@ TableOffsets table_offsets(int d) {
   o.St = align_up(o.S + 2ull * d * d, 256);
   o.cb = align_up(o.St + 2ull * d * d, 256);
   o.S_sw = align_up(o.cb + sizeof(float) * kCbFloats, 1024);
-  o.HD_sw = align_up(o.S_sw + (d == 128 ? 2ull * d * d : 0), 1024);
-  o.S_frag = align_up(o.HD_sw + (d == 128 ? 2ull * d * d : 0), 256);
+  o.HD_sw = align_up(o.S_sw + (d >= 128 ? 2ull * d * d : 0), 1024);
+  // head_dim 256: H diag(D) for each 128-coordinate half of D (2 x 128 x 128)
+  o.S_frag = align_up(o.HD_sw + (d == 128 ? 2ull * d * d : d == 256 ? 2ull * 2 * 128 * 128 : 0), 256);
   o.bytes = align_up(o.S_frag + 2ull * d * d, 256);
   return o;
 }
@@ -445,6 +446,23 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
     cb[tq::kCbSmax] = (float)(m * (1.0 + 1e-6));
   }
   std::memcpy(host.data() + ctx->to.cb, cb, sizeof(cb));
+  if (d == 256) {
+    // S (256 rows) K-major in the 128-byte swizzle: four 32 KB atoms, atom c = columns [64c, 64c + 64)
+    uint8_t* sw = host.data() + ctx->to.S_sw;
+    for (int n = 0; n < d; ++n)
+      for (int k = 0; k < d; ++k)
+        std::memcpy(sw + tq::sw128_offset_rows(n, k, 256), &ctx->S[(size_t)n * d + k], 2);
+    // H diag(D1) and H diag(D2) for the halves D1 = D[0, 128), D2 = D[128, 256) of the sign vector, with H
+    // the 128-point Hadamard: H_256 = [[H, H], [H, -H]] makes the 256-point rotation two of them
+    uint8_t* hd = host.data() + ctx->to.HD_sw;
+    for (int half = 0; half < 2; ++half)
+      for (int i = 0; i < 128; ++i)
+        for (int j = 0; j < 128; ++j) {
+          const bool neg = (__builtin_popcount((unsigned)(i & j)) & 1) != (ctx->D[128 * half + j] < 0.f);
+          const uint16_t v = neg ? 0xBF80u : 0x3F80u;
+          std::memcpy(hd + (size_t)half * 32768 + tq::sw128_offset(i, j), &v, 2);
+        }
+  }
   if (d == 128) {
     uint8_t* sw = host.data() + ctx->to.S_sw;
     for (int n = 0; n < d; ++n)

@@ -121,6 +121,11 @@ TQ_HD int vscale_idx(int d, int t, int q) { return ((t >> 1) * (d / 32) + q) * 2
 // Byte offset of element (row n, column k) of a 128 x 128 bf16 matrix stored K-major in the
 // tcgen05 canonical 128-byte-swizzled layout: two 64-column atoms of 128 rows; within an atom,
 // 8-row groups of 1024 B, and the 16-byte chunk c of row r stored at chunk c ^ (r & 7).
+// The same layout for a tile of `rows` rows (a multiple of 8): 64-column atoms of rows x 128 B.
+TQ_HD uint32_t sw128_offset_rows(int n, int k, int rows) {
+  return (uint32_t)((k >> 6) * rows * 128 + (n >> 3) * 1024 + (n & 7) * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) +
+                    (k & 7) * 2);
+}
 TQ_HD uint32_t sw128_offset(int n, int k) {
   return (uint32_t)((k >> 6) * 16384 + (n >> 3) * 1024 + (n & 7) * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) +
                     (k & 7) * 2);
@@ -128,7 +133,9 @@ TQ_HD uint32_t sw128_offset(int n, int k) {
 
 // Device tables (inside the caller's d_tables buffer). S_sw is S (rows = projection index,
 // columns = coordinate) in the swizzled layout above; HD_sw is H diag(D) (entries +-1, bf16) in the
-// same layout; both present for head_dim 128. S_frag is S in f16
+// same layout; both present for head_dim 128. For head_dim 256, S_sw holds S with 256 rows (sw128_offset_rows
+// with 256 rows: four 32 KB atoms of 64 columns) and HD_sw holds H diag(D1) and H diag(D2) (128 x 128
+// each) for the two halves of D, with H the 128-point Hadamard. S_frag is S in f16
 // as m16n8k16 A fragments (see sfrag_idx), for the decode kernels' query projection.
 struct TableOffsets {
   size_t D, S, St, cb, S_sw, HD_sw, S_frag, bytes;
@@ -183,9 +190,9 @@ struct LayerView {
   const uint16_t* S;   // bf16 [d][d]
   const uint16_t* St;  // bf16 [d][d] transposed
   const float* cb;
-  const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128)
+  const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128 and 256)
   const uint4* S_frag;   // S in f16 m16n8k16 A fragments (sfrag_idx)
-  const uint16_t* HD_sw;  // H diag(D) in the tcgen05 swizzled K-major layout (head_dim 128)
+  const uint16_t* HD_sw;  // H diag(D) (head_dim 128; 256: H diag(D1), H diag(D2)) swizzled K-major
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes], or paged: [block][head][page_bytes]
   const int32_t* btab; // paged cache: block table [slot][max_pages] (all layers); nullptr: contiguous
   int n_blocks;        // paged cache: blocks per layer

@@ -1,9 +1,9 @@
 // Quantize-on-append ([Guide] §二, five-step pipeline). Two paths write packed pages (128 tokens of
 // one KV head):
-//   - CUDA-core kernels (one CTA per page) for ring flushes, decode-sized appends, f32 inputs and
-//     head_dim 256; their QJL projection z = S r is an fp32 FMA contraction against S^T in shared memory;
-//   - a persistent tcgen05 kernel for bulk bf16 appends at head_dim 128 (rotation and projection on
-//     the tensor cores).
+//   - CUDA-core kernels (four 32-token CTAs per page) for ring flushes, decode-sized appends, f32
+//     inputs and head_dim 64; their QJL projection z = S r is an f16 mma.sync GEMM per block;
+//   - persistent tcgen05 kernels for bulk bf16 appends at head_dim 128 (below) and 256
+//     (tq_quantize256.cu), with the rotation and the projection on the tensor cores.
 #include <algorithm>
 
 #include <cuda.h>
@@ -15,39 +15,6 @@
 
 namespace tq {
 namespace {
-
-// Which page this CTA writes, from the sequence state. Returns false when the CTA has no work.
-// An append codes every 128-token block that it completes, including the one that fills the ring to
-// 128 tokens (those stay in the ring as well until the next token starts a new ring block). So the
-// blocks below 128 floor(L / 128) are always coded, and a ring that rolls over finds its block coded.
-__device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int& slot, int& L, int& Np, int& pg,
-                                          int& valid, bool report) {
-  slot = a.seq_ids[b];
-  if (slot < 0 || slot >= a.lv.max_seqs) {
-    if (report) set_status(a.lv.status, TQ_DEV_ERR_SEQ_ID);
-    return false;
-  }
-  L = a.lv.state[2 * slot];
-  Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
-  if (a.flush) {
-    const int R = L - Np;
-    if (R <= 0 || j > 0) return false;
-    pg = Np / kPage;
-    valid = R;
-    return true;
-  }
-  const int nn = new_count(a, b);
-  const int L2 = L + nn;
-  if (nn < 0 || nn > a.max_new || L2 > a.lv.max_ctx) {
-    if (report) set_status(a.lv.status, TQ_DEV_ERR_CAPACITY);
-    return false;
-  }
-  const int C = kPage * (L / kPage), C2 = kPage * (L2 / kPage);  // complete blocks before and after
-  if (j >= (C2 - C) / kPage) return false;
-  pg = C / kPage + j;
-  valid = kPage;
-  return true;
-}
 
 // full_tq appends: codes tokens [t_lo, t_hi) of page pg (page-relative, one 32-token block at most)
 // and writes only their bits. Key words, {n, gamma} and value scales belong to one token each; a value
@@ -291,7 +258,7 @@ constexpr uint32_t kQbHD = 0, kQbS = 32768, kQbBuf = 65536;  // 2 x [K tile 32 K
 constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 value codes
 constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
 // mbarriers [8] (slot 6 holds the TMEM address), then the arming and completion counts of each barrier
-// ([8] + [8] u32, see bulk128_drain)
+// ([8] + [8] u32, see bulk_drain)
 constexpr uint32_t kQbBar = kQbX + 2048 + 6144 + 2048, kQbEnd = kQbBar + 128;
 constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 
@@ -301,7 +268,7 @@ constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byt
 // `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
 // all threads (at most one page per row and append).
 // The copy is made by the nthr threads whose index relative to `first` is in [0, nthr).
-// `armed` counts the copies armed on `bar` (see bulk128_drain).
+// `armed` counts the copies armed on `bar` (see bulk_drain).
 __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
                                              uint64_t* bar, uint32_t* armed, int first, int nthr) {
@@ -360,39 +327,6 @@ __device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint
   ++*armed;
 }
 
-// After the page loop of k_quantize_bulk128 (thread 0): every copy or MMA batch armed on one of the
-// CTA's barriers and not seen complete by the thread that counts it is waited for (bounded), so that
-// nothing lands in shared memory or TMEM after the CTA frees them. armed / done: per barrier, the
-// phases armed and the phases seen complete. In a run without a failed wait the counts are equal.
-// Returns false if a wait gives up here too.
-__device__ __forceinline__ bool bulk128_drain(uint64_t* bars, uint32_t* armed, uint32_t* done) {
-  bool ok = true;
-  for (int i = 0; i < 8; ++i) {
-    if (i == 6) continue;  // the TMEM address slot
-    while (done[i] < armed[i]) {
-      if (!mbar_wait(bars + i, done[i] & 1u)) {
-        ok = false;
-        break;
-      }
-      ++done[i];
-    }
-  }
-  return ok;
-}
-
-// Next task (>= task, stepping by the grid) that has a page to write, or ntasks.
-__device__ __forceinline__ int bulk128_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, int& b,
-                                            int& h, int& slot, int& L, int& Np, int& pg) {
-  for (; task < ntasks; task += gridDim.x) {
-    b = task / (a.lv.Hkv * pages_per_row);
-    h = (task / pages_per_row) % a.lv.Hkv;
-    const int j = task % pages_per_row;
-    int valid;
-    if (page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && threadIdx.x == 0)) return task;
-  }
-  return ntasks;
-}
-
 // KB = key bits: 3 (2-bit Lloyd-Max index + sign) or 4 (3-bit index + sign, served with 4-bit values).
 template <int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -442,7 +376,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t hd_addr = smem_u32(sm + kQbHD), s_addr = smem_u32(sm + kQbS), buf0 = smem_u32(sm + kQbBuf);
   const int ntasks = batch * lv.Hkv * pages_per_row;
   int b, h, slot, L, Np, pg;
-  int cur = bulk128_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+  int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
   bool tma_cur = cur < ntasks &&
                  bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0, kTcThreads);
@@ -517,7 +451,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   };
   while (ok && cur < ntasks) {
     const int cslot = slot, chead = h, cpg = pg;
-    const int nxt = bulk128_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+    const int nxt = bulk_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
     const bool rot_ok = mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u);
     if (tid == 0 && rot_ok) ++done[4 + bufi];
     ok = __syncthreads_and(rot_ok) != 0;
@@ -667,18 +601,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float sv = __half2float(sh);
         uint32_t cw[8];
         if (lv.vb == 2) {
-          // code = clamp(floor(fl(x / s)), -2, 1) + 2 = [fl(x/s) >= -1] + [fl(x/s) >= 0] + [fl(x/s) >= 1], and
-          // for s > 0: fl(x/s) >= -1  <=>  x/s >= -(1 + 2^-24)  <=>  x + s >= -s 2^-24 (ties round to the even
-          // -1); fl(x/s) >= 1  <=>  x - s >= -s 2^-25; fl(x/s) >= 0  <=>  x >= 0. x + s and x - s are exact
-          // where the comparison is close (Sterbenz), so no division is needed.
-          const float t_lo = -sv * 5.9604644775390625e-8f, t_hi = -sv * 2.98023223876953125e-8f;
+          // code = clamp(floor(fl(x / s)), -2, 1) + 2 = [x >= -s] + [x >= 0] + [x >= s] for fp32 x and s > 0
+          // (the rounded quotient's thresholds -(1 + 2^-24) and 1 - 2^-25 fall between s and its fp32
+          // neighbours; see value_code), so no division is needed.
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             uint32_t w = 0;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float xv = x[4 * k + e];
-              const uint32_t code = (uint32_t)(xv + sv >= t_lo) + (uint32_t)(xv >= 0.f) + (uint32_t)(xv - sv >= t_hi);
+              const uint32_t code = (uint32_t)(xv >= -sv) + (uint32_t)(xv >= 0.f) + (uint32_t)(xv >= sv);
               w |= code << (8 * e);
             }
             cw[k] = sv > 0.f ? w : 0x02020202u;  // a zero group: every code 2
@@ -783,7 +715,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();  // every count is final
   // copies or MMAs still pending after a failed wait are waited for before shared memory and TMEM are
   // given up; a no-op after a run without one
-  if (tid == 0 && !bulk128_drain(bar_tab, armed, done)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  if (tid == 0 && !bulk_drain(bar_tab, 8, 6, armed, done)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   __syncthreads();
   tc_fence_after();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
@@ -918,28 +850,6 @@ cudaError_t launch_append_small(const AppendArgs& a, int batch, cudaStream_t s) 
   return k4 ? launch_append_small_dk<256, 4>(a, batch, s) : launch_append_small_dk<256, 3>(a, batch, s);
 }
 
-// Bulk appends of head_dim 128 use the tcgen05 kernel: one persistent CTA per SM over all pages.
-// Tensor map of k or v ([batch][max_new][Hkv][128] bf16) for 64 x 1 x 128 x 1 boxes, 128-byte swizzle.
-cudaError_t bulk128_tensor_map(const void* base, int batch, int max_new, int hkv, CUtensorMap* m) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  if (!encode) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  }
-  const cuuint64_t dims[4] = {128, (cuuint64_t)hkv, (cuuint64_t)max_new, (cuuint64_t)batch};
-  const cuuint64_t strides[3] = {256, (cuuint64_t)hkv * 256, (cuuint64_t)max_new * hkv * 256};
-  const cuuint32_t box[4] = {64, 1, 128, 1};
-  const cuuint32_t estr[4] = {1, 1, 1, 1};
-  const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <int KB>
 cudaError_t launch_quantize_bulk128_k(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
   static bool attr_set = false;  // set once, outside any stream capture that follows
@@ -951,8 +861,8 @@ cudaError_t launch_quantize_bulk128_k(const AppendArgs& a, int batch, int pages,
   const int ntasks = batch * a.lv.Hkv * pages;
   const int grid = std::max(1, std::min(ntasks, sms));
   CUtensorMap tmk, tmv;
-  cudaError_t e = bulk128_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, &tmk);
-  if (e == cudaSuccess) e = bulk128_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, &tmv);
+  cudaError_t e = bulk_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, 128, &tmk);
+  if (e == cudaSuccess) e = bulk_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, 128, &tmv);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_quantize_bulk128<KB>, dim3(grid), dim3(kTcThreads), kTcSmem, s, tmk, tmv, a, pages, batch);
 }
@@ -962,6 +872,29 @@ cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, i
 }
 
 }  // namespace
+
+// Tensor map of k or v ([batch][max_new][Hkv][d] bf16, d = 128 or 256) for 64 x 1 x 128 x 1 boxes
+// (64 coordinates of 128 consecutive tokens of one head), 128-byte swizzle: the tcgen05 coders' page loads.
+cudaError_t bulk_tensor_map(const void* base, int batch, int max_new, int hkv, int d, CUtensorMap* m) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t row = 2ull * d;
+  const cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)hkv, (cuuint64_t)max_new, (cuuint64_t)batch};
+  const cuuint64_t strides[3] = {row, (cuuint64_t)hkv * row, (cuuint64_t)max_new * hkv * row};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const void* v, int dt,
                           const int32_t* seq_ids, const int32_t* n_new, int batch, int max_new, cudaStream_t s) {
@@ -977,10 +910,12 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.full = ctx->cfg.ring_size == 0;
   if (max_new < kPage) return launch_append_small(a, batch, s);  // page on ring overflow + ring rows + state
   const int pages = (max_new + kPage - 1) / kPage;
-  // the tcgen05 bulk coder serves head_dim 128 (key_bits 3 and 4); other shapes use the CUDA-core coder
-  cudaError_t e = (a.lv.d == 128 && max_new >= kPage && dt == 0)
-                      ? launch_quantize_bulk128(a, batch, pages, ctx->sm_count > 0 ? ctx->sm_count : 152, s)
-                      : launch_quantize(a, batch, pages, s);
+  // the tcgen05 bulk coders serve bf16 appends at head_dim 128 and 256 (key_bits 3 and 4); head_dim 64
+  // and f32 inputs use the CUDA-core coder
+  const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
+  cudaError_t e = (a.lv.d == 128 && dt == 0)   ? launch_quantize_bulk128(a, batch, pages, sms, s)
+                  : (a.lv.d == 256 && dt == 0) ? launch_quantize_bulk256(a, batch, pages, sms, s)
+                                               : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;
   // ring rows: up to 128 tokens x Hkv x (K, V) x d / 4 items per row, about 4 items per thread
   const int row_items = kPage * a.lv.Hkv * 2 * (a.lv.d / 4);

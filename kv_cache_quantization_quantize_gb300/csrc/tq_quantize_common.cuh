@@ -7,10 +7,11 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <cuda.h>
+
 #include "tq_device.cuh"
 
 namespace tq {
-namespace {
 
 constexpr int kQThreads = 256;  // 8 warps; warp w quantises tokens w, w + 8, ...
 
@@ -25,6 +26,14 @@ struct AppendArgs {
   int flush;  // 1: quantise the current ring block (tq_ring_flush)
   int full;   // 1: full_tq mode (ring_size 0): every appended token is quantised by the append itself
 };
+
+// Tensor map of k or v ([batch][max_new][Hkv][d] bf16) for the tcgen05 coders' page loads (tq_quantize.cu).
+cudaError_t bulk_tensor_map(const void* base, int batch, int max_new, int hkv, int d, CUtensorMap* m);
+// The head_dim 256 tcgen05 bulk coder (tq_quantize256.cu): `pages` page tasks per row, one persistent
+// CTA per SM (`sms`).
+cudaError_t launch_quantize_bulk256(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s);
+
+namespace {
 
 // New tokens of row b: n_new[b], or one per row when n_new is null (a decode step's append).
 __device__ __forceinline__ int new_count(const AppendArgs& a, int b) { return a.n_new ? a.n_new[b] : 1; }
@@ -144,15 +153,16 @@ constexpr size_t quantize_smem_bytes_d() {
 
 // Mid-rise value code clamp(floor(fl(x / s)), -2^(vb-1), 2^(vb-1) - 1) + 2^(vb-1) for a scale s > 0 (the
 // decision of an IEEE division rounded to nearest), without a division on the common path:
-//   2 bits: three comparisons. fl(x / s) >= -1 exactly when x / s >= -(1 + 2^-24) (the midpoint below -1
-//     rounds to the even -1), i.e. x + s >= -s 2^-24; fl(x / s) >= 0 exactly when x >= 0; fl(x / s) >= 1
-//     exactly when x / s >= 1 - 2^-25, i.e. x - s >= -s 2^-25. Near those points x + s and x - s are exact
-//     (Sterbenz), and away from them rounding cannot change the comparison.
+//   2 bits: three comparisons, code = [x >= -s] + [x >= 0] + [x >= s]. fl(x / s) >= -1 exactly when
+//     x / s >= -(1 + 2^-24) (the midpoint below -1 rounds to the even -1), and no fp32 lies strictly between
+//     -s (1 + 2^-24) and -s (the fp32 next to -s is an ulp of s > s 2^-24 away), so for fp32 x that is
+//     x >= -s. Likewise fl(x / s) >= 1 exactly when x / s >= 1 - 2^-25, i.e. x >= s, and fl(x / s) >= 0
+//     exactly when x >= 0.
 //   4 bits: the floor of x * (1 / s), which lies within a few ulps of the rounded quotient, so it is
 //     exact unless the product is within 4 ulps of an integer; those take the division.
 __device__ __forceinline__ int value_code(float x, float s, float rcp, int vb) {
   if (vb == 2)
-    return (int)(x + s >= -s * 5.9604644775390625e-8f) + (int)(x >= 0.f) + (int)(x - s >= -s * 2.98023223876953125e-8f);
+    return (int)(x >= -s) + (int)(x >= 0.f) + (int)(x >= s);
   const int vhalf = 1 << (vb - 1);
   const float qv = x * rcp;
   float fq = floorf(qv);
@@ -419,6 +429,73 @@ __device__ __forceinline__ void quantize_page_cta(const AppendArgs& a, int b, in
   uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
   for (int i = t0 * (D / 32) + tid; i < t1 * (D / 32); i += NT)
     sw[vscale_idx(D, i / (D / 32), i % (D / 32))] = scales[i - t0 * (D / 32)];
+}
+
+// Which page this CTA writes, from the sequence state. Returns false when the CTA has no work.
+// An append codes every 128-token block that it completes, including the one that fills the ring to
+// 128 tokens (those stay in the ring as well until the next token starts a new ring block). So the
+// blocks below 128 floor(L / 128) are always coded, and a ring that rolls over finds its block coded.
+__device__ __forceinline__ bool page_task(const AppendArgs& a, int b, int j, int& slot, int& L, int& Np, int& pg,
+                                          int& valid, bool report) {
+  slot = a.seq_ids[b];
+  if (slot < 0 || slot >= a.lv.max_seqs) {
+    if (report) set_status(a.lv.status, TQ_DEV_ERR_SEQ_ID);
+    return false;
+  }
+  L = a.lv.state[2 * slot];
+  Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+  if (a.flush) {
+    const int R = L - Np;
+    if (R <= 0 || j > 0) return false;
+    pg = Np / kPage;
+    valid = R;
+    return true;
+  }
+  const int nn = new_count(a, b);
+  const int L2 = L + nn;
+  if (nn < 0 || nn > a.max_new || L2 > a.lv.max_ctx) {
+    if (report) set_status(a.lv.status, TQ_DEV_ERR_CAPACITY);
+    return false;
+  }
+  const int C = kPage * (L / kPage), C2 = kPage * (L2 / kPage);  // complete blocks before and after
+  if (j >= (C2 - C) / kPage) return false;
+  pg = C / kPage + j;
+  valid = kPage;
+  return true;
+}
+
+// After the page loop of a persistent tcgen05 coder (thread 0): every copy or MMA batch armed on one
+// of the CTA's barriers and not seen complete by the thread that counts it is waited for (bounded), so
+// that nothing lands in shared memory or TMEM after the CTA frees them. armed / done: per barrier, the
+// phases armed and the phases seen complete. In a run without a failed wait the counts are equal.
+// Slot `skip` of the n barrier slots holds the TMEM address. Returns false if a wait gives up here too.
+__device__ __forceinline__ bool bulk_drain(uint64_t* bars, int n, int skip, uint32_t* armed, uint32_t* done) {
+  bool ok = true;
+  for (int i = 0; i < n; ++i) {
+    if (i == skip) continue;  // the TMEM address slot
+    while (done[i] < armed[i]) {
+      if (!mbar_wait(bars + i, done[i] & 1u)) {
+        ok = false;
+        break;
+      }
+      ++done[i];
+    }
+  }
+  return ok;
+}
+
+// Next task (>= task, stepping by the grid) that has a page to write, or ntasks. Thread `reporter` of
+// the CTA reports a row's bad sequence id or capacity (at the row's first task).
+__device__ __forceinline__ int bulk_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, int& b,
+                                         int& h, int& slot, int& L, int& Np, int& pg, int reporter = 0) {
+  for (; task < ntasks; task += gridDim.x) {
+    b = task / (a.lv.Hkv * pages_per_row);
+    h = (task / pages_per_row) % a.lv.Hkv;
+    const int j = task % pages_per_row;
+    int valid;
+    if (page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && (int)threadIdx.x == reporter)) return task;
+  }
+  return ntasks;
 }
 
 }  // namespace

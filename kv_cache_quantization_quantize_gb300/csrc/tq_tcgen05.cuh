@@ -15,6 +15,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
          ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
+// The same descriptor as two 32-bit words: the low word holds the start address (bits 0-13, in 16-byte
+// units) and the leading byte offset; the high word the stride byte offset, the version bit and the
+// swizzle mode. For shared addresses below 256 KB, lo(addr + off) = lo(addr) + off / 16 (off a multiple of
+// 16), so an MMA loop can step its operands with one add per descriptor.
+__device__ __forceinline__ uint32_t umma_desc_sw128_lo(uint32_t smem_addr) { return (smem_addr >> 4) | (1u << 16); }
+constexpr uint32_t kUmmaDescSw128Hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ void umma_bf16_lo(uint32_t tmem_d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 da, db;\n setp.ne.b32 p, %4, 0;\n mov.b64 da, {%1, %5};\n mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kUmmaDescSw128Hi));
+}
 // Instruction descriptor, kind::f16: D = f32, A = B = bf16, both K-major, N = 128, M = 128.
 constexpr uint32_t kIdescBf16M128N128 = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 
