@@ -770,8 +770,8 @@ def profile_quantize(passes):
     from kv_cache_quantization_quantize_gb300 import synth
     dev = torch.device("cuda", 0)
     T, Hkv, d, vb = PREFILL["tokens"], PREFILL["hkv"], PREFILL["d"], PREFILL["vb"]
-    cfg = tqm.config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=4 * Hkv, max_seqs=1,
-                     max_ctx=T, seed=PREFILL["seed"])
+    cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=PREFILL["kb"], n_layers=1, n_kv_heads=Hkv,
+                     n_q_heads=4 * Hkv, max_seqs=1, max_ctx=T, seed=PREFILL["seed"])
     qc = tqm.TurboQuantCache(cfg, device=dev)
     k, v = synth.kv_tokens(T, Hkv, d, seed=PREFILL["seed"], outliers=WL["outliers"], device=dev)
     k, v = k[None].contiguous(), v[None].contiguous()

@@ -312,17 +312,14 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
 __device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar,
                                                uint32_t* armed) {
   tc_fence_after();
+  const uint32_t xa = umma_desc_sw128_lo(buf), hb = umma_desc_sw128_lo(hd_addr);
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-    umma_bf16(tcol, umma_desc_sw128(buf + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128, ks > 0);
-  }
+  for (int part = 0; part < 2; ++part)  // K, then V (+32 KB = 2048 descriptor units)
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-    umma_bf16(tcol + 128, umma_desc_sw128(buf + 32768 + koff), umma_desc_sw128(hd_addr + koff), kIdescBf16M128N128,
-              ks > 0);
-  }
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t koff = (ks >> 2) * 1024u + (ks & 3) * 2u;  // atom 16 KB, k step 32 B, in 16-byte units
+      umma_bf16_lo(tcol + 128u * part, xa + part * 2048u + koff, hb + koff, kIdescBf16M128N128, ks > 0);
+    }
   umma_commit(bar);
   ++*armed;
 }
@@ -376,7 +373,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t hd_addr = smem_u32(sm + kQbHD), s_addr = smem_u32(sm + kQbS), buf0 = smem_u32(sm + kQbBuf);
   const int ntasks = batch * lv.Hkv * pages_per_row;
   int b, h, slot, L, Np, pg;
-  int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+  RowTask rc;  // this thread's cached row lookup
+  int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
   bool tma_cur = cur < ntasks &&
                  bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0, kTcThreads);
@@ -410,17 +408,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int t = 32 * q4 + lane;
   float* xs = reinterpret_cast<float*>(sm + kQbX);                  // [2 halves][128] partial |y'|^2
   float* xr = xs + 256;                                             // [2][128] partial |r|^2
-  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [128][4 MB] half-1 index words
-  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 8192);     // [128][4] half-1 sign words
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [4 MB][128] half-1 index words
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 8192);     // [4][128] half-1 sign words
   const PageLayout pl = page_layout(D, lv.vb, KB);
   uint8_t* prev_page = nullptr;  // page whose QJL signs are still to be written (its MMAs are in flight)
   bool prev = false;
-  // QJL signs of the page in TMEM half `hb` (value warps): wait for its projection, threshold z = S r,
-  // write the sign plane. Returns false if the wait gave up.
-  auto qjl_signs = [&](uint32_t hb, uint8_t* page) -> bool {
+  // Wait for the projection of the page in TMEM half `hb` (value warps); false if the wait gave up.
+  auto qjl_wait = [&](uint32_t hb) -> bool {
     const bool w_ok = mbar_wait(bar_qjl2(hb), (ph_qjl >> hb) & 1u);
     if (tid == 256 && w_ok) ++done[qjl_idx(hb)];
     ph_qjl ^= 1u << hb;
+    return w_ok;
+  };
+  // QJL signs of the page in TMEM half `hb` (value warps, after qjl_wait): threshold z = S r, write the
+  // sign plane.
+  auto qjl_signs = [&](uint32_t hb, uint8_t* page) {
     tc_fence_after();
     const uint32_t prow = tmem + 256u * hb + ((uint32_t)(32 * q4) << 16);
     uint32_t wsg[4] = {0u, 0u, 0u, 0u};
@@ -437,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (half) {
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) xg[t * 4 + cw] = wsg[cw] << 8;
+      for (int cw = 0; cw < 4; ++cw) xg[cw * 128 + t] = wsg[cw] << 8;
     }
     tc_fence_before();
     named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
@@ -445,13 +447,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
       const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[t * 4 + cw];
+      for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[cw * 128 + t];
     }
-    return w_ok;
   };
   while (ok && cur < ntasks) {
     const int cslot = slot, chead = h, cpg = pg;
-    const int nxt = bulk_next(a, cur + gridDim.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+    const int nxt = bulk_next(a, cur + gridDim.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
     const bool rot_ok = mbar_wait(bar_rot + bufi, (ph_rot >> bufi) & 1u);
     if (tid == 0 && rot_ok) ++done[4 + bufi];
     ok = __syncthreads_and(rot_ok) != 0;
@@ -477,12 +478,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       named_barrier(1, 256);
       const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
       const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
+      // The index of y = v / nrot (v = the rotated coordinate before normalisation) is decided as v > t nrot
+      // for each boundary t (a zero vector compares v = 0 with t itself: y = 0), and the residual is
+      // y - c = fma(v, 1 / nrot, -c).
       constexpr int NL = 1 << MB;  // Lloyd-Max levels
-      float cent[NL], bnd[NL - 1];
+      float ncent[NL], bnd[NL - 1];
 #pragma unroll
-      for (int i = 0; i < NL; ++i) cent[i] = lv.cb[kCbCent + i];
+      for (int i = 0; i < NL; ++i) ncent[i] = -lv.cb[kCbCent + i];
 #pragma unroll
-      for (int i = 0; i < NL - 1; ++i) bnd[i] = lv.cb[kCbBnd + i];
+      for (int i = 0; i < NL - 1; ++i) bnd[i] = nrot > 0.f ? lv.cb[kCbBnd + i] * nrot : lv.cb[kCbBnd + i];
       uint32_t wix[MB][4];  // index planes, highest bit first
 #pragma unroll
       for (int p = 0; p < MB; ++p) wix[p][0] = wix[p][1] = wix[p][2] = wix[p][3] = 0u;
@@ -500,22 +504,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate 64 half + jl
-              const float yy = __uint_as_float(v[i]) * scale;
-              // index = #{boundaries below yy}, by binary search over the sorted boundaries
+              const float vv = __uint_as_float(v[i]);
+              // index = #{boundaries below y}, by binary search over the sorted (scaled) boundaries
               bool ib[MB];
-              float cv;
+              float ncv;
               if constexpr (MB == 2) {
-                ib[0] = yy > bnd[1];
-                ib[1] = yy > (ib[0] ? bnd[2] : bnd[0]);
-                cv = ib[0] ? (ib[1] ? cent[3] : cent[2]) : (ib[1] ? cent[1] : cent[0]);
+                ib[0] = vv > bnd[1];
+                ib[1] = vv > (ib[0] ? bnd[2] : bnd[0]);
+                ncv = ib[0] ? (ib[1] ? ncent[3] : ncent[2]) : (ib[1] ? ncent[1] : ncent[0]);
               } else {
-                ib[0] = yy > bnd[3];
-                ib[1] = yy > (ib[0] ? bnd[5] : bnd[1]);
-                ib[2] = yy > (ib[0] ? (ib[1] ? bnd[6] : bnd[4]) : (ib[1] ? bnd[2] : bnd[0]));
-                cv = ib[0] ? (ib[1] ? (ib[2] ? cent[7] : cent[6]) : (ib[2] ? cent[5] : cent[4]))
-                           : (ib[1] ? (ib[2] ? cent[3] : cent[2]) : (ib[2] ? cent[1] : cent[0]));
+                ib[0] = vv > bnd[3];
+                ib[1] = vv > (ib[0] ? bnd[5] : bnd[1]);
+                ib[2] = vv > (ib[0] ? (ib[1] ? bnd[6] : bnd[4]) : (ib[1] ? bnd[2] : bnd[0]));
+                ncv = ib[0] ? (ib[1] ? (ib[2] ? ncent[7] : ncent[6]) : (ib[2] ? ncent[5] : ncent[4]))
+                            : (ib[1] ? (ib[2] ? ncent[3] : ncent[2]) : (ib[2] ? ncent[1] : ncent[0]));
               }
-              const float res = yy - cv;
+              const float res = fmaf(vv, scale, ncv);
               rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
               res2[e] = res;
               // bit of coordinate j = 64 half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
@@ -540,7 +544,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int p = 0; p < MB; ++p)
 #pragma unroll
-          for (int cw = 0; cw < 4; ++cw) xw[t * 4 * MB + 4 * p + cw] = wix[p][cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
+          for (int cw = 0; cw < 4; ++cw) xw[(4 * p + cw) * 128 + t] = wix[p][cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
@@ -548,11 +552,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t buf = buf0 + bufi * 65536u;
       if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
         tc_fence_after();
+        const uint32_t ra = umma_desc_sw128_lo(buf), sa = umma_desc_sw128_lo(s_addr);
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {
-          const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32 + (ks >> 3) * 32768;
-          umma_bf16(tmem + 256u * bufi, umma_desc_sw128(buf + koff),
-                    umma_desc_sw128(s_addr + ((ks & 7) >> 2) * 16384 + (ks & 3) * 32), kIdescBf16M128N128, ks > 0);
+        for (int ks = 0; ks < 16; ++ks) {  // hi (ks < 8), then lo (+32 KB); atoms of 16 KB, k steps of 32 B
+          const uint32_t koff = ((ks & 7) >> 2) * 1024u + (ks & 3) * 2u;
+          umma_bf16_lo(tmem + 256u * bufi, ra + koff + (ks >> 3) * 2048u, sa + koff, kIdescBf16M128N128, ks > 0);
         }
         umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
         ++armed[qjl_idx(bufi)];
@@ -569,16 +573,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int p = 0; p < MB; ++p)
 #pragma unroll
           for (int cw = 0; cw < 4; ++cw)
-            kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[t * 4 * MB + 4 * p + cw];
+            kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[(4 * p + cw) * 128 + t];
       }
     } else {
-      // ---- the previous page's QJL signs; this frees buffer and TMEM half bufi ^ 1 ----
-      if (prev) ok_p = qjl_signs(bufi ^ 1u, prev_page);
-      // ---- start the copy of the next page into buffer bufi ^ 1 ----
-      bool tma_nxt = false;
-      if (nxt < ntasks)
-        tma_nxt = bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u,
-                               bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 256);
+      // ---- the previous page's projection (it reads buffer bufi ^ 1); then the next page's copy starts
+      // there at once (a TMA copy, by thread 256), and the signs of the previous page are written ----
+      const bool nxt_tma = nxt < ntasks && pg * kPage >= L;  // b..pg describe the next page here
+      if (prev) ok_p = qjl_wait(bufi ^ 1u);
+      if (nxt_tma && ok_p)
+        bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u, bar_ld + (bufi ^ 1u),
+                     armed + 2 + (bufi ^ 1u), 256, 1);
+      if (prev) qjl_signs(bufi ^ 1u, prev_page);
+      // a next page that starts in the ring is copied by all value threads (TMEM half bufi ^ 1 is free now)
+      if (nxt < ntasks && !nxt_tma)
+        bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u, bar_ld + (bufi ^ 1u),
+                     armed + 2 + (bufi ^ 1u), 256, 256);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
       // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
       const int vhalf = 1 << (lv.vb - 1);
@@ -654,7 +663,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (tid == 256 && nxt < ntasks) {  // rotation of the next page into TMEM half bufi ^ 1
         tc_fence_after();
         bool landed = true;
-        if (tma_nxt) {
+        if (nxt_tma) {
           landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
           if (landed) ++done[2 + (bufi ^ 1u)];
           else set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
@@ -664,7 +673,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                          armed + 4 + (bufi ^ 1u));
         else ok_p = false;
       }
-      if (tma_nxt) ph_ld ^= 1u << (bufi ^ 1u);
+      if (nxt_tma) ph_ld ^= 1u << (bufi ^ 1u);
       // ---- pack the value codes (fragment-major layout) ----
       const int vt = tid - 256;
       uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
@@ -709,7 +718,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     bufi ^= 1u;
   }
   // the last page's QJL signs (its projection was issued in the final iteration)
-  if (ok && prev && !kpath && !qjl_signs(bufi ^ 1u, prev_page)) ok = false;
+  if (ok && prev && !kpath) {
+    if (qjl_wait(bufi ^ 1u)) qjl_signs(bufi ^ 1u, prev_page);
+    else ok = false;
+  }
   if (!ok && (tid == 0 || tid == 256)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();  // every count is final

@@ -101,6 +101,19 @@ __device__ __forceinline__ bool bulk256_load(const AppendArgs& a, const CUtensor
   return false;
 }
 
+// Prefetch of page pg's K and V rows (new input only) into L2, by the calling thread: the page copy
+// that follows the next projection then reads L2 instead of HBM.
+__device__ __forceinline__ void bulk256_prefetch(const CUtensorMap* tmk, const CUtensorMap* tmv, int b, int h, int L,
+                                                 int pg) {
+  const int z = pg * kPage - L;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];\n" ::"l"(
+                     reinterpret_cast<uint64_t>(i < 4 ? tmk : tmv)),
+                 "r"(64 * (i & 3)), "r"(h), "r"(z), "r"(b)
+                 : "memory");
+}
+
 // Rotation products of the page in X (thread 0): TMEM columns [0, 128) = u1 of K, [128, 256) = u2 of K,
 // [256, 384) = u1 of V, [384, 512) = u2 of V, with u_i[t][n] = sum_j x_i[t][j] (H diag(D_i))[n][j].
 __device__ __forceinline__ void bulk256_rotate(uint32_t tmem, uint32_t x_addr, uint32_t hd_addr, uint64_t* bar,
@@ -194,7 +207,7 @@ __device__ __forceinline__ void bulk256_keys(const LayerView& lv, uint32_t lrow,
   constexpr int D = 256, MB = KB - 1;
   float* xs = reinterpret_cast<float*>(sb + kSbXs);      // [2][128] partial |u1|^2 + |u2|^2
   float* xr = reinterpret_cast<float*>(sb + kSbXr);      // [2][128] partial |r|^2
-  uint32_t* xw = reinterpret_cast<uint32_t*>(sb + kSbXw);  // [half][128][4 MB] partner's index-word partials
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sb + kSbXw);  // [half][4 MB][128] partner's index-word partials
   // ---- |y'|^2 = |u1 + u2|^2 + |u1 - u2|^2 = 2 (|u1|^2 + |u2|^2) ----
   float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -281,7 +294,7 @@ __device__ __forceinline__ void bulk256_keys(const LayerView& lv, uint32_t lrow,
 #pragma unroll
       for (int p = 0; p < MB; ++p)
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) xw[((1 - hp) * 128 + t) * 4 * MB + 4 * p + cw] = wix[p][cw];
+        for (int cw = 0; cw < 4; ++cw) xw[((1 - hp) * 4 * MB + 4 * p + cw) * 128 + t] = wix[p][cw];
     }
   }
   xr[hp * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
@@ -294,7 +307,7 @@ __device__ __forceinline__ void bulk256_keys(const LayerView& lv, uint32_t lrow,
 #pragma unroll
       for (int cw = 0; cw < 4; ++cw) {
         const uint32_t own = wix[p][cw];
-        const uint32_t other = xw[(hp * 128 + t) * 4 * MB + 4 * p + cw];
+        const uint32_t other = xw[(hp * 4 * MB + 4 * p + cw) * 128 + t];
         kw[(((tile * KB + p) * 2 + hp) * 32 + 4 * g + cw) * 2 + r] = (own << (8 * hp)) | (other << (8 * (1 - hp)));
       }
     if (hp == 0) {  // n and gamma of token t
@@ -459,7 +472,7 @@ __device__ __forceinline__ void bulk256_signs(uint32_t tmem, int warp, int lane,
                                               const PageLayout& pl) {
   const int q4 = warp & 3, qc = warp >> 2, half = qc >> 1, sl = qc & 1;
   const int t = 32 * q4 + lane;
-  uint32_t* xg = reinterpret_cast<uint32_t*>(sb);  // [half][128][4]
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sb);  // [half][4][128]
   uint32_t wsg[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
   for (int cc = 0; cc < 2; ++cc) {
@@ -473,7 +486,7 @@ __device__ __forceinline__ void bulk256_signs(uint32_t tmem, int warp, int lane,
   }
   if (sl) {
 #pragma unroll
-    for (int cw = 0; cw < 4; ++cw) xg[(half * 128 + t) * 4 + cw] = wsg[cw] << 8;
+    for (int cw = 0; cw < 4; ++cw) xg[(half * 4 + cw) * 128 + t] = wsg[cw] << 8;
   }
   tc_fence_before();
   __syncthreads();
@@ -483,7 +496,7 @@ __device__ __forceinline__ void bulk256_signs(uint32_t tmem, int warp, int lane,
     const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
 #pragma unroll
     for (int cw = 0; cw < 4; ++cw)
-      kw[(((tile * KB + MB) * 2 + half) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[(half * 128 + t) * 4 + cw];
+      kw[(((tile * KB + MB) * 2 + half) * 32 + 4 * g + cw) * 2 + r] = wsg[cw] | xg[(half * 4 + cw) * 128 + t];
   }
 }
 
@@ -528,7 +541,8 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
   const int ntasks = batch * lv.Hkv * pages_per_row;
   const PageLayout pl = page_layout(D, lv.vb, KB);
   int b, h, slot, L, Np, pg;
-  int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, b, h, slot, L, Np, pg);
+  RowTask rc;  // this thread's cached row lookup
+  int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
   bool tma = cur < ntasks && bulk256_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, x, bars + kB2Ld, armed + kB2Ld);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
   __syncthreads();  // every plain-copied row is in X before thread 0 issues the rotation
@@ -549,7 +563,10 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
     }
     if (tid == 32) {  // the next task, while the rotation runs (its state loads are off every other path)
       int* nt = reinterpret_cast<int*>(sm + kQ2Next);
-      nt[0] = bulk_next(a, cur + gridDim.x, ntasks, pages_per_row, nt[1], nt[2], nt[3], nt[4], nt[5], nt[6], 32);
+      int nb, nh, ns, nL, nNp, npg;
+      const int nx = bulk_next(a, cur + gridDim.x, ntasks, pages_per_row, rc, nb, nh, ns, nL, nNp, npg, 32);
+      if (nx < ntasks && npg * kPage >= nL) bulk256_prefetch(&tmk, &tmv, nb, nh, nL, npg);
+      nt[0] = nx, nt[1] = nb, nt[2] = nh, nt[3] = ns, nt[4] = nL, nt[5] = nNp, nt[6] = npg;
     }
     ok = __syncthreads_and(ok) != 0;
     if (!ok) break;

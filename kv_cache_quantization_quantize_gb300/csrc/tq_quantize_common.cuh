@@ -484,16 +484,46 @@ __device__ __forceinline__ bool bulk_drain(uint64_t* bars, int n, int skip, uint
   return ok;
 }
 
-// Next task (>= task, stepping by the grid) that has a page to write, or ntasks. Thread `reporter` of
-// the CTA reports a row's bad sequence id or capacity (at the row's first task).
-__device__ __forceinline__ int bulk_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, int& b,
-                                         int& h, int& slot, int& L, int& Np, int& pg, int reporter = 0) {
+// The pages one row of a bulk append writes (page_task's per-row part, for appends): its slot, L and the
+// page count (from page L / 128 on); npages = 0 for a row with a bad sequence id or capacity (reported
+// when `report`). b = -1: nothing cached yet.
+struct RowTask {
+  int b = -1, slot = 0, L = 0, npages = 0;
+};
+__device__ __forceinline__ void row_task(const AppendArgs& a, int b, RowTask& r, bool report) {
+  r.b = b;
+  r.npages = 0;
+  r.slot = a.seq_ids[b];
+  if (r.slot < 0 || r.slot >= a.lv.max_seqs) {
+    if (report) set_status(a.lv.status, TQ_DEV_ERR_SEQ_ID);
+    return;
+  }
+  r.L = a.lv.state[2 * r.slot];
+  const int nn = new_count(a, b), L2 = r.L + nn;
+  if (nn < 0 || nn > a.max_new || L2 > a.lv.max_ctx) {
+    if (report) set_status(a.lv.status, TQ_DEV_ERR_CAPACITY);
+    return;
+  }
+  r.npages = L2 / kPage - r.L / kPage;  // complete blocks after the append minus those before (as page_task)
+}
+
+// Next task (>= task, stepping by the grid) that has a page to write, or ntasks; for appends (not
+// flushes). The row lookup is cached in rc, so a CTA whose tasks stay in one row reads the row's state
+// once. Thread `reporter` of the CTA reports a row's bad sequence id or capacity (at the row's first
+// task, which is also the first task of that row any CTA visits).
+__device__ __forceinline__ int bulk_next(const AppendArgs& a, int task, int ntasks, int pages_per_row, RowTask& rc,
+                                         int& b, int& h, int& slot, int& L, int& Np, int& pg, int reporter = 0) {
   for (; task < ntasks; task += gridDim.x) {
     b = task / (a.lv.Hkv * pages_per_row);
     h = (task / pages_per_row) % a.lv.Hkv;
     const int j = task % pages_per_row;
-    int valid;
-    if (page_task(a, b, j, slot, L, Np, pg, valid, h == 0 && j == 0 && (int)threadIdx.x == reporter)) return task;
+    if (b != rc.b) row_task(a, b, rc, h == 0 && j == 0 && (int)threadIdx.x == reporter);
+    if (j >= rc.npages) continue;
+    slot = rc.slot;
+    L = rc.L;
+    Np = L > 0 ? kPage * ((L - 1) / kPage) : 0;
+    pg = L / kPage + j;
+    return task;
   }
   return ntasks;
 }
