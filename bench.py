@@ -268,7 +268,7 @@ def bench_config(world, mode="hybrid", layout="contiguous"):
     return cfg
 
 
-DECODE_SOURCES = ("tq_decode.cu", "tq_decode_common.cuh", "tq_device.cuh", "tq_internal.h")
+DECODE_SOURCES = ("tq_decode.cu", "tq_decode_common.cuh", "tq_quantize_common.cuh", "tq_device.cuh", "tq_internal.h")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "k_decode_llama8b_b1_ctx32k.md")
 
 
