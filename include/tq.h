@@ -272,6 +272,19 @@ tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, flo
  * Process-wide; set it only while no other thread launches decodes. */
 tq_status tq_debug_decode_wait_fault(int stage, int polls);
 
+/* Test hook for the bounded waits of the tcgen05 bulk coders (bf16 appends of >= 128 tokens at head_dim 128
+ * and 256; not part of the append itself). task >= 0 makes every following such tq_quantize_append skip the
+ * TMA copy of page task `task`, numbered (row * n_kv_heads + head) * pages_per_row + j with
+ * pages_per_row = ceil(max_new / 128) and j the j-th complete block the append codes for that row: the CTA
+ * that owns the task issues neither the copy nor its expected-byte count, and its wait on it gives up after
+ * `polls` polls (1 .. 2^22). That CTA then sets TQ_DEV_ERR_TIMEOUT, waits (bounded) for every copy and MMA
+ * batch it did issue, frees its tensor memory and returns: the pages it had not finished are unspecified,
+ * every other page is exact, and the cache stays usable. A task that is not a TMA copy (a page that starts
+ * in the ring, or no such task) changes nothing. Nothing faults or hangs. task = -1 turns the hook off (the
+ * default). Returns TQ_ERR_INVALID_ARG for values out of range. Process-wide; set it only while no other
+ * thread appends. */
+tq_status tq_debug_append_wait_fault(int task, int polls);
+
 /* Test hook for the two prefill paths (not part of the prefill itself): mode 1 makes every following
  * tq_prefill_attention (and tq_prefill_workspace_bytes) take the CUDA-core decode-kernel path even where
  * the tcgen05 path applies; mode 0 (the default) chooses automatically. Returns TQ_ERR_INVALID_ARG for

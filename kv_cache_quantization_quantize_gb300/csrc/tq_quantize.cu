@@ -5,6 +5,7 @@
 //   - persistent tcgen05 kernels for bulk bf16 appends at head_dim 128 (below) and 256
 //     (tq_quantize256.cu), with the rotation and the projection on the tensor cores.
 #include <algorithm>
+#include <atomic>
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -14,6 +15,12 @@
 #include "tq_tcgen05.cuh"
 
 namespace tq {
+
+// tq_debug_append_wait_fault: the page task whose TMA copy the tcgen05 coders skip (-1: none) and the polls
+// of its wait
+std::atomic<int> g_qfault_task{-1};
+std::atomic<int> g_qfault_polls{0};
+
 namespace {
 
 // full_tq appends: codes tokens [t_lo, t_hi) of page pg (page-relative, one 32-token block at most)
@@ -268,15 +275,16 @@ constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byt
 // `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
 // all threads (at most one page per row and append).
 // The copy is made by the nthr threads whose index relative to `first` is in [0, nthr).
-// `armed` counts the copies armed on `bar` (see bulk_drain).
+// `armed` counts the copies armed on `bar` (see bulk_drain). skip (test hook): a TMA copy is not issued
+// at all (no expected bytes either), so its wait gives up.
 __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
-                                             uint64_t* bar, uint32_t* armed, int first, int nthr) {
+                                             uint64_t* bar, uint32_t* armed, int first, int nthr, bool skip = false) {
   constexpr int D = 128;
   const int rel = (int)threadIdx.x - first;
   if (rel < 0 || rel >= nthr) return pg * kPage >= L;
   if (pg * kPage >= L) {
-    if (rel == 0) {
+    if (rel == 0 && !skip) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_expect_tx(bar, 4u * 16384u);
       ++*armed;
@@ -376,8 +384,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   RowTask rc;  // this thread's cached row lookup
   int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
-  bool tma_cur = cur < ntasks &&
-                 bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0, kTcThreads);
+  bool ld_skipped = cur == a.fault_task;  // the wait-timeout test hook: this page's copy is not issued
+  bool tma_cur = cur < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0,
+                                              kTcThreads, ld_skipped);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   const bool tab_ok = mbar_wait(bar_tab, 0);
   if (tid == 0 && tab_ok) ++done[0];
@@ -394,7 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // issued here.
   if (ok && cur < ntasks && tid == 0) {
     if (tma_cur) {
-      if (mbar_wait(bar_ld, 0)) ++done[2];
+      if (mbar_wait(bar_ld, 0, ld_skipped ? a.fault_polls : kWaitPolls)) ++done[2];
       else ok = false;
     }
     if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot, armed + 4);
@@ -580,9 +589,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       // there at once (a TMA copy, by thread 256), and the signs of the previous page are written ----
       const bool nxt_tma = nxt < ntasks && pg * kPage >= L;  // b..pg describe the next page here
       if (prev) ok_p = qjl_wait(bufi ^ 1u);
+      ld_skipped = nxt == a.fault_task;
       if (nxt_tma && ok_p)
         bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u, bar_ld + (bufi ^ 1u),
-                     armed + 2 + (bufi ^ 1u), 256, 1);
+                     armed + 2 + (bufi ^ 1u), 256, 1, ld_skipped);
       if (prev) qjl_signs(bufi ^ 1u, prev_page);
       // a next page that starts in the ring is copied by all value threads (TMEM half bufi ^ 1 is free now)
       if (nxt < ntasks && !nxt_tma)
@@ -664,7 +674,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after();
         bool landed = true;
         if (nxt_tma) {
-          landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u);
+          landed = mbar_wait(bar_ld + (bufi ^ 1u), (ph_ld >> (bufi ^ 1u)) & 1u, ld_skipped ? a.fault_polls : kWaitPolls);
           if (landed) ++done[2 + (bufi ^ 1u)];
           else set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
         }
@@ -920,6 +930,8 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.max_new = max_new;
   a.flush = 0;
   a.full = ctx->cfg.ring_size == 0;
+  a.fault_task = g_qfault_task.load();
+  a.fault_polls = (uint32_t)g_qfault_polls.load();
   if (max_new < kPage) return launch_append_small(a, batch, s);  // page on ring overflow + ring rows + state
   const int pages = (max_new + kPage - 1) / kPage;
   // the tcgen05 bulk coders serve bf16 appends at head_dim 128 and 256 (key_bits 3 and 4); head_dim 64
@@ -959,3 +971,12 @@ cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
 }
 
 }  // namespace tq
+
+extern "C" tq_status tq_debug_append_wait_fault(int task, int polls) {
+  if (task < -1) return tq::set_error(TQ_ERR_INVALID_ARG, "task must be -1 (off) or >= 0");
+  if (task >= 0 && (polls < 1 || polls > (int)tq::kWaitPolls))
+    return tq::set_error(TQ_ERR_INVALID_ARG, "polls must be in [1, 2^22]");
+  tq::g_qfault_polls.store(task >= 0 ? polls : 0);
+  tq::g_qfault_task.store(task);
+  return tq::set_error(TQ_OK, "");
+}

@@ -64,13 +64,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
 // atoms of 64 coordinates (element (t, j) at sw128_offset(t, j)). Pages made of new input only are
 // fetched by eight TMA tensor copies that complete on `bar` (returns true; thread 0 issues them and
 // counts the arming in *armed). Pages that start in the ring are copied by all threads with plain loads.
+// skip (test hook): a TMA copy is not issued at all (no expected bytes either), so its wait gives up.
 __device__ __forceinline__ bool bulk256_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* x,
-                                             uint64_t* bar, uint32_t* armed) {
+                                             uint64_t* bar, uint32_t* armed, bool skip) {
   constexpr int D = 256;
   const int tid = threadIdx.x;
   if (pg * kPage >= L) {
-    if (tid == 0) {
+    if (tid == 0 && !skip) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       mbar_expect_tx(bar, 8u * 16384u);
       ++*armed;
@@ -146,8 +147,8 @@ __device__ __forceinline__ void bulk256_s_chunk(uint8_t* dst, const uint8_t* s_s
 // Per-barrier parity bits of the next waits, and the bounded wait that counts completions in done[].
 struct Phases {
   uint32_t bits = 0;
-  __device__ __forceinline__ bool wait(uint64_t* bars, int i, uint32_t* done) {
-    if (!mbar_wait(bars + i, (bits >> i) & 1u)) return false;
+  __device__ __forceinline__ bool wait(uint64_t* bars, int i, uint32_t* done, uint32_t polls = kWaitPolls) {
+    if (!mbar_wait(bars + i, (bits >> i) & 1u, polls)) return false;
     ++done[i];
     bits ^= 1u << i;
     return true;
@@ -543,7 +544,9 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
   int b, h, slot, L, Np, pg;
   RowTask rc;  // this thread's cached row lookup
   int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
-  bool tma = cur < ntasks && bulk256_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, x, bars + kB2Ld, armed + kB2Ld);
+  bool ld_skipped = cur == a.fault_task;  // the wait-timeout test hook: this page's copy is not issued
+  bool tma = cur < ntasks && bulk256_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, x, bars + kB2Ld, armed + kB2Ld,
+                                          ld_skipped);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
   __syncthreads();  // every plain-copied row is in X before thread 0 issues the rotation
   bool ok = true;
@@ -557,7 +560,8 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
     uint8_t* page = page_addr(lv, slot, h, pg);
     // ---- rotation of the page in X, once its copy and the tables have landed ----
     if (tid == 0) {
-      const bool landed = ph.wait(bars, kB2Tab, done) && (!tma || ph.wait(bars, kB2Ld, done));
+      const bool landed =
+          ph.wait(bars, kB2Tab, done) && (!tma || ph.wait(bars, kB2Ld, done, ld_skipped ? a.fault_polls : kWaitPolls));
       if (landed) bulk256_rotate(tmem, x_addr, hd_addr, bars + kB2Rot, armed + kB2Rot);
       else ok = false;
     }
@@ -607,7 +611,8 @@ __global__ void __launch_bounds__(kQ2Threads, 1)
     if (!ok) break;
     tc_fence_after();
     // ---- the next page's copy (X is free: the projection has completed), then the signs ----
-    tma = nxt < ntasks && bulk256_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, x, bars + kB2Ld, armed + kB2Ld);
+    ld_skipped = nxt == a.fault_task;
+    tma = nxt < ntasks && bulk256_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, x, bars + kB2Ld, armed + kB2Ld, ld_skipped);
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     bulk256_signs<KB>(tmem, warp, lane, sb, page, wr, pl);
     tc_fence_before();

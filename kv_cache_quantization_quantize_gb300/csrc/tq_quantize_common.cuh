@@ -25,6 +25,11 @@ struct AppendArgs {
   int max_new;
   int flush;  // 1: quantise the current ring block (tq_ring_flush)
   int full;   // 1: full_tq mode (ring_size 0): every appended token is quantised by the append itself
+  // Wait-timeout test hook of the tcgen05 coders (tq_debug_append_wait_fault): the TMA copy of page task
+  // fault_task ((row * Hkv + head) * pages per row + page of the append) is not issued, nor its expected
+  // bytes, and the wait on it gives up after fault_polls polls. -1 in normal use.
+  int fault_task = -1;
+  uint32_t fault_polls = 0;
 };
 
 // Tensor map of k or v ([batch][max_new][Hkv][d] bf16) for the tcgen05 coders' page loads (tq_quantize.cu).

@@ -300,3 +300,15 @@ def test_codec_entry_points_validate_before_launching():
     assert lib.tq_bonsai1_quantize(a16, None, -1, 128, a16, a16, None, None, None) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_bonsai1_quantize(a16, a16, 0, 128, a16, a16, a16, a16, None) == _abi.TQ_OK
     assert lib.tq_bonsai1_dequantize(a16, a16, a16, a16, 4, 128, mis, None, None) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_debug_hooks_validate_their_arguments():
+    """The wait-timeout test hooks only set process-wide knobs: their argument checks run on the host."""
+    lib = _abi.load()
+    assert lib.tq_debug_append_wait_fault(-2, 8) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_append_wait_fault(0, 0) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_append_wait_fault(0, (1 << 22) + 1) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_append_wait_fault(5, 8) == _abi.TQ_OK
+    assert lib.tq_debug_append_wait_fault(-1, 0) == _abi.TQ_OK
+    assert lib.tq_debug_decode_wait_fault(4, 8) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_decode_wait_fault(-1, 0) == _abi.TQ_OK
