@@ -272,8 +272,8 @@ tq_status tq_decode_attention_noalloc(tq_ctx* ctx, int layer, const void* q, flo
  * Process-wide; set it only while no other thread launches decodes. */
 tq_status tq_debug_decode_wait_fault(int stage, int polls);
 
-/* Test hook for the bounded waits of the tcgen05 bulk coders (bf16 appends of >= 128 tokens at head_dim 128
- * and 256; not part of the append itself). task >= 0 makes every following such tq_quantize_append skip the
+/* Test hook for the bounded waits of the tcgen05 bulk coders (bf16 appends of >= 128 tokens at head_dim 64,
+ * 128 and 256; not part of the append itself). task >= 0 makes every following such tq_quantize_append skip the
  * TMA copy of page task `task`, numbered (row * n_kv_heads + head) * pages_per_row + j with
  * pages_per_row = ceil(max_new / 128) and j the j-th complete block the append codes for that row: the CTA
  * that owns the task issues neither the copy nor its expected-byte count, and its wait on it gives up after

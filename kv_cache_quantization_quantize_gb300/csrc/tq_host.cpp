@@ -231,9 +231,9 @@ TableOffsets table_offsets(int d) {
   o.St = align_up(o.S + 2ull * d * d, 256);
   o.cb = align_up(o.St + 2ull * d * d, 256);
   o.S_sw = align_up(o.cb + sizeof(float) * kCbFloats, 1024);
-  o.HD_sw = align_up(o.S_sw + (d >= 128 ? 2ull * d * d : 0), 1024);
+  o.HD_sw = align_up(o.S_sw + 2ull * d * d, 1024);
   // head_dim 256: H diag(D) for each 128-coordinate half of D (2 x 128 x 128)
-  o.S_frag = align_up(o.HD_sw + (d == 128 ? 2ull * d * d : d == 256 ? 2ull * 2 * 128 * 128 : 0), 256);
+  o.S_frag = align_up(o.HD_sw + (d <= 128 ? 2ull * d * d : 2ull * 2 * 128 * 128), 256);
   o.bytes = align_up(o.S_frag + 2ull * d * d, 256);
   return o;
 }
@@ -463,7 +463,7 @@ tq_status tq_init_codebooks(const tq_config* cfg, void* d_tables, size_t tables_
           std::memcpy(hd + (size_t)half * 32768 + tq::sw128_offset(i, j), &v, 2);
         }
   }
-  if (d == 128) {
+  if (d <= 128) {  // head_dim 64 and 128: one tile of d rows (one or two 64-column atoms)
     uint8_t* sw = host.data() + ctx->to.S_sw;
     for (int n = 0; n < d; ++n)
       for (int k = 0; k < d; ++k) std::memcpy(sw + tq::sw128_offset(n, k), &ctx->S[(size_t)n * d + k], 2);

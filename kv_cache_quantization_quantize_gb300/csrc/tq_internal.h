@@ -133,7 +133,7 @@ TQ_HD uint32_t sw128_offset(int n, int k) {
 
 // Device tables (inside the caller's d_tables buffer). S_sw is S (rows = projection index,
 // columns = coordinate) in the swizzled layout above; HD_sw is H diag(D) (entries +-1, bf16) in the
-// same layout; both present for head_dim 128. For head_dim 256, S_sw holds S with 256 rows (sw128_offset_rows
+// same layout (head_dim 64 and 128: d rows, one or two 64-column atoms). For head_dim 256, S_sw holds S with 256 rows (sw128_offset_rows
 // with 256 rows: four 32 KB atoms of 64 columns) and HD_sw holds H diag(D1) and H diag(D2) (128 x 128
 // each) for the two halves of D, with H the 128-point Hadamard. S_frag is S in f16
 // as m16n8k16 A fragments (see sfrag_idx), for the decode kernels' query projection.
@@ -190,9 +190,9 @@ struct LayerView {
   const uint16_t* S;   // bf16 [d][d]
   const uint16_t* St;  // bf16 [d][d] transposed
   const float* cb;
-  const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 128 and 256)
+  const uint16_t* S_sw;  // S in the tcgen05 swizzled K-major layout (head_dim 64, 128 and 256)
   const uint4* S_frag;   // S in f16 m16n8k16 A fragments (sfrag_idx)
-  const uint16_t* HD_sw;  // H diag(D) (head_dim 128; 256: H diag(D1), H diag(D2)) swizzled K-major
+  const uint16_t* HD_sw;  // H diag(D) (head_dim 64, 128; 256: H diag(D1), H diag(D2)) swizzled K-major
   uint8_t* pages;      // this layer: [slot][head][page][page_bytes], or paged: [block][head][page_bytes]
   const int32_t* btab; // paged cache: block table [slot][max_pages] (all layers); nullptr: contiguous
   int n_blocks;        // paged cache: blocks per layer

@@ -1,8 +1,8 @@
 // Quantize-on-append ([Guide] §二, five-step pipeline). Two paths write packed pages (128 tokens of
 // one KV head):
-//   - CUDA-core kernels (four 32-token CTAs per page) for ring flushes, decode-sized appends, f32
-//     inputs and head_dim 64; their QJL projection z = S r is an f16 mma.sync GEMM per block;
-//   - persistent tcgen05 kernels for bulk bf16 appends at head_dim 128 (below) and 256
+//   - CUDA-core kernels (four 32-token CTAs per page) for ring flushes, decode-sized appends and f32
+//     inputs; their QJL projection z = S r is an f16 mma.sync GEMM per block;
+//   - persistent tcgen05 kernels for bulk bf16 appends at head_dim 64 and 128 (below) and 256
 //     (tq_quantize256.cu), with the rotation and the projection on the tensor cores.
 #include <algorithm>
 #include <atomic>
@@ -247,62 +247,73 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
 }
 
 // =============================================================================================
-// Bulk quantise (head_dim 128) on tcgen05 tensor cores. One persistent CTA per SM walks its pages:
+// Bulk quantise (head_dim 64 and 128) on tcgen05 tensor cores. One persistent CTA per SM walks its pages:
 //   - The bf16 K and V rows of the next page stream into shared memory (cp.async, 128-byte swizzled
 //     K-major tiles) while the current page is coded.
-//   - Rotation: y' = (H diag(D)) x for all 128 tokens of K and of V as two M = N = 128, K = 128 MMAs
+//   - Rotation: y' = (H diag(D)) x for all 128 tokens of K and of V as two M = 128, N = K = D MMAs
 //     (the +-1 entries are exact in bf16, products are exact, fp32 accumulation) into TMEM.
 //   - Warps 0-7 code the keys, two threads per token row, from TMEM: norm, Lloyd-Max index,
 //     residual, bf16 hi + lo split of the residual (written over the consumed K tile); then thread 0
-//     issues the QJL projection z = S r as 16 more MMAs (|r - hi - lo| <= 2^-18 |r|).
+//     issues the QJL projection z = S r as 2 D / 16 more MMAs (|r - hi - lo| <= 2^-18 |r|).
 //   - Warps 8-15 code the values the same way (groups of 32, fp16 scale, mid-rise codes) and then
 //     take the signs of z, so the key warps need not wait for the projection.
 //   - Key words, norms and value scales go to the page straight from registers; value codes are
 //     staged in shared memory for the fragment-major value layout.
 // =============================================================================================
 constexpr int kTcThreads = 512;  // warps 0-7 keys, 8-15 values; two warps (column halves) per token row
-constexpr uint32_t kQbHD = 0, kQbS = 32768, kQbBuf = 65536;  // 2 x [K tile 32 KB | V tile 32 KB]
-constexpr uint32_t kQbVcode = kQbBuf + 2 * 65536;             // [128][128] u8 value codes
-constexpr uint32_t kQbX = kQbVcode + 16384;                   // half-row exchange (see below)
-// mbarriers [8] (slot 6 holds the TMEM address), then the arming and completion counts of each barrier
-// ([8] + [8] u32, see bulk_drain)
-constexpr uint32_t kQbBar = kQbX + 2048 + 6144 + 2048, kQbEnd = kQbBar + 128;
-constexpr size_t kTcSmem = kQbEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+// Shared memory of the head_dim-D coder (D = 64 or 128), byte offsets: H diag(D) and S (2 D^2 each), two page
+// buffers [K tile | V tile] of 128 x D bf16 each, the value codes [128][D] u8, the half-row exchange, and
+// the mbarriers [8] (slot 6 holds the TMEM address) with the arming and completion counts of each barrier
+// ([8] + [8] u32, see bulk_drain).
+template <int D> struct QbLayout {
+  static constexpr uint32_t kTile = 128u * D * 2;  // one 128 x D bf16 tile
+  static constexpr uint32_t kBufBytes = 2 * kTile;
+  static constexpr uint32_t kHD = 0, kS = 2u * D * D, kBuf = 4u * D * D;
+  static constexpr uint32_t kVcode = kBuf + 2 * kBufBytes;
+  static constexpr uint32_t kX = kVcode + 128u * D;
+  static constexpr uint32_t kBar = kX + 2048 + 6144 + 2048, kEnd = kBar + 128;
+  static constexpr size_t kSmem = kEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
+};
+static_assert(QbLayout<128>::kSmem == 224384 && QbLayout<64>::kBuf % 1024 == 0, "layouts");
+// Chunk swizzle of the value-code staging rows (16-byte chunk c of row t at chunk c ^ vsw(t)): conflict-free
+// row writes for 128-byte rows (D = 128) and for 64-byte rows (D = 64, two rows per 128 bytes).
+template <int D> __device__ __forceinline__ int vsw(int t) { return D == 128 ? (t & 7) : ((t >> 1) & 3); }
 
-// Loads page pg's K and V rows (bf16) into buffer `buf` (K tile at 0, V tile at 32 KB; each two
-// 16 KB swizzle atoms of 64 coordinates). Pages made of new input only are fetched by four TMA tensor
-// copies (tensor [batch][max_new][Hkv][128], box 64 x 1 x 128 x 1, 128-byte swizzle) that complete on
+// Loads page pg's K and V rows (bf16) into buffer `buf` (K tile at 0, V tile at 128 D 2 bytes; each D / 64
+// 16 KB swizzle atoms of 64 coordinates). Pages made of new input only are fetched by 2 D / 64 TMA tensor
+// copies (tensor [batch][max_new][Hkv][D], box 64 x 1 x 128 x 1, 128-byte swizzle) that complete on
 // `bar`; returns true then. Pages that start in the ring are copied with plain loads and stores by
 // all threads (at most one page per row and append).
 // The copy is made by the nthr threads whose index relative to `first` is in [0, nthr).
 // `armed` counts the copies armed on `bar` (see bulk_drain). skip (test hook): a TMA copy is not issued
 // at all (no expected bytes either), so its wait gives up.
-__device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
+template <int D>
+__device__ __forceinline__ bool bulk_tc_load(const AppendArgs& a, const CUtensorMap* tmk, const CUtensorMap* tmv,
                                              int b, int h, int slot, int L, int Np, int pg, uint8_t* buf,
                                              uint64_t* bar, uint32_t* armed, int first, int nthr, bool skip = false) {
-  constexpr int D = 128;
+  constexpr int NB = D / 64;  // boxes (64-coordinate atoms) per tile
   const int rel = (int)threadIdx.x - first;
   if (rel < 0 || rel >= nthr) return pg * kPage >= L;
   if (pg * kPage >= L) {
     if (rel == 0 && !skip) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_expect_tx(bar, 4u * 16384u);
+      mbar_expect_tx(bar, 2u * NB * 16384u);
       ++*armed;
       const int z = pg * kPage - L;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const CUtensorMap* m = i < 2 ? tmk : tmv;
+      for (int i = 0; i < 2 * NB; ++i) {
+        const CUtensorMap* m = i < NB ? tmk : tmv;
         asm volatile(
             "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], [%6];\n" ::"r"(
                 smem_u32(buf + i * 16384)),
-            "l"(reinterpret_cast<uint64_t>(m)), "r"(64 * (i & 1)), "r"(h), "r"(z), "r"(b), "r"(smem_u32(bar))
+            "l"(reinterpret_cast<uint64_t>(m)), "r"(64 * (i % NB)), "r"(h), "r"(z), "r"(b), "r"(smem_u32(bar))
             : "memory");
       }
     }
     return true;
   }
   for (int q = rel; q < 2 * kPage * (D / 8); q += nthr) {
-    const int which = q >> 11, t = (q >> 4) & 127, c = q & 15;
+    const int which = q / (kPage * (D / 8)), t = (q / (D / 8)) % kPage, c = q % (D / 8);
     const int pos = pg * kPage + t;
     const uint16_t* src;
     if (pos < L) {
@@ -310,39 +321,49 @@ __device__ __forceinline__ bool bulk128_load(const AppendArgs& a, const CUtensor
     } else {
       src = static_cast<const uint16_t*>(which ? a.v : a.k) + (((size_t)b * a.max_new + (pos - L)) * a.lv.Hkv + h) * D;
     }
-    *reinterpret_cast<uint4*>(buf + which * 32768u + sw128_offset(t, 8 * c)) = *reinterpret_cast<const uint4*>(src + 8 * c);
+    *reinterpret_cast<uint4*>(buf + which * QbLayout<D>::kTile + sw128_offset(t, 8 * c)) =
+        *reinterpret_cast<const uint4*>(src + 8 * c);
   }
   return false;
 }
 
+// kind::f16 instruction descriptor, bf16 operands, f32 accumulator, M = 128, N = D.
+template <int D>
+constexpr uint32_t kIdescBf16M128 = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(D >> 3) << 17) | ((128u >> 4) << 24);
+
 // Rotation of the K and V tiles of one page (buffer at smem address buf) by the tensor cores:
-// D[t][i] = sum_j x[t][j] (H D)[i][j], K into TMEM columns [0, 128) of `tcol`, V into [128, 256).
-__device__ __forceinline__ void bulk128_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar,
+// D[t][i] = sum_j x[t][j] (H D)[i][j], K into TMEM columns [0, D) of `tcol`, V into [D, 2 D).
+template <int D>
+__device__ __forceinline__ void bulk_tc_rotate(uint32_t tcol, uint32_t buf, uint32_t hd_addr, uint64_t* bar,
                                                uint32_t* armed) {
   tc_fence_after();
   const uint32_t xa = umma_desc_sw128_lo(buf), hb = umma_desc_sw128_lo(hd_addr);
 #pragma unroll
-  for (int part = 0; part < 2; ++part)  // K, then V (+32 KB = 2048 descriptor units)
+  for (int part = 0; part < 2; ++part)  // K, then V (+one tile = 16 D descriptor units)
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < D / 16; ++ks) {
       const uint32_t koff = (ks >> 2) * 1024u + (ks & 3) * 2u;  // atom 16 KB, k step 32 B, in 16-byte units
-      umma_bf16_lo(tcol + 128u * part, xa + part * 2048u + koff, hb + koff, kIdescBf16M128N128, ks > 0);
+      umma_bf16_lo(tcol + (uint32_t)D * part, xa + part * (16u * D) + koff, hb + koff, kIdescBf16M128<D>, ks > 0);
     }
   umma_commit(bar);
   ++*armed;
 }
 
-// KB = key bits: 3 (2-bit Lloyd-Max index + sign) or 4 (3-bit index + sign, served with 4-bit values).
-template <int KB>
+// D = head_dim (64 or 128). KB = key bits: 3 (2-bit Lloyd-Max index + sign) or 4 (3-bit index + sign,
+// served with 4-bit values).
+template <int D, int KB>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    k_quantize_bulk128(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AppendArgs a,
+    k_quantize_bulk_tc(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AppendArgs a,
                        int pages_per_row, int batch) {
-  constexpr int D = 128;
-  constexpr int MB = KB - 1;  // index bits = index planes
+  using Lq = QbLayout<D>;
+  constexpr int MB = KB - 1;        // index bits = index planes
+  constexpr int HC = D / 2;         // coordinates (TMEM columns) of one thread: a column half of its token row
+  constexpr int PS = D / 16;        // bit positions between the two column halves' coordinates in a key word
+  constexpr uint32_t TH = 2u * D;   // TMEM columns of one page half: [rotated K (then z = S r) | rotated V]
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* vcode = sm + kQbVcode;
-  uint64_t* bar_tab = reinterpret_cast<uint64_t*>(sm + kQbBar);
+  uint8_t* vcode = sm + Lq::kVcode;
+  uint64_t* bar_tab = reinterpret_cast<uint64_t*>(sm + Lq::kBar);
   // QJL projections of pages in buffers 0 / 1: two barriers, so that a projection can never complete
   // twice before the value warps wait for it
   auto bar_qjl2 = [bar_tab](uint32_t i) { return i ? bar_tab + 7 : bar_tab + 1; };
@@ -366,11 +387,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(bar_tab, 4u * D * D);
     armed[0] = 1u;
-    bulk_g2s(sm + kQbHD, lv.HD_sw, 2u * D * D, bar_tab);
-    bulk_g2s(sm + kQbS, lv.S_sw, 2u * D * D, bar_tab);
+    bulk_g2s(sm + Lq::kHD, lv.HD_sw, 2u * D * D, bar_tab);
+    bulk_g2s(sm + Lq::kS, lv.S_sw, 2u * D * D, bar_tab);
   }
-  if (warp == 0) {  // 512 TMEM columns: two halves of [rotated K (then z = S r) | rotated V], by page parity
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot))
+  if (warp == 0) {  // 4 D TMEM columns: two halves of [rotated K (then z = S r) | rotated V], by page parity
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_u32(tslot)),
+                 "n"(4 * D)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
@@ -378,15 +400,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tslot;
-  const uint32_t hd_addr = smem_u32(sm + kQbHD), s_addr = smem_u32(sm + kQbS), buf0 = smem_u32(sm + kQbBuf);
+  const uint32_t hd_addr = smem_u32(sm + Lq::kHD), s_addr = smem_u32(sm + Lq::kS), buf0 = smem_u32(sm + Lq::kBuf);
   const int ntasks = batch * lv.Hkv * pages_per_row;
   int b, h, slot, L, Np, pg;
   RowTask rc;  // this thread's cached row lookup
   int cur = bulk_next(a, blockIdx.x, ntasks, pages_per_row, rc, b, h, slot, L, Np, pg);
   __syncthreads();  // barriers initialised
   bool ld_skipped = cur == a.fault_task;  // the wait-timeout test hook: this page's copy is not issued
-  bool tma_cur = cur < ntasks && bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf, bar_ld, armed + 2, 0,
-                                              kTcThreads, ld_skipped);
+  bool tma_cur = cur < ntasks && bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf, bar_ld, armed + 2,
+                                                 0, kTcThreads, ld_skipped);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   const bool tab_ok = mbar_wait(bar_tab, 0);
   if (tid == 0 && tab_ok) ++done[0];
@@ -406,7 +428,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (mbar_wait(bar_ld, 0, ld_skipped ? a.fault_polls : kWaitPolls)) ++done[2];
       else ok = false;
     }
-    if (ok) bulk128_rotate(tmem, smem_u32(sm + kQbBuf), smem_u32(sm + kQbHD), bar_rot, armed + 4);
+    if (ok) bulk_tc_rotate<D>(tmem, smem_u32(sm + Lq::kBuf), smem_u32(sm + Lq::kHD), bar_rot, armed + 4);
   }
   if (tma_cur) ph_ld ^= 1u;
   ok = __syncthreads_and(ok) != 0;
@@ -415,11 +437,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const bool kpath = warp < 8;
   const int pw = warp & 7, q4 = pw & 3, half = pw >> 2;
   const int t = 32 * q4 + lane;
-  float* xs = reinterpret_cast<float*>(sm + kQbX);                  // [2 halves][128] partial |y'|^2
-  float* xr = xs + 256;                                             // [2][128] partial |r|^2
-  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + kQbX + 2048);     // [4 MB][128] half-1 index words
-  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + kQbX + 8192);     // [4][128] half-1 sign words
+  float* xs = reinterpret_cast<float*>(sm + Lq::kX);                  // [2 halves][128] partial |y'|^2
+  float* xr = xs + 256;                                               // [2][128] partial |r|^2
+  uint32_t* xw = reinterpret_cast<uint32_t*>(sm + Lq::kX + 2048);     // [4 MB][128] half-1 index words
+  uint32_t* xg = reinterpret_cast<uint32_t*>(sm + Lq::kX + 8192);     // [4][128] half-1 sign words
   const PageLayout pl = page_layout(D, lv.vb, KB);
+  // Writes key word cw of plane p for token t (column-half-0 threads, every lane of the warp), from both
+  // column halves' bits (kbit_loc): at head_dim 128 one word per (token, plane, c); at head_dim 64 a word also
+  // holds the odd 16-token tile of the token's 32-token group 8 bit positions up (lane ^ 16).
+  auto put_word = [&](uint8_t* page, int p, int cw, uint32_t w) {
+    uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+    const int g = t & 7, r = (t >> 3) & 1;
+    if constexpr (D == 128) {
+      if (page) kw[(((t >> 4) * KB + p) * 32 + 4 * g + cw) * 2 + r] = w;
+    } else {
+      const uint32_t wo = __shfl_xor_sync(0xffffffffu, w, 16);
+      if (page && ((t >> 4) & 1) == 0) kw[(((t >> 5) * KB + p) * 32 + 4 * g + cw) * 2 + r] = w | (wo << 8);
+    }
+  };
   uint8_t* prev_page = nullptr;  // page whose QJL signs are still to be written (its MMAs are in flight)
   bool prev = false;
   // Wait for the projection of the page in TMEM half `hb` (value warps); false if the wait gave up.
@@ -433,12 +468,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // sign plane.
   auto qjl_signs = [&](uint32_t hb, uint8_t* page) {
     tc_fence_after();
-    const uint32_t prow = tmem + 256u * hb + ((uint32_t)(32 * q4) << 16);
+    const uint32_t prow = tmem + TH * hb + ((uint32_t)(32 * q4) << 16);
     uint32_t wsg[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-    for (int cc = 0; cc < 2; ++cc) {
+    for (int cc = 0; cc < HC / 32; ++cc) {
       uint32_t z[32];
-      tmem_ld32(prow + 64 * half + 32 * cc, z);
+      tmem_ld32(prow + HC * half + 32 * cc, z);
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int jl = 32 * cc + i;
@@ -448,15 +483,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (half) {
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) xg[cw * 128 + t] = wsg[cw] << 8;
+      for (int cw = 0; cw < 4; ++cw) xg[cw * 128 + t] = wsg[cw] << PS;
     }
     tc_fence_before();
     named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
-    if (!half && page) {
-      uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-      const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
+    if (!half) {
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[cw * 128 + t];
+      for (int cw = 0; cw < 4; ++cw) put_word(page, MB, cw, wsg[cw] | xg[cw * 128 + t]);
     }
   };
   while (ok && cur < ntasks) {
@@ -471,15 +504,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint8_t* page = page_addr(lv, cslot, chead, cpg);
     const bool wr = page != nullptr;  // paged cache without a block for this page: code it, write nothing
     if (!wr && tid == 0) set_status(lv.status, TQ_DEV_ERR_BLOCK);
-    const uint32_t lrow = tmem + 256u * bufi + ((uint32_t)(32 * q4) << 16);
+    const uint32_t lrow = tmem + TH * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
     if (kpath) {
-      // ---- keys, two threads per token (64 coordinates each): |y'|, y = y' / |y'|, index, residual ----
+      // ---- keys, two threads per token (D / 2 coordinates each): |y'|, y = y' / |y'|, index, residual ----
       float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < HC / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld32(lrow + 64 * half + 32 * cc, v);
+        tmem_ld32(lrow + HC * half + 32 * cc, v);
 #pragma unroll
         for (int i = 0; i < 32; ++i) ss4[i & 3] = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss4[i & 3]);
       }
@@ -501,9 +534,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int p = 0; p < MB; ++p) wix[p][0] = wix[p][1] = wix[p][2] = wix[p][3] = 0u;
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
+      for (int cc = 0; cc < HC / 32; ++cc) {
         uint32_t v[32];
-        tmem_ld32(lrow + 64 * half + 32 * cc, v);
+        tmem_ld32(lrow + HC * half + 32 * cc, v);
 #pragma unroll
         for (int oc = 0; oc < 4; ++oc) {  // 8 coordinates = one 16-byte chunk of the A rows
           uint32_t hi[4], lo[4];
@@ -512,7 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float res2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate 64 half + jl
+              const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate HC half + jl
               const float vv = __uint_as_float(v[i]);
               // index = #{boundaries below y}, by binary search over the sorted (scaled) boundaries
               bool ib[MB];
@@ -531,8 +564,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float res = fmaf(vv, scale, ncv);
               rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
               res2[e] = res;
-              // bit of coordinate j = 64 half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
-              // 64 half adds 8 to 2 (j >> 4)
+              // bit of coordinate j = HC half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
+              // HC half adds PS = D / 16 to 2 (j >> 4)
               const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
 #pragma unroll
               for (int p = 0; p < MB; ++p) wix[p][cw] |= ib[p] ? (1u << bit) : 0u;
@@ -543,9 +576,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             hi[e2] = *reinterpret_cast<const uint32_t*>(&h2);
             lo[e2] = *reinterpret_cast<const uint32_t*>(&l2);
           }
-          const uint32_t off = sw128_offset(t, 64 * half + 32 * cc + 8 * oc);
-          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm + kQbBuf + bufi * 65536u + 32768 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          const uint32_t off = sw128_offset(t, HC * half + 32 * cc + 8 * oc);
+          *reinterpret_cast<uint4*>(sm + Lq::kBuf + bufi * Lq::kBufBytes + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + Lq::kBuf + bufi * Lq::kBufBytes + Lq::kTile + off) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       xr[half * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
@@ -553,36 +587,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int p = 0; p < MB; ++p)
 #pragma unroll
-          for (int cw = 0; cw < 4; ++cw) xw[(4 * p + cw) * 128 + t] = wix[p][cw] << 8;  // the upper 64 coordinates sit 8 bit positions higher
+          for (int cw = 0; cw < 4; ++cw) xw[(4 * p + cw) * 128 + t] = wix[p][cw] << PS;  // the upper half sits PS bit positions higher
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
       named_barrier(1, 256);
-      const uint32_t buf = buf0 + bufi * 65536u;
+      const uint32_t buf = buf0 + bufi * Lq::kBufBytes;
       if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
         tc_fence_after();
         const uint32_t ra = umma_desc_sw128_lo(buf), sa = umma_desc_sw128_lo(s_addr);
+        constexpr int KS = D / 16;  // k steps per product
 #pragma unroll
-        for (int ks = 0; ks < 16; ++ks) {  // hi (ks < 8), then lo (+32 KB); atoms of 16 KB, k steps of 32 B
-          const uint32_t koff = ((ks & 7) >> 2) * 1024u + (ks & 3) * 2u;
-          umma_bf16_lo(tmem + 256u * bufi, ra + koff + (ks >> 3) * 2048u, sa + koff, kIdescBf16M128N128, ks > 0);
+        for (int ks = 0; ks < 2 * KS; ++ks) {  // hi (ks < KS), then lo (+one tile); atoms of 16 KB, k steps of 32 B
+          const uint32_t koff = ((ks % KS) >> 2) * 1024u + (ks & 3) * 2u;
+          umma_bf16_lo(tmem + TH * bufi, ra + koff + (ks / KS) * (16u * D), sa + koff, kIdescBf16M128<D>, ks > 0);
         }
         umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
         ++armed[qjl_idx(bufi)];
       }
-      if (!half && wr) {  // planes 0-1, n and gamma of token t
-        const float n = nrot * rsqrtf((float)D);
-        const float rr = xr[t] + xr[128 + t];
-        const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
-        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
-        const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
-        reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
-            (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+      if (!half) {  // index planes, n and gamma of token t
+        if (wr) {
+          const float n = nrot * rsqrtf((float)D);
+          const float rr = xr[t] + xr[128 + t];
+          const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
+          reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
+              (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
+        }
 #pragma unroll
         for (int p = 0; p < MB; ++p)
 #pragma unroll
-          for (int cw = 0; cw < 4; ++cw)
-            kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[(4 * p + cw) * 128 + t];
+          for (int cw = 0; cw < 4; ++cw) put_word(page, p, cw, wix[p][cw] | xw[(4 * p + cw) * 128 + t]);
       }
     } else {
       // ---- the previous page's projection (it reads buffer bufi ^ 1); then the next page's copy starts
@@ -591,23 +625,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (prev) ok_p = qjl_wait(bufi ^ 1u);
       ld_skipped = nxt == a.fault_task;
       if (nxt_tma && ok_p)
-        bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u, bar_ld + (bufi ^ 1u),
-                     armed + 2 + (bufi ^ 1u), 256, 1, ld_skipped);
+        bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf + (bufi ^ 1u) * Lq::kBufBytes,
+                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 1, ld_skipped);
       if (prev) qjl_signs(bufi ^ 1u, prev_page);
       // a next page that starts in the ring is copied by all value threads (TMEM half bufi ^ 1 is free now)
       if (nxt < ntasks && !nxt_tma)
-        bulk128_load(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + kQbBuf + (bufi ^ 1u) * 65536u, bar_ld + (bufi ^ 1u),
-                     armed + 2 + (bufi ^ 1u), 256, 256);
+        bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf + (bufi ^ 1u) * Lq::kBufBytes,
+                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 256);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
-      // ---- values, two threads per token (groups 2 half, 2 half + 1): fp16 scale, mid-rise codes ----
+      // ---- values, two threads per token (the D / 64 groups of 32 of the column half): fp16 scale, mid-rise
+      // codes ----
       const int vhalf = 1 << (lv.vb - 1);
       const float inv_sqrt_d = rsqrtf((float)D);
       uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
 #pragma unroll 1
-      for (int gg = 0; gg < 2; ++gg) {
-        const int grp = 2 * half + gg;
+      for (int gg = 0; gg < D / 64; ++gg) {
+        const int grp = (D / 64) * half + gg;
         uint32_t v[32];
-        tmem_ld32(lrow + 128 + 32 * grp, v);
+        tmem_ld32(lrow + D + 32 * grp, v);
         float x[32], am4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
@@ -663,9 +698,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             cw[k] = w;
           }
         }
-        // vcode row t holds its 16-byte chunk k at chunk k ^ (t & 7) (conflict-free row writes)
-        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ (t & 7)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ (t & 7)) << 4)) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        // vcode row t holds its 16-byte chunk k at chunk k ^ vsw(t) (conflict-free row writes)
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp) ^ vsw<D>(t)) << 4)) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        *reinterpret_cast<uint4*>(vcode + t * D + (((2 * grp + 1) ^ vsw<D>(t)) << 4)) =
+            make_uint4(cw[4], cw[5], cw[6], cw[7]);
         if (wr) sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
       }
       tc_fence_before();
@@ -679,7 +715,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           else set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
         }
         if (landed)
-          bulk128_rotate(tmem + 256u * (bufi ^ 1u), buf0 + (bufi ^ 1u) * 65536u, hd_addr, bar_rot + (bufi ^ 1u),
+          bulk_tc_rotate<D>(tmem + TH * (bufi ^ 1u), buf0 + (bufi ^ 1u) * Lq::kBufBytes, hd_addr, bar_rot + (bufi ^ 1u),
                          armed + 4 + (bufi ^ 1u));
         else ok_p = false;
       }
@@ -699,7 +735,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
               for (int e = 0; e < 2; ++e) {
                 const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
-                word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
+                word |= (uint32_t)vcode[tt * D + ((mt ^ vsw<D>(tt)) << 4) + 8 * (rg & 1) + g] << (16 * e + 2 * vfield2(kap, rg));
               }
           if (wr) vw[w] = word;
         }
@@ -713,7 +749,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int tt = 32 * blk + 16 * kap + 8 * (rg >> 1) + 2 * c + e;
-              word |= (uint32_t)vcode[tt * D + ((mt ^ (tt & 7)) << 4) + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
+              word |= (uint32_t)vcode[tt * D + ((mt ^ vsw<D>(tt)) << 4) + 8 * (rg & 1) + g] << (16 * e + 4 * vfield4(rg));
             }
           if (wr) vw[w] = word;
         }
@@ -740,7 +776,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0 && !bulk_drain(bar_tab, 8, 6, armed, done)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+  if (warp == 0)  // the 4 D columns allocated above
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "n"(4 * D) : "memory");
 }
 
 // Ring rows of a bulk append: the tokens past the last full page, [batch][pos][Hkv][K|V][d] items of
@@ -872,25 +909,29 @@ cudaError_t launch_append_small(const AppendArgs& a, int batch, cudaStream_t s) 
   return k4 ? launch_append_small_dk<256, 4>(a, batch, s) : launch_append_small_dk<256, 3>(a, batch, s);
 }
 
-template <int KB>
-cudaError_t launch_quantize_bulk128_k(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+template <int D, int KB>
+cudaError_t launch_quantize_bulk_tc_k(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+  constexpr size_t smem = QbLayout<D>::kSmem;
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk128<KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk_tc<D, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int ntasks = batch * a.lv.Hkv * pages;
   const int grid = std::max(1, std::min(ntasks, sms));
   CUtensorMap tmk, tmv;
-  cudaError_t e = bulk_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, 128, &tmk);
-  if (e == cudaSuccess) e = bulk_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, 128, &tmv);
+  cudaError_t e = bulk_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, D, &tmk);
+  if (e == cudaSuccess) e = bulk_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, D, &tmv);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_quantize_bulk128<KB>, dim3(grid), dim3(kTcThreads), kTcSmem, s, tmk, tmv, a, pages, batch);
+  return launch_pdl(k_quantize_bulk_tc<D, KB>, dim3(grid), dim3(kTcThreads), smem, s, tmk, tmv, a, pages, batch);
 }
-cudaError_t launch_quantize_bulk128(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
-  return a.lv.kb == 4 ? launch_quantize_bulk128_k<4>(a, batch, pages, sms, s)
-                      : launch_quantize_bulk128_k<3>(a, batch, pages, sms, s);
+// head_dim 64 or 128
+cudaError_t launch_quantize_bulk_tc(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+  const bool k4 = a.lv.kb == 4;
+  if (a.lv.d == 64)
+    return k4 ? launch_quantize_bulk_tc_k<64, 4>(a, batch, pages, sms, s) : launch_quantize_bulk_tc_k<64, 3>(a, batch, pages, sms, s);
+  return k4 ? launch_quantize_bulk_tc_k<128, 4>(a, batch, pages, sms, s) : launch_quantize_bulk_tc_k<128, 3>(a, batch, pages, sms, s);
 }
 
 }  // namespace
@@ -934,10 +975,10 @@ cudaError_t launch_append(const tq_ctx* ctx, int layer, const void* k, const voi
   a.fault_polls = (uint32_t)g_qfault_polls.load();
   if (max_new < kPage) return launch_append_small(a, batch, s);  // page on ring overflow + ring rows + state
   const int pages = (max_new + kPage - 1) / kPage;
-  // the tcgen05 bulk coders serve bf16 appends at head_dim 128 and 256 (key_bits 3 and 4); head_dim 64
-  // and f32 inputs use the CUDA-core coder
+  // the tcgen05 bulk coders serve bf16 appends at head_dim 64, 128 and 256 (key_bits 3 and 4); f32 inputs
+  // use the CUDA-core coder
   const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
-  cudaError_t e = (a.lv.d == 128 && dt == 0)   ? launch_quantize_bulk128(a, batch, pages, sms, s)
+  cudaError_t e = (a.lv.d <= 128 && dt == 0)   ? launch_quantize_bulk_tc(a, batch, pages, sms, s)
                   : (a.lv.d == 256 && dt == 0) ? launch_quantize_bulk256(a, batch, pages, sms, s)
                                                : launch_quantize(a, batch, pages, s);
   if (e != cudaSuccess) return e;

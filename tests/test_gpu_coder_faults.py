@@ -1,4 +1,4 @@
-"""Bounded waits of the tcgen05 bulk coders (head_dim 128 and 256), tested without a GPU fault.
+"""Bounded waits of the tcgen05 bulk coders (head_dim 64, 128 and 256), tested without a GPU fault.
 
 A host-set hook (tq_debug_append_wait_fault) makes one page task's TMA copy go unissued: no copy and no
 expected-byte count, so nothing can land later. The wait on it gives up after a few polls, and the owning
@@ -36,7 +36,7 @@ def _check_pages(cache, slot, h, k_all, v_all, tables, pages):
     check_value_records(vs, f64(v_all[tr, h]), D, cfg.value_bits)
 
 
-@pytest.mark.parametrize("d", [128, 256])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_bulk_coder_wait_timeout_is_reported_and_the_cache_stays_usable(d):
     lib = _abi.load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
