@@ -644,7 +644,7 @@ def bench_quantize(tqm, synth, dev, args, peak):
     return {"tok_s": T / (ms * 1e-3), "token_head_layers_per_s": T * Hkv * L_layers / (ms * 1e-3),
             "ms_per_pass": ms, "passes": reps, "clocks": sampler.summary(t0, t1), "workload": f"bulk prefill {T} bf16 tokens x {Hkv} KV heads x {L_layers} layers, d={d}, K{PREFILL['kb']}/V{vb}",
             "path": ("tcgen05 rotation (H diag(D)) and QJL projection (bf16 hi/lo) into TMEM, thread-per-token "
-                     "coding, TMA page loads" if d == 128 else
+                     "coding, TMA page loads" if d in (64, 128) else
                      "tcgen05 rotation (two 128-point H diag(D_i) products, butterfly on CUDA cores) and QJL "
                      "projection (bf16 hi/lo, S streamed in 32-row chunks) into TMEM, thread-per-token coding, "
                      "TMA page loads" if d == 256 else

@@ -487,7 +487,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     tc_fence_before();
     named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
-    if (!half) {
+    if constexpr (D == 128) {
+      if (!half && page) {
+        uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+        const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
+#pragma unroll
+        for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[cw * 128 + t];
+      }
+    } else if (!half) {
 #pragma unroll
       for (int cw = 0; cw < 4; ++cw) put_word(page, MB, cw, wsg[cw] | xg[cw * 128 + t]);
     }
@@ -605,7 +612,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         umma_commit(bar_qjl2(bufi));  // waited on by the value warps in the next iteration (or after the loop)
         ++armed[qjl_idx(bufi)];
       }
-      if (!half) {  // index planes, n and gamma of token t
+      if (D == 128 ? (!half && wr) : !half) {  // index planes, n and gamma of token t
         if (wr) {
           const float n = nrot * rsqrtf((float)D);
           const float rr = xr[t] + xr[128 + t];
@@ -613,10 +620,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
               (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
         }
+        if constexpr (D == 128) {
+          uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
+          const int tile = t >> 4, g = t & 7, r = (t >> 3) & 1;
 #pragma unroll
-        for (int p = 0; p < MB; ++p)
+          for (int p = 0; p < MB; ++p)
 #pragma unroll
-          for (int cw = 0; cw < 4; ++cw) put_word(page, p, cw, wix[p][cw] | xw[(4 * p + cw) * 128 + t]);
+            for (int cw = 0; cw < 4; ++cw)
+              kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[(4 * p + cw) * 128 + t];
+        } else {
+#pragma unroll
+          for (int p = 0; p < MB; ++p)
+#pragma unroll
+            for (int cw = 0; cw < 4; ++cw) put_word(page, p, cw, wix[p][cw] | xw[(4 * p + cw) * 128 + t]);
+        }
       }
     } else {
       // ---- the previous page's projection (it reads buffer bufi ^ 1); then the next page's copy starts
