@@ -141,8 +141,10 @@ tq_status tq_reset_seqs(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
  *     quantised from the f32 values.
  *   - A row that would exceed max_ctx is skipped and sets TQ_DEV_ERR_CAPACITY.
  *   - Launches: for max_new < 128, one kernel (the page of a block the append completes, the ring rows
- *     and the new length); otherwise one quantize kernel over the pages to write, then one ring-update
- *     kernel (in full_tq mode followed by the two launches of tq_ring_flush). */
+ *     and the new length); otherwise one quantize kernel over the pages to write (for bf16 tokens a
+ *     persistent tensor-core coder, one CTA per SM, at head_dim 64, 128 and 256; for f32 tokens four
+ *     CTAs per page), then the ring rows and the new lengths (two kernels; in full_tq mode followed by
+ *     the two launches of tq_ring_flush). */
 tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* v, tq_dtype dt,
                              const int32_t* d_seq_ids, const int32_t* d_n_new, int batch, int max_new,
                              tq_stream_t stream);
