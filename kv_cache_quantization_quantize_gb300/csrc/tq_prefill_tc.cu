@@ -106,13 +106,14 @@ __device__ __forceinline__ void pt_expand_plane(const uint32_t* kw, int p, int t
   }
 }
 
-// Issues 8 MMAs (K = 128) of an f16 A tile against an f16 B tile into TMEM column t_d.
+// Issues 8 MMAs (K = 128) of an f16 A tile against an f16 B tile into TMEM column t_d (descriptors stepped
+// by one add: atom 16 KB = 1024, k step 32 B = 2, in 16-byte units).
 __device__ __forceinline__ void pt_mma_k128(uint32_t t_d, uint32_t a_addr, uint32_t b_addr, bool accumulate_first) {
+  const uint32_t ad = umma_desc_sw128_lo(a_addr), bd = umma_desc_sw128_lo(b_addr);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    const uint32_t koff = (ks >> 2) * 16384 + (ks & 3) * 32;
-    umma_bf16(t_d, umma_desc_sw128(a_addr + koff), umma_desc_sw128(b_addr + koff), kIdescF16M128N128,
-              (accumulate_first || ks > 0) ? 1u : 0u);
+    const uint32_t koff = (ks >> 2) * 1024u + (ks & 3) * 2u;
+    umma_bf16_lo(t_d, ad + koff, bd + koff, kIdescF16M128N128, (accumulate_first || ks > 0) ? 1u : 0u);
   }
 }
 
