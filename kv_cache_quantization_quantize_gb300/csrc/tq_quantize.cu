@@ -260,7 +260,6 @@ __global__ void __launch_bounds__(kQThreads) k_append_small(AppendArgs a) {
 //   - Key words, norms and value scales go to the page straight from registers; value codes are
 //     staged in shared memory for the fragment-major value layout.
 // =============================================================================================
-constexpr int kTcThreads = 512;  // warps 0-7 keys, 8-15 values; two warps (column halves) per token row
 // Shared memory of the head_dim-D coder (D = 64 or 128), byte offsets: H diag(D) and S (2 D^2 each), two page
 // buffers [K tile | V tile] of 128 x D bf16 each, the value codes [128][D] u8, the half-row exchange, and
 // the mbarriers [8] (slot 6 holds the TMEM address) with the arming and completion counts of each barrier
@@ -275,6 +274,8 @@ template <int D> struct QbLayout {
   static constexpr size_t kSmem = kEnd + 1024;  // + alignment slack for the 1024-byte swizzle atoms
 };
 static_assert(QbLayout<128>::kSmem == 224384 && QbLayout<64>::kBuf % 1024 == 0, "layouts");
+// two head_dim-64 CTAs per SM: 2 x (dynamic + 1 KB reserved) within the 228 KB of an SM
+static_assert(2 * (QbLayout<64>::kSmem + 1024) <= 233472, "two CTAs per SM at head_dim 64");
 // Chunk swizzle of the value-code staging rows (16-byte chunk c of row t at chunk c ^ vsw(t)): conflict-free
 // row writes for 128-byte rows (D = 128) and for 64-byte rows (D = 64, two rows per 128 bytes).
 template <int D> __device__ __forceinline__ int vsw(int t) { return D == 128 ? (t & 7) : ((t >> 1) & 3); }
@@ -350,14 +351,18 @@ __device__ __forceinline__ void bulk_tc_rotate(uint32_t tcol, uint32_t buf, uint
 }
 
 // D = head_dim (64 or 128). KB = key bits: 3 (2-bit Lloyd-Max index + sign) or 4 (3-bit index + sign,
-// served with 4-bit values).
-template <int D, int KB>
-__global__ void __launch_bounds__(kTcThreads, 1)
+// served with 4-bit values). TPT = threads per token row and role: 2 (512 threads, each a column half; one
+// CTA per SM) or 1 (256 threads, each a whole row; at head_dim 64 two CTAs share an SM).
+template <int D, int KB, int TPT>
+__global__ void __launch_bounds__(256 * TPT, TPT == 1 ? 2 : 1)
     k_quantize_bulk_tc(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AppendArgs a,
                        int pages_per_row, int batch) {
   using Lq = QbLayout<D>;
+  constexpr int NT = 256 * TPT;     // threads: key warps, then value warps
+  constexpr int HT = 128 * TPT;     // threads of one role
+  constexpr int VL = HT;            // the value warps' leader (issues their copies and rotations, counts their waits)
   constexpr int MB = KB - 1;        // index bits = index planes
-  constexpr int HC = D / 2;         // coordinates (TMEM columns) of one thread: a column half of its token row
+  constexpr int HC = D / TPT;       // coordinates (TMEM columns) of one thread: its token row, or a column half
   constexpr int PS = D / 16;        // bit positions between the two column halves' coordinates in a key word
   constexpr uint32_t TH = 2u * D;   // TMEM columns of one page half: [rotated K (then z = S r) | rotated V]
   extern __shared__ uint8_t smem_raw[];
@@ -371,8 +376,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t* bar_rot = bar_tab + 4;  // [2]: rotations into TMEM half 0 / 1
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar_tab + 6);
   // phases armed on barrier i and seen complete by the thread that counts it: barrier 0 (tables) and the
-  // rotations by thread 0; the page loads by the thread that waits for them (0 for the first, 256
-  // after); the QJL projections by thread 256
+  // rotations by thread 0; the page loads by the thread that waits for them (0 for the first, the value
+  // leader after); the QJL projections by the value leader
   uint32_t* armed = reinterpret_cast<uint32_t*>(bar_tab + 8);
   uint32_t* done = armed + 8;
   auto qjl_idx = [](uint32_t i) { return i ? 7 : 1; };
@@ -408,7 +413,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();  // barriers initialised
   bool ld_skipped = cur == a.fault_task;  // the wait-timeout test hook: this page's copy is not issued
   bool tma_cur = cur < ntasks && bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf, bar_ld, armed + 2,
-                                                 0, kTcThreads, ld_skipped);
+                                                 0, NT, ld_skipped);
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   const bool tab_ok = mbar_wait(bar_tab, 0);
   if (tid == 0 && tab_ok) ++done[0];
@@ -432,10 +437,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (tma_cur) ph_ld ^= 1u;
   ok = __syncthreads_and(ok) != 0;
-  // warp roles: key path (warps 0-7) or value path (8-15); in each, warp w covers TMEM lane quarter
-  // w % 4 (tokens 32 (w % 4) + lane) and column half (w % 8) / 4
-  const bool kpath = warp < 8;
-  const int pw = warp & 7, q4 = pw & 3, half = pw >> 2;
+  // warp roles: key path (the first 4 TPT warps) or value path; in each, warp w covers TMEM lane quarter
+  // w % 4 (tokens 32 (w % 4) + lane) and, with two threads per row, column half (w % 8) / 4
+  const bool kpath = warp < 4 * TPT;
+  const int pw = warp % (4 * TPT), q4 = pw & 3, half = TPT == 2 ? (pw >> 2) : 0;
   const int t = 32 * q4 + lane;
   float* xs = reinterpret_cast<float*>(sm + Lq::kX);                  // [2 halves][128] partial |y'|^2
   float* xr = xs + 256;                                               // [2][128] partial |r|^2
@@ -460,7 +465,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // Wait for the projection of the page in TMEM half `hb` (value warps); false if the wait gave up.
   auto qjl_wait = [&](uint32_t hb) -> bool {
     const bool w_ok = mbar_wait(bar_qjl2(hb), (ph_qjl >> hb) & 1u);
-    if (tid == 256 && w_ok) ++done[qjl_idx(hb)];
+    if (tid == VL && w_ok) ++done[qjl_idx(hb)];
     ph_qjl ^= 1u << hb;
     return w_ok;
   };
@@ -486,17 +491,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int cw = 0; cw < 4; ++cw) xg[cw * 128 + t] = wsg[cw] << PS;
     }
     tc_fence_before();
-    named_barrier(2, 256);  // every value thread has read z (the half may be rotated into next)
+    named_barrier(2, HT);  // every value thread has read z (the half may be rotated into next)
     if constexpr (D == 128) {
       if (!half && page) {
         uint32_t* kw = reinterpret_cast<uint32_t*>(page + pl.kbits_off);
         const int ktile = t >> 4, kg = t & 7, kr = (t >> 3) & 1;
 #pragma unroll
-        for (int cw = 0; cw < 4; ++cw) kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | xg[cw * 128 + t];
+        for (int cw = 0; cw < 4; ++cw)
+          kw[((ktile * KB + MB) * 32 + 4 * kg + cw) * 2 + kr] = wsg[cw] | (TPT == 2 ? xg[cw * 128 + t] : 0u);
       }
     } else if (!half) {
 #pragma unroll
-      for (int cw = 0; cw < 4; ++cw) put_word(page, MB, cw, wsg[cw] | xg[cw * 128 + t]);
+      for (int cw = 0; cw < 4; ++cw) put_word(page, MB, cw, wsg[cw] | (TPT == 2 ? xg[cw * 128 + t] : 0u));
     }
   };
   while (ok && cur < ntasks) {
@@ -514,7 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint32_t lrow = tmem + TH * bufi + ((uint32_t)(32 * q4) << 16);
     bool ok_p = true;
     if (kpath) {
-      // ---- keys, two threads per token (D / 2 coordinates each): |y'|, y = y' / |y'|, index, residual ----
+      // ---- keys, TPT threads per token (HC coordinates each): |y'|, y = y' / |y'|, index, residual ----
       float ss4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int cc = 0; cc < HC / 32; ++cc) {
@@ -523,9 +529,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) ss4[i & 3] = fmaf(__uint_as_float(v[i]), __uint_as_float(v[i]), ss4[i & 3]);
       }
-      xs[half * 128 + t] = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
-      named_barrier(1, 256);
-      const float nrot = sqrtf(xs[t] + xs[128 + t]);  // = sqrt(d) |k|
+      const float ssum = (ss4[0] + ss4[1]) + (ss4[2] + ss4[3]);
+      float nrot;  // = sqrt(d) |k|
+      if constexpr (TPT == 2) {
+        xs[half * 128 + t] = ssum;
+        named_barrier(1, HT);
+        nrot = sqrtf(xs[t] + xs[128 + t]);
+      } else {
+        nrot = sqrtf(ssum);
+      }
       const float scale = nrot > 0.f ? 1.0f / nrot : 0.f;
       // The index of y = v / nrot (v = the rotated coordinate before normalisation) is decided as v > t nrot
       // for each boundary t (a zero vector compares v = 0 with t itself: y = 0), and the residual is
@@ -540,10 +552,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int p = 0; p < MB; ++p) wix[p][0] = wix[p][1] = wix[p][2] = wix[p][3] = 0u;
       float rr4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+      // a whole row of 3-bit indices is coded in a rolled loop over its 32-column chunks (the unrolled
+      // body outgrows the instruction cache); the chunk's bits are then 4 cc positions up
+      constexpr int KCU = (TPT == 1 && MB == 3) ? 1 : HC / 32;
+#pragma unroll KCU
       for (int cc = 0; cc < HC / 32; ++cc) {
         uint32_t v[32];
         tmem_ld32(lrow + HC * half + 32 * cc, v);
+        uint32_t cwx[MB][4];  // the rolled loop: this chunk's index bits
+#pragma unroll
+        for (int p = 0; p < MB; ++p) cwx[p][0] = cwx[p][1] = cwx[p][2] = cwx[p][3] = 0u;
+        (void)cwx;
 #pragma unroll
         for (int oc = 0; oc < 4; ++oc) {  // 8 coordinates = one 16-byte chunk of the A rows
           uint32_t hi[4], lo[4];
@@ -552,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             float res2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
-              const int i = 8 * oc + 2 * e2 + e, jl = 32 * cc + i;  // coordinate HC half + jl
+              const int i = 8 * oc + 2 * e2 + e;  // coordinate HC half + 32 cc + i
               const float vv = __uint_as_float(v[i]);
               // index = #{boundaries below y}, by binary search over the sorted (scaled) boundaries
               bool ib[MB];
@@ -571,11 +590,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
               const float res = fmaf(vv, scale, ncv);
               rr4[i & 3] = fmaf(res, res, rr4[i & 3]);
               res2[e] = res;
-              // bit of coordinate j = HC half + jl: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) + 16 (j & 1);
-              // HC half adds PS = D / 16 to 2 (j >> 4)
-              const int cw = (jl >> 1) & 3, bit = 2 * (jl >> 4) + ((jl >> 3) & 1) + 16 * (jl & 1);
+              // bit of coordinate j = HC half + 32 cc + i: word (j >> 1) & 3, bit 2 (j >> 4) + ((j >> 3) & 1) +
+              // 16 (j & 1); 32 cc adds 4 cc to it and HC half adds PS = D / 16
+              const int cw = (i >> 1) & 3, bit = 2 * (i >> 4) + ((i >> 3) & 1) + 16 * (i & 1);
+              if constexpr (KCU == 1) {
 #pragma unroll
-              for (int p = 0; p < MB; ++p) wix[p][cw] |= ib[p] ? (1u << bit) : 0u;
+                for (int p = 0; p < MB; ++p) cwx[p][cw] |= ib[p] ? (1u << bit) : 0u;
+              } else {
+#pragma unroll
+                for (int p = 0; p < MB; ++p) wix[p][cw] |= ib[p] ? (1u << (bit + 4 * cc)) : 0u;
+              }
             }
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(res2[0], res2[1]);
             const float2 hf2 = __bfloat1622float2(h2);
@@ -588,8 +612,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           *reinterpret_cast<uint4*>(sm + Lq::kBuf + bufi * Lq::kBufBytes + Lq::kTile + off) =
               make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+        if constexpr (KCU == 1) {
+#pragma unroll
+          for (int p = 0; p < MB; ++p)
+#pragma unroll
+            for (int cw = 0; cw < 4; ++cw) wix[p][cw] |= cwx[p][cw] << (4 * cc);
+        }
       }
-      xr[half * 128 + t] = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+      const float rsum = (rr4[0] + rr4[1]) + (rr4[2] + rr4[3]);
+      if constexpr (TPT == 2) xr[half * 128 + t] = rsum;
       if (half) {
 #pragma unroll
         for (int p = 0; p < MB; ++p)
@@ -598,7 +629,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
-      named_barrier(1, 256);
+      named_barrier(1, HT);
       const uint32_t buf = buf0 + bufi * Lq::kBufBytes;
       if (tid == 0) {  // QJL: z = S r on the tensor cores (A = r hi, then r lo) over the consumed K columns
         tc_fence_after();
@@ -615,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (D == 128 ? (!half && wr) : !half) {  // index planes, n and gamma of token t
         if (wr) {
           const float n = nrot * rsqrtf((float)D);
-          const float rr = xr[t] + xr[128 + t];
+          const float rr = TPT == 2 ? xr[t] + xr[128 + t] : rsum;
           const __half nh = __float2half_rn(fminf(n, 65504.f)), gh = __float2half_rn(sqrtf(rr));
           reinterpret_cast<uint32_t*>(page + pl.norms_off)[t] =
               (uint32_t)__half_as_ushort(nh) | ((uint32_t)__half_as_ushort(gh) << 16);
@@ -627,37 +658,38 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int p = 0; p < MB; ++p)
 #pragma unroll
             for (int cw = 0; cw < 4; ++cw)
-              kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | xw[(4 * p + cw) * 128 + t];
+              kw[((tile * KB + p) * 32 + 4 * g + cw) * 2 + r] = wix[p][cw] | (TPT == 2 ? xw[(4 * p + cw) * 128 + t] : 0u);
         } else {
 #pragma unroll
           for (int p = 0; p < MB; ++p)
 #pragma unroll
-            for (int cw = 0; cw < 4; ++cw) put_word(page, p, cw, wix[p][cw] | xw[(4 * p + cw) * 128 + t]);
+            for (int cw = 0; cw < 4; ++cw)
+              put_word(page, p, cw, wix[p][cw] | (TPT == 2 ? xw[(4 * p + cw) * 128 + t] : 0u));
         }
       }
     } else {
       // ---- the previous page's projection (it reads buffer bufi ^ 1); then the next page's copy starts
-      // there at once (a TMA copy, by thread 256), and the signs of the previous page are written ----
+      // there at once (a TMA copy, by the value leader), and the signs of the previous page are written ----
       const bool nxt_tma = nxt < ntasks && pg * kPage >= L;  // b..pg describe the next page here
       if (prev) ok_p = qjl_wait(bufi ^ 1u);
       ld_skipped = nxt == a.fault_task;
       if (nxt_tma && ok_p)
         bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf + (bufi ^ 1u) * Lq::kBufBytes,
-                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 1, ld_skipped);
+                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), VL, 1, ld_skipped);
       if (prev) qjl_signs(bufi ^ 1u, prev_page);
       // a next page that starts in the ring is copied by all value threads (TMEM half bufi ^ 1 is free now)
       if (nxt < ntasks && !nxt_tma)
         bulk_tc_load<D>(a, &tmk, &tmv, b, h, slot, L, Np, pg, sm + Lq::kBuf + (bufi ^ 1u) * Lq::kBufBytes,
-                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), 256, 256);
+                        bar_ld + (bufi ^ 1u), armed + 2 + (bufi ^ 1u), VL, HT);
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // plain-copied rows -> tensor cores
-      // ---- values, two threads per token (the D / 64 groups of 32 of the column half): fp16 scale, mid-rise
-      // codes ----
+      // ---- values, TPT threads per token (the D / (32 TPT) groups of 32 of its columns): fp16 scale,
+      // mid-rise codes ----
       const int vhalf = 1 << (lv.vb - 1);
       const float inv_sqrt_d = rsqrtf((float)D);
       uint16_t* sw = reinterpret_cast<uint16_t*>(page + pl.vscale_off);
 #pragma unroll 1
-      for (int gg = 0; gg < D / 64; ++gg) {
-        const int grp = (D / 64) * half + gg;
+      for (int gg = 0; gg < D / (32 * TPT); ++gg) {
+        const int grp = (D / (32 * TPT)) * half + gg;
         uint32_t v[32];
         tmem_ld32(lrow + D + 32 * grp, v);
         float x[32], am4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -722,8 +754,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (wr) sw[vscale_idx(D, t, grp)] = __half_as_ushort(sh);
       }
       tc_fence_before();
-      named_barrier(2, 256);  // value codes staged; V columns of this half read; next page's rows copied
-      if (tid == 256 && nxt < ntasks) {  // rotation of the next page into TMEM half bufi ^ 1
+      named_barrier(2, HT);  // value codes staged; V columns of this half read; next page's rows copied
+      if (tid == VL && nxt < ntasks) {  // rotation of the next page into TMEM half bufi ^ 1
         tc_fence_after();
         bool landed = true;
         if (nxt_tma) {
@@ -738,10 +770,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       if (nxt_tma) ph_ld ^= 1u << (bufi ^ 1u);
       // ---- pack the value codes (fragment-major layout) ----
-      const int vt = tid - 256;
+      const int vt = tid - VL;
       uint32_t* vw = reinterpret_cast<uint32_t*>(page + pl.vbits_off);
       if (lv.vb == 2) {
-        for (int w = vt; w < 4 * (D / 16) * 32; w += 256) {
+        for (int w = vt; w < 4 * (D / 16) * 32; w += HT) {
           const int ln = w & 31, mt = (w >> 5) % (D / 16), blk = w / (32 * (D / 16));
           const int g = ln >> 2, c = ln & 3;
           uint32_t word = 0;
@@ -757,7 +789,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (wr) vw[w] = word;
         }
       } else {
-        for (int w = vt; w < 4 * (D / 16) * 32 * 2; w += 256) {
+        for (int w = vt; w < 4 * (D / 16) * 32 * 2; w += HT) {
           const int kap = w & 1, ln = (w >> 1) & 31, mt = (w >> 6) % (D / 16), blk = w / (64 * (D / 16));
           const int g = ln >> 2, c = ln & 3;
           uint32_t word = 0;
@@ -785,7 +817,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (qjl_wait(bufi ^ 1u)) qjl_signs(bufi ^ 1u, prev_page);
     else ok = false;
   }
-  if (!ok && (tid == 0 || tid == 256)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+  if (!ok && (tid == 0 || tid == VL)) set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
   tc_fence_before();
   __syncthreads();  // every count is final
   // copies or MMAs still pending after a failed wait are waited for before shared memory and TMEM are
@@ -928,20 +960,27 @@ cudaError_t launch_append_small(const AppendArgs& a, int batch, cudaStream_t s) 
 
 template <int D, int KB>
 cudaError_t launch_quantize_bulk_tc_k(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {
+  // head_dim 64: a thread per token row and two CTAs per SM (101.5 KB of shared memory and 256 TMEM columns each)
+  constexpr int TPT = D == 64 ? 1 : 2;
   constexpr size_t smem = QbLayout<D>::kSmem;
   static bool attr_set = false;  // set once, outside any stream capture that follows
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(k_quantize_bulk_tc<D, KB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(k_quantize_bulk_tc<D, KB, TPT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    if (TPT == 1) {  // the whole shared-memory carve-out, so that two CTAs fit on an SM
+      e = cudaFuncSetAttribute(k_quantize_bulk_tc<D, KB, TPT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const int ntasks = batch * a.lv.Hkv * pages;
-  const int grid = std::max(1, std::min(ntasks, sms));
+  const int grid = std::max(1, std::min(ntasks, sms * (TPT == 1 ? 2 : 1)));
   CUtensorMap tmk, tmv;
   cudaError_t e = bulk_tensor_map(a.k, batch, a.max_new, a.lv.Hkv, D, &tmk);
   if (e == cudaSuccess) e = bulk_tensor_map(a.v, batch, a.max_new, a.lv.Hkv, D, &tmv);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_quantize_bulk_tc<D, KB>, dim3(grid), dim3(kTcThreads), smem, s, tmk, tmv, a, pages, batch);
+  return launch_pdl(k_quantize_bulk_tc<D, KB, TPT>, dim3(grid), dim3(256 * TPT), smem, s, tmk, tmv, a, pages, batch);
 }
 // head_dim 64 or 128
 cudaError_t launch_quantize_bulk_tc(const AppendArgs& a, int batch, int pages, int sms, cudaStream_t s) {

@@ -40,12 +40,13 @@ def _check_pages(cache, slot, h, k_all, v_all, tables, pages):
 def test_bulk_coder_wait_timeout_is_reported_and_the_cache_stays_usable(d):
     lib = _abi.load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ctas = sms * (2 if d == 64 else 1)  # persistent CTAs: two per SM at head_dim 64, else one
     Hkv, G, B = 8, 4, 2
-    npg = -(-(sms + 1) // (B * Hkv))  # complete pages per row: more page tasks than SMs
+    npg = -(-(ctas + 1) // (B * Hkv))  # complete pages per row: more page tasks than CTAs
     T = 128 * npg + 37                  # npg complete pages and a 37-token ring per row
     ppr = -(-T // 128)                  # page tasks per row as the append numbers them: ceil(max_new / 128)
     ntasks = B * Hkv * ppr
-    grid = min(ntasks, sms)             # one CTA per SM; CTA 0 owns tasks 0, grid, 2 grid, ...
+    grid = min(ntasks, ctas)            # CTA 0 owns tasks 0, grid, 2 grid, ...
     assert ntasks > grid
     cfg = config(head_dim=d, value_bits=2, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=B,
                  max_ctx=T + 128, seed=41)
