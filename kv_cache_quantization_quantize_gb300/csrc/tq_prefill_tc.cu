@@ -29,15 +29,21 @@
 namespace tq {
 namespace {
 
-constexpr int kPtThreads = 512;  // 16 warps: warp w covers TMEM lanes 32 (w % 4).. and column quarter w / 4
-constexpr int kPtQ = kPtThreads / 128;  // column quarters: 32 columns (and 32 coordinates of a row) per thread
-// shared memory (offsets from a 1024-byte aligned base): four A tiles, two B tiles, two page stages
-constexpr uint32_t kPtAhi = 0, kPtAlo = 32768, kPtAl = 65536, kPtAqp = 98304;
-constexpr uint32_t kPtBX = 131072, kPtBY = 163840, kPtStg = 196608;
-// after the stages: per-token logit factors [128], row exchange [4][128], block maximum [16], barriers [10]
-constexpr uint32_t kPtTail = 128 * 4 + 512 * 4 + 16 * 4 + 10 * 8;
-// barriers: S table, projection, page stages 0 / 1, MMA groups h, l, sigma, P.V
-enum { kBarTab = 0, kBarProj = 1, kBarPg = 2, kBarH = 4, kBarL = 5, kBarSg = 6, kBarO = 7, kNumBars = 8 };
+// 16 worker warps (warp w covers TMEM lanes 32 (w % 4).. and column quarter w / 4) and one more warp whose
+// lane 0 issues every MMA and polls the barriers
+constexpr int kPtWorkers = 512, kPtThreads = kPtWorkers + 32, kPtIssuer = kPtWorkers;
+constexpr int kPtQ = kPtWorkers / 128;  // column quarters: 32 columns (and 32 coordinates of a row) per thread
+// Shared memory (offsets from a 1024-byte aligned base): six 32 KB operand tiles that rotate through the
+// page pipeline (the h, l and QJL planes of the scores, V^T, and P over the h plane), two page stages, then
+// the per-token logit factors [2 pages][128], the per-warp operand maxima [16], the barriers and the TMEM
+// address.
+constexpr uint32_t kPtTileBytes = 32768, kPtSlots = 6, kPtStg = kPtSlots * kPtTileBytes;
+constexpr uint32_t kPtTail = 2 * 128 * 4 + 16 * 4 + 8 * 8 + 8;
+// barriers: S table, projection, page stages 0 / 1, score MMAs (QJL part), P.V MMAs, score MMAs (h and l part)
+enum { kBarTab = 0, kBarProj = 1, kBarPg = 2, kBarS = 4, kBarO = 5, kBarHL = 6, kNumBars = 7 };
+// TMEM (512 columns): scores S at 0, output O at 128, and from 256 the four f16 A tiles of the scores, 64
+// columns each: lambda a_h q_rot (f16 hi), its remainder, lambda a_l q_rot, lambda kappa S q_rot
+constexpr uint32_t kPtTmS = 0, kPtTmO = 128, kPtTmA = 256;
 
 struct PrefillTcArgs {
   LayerView lv;
@@ -53,6 +59,7 @@ struct PrefillTcArgs {
 __host__ __device__ constexpr size_t prefill_tc_smem(uint32_t page_bytes) {
   return 1024 + kPtStg + 2 * ((page_bytes + 127) / 128 * 128) + kPtTail;
 }
+static_assert(prefill_tc_smem(15872) <= 232448, "K3/V4 pages fit the operand tiles' pipeline");
 
 // Address of page pg of (slot, KV head h); a paged cache's page without a valid block reads block 0 and
 // is reported (TQ_DEV_ERR_BLOCK), as in the decode kernel.
@@ -63,14 +70,6 @@ __device__ __forceinline__ const uint8_t* pt_page(const LayerView& lv, int slot,
     p = lv.pages;
   }
   return p;
-}
-
-// One bounded mbarrier wait that every thread of the CTA agrees on. Thread 0 alone polls; the others
-// wait at the block barrier, which keeps 500 pollers off the shared-memory pipe that the tensor cores
-// read their operands through (the try_wait acquire of thread 0 and the barrier make the completed
-// copy or MMA results visible to every thread).
-__device__ __forceinline__ bool pt_wait_all(uint64_t* bar, uint32_t parity) {
-  return __syncthreads_and(threadIdx.x == 0 ? mbar_wait(bar, parity) : true) != 0;
 }
 
 // 2^x (the PTX approximate base-2 exponential; 2^-inf = 0).
@@ -106,14 +105,56 @@ __device__ __forceinline__ void pt_expand_plane(const uint32_t* kw, int p, int t
   }
 }
 
-// Issues 8 MMAs (K = 128) of an f16 A tile against an f16 B tile into TMEM column t_d (descriptors stepped
-// by one add: atom 16 KB = 1024, k step 32 B = 2, in 16-byte units).
+// The dequantised values of a page as the B tile of P.V: V^T[j][token] = s_g (code - offset) (f16), row j = tk,
+// tokens 32 hv .. 32 hv + 31 (4 chunks of 8).
+template <int VB>
+__device__ __forceinline__ void pt_expand_values(const uint8_t* page, const PageLayout& pl, int tk, int hv,
+                                                 __half2 voff2, uint8_t* tile) {
+  constexpr int D = 128;
+  const int j = tk;
+  const int mt = j >> 4, g8 = j & 7, rowhi = (j >> 3) & 1, grp = j >> 5;
+  const uint32_t* vw = reinterpret_cast<const uint32_t*>(page + pl.vbits_off);
+  const uint32_t* vsc = reinterpret_cast<const uint32_t*>(page + pl.vscale_off);  // [token pair][group] f16x2
+#pragma unroll
+  for (int mm = 0; mm < 4; ++mm) {
+    const int m = 4 * hv + mm, blk = m >> 2, kap = (m >> 1) & 1, hiT = m & 1, rr = rowhi + 2 * hiT;
+    uint32_t u4[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t x;
+      if (VB == 2) {
+        x = code_pair_512<2>(vw[(blk * (D / 16) + mt) * 32 + 4 * g8 + c], 2 * vfield2(kap, rr));
+      } else {
+        x = code_pair_512<4>(vw[((blk * (D / 16) + mt) * 32 + 4 * g8 + c) * 2 + kap], 4 * vfield4(rr));
+      }
+      const int t0 = 8 * m + 2 * c;  // the pair (t0, t0 + 1)
+      const uint32_t s2 = vsc[(t0 >> 1) * (D / 32) + grp];
+      const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&x), voff2),
+                                *reinterpret_cast<const __half2*>(&s2));
+      u4[c] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    *reinterpret_cast<uint4*>(tile + sw128_offset(j, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+  }
+}
+
+// Issues 8 MMAs (K = 128) of an f16 A tile against an f16 B tile, both in shared memory, into TMEM column t_d
+// (descriptors stepped by one add: atom 16 KB = 1024, k step 32 B = 2, in 16-byte units).
 __device__ __forceinline__ void pt_mma_k128(uint32_t t_d, uint32_t a_addr, uint32_t b_addr, bool accumulate_first) {
   const uint32_t ad = umma_desc_sw128_lo(a_addr), bd = umma_desc_sw128_lo(b_addr);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
     const uint32_t koff = (ks >> 2) * 1024u + (ks & 3) * 2u;
     umma_bf16_lo(t_d, ad + koff, bd + koff, kIdescF16M128N128, (accumulate_first || ks > 0) ? 1u : 0u);
+  }
+}
+
+// The same with the A tile in TMEM at column t_a (8 columns per K = 16 step).
+__device__ __forceinline__ void pt_mma_ts_k128(uint32_t t_d, uint32_t t_a, uint32_t b_addr, bool accumulate_first) {
+  const uint32_t bd = umma_desc_sw128_lo(b_addr);
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint32_t koff = (ks >> 2) * 1024u + (ks & 3) * 2u;
+    umma_ts_lo(t_d, t_a + 8u * ks, bd + koff, kIdescF16M128N128, (accumulate_first || ks > 0) ? 1u : 0u);
   }
 }
 
@@ -130,17 +171,18 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const PageLayout pl = page_layout(D, VB, KB);
   const uint32_t PB = pl.bytes, PBS = (pl.bytes + 127) / 128 * 128;
   uint8_t* stg = sm + kPtStg;
-  float* ns = reinterpret_cast<float*>(stg + 2 * PBS);  // [128] logit factor n_t scale log2e / lambda
-  float* xrow = ns + 128;                                 // [4][128] row maxima / sums of the four quarters
-  float* bmax = xrow + 512;                               // [16] per-warp operand maxima
+  float* ns = reinterpret_cast<float*>(stg + 2 * PBS);  // [2][128] logit factors n_t scale log2e / lambda, by page parity
+  float* bmax = ns + 256;                                 // [16] per-warp operand maxima
   uint64_t* bars = reinterpret_cast<uint64_t*>(bmax + 16);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
+  auto tile_at = [sm](int i) { return sm + i * kPtTileBytes; };
   // this thread's query row (TMEM lane) and column quarter: columns 32 ch .. 32 ch + 31
   const int r = 32 * (warp & 3) + lane, ch = warp >> 2;
   const int qi = r >> 2, g = r & 3, qidx = 32 * tile + qi;
   // expansion roles: token / coordinate tk = tid % 128 and quarter hv = tid / 128 (a warp's 32 threads write
   // 32 consecutive rows of a tile at the same chunk: conflict-free under the 128-byte swizzle)
   const int tk = tid & 127, hv = tid >> 7;
+  const bool worker = tid < kPtWorkers;
   pdl_wait();  // sequence state, pages and queries come from earlier work on the stream
   pdl_launch();
   const int slot = a.seq_ids[b], nq = a.n_q[b];
@@ -160,7 +202,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const int vis_r = vis(qidx);
   // pages below this warp's smallest causal extent need no mask
   const int vis_w = __reduce_min_sync(0xffffffffu, (unsigned)vis_r);
-  const bool row_out = qidx < a.qpr;  // a virtual row of the launch (padding rows get an empty partial)
+  const bool row_out = worker && qidx < a.qpr;  // a virtual row of the launch (padding rows get an empty partial)
   float* part = row_out ? reinterpret_cast<float*>(a.ws + a.plan.part_off +
                                                    ((((size_t)b * a.qpr + qidx) * lv.Hkv + h) * (S + 1) + split) *
                                                        a.plan.part_stride)
@@ -176,25 +218,27 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     return;
   }
 
-  // ---- setup: barriers, TMEM (256 columns: S at 0, O at 128), the S table for the projection ----
+  // ---- setup: barriers, TMEM (512 columns), the S table for the projection, the first two pages ----
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(&bars[kBarTab], 2u * D * D);
-    bulk_g2s(sm + kPtAl, lv.S_sw, 2u * D * D, &bars[kBarTab]);  // A_l's place until the projection is done
-    mbar_expect_tx(&bars[kBarPg], PB);                         // the first page
-    bulk_g2s(stg, pt_page(lv, slot, h, pg0), PB, &bars[kBarPg]);
+    bulk_g2s(tile_at(2), lv.S_sw, 2u * D * D, &bars[kBarTab]);
+    for (int k = 0; k < 2 && k < n; ++k) {
+      mbar_expect_tx(&bars[kBarPg + k], PB);
+      bulk_g2s(stg + k * PBS, pt_page(lv, slot, h, pg0 + k), PB, &bars[kBarPg + k]);
+    }
   }
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;\n" ::"r"(smem_u32(tslot))
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot))
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
   // ---- query rows: q_rot = Pi q (warp-per-row FWHT), bf16 hi / lo for the projection, fp32 copy ----
-  float* qr = reinterpret_cast<float*>(sm + kPtBX);  // [128][128] fp32 q_rot (the B tiles until the pages)
+  float* qr = reinterpret_cast<float*>(tile_at(4));  // [128][128] fp32 q_rot (tiles 4-5 until the first page)
   const float rs = rsqrtf((float)D);
   float amax = 0.f;
-  for (int rr = warp; rr < 128; rr += kPtThreads / 32) {
+  for (int rr = warp; rr < 128 && worker; rr += kPtWorkers / 32) {
     const int i = 32 * tile + (rr >> 2), gg = rr & 3;
     float x[4];
 #pragma unroll
@@ -220,256 +264,287 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
       hb[e2] = *reinterpret_cast<const uint32_t*>(&hi);
       lb[e2] = *reinterpret_cast<const uint32_t*>(&lo);
     }
-    *reinterpret_cast<uint2*>(sm + kPtAhi + sw128_offset(rr, 4 * lane)) = make_uint2(hb[0], hb[1]);
-    *reinterpret_cast<uint2*>(sm + kPtAlo + sw128_offset(rr, 4 * lane)) = make_uint2(lb[0], lb[1]);
+    *reinterpret_cast<uint2*>(tile_at(0) + sw128_offset(rr, 4 * lane)) = make_uint2(hb[0], hb[1]);
+    *reinterpret_cast<uint2*>(tile_at(1) + sw128_offset(rr, 4 * lane)) = make_uint2(lb[0], lb[1]);
   }
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot, t_s = tmem, t_o = tmem + 128;
+  const uint32_t tmem = *tslot, t_s = tmem + kPtTmS, t_o = tmem + kPtTmO, t_a = tmem + kPtTmA;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  const uint32_t a_hi = smem_u32(sm + kPtAhi), a_lo = smem_u32(sm + kPtAlo), a_l = smem_u32(sm + kPtAl),
-                 a_qp = smem_u32(sm + kPtAqp), b_x = smem_u32(sm + kPtBX), b_y = smem_u32(sm + kPtBY);
   // per barrier, kept alike by every thread: the parity of the next phase to wait for (bit i of par) and
   // the phases armed (a copy or an MMA batch that completes it) but not seen complete (2 bits i of pend),
-  // for the drain after a wait that gave up. Armed now: the S table and the first page.
-  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (1u << (2 * kBarPg));
+  // for the drain after a wait that gave up. Armed now: the S table and the first one or two pages.
+  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (1u << (2 * kBarPg)) | (n > 1 ? 1u << (2 * (kBarPg + 1)) : 0u);
   auto arm = [&](int i) { pend += 1u << (2 * i); };
-  auto wait_bar = [&](int i) {  // waits for the oldest armed phase of barrier i not seen yet
-    const bool w = pt_wait_all(&bars[i], (par >> i) & 1u);
+  // Waits (bounded) for the oldest armed phase not seen yet of barrier i and, if j >= 0, of barrier j. The
+  // issuing thread alone polls; the others wait at the block barrier, which keeps 500 pollers off the
+  // shared-memory pipe that the tensor cores read their operands through (the try_wait acquire of the
+  // poller and the barrier make the completed copy or MMA results visible to every thread). Every thread
+  // gets the same answer.
+  auto wait_bars = [&](int i, int j) {
+    bool w = true;
+    if (tid == kPtIssuer) {
+      if (i >= 0) w = mbar_wait(&bars[i], (par >> i) & 1u);
+      if (w && j >= 0) w = mbar_wait(&bars[j], (par >> j) & 1u);
+    }
+    w = __syncthreads_and(w) != 0;
     if (w) {
-      par ^= 1u << i;
-      pend -= 1u << (2 * i);
+      if (i >= 0) {
+        par ^= 1u << i;
+        pend -= 1u << (2 * i);
+      }
+      if (j >= 0) {
+        par ^= 1u << j;
+        pend -= 1u << (2 * j);
+      }
     }
     return w;
   };
-  bool ok = wait_bar(kBarTab);  // S table landed
+  bool ok = wait_bars(kBarTab, -1);  // S table landed
   if (ok) {  // projection q_proj = S q_rot into TMEM columns [0, 128): A = q_rot hi, lo (bf16)
-    if (tid == 0) {
+    if (tid == kPtIssuer) {
       tc_fence_after();
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks) {
         const uint32_t koff = ((ks & 7) >> 2) * 16384 + (ks & 3) * 32;
-        umma_bf16(t_s, umma_desc_sw128((ks < 8 ? a_hi : a_lo) + koff), umma_desc_sw128(a_l + koff),
-                  kIdescBf16M128N128, ks > 0);
+        umma_bf16(t_s, umma_desc_sw128(smem_u32(tile_at(ks < 8 ? 0 : 1)) + koff),
+                  umma_desc_sw128(smem_u32(tile_at(2)) + koff), kIdescBf16M128N128, ks > 0);
       }
       umma_commit(&bars[kBarProj]);
     }
     arm(kBarProj);
-    ok = wait_bar(kBarProj);
+    ok = wait_bars(kBarProj, -1);
   }
   tc_fence_after();
   // operand scale lambda: the largest of |a_h q_rot|, |a_l q_rot| and |kappa q_proj| maps to [2^12, 2^13)
   const float w_h = lv.cb[kCbW + 0], w_l = lv.cb[kCbW + 1];
   const float kappa = 1.2533141373155003f / (float)D;  // sqrt(pi/2) / d
-  uint32_t qpv[32];
+  float lam;
+  {
+    uint32_t qpv[32];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) qpv[i] = 0u;
-  if (ok) tmem_ld32(t_s + lane_base + 32 * ch, qpv);
-  float pmax = 0.f;
+    for (int i = 0; i < 32; ++i) qpv[i] = 0u;
+    if (ok && worker) tmem_ld32(t_s + lane_base + 32 * ch, qpv);
+    float pmax = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) pmax = fmaxf(pmax, fabsf(__uint_as_float(qpv[i])));
-  const float wmax = warp_max(fmaxf(fmaxf(fabsf(w_h), fabsf(w_l)) * amax, kappa * pmax));
-  if (lane == 0) bmax[warp] = wmax;
-  __syncthreads();  // also: every projection MMA has read A_hi, A_lo and the S table (waited above)
-  float tmax = 0.f;
+    for (int i = 0; i < 32; ++i) pmax = fmaxf(pmax, fabsf(__uint_as_float(qpv[i])));
+    const float wmax = warp_max(fmaxf(fmaxf(fabsf(w_h), fabsf(w_l)) * amax, kappa * pmax));
+    if (lane == 0 && worker) bmax[warp] = wmax;
+    __syncthreads();  // also: every projection MMA has read its operands (waited above)
+    float tmax = 0.f;
 #pragma unroll
-  for (int w = 0; w < kPtThreads / 32; ++w) tmax = fmaxf(tmax, bmax[w]);
-  const float lam = tmax > 0.f ? exp2f(floorf(log2f(4096.f / tmax))) : 1.f;
-  // A_qp = lambda kappa q_proj; A_hi / A_lo = f16 hi / remainder of lambda a_h q_rot; A_l = lambda a_l q_rot
+    for (int w = 0; w < kPtWorkers / 32; ++w) tmax = fmaxf(tmax, bmax[w]);
+    lam = tmax > 0.f ? exp2f(floorf(log2f(4096.f / tmax))) : 1.f;
+    // The A tiles into TMEM, row r, coordinates 32 ch .. 32 ch + 31 = columns 16 ch .. 16 ch + 15 of each:
+    // A_qp = lambda kappa q_proj; A_hi / A_lo = f16 hi / remainder of lambda a_h q_rot; A_l = lambda a_l q_rot
+    uint32_t u[16];
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    uint32_t u4[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int j = 8 * m + 2 * c;
-      const __half2 hv2 = __floats2half2_rn(lam * kappa * __uint_as_float(qpv[j]), lam * kappa * __uint_as_float(qpv[j + 1]));
-      u4[c] = *reinterpret_cast<const uint32_t*>(&hv2);
+    for (int i = 0; i < 16; ++i) {
+      const __half2 hv2 = __floats2half2_rn(lam * kappa * __uint_as_float(qpv[2 * i]),
+                                            lam * kappa * __uint_as_float(qpv[2 * i + 1]));
+      u[i] = *reinterpret_cast<const uint32_t*>(&hv2);
     }
-    *reinterpret_cast<uint4*>(sm + kPtAqp + sw128_offset(r, 32 * ch + 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+    if (ok && worker) tmem_st16(t_a + 192 + lane_base + 16 * ch, u);
   }
+  {
+    uint32_t hi16[16], lo16[16], l16[16];
 #pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    uint32_t hi4[4], lo4[4], l4[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const int j = 32 * ch + 8 * m + 2 * c;
+    for (int i = 0; i < 16; ++i) {
+      const int j = (32 * ch + 2 * i) & (D - 1);  // (the issuing warp's values are not stored)
       const float q0 = qr[r * D + j], q1 = qr[r * D + j + 1];
       const float x0 = lam * w_h * q0, x1 = lam * w_h * q1;
       const __half2 hi = __floats2half2_rn(x0, x1);
       const float2 hf = __half22float2(hi);
       const __half2 lo = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
       const __half2 lp = __floats2half2_rn(lam * w_l * q0, lam * w_l * q1);
-      hi4[c] = *reinterpret_cast<const uint32_t*>(&hi);
-      lo4[c] = *reinterpret_cast<const uint32_t*>(&lo);
-      l4[c] = *reinterpret_cast<const uint32_t*>(&lp);
+      hi16[i] = *reinterpret_cast<const uint32_t*>(&hi);
+      lo16[i] = *reinterpret_cast<const uint32_t*>(&lo);
+      l16[i] = *reinterpret_cast<const uint32_t*>(&lp);
     }
-    const uint32_t off = sw128_offset(r, 32 * ch + 8 * m);
-    *reinterpret_cast<uint4*>(sm + kPtAhi + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
-    *reinterpret_cast<uint4*>(sm + kPtAlo + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
-    *reinterpret_cast<uint4*>(sm + kPtAl + off) = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+    if (ok && worker) {
+      tmem_st16(t_a + 0 + lane_base + 16 * ch, hi16);
+      tmem_st16(t_a + 64 + lane_base + 16 * ch, lo16);
+      tmem_st16(t_a + 128 + lane_base + 16 * ch, l16);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
   }
   const float logit = a.scale * 1.4426950408889634f / lam;  // S n_t logit = score in log2 units
   constexpr float kVoff = VB == 2 ? 513.5f : 519.5f;  // 512 + the mid-rise offset 2^(VB-1) - 1/2
   const __half2 voff2 = __floats2half2_rn(kVoff, kVoff);
+  tc_fence_before();
+  __syncthreads();  // the A tiles are in TMEM; every qr read is done, so all six operand tiles are free
+  // Page pipeline. Page k's h, l, QJL and V^T tiles sit in tiles sH, sL, sG, sV; f1 and f2 are free. The
+  // score MMAs of a page are issued in two parts: the h and l planes (24 MMAs) as soon as the previous
+  // page's softmax has read S, the QJL plane (8) once it is expanded. In iteration k:
+  //   - after a wait for page k + 1 and the previous P.V MMAs, the issuer copies page k + 2 into page k's
+  //     stage and issues the QJL part of page k's scores, while the workers expand page k + 1's h and l
+  //     planes into f1 and f2;
+  //   - the softmax of page k reads S; then the issuer issues the h and l part of page k + 1's scores while
+  //     the workers finish the softmax, with P (f16) over the h tile;
+  //   - the issuer issues the P.V MMAs while the workers expand page k + 1's QJL plane and values into the
+  //     l and QJL tiles of page k.
+  // The tiles then rotate: page k + 1 has h = f1, l = f2, QJL = sL, V = sG, and sH, sV (P and V of page k)
+  // are free once the P.V MMAs have read them.
+  int sH = 0, sL = 1, sG = 2, sV = 3, f1 = 4, f2 = 5;
+  auto expand_hl = [&](const uint8_t* page, int parity, int th, int tl) {
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
+    const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
+    if (hv == 0) ns[128 * parity + tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu))) * logit;
+    pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, tile_at(th));
+    pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, tile_at(tl));
+  };
+  auto expand_gv = [&](const uint8_t* page, int tg, int tv) {
+    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
+    const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
+    pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, tile_at(tg));  // +-gamma_t (f16 bits)
+    pt_expand_values<VB>(page, pl, tk, hv, voff2, tile_at(tv));
+  };
+  // S = A_hi H + A_lo H + A_l L (issue_hl) + A_qp G (issue_g)
+  auto issue_hl = [&](int th, int tl) {
+    tc_fence_after();
+    pt_mma_ts_k128(t_s, t_a + 0, smem_u32(tile_at(th)), false);
+    pt_mma_ts_k128(t_s, t_a + 64, smem_u32(tile_at(th)), true);
+    pt_mma_ts_k128(t_s, t_a + 128, smem_u32(tile_at(tl)), true);
+    umma_commit(&bars[kBarHL]);
+  };
+  ok = ok && wait_bars(kBarPg, -1);  // page 0
+  if (ok && worker) {
+    expand_hl(stg, 0, sH, sL);
+    expand_gv(stg, sG, sV);
+  }
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  tc_fence_before();
+  __syncthreads();
+  if (ok && tid == kPtIssuer) issue_hl(sH, sL);
+  if (ok) arm(kBarHL);
   float m_used = -INFINITY, l_loc = 0.f;
   for (int k = 0; k < n && ok; ++k) {
-    const int pg = pg0 + k, buf = k & 1;
-    const uint8_t* page = stg + buf * PBS;
-    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
-    if (k + 1 < n) {  // next page into the other stage (its last reader finished before the barriers below)
-      if (tid == 0) {
+    const int pg = pg0 + k, st = k & 1;
+    const bool more = k + 1 < n;
+    const uint8_t* npage = stg + (st ^ 1) * PBS;  // page k + 1
+    // page k + 1 landed, and the previous P.V MMAs are done (f1, f2 free, O stable); the barrier also ends the
+    // previous iteration's expansions
+    if (more || k > 0) ok = wait_bars(more ? kBarPg + (st ^ 1) : -1, k > 0 ? kBarO : -1);
+    if (!ok) break;
+    if (tid == kPtIssuer) {
+      if (k + 2 < n) {  // page k + 2 into page k's stage (its last readers finished before the barrier above)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        mbar_expect_tx(&bars[kBarPg + (buf ^ 1)], PB);
-        bulk_g2s(stg + (buf ^ 1) * PBS, pt_page(lv, slot, h, pg + 1), PB, &bars[kBarPg + (buf ^ 1)]);
+        mbar_expect_tx(&bars[kBarPg + st], PB);
+        bulk_g2s(stg + st * PBS, pt_page(lv, slot, h, pg + 2), PB, &bars[kBarPg + st]);
       }
-      arm(kBarPg + (buf ^ 1));
+      tc_fence_after();
+      pt_mma_ts_k128(t_s, t_a + 192, smem_u32(tile_at(sG)), true);
+      umma_commit(&bars[kBarS]);
     }
-    ok = wait_bar(kBarPg + buf);
-    if (ok && k > 0) ok = wait_bar(kBarO);  // the previous P.V MMAs have read BX and BY
+    if (k + 2 < n) arm(kBarPg + st);
+    arm(kBarS);
+    // ---- page k + 1's h and l planes into f1, f2 ----
+    if (more && worker) {
+      expand_hl(npage, st ^ 1, f1, f2);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    }
+    // ---- softmax of row r over tokens 32 ch .. 32 ch + 31 of page k ----
+    ok = wait_bars(kBarS, kBarHL);
     if (!ok) break;
     tc_fence_after();
-    // ---- h and l planes (+-1, +-1 with the weights in A), per-token logit factors ----
-    {
-      const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
-      if (hv == 0) ns[tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu))) * logit;
-      pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, sm + kPtBX);
-      pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, sm + kPtBY);
+    float* xrow = reinterpret_cast<float*>(tile_at(sL));  // [4][128] row maxima of the quarters (the l tile is read)
+    uint32_t sv[32];
+    float mx = -INFINITY;
+    if (worker) {
+      tmem_ld32(t_s + lane_base + 32 * ch, sv);
+      const bool full = pg * kPage + kPage <= vis_w;  // every token of the page is visible to the whole warp
+      const float* nsk = ns + 128 * st;
+#pragma unroll
+      for (int i4 = 0; i4 < 8; ++i4) {
+        const float4 f = *reinterpret_cast<const float4*>(nsk + 32 * ch + 4 * i4);
+        const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = 4 * i4 + e, t = 32 * ch + i;
+          float s = __uint_as_float(sv[i]) * fv[e];
+          if (!full && pg * kPage + t >= vis_r) s = -INFINITY;
+          sv[i] = __float_as_uint(s);
+          mx = fmaxf(mx, s);
+        }
+      }
+      xrow[128 * ch + r] = mx;
     }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // S = A_hi B_h + A_lo B_h (commit h), + A_l B_l (commit l)
-      tc_fence_after();
-      pt_mma_k128(t_s, a_hi, b_x, false);
-      pt_mma_k128(t_s, a_lo, b_x, true);
-      umma_commit(&bars[kBarH]);
-      pt_mma_k128(t_s, a_l, b_y, true);
-      umma_commit(&bars[kBarL]);
-    }
-    arm(kBarH);
-    arm(kBarL);
-    // ---- the QJL plane (+-gamma_t) into BX once the h MMAs have read it ----
-    ok = wait_bar(kBarH);
-    if (!ok) break;
-    {
-      const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
-      pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, sm + kPtBX);
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {  // S += A_qp B_s
-      tc_fence_after();
-      pt_mma_k128(t_s, a_qp, b_x, true);
-      umma_commit(&bars[kBarSg]);
-    }
-    arm(kBarSg);
-    // ---- values into BY once the l MMAs have read it: V^T[j][token] = s_g (code - offset) ----
-    ok = wait_bar(kBarL);
-    if (!ok) break;
-    {
-      const int j = tk, th = hv;
-      const int mt = j >> 4, g8 = j & 7, rowhi = (j >> 3) & 1, grp = j >> 5;
-      const uint32_t* vw = reinterpret_cast<const uint32_t*>(page + pl.vbits_off);
-      const uint32_t* vsc = reinterpret_cast<const uint32_t*>(page + pl.vscale_off);  // [token pair][group] f16x2
+    __syncthreads();  // S is read: the next page's h and l MMAs may overwrite it
+    if (more && tid == kPtIssuer) issue_hl(f1, f2);
+    if (more) arm(kBarHL);
+    if (worker) {
+#pragma unroll
+      for (int q = 1; q < kPtQ; ++q) mx = fmaxf(mx, xrow[128 * ((ch + q) % kPtQ) + r]);
+      // the row maximum grew by more than 2^8: move to the new maximum (O and l scaled by alpha). The TMEM
+      // loads and stores are warp-wide, so a warp rescales when any of its rows needs it (alpha = 1 for the
+      // rest). The previous P.V MMAs are done (waited above).
+      const bool grow = mx > m_used + 8.f;
+      const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : pt_ex2(m_used - mx));
+      if (__any_sync(0xffffffffu, grow && k > 0)) {
+        uint32_t ov[32];
+        tmem_ld32(t_o + lane_base + 32 * ch, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+        tmem_st32(t_o + lane_base + 32 * ch, ov);
+      }
+      if (grow) {
+        l_loc *= alpha;
+        m_used = mx;
+      }
+      const float mref = m_used == -INFINITY ? 0.f : m_used;  // every s is -inf while nothing is visible
 #pragma unroll
       for (int mm = 0; mm < 4; ++mm) {
-        const int m = 4 * th + mm, blk = m >> 2, kap = (m >> 1) & 1, hiT = m & 1, rr = rowhi + 2 * hiT;
         uint32_t u4[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t x;
-          if (VB == 2) {
-            x = code_pair_512<2>(vw[(blk * (D / 16) + mt) * 32 + 4 * g8 + c], 2 * vfield2(kap, rr));
-          } else {
-            x = code_pair_512<4>(vw[((blk * (D / 16) + mt) * 32 + 4 * g8 + c) * 2 + kap], 4 * vfield4(rr));
-          }
-          const int t0 = 8 * m + 2 * c;  // the pair (t0, t0 + 1)
-          const uint32_t s2 = vsc[(t0 >> 1) * (D / 32) + grp];
-          const __half2 v = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&x), voff2),
-                                    *reinterpret_cast<const __half2*>(&s2));
-          u4[c] = *reinterpret_cast<const uint32_t*>(&v);
+          const int i = 8 * mm + 2 * c;
+          const float p0 = pt_ex2(__uint_as_float(sv[i]) - mref), p1 = pt_ex2(__uint_as_float(sv[i + 1]) - mref);
+          l_loc += p0 + p1;
+          const __half2 ph = __floats2half2_rn(p0, p1);
+          u4[c] = *reinterpret_cast<const uint32_t*>(&ph);
         }
-        *reinterpret_cast<uint4*>(sm + kPtBY + sw128_offset(j, 8 * m)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
+        *reinterpret_cast<uint4*>(tile_at(sH) + sw128_offset(r, 32 * ch + 8 * mm)) =
+            make_uint4(u4[0], u4[1], u4[2], u4[3]);
       }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     }
-    // ---- softmax of row r over tokens 32 ch .. 32 ch + 31 ----
-    ok = wait_bar(kBarSg);
-    if (!ok) break;
-    tc_fence_after();
-    uint32_t sv[32];
-    tmem_ld32(t_s + lane_base + 32 * ch, sv);
-    const bool full = pg * kPage + kPage <= vis_w;  // every token of the page is visible to the whole warp
-    float mx = -INFINITY;
-#pragma unroll
-    for (int i4 = 0; i4 < 8; ++i4) {
-      const float4 f = *reinterpret_cast<const float4*>(ns + 32 * ch + 4 * i4);
-      const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * i4 + e, t = 32 * ch + i;
-        float s = __uint_as_float(sv[i]) * fv[e];
-        if (!full && pg * kPage + t >= vis_r) s = -INFINITY;
-        sv[i] = __float_as_uint(s);
-        mx = fmaxf(mx, s);
-      }
-    }
-    xrow[128 * ch + r] = mx;
-    __syncthreads();
-#pragma unroll
-    for (int q = 1; q < kPtQ; ++q) mx = fmaxf(mx, xrow[128 * ((ch + q) % kPtQ) + r]);
-    // the row maximum grew by more than 2^8: move to the new maximum (O and l scaled by alpha). The TMEM
-    // loads and stores are warp-wide, so a warp rescales when any of its rows needs it (alpha = 1 for the rest)
-    const bool grow = mx > m_used + 8.f;
-    const float alpha = !grow ? 1.f : (m_used == -INFINITY ? 0.f : pt_ex2(m_used - mx));
-    if (__any_sync(0xffffffffu, grow && k > 0)) {
-      uint32_t ov[32];
-      tmem_ld32(t_o + lane_base + 32 * ch, ov);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-      tmem_st32(t_o + lane_base + 32 * ch, ov);
-    }
-    if (grow) {
-      l_loc *= alpha;
-      m_used = mx;
-    }
-    const float mref = m_used == -INFINITY ? 0.f : m_used;  // every s is -inf while nothing is visible
-#pragma unroll
-    for (int mm = 0; mm < 4; ++mm) {
-      uint32_t u4[4];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int i = 8 * mm + 2 * c;
-        const float p0 = pt_ex2(__uint_as_float(sv[i]) - mref), p1 = pt_ex2(__uint_as_float(sv[i + 1]) - mref);
-        l_loc += p0 + p1;
-        const __half2 ph = __floats2half2_rn(p0, p1);
-        u4[c] = *reinterpret_cast<const uint32_t*>(&ph);
-      }
-      *reinterpret_cast<uint4*>(sm + kPtBX + sw128_offset(r, 32 * ch + 8 * mm)) = make_uint4(u4[0], u4[1], u4[2], u4[3]);
-    }
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // O += P V: A = P [rows x tokens] (BX), B = V^T [coordinates x tokens] (BY)
+    if (tid == kPtIssuer) {  // O += P V: A = P [rows x tokens] (over the h tile), B = V^T [coordinates x tokens]
       tc_fence_after();
-      pt_mma_k128(t_o, b_x, b_y, k > 0);
-      umma_commit(&bars[kBarO]);
+      pt_mma_k128(t_o, smem_u32(tile_at(sH)), smem_u32(tile_at(sV)), k > 0);
+      umma_commit(&bars[kBarO]);  // (also covers the next page's h and l MMAs issued before)
     }
     arm(kBarO);
+    // ---- page k + 1's QJL plane and values into the l and QJL tiles of page k (its scores are done) ----
+    if (more && worker) {  // (the next iteration's first wait is the barrier after these)
+      expand_gv(npage, sL, sG);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      tc_fence_before();
+    }
+    const int oH = sH, oL = sL, oG = sG, oV = sV;
+    sH = f1;
+    sL = f2;
+    sG = oL;
+    sV = oG;
+    f1 = oH;
+    f2 = oV;
   }
-  if (ok && ((pend >> (2 * kBarO)) & 3u)) ok = wait_bar(kBarO);
+  if (ok && ((pend >> (2 * kBarO)) & 3u)) ok = wait_bars(kBarO, -1);
   tc_fence_after();
   // ---- the partial of row r: m (log2 units), l, o (rotated basis, relative to m) ----
   __syncthreads();  // every thread has read the row maxima above
-  xrow[128 * ch + r] = l_loc;
+  float* xrow = reinterpret_cast<float*>(tile_at(f1));  // free: no MMA reads it any more
+  if (worker) xrow[128 * ch + r] = l_loc;
   __syncthreads();
   float l_row = 0.f;
 #pragma unroll
-  for (int q = 0; q < kPtQ; ++q) l_row += xrow[128 * q + r];
+  for (int q = 0; q < kPtQ; ++q) l_row += worker ? xrow[128 * q + r] : 0.f;
   const bool has = ok && m_used != -INFINITY;  // this row saw a token
-  {
+  if (worker) {
     uint32_t ov[32];
     if (ok) tmem_ld32(t_o + lane_base + 32 * ch, ov);  // warp-wide (ok is the same in every thread)
 #pragma unroll
@@ -493,7 +568,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;\n" ::"r"(tmem) : "memory");
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
 }
 
 }  // namespace

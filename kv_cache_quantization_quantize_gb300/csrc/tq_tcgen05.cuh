@@ -63,5 +63,24 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 
+// Stores 16 consecutive 32-bit columns of this thread's TMEM lane (warp w writes lanes 32(w%4)..+31).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+               "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+               : "memory");
+}
+
+// D (+)= A B^T with A (M = 128 rows, K = 16) in tensor memory at column a_tmem: lane m holds row m, and 32-bit
+// column c holds K elements 2c (low half) and 2c + 1 (high half), so one K = 16 step spans 8 columns. B is a
+// shared-memory operand given by the low word of its descriptor (umma_desc_sw128_lo).
+__device__ __forceinline__ void umma_ts_lo(uint32_t tmem_d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n .reg .b64 db;\n setp.ne.b32 p, %4, 0;\n mov.b64 db, {%2, %5};\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n}\n" ::"r"(tmem_d),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kUmmaDescSw128Hi));
+}
+
 }  // namespace
 }  // namespace tq
