@@ -287,6 +287,18 @@ tq_status tq_debug_decode_wait_fault(int stage, int polls);
  * thread appends. */
 tq_status tq_debug_append_wait_fault(int task, int polls);
 
+/* Test hook for the bounded waits of the tcgen05 prefill kernel (not part of the prefill itself). While
+ * page >= 0, CTA (0, 0, 0) of every following tcgen05 prefill launch (query tile 0, KV head 0, batch row 0,
+ * history split 0) issues neither the copy of the page with index `page` within its split nor that copy's
+ * expected-byte count, and its wait for the page gives up after `polls` polls (1 .. 2^22). That CTA then
+ * sets TQ_DEV_ERR_TIMEOUT, waits (bounded) for every copy and MMA batch it did issue, frees its tensor
+ * memory and writes an empty partial: the outputs of its 32 queries x 4 query heads are unspecified, every
+ * other output is as without the hook, and the context stays usable. A page index the CTA does not reach
+ * changes nothing. Nothing faults or hangs. page = -1 turns the hook off (the default). Returns
+ * TQ_ERR_INVALID_ARG for values out of range. Process-wide; set it only while no other thread calls the
+ * prefill. */
+tq_status tq_debug_prefill_wait_fault(int page, int polls);
+
 /* Test hook for the two prefill paths (not part of the prefill itself): mode 1 makes every following
  * tq_prefill_attention (and tq_prefill_workspace_bytes) take the CUDA-core decode-kernel path even where
  * the tcgen05 path applies; mode 0 (the default) chooses automatically. Returns TQ_ERR_INVALID_ARG for

@@ -48,6 +48,7 @@ _SIGS = {
                                             c_void_p]),
     "tq_debug_decode_wait_fault": (c_int, [c_int, c_int]),
     "tq_debug_append_wait_fault": (c_int, [c_int, c_int]),
+    "tq_debug_prefill_wait_fault": (c_int, [c_int, c_int]),
     "tq_debug_prefill_path": (c_int, [c_int]),
     "tq_check_status": (c_int, [c_void_p, c_void_p, _P(ctypes.c_uint32), c_int]),
     "tq_destroy": (None, [c_void_p]),

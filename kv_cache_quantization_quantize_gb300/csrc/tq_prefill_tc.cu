@@ -20,6 +20,7 @@
 // per tile, keeps the operands inside the f16 range. P (f16) and the dequantised values V^T =
 // s_g (code - offset) (f16) feed the P.V MMA into a second TMEM accumulator; the softmax rescales it
 // lazily (only when a row maximum grows by more than 2^8).
+#include <atomic>
 #include <cmath>
 
 #include <cuda_runtime.h>
@@ -27,6 +28,12 @@
 #include "tq_tcgen05.cuh"
 
 namespace tq {
+
+// tq_debug_prefill_wait_fault: the page (index within its split) whose copy CTA (0, 0, 0) of the tcgen05
+// prefill skips (-1: none), and the polls of its wait
+std::atomic<int> g_pfault_page{-1};
+std::atomic<int> g_pfault_polls{0};
+
 namespace {
 
 // 16 worker warps (warp w covers TMEM lanes 32 (w % 4).. and column quarter w / 4) and one more warp whose
@@ -54,6 +61,8 @@ struct PrefillTcArgs {
   float scale;             // softmax scale
   uint8_t* ws;
   DecodePlan plan;         // partial layout; n_splits history splits + the ring partial
+  int fault_page;          // wait-timeout test hook: CTA (0, 0, 0) issues no copy of this page (-1: none)
+  uint32_t fault_polls;    // and gives up its wait for it after this many polls
 };
 
 __host__ __device__ constexpr size_t prefill_tc_smem(uint32_t page_bytes) {
@@ -158,7 +167,8 @@ __device__ __forceinline__ void pt_mma_ts_k128(uint32_t t_d, uint32_t t_a, uint3
   }
 }
 
-template <int VB>
+// HOOK: the instantiation with the wait-timeout test hook compiled in (launched only while it is set).
+template <int VB, bool HOOK>
 __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   constexpr int D = 128, KB = 3;
   extern __shared__ uint8_t smem_raw[];
@@ -218,6 +228,11 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     return;
   }
 
+  // the wait-timeout test hook: a page whose copy is never issued (nor its byte count expected), so the wait
+  // for it gives up after a few polls
+  const int fpage = HOOK && (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? a.fault_page : -1;
+  auto skip_copy = [fpage](int k) { return HOOK && k == fpage; };
+  auto page_polls = [fpage, &a](int k) { return HOOK && k == fpage ? a.fault_polls : kWaitPolls; };
   // ---- setup: barriers, TMEM (512 columns), the S table for the projection, the first two pages ----
   if (tid == 0) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
@@ -225,6 +240,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     mbar_expect_tx(&bars[kBarTab], 2u * D * D);
     bulk_g2s(tile_at(2), lv.S_sw, 2u * D * D, &bars[kBarTab]);
     for (int k = 0; k < 2 && k < n; ++k) {
+      if (skip_copy(k)) continue;
       mbar_expect_tx(&bars[kBarPg + k], PB);
       bulk_g2s(stg + k * PBS, pt_page(lv, slot, h, pg0 + k), PB, &bars[kBarPg + k]);
     }
@@ -276,17 +292,19 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   // per barrier, kept alike by every thread: the parity of the next phase to wait for (bit i of par) and
   // the phases armed (a copy or an MMA batch that completes it) but not seen complete (2 bits i of pend),
   // for the drain after a wait that gave up. Armed now: the S table and the first one or two pages.
-  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (1u << (2 * kBarPg)) | (n > 1 ? 1u << (2 * (kBarPg + 1)) : 0u);
+  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (skip_copy(0) ? 0u : 1u << (2 * kBarPg)) |
+                            (n > 1 && !skip_copy(1) ? 1u << (2 * (kBarPg + 1)) : 0u);
   auto arm = [&](int i) { pend += 1u << (2 * i); };
-  // Waits (bounded) for the oldest armed phase not seen yet of barrier i and, if j >= 0, of barrier j. The
+  // Waits (bounded: `polls_i` polls for barrier i) for the oldest armed phase not seen yet of barrier i and,
+  // if j >= 0, of barrier j. The
   // issuing thread alone polls; the others wait at the block barrier, which keeps 500 pollers off the
   // shared-memory pipe that the tensor cores read their operands through (the try_wait acquire of the
   // poller and the barrier make the completed copy or MMA results visible to every thread). Every thread
   // gets the same answer.
-  auto wait_bars = [&](int i, int j) {
+  auto wait_bars = [&](int i, int j, uint32_t polls_i = kWaitPolls) {
     bool w = true;
     if (tid == kPtIssuer) {
-      if (i >= 0) w = mbar_wait(&bars[i], (par >> i) & 1u);
+      if (i >= 0) w = mbar_wait(&bars[i], (par >> i) & 1u, polls_i);
       if (w && j >= 0) w = mbar_wait(&bars[j], (par >> j) & 1u);
     }
     w = __syncthreads_and(w) != 0;
@@ -386,8 +404,12 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   //   - the issuer issues the P.V MMAs while the workers expand page k + 1's QJL plane and values into the
   //     l and QJL tiles of page k.
   // The tiles then rotate: page k + 1 has h = f1, l = f2, QJL = sL, V = sG, and sH, sV (P and V of page k)
-  // are free once the P.V MMAs have read them.
-  int sH = 0, sL = 1, sG = 2, sV = 3, f1 = 4, f2 = 5;
+  // are free once the P.V MMAs have read them. The rotation has period 4 (page 0: h, l, QJL, V = tiles 0-3,
+  // f1, f2 = 4, 5); tile_of reads role r's tile for page k from a table of 4-bit fields, one per k % 4.
+  constexpr uint32_t kRoleH = 0x4040, kRoleL = 0x2351, kRoleG = 0x3512, kRoleV = 0x5123, kRoleF1 = 0x0404,
+                     kRoleF2 = 0x1235;
+  auto tile_of = [](uint32_t role, int k) { return (int)((role >> (4 * (k & 3))) & 7u); };
+  int sH = 0, sL = 1, sG = 2, sV = 3;
   auto expand_hl = [&](const uint8_t* page, int parity, int th, int tl) {
     const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
     const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
@@ -409,7 +431,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     pt_mma_ts_k128(t_s, t_a + 128, smem_u32(tile_at(tl)), true);
     umma_commit(&bars[kBarHL]);
   };
-  ok = ok && wait_bars(kBarPg, -1);  // page 0
+  ok = ok && wait_bars(kBarPg, -1, page_polls(0));  // page 0
   if (ok && worker) {
     expand_hl(stg, 0, sH, sL);
     expand_gv(stg, sG, sV);
@@ -422,14 +444,19 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   float m_used = -INFINITY, l_loc = 0.f;
   for (int k = 0; k < n && ok; ++k) {
     const int pg = pg0 + k, st = k & 1;
+    sH = tile_of(kRoleH, k);
+    sL = tile_of(kRoleL, k);
+    sG = tile_of(kRoleG, k);
+    sV = tile_of(kRoleV, k);
+    const int f1 = tile_of(kRoleF1, k), f2 = tile_of(kRoleF2, k);
     const bool more = k + 1 < n;
     const uint8_t* npage = stg + (st ^ 1) * PBS;  // page k + 1
     // page k + 1 landed, and the previous P.V MMAs are done (f1, f2 free, O stable); the barrier also ends the
     // previous iteration's expansions
-    if (more || k > 0) ok = wait_bars(more ? kBarPg + (st ^ 1) : -1, k > 0 ? kBarO : -1);
+    if (more || k > 0) ok = wait_bars(more ? kBarPg + (st ^ 1) : -1, k > 0 ? kBarO : -1, page_polls(k + 1));
     if (!ok) break;
     if (tid == kPtIssuer) {
-      if (k + 2 < n) {  // page k + 2 into page k's stage (its last readers finished before the barrier above)
+      if (k + 2 < n && !skip_copy(k + 2)) {  // page k + 2 into page k's stage (its last readers finished before the barrier above)
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         mbar_expect_tx(&bars[kBarPg + st], PB);
         bulk_g2s(stg + st * PBS, pt_page(lv, slot, h, pg + 2), PB, &bars[kBarPg + st]);
@@ -438,7 +465,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
       pt_mma_ts_k128(t_s, t_a + 192, smem_u32(tile_at(sG)), true);
       umma_commit(&bars[kBarS]);
     }
-    if (k + 2 < n) arm(kBarPg + st);
+    if (k + 2 < n && !skip_copy(k + 2)) arm(kBarPg + st);
     arm(kBarS);
     // ---- page k + 1's h and l planes into f1, f2 ----
     if (more && worker) {
@@ -525,19 +552,13 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
       asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       tc_fence_before();
     }
-    const int oH = sH, oL = sL, oG = sG, oV = sV;
-    sH = f1;
-    sL = f2;
-    sG = oL;
-    sV = oG;
-    f1 = oH;
-    f2 = oV;
   }
   if (ok && ((pend >> (2 * kBarO)) & 3u)) ok = wait_bars(kBarO, -1);
   tc_fence_after();
   // ---- the partial of row r: m (log2 units), l, o (rotated basis, relative to m) ----
   __syncthreads();  // every thread has read the row maxima above
-  float* xrow = reinterpret_cast<float*>(tile_at(f1));  // free: no MMA reads it any more
+  float* xrow = reinterpret_cast<float*>(tile_at(0));  // free: no MMA reads it any more (after a wait that
+                                                        // gave up, the partial written is empty anyway)
   if (worker) xrow[128 * ch + r] = l_loc;
   __syncthreads();
   float l_row = 0.f;
@@ -586,6 +607,17 @@ int prefill_tc_splits(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_h
   return std::max(1, std::min(max_pages, sms / std::max(1, ctas)));
 }
 
+template <int VB, bool HOOK>
+cudaError_t launch_prefill_tc_k(const PrefillTcArgs& a, dim3 grid, size_t smem, cudaStream_t s) {
+  static bool attr = false;  // set once, outside any stream capture that follows
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<VB, HOOK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(k_prefill_tc<VB, HOOK>, grid, dim3(kPtThreads), smem, s, a);
+}
+
 cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const int32_t* seq_ids, const int32_t* n_q,
                               int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, cudaStream_t s) {
   PrefillTcArgs a;
@@ -597,25 +629,23 @@ cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const
   a.scale = scale;
   a.ws = static_cast<uint8_t*>(ws);
   a.plan = plan;
+  a.fault_page = g_pfault_page.load();
+  a.fault_polls = (uint32_t)g_pfault_polls.load();
   const dim3 grid((q_per_row + 31) / 32, a.lv.Hkv, batch * plan.n_splits);
   const size_t smem = prefill_tc_smem(a.lv.page_bytes);
   if (smem > kMaxSmemPerCta) return cudaErrorInvalidValue;
-  if (a.lv.vb == 2) {
-    static bool attr = false;  // set once, outside any stream capture that follows
-    if (!attr) {
-      cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
-    return launch_pdl(k_prefill_tc<2>, grid, dim3(kPtThreads), smem, s, a);
-  }
-  static bool attr4 = false;
-  if (!attr4) {
-    cudaError_t e = cudaFuncSetAttribute(k_prefill_tc<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr4 = true;
-  }
-  return launch_pdl(k_prefill_tc<4>, grid, dim3(kPtThreads), smem, s, a);
+  const bool hook = a.fault_page >= 0;
+  return a.lv.vb == 2 ? (hook ? launch_prefill_tc_k<2, true>(a, grid, smem, s) : launch_prefill_tc_k<2, false>(a, grid, smem, s))
+                      : (hook ? launch_prefill_tc_k<4, true>(a, grid, smem, s) : launch_prefill_tc_k<4, false>(a, grid, smem, s));
 }
 
 }  // namespace tq
+
+extern "C" tq_status tq_debug_prefill_wait_fault(int page, int polls) {
+  if (page < -1) return tq::set_error(TQ_ERR_INVALID_ARG, "page must be -1 (off) or >= 0");
+  if (page >= 0 && (polls < 1 || polls > (int)tq::kWaitPolls))
+    return tq::set_error(TQ_ERR_INVALID_ARG, "polls must be in [1, 2^22]");
+  tq::g_pfault_polls.store(page >= 0 ? polls : 0);
+  tq::g_pfault_page.store(page);
+  return tq::set_error(TQ_OK, "");
+}

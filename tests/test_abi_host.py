@@ -310,5 +310,10 @@ def test_debug_hooks_validate_their_arguments():
     assert lib.tq_debug_append_wait_fault(0, (1 << 22) + 1) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_debug_append_wait_fault(5, 8) == _abi.TQ_OK
     assert lib.tq_debug_append_wait_fault(-1, 0) == _abi.TQ_OK
+    assert lib.tq_debug_prefill_wait_fault(-2, 8) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_prefill_wait_fault(1, 0) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_prefill_wait_fault(1, (1 << 22) + 1) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_debug_prefill_wait_fault(3, 8) == _abi.TQ_OK
+    assert lib.tq_debug_prefill_wait_fault(-1, 0) == _abi.TQ_OK
     assert lib.tq_debug_decode_wait_fault(4, 8) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_debug_decode_wait_fault(-1, 0) == _abi.TQ_OK
