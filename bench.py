@@ -568,6 +568,14 @@ def run_ours(args):
             r["config"] = workload_config(wl)
             nested[name] = r
 
+    # prefill attention of a 512-query chunk at the end of the 32K sequence, on the default path and on the
+    # CUDA-core path it replaces, as a nested record
+    prefill = None
+    if args.nested and WL["name"] == WORKLOADS["llama8b"]["name"] and not full and not paged and rank == 0:
+        prefill = measure_prefill(tqm, synth, dev, 512, False, 5)
+        cc = measure_prefill(tqm, synth, dev, 512, True, 2, warm=1)
+        prefill["cuda_core_path_ms_per_layer"] = cc["ms_per_layer"]
+
     line = {
         "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -584,6 +592,8 @@ def run_ours(args):
         line["quantize"] = quant
     if nested:
         line["workloads"] = nested
+    if prefill is not None:
+        line["prefill"] = prefill
     if (rank == 0 and world == 1 and not args.no_cpu_baseline and not full and not paged
             and WL["kb"] == 3 and args.head_dim == 128):  # the oracle on this workload
         line["cpu_baseline"] = cpu_baseline(args)
@@ -652,24 +662,19 @@ def bench_quantize(tqm, synth, dev, args, peak):
             "hbm_gbs": gbs, "frac_of_measured_hbm": gbs / peak, "bytes_per_pass": bytes_pass}
 
 
-def bench_prefill(args):
+def measure_prefill(tqm, synth, dev, Tq, force_cc, reps, warm=3):
     """Prefill attention of one chunk over the cache: the Llama-3.1-8B shape (8 KV heads, 32 q heads,
-    d=128, K3/V2), one sequence of 32768 tokens whose last `args.prefill_chunk` tokens are the chunk,
-    all 32 layers. Prints one JSON line (query tokens/s); it is not the bench line of the decode step."""
+    d=128, K3/V2), one sequence of 32768 tokens whose last `Tq` tokens are the chunk, all 32 layers (32
+    layers of packed history, 785 MB, more than L2). `warm` untimed passes, then `reps` timed passes of
+    all layers (CUDA events on the stream). Returns a dict."""
     import torch
-    import kv_cache_quantization_quantize_gb300 as tqm
-    from kv_cache_quantization_quantize_gb300 import synth
-    dev = torch.device("cuda", 0)
+    from kv_cache_quantization_quantize_gb300 import _abi
     L_layers, Hq, Hkv, d, ctx, vb = WL["layers"], WL["hq"], WL["hkv"], WL["d"], WL["ctx"], WL["vb"]
-    Tq = args.prefill_chunk
-    from kv_cache_quantization_quantize_gb300 import _abi, build as _build
-    _build.build()
-    force_cc = getattr(args, "prefill_path", "auto") == "cuda-core"
-    _abi.load().tq_debug_prefill_path(1 if force_cc else 0)
+    lib = _abi.load()
+    lib.tq_debug_prefill_path(1 if force_cc else 0)
     tc = not force_cc and d == 128 and WL["kb"] == 3 and Hq == 4 * Hkv and Tq >= 32
     cfg = tqm.config(head_dim=d, value_bits=vb, key_bits=WL["kb"], n_layers=L_layers, n_kv_heads=Hkv, n_q_heads=Hq,
-                     max_seqs=1,
-                     max_ctx=ctx, seed=1)
+                     max_seqs=1, max_ctx=ctx, seed=1)
     cache = tqm.TurboQuantCache(cfg, device=dev)
     ids = torch.zeros(1, dtype=torch.int32, device=dev)
     for l in range(L_layers):
@@ -683,27 +688,47 @@ def bench_prefill(args):
     out = torch.empty((L_layers, 1, Tq, Hq, d), dtype=torch.float32, device=dev)
     nq = torch.full((1,), Tq, dtype=torch.int32, device=dev)
     ws = cache.prefill_workspace(1, Tq, ctx)
-    for l in range(L_layers):
-        cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
-    torch.cuda.synchronize()
-    reps = max(1, min(args.steps, 5))
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(reps):
-        for l in range(L_layers):
-            cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
-    e1.record()
-    torch.cuda.synchronize()
+    try:
+        for _ in range(warm):
+            for l in range(L_layers):
+                cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            for l in range(L_layers):
+                cache.prefill(l, q[l], ids, nq, out=out[l], max_ctx_hint=ctx, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+    finally:
+        lib.tq_debug_prefill_path(0)
     ms = e0.elapsed_time(e1) / reps
     status = cache.check_status()
-    print(json.dumps({"metric": "prefill attention query tokens/s (all layers)", "value": Tq / (ms * 1e-3),
-                      "unit": "query-tok/s", "ms_per_chunk": ms, "ms_per_layer": ms / L_layers,
-                      "config": {"workload": f"{WL['name']}: prefill chunk of {Tq} queries at the end of a "
-                                             f"{ctx}-token sequence", "layers": L_layers},
-                      "path": ("tcgen05: tiles of 32 queries x 4 heads, key planes and values expanded once per page "
-                               "and tile, scores and P.V into TMEM; then a ring-only decode launch") if tc
-                      else "one split-K decode launch over chunk-query rows (causal length per row)",
-                      "device_status": status}), flush=True)
+    del cache, q, out, ws
+    torch.cuda.empty_cache()
+    return {"value": Tq / (ms * 1e-3), "unit": "query-tok/s", "ms_per_chunk": ms, "ms_per_layer": ms / L_layers,
+            "passes": reps, "warmup": warm,
+            "config": {"workload": f"{WL['name']}: prefill chunk of {Tq} queries at the end of a "
+                                   f"{ctx}-token sequence", "layers": L_layers},
+            "path": ("tcgen05: tiles of 32 queries x 4 heads; query operands in TMEM, key planes and values "
+                     "expanded once per page and tile into rotating shared-memory tiles while the previous "
+                     "MMAs run, scores and P.V into TMEM; then a ring-only decode launch") if tc
+            else "one split-K decode launch over chunk-query rows (causal length per row)",
+            "device_status": status}
+
+
+def bench_prefill(args):
+    """`--prefill-chunk TQ`: one JSON line (query tokens/s) for the prefill of a TQ-query chunk; it is not
+    the bench line of the decode step."""
+    import torch
+    import kv_cache_quantization_quantize_gb300 as tqm
+    from kv_cache_quantization_quantize_gb300 import synth, build as _build
+    _build.build()
+    dev = torch.device("cuda", 0)
+    force_cc = getattr(args, "prefill_path", "auto") == "cuda-core"
+    r = measure_prefill(tqm, synth, dev, args.prefill_chunk, force_cc, max(1, min(args.steps, 5)),
+                        warm=max(1, min(args.warmup, 3)))
+    print(json.dumps(dict({"metric": "prefill attention query tokens/s (all layers)"}, **r)), flush=True)
 
 
 def bench_codec(args):
@@ -972,7 +997,8 @@ def main():
     p.add_argument("--codec-layers", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-nested", dest="nested", action="store_false",
-                   help="skip the nested records of the other decode workloads (batched, d256, d256_v4, long)")
+                   help="skip the nested records of the other decode workloads (batched, d256, d256_v4, long) "
+                        "and of the 512-query prefill")
     p.add_argument("--oracle-sample", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--oracle-full-step", type=int, default=0, help=argparse.SUPPRESS)
     p.add_argument("--profile-quantize", type=int, default=0, metavar="PASSES",
