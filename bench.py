@@ -308,6 +308,28 @@ def profiled_traffic(path=DECODE_PROFILE):
         return None
 
 
+def fidelity_report(cache, k, v, L, n_max=4096):
+    """Mean per-vector cosine similarity of dequantised packed tokens against the inputs they were coded
+    from (the guide's §六 fidelity figure): layer 0, row 0, every KV head, the first min(n_max, packed)
+    tokens. Keys with and without the QJL term, values at the workload's value bits.
+    Dequantised on the device by tq_dequantize_tokens."""
+    import torch
+    import torch.nn.functional as F
+    Hkv = k.shape[1]
+    n = min(n_max, 128 * ((L - 1) // 128))  # packed tokens of the row (the ring holds the rest)
+    acc = {"key_cos_mse": 0.0, "key_cos_qjl": 0.0, "value_cos": 0.0}
+    for h in range(Hkv):
+        ko, vo = k[:n, h].float(), v[:n, h].float()
+        k_mse, v_hat = cache.dequantize(0, 0, h, 0, n, with_qjl=False)
+        k_qjl, _ = cache.dequantize(0, 0, h, 0, n, with_qjl=True)
+        acc["key_cos_mse"] += F.cosine_similarity(k_mse, ko, dim=1).mean().item() / Hkv
+        acc["key_cos_qjl"] += F.cosine_similarity(k_qjl, ko, dim=1).mean().item() / Hkv
+        acc["value_cos"] += F.cosine_similarity(v_hat, vo, dim=1).mean().item() / Hkv
+    acc["tokens"] = n * Hkv
+    acc["sample"] = f"layer 0, row 0, {Hkv} KV heads x the first {n} packed tokens, against the bf16 inputs"
+    return acc
+
+
 def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
     """One decode workload: prefill the cache, capture the step (append 1 token + decode, every layer) as
     a CUDA graph, time K replays after W warm-up replays, and time the split-K kernel alone. With
@@ -342,6 +364,8 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
                                device=dev)
         for b in range(B):  # one row per call: rows share the layer's tokens, each with its own length
             cache.append(l, k[None], v[None], ids[b:b + 1], torch.full((1,), L0[b], dtype=torch.int32, device=dev))
+        if l == 0:
+            fidelity = fidelity_report(cache, k, v, L0[0])
         del k, v
     torch.cuda.synchronize()
     if cache.check_status():
@@ -457,7 +481,8 @@ def measure_decode(tqm, synth, dev, wl, args, K, W, world, headline):
            "pct_of_measured_hbm": 100.0 * hbm_gbs / peak, "step_bytes": step_bytes, "roofline": roof,
            "clocks": clocks, "gpu_launches": launches_per_step * K, "device_status": status,
            "step_call": "tq_decode_step (append + decode in one launch per layer)" if fused
-           else "tq_quantize_append + tq_decode_attention (two launches per layer)"}
+           else "tq_quantize_append + tq_decode_attention (two launches per layer)",
+           "cos_sim": fidelity}
     del g2
     if headline:
         res.update(measure_e2e(cache, s, qs, knew, vnew, outs, ids, ones, ws, max_ctx, g, K, n_e2e_warm, world, B,
@@ -585,7 +610,7 @@ def run_ours(args):
         "pct_of_measured_hbm": head["pct_of_measured_hbm"],
         "roofline": head["roofline"], "e2e": head["e2e"], "e2e_api": head["e2e_api"],
         "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "device_status": head["device_status"],
-        "step_call": head["step_call"],
+        "step_call": head["step_call"], "cos_sim": head["cos_sim"],
     }
     if quant is not None:
         line["quantize_tok_s"] = quant["tok_s"]

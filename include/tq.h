@@ -157,6 +157,23 @@ tq_status tq_quantize_append(tq_ctx* ctx, int layer, const void* k, const void* 
  *   - Rows with an empty ring are unchanged. */
 tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int batch, tq_stream_t stream);
 
+/* tq_dequantize_tokens: reconstructs packed tokens [t0, t0 + count) of (layer, seq_slot, kv_head) in the
+ * original basis, for fidelity reports and tests (the decode never dequantises keys; [Guide] §六 quotes the
+ * cosine similarity of such reconstructions):
+ *   k_hat = n Pi^T (c[idx] + sqrt(pi/2)/d gamma S^T sigma)   (with_qjl = 1; with_qjl = 0 drops the QJL term)
+ *   v_hat = Pi^T ((code - 2^(value_bits-1) + 1/2) s_g)
+ * with Pi = H diag(D) / sqrt(d), sigma_i = +1 where the stored sign bit is set and -1 elsewhere, and n,
+ * gamma, s_g the stored fp16 values ([Guide] §二 steps 1-4).
+ *   - d_k_out, d_v_out: device fp32 [count][head_dim], row i for token t0 + i. Caller-owned; not aliased.
+ *   - Tokens are positions in the sequence; only positions below the row's packed count (its length less
+ *     the ring) hold codes, and others give unspecified values. A paged cache's page without a block gives
+ *     zeros and TQ_DEV_ERR_BLOCK on the status word.
+ *   - Asynchronous on `stream`, ordered after earlier appends on it. Errors (on the host, before launch):
+ *     TQ_ERR_INVALID_ARG for a bad layer, slot, head, negative t0 or count, with_qjl not 0 or 1, NULL
+ *     outputs with count > 0, or no cache bound; TQ_ERR_CAPACITY for tokens past the sequence's pages. */
+tq_status tq_dequantize_tokens(tq_ctx* ctx, int layer, int seq_slot, int kv_head, int t0, int count, int with_qjl,
+                               float* d_k_out, float* d_v_out, tq_stream_t stream);
+
 /* Bytes of the decode workspace for `batch` rows and a longest sequence of `max_ctx_hint` tokens
  * (0 = cfg.max_ctx). The same workspace serves tq_decode_attention, tq_decode_phase and
  * tq_decode_step. */

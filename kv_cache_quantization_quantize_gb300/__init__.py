@@ -128,6 +128,16 @@ class TurboQuantCache(HostTables):
     def reset(self, seq_ids, layer=-1, stream=None):
         check(self.lib.tq_reset_seqs(self.ctx, layer, _ptr(seq_ids), seq_ids.numel(), _stream(stream)))
 
+    def dequantize(self, layer, slot, head, t0, count, with_qjl=True, stream=None):
+        """Packed tokens [t0, t0 + count) of (layer, slot, KV head) reconstructed in the original basis:
+        (k_hat, v_hat), fp32 [count, d] CUDA tensors (tq_dequantize_tokens)."""
+        d = self.cfg.head_dim
+        k_hat = torch.empty((count, d), dtype=torch.float32, device=self.device)
+        v_hat = torch.empty((count, d), dtype=torch.float32, device=self.device)
+        check(self.lib.tq_dequantize_tokens(self.ctx, layer, slot, head, t0, count, 1 if with_qjl else 0,
+                                            _ptr(k_hat), _ptr(v_hat), _stream(stream)))
+        return k_hat, v_hat
+
     def workspace_bytes(self, batch, max_ctx_hint=0):
         return self.lib.tq_workspace_bytes(self.ctx, batch, max_ctx_hint)
 

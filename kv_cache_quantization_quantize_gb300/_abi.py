@@ -34,6 +34,8 @@ _SIGS = {
     "tq_reset_seqs": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p]),
     "tq_quantize_append": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_int, c_int, c_void_p]),
     "tq_ring_flush": (c_int, [c_void_p, c_int, c_void_p, c_int, c_void_p]),
+    "tq_dequantize_tokens": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
+                                     c_void_p]),
     "tq_workspace_bytes": (c_size_t, [c_void_p, c_int, c_int]),
     "tq_decode_attention": (c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p, c_size_t,
                                     c_int, c_void_p]),

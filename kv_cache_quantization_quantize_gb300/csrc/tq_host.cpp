@@ -576,6 +576,26 @@ tq_status tq_ring_flush(tq_ctx* ctx, int layer, const int32_t* d_seq_ids, int ba
   return e == cudaSuccess ? ok() : cuda_fail(e, "flush kernel");
 }
 
+tq_status tq_dequantize_tokens(tq_ctx* ctx, int layer, int seq_slot, int kv_head, int t0, int count, int with_qjl,
+                               float* d_k_out, float* d_v_out, tq_stream_t stream) {
+  const tq::NvtxRange nvtx_range("tq_dequantize_tokens");
+  tq_status st = check_ready(ctx, layer);
+  if (st != TQ_OK) return st;
+  const tq_config& c = ctx->cfg;
+  if (seq_slot < 0 || seq_slot >= c.max_seqs) return fail(TQ_ERR_INVALID_ARG, "seq_slot %d out of range", seq_slot);
+  if (kv_head < 0 || kv_head >= c.n_kv_heads) return fail(TQ_ERR_INVALID_ARG, "kv_head %d out of range", kv_head);
+  if (t0 < 0 || count < 0) return fail(TQ_ERR_INVALID_ARG, "t0 %d / count %d negative", t0, count);
+  if ((long long)t0 + count > (long long)ctx->max_pages * tq::kPage)
+    return fail(TQ_ERR_CAPACITY, "tokens [%d, %lld) beyond the %d pages of a sequence", t0, (long long)t0 + count,
+                ctx->max_pages);
+  if (with_qjl != 0 && with_qjl != 1) return fail(TQ_ERR_INVALID_ARG, "with_qjl must be 0 or 1");
+  if (count == 0) return ok();
+  if (!d_k_out || !d_v_out) return fail(TQ_ERR_INVALID_ARG, "NULL output");
+  cudaError_t e = tq::launch_dequantize(ctx, layer, seq_slot, kv_head, t0, count, with_qjl, d_k_out, d_v_out,
+                                        (cudaStream_t)stream);
+  return e == cudaSuccess ? ok() : cuda_fail(e, "dequantize kernel");
+}
+
 size_t tq_workspace_bytes(const tq_ctx* ctx, int batch, int max_ctx_hint) {
   if (!ctx || batch < 1) return 0;
   return tq::decode_plan(ctx, batch, max_ctx_hint).bytes;

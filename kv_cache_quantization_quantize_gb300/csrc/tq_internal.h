@@ -243,6 +243,10 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
 // partials of every (query, KV head), n_splits per unit, into the workspace in the decode's layout.
 bool prefill_tc_eligible(const tq_ctx* ctx);
 int prefill_tc_splits(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint);
+// Packed tokens [t0, t0 + count) of (layer, slot, KV head h) dequantised to fp32 k_hat, v_hat [count][d]
+// (tq_dequantize_tokens).
+cudaError_t launch_dequantize(const tq_ctx* ctx, int layer, int slot, int h, int t0, int count, int with_qjl,
+                              float* k_out, float* v_out, cudaStream_t s);
 cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const int32_t* seq_ids, const int32_t* n_q,
                               int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, cudaStream_t s);
 // Decode launches read a row's state (and the pages it implies) before their stream wait. That is safe

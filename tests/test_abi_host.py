@@ -99,6 +99,7 @@ def test_null_and_host_only_misuse_is_rejected():
     assert lib.tq_quantize_append(h.ctx, 0, None, None, 0, None, None, 1, 1, None) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_attention(h.ctx, 0, None, None, None, 1, 0.0, None, 0, 0, None) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_ring_flush(h.ctx, 0, None, 1, None) == _abi.TQ_ERR_INVALID_ARG
+    assert lib.tq_dequantize_tokens(h.ctx, 0, 0, 0, 0, 1, 1, None, None, None) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_decode_step(h.ctx, 0, None, None, 0, None, None, None, 1, 0.0, None, 0, 0, None) \
         == _abi.TQ_ERR_INVALID_ARG
     # tq_decode_phase has two phases (0: zero the counters, 1: the decode launch); others are refused
