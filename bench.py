@@ -315,9 +315,12 @@ def fidelity_report(cache, k, v, L, n_max=4096):
     Dequantised on the device by tq_dequantize_tokens."""
     import torch
     import torch.nn.functional as F
-    Hkv = k.shape[1]
+    Hkv, d = k.shape[1], k.shape[2]
     n = min(n_max, 128 * ((L - 1) // 128))  # packed tokens of the row (the ring holds the rest)
-    acc = {"key_cos_mse": 0.0, "key_cos_qjl": 0.0, "value_cos": 0.0}
+    nq = 16  # N(0, 1) queries per head for the score vectors
+    gen = torch.Generator(device=k.device)
+    gen.manual_seed(17)
+    acc = {"key_cos_mse": 0.0, "key_cos_qjl": 0.0, "value_cos": 0.0, "score_cos_mse": 0.0, "score_cos_qjl": 0.0}
     for h in range(Hkv):
         ko, vo = k[:n, h].float(), v[:n, h].float()
         k_mse, v_hat = cache.dequantize(0, 0, h, 0, n, with_qjl=False)
@@ -325,8 +328,14 @@ def fidelity_report(cache, k, v, L, n_max=4096):
         acc["key_cos_mse"] += F.cosine_similarity(k_mse, ko, dim=1).mean().item() / Hkv
         acc["key_cos_qjl"] += F.cosine_similarity(k_qjl, ko, dim=1).mean().item() / Hkv
         acc["value_cos"] += F.cosine_similarity(v_hat, vo, dim=1).mean().item() / Hkv
+        # the score vector of a query over the tokens: <q, k_hat_t> is the decode's estimate of <q, k_t>
+        q = torch.randn((nq, d), generator=gen, device=k.device)
+        s_ref = q @ ko.T
+        acc["score_cos_mse"] += F.cosine_similarity(q @ k_mse.T, s_ref, dim=1).mean().item() / Hkv
+        acc["score_cos_qjl"] += F.cosine_similarity(q @ k_qjl.T, s_ref, dim=1).mean().item() / Hkv
     acc["tokens"] = n * Hkv
-    acc["sample"] = f"layer 0, row 0, {Hkv} KV heads x the first {n} packed tokens, against the bf16 inputs"
+    acc["sample"] = (f"layer 0, row 0, {Hkv} KV heads x the first {n} packed tokens, against the bf16 inputs; "
+                     f"score vectors of {nq} N(0,1) queries per head over those tokens")
     return acc
 
 
