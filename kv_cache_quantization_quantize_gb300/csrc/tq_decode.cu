@@ -67,8 +67,9 @@ __device__ __noinline__ void step_code_block(const DecodeArgs& a, int b, int h, 
   }
 }
 
-template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1>
-__global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 : 1) k_decode(DecodeArgs a) {
+template <int D, int VB, int STAGES, bool PAGED, int KB, int QP = 1, bool WIDE = false>
+__global__ void __launch_bounds__(decode_threads<D, WIDE>(), (D == 256 && VB == 2) || WIDE ? 2 : 1)
+    k_decode(DecodeArgs a) {
   constexpr int NCOL = qcols<QP>();
   constexpr int NBP = key_loop_planes(KB, D, QP);  // B planes the key MMAs run (stored planes: KB)
   constexpr int RP = key_rem_plane(KB, D);
@@ -77,8 +78,8 @@ __global__ void __launch_bounds__(decode_threads<D>(), D == 256 && VB == 2 ? 2 :
   constexpr int HALVES = D / CW;
   constexpr int KS = CW / 16;           // key-MMA k-steps per warp
   constexpr int QG = CW / 32;           // value groups per warp
-  constexpr int NT = decode_threads<D>();
-  constexpr int NS = decode_streams<D>();
+  constexpr int NT = decode_threads<D, WIDE>();
+  constexpr int NS = decode_streams<D, WIDE>();
   constexpr int SW = 4 * HALVES;  // warps per stream
   constexpr int NG = D / 32;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -496,16 +497,16 @@ constexpr int decode_stages() {  // pages in flight per stream
   return D <= 128 ? 4 : 3;
 }
 
-template <int D, int VB, int KB, int QP = 1, int STAGES = decode_stages<D, VB>()>
+template <int D, int VB, int KB, int QP = 1, int STAGES = decode_stages<D, VB>(), bool WIDE = false>
 size_t decode_smem_bytes() {
   const PageLayout pl = page_layout(D, VB, KB);
-  constexpr int NT = decode_threads<D>();
-  constexpr int NGRP = 4 * decode_streams<D>();
+  constexpr int NT = decode_threads<D, WIDE>();
+  constexpr int NGRP = 4 * decode_streams<D, WIDE>();
   constexpr int NCOL = qcols<QP>();
   const size_t merge_bytes = sizeof(float) * (3 * NGRP * NCOL + NGRP * NCOL * D);
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
-  size_t smem = 128 + (size_t)decode_streams<D>() * STAGES * pl.bytes + xbuf_bytes +
-                prep_scratch_bytes<D, KB, QP>();
+  size_t smem = 128 + (size_t)decode_streams<D, WIDE>() * STAGES * pl.bytes + xbuf_bytes +
+                prep_scratch_bytes<D, KB, QP, NT>();
   smem = std::max(smem, 128 + merge_bytes);
   smem = std::max(smem, ring_smem_bytes<D, QP>());
   smem = std::max(smem, 128 + sizeof(float) * (4 * (NT / 32) + 2 * NCOL * 1026));  // combine: split (m, l)
@@ -527,6 +528,25 @@ int decode_setup() {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<D, VB, STAGES, false, KB>, decode_threads<D>(),
                                                       smem) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    resident = n;
+  }
+  return resident;
+}
+
+// The WIDE variant (head_dim 128, K3/V2, contiguous cache): attributes set once; resident CTAs per SM.
+int decode_setup_wide() {
+  static int resident = 0;  // set once, outside any stream capture that follows
+  if (resident == 0) {
+    constexpr int STAGES = decode_stages<128, 2>();
+    const size_t smem = decode_smem_bytes<128, 2, 3, 1, STAGES, true>();
+    if (cudaFuncSetAttribute(k_decode<128, 2, STAGES, false, 3, 1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem) != cudaSuccess)
+      return -1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_decode<128, 2, STAGES, false, 3, 1, true>,
+                                                      decode_threads<128, true>(), smem) != cudaSuccess ||
         n < 1)
       n = 1;
     resident = n;
@@ -569,6 +589,13 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
   }
   if (phase < 0 || phase == 1) {
     const dim3 grid(a.ring_only ? 1 : a.plan.n_splits + 1, a.lv.Hkv, batch);
+    if constexpr (D == 128 && VB == 2 && KB == 3) {
+      if (a.plan.wide && qp == 1 && !a.lv.btab) {  // decode_plan chose the two-CTAs-per-SM variant
+        if (decode_setup_wide() < 0) return cudaErrorInvalidValue;
+        return launch_pdl(k_decode<128, 2, STAGES, false, 3, 1, true>, grid, dim3(decode_threads<128, true>()),
+                          decode_smem_bytes<128, 2, 3, 1, STAGES, true>(), s, a);
+      }
+    }
     cudaError_t e =
         qp == 2 ? launch_pdl(k_decode<D, VB, PSTAGES, false, KB, 2>, grid, dim3(decode_threads<D>()), smem, s, a)
         : a.lv.btab ? launch_pdl(k_decode<D, VB, STAGES, true, KB>, grid, dim3(decode_threads<D>()), smem, s, a)
@@ -601,9 +628,13 @@ bool decode_pairs_fit(const tq_ctx* ctx) {
 }
 
 // key_bits 4 is served with value_bits 4 (validated on the host).
-int decode_resident_ctas(const tq_ctx* ctx) {
+int decode_resident_ctas(const tq_ctx* ctx, bool wide) {
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   int n;
+  if (wide) {
+    n = decode_setup_wide();
+    return n > 0 ? n : 1;
+  }
   if (kb == 4) n = d == 64 ? decode_setup<64, 4, 4>() : d == 128 ? decode_setup<128, 4, 4>() : decode_setup<256, 4, 4>();
   else if (d == 64 && vb == 2) n = decode_setup<64, 2, 3>();
   else if (d == 64 && vb == 4) n = decode_setup<64, 4, 3>();

@@ -160,7 +160,7 @@ __device__ __forceinline__ int row_len(const DecodeArgs& a, int b, int L) {
   return i < nq ? max(0, L - (nq - 1 - i)) : 0;
 }
 
-template <int D>
+template <int D, bool WIDE = false>
 __host__ __device__ constexpr int decode_threads();
 // Floats of the d=256 partial-score exchange buffer of a split CTA ([NT][2 tiles][8]).
 template <int D>
@@ -170,19 +170,21 @@ __host__ __device__ constexpr int decode_xbuf_floats() {
 
 // Split CTAs run `decode_streams` independent page streams of 4 token-group warps x (d/128) coordinate
 // halves: 3 streams (12 warps, one CTA per SM) for head_dim 128, 1 stream (8 warps) for head_dim 256.
-// (Four streams of 16 warps measured slower at batch 1 and no faster at batch 32.)
-template <int D>
+// (Four streams of 16 warps measured slower at batch 1 and no faster at batch 32.) The WIDE variant of
+// head_dim 128 (K3/V2, contiguous cache) runs 2 streams in CTAs of which two share an SM: at batch 32 x
+// 128K it hides more latency (1145 against 1205 us per launch); at batch 1 its extra splits cost more.
+template <int D, bool WIDE = false>
 __host__ __device__ constexpr int decode_streams() {
-  return D <= 128 ? 3 : 1;
+  return D <= 128 ? (WIDE ? 2 : 3) : 1;
 }
 // Coordinates of one warp (a 128-coordinate half, or all 64) and key-MMA k-steps per warp.
 template <int D>
 __host__ __device__ constexpr int warp_coords() {
   return D < 128 ? D : 128;
 }
-template <int D>
+template <int D, bool WIDE>
 __host__ __device__ constexpr int decode_threads() {
-  return decode_streams<D>() * 32 * 4 * (D / warp_coords<D>());
+  return decode_streams<D, WIDE>() * 32 * 4 * (D / warp_coords<D>());
 }
 
 // =============================================================================================
@@ -218,12 +220,12 @@ __host__ __device__ constexpr int qcols() {
 }
 
 // Bytes of a split CTA's query-prep scratch.
-template <int D, int KB, int QP = 1>
+template <int D, int KB, int QP = 1, int NT = decode_threads<D>()>
 __host__ __device__ constexpr size_t prep_scratch_bytes() {
   // q_rot, q_proj [columns][D] fp32; 32 floats of scales; B fragments [planes D/16 items][32 lanes]
   // uint2; per-warp offset sums [warps][2][8 B columns]
   return sizeof(float) * (2 * qcols<QP>() * D + 32) + 8 * 32 * (key_loop_planes(KB, D, QP) * D / 16) +
-         sizeof(float) * 2 * 8 * (decode_threads<D>() / 32);
+         sizeof(float) * 2 * 8 * (NT / 32);
 }
 
 // 2^(24 - pos) for the f16 bit position that carries coordinate pair q = 2s + sub (kpair_pos).

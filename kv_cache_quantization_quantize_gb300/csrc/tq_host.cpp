@@ -282,7 +282,13 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
   const int max_pages = std::max(1, (hint + kPage - 1) / kPage);
   const int units = batch * c.n_kv_heads;
   const int sms = ctx->sm_count > 0 ? ctx->sm_count : 152;
-  const int per_sm = ctx->host_only ? 2 : decode_resident_ctas(ctx);
+  // The wide variant (head_dim 128, K3/V2, contiguous cache, decode rows) when there are at least 128
+  // packed pages per CTA slot of two per SM: at batch 32 x 128K it ran 1145 against 1205 us per launch;
+  // at batch 1 x 32K (8 pages per slot) and batch 16 x 8K (27) its extra splits made it slower.
+  const bool wide = !ctx->host_only && c.head_dim == 128 && c.value_bits == 2 && c.key_bits == 3 &&
+                    c.n_blocks == 0 && cnt_rows == 0 && ncol == kMaxG &&
+                    (double)units * max_pages >= 128.0 * 2 * sms;
+  const int per_sm = ctx->host_only ? 2 : decode_resident_ctas(ctx, wide);
   const int target = per_sm * sms;  // split-K CTAs that fit in one wave
   // Splits per (row, KV head): the fewest whose estimated time is within 3 % of the least, with every
   // row taken at the hint's length. Time = waves x (page rounds of a split + the fixed cost of a split
@@ -290,7 +296,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
   // and one at 256; its fixed cost is about 2.5 page rounds (batch-1 trace: 2.5 us query prep and
   // 2.7 us merge and arrival against 2.1 us per page round). The ring CTA of a (row, KV head) is short:
   // it counts as that fixed cost's share of a wave slot.
-  const int ns = c.head_dim <= 128 ? 3 : 1;
+  const int ns = c.head_dim <= 128 ? (wide ? 2 : 3) : 1;
   const double fixed_rounds = 2.5;
   const int max_splits = std::min(max_pages, 1024);  // the combine keeps 4 weights per split in shared memory
   auto cost_of = [&](int pps) {
@@ -310,6 +316,7 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
     }
   }
   DecodePlan p;
+  p.wide = wide ? 1 : 0;
   p.pages_per_split = best_pps;
   p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
   const int d = c.head_dim;

@@ -208,6 +208,7 @@ LayerView layer_view(const tq_ctx* ctx, int layer);
 struct DecodePlan {
   int n_splits;        // history splits per (row, kv head); the ring is one extra split
   int pages_per_split;
+  int wide;            // 1: the split CTAs run the wide variant (two page streams, two CTAs per SM)
   size_t part_off, part_stride;  // per (row, kv head, split) partial
   size_t cnt_off;                // per (row, kv head) int32 arrival counters at offset 0, room for
                                  // max_seqs rows (left at zero by every call)
@@ -217,8 +218,9 @@ struct DecodePlan {
 // cnt_rows: rows the arrival counters have room for (at least max_seqs; prefill rows per query).
 DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows = 0, int ncol = kMaxG);
 
-// Split-K decode CTAs resident per SM for ctx's (head_dim, value_bits); sets kernel attributes once.
-int decode_resident_ctas(const tq_ctx* ctx);
+// Split-K decode CTAs resident per SM for ctx's (head_dim, value_bits), or for the wide variant (head_dim
+// 128, K3/V2: two streams, two CTAs per SM); sets kernel attributes once.
+int decode_resident_ctas(const tq_ctx* ctx, bool wide = false);
 // Largest dynamic shared memory of one CTA on sm_103 (227 KB).
 constexpr size_t kMaxSmemPerCta = 232448;
 // True when the query-pair (prefill) decode kernel of ctx's shape fits kMaxSmemPerCta.
