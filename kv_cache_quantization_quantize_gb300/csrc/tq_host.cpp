@@ -316,6 +316,8 @@ DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_r
     }
   }
   DecodePlan p;
+  p.px_off = 0;
+  p.px_pages = 0;
   p.wide = wide ? 1 : 0;
   p.pages_per_split = best_pps;
   p.n_splits = (max_pages + p.pages_per_split - 1) / p.pages_per_split;
@@ -630,11 +632,16 @@ static bool prefill_tc(const tq_ctx* ctx, int q_per_row) {
 
 // Workspace plan of the tcgen05 prefill: one query per row (4 columns), n_splits history partials from the
 // tensor-core kernel and the ring partial.
+// After the partials: every page of every (row, KV head), expanded once for all query tiles (kPxBytes each,
+// for the pages of a `max_ctx_hint`-token sequence).
 static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
   const int rows = batch * q_per_row;
   tq::DecodePlan p = tq::decode_plan(ctx, rows, max_ctx_hint, rows, tq::kMaxG);
   p.n_splits = tq::prefill_tc_splits(ctx, batch, q_per_row, max_ctx_hint);
-  p.bytes = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * (p.n_splits + 1), 256);
+  const int hint = (max_ctx_hint <= 0 || max_ctx_hint > ctx->cfg.max_ctx) ? ctx->cfg.max_ctx : max_ctx_hint;
+  p.px_pages = std::max(1, (hint + tq::kPage - 1) / tq::kPage);
+  p.px_off = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * (p.n_splits + 1), 1024);
+  p.bytes = align_up(p.px_off + tq::kPxBytes * (size_t)batch * ctx->cfg.n_kv_heads * p.px_pages, 256);
   return p;
 }
 

@@ -213,8 +213,14 @@ struct DecodePlan {
   size_t cnt_off;                // per (row, kv head) int32 arrival counters at offset 0, room for
                                  // max_seqs rows (left at zero by every call)
   size_t row_cnt_off;            // per row int32 counters of the decode step's units (left at zero)
+  size_t px_off;                 // tcgen05 prefill: expanded pages [row][KV head][px_pages][kPxBytes]
+  int px_pages;                  // pages per (row, KV head) in that region
   size_t bytes;
 };
+// One page of one KV head expanded for the tcgen05 prefill: the f16 B tiles of the h, l and QJL planes
+// (128 tokens x 128 coordinates) and V^T (128 coordinates x 128 tokens), 32 KB each in the tcgen05 128-byte
+// swizzled K-major layout, then n_t as fp32 [128].
+constexpr size_t kPxTileBytes = 32768, kPxBytes = 4 * kPxTileBytes + 512;
 // cnt_rows: rows the arrival counters have room for (at least max_seqs; prefill rows per query).
 DecodePlan decode_plan(const tq_ctx* ctx, int batch, int max_ctx_hint, int cnt_rows = 0, int ncol = kMaxG);
 

@@ -1,8 +1,9 @@
 // Prefill attention over the packed history on tcgen05 tensor cores (TurboQuant vLLM guide §七, first
 // item: prefill that reads the quantised cache; §三 hybrid estimator, §二 codes). A prefill chunk gives
-// every KV head n_q x G query rows against the same packed pages, so here the key operands are
-// expanded once per page and shared by a tile of 128 query rows (32 queries x the 4 query heads of one
-// KV head), instead of by the 8 query columns of the decode kernel's mma.sync path.
+// every KV head n_q x G query rows against the same packed pages. Here each page is expanded once per
+// launch (k_prefill_expand) into the f16 B tiles of the score and P.V MMAs, in the layout the tensor
+// cores read, and every tile of 128 query rows (32 queries x the 4 query heads of one KV head) copies
+// them into shared memory, instead of by the 8 query columns of the decode kernel's mma.sync path.
 //
 // One CTA = one tile, one KV head, one split of the tile's visible pages. It writes one partial per
 // (query, KV head, split) in the decode workspace's layout (m, l, o in the rotated basis, log2 units);
@@ -14,9 +15,7 @@
 //     A_hi + A_lo = lambda a_h q_rot (f16 hi + remainder), A_l = lambda a_l q_rot, A_qp = lambda kappa
 //     (S q_rot) (f16), B_h = B_l = +-1, B_s = +-gamma_t (gamma_t is stored as f16, so exactly),
 // so S = lambda (<q_rot, c[idx_t]> + kappa gamma_t <S q_rot, s_t>) up to the f16 rounding of the l and
-// QJL operands (as in the decode kernel), and the logit is S n_t scale / lambda. The MMAs run in three
-// groups (h, l, QJL) with a commit each, so the QJL plane and the values are expanded while the
-// remaining groups run. lambda, a power of two
+// QJL operands (as in the decode kernel), and the logit is S n_t scale / lambda. lambda, a power of two
 // per tile, keeps the operands inside the f16 range. P (f16) and the dequantised values V^T =
 // s_g (code - offset) (f16) feed the P.V MMA into a second TMEM accumulator; the softmax rescales it
 // lazily (only when a row maximum grows by more than 2^8).
@@ -37,17 +36,18 @@ std::atomic<int> g_pfault_polls{0};
 namespace {
 
 // 16 worker warps (warp w covers TMEM lanes 32 (w % 4).. and column quarter w / 4) and one more warp whose
-// lane 0 issues every MMA and polls the barriers
+// lane 0 issues every copy and MMA and polls the barriers
 constexpr int kPtWorkers = 512, kPtThreads = kPtWorkers + 32, kPtIssuer = kPtWorkers;
 constexpr int kPtQ = kPtWorkers / 128;  // column quarters: 32 columns (and 32 coordinates of a row) per thread
 // Shared memory (offsets from a 1024-byte aligned base): six 32 KB operand tiles that rotate through the
-// page pipeline (the h, l and QJL planes of the scores, V^T, and P over the h plane), two page stages, then
-// the per-token logit factors [2 pages][128], the per-warp operand maxima [16], the barriers and the TMEM
-// address.
-constexpr uint32_t kPtTileBytes = 32768, kPtSlots = 6, kPtStg = kPtSlots * kPtTileBytes;
-constexpr uint32_t kPtTail = 2 * 128 * 4 + 16 * 4 + 8 * 8 + 8;
-// barriers: S table, projection, page stages 0 / 1, score MMAs (QJL part), P.V MMAs, score MMAs (h and l part)
-enum { kBarTab = 0, kBarProj = 1, kBarPg = 2, kBarS = 4, kBarO = 5, kBarHL = 6, kNumBars = 7 };
+// page pipeline (the h, l and QJL planes of the scores, V^T, and P over the h plane), then n_t of the pages
+// in flight [2][128], the row exchange [4][128], the per-warp operand maxima [16], the barriers and the
+// TMEM address.
+constexpr uint32_t kPtTileBytes = (uint32_t)kPxTileBytes, kPtSlots = 6, kPtTail0 = kPtSlots * kPtTileBytes;
+constexpr uint32_t kPtTail = 2 * 128 * 4 + 4 * 128 * 4 + 16 * 4 + 8 * 8 + 8;
+// barriers: S table, projection, the h / l tiles and n_t of a page (two, by page parity), its QJL / V^T
+// tiles, score MMAs (QJL part; the h and l part has its own), P.V MMAs
+enum { kBarTab = 0, kBarProj = 1, kBarA = 2, kBarB = 4, kBarS = 5, kBarO = 6, kBarHL = 7, kNumBars = 8 };
 // TMEM (512 columns): scores S at 0, output O at 128, and from 256 the four f16 A tiles of the scores, 64
 // columns each: lambda a_h q_rot (f16 hi), its remainder, lambda a_l q_rot, lambda kappa S q_rot
 constexpr uint32_t kPtTmS = 0, kPtTmO = 128, kPtTmA = 256;
@@ -60,15 +60,16 @@ struct PrefillTcArgs {
   int qpr;                 // query slots per batch row
   float scale;             // softmax scale
   uint8_t* ws;
-  DecodePlan plan;         // partial layout; n_splits history splits + the ring partial
-  int fault_page;          // wait-timeout test hook: CTA (0, 0, 0) issues no copy of this page (-1: none)
-  uint32_t fault_polls;    // and gives up its wait for it after this many polls
+  DecodePlan plan;         // partial layout (n_splits history splits + the ring partial), expanded pages
+  int fault_page;          // wait-timeout test hook: CTA (0, 0, 0) issues no copy of this page's h / l tiles
+  uint32_t fault_polls;    // and gives up its wait for them after this many polls
 };
 
-__host__ __device__ constexpr size_t prefill_tc_smem(uint32_t page_bytes) {
-  return 1024 + kPtStg + 2 * ((page_bytes + 127) / 128 * 128) + kPtTail;
-}
-static_assert(prefill_tc_smem(15872) <= 232448, "K3/V4 pages fit the operand tiles' pipeline");
+constexpr size_t prefill_tc_smem() { return 1024 + kPtTail0 + kPtTail; }
+// the expansion kernel: one expanded page (kPxBytes), then the packed page (at most K3/V4's 15872 B) and
+// its barrier
+constexpr size_t prefill_expand_smem() { return 1024 + kPxBytes + 15872 + 16; }
+static_assert(prefill_tc_smem() <= 232448 && prefill_expand_smem() <= 232448, "shared memory");
 
 // Address of page pg of (slot, KV head h); a paged cache's page without a valid block reads block 0 and
 // is reported (TQ_DEV_ERR_BLOCK), as in the decode kernel.
@@ -167,10 +168,63 @@ __device__ __forceinline__ void pt_mma_ts_k128(uint32_t t_d, uint32_t t_a, uint3
   }
 }
 
+// One page of one KV head expanded for every query tile of the launch (grid: pages x KV heads x batch
+// rows): the packed page is copied in, its h, l and QJL planes and V^T are expanded into shared memory in
+// the tensor cores' layout, with n_t as fp32, and the kPxBytes go out to the workspace by bulk copies.
+template <int VB>
+__global__ void __launch_bounds__(kPtWorkers, 1) k_prefill_expand(PrefillTcArgs a) {
+  constexpr int D = 128, KB = 3;
+  constexpr float kVoff = VB == 2 ? 513.5f : 519.5f;  // 512 + the mid-rise offset 2^(VB-1) - 1/2
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  const LayerView& lv = a.lv;
+  const int tid = threadIdx.x, tk = tid & 127, hv = tid >> 7;
+  const int pg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const PageLayout pl = page_layout(D, VB, KB);
+  uint8_t* stg = sm + kPxBytes;  // the packed page
+  uint64_t* bar = reinterpret_cast<uint64_t*>(stg + 15872);
+  pdl_wait();  // pages and sequence state come from earlier work on the stream
+  pdl_launch();
+  const int slot = a.seq_ids[b];
+  if (slot < 0 || slot >= lv.max_seqs) return;
+  const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
+  const int P = (L > 0 ? kPage * ((L - 1) / kPage) : 0) + F;  // packed tokens
+  if (pg * kPage >= P) return;
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    mbar_expect_tx(bar, pl.bytes);
+    bulk_g2s(stg, pt_page(lv, slot, h, pg), pl.bytes, bar);
+  }
+  // thread 0 polls; the barrier makes the landed page visible to every thread
+  if (!__syncthreads_and(tid == 0 ? mbar_wait(bar, 0) : true)) {
+    if (tid == 0) {  // the copy may still land: wait again (bounded) before the CTA leaves its shared memory
+      set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
+      mbar_wait(bar, 0);
+    }
+    return;
+  }
+  const uint32_t* kw = reinterpret_cast<const uint32_t*>(stg + pl.kbits_off);
+  const uint32_t nw = reinterpret_cast<const uint32_t*>(stg + pl.norms_off)[tk];
+  if (hv == 0) reinterpret_cast<float*>(sm + 4 * kPxTileBytes)[tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu)));
+  pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, sm);                                   // h: +-1
+  pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, sm + kPxTileBytes);                    // l: +-1
+  pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, sm + 2 * kPxTileBytes);   // QJL: +-gamma_t
+  pt_expand_values<VB>(stg, pl, tk, hv, __floats2half2_rn(kVoff, kVoff), sm + 3 * kPxTileBytes);
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic-proxy writes -> the bulk copy
+  __syncthreads();
+  if (tid == 0) {
+    uint8_t* dst = a.ws + a.plan.px_off + (((size_t)b * lv.Hkv + h) * a.plan.px_pages + pg) * kPxBytes;
+    for (int i = 0; i < 4; ++i) bulk_s2g(dst + i * kPxTileBytes, sm + i * kPxTileBytes, (uint32_t)kPxTileBytes);
+    bulk_s2g(dst + 4 * kPxTileBytes, sm + 4 * kPxTileBytes, 512);
+    bulk_s2g_wait();  // written before the CTA leaves its shared memory
+  }
+}
+
 // HOOK: the instantiation with the wait-timeout test hook compiled in (launched only while it is set).
 template <int VB, bool HOOK>
 __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
-  constexpr int D = 128, KB = 3;
+  constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const LayerView& lv = a.lv;
@@ -178,22 +232,17 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const int tile = blockIdx.x, h = blockIdx.y;
   const int S = a.plan.n_splits;
   const int b = blockIdx.z / S, split = blockIdx.z % S;
-  const PageLayout pl = page_layout(D, VB, KB);
-  const uint32_t PB = pl.bytes, PBS = (pl.bytes + 127) / 128 * 128;
-  uint8_t* stg = sm + kPtStg;
-  float* ns = reinterpret_cast<float*>(stg + 2 * PBS);  // [2][128] logit factors n_t scale log2e / lambda, by page parity
-  float* bmax = ns + 256;                                 // [16] per-warp operand maxima
+  float* ns = reinterpret_cast<float*>(sm + kPtTail0);  // [2][128] n_t of the pages in flight, by page parity
+  float* xrow = ns + 256;                                // [4][128] row maxima / sums of the four quarters
+  float* bmax = xrow + 512;                              // [16] per-warp operand maxima
   uint64_t* bars = reinterpret_cast<uint64_t*>(bmax + 16);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 8);
   auto tile_at = [sm](int i) { return sm + i * kPtTileBytes; };
   // this thread's query row (TMEM lane) and column quarter: columns 32 ch .. 32 ch + 31
   const int r = 32 * (warp & 3) + lane, ch = warp >> 2;
   const int qi = r >> 2, g = r & 3, qidx = 32 * tile + qi;
-  // expansion roles: token / coordinate tk = tid % 128 and quarter hv = tid / 128 (a warp's 32 threads write
-  // 32 consecutive rows of a tile at the same chunk: conflict-free under the 128-byte swizzle)
-  const int tk = tid & 127, hv = tid >> 7;
   const bool worker = tid < kPtWorkers;
-  pdl_wait();  // sequence state, pages and queries come from earlier work on the stream
+  pdl_wait();  // sequence state, expanded pages and queries come from earlier work on the stream
   pdl_launch();
   const int slot = a.seq_ids[b], nq = a.n_q[b];
   const bool slot_ok = slot >= 0 && slot < lv.max_seqs;
@@ -206,7 +255,11 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   // packed tokens that query i sees (causal: every position up to its own, L - (nq - 1 - i) tokens)
   auto vis = [&](int i) { return (i < nq && i < a.qpr) ? min(P, max(0, L - (nq - 1 - i))) : 0; };
   const int i_last = min(32 * tile + 31, min(nq, a.qpr) - 1);
-  const int npg_tile = i_last >= 32 * tile ? (vis(i_last) + kPage - 1) / kPage : 0;
+  int npg_tile = i_last >= 32 * tile ? (vis(i_last) + kPage - 1) / kPage : 0;
+  if (npg_tile > a.plan.px_pages) {  // a max_ctx_hint below the row's length: the pages past it were not expanded
+    if (tid == 0 && split == 0) set_status(lv.status, TQ_DEV_ERR_SPLITS);
+    npg_tile = a.plan.px_pages;
+  }
   const int pps = (npg_tile + S - 1) / S;
   const int pg0 = min(npg_tile, split * pps), pg1 = min(npg_tile, pg0 + pps), n = pg1 - pg0;
   const int vis_r = vis(qidx);
@@ -227,23 +280,21 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     }
     return;
   }
-
-  // the wait-timeout test hook: a page whose copy is never issued (nor its byte count expected), so the wait
-  // for it gives up after a few polls
+  // this (row, KV head)'s expanded pages: page pg0 + k of the split at px(k)
+  const uint8_t* px0 = a.ws + a.plan.px_off + ((size_t)b * lv.Hkv + h) * a.plan.px_pages * kPxBytes;
+  auto px = [&](int k) { return px0 + (size_t)(pg0 + k) * kPxBytes; };
+  // the wait-timeout test hook: a page whose h / l tiles are never copied (nor their bytes expected), so the
+  // wait for them gives up after a few polls
   const int fpage = HOOK && (blockIdx.x | blockIdx.y | blockIdx.z) == 0 ? a.fault_page : -1;
   auto skip_copy = [fpage](int k) { return HOOK && k == fpage; };
   auto page_polls = [fpage, &a](int k) { return HOOK && k == fpage ? a.fault_polls : kWaitPolls; };
-  // ---- setup: barriers, TMEM (512 columns), the S table for the projection, the first two pages ----
-  if (tid == 0) {
+
+  // ---- setup: barriers, TMEM (512 columns), the S table for the projection ----
+  if (tid == kPtIssuer) {
     for (int i = 0; i < kNumBars; ++i) mbar_init(&bars[i], 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     mbar_expect_tx(&bars[kBarTab], 2u * D * D);
     bulk_g2s(tile_at(2), lv.S_sw, 2u * D * D, &bars[kBarTab]);
-    for (int k = 0; k < 2 && k < n; ++k) {
-      if (skip_copy(k)) continue;
-      mbar_expect_tx(&bars[kBarPg + k], PB);
-      bulk_g2s(stg + k * PBS, pt_page(lv, slot, h, pg0 + k), PB, &bars[kBarPg + k]);
-    }
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;\n" ::"r"(smem_u32(tslot))
@@ -289,22 +340,35 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tslot, t_s = tmem + kPtTmS, t_o = tmem + kPtTmO, t_a = tmem + kPtTmA;
   const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-  // per barrier, kept alike by every thread: the parity of the next phase to wait for (bit i of par) and
-  // the phases armed (a copy or an MMA batch that completes it) but not seen complete (2 bits i of pend),
-  // for the drain after a wait that gave up. Armed now: the S table and the first one or two pages.
-  uint32_t par = 0u, pend = (1u << (2 * kBarTab)) | (skip_copy(0) ? 0u : 1u << (2 * kBarPg)) |
-                            (n > 1 && !skip_copy(1) ? 1u << (2 * (kBarPg + 1)) : 0u);
+  // per barrier: the parity of the next phase to wait for (bit i of par) and the phases armed (a copy or an
+  // MMA batch that completes it) but not seen complete (2 bits i of pend), for the drain after a wait that
+  // gave up. Every thread keeps them alike for the barriers that all threads wait for; the copy barriers
+  // (kBarA, kBarB) only the issuing thread waits for and counts, and that thread runs the drain. Armed now:
+  // the S table.
+  uint32_t par = 0u, pend = 1u << (2 * kBarTab);
+  bool iss_ok = true;  // the issuing thread's own waits all succeeded
   auto arm = [&](int i) { pend += 1u << (2 * i); };
-  // Waits (bounded: `polls_i` polls for barrier i) for the oldest armed phase not seen yet of barrier i and,
-  // if j >= 0, of barrier j. The
+  // A wait of the issuing thread alone (the copies it issued); a failure reaches the others at the next
+  // block wait.
+  auto iss_wait = [&](int i, uint32_t polls) {
+    const bool w = iss_ok && mbar_wait(&bars[i], (par >> i) & 1u, polls);
+    if (w) {
+      par ^= 1u << i;
+      pend -= 1u << (2 * i);
+    }
+    iss_ok = w;
+    return w;
+  };
+  // Waits (bounded) for the oldest armed phase not seen yet of barrier i and, if j >= 0, of barrier j. The
   // issuing thread alone polls; the others wait at the block barrier, which keeps 500 pollers off the
   // shared-memory pipe that the tensor cores read their operands through (the try_wait acquire of the
   // poller and the barrier make the completed copy or MMA results visible to every thread). Every thread
   // gets the same answer.
-  auto wait_bars = [&](int i, int j, uint32_t polls_i = kWaitPolls) {
+  auto wait_bars = [&](int i, int j) {
     bool w = true;
     if (tid == kPtIssuer) {
-      if (i >= 0) w = mbar_wait(&bars[i], (par >> i) & 1u, polls_i);
+      w = iss_ok;
+      if (w && i >= 0) w = mbar_wait(&bars[i], (par >> i) & 1u);
       if (w && j >= 0) w = mbar_wait(&bars[j], (par >> j) & 1u);
     }
     w = __syncthreads_and(w) != 0;
@@ -389,94 +453,85 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
   }
   const float logit = a.scale * 1.4426950408889634f / lam;  // S n_t logit = score in log2 units
-  constexpr float kVoff = VB == 2 ? 513.5f : 519.5f;  // 512 + the mid-rise offset 2^(VB-1) - 1/2
-  const __half2 voff2 = __floats2half2_rn(kVoff, kVoff);
   tc_fence_before();
   __syncthreads();  // the A tiles are in TMEM; every qr read is done, so all six operand tiles are free
   // Page pipeline. Page k's h, l, QJL and V^T tiles sit in tiles sH, sL, sG, sV; f1 and f2 are free. The
-  // score MMAs of a page are issued in two parts: the h and l planes (24 MMAs) as soon as the previous
-  // page's softmax has read S, the QJL plane (8) once it is expanded. In iteration k:
-  //   - after a wait for page k + 1 and the previous P.V MMAs, the issuer copies page k + 2 into page k's
-  //     stage and issues the QJL part of page k's scores, while the workers expand page k + 1's h and l
-  //     planes into f1 and f2;
-  //   - the softmax of page k reads S; then the issuer issues the h and l part of page k + 1's scores while
-  //     the workers finish the softmax, with P (f16) over the h tile;
-  //   - the issuer issues the P.V MMAs while the workers expand page k + 1's QJL plane and values into the
-  //     l and QJL tiles of page k.
+  // issuing thread copies the expanded tiles in and issues the MMAs; the workers run the softmax. Page k's
+  // score MMAs run in two parts: the h and l planes (24 MMAs) as soon as page k - 1's softmax has read S,
+  // the QJL plane (8) right after page k - 1's P.V MMAs. The MMAs of one thread run in issue order, so S of
+  // page k is complete only after the P.V MMAs of page k - 1. In iteration k:
+  //   - once the previous P.V MMAs are done (f1, f2 free), the issuer copies page k + 1's h and l tiles
+  //     and n_t into f1, f2; everyone waits for page k's scores;
+  //   - the workers read S, exchange row maxima, then finish the softmax, with P (f16) over the h tile;
+  //     meanwhile the issuer copies page k + 1's QJL and V^T tiles into the l and QJL tiles of page k
+  //     (its scores are done) and issues page k + 1's h and l MMAs once their tiles have landed;
+  //   - the issuer issues the P.V MMAs of page k, then page k + 1's QJL MMAs once its QJL tile has landed.
   // The tiles then rotate: page k + 1 has h = f1, l = f2, QJL = sL, V = sG, and sH, sV (P and V of page k)
   // are free once the P.V MMAs have read them. The rotation has period 4 (page 0: h, l, QJL, V = tiles 0-3,
   // f1, f2 = 4, 5); tile_of reads role r's tile for page k from a table of 4-bit fields, one per k % 4.
   constexpr uint32_t kRoleH = 0x4040, kRoleL = 0x2351, kRoleG = 0x3512, kRoleV = 0x5123, kRoleF1 = 0x0404,
                      kRoleF2 = 0x1235;
   auto tile_of = [](uint32_t role, int k) { return (int)((role >> (4 * (k & 3))) & 7u); };
-  int sH = 0, sL = 1, sG = 2, sV = 3;
-  auto expand_hl = [&](const uint8_t* page, int parity, int th, int tl) {
-    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
-    const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
-    if (hv == 0) ns[128 * parity + tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu))) * logit;
-    pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, tile_at(th));
-    pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, tile_at(tl));
+  // copies of page k's h and l tiles with n_t (barrier kBarA + k % 2), and of its QJL and V^T tiles (kBarB)
+  auto copy_hl = [&](int k, int th, int tl) {
+    if (skip_copy(k)) return;
+    uint64_t* bar = &bars[kBarA + (k & 1)];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(bar, 2u * kPtTileBytes + 512u);
+    bulk_g2s(tile_at(th), px(k), kPtTileBytes, bar);
+    bulk_g2s(tile_at(tl), px(k) + kPxTileBytes, kPtTileBytes, bar);
+    bulk_g2s(ns + 128 * (k & 1), px(k) + 4 * kPxTileBytes, 512u, bar);
+    arm(kBarA + (k & 1));
   };
-  auto expand_gv = [&](const uint8_t* page, int tg, int tv) {
-    const uint32_t* kw = reinterpret_cast<const uint32_t*>(page + pl.kbits_off);
-    const uint32_t nw = reinterpret_cast<const uint32_t*>(page + pl.norms_off)[tk];
-    pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, tile_at(tg));  // +-gamma_t (f16 bits)
-    pt_expand_values<VB>(page, pl, tk, hv, voff2, tile_at(tv));
+  auto copy_gv = [&](int k, int tg, int tv) {
+    uint64_t* bar = &bars[kBarB];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(bar, 2u * kPtTileBytes);
+    bulk_g2s(tile_at(tg), px(k) + 2 * kPxTileBytes, kPtTileBytes, bar);
+    bulk_g2s(tile_at(tv), px(k) + 3 * kPxTileBytes, kPtTileBytes, bar);
+    arm(kBarB);
   };
-  // S = A_hi H + A_lo H + A_l L (issue_hl) + A_qp G (issue_g)
+  // S = A_hi H + A_lo H + A_l L (issue_hl, committed to kBarHL) + A_qp G (committed to kBarS)
   auto issue_hl = [&](int th, int tl) {
     tc_fence_after();
     pt_mma_ts_k128(t_s, t_a + 0, smem_u32(tile_at(th)), false);
     pt_mma_ts_k128(t_s, t_a + 64, smem_u32(tile_at(th)), true);
     pt_mma_ts_k128(t_s, t_a + 128, smem_u32(tile_at(tl)), true);
     umma_commit(&bars[kBarHL]);
+    arm(kBarHL);
   };
-  ok = ok && wait_bars(kBarPg, -1, page_polls(0));  // page 0
-  if (ok && worker) {
-    expand_hl(stg, 0, sH, sL);
-    expand_gv(stg, sG, sV);
+  // page 0's QJL MMAs (committed to kBarS)
+  auto issue_g = [&](int tg) {
+    tc_fence_after();
+    pt_mma_ts_k128(t_s, t_a + 192, smem_u32(tile_at(tg)), true);
+    umma_commit(&bars[kBarS]);
+    arm(kBarS);
+  };
+  if (ok && tid == kPtIssuer) {  // page 0's four tiles, page 1's h and l tiles; page 0's score MMAs
+    copy_hl(0, 0, 1);
+    copy_gv(0, 2, 3);
+    if (n > 1) copy_hl(1, 4, 5);
+    if (iss_wait(kBarA, page_polls(0))) issue_hl(0, 1);
+    if (iss_wait(kBarB, kWaitPolls)) issue_g(2);
   }
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-  tc_fence_before();
-  __syncthreads();
-  if (ok && tid == kPtIssuer) issue_hl(sH, sL);
-  if (ok) arm(kBarHL);
+  if (tid != kPtIssuer && ok) {  // (the issuer counts them only if issued)
+    arm(kBarHL);
+    arm(kBarS);
+  }
   float m_used = -INFINITY, l_loc = 0.f;
   for (int k = 0; k < n && ok; ++k) {
     const int pg = pg0 + k, st = k & 1;
-    sH = tile_of(kRoleH, k);
-    sL = tile_of(kRoleL, k);
-    sG = tile_of(kRoleG, k);
-    sV = tile_of(kRoleV, k);
-    const int f1 = tile_of(kRoleF1, k), f2 = tile_of(kRoleF2, k);
     const bool more = k + 1 < n;
-    const uint8_t* npage = stg + (st ^ 1) * PBS;  // page k + 1
-    // page k + 1 landed, and the previous P.V MMAs are done (f1, f2 free, O stable); the barrier also ends the
-    // previous iteration's expansions
-    if (more || k > 0) ok = wait_bars(more ? kBarPg + (st ^ 1) : -1, k > 0 ? kBarO : -1, page_polls(k + 1));
-    if (!ok) break;
-    if (tid == kPtIssuer) {
-      if (k + 2 < n && !skip_copy(k + 2)) {  // page k + 2 into page k's stage (its last readers finished before the barrier above)
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-        mbar_expect_tx(&bars[kBarPg + st], PB);
-        bulk_g2s(stg + st * PBS, pt_page(lv, slot, h, pg + 2), PB, &bars[kBarPg + st]);
-      }
-      tc_fence_after();
-      pt_mma_ts_k128(t_s, t_a + 192, smem_u32(tile_at(sG)), true);
-      umma_commit(&bars[kBarS]);
-    }
-    if (k + 2 < n && !skip_copy(k + 2)) arm(kBarPg + st);
-    arm(kBarS);
-    // ---- page k + 1's h and l planes into f1, f2 ----
-    if (more && worker) {
-      expand_hl(npage, st ^ 1, f1, f2);
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    }
+    const int sH = tile_of(kRoleH, k), sL = tile_of(kRoleL, k), sG = tile_of(kRoleG, k), sV = tile_of(kRoleV, k);
+    const int f1 = tile_of(kRoleF1, k), f2 = tile_of(kRoleF2, k);
+    // the previous P.V MMAs are done: f1, f2 are free (page 1's h and l tiles were copied before the loop).
+    // Every P.V batch is waited for here, the last page's predecessor too: a parity wait cannot tell a
+    // phase from the one two later, so no two phases of a barrier may complete unseen.
+    if (tid == kPtIssuer && k > 0 && iss_wait(kBarO, kWaitPolls) && more) copy_hl(k + 1, f1, f2);
     // ---- softmax of row r over tokens 32 ch .. 32 ch + 31 of page k ----
-    ok = wait_bars(kBarS, kBarHL);
+    ok = wait_bars(kBarS, kBarHL);  // page k's scores (and so the previous P.V MMAs) are complete
     if (!ok) break;
     tc_fence_after();
-    float* xrow = reinterpret_cast<float*>(tile_at(sL));  // [4][128] row maxima of the quarters (the l tile is read)
     uint32_t sv[32];
     float mx = -INFINITY;
     if (worker) {
@@ -486,7 +541,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 #pragma unroll
       for (int i4 = 0; i4 < 8; ++i4) {
         const float4 f = *reinterpret_cast<const float4*>(nsk + 32 * ch + 4 * i4);
-        const float fv[4] = {f.x, f.y, f.z, f.w};
+        const float fv[4] = {f.x * logit, f.y * logit, f.z * logit, f.w * logit};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int i = 4 * i4 + e, t = 32 * ch + i;
@@ -500,8 +555,11 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     }
     tc_fence_before();
     __syncthreads();  // S is read: the next page's h and l MMAs may overwrite it
-    if (more && tid == kPtIssuer) issue_hl(f1, f2);
-    if (more) arm(kBarHL);
+    if (tid == kPtIssuer && more) {
+      copy_gv(k + 1, sL, sG);  // page k's scores are done: its l and QJL tiles are free
+      if (iss_wait(kBarA + ((k + 1) & 1), page_polls(k + 1))) issue_hl(f1, f2);
+    }
+    if (tid != kPtIssuer && more) arm(kBarHL);
     if (worker) {
 #pragma unroll
       for (int q = 1; q < kPtQ; ++q) mx = fmaxf(mx, xrow[128 * ((ch + q) % kPtQ) + r]);
@@ -540,25 +598,21 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     }
     tc_fence_before();
     __syncthreads();
-    if (tid == kPtIssuer) {  // O += P V: A = P [rows x tokens] (over the h tile), B = V^T [coordinates x tokens]
+    if (tid == kPtIssuer && iss_ok) {  // O += P V: A = P [rows x tokens] (over the h tile), B = V^T
       tc_fence_after();
       pt_mma_k128(t_o, smem_u32(tile_at(sH)), smem_u32(tile_at(sV)), k > 0);
       umma_commit(&bars[kBarO]);  // (also covers the next page's h and l MMAs issued before)
+      arm(kBarO);
+      if (more && iss_wait(kBarB, kWaitPolls)) issue_g(sL);  // page k + 1's QJL tile sits in page k's l tile
     }
-    arm(kBarO);
-    // ---- page k + 1's QJL plane and values into the l and QJL tiles of page k (its scores are done) ----
-    if (more && worker) {  // (the next iteration's first wait is the barrier after these)
-      expand_gv(npage, sL, sG);
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      tc_fence_before();
-    }
+    if (tid != kPtIssuer && more) arm(kBarS);
   }
-  if (ok && ((pend >> (2 * kBarO)) & 3u)) ok = wait_bars(kBarO, -1);
+  // the last P.V batch (the issuing thread's wait, which the others learn of at the block barrier)
+  if (tid == kPtIssuer && ok && ((pend >> (2 * kBarO)) & 3u)) iss_wait(kBarO, kWaitPolls);
+  ok = __syncthreads_and(tid == kPtIssuer ? ok && iss_ok : ok) != 0;
   tc_fence_after();
   // ---- the partial of row r: m (log2 units), l, o (rotated basis, relative to m) ----
   __syncthreads();  // every thread has read the row maxima above
-  float* xrow = reinterpret_cast<float*>(tile_at(0));  // free: no MMA reads it any more (after a wait that
-                                                        // gave up, the partial written is empty anyway)
   if (worker) xrow[128 * ch + r] = l_loc;
   __syncthreads();
   float l_row = 0.f;
@@ -579,7 +633,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     part[g] = has ? m_used : -INFINITY;
     part[kMaxG + g] = has ? l_row : 0.f;
   }
-  if (!ok && tid == 0) {
+  if (!ok && tid == kPtIssuer) {
     // a wait gave up: nothing more is issued; wait (bounded) for every armed phase not seen complete - the
     // MMA batches before TMEM is freed, the copies before the CTA leaves its shared memory
     set_status(lv.status, TQ_DEV_ERR_TIMEOUT);
@@ -607,6 +661,18 @@ int prefill_tc_splits(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_h
   return std::max(1, std::min(max_pages, sms / std::max(1, ctas)));
 }
 
+template <int VB>
+cudaError_t launch_prefill_expand_k(const PrefillTcArgs& a, int batch, cudaStream_t s) {
+  constexpr size_t smem = prefill_expand_smem();
+  static bool attr = false;  // set once, outside any stream capture that follows
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_prefill_expand<VB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  return launch_pdl(k_prefill_expand<VB>, dim3(a.plan.px_pages, a.lv.Hkv, batch), dim3(kPtWorkers), smem, s, a);
+}
+
 template <int VB, bool HOOK>
 cudaError_t launch_prefill_tc_k(const PrefillTcArgs& a, dim3 grid, size_t smem, cudaStream_t s) {
   static bool attr = false;  // set once, outside any stream capture that follows
@@ -632,8 +698,10 @@ cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const
   a.fault_page = g_pfault_page.load();
   a.fault_polls = (uint32_t)g_pfault_polls.load();
   const dim3 grid((q_per_row + 31) / 32, a.lv.Hkv, batch * plan.n_splits);
-  const size_t smem = prefill_tc_smem(a.lv.page_bytes);
-  if (smem > kMaxSmemPerCta) return cudaErrorInvalidValue;
+  const size_t smem = prefill_tc_smem();
+  // every page of every row, expanded once for all query tiles
+  cudaError_t e = a.lv.vb == 2 ? launch_prefill_expand_k<2>(a, batch, s) : launch_prefill_expand_k<4>(a, batch, s);
+  if (e != cudaSuccess) return e;
   const bool hook = a.fault_page >= 0;
   return a.lv.vb == 2 ? (hook ? launch_prefill_tc_k<2, true>(a, grid, smem, s) : launch_prefill_tc_k<2, false>(a, grid, smem, s))
                       : (hook ? launch_prefill_tc_k<4, true>(a, grid, smem, s) : launch_prefill_tc_k<4, false>(a, grid, smem, s));
