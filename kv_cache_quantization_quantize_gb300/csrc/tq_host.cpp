@@ -640,6 +640,9 @@ static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_ro
   p.n_splits = tq::prefill_tc_splits(ctx, batch, q_per_row, max_ctx_hint);
   const int hint = (max_ctx_hint <= 0 || max_ctx_hint > ctx->cfg.max_ctx) ? ctx->cfg.max_ctx : max_ctx_hint;
   p.px_pages = std::max(1, (hint + tq::kPage - 1) / tq::kPage);
+  // the ring-only decode launch that follows runs one short CTA per (query, KV head): the wide decode
+  // variant (two CTAs per SM) where it exists (K3/V2, contiguous cache)
+  p.wide = ctx->cfg.value_bits == 2 && ctx->cfg.n_blocks == 0 ? 1 : 0;
   p.px_off = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * (p.n_splits + 1), 1024);
   p.bytes = align_up(p.px_off + tq::kPxBytes * (size_t)batch * ctx->cfg.n_kv_heads * p.px_pages, 256);
   return p;
