@@ -244,11 +244,14 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *   - d_workspace: at least tq_prefill_workspace_bytes(ctx, batch, q_per_row, max_ctx_hint) bytes,
  *     256-byte aligned; its arrival counters are zeroed by every call (one memset).
  *   - batch * q_per_row <= 65535.
- *   - Launches, head_dim 128 with key_bits 3, 4 query heads per KV head and q_per_row >= 32: a tcgen05 kernel over
- *     tiles of 128 query rows (32 queries x the 4 query heads of one KV head) that expands each page's
- *     key bits and values once per tile and computes scores and P.V on the tensor cores into TMEM,
- *     writing one partial per (query, KV head, history split); then a decode launch that runs only
- *     the exact ring split of each (query, KV head) and combines.
+ *   - Launches, head_dim 128 with key_bits 3, 4 query heads per KV head and q_per_row >= 32:
+ *       1. a kernel that expands every packed page of every (row, KV head) once, into f16 tensor-core
+ *          tiles in the workspace (128.5 KB per page and KV head, for the pages of max_ctx_hint tokens);
+ *       2. a tcgen05 kernel over tiles of 128 query rows (32 queries x the 4 query heads of one KV head)
+ *          that copies those tiles in and computes scores and P.V on the tensor cores into TMEM, writing
+ *          one partial per (query, KV head, history split);
+ *       3. a decode launch that runs only the exact ring split of each (query, KV head) and combines.
+ *     A row longer than max_ctx_hint sets TQ_DEV_ERR_SPLITS and leaves its pages past the hint out.
  *   - Other shapes: the memset and one split-K decode kernel over batch * q_per_row query rows (the
  *     rows of one sequence read the same pages, mostly from L2). With an even q_per_row and a
  *     contiguous cache, each CTA takes two adjacent query rows of a sequence in the MMAs' 8 query
@@ -306,8 +309,9 @@ tq_status tq_debug_append_wait_fault(int task, int polls);
 
 /* Test hook for the bounded waits of the tcgen05 prefill kernel (not part of the prefill itself). While
  * page >= 0, CTA (0, 0, 0) of every following tcgen05 prefill launch (query tile 0, KV head 0, batch row 0,
- * history split 0) issues neither the copy of the page with index `page` within its split nor that copy's
- * expected-byte count, and its wait for the page gives up after `polls` polls (1 .. 2^22). That CTA then
+ * history split 0) issues neither the copy of the expanded h and l tiles of the page with index `page`
+ * within its split nor that copy's expected-byte count, and its wait for them gives up after `polls` polls
+ * (1 .. 2^22). That CTA then
  * sets TQ_DEV_ERR_TIMEOUT, waits (bounded) for every copy and MMA batch it did issue, frees its tensor
  * memory and writes an empty partial: the outputs of its 32 queries x 4 query heads are unspecified, every
  * other output is as without the hook, and the context stays usable. A page index the CTA does not reach
