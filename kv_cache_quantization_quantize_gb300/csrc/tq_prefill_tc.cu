@@ -66,9 +66,10 @@ struct PrefillTcArgs {
 };
 
 constexpr size_t prefill_tc_smem() { return 1024 + kPtTail0 + kPtTail; }
-// the expansion kernel: one expanded page (kPxBytes), then the packed page (at most K3/V4's 15872 B) and
-// its barrier
-constexpr size_t prefill_expand_smem() { return 1024 + kPxBytes + 15872 + 16; }
+// the expansion kernel: half an expanded page (two tiles and n_t), then the packed page (at most K3/V4's
+// 15872 B) and its barrier
+constexpr size_t prefill_expand_smem() { return 1024 + 2 * kPxTileBytes + 512 + 15872 + 16; }
+static_assert(2 * (prefill_expand_smem() + 1024) <= 233472, "two expansion CTAs per SM");
 static_assert(prefill_tc_smem() <= 232448 && prefill_expand_smem() <= 232448, "shared memory");
 
 // Address of page pg of (slot, KV head h); a paged cache's page without a valid block reads block 0 and
@@ -168,20 +169,22 @@ __device__ __forceinline__ void pt_mma_ts_k128(uint32_t t_d, uint32_t t_a, uint3
   }
 }
 
-// One page of one KV head expanded for every query tile of the launch (grid: pages x KV heads x batch
-// rows): the packed page is copied in, its h, l and QJL planes and V^T are expanded into shared memory in
-// the tensor cores' layout, with n_t as fp32, and the kPxBytes go out to the workspace by bulk copies.
+// One page of one KV head expanded for every query tile of the launch (grid: 2 x pages, KV heads, batch
+// rows; CTA 2 p + half does half `half` of page p): the packed page is copied in; half 0 expands the h and
+// l planes with n_t as fp32, half 1 the QJL plane and V^T, into shared memory in the tensor cores' layout;
+// the bytes go out to the workspace by bulk copies. (Halves of 80 KB of shared memory let two CTAs share
+// an SM.)
 template <int VB>
-__global__ void __launch_bounds__(kPtWorkers, 1) k_prefill_expand(PrefillTcArgs a) {
+__global__ void __launch_bounds__(kPtWorkers, 2) k_prefill_expand(PrefillTcArgs a) {
   constexpr int D = 128, KB = 3;
   constexpr float kVoff = VB == 2 ? 513.5f : 519.5f;  // 512 + the mid-rise offset 2^(VB-1) - 1/2
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const LayerView& lv = a.lv;
   const int tid = threadIdx.x, tk = tid & 127, hv = tid >> 7;
-  const int pg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int pg = blockIdx.x >> 1, half = blockIdx.x & 1, h = blockIdx.y, b = blockIdx.z;
   const PageLayout pl = page_layout(D, VB, KB);
-  uint8_t* stg = sm + kPxBytes;  // the packed page
+  uint8_t* stg = sm + 2 * kPxTileBytes + 512;  // the packed page
   uint64_t* bar = reinterpret_cast<uint64_t*>(stg + 15872);
   pdl_wait();  // pages and sequence state come from earlier work on the stream
   pdl_launch();
@@ -206,17 +209,21 @@ __global__ void __launch_bounds__(kPtWorkers, 1) k_prefill_expand(PrefillTcArgs 
   }
   const uint32_t* kw = reinterpret_cast<const uint32_t*>(stg + pl.kbits_off);
   const uint32_t nw = reinterpret_cast<const uint32_t*>(stg + pl.norms_off)[tk];
-  if (hv == 0) reinterpret_cast<float*>(sm + 4 * kPxTileBytes)[tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu)));
-  pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, sm);                                   // h: +-1
-  pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, sm + kPxTileBytes);                    // l: +-1
-  pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, sm + 2 * kPxTileBytes);   // QJL: +-gamma_t
-  pt_expand_values<VB>(stg, pl, tk, hv, __floats2half2_rn(kVoff, kVoff), sm + 3 * kPxTileBytes);
+  if (half == 0) {
+    if (hv == 0) reinterpret_cast<float*>(sm + 2 * kPxTileBytes)[tk] = __half2float(__ushort_as_half((uint16_t)(nw & 0xffffu)));
+    pt_expand_plane(kw, 0, tk, hv, 0x3C003C00u, sm);                  // h: +-1
+    pt_expand_plane(kw, 1, tk, hv, 0x3C003C00u, sm + kPxTileBytes);   // l: +-1
+  } else {
+    pt_expand_plane(kw, 2, tk, hv, (nw >> 16) * 0x00010001u, sm);     // QJL: +-gamma_t
+    pt_expand_values<VB>(stg, pl, tk, hv, __floats2half2_rn(kVoff, kVoff), sm + kPxTileBytes);
+  }
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic-proxy writes -> the bulk copy
   __syncthreads();
   if (tid == 0) {
     uint8_t* dst = a.ws + a.plan.px_off + (((size_t)b * lv.Hkv + h) * a.plan.px_pages + pg) * kPxBytes;
-    for (int i = 0; i < 4; ++i) bulk_s2g(dst + i * kPxTileBytes, sm + i * kPxTileBytes, (uint32_t)kPxTileBytes);
-    bulk_s2g(dst + 4 * kPxTileBytes, sm + 4 * kPxTileBytes, 512);
+    bulk_s2g(dst + 2 * half * kPxTileBytes, sm, (uint32_t)kPxTileBytes);
+    bulk_s2g(dst + (2 * half + 1) * kPxTileBytes, sm + kPxTileBytes, (uint32_t)kPxTileBytes);
+    if (half == 0) bulk_s2g(dst + 4 * kPxTileBytes, sm + 2 * kPxTileBytes, 512);
     bulk_s2g_wait();  // written before the CTA leaves its shared memory
   }
 }
@@ -670,7 +677,7 @@ cudaError_t launch_prefill_expand_k(const PrefillTcArgs& a, int batch, cudaStrea
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  return launch_pdl(k_prefill_expand<VB>, dim3(a.plan.px_pages, a.lv.Hkv, batch), dim3(kPtWorkers), smem, s, a);
+  return launch_pdl(k_prefill_expand<VB>, dim3(2 * a.plan.px_pages, a.lv.Hkv, batch), dim3(kPtWorkers), smem, s, a);
 }
 
 template <int VB, bool HOOK>
