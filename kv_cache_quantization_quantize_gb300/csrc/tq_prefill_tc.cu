@@ -312,16 +312,25 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   float* qr = reinterpret_cast<float*>(tile_at(4));  // [128][128] fp32 q_rot (tiles 4-5 until the first page)
   const float rs = rsqrtf((float)D);
   float amax = 0.f;
-  for (int rr = warp; rr < 128 && worker; rr += kPtWorkers / 32) {
-    const int i = 32 * tile + (rr >> 2), gg = rr & 3;
+  constexpr int kRowStep = kPtWorkers / 32, kWarpRows = 128 / kRowStep;  // warp w: rows w, w + 16, ...
+  uint16_t qraw[kWarpRows][4];  // every row's loads in flight before the first row's transform
+  float dsg[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) dsg[e] = worker ? lv.D[4 * lane + e] : 0.f;
+#pragma unroll
+  for (int u = 0; u < kWarpRows; ++u) {
+    const int rr = warp + u * kRowStep, i = 32 * tile + (rr >> 2), gg = rr & 3;
+    const bool live = worker && i < nq && i < a.qpr && slot_ok;
+    const uint16_t* src = a.q + (((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + gg) * D + 4 * lane;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) qraw[u][e] = live ? src[e] : (uint16_t)0;
+  }
+#pragma unroll
+  for (int u = 0; u < kWarpRows && worker; ++u) {
+    const int rr = warp + u * kRowStep;
     float x[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = 4 * lane + e;
-      x[e] = (i < nq && i < a.qpr && slot_ok)
-                 ? bf16_to_f32(a.q[(((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + gg) * D + j]) * lv.D[j]
-                 : 0.f;
-    }
+    for (int e = 0; e < 4; ++e) x[e] = bf16_to_f32(qraw[u][e]) * dsg[e];
     warp_fwht<4>(x, lane);
     uint32_t hb[2], lb[2];
 #pragma unroll
@@ -391,6 +400,25 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     }
     return w;
   };
+  // copies of page k's h and l tiles with n_t (barrier kBarA + k % 2), and of its QJL and V^T tiles (kBarB)
+  auto copy_hl = [&](int k, int th, int tl) {
+    if (skip_copy(k)) return;
+    uint64_t* bar = &bars[kBarA + (k & 1)];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(bar, 2u * kPtTileBytes + 512u);
+    bulk_g2s(tile_at(th), px(k), kPtTileBytes, bar);
+    bulk_g2s(tile_at(tl), px(k) + kPxTileBytes, kPtTileBytes, bar);
+    bulk_g2s(ns + 128 * (k & 1), px(k) + 4 * kPxTileBytes, 512u, bar);
+    arm(kBarA + (k & 1));
+  };
+  auto copy_gv = [&](int k, int tg, int tv) {
+    uint64_t* bar = &bars[kBarB];
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    mbar_expect_tx(bar, 2u * kPtTileBytes);
+    bulk_g2s(tile_at(tg), px(k) + 2 * kPxTileBytes, kPtTileBytes, bar);
+    bulk_g2s(tile_at(tv), px(k) + 3 * kPxTileBytes, kPtTileBytes, bar);
+    arm(kBarB);
+  };
   bool ok = wait_bars(kBarTab, -1);  // S table landed
   if (ok) {  // projection q_proj = S q_rot into TMEM columns [0, 128): A = q_rot hi, lo (bf16)
     if (tid == kPtIssuer) {
@@ -405,6 +433,11 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     }
     arm(kBarProj);
     ok = wait_bars(kBarProj, -1);
+  }
+  // the projection has read tiles 0-2 (tile 3 was free): page 0's tiles land while the A tiles are built
+  if (ok && tid == kPtIssuer) {
+    copy_hl(0, 0, 1);
+    copy_gv(0, 2, 3);
   }
   tc_fence_after();
   // operand scale lambda: the largest of |a_h q_rot|, |a_l q_rot| and |kappa q_proj| maps to [2^12, 2^13)
@@ -479,25 +512,6 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   constexpr uint32_t kRoleH = 0x4040, kRoleL = 0x2351, kRoleG = 0x3512, kRoleV = 0x5123, kRoleF1 = 0x0404,
                      kRoleF2 = 0x1235;
   auto tile_of = [](uint32_t role, int k) { return (int)((role >> (4 * (k & 3))) & 7u); };
-  // copies of page k's h and l tiles with n_t (barrier kBarA + k % 2), and of its QJL and V^T tiles (kBarB)
-  auto copy_hl = [&](int k, int th, int tl) {
-    if (skip_copy(k)) return;
-    uint64_t* bar = &bars[kBarA + (k & 1)];
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    mbar_expect_tx(bar, 2u * kPtTileBytes + 512u);
-    bulk_g2s(tile_at(th), px(k), kPtTileBytes, bar);
-    bulk_g2s(tile_at(tl), px(k) + kPxTileBytes, kPtTileBytes, bar);
-    bulk_g2s(ns + 128 * (k & 1), px(k) + 4 * kPxTileBytes, 512u, bar);
-    arm(kBarA + (k & 1));
-  };
-  auto copy_gv = [&](int k, int tg, int tv) {
-    uint64_t* bar = &bars[kBarB];
-    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-    mbar_expect_tx(bar, 2u * kPtTileBytes);
-    bulk_g2s(tile_at(tg), px(k) + 2 * kPxTileBytes, kPtTileBytes, bar);
-    bulk_g2s(tile_at(tv), px(k) + 3 * kPxTileBytes, kPtTileBytes, bar);
-    arm(kBarB);
-  };
   // S = A_hi H + A_lo H + A_l L (issue_hl, committed to kBarHL) + A_qp G (committed to kBarS)
   auto issue_hl = [&](int th, int tl) {
     tc_fence_after();
@@ -514,9 +528,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     umma_commit(&bars[kBarS]);
     arm(kBarS);
   };
-  if (ok && tid == kPtIssuer) {  // page 0's four tiles, page 1's h and l tiles; page 0's score MMAs
-    copy_hl(0, 0, 1);
-    copy_gv(0, 2, 3);
+  if (ok && tid == kPtIssuer) {  // page 1's h and l tiles (the A tiles have read qr); page 0's score MMAs
     if (n > 1) copy_hl(1, 4, 5);
     if (iss_wait(kBarA, page_polls(0))) issue_hl(0, 1);
     if (iss_wait(kBarB, kWaitPolls)) issue_g(2);
@@ -626,15 +638,35 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 #pragma unroll
   for (int q = 0; q < kPtQ; ++q) l_row += worker ? xrow[128 * q + r] : 0.f;
   const bool has = ok && m_used != -INFINITY;  // this row saw a token
-  if (worker) {
-    uint32_t ov[32];
-    if (ok) tmem_ld32(t_o + lane_base + 32 * ch, ov);  // warp-wide (ok is the same in every thread)
+  if (ok) {
+    // O through shared memory (tiles 0-2 are free: every copy and MMA was seen complete), rows padded to
+    // 132 floats so that eight rows' float4 stores meet eight bank quads; then warp w stores rows w, w + 16,
+    // ..., a whole 512-byte row per store
+    float* ost = reinterpret_cast<float*>(sm);
+    if (worker) {
+      uint32_t ov[32];
+      tmem_ld32(t_o + lane_base + 32 * ch, ov);
 #pragma unroll
-    for (int i4 = 0; i4 < 8 && row_out; ++i4)
-      *reinterpret_cast<float4*>(part + 2 * kMaxG + g * D + 32 * ch + 4 * i4) =
-          has ? make_float4(__uint_as_float(ov[4 * i4]), __uint_as_float(ov[4 * i4 + 1]),
-                            __uint_as_float(ov[4 * i4 + 2]), __uint_as_float(ov[4 * i4 + 3]))
-              : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int i4 = 0; i4 < 8; ++i4)
+        *reinterpret_cast<float4*>(ost + r * 132 + 32 * ch + 4 * i4) =
+            has ? make_float4(__uint_as_float(ov[4 * i4]), __uint_as_float(ov[4 * i4 + 1]),
+                              __uint_as_float(ov[4 * i4 + 2]), __uint_as_float(ov[4 * i4 + 3]))
+                : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncthreads();
+    for (int rr = warp; rr < 128 && worker; rr += kPtWorkers / 32) {
+      const int qx = 32 * tile + (rr >> 2);
+      if (qx >= a.qpr) continue;
+      float* pr = reinterpret_cast<float*>(a.ws + a.plan.part_off +
+                                           ((((size_t)b * a.qpr + qx) * lv.Hkv + h) * (S + 1) + split) *
+                                               a.plan.part_stride);
+      *reinterpret_cast<float4*>(pr + 2 * kMaxG + (rr & 3) * D + 4 * lane) =
+          *reinterpret_cast<const float4*>(ost + rr * 132 + 4 * lane);
+    }
+  } else if (row_out) {  // a wait gave up (copies may still land in shared memory): an empty O
+#pragma unroll
+    for (int i4 = 0; i4 < 8; ++i4)
+      *reinterpret_cast<float4*>(part + 2 * kMaxG + g * D + 32 * ch + 4 * i4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   if (row_out && ch == 0) {
     part[g] = has ? m_used : -INFINITY;
