@@ -746,7 +746,7 @@ def measure_prefill(tqm, synth, dev, Tq, force_cc, reps, warm=3):
                                    f"{ctx}-token sequence", "layers": L_layers},
             "path": ("tcgen05: tiles of 32 queries x 4 heads; query operands in TMEM, key planes and values "
                      "expanded once per page and tile into rotating shared-memory tiles while the previous "
-                     "MMAs run, scores and P.V into TMEM; then a ring-only decode launch") if tc
+                     "MMAs run, scores and P.V into TMEM; then the exact ring split and the combine, one CTA per (query, KV head)") if tc
             else "one split-K decode launch over chunk-query rows (causal length per row)",
             "device_status": status}
 

@@ -250,7 +250,8 @@ tq_status tq_decode_phase(tq_ctx* ctx, int phase, int layer, const void* q, floa
  *       2. a tcgen05 kernel over tiles of 128 query rows (32 queries x the 4 query heads of one KV head)
  *          that copies those tiles in and computes scores and P.V on the tensor cores into TMEM, writing
  *          one partial per (query, KV head, history split);
- *       3. a decode launch that runs only the exact ring split of each (query, KV head) and combines.
+ *       3. a kernel with one CTA per (query, KV head): the exact ring split of the ring tokens that the
+ *          query sees, the log-sum-exp merge of the history partials, the inverse rotation, the merge.
  *     A row longer than max_ctx_hint sets TQ_DEV_ERR_SPLITS and leaves its pages past the hint out.
  *   - Other shapes: the memset and one split-K decode kernel over batch * q_per_row query rows (the
  *     rows of one sequence read the same pages, mostly from L2). With an even q_per_row and a

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(decode_threads<D, WIDE>(), (D == 256 && VB == 
   constexpr int NG = D / 32;
   extern __shared__ __align__(128) uint8_t smem[];
   const LayerView& lv = a.lv;
-  const int sp = a.ring_only ? a.plan.n_splits : (int)blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int sp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int stream = warp / SW, tg = warp & 3, hf = (warp % SW) >> 2;
   const int nsp = a.plan.n_splits;
@@ -588,7 +588,7 @@ cudaError_t launch_decode_dv(const DecodeArgs& a, int batch, int phase, cudaStre
     if (e != cudaSuccess) return e;
   }
   if (phase < 0 || phase == 1) {
-    const dim3 grid(a.ring_only ? 1 : a.plan.n_splits + 1, a.lv.Hkv, batch);
+    const dim3 grid(a.plan.n_splits + 1, a.lv.Hkv, batch);
     if constexpr (D == 128 && VB == 2 && KB == 3) {
       if (a.plan.wide && qp == 1 && !a.lv.btab) {  // decode_plan chose the two-CTAs-per-SM variant
         if (decode_setup_wide() < 0) return cudaErrorInvalidValue;
@@ -647,8 +647,7 @@ int decode_resident_ctas(const tq_ctx* ctx, bool wide) {
 
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr,
-                          const int32_t* n_q, int qp, const void* k_new, const void* v_new, int new_dt, int late_state,
-                          int ring_only) {
+                          const int32_t* n_q, int qp, const void* k_new, const void* v_new, int new_dt, int late_state) {
   if (qp == 2 && (qpr % 2 != 0 || ctx->cfg.n_blocks > 0)) return cudaErrorInvalidValue;
   DecodeArgs a;
   a.lv = layer_view(ctx, layer);
@@ -666,7 +665,6 @@ cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* ou
   a.v_new = v_new;
   a.new_dt = new_dt;
   a.late_state = late_state;
-  a.ring_only = ring_only;
   const int d = ctx->cfg.head_dim, vb = ctx->cfg.value_bits, kb = ctx->cfg.key_bits;
   if (kb == 4) {
     if (d == 64) return launch_decode_dv<64, 4, 4>(a, batch, phase, s, qp);

@@ -34,9 +34,6 @@ struct DecodeArgs {
   // state and may code a page after it released its dependents; this launch then reads the state and
   // pages only after its stream wait.
   int late_state;
-  // 1: the history partials 0 .. n_splits - 1 of every (row, KV head) were written by the tensor-core
-  // prefill kernel; this launch runs only the ring split of each unit (grid x = 1) and combines at once.
-  int ring_only;
 };
 
 namespace {
@@ -807,9 +804,7 @@ template <int D, int NT, int QP = 1>
 __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, float* scratch, bool smem_ok = true) {
   __shared__ int s_last;
   __syncthreads();  // every thread's part of the partial is written
-  if (a.ring_only) {
-    if (threadIdx.x == 0) s_last = 1;  // the only CTA of its unit: the other partials are complete
-  } else if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) {
     // acq_rel at gpu scope: releases this CTA's partial (ordered before by the barrier) and, in the
     // last CTA, acquires every other CTA's
     int* cnt = reinterpret_cast<int*>(a.ws + a.plan.cnt_off) + b * a.lv.Hkv + h;

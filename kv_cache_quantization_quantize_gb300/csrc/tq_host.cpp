@@ -631,7 +631,7 @@ static bool prefill_tc(const tq_ctx* ctx, int q_per_row) {
 }
 
 // Workspace plan of the tcgen05 prefill: one query per row (4 columns), n_splits history partials from the
-// tensor-core kernel and the ring partial.
+// tensor-core kernel (the ring split runs inside the combine kernel and keeps its part in registers).
 // After the partials: every page of every (row, KV head), expanded once for all query tiles (kPxBytes each,
 // for the pages of a `max_ctx_hint`-token sequence).
 static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint) {
@@ -640,10 +640,7 @@ static tq::DecodePlan prefill_tc_plan(const tq_ctx* ctx, int batch, int q_per_ro
   p.n_splits = tq::prefill_tc_splits(ctx, batch, q_per_row, max_ctx_hint);
   const int hint = (max_ctx_hint <= 0 || max_ctx_hint > ctx->cfg.max_ctx) ? ctx->cfg.max_ctx : max_ctx_hint;
   p.px_pages = std::max(1, (hint + tq::kPage - 1) / tq::kPage);
-  // the ring-only decode launch that follows runs one short CTA per (query, KV head): the wide decode
-  // variant (two CTAs per SM) where it exists (K3/V2, contiguous cache)
-  p.wide = ctx->cfg.value_bits == 2 && ctx->cfg.n_blocks == 0 ? 1 : 0;
-  p.px_off = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * (p.n_splits + 1), 1024);
+  p.px_off = align_up(p.part_off + p.part_stride * (size_t)rows * ctx->cfg.n_kv_heads * p.n_splits, 1024);
   p.bytes = align_up(p.px_off + tq::kPxBytes * (size_t)batch * ctx->cfg.n_kv_heads * p.px_pages, 256);
   return p;
 }
@@ -683,13 +680,10 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
       return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
     const cudaStream_t s = (cudaStream_t)stream;
-    // Both kernels read the sequence state after their stream wait; the ring-only decode launch needs no
-    // arrival counters (each of its CTAs is the only one of its unit).
+    // Every kernel reads the sequence state after its stream wait; none uses arrival counters.
     tq::step_follows(ctx, layer, s);
-    cudaError_t e = tq::launch_prefill_tc(ctx, layer, q, d_seq_ids, d_n_q, batch, q_per_row, scale, d_workspace, plan, s);
-    if (e == cudaSuccess)
-      e = tq::launch_decode(ctx, layer, q, out, d_seq_ids, batch * q_per_row, scale, d_workspace, plan, 1, s, q_per_row,
-                            d_n_q, 1, nullptr, nullptr, 0, 0, 1);
+    const cudaError_t e =
+        tq::launch_prefill_tc(ctx, layer, q, d_seq_ids, d_n_q, batch, q_per_row, scale, d_workspace, plan, out, s);
     return e == cudaSuccess ? ok() : cuda_fail(e, "prefill attention kernels");
   }
   const int qp = prefill_qp(ctx, q_per_row), cta_rows = batch * q_per_row / qp;

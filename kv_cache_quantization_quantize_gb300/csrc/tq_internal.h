@@ -246,9 +246,10 @@ cudaError_t launch_reset(const tq_ctx* ctx, int layer, const int32_t* seq_ids, i
 cudaError_t launch_decode(const tq_ctx* ctx, int layer, const void* q, float* out, const int32_t* seq_ids,
                           int batch, float scale, void* ws, const DecodePlan& plan, int phase, cudaStream_t s, int qpr = 1,
                           const int32_t* n_q = nullptr, int qp = 1, const void* k_new = nullptr,
-                          const void* v_new = nullptr, int new_dt = 0, int late_state = 0, int ring_only = 0);
+                          const void* v_new = nullptr, int new_dt = 0, int late_state = 0);
 // Prefill attention on tcgen05 (head_dim 128, key_bits 3, 4 query heads per KV head): the history
-// partials of every (query, KV head), n_splits per unit, into the workspace in the decode's layout.
+// partials of every (query, KV head), n_splits per unit, into the workspace in the decode's layout; then
+// the exact ring split and the combine of every (query, KV head) into out.
 bool prefill_tc_eligible(const tq_ctx* ctx);
 int prefill_tc_splits(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_hint);
 // Packed tokens [t0, t0 + count) of (layer, slot, KV head h) dequantised to fp32 k_hat, v_hat [count][d]
@@ -256,7 +257,8 @@ int prefill_tc_splits(const tq_ctx* ctx, int batch, int q_per_row, int max_ctx_h
 cudaError_t launch_dequantize(const tq_ctx* ctx, int layer, int slot, int h, int t0, int count, int with_qjl,
                               float* k_out, float* v_out, cudaStream_t s);
 cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const int32_t* seq_ids, const int32_t* n_q,
-                              int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, cudaStream_t s);
+                              int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, float* out,
+                              cudaStream_t s);
 // Decode launches read a row's state (and the pages it implies) before their stream wait. That is safe
 // after every launch of this library except a decode step of the same layer on the same stream (it
 // publishes the state at its end). step_follows() says whether the last launch of ctx on stream s was

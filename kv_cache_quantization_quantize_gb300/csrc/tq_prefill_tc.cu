@@ -7,7 +7,7 @@
 //
 // One CTA = one tile, one KV head, one split of the tile's visible pages. It writes one partial per
 // (query, KV head, split) in the decode workspace's layout (m, l, o in the rotated basis, log2 units);
-// a ring-only launch of the decode kernel then adds the exact ring tokens and combines.
+// k_prefill_ring then adds the exact ring tokens and combines, one small CTA per (query, KV head).
 //
 // Scores, with the odd-symmetric 2-bit codebook c[idx] = a_h (2 h - 1) + a_l (2 l - 1) and the QJL
 // sign s = 2 sigma - 1, are one fp32 accumulator in TMEM:
@@ -60,7 +60,7 @@ struct PrefillTcArgs {
   int qpr;                 // query slots per batch row
   float scale;             // softmax scale
   uint8_t* ws;
-  DecodePlan plan;         // partial layout (n_splits history splits + the ring partial), expanded pages
+  DecodePlan plan;         // partial layout (n_splits history splits per unit), expanded pages
   int fault_page;          // wait-timeout test hook: CTA (0, 0, 0) issues no copy of this page's h / l tiles
   uint32_t fault_polls;    // and gives up its wait for them after this many polls
 };
@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const int vis_w = __reduce_min_sync(0xffffffffu, (unsigned)vis_r);
   const bool row_out = worker && qidx < a.qpr;  // a virtual row of the launch (padding rows get an empty partial)
   float* part = row_out ? reinterpret_cast<float*>(a.ws + a.plan.part_off +
-                                                   ((((size_t)b * a.qpr + qidx) * lv.Hkv + h) * (S + 1) + split) *
+                                                   ((((size_t)b * a.qpr + qidx) * lv.Hkv + h) * S + split) *
                                                        a.plan.part_stride)
                         : nullptr;
   if (n == 0) {  // nothing visible in this split: empty partials (m = -inf, l = 0, o = 0)
@@ -658,7 +658,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
       const int qx = 32 * tile + (rr >> 2);
       if (qx >= a.qpr) continue;
       float* pr = reinterpret_cast<float*>(a.ws + a.plan.part_off +
-                                           ((((size_t)b * a.qpr + qx) * lv.Hkv + h) * (S + 1) + split) *
+                                           ((((size_t)b * a.qpr + qx) * lv.Hkv + h) * S + split) *
                                                a.plan.part_stride);
       *reinterpret_cast<float4*>(pr + 2 * kMaxG + (rr & 3) * D + 4 * lane) =
           *reinterpret_cast<const float4*>(ost + rr * 132 + 4 * lane);
@@ -683,6 +683,147 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   __syncthreads();
   tc_fence_after();
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;\n" ::"r"(tmem) : "memory");
+}
+
+// The third launch: for each (query, KV head), the exact ring split and the combine. The ring tokens the
+// query sees (positions P .. its own) are bf16 K and V rows of the ring, attended exactly in fp32 in the
+// original basis (TurboQuant vLLM guide, §五.1: the recent tokens kept unquantised; §三: the hybrid decode
+// merges both parts). The history partials of the tile kernel's splits (m in log2 units, l, o in the rotated
+// basis relative to m) merge by log-sum-exp, o goes back through Pi^T = diag(D) H / sqrt(d), and the two
+// parts merge exactly. One CTA per (query, KV head): warp g takes query head g of the group, lane l holds
+// coordinates 4 l .. 4 l + 3. Queries past n_q, and rows with an invalid sequence id, get zeros.
+__global__ void __launch_bounds__(32 * kMaxG, 6) k_prefill_ring(PrefillTcArgs a, float* out) {
+  constexpr int D = 128;
+  const LayerView& lv = a.lv;
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const int i = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  __shared__ float qs[kMaxG][D];
+  pdl_wait();  // the partials of the tile kernel (and the state, ring and queries of earlier work)
+  pdl_launch();
+  // the history partials first: their loads depend on nothing else (every row < q_per_row has them)
+  const int S = a.plan.n_splits;
+  const size_t stride = a.plan.part_stride / sizeof(float);
+  const float* base = reinterpret_cast<const float*>(a.ws + a.plan.part_off +
+                                                     (((size_t)b * a.qpr + i) * lv.Hkv + h) * S *
+                                                         a.plan.part_stride);
+  float ms[2], ls[2];  // splits lane and lane + 32 (S <= 64)
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int sp = lane + 32 * u;
+    ms[u] = sp < S ? __ldcg(base + sp * stride + g) : -INFINITY;
+    ls[u] = sp < S ? __ldcg(base + sp * stride + kMaxG + g) : 0.f;
+  }
+  constexpr int kPre = 8;  // the first splits' o rows, in flight with the loads above
+  float4 opre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    opre[u] = u < S ? __ldcg(reinterpret_cast<const float4*>(base + u * stride + 2 * kMaxG + g * D + 4 * lane))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+  float* dst = out + (((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + g) * D + 4 * lane;
+  const int slot = a.seq_ids[b], nq = a.n_q[b];
+  if (i >= nq || slot < 0 || slot >= lv.max_seqs) {
+    *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
+  const int P = (L > 0 ? kPage * ((L - 1) / kPage) : 0) + F;  // packed tokens read through their codes
+  const int n = max(0, L - (nq - 1 - i)) - P;                  // ring tokens this query sees (<= 128)
+  // ---- ring split: scores of tokens lane, lane + 32, ...; P.V over this lane's four coordinates ----
+  float m_r = -INFINITY, l_r = 0.f, o_r[4] = {0.f, 0.f, 0.f, 0.f};
+  if (n > 0) {
+    const uint16_t* qrow = a.q + (((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + g) * D + 4 * lane;
+    const uint2 qw = *reinterpret_cast<const uint2*>(qrow);
+    qs[g][4 * lane + 0] = __uint_as_float(qw.x << 16);
+    qs[g][4 * lane + 1] = __uint_as_float(qw.x & 0xffff0000u);
+    qs[g][4 * lane + 2] = __uint_as_float(qw.y << 16);
+    qs[g][4 * lane + 3] = __uint_as_float(qw.y & 0xffff0000u);
+    __syncwarp();
+    const uint16_t* rk = lv.ring + ((size_t)slot * lv.Hkv + h) * 2 * kPage * D + (size_t)F * D;
+    const uint16_t* rv = rk + (size_t)kPage * D;
+    const float s2 = a.scale * 1.4426950408889634f;  // scores in log2 units
+    float sc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = lane + 32 * u;
+      float acc = 0.f;
+      if (t < n) {
+        const uint4* krow = reinterpret_cast<const uint4*>(rk + (size_t)t * D);
+#pragma unroll 4
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 kw = krow[c];
+          const float4 q0 = *reinterpret_cast<const float4*>(&qs[g][8 * c]);
+          const float4 q1 = *reinterpret_cast<const float4*>(&qs[g][8 * c + 4]);
+          acc = fmaf(q0.x, __uint_as_float(kw.x << 16), acc);
+          acc = fmaf(q0.y, __uint_as_float(kw.x & 0xffff0000u), acc);
+          acc = fmaf(q0.z, __uint_as_float(kw.y << 16), acc);
+          acc = fmaf(q0.w, __uint_as_float(kw.y & 0xffff0000u), acc);
+          acc = fmaf(q1.x, __uint_as_float(kw.z << 16), acc);
+          acc = fmaf(q1.y, __uint_as_float(kw.z & 0xffff0000u), acc);
+          acc = fmaf(q1.z, __uint_as_float(kw.w << 16), acc);
+          acc = fmaf(q1.w, __uint_as_float(kw.w & 0xffff0000u), acc);
+        }
+      }
+      sc[u] = t < n ? acc * s2 : -INFINITY;
+    }
+    m_r = warp_max(fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3])));
+    float pl = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      sc[u] = lane + 32 * u < n ? exp2f(sc[u] - m_r) : 0.f;
+      pl += sc[u];
+    }
+    l_r = warp_sum(pl);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (32 * u >= n) break;  // (n is the same in every lane)
+#pragma unroll 16
+      for (int tt = 0; tt < 32; ++tt) {
+        const float pt = __shfl_sync(0xffffffffu, sc[u], tt);  // 0 past n
+        const uint2 vw = *reinterpret_cast<const uint2*>(rv + (size_t)min(32 * u + tt, n - 1) * D + 4 * lane);
+        o_r[0] = fmaf(pt, __uint_as_float(vw.x << 16), o_r[0]);
+        o_r[1] = fmaf(pt, __uint_as_float(vw.x & 0xffff0000u), o_r[1]);
+        o_r[2] = fmaf(pt, __uint_as_float(vw.y << 16), o_r[2]);
+        o_r[3] = fmaf(pt, __uint_as_float(vw.y & 0xffff0000u), o_r[3]);
+      }
+    }
+  }
+  // ---- the history splits: weights 2^(m_s - m) with m their maximum ----
+  const float m = warp_max(fmaxf(ms[0], ms[1]));
+  float wl = 0.f;
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    ms[u] = ms[u] == -INFINITY ? 0.f : exp2f(ms[u] - m);  // the split's weight
+    wl = fmaf(ms[u], ls[u], wl);
+  }
+  const float l = warp_sum(wl);
+  float o[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const float w = __shfl_sync(0xffffffffu, ms[0], u);  // 0 past S
+    o[0] = fmaf(w, opre[u].x, o[0]);
+    o[1] = fmaf(w, opre[u].y, o[1]);
+    o[2] = fmaf(w, opre[u].z, o[2]);
+    o[3] = fmaf(w, opre[u].w, o[3]);
+  }
+#pragma unroll 8
+  for (int sp = kPre; sp < S; ++sp) {
+    const float w = __shfl_sync(0xffffffffu, sp < 32 ? ms[0] : ms[1], sp & 31);
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(base + sp * stride + 2 * kMaxG + g * D + 4 * lane));
+    o[0] = fmaf(w, v.x, o[0]);
+    o[1] = fmaf(w, v.y, o[1]);
+    o[2] = fmaf(w, v.z, o[2]);
+    o[3] = fmaf(w, v.w, o[3]);
+  }
+  // Pi^T o = D * (H o) / sqrt(d), then the exact merge with the ring
+  warp_fwht<4>(o, lane);
+  const float rs = rsqrtf((float)D);
+  const float mm = fmaxf(m, m_r);
+  const float fh = m == -INFINITY ? 0.f : exp2f(m - mm), fr = m_r == -INFINITY ? 0.f : exp2f(m_r - mm);
+  const float den = fh * l + fr * l_r, inv = den > 0.f ? 1.f / den : 0.f;
+  float r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) r[e] = (fh * o[e] * rs * lv.D[4 * lane + e] + fr * o_r[e]) * inv;
+  *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
 }
 
 }  // namespace
@@ -739,7 +880,8 @@ cudaError_t launch_prefill_tc_k(const PrefillTcArgs& a, dim3 grid, size_t smem, 
 }
 
 cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const int32_t* seq_ids, const int32_t* n_q,
-                              int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, cudaStream_t s) {
+                              int batch, int q_per_row, float scale, void* ws, const DecodePlan& plan, float* out,
+                              cudaStream_t s) {
   PrefillTcArgs a;
   a.lv = layer_view(ctx, layer);
   a.q = static_cast<const uint16_t*>(q);
@@ -757,8 +899,11 @@ cudaError_t launch_prefill_tc(const tq_ctx* ctx, int layer, const void* q, const
   cudaError_t e = a.lv.vb == 2 ? launch_prefill_expand_k<2>(a, batch, s) : launch_prefill_expand_k<4>(a, batch, s);
   if (e != cudaSuccess) return e;
   const bool hook = a.fault_page >= 0;
-  return a.lv.vb == 2 ? (hook ? launch_prefill_tc_k<2, true>(a, grid, smem, s) : launch_prefill_tc_k<2, false>(a, grid, smem, s))
-                      : (hook ? launch_prefill_tc_k<4, true>(a, grid, smem, s) : launch_prefill_tc_k<4, false>(a, grid, smem, s));
+  e = a.lv.vb == 2 ? (hook ? launch_prefill_tc_k<2, true>(a, grid, smem, s) : launch_prefill_tc_k<2, false>(a, grid, smem, s))
+                   : (hook ? launch_prefill_tc_k<4, true>(a, grid, smem, s) : launch_prefill_tc_k<4, false>(a, grid, smem, s));
+  if (e != cudaSuccess) return e;
+  // the ring split and the combine of every (query, KV head)
+  return launch_pdl(k_prefill_ring, dim3(q_per_row, a.lv.Hkv, batch), dim3(32 * kMaxG), 0, s, a, out);
 }
 
 }  // namespace tq
