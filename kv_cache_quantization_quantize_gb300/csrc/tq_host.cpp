@@ -680,7 +680,8 @@ tq_status tq_prefill_attention(tq_ctx* ctx, int layer, const void* q, float* out
       return fail(TQ_ERR_INVALID_ARG, "workspace_bytes %zu < %zu", workspace_bytes, plan.bytes);
     const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / std::sqrt((float)ctx->cfg.head_dim);
     const cudaStream_t s = (cudaStream_t)stream;
-    // Every kernel reads the sequence state after its stream wait; none uses arrival counters.
+    // The expansion and combine kernels read the sequence state after their stream wait, the tile kernel
+    // before it (what it reads was complete when the expansion passed its wait). None uses arrival counters.
     tq::step_follows(ctx, layer, s);
     const cudaError_t e =
         tq::launch_prefill_tc(ctx, layer, q, d_seq_ids, d_n_q, batch, q_per_row, scale, d_workspace, plan, out, s);

@@ -249,8 +249,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
   const int r = 32 * (warp & 3) + lane, ch = warp >> 2;
   const int qi = r >> 2, g = r & 3, qidx = 32 * tile + qi;
   const bool worker = tid < kPtWorkers;
-  pdl_wait();  // sequence state, expanded pages and queries come from earlier work on the stream
-  pdl_launch();
+  // The stream wait comes only before the first page copy: the sequence state, the queries and the tables
+  // come from work before the expansion kernel, which was complete when that kernel passed its own wait
+  // (and started this one). The setup below overlaps the expansion's last CTAs.
   const int slot = a.seq_ids[b], nq = a.n_q[b];
   const bool slot_ok = slot >= 0 && slot < lv.max_seqs;
   int P = 0, L = 0;
@@ -434,6 +435,8 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     arm(kBarProj);
     ok = wait_bars(kBarProj, -1);
   }
+  pdl_wait();  // the expanded pages
+  pdl_launch();
   // the projection has read tiles 0-2 (tile 3 was free): page 0's tiles land while the A tiles are built
   if (ok && tid == kPtIssuer) {
     copy_hl(0, 0, 1);
