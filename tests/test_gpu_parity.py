@@ -529,3 +529,49 @@ def test_decode_wait_timeout_is_reported_and_the_workspace_stays_usable():
                 assert rel_l2(out[i, hq], refs[i][hq]) <= 2e-3, ("after", stage, i, hq)
     assert lib.tq_debug_decode_wait_fault(7, 8) == _abi.TQ_ERR_INVALID_ARG
     assert lib.tq_debug_decode_wait_fault(0, 0) == _abi.TQ_ERR_INVALID_ARG
+
+
+def test_prefill_tcgen05_after_a_ring_flush_and_an_invalid_row():
+    """The tcgen05 prefill where the ring's first F tokens were coded by a flush: 300 tokens, a flush (256
+    packed + a 44-token ring block coded in full, F = 44), then a 70-token chunk (L = 370, ring tokens
+    [44, 114) exact). Chunk queries before position 300 see only packed tokens; the rest see a growing part
+    of the ring, read from ring row F on. A second batch row names slot -1 (invalid): its outputs are zero,
+    and the valid row's outputs agree with the ones of a call without it."""
+    d, vb, Hkv, G, slot = 128, 2, 2, 4, 1
+    cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
+                 max_ctx=640, seed=61)
+    cache = TurboQuantCache(cfg)
+    tables = _oracle_tables(cache)
+    k, v = synth.kv_tokens(370, Hkv, d, seed=6100, outliers=("random", 4, 10.0))
+    cache.append(0, k[None, :300].to(DEV).contiguous(), v[None, :300].to(DEV).contiguous(), _i32([slot]),
+                 _i32([300]))
+    cache.flush(0, _i32([slot]))
+    cache.append(0, k[None, 300:].to(DEV).contiguous(), v[None, 300:].to(DEV).contiguous(), _i32([slot]),
+                 _i32([70]))
+    torch.cuda.synchronize()
+    assert cache.check_status() == 0
+    L, F = cache.state(0, slot)
+    Np, R = oracle.history_split(L)
+    assert (L, F, Np, R) == (370, 44, 256, 114)
+    nq = 70
+    q = synth.queries(2 * nq, Hkv * G, d, seed=6101).view(2, nq, Hkv * G, d).contiguous()
+    out = cache.prefill(0, q.to(DEV), _i32([slot, -1]), _i32([nq, nq])).cpu().numpy()
+    alone = cache.prefill(0, q[:1].contiguous().to(DEV), _i32([slot]), _i32([nq])).cpu().numpy()
+    assert np.all(out[1] == 0)
+    assert np.allclose(out[0], alone[0], rtol=1e-5, atol=1e-7)  # (the split count may differ with the batch)
+    D, S, c, _ = tables
+    P = Np + F
+    worst = 0.0
+    for h in range(Hkv):
+        kr, vr = cache.records(0, slot, h, P)
+        keys = oracle.unpack_key_records(kr, d, cfg.key_bits)
+        vals = oracle.unpack_value_records(vr, d, vb)
+        rk, rv = cache.ring(0, slot, h)
+        ref = oracle.prefill_attention(_f64(q[0, :, h * G:(h + 1) * G]), keys, vals, _f64(rk[F:R]), _f64(rv[F:R]),
+                                       L, D, S, c)
+        for j in range(nq):
+            for g in range(G):
+                err = rel_l2(out[0, j, h * G + g], ref[j, g])
+                worst = max(worst, err)
+                assert err <= 2e-3, (j, h, g, err)
+    print(f"tcgen05 prefill after a flush: worst rel-L2 {worst:.2e}")
