@@ -426,9 +426,18 @@ def test_prefill_tcgen05_long_history(vb, paged):
     print(f"tcgen05 against CUDA-core prefill: worst rel-L2 {diff:.2e}")
 
 
+
+@pytest.mark.parametrize("hist,chunk,max_ctx", [(3000, 40, 4096), (8000, 32, 8192)])
+def test_prefill_tcgen05_many_history_splits(hist, chunk, max_ctx):
+    """Few query tiles over a long history give many history splits: 2 x 2 tiles of 32 pages take 32 splits
+    of one page, and 1 x 2 tiles of 64 pages take 64 (the most the combine takes). The combine then merges
+    more partials than it loads ahead, and (at 64) weights held in a second register per lane."""
+    _prefill_chunk_case(128, 2, 3, (chunk,), 4, [hist], max_ctx=max_ctx)
+
 def _prefill_chunk_case(d, vb, kbits, chunk, G, hist, paged=False, max_ctx=640):
     Hkv = 2
-    hist, chunk, slots = list(hist), list(chunk), [1, 0]
+    hist, chunk = list(hist), list(chunk)
+    slots = [1, 0][:len(hist)]
     B, Tq = len(hist), max(chunk)
     max_pages = (max_ctx + 127) // 128
     cfg = config(head_dim=d, value_bits=vb, n_layers=1, n_kv_heads=Hkv, n_q_heads=Hkv * G, max_seqs=2,
