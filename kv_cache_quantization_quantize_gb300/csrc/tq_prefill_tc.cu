@@ -693,9 +693,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 // original basis (TurboQuant vLLM guide, §五.1: the recent tokens kept unquantised; §三: the hybrid decode
 // merges both parts). The history partials of the tile kernel's splits (m in log2 units, l, o in the rotated
 // basis relative to m) merge by log-sum-exp, o goes back through Pi^T = diag(D) H / sqrt(d), and the two
-// parts merge exactly. One CTA per (query, KV head): warp g takes query head g of the group, lane l holds
+// parts merge exactly. One CTA per (query, KV head): warp g ends with query head g of the group, lane l with
 // coordinates 4 l .. 4 l + 3. Queries past n_q, and rows with an invalid sequence id, get zeros.
-__global__ void __launch_bounds__(32 * kMaxG, 6) k_prefill_ring(PrefillTcArgs a, float* out) {
+__global__ void __launch_bounds__(32 * kMaxG, 4) k_prefill_ring(PrefillTcArgs a, float* out) {
   constexpr int D = 128;
   const LayerView& lv = a.lv;
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
@@ -731,63 +731,108 @@ __global__ void __launch_bounds__(32 * kMaxG, 6) k_prefill_ring(PrefillTcArgs a,
   const int L = lv.state[2 * slot], F = lv.state[2 * slot + 1];
   const int P = (L > 0 ? kPage * ((L - 1) / kPage) : 0) + F;  // packed tokens read through their codes
   const int n = max(0, L - (nq - 1 - i)) - P;                  // ring tokens this query sees (<= 128)
-  // ---- ring split: scores of tokens lane, lane + 32, ...; P.V over this lane's four coordinates ----
+  // ---- ring split (n is the same in the whole CTA). Thread t scores ring token t for the four heads;
+  // warp w takes tokens 32 w .. 32 w + 31 of P.V for the four heads over this lane's coordinates, and
+  // warp g then sums head g's four parts. ----
   float m_r = -INFINITY, l_r = 0.f, o_r[4] = {0.f, 0.f, 0.f, 0.f};
   if (n > 0) {
-    const uint16_t* qrow = a.q + (((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + g) * D + 4 * lane;
-    const uint2 qw = *reinterpret_cast<const uint2*>(qrow);
-    qs[g][4 * lane + 0] = __uint_as_float(qw.x << 16);
-    qs[g][4 * lane + 1] = __uint_as_float(qw.x & 0xffff0000u);
-    qs[g][4 * lane + 2] = __uint_as_float(qw.y << 16);
-    qs[g][4 * lane + 3] = __uint_as_float(qw.y & 0xffff0000u);
-    __syncwarp();
+    __shared__ float ps[kMaxG][kPage];      // p_t of each head
+    __shared__ float red[2][kMaxG][kMaxG];  // per-warp maxima, then sums, of each head
+    __shared__ float4 ored[kMaxG][kMaxG][32];  // [warp][head][lane] parts of P.V
+    const int t = threadIdx.x;
+    {
+      const uint16_t* qrow = a.q + (((size_t)b * a.qpr + i) * lv.Hq + h * kMaxG + g) * D + 4 * lane;
+      const uint2 qw = *reinterpret_cast<const uint2*>(qrow);
+      qs[g][4 * lane + 0] = __uint_as_float(qw.x << 16);
+      qs[g][4 * lane + 1] = __uint_as_float(qw.x & 0xffff0000u);
+      qs[g][4 * lane + 2] = __uint_as_float(qw.y << 16);
+      qs[g][4 * lane + 3] = __uint_as_float(qw.y & 0xffff0000u);
+    }
+    __syncthreads();
     const uint16_t* rk = lv.ring + ((size_t)slot * lv.Hkv + h) * 2 * kPage * D + (size_t)F * D;
     const uint16_t* rv = rk + (size_t)kPage * D;
     const float s2 = a.scale * 1.4426950408889634f;  // scores in log2 units
-    float sc[4];
+    float sc[kMaxG] = {0.f, 0.f, 0.f, 0.f};
+    if (t < n) {
+      const uint4* krow = reinterpret_cast<const uint4*>(rk + (size_t)t * D);
+      constexpr int KH = D / 16;  // the row in two halves of 8 chunks: half the registers in flight
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int t = lane + 32 * u;
-      float acc = 0.f;
-      if (t < n) {
-        const uint4* krow = reinterpret_cast<const uint4*>(rk + (size_t)t * D);
-#pragma unroll 4
-        for (int c = 0; c < D / 8; ++c) {
-          const uint4 kw = krow[c];
-          const float4 q0 = *reinterpret_cast<const float4*>(&qs[g][8 * c]);
-          const float4 q1 = *reinterpret_cast<const float4*>(&qs[g][8 * c + 4]);
-          acc = fmaf(q0.x, __uint_as_float(kw.x << 16), acc);
-          acc = fmaf(q0.y, __uint_as_float(kw.x & 0xffff0000u), acc);
-          acc = fmaf(q0.z, __uint_as_float(kw.y << 16), acc);
-          acc = fmaf(q0.w, __uint_as_float(kw.y & 0xffff0000u), acc);
-          acc = fmaf(q1.x, __uint_as_float(kw.z << 16), acc);
-          acc = fmaf(q1.y, __uint_as_float(kw.z & 0xffff0000u), acc);
-          acc = fmaf(q1.z, __uint_as_float(kw.w << 16), acc);
-          acc = fmaf(q1.w, __uint_as_float(kw.w & 0xffff0000u), acc);
+      for (int hk = 0; hk < 2; ++hk) {
+        uint4 kw[KH];
+#pragma unroll
+        for (int u = 0; u < KH; ++u) kw[u] = krow[KH * hk + u];
+#pragma unroll
+        for (int u = 0; u < KH; ++u) {
+          const int c = KH * hk + u;
+          const float k8[8] = {__uint_as_float(kw[u].x << 16), __uint_as_float(kw[u].x & 0xffff0000u),
+                               __uint_as_float(kw[u].y << 16), __uint_as_float(kw[u].y & 0xffff0000u),
+                               __uint_as_float(kw[u].z << 16), __uint_as_float(kw[u].z & 0xffff0000u),
+                               __uint_as_float(kw[u].w << 16), __uint_as_float(kw[u].w & 0xffff0000u)};
+#pragma unroll
+          for (int gg = 0; gg < kMaxG; ++gg) {
+            const float4 q0 = *reinterpret_cast<const float4*>(&qs[gg][8 * c]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&qs[gg][8 * c + 4]);
+            float acc = sc[gg];
+            acc = fmaf(q0.x, k8[0], acc);
+            acc = fmaf(q0.y, k8[1], acc);
+            acc = fmaf(q0.z, k8[2], acc);
+            acc = fmaf(q0.w, k8[3], acc);
+            acc = fmaf(q1.x, k8[4], acc);
+            acc = fmaf(q1.y, k8[5], acc);
+            acc = fmaf(q1.z, k8[6], acc);
+            acc = fmaf(q1.w, k8[7], acc);
+            sc[gg] = acc;
+          }
         }
       }
-      sc[u] = t < n ? acc * s2 : -INFINITY;
     }
-    m_r = warp_max(fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3])));
-    float pl = 0.f;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      sc[u] = lane + 32 * u < n ? exp2f(sc[u] - m_r) : 0.f;
-      pl += sc[u];
+    for (int gg = 0; gg < kMaxG; ++gg) {
+      sc[gg] = t < n ? sc[gg] * s2 : -INFINITY;
+      const float wm = warp_max(sc[gg]);
+      if (lane == 0) red[0][g][gg] = wm;
     }
-    l_r = warp_sum(pl);
+    __syncthreads();
+    float mh[kMaxG];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      if (32 * u >= n) break;  // (n is the same in every lane)
+    for (int gg = 0; gg < kMaxG; ++gg) {
+      mh[gg] = fmaxf(fmaxf(red[0][0][gg], red[0][1][gg]), fmaxf(red[0][2][gg], red[0][3][gg]));
+      const float p = t < n ? exp2f(sc[gg] - mh[gg]) : 0.f;
+      ps[gg][t] = p;
+      const float ws = warp_sum(p);
+      if (lane == 0) red[1][g][gg] = ws;
+    }
+    __syncthreads();
+    m_r = mh[g];
+    l_r = (red[1][0][g] + red[1][1][g]) + (red[1][2][g] + red[1][3][g]);
+    float4 op[kMaxG];
+#pragma unroll
+    for (int gg = 0; gg < kMaxG; ++gg) op[gg] = make_float4(0.f, 0.f, 0.f, 0.f);
+    const int t1 = min(n, 32 * g + 32);  // this warp's tokens 32 g .. t1 - 1
 #pragma unroll 16
-      for (int tt = 0; tt < 32; ++tt) {
-        const float pt = __shfl_sync(0xffffffffu, sc[u], tt);  // 0 past n
-        const uint2 vw = *reinterpret_cast<const uint2*>(rv + (size_t)min(32 * u + tt, n - 1) * D + 4 * lane);
-        o_r[0] = fmaf(pt, __uint_as_float(vw.x << 16), o_r[0]);
-        o_r[1] = fmaf(pt, __uint_as_float(vw.x & 0xffff0000u), o_r[1]);
-        o_r[2] = fmaf(pt, __uint_as_float(vw.y << 16), o_r[2]);
-        o_r[3] = fmaf(pt, __uint_as_float(vw.y & 0xffff0000u), o_r[3]);
+    for (int tt = 32 * g; tt < t1; ++tt) {
+      const uint2 vw = *reinterpret_cast<const uint2*>(rv + (size_t)tt * D + 4 * lane);
+      const float v0 = __uint_as_float(vw.x << 16), v1 = __uint_as_float(vw.x & 0xffff0000u);
+      const float v2 = __uint_as_float(vw.y << 16), v3 = __uint_as_float(vw.y & 0xffff0000u);
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        const float p = ps[gg][tt];
+        op[gg].x = fmaf(p, v0, op[gg].x);
+        op[gg].y = fmaf(p, v1, op[gg].y);
+        op[gg].z = fmaf(p, v2, op[gg].z);
+        op[gg].w = fmaf(p, v3, op[gg].w);
       }
+    }
+#pragma unroll
+    for (int gg = 0; gg < kMaxG; ++gg) ored[g][gg][lane] = op[gg];
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kMaxG; ++w) {
+      const float4 v = ored[w][g][lane];
+      o_r[0] += v.x;
+      o_r[1] += v.y;
+      o_r[2] += v.z;
+      o_r[3] += v.w;
     }
   }
   // ---- the history splits: weights 2^(m_s - m) with m their maximum ----
