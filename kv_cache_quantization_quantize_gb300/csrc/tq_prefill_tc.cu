@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
   }
   // ---- query rows: q_rot = Pi q (warp-per-row FWHT), bf16 hi / lo for the projection, fp32 copy ----
-  float* qr = reinterpret_cast<float*>(tile_at(4));  // [128][128] fp32 q_rot (tiles 4-5 until the first page)
+  // [128][128] fp32 q_rot (tiles 4-5 until the first page); column j of row r at j ^ (r mod 32), so that the
+  // row-per-thread reads of the A tiles meet 32 banks
+  float* qr = reinterpret_cast<float*>(tile_at(4));
   const float rs = rsqrtf((float)D);
   float amax = 0.f;
   constexpr int kRowStep = kPtWorkers / 32, kWarpRows = 128 / kRowStep;  // warp w: rows w, w + 16, ...
@@ -337,7 +339,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       x[e] *= rs;
-      qr[rr * D + 4 * lane + e] = x[e];
+      qr[rr * D + ((4 * lane + e) ^ (rr & 31))] = x[e];
       amax = fmaxf(amax, fabsf(x[e]));
     }
 #pragma unroll
@@ -478,7 +480,7 @@ __global__ void __launch_bounds__(kPtThreads, 1) k_prefill_tc(PrefillTcArgs a) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int j = (32 * ch + 2 * i) & (D - 1);  // (the issuing warp's values are not stored)
-      const float q0 = qr[r * D + j], q1 = qr[r * D + j + 1];
+      const float q0 = qr[r * D + (j ^ (r & 31))], q1 = qr[r * D + ((j + 1) ^ (r & 31))];
       const float x0 = lam * w_h * q0, x1 = lam * w_h * q1;
       const __half2 hi = __floats2half2_rn(x0, x1);
       const float2 hf = __half22float2(hi);
