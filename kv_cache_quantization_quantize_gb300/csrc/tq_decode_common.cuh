@@ -778,7 +778,6 @@ __device__ __forceinline__ void zero_unit_out(const DecodeArgs& a, int b, int h)
 // after all of its CTAs arrived, and they read the state before arriving. The per-row counters follow
 // the per-unit ones in the workspace and are left at zero.
 __device__ __noinline__ void row_arrive(const DecodeArgs& a, int b) {
-  if (threadIdx.x != 0) return;
   int* rc = reinterpret_cast<int*>(a.ws + a.plan.row_cnt_off) + b;
   int old;
   asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;\n" : "=r"(old) : "l"(rc) : "memory");
@@ -815,9 +814,13 @@ __device__ __noinline__ void finish_unit(const DecodeArgs& a, int b, int h, floa
   }
   __syncthreads();
   if (!s_last) return;
+  // The row's arrival does not depend on the merge: the first thread after the merging warps takes it while
+  // they merge (the merge has no block barrier).
+  constexpr int kArriveTid = 32 * qcols<QP>();
+  static_assert(QP != 1 || NT > kArriveTid, "a thread outside the merging warps");
+  if (QP == 1 && a.k_new && threadIdx.x == kArriveTid) row_arrive(a, b);
   if (!smem_ok) zero_unit_out<D, NT, QP>(a, b, h);
   else combine_unit<D, NT, QP>(a, b, h, scratch);
-  if (QP == 1 && a.k_new) row_arrive(a, b);
 }
 
 }  // namespace
