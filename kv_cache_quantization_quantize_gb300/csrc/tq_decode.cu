@@ -436,7 +436,8 @@ __global__ void __launch_bounds__(decode_threads<D, WIDE>(), (D == 256 && VB == 
   const int grp = 4 * stream + tg;
   float* wm = reinterpret_cast<float*>(stage0);  // [NGRP][NCOL query columns]
   float* wl = wm + NCOL * NGRP;                  // [NGRP][NCOL]
-  float* wo = wl + NCOL * NGRP;                  // [NGRP][NCOL][D]
+  float* wo = wl + NCOL * NGRP;                  // [NGRP][NCOL][D + 4] (rows padded: the c lanes meet other banks)
+  constexpr int WS = D + 4;
   {
     float l0 = l_acc[0], l1 = l_acc[1];
 #pragma unroll
@@ -454,37 +455,30 @@ __global__ void __launch_bounds__(decode_threads<D, WIDE>(), (D == 256 && VB == 
 #pragma unroll
       for (int mt = 0; mt < 2 * QG; ++mt) {
         const int j0 = CW * hf + 16 * mt + g;
-        wo[(grp * NCOL + 2 * c) * D + j0] = O[mt][0];
-        wo[(grp * NCOL + 2 * c + 1) * D + j0] = O[mt][1];
-        wo[(grp * NCOL + 2 * c) * D + j0 + 8] = O[mt][2];
-        wo[(grp * NCOL + 2 * c + 1) * D + j0 + 8] = O[mt][3];
+        wo[(grp * NCOL + 2 * c) * WS + j0] = O[mt][0];
+        wo[(grp * NCOL + 2 * c + 1) * WS + j0] = O[mt][1];
+        wo[(grp * NCOL + 2 * c) * WS + j0 + 8] = O[mt][2];
+        wo[(grp * NCOL + 2 * c + 1) * WS + j0 + 8] = O[mt][3];
       }
     }
   }
   __syncthreads();
-  float* wf = wo + NGRP * NCOL * D;  // [NGRP][NCOL] group weights exp2(m_group - m)
-  if (tid < NCOL * NGRP) {
-    const int hd = tid % NCOL, w = tid / NCOL;
-    float m = -INFINITY;
-#pragma unroll
-    for (int v = 0; v < NGRP; ++v) m = fmaxf(m, wm[v * NCOL + hd]);
-    const float mw = wm[w * NCOL + hd];
-    wf[w * NCOL + hd] = (m == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - m);
-  }
-  __syncthreads();
+  // each output element takes the groups' maximum and weights exp2(m_group - m) itself (no third barrier)
   for (int i = tid; i < NCOL * D; i += NT) {
     const int hd = i / D, j = i % D;
-    float o = 0.f;
+    float m = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < NGRP; ++w) o = fmaf(wf[w * NCOL + hd], wo[(w * NCOL + hd) * D + j], o);
+    for (int w = 0; w < NGRP; ++w) m = fmaxf(m, wm[w * NCOL + hd]);
+    float o = 0.f, l = 0.f;
+#pragma unroll
+    for (int w = 0; w < NGRP; ++w) {
+      const float mw = wm[w * NCOL + hd];
+      const float f = (m == -INFINITY || mw == -INFINITY) ? 0.f : exp2f(mw - m);
+      o = fmaf(f, wo[(w * NCOL + hd) * WS + j], o);
+      l = fmaf(f, wl[w * NCOL + hd], l);
+    }
     part[2 * NCOL + hd * D + j] = o;
     if (j == 0) {
-      float m = -INFINITY, l = 0.f;
-#pragma unroll
-      for (int w = 0; w < NGRP; ++w) {
-        m = fmaxf(m, wm[w * NCOL + hd]);
-        l = fmaf(wf[w * NCOL + hd], wl[w * NCOL + hd], l);
-      }
       part[hd] = m;
       part[NCOL + hd] = l;
     }
@@ -503,7 +497,7 @@ size_t decode_smem_bytes() {
   constexpr int NT = decode_threads<D, WIDE>();
   constexpr int NGRP = 4 * decode_streams<D, WIDE>();
   constexpr int NCOL = qcols<QP>();
-  const size_t merge_bytes = sizeof(float) * (3 * NGRP * NCOL + NGRP * NCOL * D);
+  const size_t merge_bytes = sizeof(float) * (3 * NGRP * NCOL + NGRP * NCOL * (D + 4));
   const size_t xbuf_bytes = sizeof(float) * decode_xbuf_floats<D>();
   size_t smem = 128 + (size_t)decode_streams<D, WIDE>() * STAGES * pl.bytes + xbuf_bytes +
                 prep_scratch_bytes<D, KB, QP, NT>();
